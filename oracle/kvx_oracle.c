@@ -1,0 +1,248 @@
+/*
+ * kvx_oracle.c -- plain fp64 CPU oracle of the cross-model KV-cache transfer.
+ *
+ * TEST INFRASTRUCTURE ONLY (tests, smoke check, CPU baseline leg of the
+ * benchmark).  Every function is the plain definition written out as nested
+ * loops in double precision; there is no blocking, fusion or reordering.
+ * The sources and readings are listed in kvx_oracle.h.
+ */
+#include "kvx_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* [HIR] "Why carrying the cache across is the hard part": the position is
+ * folded into a key as a rotation.  [QKV] "Линейного моста...": strip the
+ * source RoPE, apply the target RoPE.  Half-split pairing (i, i + d/2) with
+ * frequency theta^(-2i/d). */
+void kvxo_rope(const double *x, int d, double pos, double theta, int sign,
+               double *out) {
+  int half = d / 2;
+  for (int i = 0; i < half; ++i) {
+    double w = pow(theta, -2.0 * (double)i / (double)d);
+    double a = (double)sign * pos * w;
+    double c = cos(a), s = sin(a);
+    double x0 = x[i], x1 = x[i + half];
+    out[i] = x0 * c - x1 * s;
+    out[i + half] = x0 * s + x1 * c;
+  }
+}
+
+/* One token of one (target layer, head): [HIR] steps 1-3, [QKV] feature
+ * concatenation and the per-(layer, head) map x @ w + b. */
+void kvxo_map_token(int d, int k, double theta_src, double theta_tgt,
+                    const double *const *src_k_rows,
+                    const double *const *src_v_rows,
+                    const double *Wk, const double *Wv,
+                    const double *bk, const double *bv,
+                    double p_src, double p_tgt,
+                    double *out_k, double *out_v) {
+  int kd = k * d;
+  double *xk = (double *)malloc(sizeof(double) * (size_t)kd);
+  double *xv = (double *)malloc(sizeof(double) * (size_t)kd);
+  double *yk = (double *)malloc(sizeof(double) * (size_t)d);
+
+  /* step 1 + concatenation: un-rotate each selected key, keep values */
+  for (int j = 0; j < k; ++j) {
+    kvxo_rope(src_k_rows[j], d, p_src, theta_src, -1, xk + j * d);
+    for (int c = 0; c < d; ++c) xv[j * d + c] = src_v_rows[j][c];
+  }
+  /* step 2: y = x W + b, separately for keys and values.  Each output
+   * element is summed as b[n] + x[0] W[0][n] + x[1] W[1][n] + ... in order. */
+  for (int n = 0; n < d; ++n) {
+    yk[n] = bk[n];
+    out_v[n] = bv[n];
+  }
+  for (int q = 0; q < kd; ++q) {
+    const double *wk_row = Wk + (size_t)q * d;
+    const double *wv_row = Wv + (size_t)q * d;
+    for (int n = 0; n < d; ++n) {
+      yk[n] += xk[q] * wk_row[n];
+      out_v[n] += xv[q] * wv_row[n];
+    }
+  }
+  /* step 3: re-rotate the mapped key into its target position */
+  kvxo_rope(yk, d, p_tgt, theta_tgt, +1, out_k);
+
+  free(xk);
+  free(xv);
+  free(yk);
+}
+
+/* Cache install.  Contiguous: one [capacity] slab per request.  Paged
+ * ([KNLP] inject through a block table): logical block p'/bs of request r is
+ * physical block block_table[r][p'/bs], slot p' % bs. */
+int64_t kvxo_dst_row(int layout, int64_t r, int64_t p_tgt,
+                     int64_t dst_capacity, int64_t block_size,
+                     int64_t num_blocks, const int32_t *block_table,
+                     int64_t max_blocks_per_req, int *bad) {
+  *bad = 0;
+  if (layout == KVXO_CONTIGUOUS) {
+    if (p_tgt >= dst_capacity) {
+      *bad = KVXO_BAD_ROW;
+      return -1;
+    }
+    return r * dst_capacity + p_tgt;
+  }
+  int64_t logical = p_tgt / block_size;
+  if (logical >= max_blocks_per_req) {
+    *bad = KVXO_BAD_BLOCK;
+    return -1;
+  }
+  int64_t phys = block_table[r * max_blocks_per_req + logical];
+  if (phys < 0 || phys >= num_blocks) {
+    *bad = KVXO_BAD_BLOCK;
+    return -1;
+  }
+  return phys * block_size + p_tgt % block_size;
+}
+
+int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
+  const int64_t Ls = P->src_layers, Lt = P->tgt_layers, H = P->kv_heads;
+  const int64_t d = P->head_dim, k = P->k, kd = k * d;
+  const int64_t ntok = P->ntok;
+  const int64_t rows = P->layout == KVXO_CONTIGUOUS
+                           ? (int64_t)P->num_requests * P->dst_capacity
+                           : P->num_blocks * P->block_size;
+  int status = 0;
+
+  const double **krows = (const double **)malloc(sizeof(double *) * (size_t)k);
+  const double **vrows = (const double **)malloc(sizeof(double *) * (size_t)k);
+  double *ok = (double *)malloc(sizeof(double) * (size_t)d);
+  double *ov = (double *)malloc(sizeof(double) * (size_t)d);
+
+  /* target layers whose selection row holds an index outside [0, Ls) */
+  char *layer_ok = (char *)malloc((size_t)Lt);
+  for (int64_t lt = 0; lt < Lt; ++lt) {
+    layer_ok[lt] = 1;
+    for (int64_t j = 0; j < k; ++j) {
+      int32_t s = P->layer_idx[lt * k + j];
+      if (s < 0 || s >= Ls) layer_ok[lt] = 0;
+    }
+    if (!layer_ok[lt]) status |= KVXO_BAD_LAYER_INDEX;
+  }
+
+  for (int64_t r = 0; r < P->num_requests; ++r) {
+    int64_t beg = P->cu_seqlens ? P->cu_seqlens[r] : 0;
+    int64_t end = P->cu_seqlens ? P->cu_seqlens[r + 1] : ntok;
+    if (beg < 0 || end < beg || end > ntok) {
+      status |= KVXO_BAD_SEQLENS;
+      continue;
+    }
+    for (int64_t g = beg; g < end; ++g) {
+      int64_t p = P->src_pos ? P->src_pos[g] : g - beg;
+      int64_t off = P->tgt_offset ? P->tgt_offset[r] : 0;
+      int64_t pt = P->tgt_pos ? P->tgt_pos[g] : p + off;
+      if (p < 0 || p >= P->max_position || pt < 0 || pt >= P->max_position) {
+        status |= KVXO_BAD_POSITION;
+        continue;
+      }
+      int bad = 0;
+      int64_t row = kvxo_dst_row(P->layout, r, pt, P->dst_capacity,
+                                 P->block_size, P->num_blocks, P->block_table,
+                                 P->max_blocks_per_req, &bad);
+      if (row < 0) {
+        status |= bad;
+        continue;
+      }
+      for (int64_t lt = 0; lt < Lt; ++lt) {
+        if (!layer_ok[lt]) continue;
+        for (int64_t h = 0; h < H; ++h) {
+          for (int64_t j = 0; j < k; ++j) {
+            int64_t s = P->layer_idx[lt * k + j];
+            krows[j] = P->src_k + ((s * ntok + g) * H + h) * d;
+            vrows[j] = P->src_v + ((s * ntok + g) * H + h) * d;
+          }
+          const double *Wk = P->w + ((lt * H + h) * 2 + 0) * kd * d;
+          const double *Wv = P->w + ((lt * H + h) * 2 + 1) * kd * d;
+          const double *bk = P->b + ((lt * H + h) * 2 + 0) * d;
+          const double *bv = P->b + ((lt * H + h) * 2 + 1) * d;
+          kvxo_map_token((int)d, (int)k, P->theta_src, P->theta_tgt, krows,
+                         vrows, Wk, Wv, bk, bv, (double)p, (double)pt, ok, ov);
+          double *dk = dst_k + ((lt * rows + row) * H + h) * d;
+          double *dv = dst_v + ((lt * rows + row) * H + h) * d;
+          memcpy(dk, ok, sizeof(double) * (size_t)d);
+          memcpy(dv, ov, sizeof(double) * (size_t)d);
+        }
+      }
+    }
+  }
+  free(layer_ok);
+  free(krows);
+  free(vrows);
+  free(ok);
+  free(ov);
+  return status;
+}
+
+/* Ridge demo of [QKV] ("Линейного моста, как ни странно, хватает"): centre
+ * X and Y on their column means, solve (XcT Xc + lam I) W = XcT Yc, and set
+ * b = ybar - xbar W.  The solve is a plain Cholesky factorisation. */
+int kvxo_ridge_fit(const double *X, const double *Y, int64_t n, int p, int q,
+                   double lam, double *W, double *b) {
+  double *xm = (double *)calloc((size_t)p, sizeof(double));
+  double *ym = (double *)calloc((size_t)q, sizeof(double));
+  double *A = (double *)calloc((size_t)p * p, sizeof(double));
+  double *B = (double *)calloc((size_t)p * q, sizeof(double));
+  int rc = 0;
+
+  for (int64_t t = 0; t < n; ++t) {
+    for (int i = 0; i < p; ++i) xm[i] += X[t * p + i];
+    for (int i = 0; i < q; ++i) ym[i] += Y[t * q + i];
+  }
+  for (int i = 0; i < p; ++i) xm[i] /= (double)n;
+  for (int i = 0; i < q; ++i) ym[i] /= (double)n;
+
+  /* A = XcT Xc + lam I ; B = XcT Yc */
+  for (int64_t t = 0; t < n; ++t) {
+    for (int i = 0; i < p; ++i) {
+      double xi = X[t * p + i] - xm[i];
+      for (int j = 0; j < p; ++j) A[i * p + j] += xi * (X[t * p + j] - xm[j]);
+      for (int j = 0; j < q; ++j) B[i * q + j] += xi * (Y[t * q + j] - ym[j]);
+    }
+  }
+  for (int i = 0; i < p; ++i) A[i * p + i] += lam;
+
+  /* Cholesky A = L LT, L stored in the lower triangle of A */
+  for (int j = 0; j < p && rc == 0; ++j) {
+    double s = A[j * p + j];
+    for (int m = 0; m < j; ++m) s -= A[j * p + m] * A[j * p + m];
+    if (!(s > 0.0)) {
+      rc = -1;
+      break;
+    }
+    double ljj = sqrt(s);
+    A[j * p + j] = ljj;
+    for (int i = j + 1; i < p; ++i) {
+      double v = A[i * p + j];
+      for (int m = 0; m < j; ++m) v -= A[i * p + m] * A[j * p + m];
+      A[i * p + j] = v / ljj;
+    }
+  }
+  if (rc == 0) {
+    /* forward solve L Z = B, then back solve LT W = Z, column by column */
+    for (int c = 0; c < q; ++c) {
+      for (int i = 0; i < p; ++i) {
+        double v = B[i * q + c];
+        for (int m = 0; m < i; ++m) v -= A[i * p + m] * W[m * q + c];
+        W[i * q + c] = v / A[i * p + i];
+      }
+      for (int i = p - 1; i >= 0; --i) {
+        double v = W[i * q + c];
+        for (int m = i + 1; m < p; ++m) v -= A[m * p + i] * W[m * q + c];
+        W[i * q + c] = v / A[i * p + i];
+      }
+    }
+    for (int c = 0; c < q; ++c) {
+      double v = ym[c];
+      for (int i = 0; i < p; ++i) v -= xm[i] * W[i * q + c];
+      b[c] = v;
+    }
+  }
+  free(xm);
+  free(ym);
+  free(A);
+  free(B);
+  return rc;
+}

@@ -1,0 +1,129 @@
+/*
+ * kvx_oracle.h -- plain fp64 CPU oracle of the cross-model KV-cache transfer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load or call this code.  It shares no
+ * code, header, table or helper with the CUDA library: it is an independent
+ * restatement of what the transfer computes, written for a reader to check by
+ * eye against the sources it cites, and deliberately slow (nested loops,
+ * double precision, one thread).
+ *
+ * Sources (page title, then section):
+ *  [HIR] "Helm Intelligent Routing" (docs.iterate.ai), section
+ *        "Why carrying the cache across is the hard part", steps 1-3:
+ *        un-rotate the pilot's keys into content space, apply a per-layer,
+ *        per-head linear map fitted offline, re-rotate into the position the
+ *        entry will occupy in the target sequence (re-rotation cannot be
+ *        skipped).  Section "Current limitation": the mapped cache is
+ *        installed into the engine's paged cache.
+ *  [QKV] "Перенос KV-кэша между моделями Qwen3 вместо повторного префилла"
+ *        (reactapp.top), section "Линейного моста, как ни странно, хватает":
+ *        pick, per target layer, the source layers that best predict it and
+ *        concatenate their features; one ridge regression per target
+ *        (layer, head), one for keys and one for values; strip the source
+ *        RoPE before mapping keys and apply the target RoPE afterwards; the
+ *        ridge demo fits Y ~ XW + b on centred X, Y with (XcT Xc + lam I).
+ *  [KNLP] knlp.io "routing" page, the connector flow's inject step: selected
+ *        entries are written into the paged cache through a block table.
+ *
+ * Readings where the sources are silent (the same readings the CUDA library
+ * documents):
+ *  - RoPE is half-split: pairs (i, i + d/2), frequency w_i = theta^(-2i/d).
+ *    rotate multiplies (x_i + j x_{i+d/2}) by exp(+j p w_i); unrotate is
+ *    rotate at -p.  Only keys carry RoPE; values are mapped as stored.
+ *  - The feature vector of target head h is the concatenation, in index-table
+ *    order, of the k selected source layers' head-h vectors (width k*d);
+ *    W[lt][h][m] is [k*d][d] row-major, m = 0 for K and 1 for V.
+ *  - Request r owns source rows [cu_seqlens[r], cu_seqlens[r+1]); a request
+ *    whose range is not inside [0, ntok] or runs backwards is skipped.
+ *  - The target position p' sets both the re-rotation angle and the cache
+ *    row.  p' = tgt_pos[g] if given, else p + tgt_offset[r] (0 if absent).
+ *    Source and target positions must lie in [0, max_position).
+ *  - Contiguous target: row = r * dst_capacity + p' (needs p' < capacity).
+ *    Paged target: row = block_table[r][p' / bs] * bs + p' % bs (needs
+ *    p' / bs < max_blocks_per_req and the block id in [0, num_blocks)).
+ *  - A row whose layer index, position, block or row is out of range is not
+ *    written; the matching KVXO_BAD_* bit is OR-ed into the return value.
+ */
+#ifndef KVX_ORACLE_H
+#define KVX_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return bits of kvxo_transfer (rows that trip one are skipped). */
+#define KVXO_BAD_LAYER_INDEX 1
+#define KVXO_BAD_POSITION    2
+#define KVXO_BAD_BLOCK       4
+#define KVXO_BAD_ROW         8
+#define KVXO_BAD_SEQLENS     32
+
+#define KVXO_CONTIGUOUS 0
+#define KVXO_PAGED      1
+
+/* Half-split RoPE of one head vector x[d] (d even) at position pos with base
+ * theta.  sign = +1 rotates (applies RoPE), sign = -1 un-rotates.  out may
+ * not alias x. */
+void kvxo_rope(const double *x, int d, double pos, double theta, int sign,
+               double *out);
+
+/* One token, one (target layer, head): gather the k selected source rows,
+ * un-rotate the keys at p_src with theta_src, concatenate, map with
+ * Wk/Wv ([k*d][d] row-major) and bk/bv ([d]), re-rotate the mapped key at
+ * p_tgt with theta_tgt.  src_k_rows[j] / src_v_rows[j] point at the head
+ * vector [d] of the j-th selected source layer. */
+void kvxo_map_token(int d, int k, double theta_src, double theta_tgt,
+                    const double *const *src_k_rows,
+                    const double *const *src_v_rows,
+                    const double *Wk, const double *Wv,
+                    const double *bk, const double *bv,
+                    double p_src, double p_tgt,
+                    double *out_k, double *out_v);
+
+/* Row of the target cache that token (request r, target position p_tgt)
+ * lands in, or -1 with *bad set to the KVXO_BAD_* reason. */
+int64_t kvxo_dst_row(int layout, int64_t r, int64_t p_tgt,
+                     int64_t dst_capacity, int64_t block_size,
+                     int64_t num_blocks, const int32_t *block_table,
+                     int64_t max_blocks_per_req, int *bad);
+
+typedef struct {
+  int32_t src_layers, tgt_layers, kv_heads, head_dim, k;
+  double theta_src, theta_tgt;
+  int64_t max_position;        /* positions must lie in [0, max_position) */
+  int32_t num_requests;
+  int64_t ntok;                /* source rows */
+  const int64_t *cu_seqlens;   /* [R+1] or NULL (then R == 1, all ntok rows) */
+  const double *src_k;         /* [Ls][ntok][H][d] */
+  const double *src_v;
+  const int32_t *layer_idx;    /* [Lt][k] */
+  const double *w;             /* [Lt][H][2][k*d][d] */
+  const double *b;             /* [Lt][H][2][d] */
+  const int64_t *src_pos;      /* [ntok] or NULL: 0..len_r-1 per request */
+  const int64_t *tgt_pos;      /* [ntok] or NULL: src_pos + tgt_offset[r] */
+  const int64_t *tgt_offset;   /* [R] or NULL: 0 */
+  int32_t layout;              /* KVXO_CONTIGUOUS or KVXO_PAGED */
+  int64_t dst_capacity;        /* contiguous: rows per request */
+  int64_t block_size, num_blocks, max_blocks_per_req;
+  const int32_t *block_table;  /* [R][max_blocks_per_req] (paged) */
+} kvxo_problem;
+
+/* Whole transfer.  dst_k / dst_v are [Lt][rows][H][d] with rows =
+ * R * dst_capacity (contiguous) or num_blocks * block_size (paged); rows not
+ * written keep their contents.  Returns the OR of KVXO_BAD_* bits. */
+int kvxo_transfer(const kvxo_problem *prob, double *dst_k, double *dst_v);
+
+/* Centred ridge regression with intercept, as in the ridge demo of [QKV]:
+ * X [n][p], Y [n][q] row-major; W [p][q] = (XcT Xc + lam I)^-1 XcT Yc,
+ * b [q] = ybar - xbar W.  Solved by Cholesky.  Returns 0, or -1 if the
+ * normal matrix is not positive definite. */
+int kvxo_ridge_fit(const double *X, const double *Y, int64_t n, int p, int q,
+                   double lam, double *W, double *b);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVX_ORACLE_H */

@@ -1,0 +1,512 @@
+"""Pins of the fp64 oracle against what the sources and mathematics fix.
+
+Each test is chosen so that a plausible mistake in the oracle fails it:
+a wrong RoPE pairing (interleaved instead of half-split), exponent or sign;
+a transposed map or wrong concatenation order; a dropped bias; a wrong cache
+row; a wrong ridge centring.  None of them re-types the oracle's loops: they
+use closed forms (complex multiplication), invariants, planted values read
+back from the destination side, and library routines for special cases.
+"""
+import cmath
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# RoPE ("Helm Intelligent Routing", "Why carrying the cache across is the
+# hard part": the position is folded into a key as a rotation; steps 1, 3)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("p", [0, 1, 7, 1000, 32767])
+def test_rope_d2_is_complex_multiplication(p):
+    # d = 2: one pair, frequency theta^0 = 1, so the rotation is (a + jb) e^{jp}.
+    a, b = 0.75, -1.25
+    z = complex(a, b) * cmath.exp(1j * p)
+    got = oracle.rope([a, b], p, 1e4, +1)
+    assert got == pytest.approx([z.real, z.imag], abs=1e-12)
+    z = complex(a, b) * cmath.exp(-1j * p)
+    got = oracle.rope([a, b], p, 1e4, -1)
+    assert got == pytest.approx([z.real, z.imag], abs=1e-12)
+
+
+@pytest.mark.parametrize("theta", [1e4, 5e5, 1e6])
+def test_rope_half_split_frequency_ladder(theta):
+    # Basis vector e_i turns within the plane (i, i + d/2) at angle
+    # p * theta^(-2i/d): catches interleaved pairing and a wrong exponent.
+    d, p = 8, 123.0
+    for i in range(d // 2):
+        w = math.pow(theta, -2.0 * i / d)
+        e = np.zeros(d)
+        e[i] = 1.0
+        want = np.zeros(d)
+        want[i], want[i + d // 2] = math.cos(p * w), math.sin(p * w)
+        np.testing.assert_allclose(oracle.rope(e, p, theta, +1), want, atol=1e-14)
+        e = np.zeros(d)
+        e[i + d // 2] = 1.0
+        want = np.zeros(d)
+        want[i], want[i + d // 2] = -math.sin(p * w), math.cos(p * w)
+        np.testing.assert_allclose(oracle.rope(e, p, theta, +1), want, atol=1e-14)
+
+
+def test_unrotate_inverts_rotate():
+    for d in (2, 64, 128):
+        x = RNG.standard_normal(d) * np.exp(RNG.standard_normal(d))
+        for p in (0, 3, 511, 32767, 32831):
+            y = oracle.rope(oracle.rope(x, p, 1e6, +1), p, 1e6, -1)
+            np.testing.assert_allclose(y, x, rtol=0, atol=1e-12 * np.abs(x).max())
+
+
+def test_rotate_after_unrotate_is_rotation_by_difference():
+    d = 128
+    x = RNG.standard_normal(d)
+    for p, q in ((100, 37), (37, 100), (32768, 5), (0, 9)):
+        lhs = oracle.rope(oracle.rope(x, q, 1e6, -1), p, 1e6, +1)
+        rhs = oracle.rope(x, p - q, 1e6, +1)
+        np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-11)
+
+
+def test_rotate_at_zero_is_exact_identity_and_norm_is_kept():
+    d = 64
+    x = RNG.standard_normal(d)
+    assert np.array_equal(oracle.rope(x, 0, 1e4, +1), x)
+    y = oracle.rope(x, 4321, 1e4, +1)
+    pair_norm = lambda v: v[: d // 2] ** 2 + v[d // 2:] ** 2
+    np.testing.assert_allclose(pair_norm(y), pair_norm(x), rtol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# The map ("Helm Intelligent Routing" step 2; Qwen3 article, linear bridge:
+# concatenated features of the selected layers, one fit per target
+# (layer, head), separately for K and V, map x @ w + b)
+# --------------------------------------------------------------------------
+
+def _planted_source(Ls, T, H, d):
+    """src[s][t][h][c] = a distinct exact integer encoding (s, t, h, c)."""
+    s, t, h, c = np.meshgrid(np.arange(Ls), np.arange(T), np.arange(H), np.arange(d),
+                             indexing="ij")
+    return (((s * 1000 + t) * 100 + h) * 1000 + c + 1).astype(np.float64)
+
+
+def test_identity_map_reproduces_source():
+    # k = 1, W = I, b = 0, same theta both sides, offset 0: the target cache is
+    # the selected source layer, keys included (un-rotate then re-rotate at
+    # the same position cancels).
+    Ls, Lt, H, d, T = 3, 4, 2, 16, 10
+    src_k = RNG.standard_normal((Ls, T, H, d))
+    src_v = RNG.standard_normal((Ls, T, H, d))
+    idx = np.array([[2], [0], [1], [2]], dtype=np.int32)
+    w = np.zeros((Lt, H, 2, d, d))
+    w[..., :, :] = np.eye(d)
+    b = np.zeros((Lt, H, 2, d))
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=w, b=b,
+                                 theta_src=1e4, theta_tgt=1e4, max_position=T,
+                                 dst_capacity=T)
+    assert st == 0
+    for lt in range(Lt):
+        np.testing.assert_array_equal(dv[lt], src_v[idx[lt, 0]])
+        np.testing.assert_allclose(dk[lt], src_k[idx[lt, 0]], rtol=0, atol=1e-13)
+
+
+def test_selection_matrix_routes_concatenated_features():
+    # W picks feature perm[n] of the concatenated vector into output n.  With
+    # positions all zero RoPE is exactly the identity, so every output must be
+    # exactly the planted source value of layer idx[lt][perm[n] // d],
+    # channel perm[n] % d: checks concatenation order and W orientation.
+    Ls, Lt, H, d, T, k = 5, 3, 2, 8, 4, 3
+    src = _planted_source(Ls, T, H, d)
+    idx = np.array([[4, 0, 2], [1, 3, 0], [2, 2, 4]], dtype=np.int32)
+    perms = RNG.permuted(np.tile(np.arange(k * d), (Lt, H, 2, 1)), axis=-1)[..., :d]
+    w = np.zeros((Lt, H, 2, k * d, d))
+    for lt in range(Lt):
+        for h in range(H):
+            for m in range(2):
+                w[lt, h, m, perms[lt, h, m], np.arange(d)] = 1.0
+    b = np.zeros((Lt, H, 2, d))
+    src_pos = np.zeros(T, dtype=np.int64)
+    tgt_pos = np.zeros(T, dtype=np.int64)
+    # all tokens land on row 0 with zero positions; use T = 1 per call instead
+    for t in range(T):
+        dk, dv, st = oracle.transfer(src_k=src[:, t:t + 1] * 2, src_v=src[:, t:t + 1],
+                                     layer_idx=idx, w=w, b=b, theta_src=1e4,
+                                     theta_tgt=1e6, max_position=1, dst_capacity=1,
+                                     src_pos=src_pos[:1], tgt_pos=tgt_pos[:1])
+        assert st == 0
+        for lt in range(Lt):
+            for h in range(H):
+                for m, (dst, mult) in enumerate(((dk, 2), (dv, 1))):
+                    q = perms[lt, h, m]
+                    want = mult * src[idx[lt, q // d], t, h, q % d]
+                    np.testing.assert_array_equal(dst[lt, 0, h], want)
+
+
+def test_bias_only_and_key_bias_is_rotated():
+    # W = 0: values equal b exactly; keys equal b turned by the target RoPE at
+    # p' (complex multiplication per pair, frequency theta^(-2i/d)).
+    Ls, Lt, H, d, T, k = 2, 2, 1, 4, 3, 2
+    src = RNG.standard_normal((Ls, T, H, d))
+    idx = np.array([[0, 1], [1, 0]], dtype=np.int32)
+    w = np.zeros((Lt, H, 2, k * d, d))
+    b = RNG.standard_normal((Lt, H, 2, d))
+    theta_t, off = 5e5, 11
+    dk, dv, st = oracle.transfer(src_k=src, src_v=src, layer_idx=idx, w=w, b=b,
+                                 theta_src=1e4, theta_tgt=theta_t, max_position=T + off,
+                                 dst_capacity=T + off, tgt_offset=[off])
+    assert st == 0
+    for lt in range(Lt):
+        for t in range(T):
+            np.testing.assert_array_equal(dv[lt, t + off, 0], b[lt, 0, 1])
+            p = t + off
+            for i in range(d // 2):
+                z = complex(b[lt, 0, 0, i], b[lt, 0, 0, i + d // 2])
+                z *= cmath.exp(1j * p * theta_t ** (-2.0 * i / d))
+                assert dk[lt, p, 0, i] == pytest.approx(z.real, abs=1e-13)
+                assert dk[lt, p, 0, i + d // 2] == pytest.approx(z.imag, abs=1e-13)
+
+
+def test_key_path_closed_form_with_different_thetas():
+    # A key stored as content c turned by the source RoPE at p, mapped with
+    # W = I (k = 1), lands as c turned by the target RoPE at p' = p + off:
+    # un-rotation really strips theta_src and re-rotation really applies
+    # theta_tgt at the target position.
+    d, T, off, ts, tt = 8, 6, 37, 1e4, 1e6
+    c = RNG.standard_normal((T, d))
+    zc = c[:, : d // 2] + 1j * c[:, d // 2:]
+    i = np.arange(d // 2)
+    p = np.arange(T)[:, None]
+    zs = zc * np.exp(1j * p * ts ** (-2.0 * i / d))
+    src_k = np.concatenate([zs.real, zs.imag], axis=1).reshape(1, T, 1, d)
+    w = np.eye(d).reshape(1, 1, 1, d, d).repeat(2, axis=2)
+    b = np.zeros((1, 1, 2, d))
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=src_k, layer_idx=[[0]], w=w, b=b,
+                                 theta_src=ts, theta_tgt=tt, max_position=T + off,
+                                 dst_capacity=T + off, tgt_offset=[off])
+    assert st == 0
+    zt = zc * np.exp(1j * (p + off) * tt ** (-2.0 * i / d))
+    want = np.concatenate([zt.real, zt.imag], axis=1)
+    np.testing.assert_allclose(dk[0, off:, 0], want, rtol=0, atol=1e-12)
+    assert np.isnan(dk[0, :off]).all()
+
+
+def test_linear_in_features_sum_of_two_terms():
+    # Two nonzeros per column: output = 0.5 * feature a + 3 * feature b + bias.
+    Ls, H, d, T, k = 3, 1, 4, 1, 2
+    src = _planted_source(Ls, T, H, d)
+    idx = np.array([[2, 1]], dtype=np.int32)
+    w = np.zeros((1, H, 2, k * d, d))
+    b = np.full((1, H, 2, d), 0.25)
+    for n in range(d):
+        w[0, 0, 1, n, n] = 0.5          # layer idx[0] = 2, channel n
+        w[0, 0, 1, d + (n + 1) % d, n] = 3.0   # layer idx[1] = 1, channel n+1
+    _, dv, st = oracle.transfer(src_k=src, src_v=src, layer_idx=idx, w=w, b=b,
+                                theta_src=1e4, theta_tgt=1e4, max_position=1,
+                                dst_capacity=1)
+    assert st == 0
+    for n in range(d):
+        want = 0.25 + 0.5 * src[2, 0, 0, n] + 3.0 * src[1, 0, 0, (n + 1) % d]
+        assert dv[0, 0, 0, n] == want
+
+
+# --------------------------------------------------------------------------
+# Cache install: contiguous rows and paged blocks ("Helm Intelligent
+# Routing", "Current limitation": installer into the engine's paged cache;
+# knlp.io routing page: inject through the block table)
+# --------------------------------------------------------------------------
+
+def _varlen_problem(bs=4, seed=5):
+    rng = np.random.default_rng(seed)
+    lens = [5, 1, 9]
+    offs = [0, 3, 6]
+    R, H, d, Ls, Lt, k = 3, 2, 4, 3, 2, 1
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(cu[-1])
+    nb = [(n + o + bs - 1) // bs for n, o in zip(lens, offs)]
+    pool = int(sum(nb)) + 2                     # two blocks nobody owns
+    perm = rng.permutation(pool).astype(np.int32)
+    table = np.full((R, max(nb) + 1), -1, dtype=np.int32)
+    at = 0
+    for r in range(R):
+        table[r, :nb[r]] = perm[at:at + nb[r]]
+        at += nb[r]
+    src = _planted_source(Ls, T, H, d)
+    idx = np.array([[2], [0]], dtype=np.int32)
+    w = np.zeros((Lt, H, 2, d, d))
+    w[...] = np.eye(d)
+    b = np.zeros((Lt, H, 2, d))
+    return dict(lens=lens, offs=offs, cu=cu, table=table, pool=pool, src=src, idx=idx,
+                w=w, b=b, bs=bs, T=T, H=H, d=d, Lt=Lt)
+
+
+def test_paged_scatter_routes_every_token_and_leaves_the_rest():
+    P = _varlen_problem()
+    bs = P["bs"]
+    dk, dv, st = oracle.transfer(src_k=P["src"], src_v=P["src"], layer_idx=P["idx"],
+                                 w=P["w"], b=P["b"], theta_src=1e4, theta_tgt=1e4,
+                                 max_position=32, cu_seqlens=P["cu"],
+                                 tgt_offset=P["offs"], layout=oracle.PAGED,
+                                 block_size=bs, num_blocks=P["pool"],
+                                 block_table=P["table"])
+    assert st == 0
+    # Read back from the destination side: physical block -> (request,
+    # logical block) from the table, slot -> target position -> source token.
+    owner = {}
+    for r in range(len(P["lens"])):
+        for lb, pb in enumerate(P["table"][r]):
+            if pb >= 0:
+                owner[int(pb)] = (r, lb)
+    written = 0
+    for pb in range(P["pool"]):
+        for slot in range(bs):
+            row = pb * bs + slot
+            tok = None
+            if pb in owner:
+                r, lb = owner[pb]
+                pt = lb * bs + slot
+                pos = pt - P["offs"][r]
+                if 0 <= pos < P["lens"][r]:
+                    tok = int(P["cu"][r]) + pos
+            for lt in range(P["Lt"]):
+                s = P["idx"][lt, 0]
+                if tok is None:
+                    assert np.isnan(dv[lt, row]).all() and np.isnan(dk[lt, row]).all()
+                else:
+                    np.testing.assert_array_equal(dv[lt, row], P["src"][s, tok])
+                    # keys: un-rotate at p, re-rotate at p' = p + off: differs
+                    # from the source by the rotation through the offset
+                    want = oracle.rope(P["src"][s, tok, 0], P["offs"][owner[pb][0]], 1e4, +1)
+                    np.testing.assert_allclose(dk[lt, row, 0], want, rtol=1e-12)
+                    written += 1
+    assert written == P["Lt"] * P["T"]
+
+
+def test_contiguous_offset_leaves_rows_below_offset():
+    T, off, d = 5, 3, 4
+    src = _planted_source(1, T, 1, d)
+    w = np.eye(d).reshape(1, 1, 1, d, d).repeat(2, axis=2)
+    b = np.zeros((1, 1, 2, d))
+    dk, dv, st = oracle.transfer(src_k=src, src_v=src, layer_idx=[[0]], w=w, b=b,
+                                 theta_src=1e4, theta_tgt=1e4, max_position=T + off,
+                                 dst_capacity=T + off + 2, tgt_offset=[off])
+    assert st == 0
+    assert np.isnan(dv[0, :off]).all() and np.isnan(dv[0, off + T:]).all()
+    np.testing.assert_array_equal(dv[0, off:off + T], src[0])
+
+
+def test_out_of_range_rows_are_skipped_and_flagged():
+    P = _varlen_problem()
+    base = dict(src_k=P["src"], src_v=P["src"], w=P["w"], b=P["b"], theta_src=1e4,
+                theta_tgt=1e4, cu_seqlens=P["cu"], tgt_offset=P["offs"],
+                layout=oracle.PAGED, block_size=P["bs"], num_blocks=P["pool"])
+    # a selection index outside [0, Ls): that target layer is left untouched
+    dk, dv, st = oracle.transfer(layer_idx=[[2], [3]], max_position=32,
+                                 block_table=P["table"], **base)
+    assert st == oracle.BAD_LAYER_INDEX
+    assert np.isnan(dv[1]).all() and not np.isnan(dv[0]).all()
+    # a position beyond the table: only those tokens are skipped
+    _, dv, st = oracle.transfer(layer_idx=P["idx"], max_position=12,
+                                block_table=P["table"], **base)
+    assert st == oracle.BAD_POSITION
+    assert np.count_nonzero(~np.isnan(dv[0, :, 0, 0])) == 5 + 1 + (12 - 6)
+    # a referenced table entry of -1
+    table = P["table"].copy()
+    table[2, 1] = -1
+    _, dv, st = oracle.transfer(layer_idx=P["idx"], max_position=32,
+                                block_table=table, **base)
+    assert st == oracle.BAD_BLOCK
+    # request 2 (offset 6) puts target positions 6 and 7 in logical block 1
+    assert np.count_nonzero(~np.isnan(dv[0, :, 0, 0])) == P["T"] - 2
+    # contiguous capacity too small
+    _, dv, st = oracle.transfer(src_k=P["src"], src_v=P["src"], w=P["w"], b=P["b"],
+                                theta_src=1e4, theta_tgt=1e4, cu_seqlens=P["cu"],
+                                tgt_offset=P["offs"], layer_idx=P["idx"], max_position=32,
+                                dst_capacity=8)
+    assert st == oracle.BAD_ROW
+    # request ranges that run backwards
+    _, dv, st = oracle.transfer(src_k=P["src"], src_v=P["src"], w=P["w"], b=P["b"],
+                                theta_src=1e4, theta_tgt=1e4, cu_seqlens=[0, 5, 4, 15],
+                                layer_idx=P["idx"], max_position=32, dst_capacity=16)
+    assert st == oracle.BAD_SEQLENS
+
+
+def test_dst_row_examples():
+    table = np.array([[7, 2, 5]], dtype=np.int32)
+    assert oracle.dst_row(oracle.PAGED, 0, 0, block_size=16, num_blocks=8,
+                          block_table=table, max_blocks_per_req=3) == (7 * 16, 0)
+    assert oracle.dst_row(oracle.PAGED, 0, 17, block_size=16, num_blocks=8,
+                          block_table=table, max_blocks_per_req=3) == (2 * 16 + 1, 0)
+    assert oracle.dst_row(oracle.PAGED, 0, 48, block_size=16, num_blocks=8,
+                          block_table=table, max_blocks_per_req=3) == (-1, oracle.BAD_BLOCK)
+    assert oracle.dst_row(oracle.CONTIGUOUS, 2, 5, dst_capacity=10) == (25, 0)
+    assert oracle.dst_row(oracle.CONTIGUOUS, 0, 10, dst_capacity=10) == (-1, oracle.BAD_ROW)
+
+
+# --------------------------------------------------------------------------
+# Brute force: a second formulation of the whole transfer in numpy (complex
+# phasors, einsum over the stacked selection, vectorised routing), on the
+# tiny workload and on a varlen paged problem.
+# --------------------------------------------------------------------------
+
+def _numpy_transfer(src_k, src_v, idx, w, b, ts, tt, cu, offs, layout, cap, bs, table,
+                    rows):
+    Ls, T, H, d = src_k.shape
+    half = d // 2
+    i = np.arange(half)
+    req = np.searchsorted(cu, np.arange(T), side="right") - 1
+    p = np.arange(T) - cu[req]
+    pt = p + np.asarray(offs)[req]
+    zs = src_k[..., :half] + 1j * src_k[..., half:]
+    zc = zs * np.exp(-1j * p[None, :, None, None] * ts ** (-2.0 * i / d))
+    kc = np.concatenate([zc.real, zc.imag], -1)                  # [Ls][T][H][d]
+    xk = np.moveaxis(kc[idx], 1, 3).reshape(idx.shape[0], T, H, -1)   # [Lt][T][H][k d]
+    xv = np.moveaxis(src_v[idx], 1, 3).reshape(idx.shape[0], T, H, -1)
+    yk = np.einsum("lthq,lhqn->lthn", xk, w[:, :, 0]) + b[:, None, :, 0]
+    yv = np.einsum("lthq,lhqn->lthn", xv, w[:, :, 1]) + b[:, None, :, 1]
+    zy = (yk[..., :half] + 1j * yk[..., half:]) * np.exp(
+        1j * pt[None, :, None, None] * tt ** (-2.0 * i / d))
+    yk = np.concatenate([zy.real, zy.imag], -1)
+    if layout == oracle.PAGED:
+        row = table[req, pt // bs] * bs + pt % bs
+    else:
+        row = req * cap + pt
+    Lt = idx.shape[0]
+    dk = np.full((Lt, rows, H, d), np.nan)
+    dv = np.full((Lt, rows, H, d), np.nan)
+    dk[:, row] = yk
+    dv[:, row] = yv
+    return dk, dv
+
+
+def test_brute_force_tiny_workload():
+    Ls, Lt, H, d, T, k = 4, 6, 2, 64, 128, 2
+    src_k = RNG.standard_normal((Ls, T, H, d)) * np.exp(RNG.standard_normal((Ls, 1, H, d)))
+    src_v = RNG.standard_normal((Ls, T, H, d)) * np.exp(RNG.standard_normal((Ls, 1, H, d)))
+    idx = np.stack([RNG.permutation(Ls)[:k] for _ in range(Lt)]).astype(np.int32)
+    w = RNG.standard_normal((Lt, H, 2, k * d, d)) / math.sqrt(k * d)
+    b = RNG.standard_normal((Lt, H, 2, d)) * 0.01
+    cu = np.array([0, T])
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=w, b=b,
+                                 theta_src=1e4, theta_tgt=1e4, max_position=T,
+                                 dst_capacity=T)
+    assert st == 0
+    nk, nv = _numpy_transfer(src_k, src_v, idx, w, b, 1e4, 1e4, cu, [0],
+                             oracle.CONTIGUOUS, T, 1, None, T)
+    np.testing.assert_allclose(dk, nk, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dv, nv, rtol=1e-12, atol=1e-12)
+
+
+def test_brute_force_varlen_paged_different_thetas():
+    rng = np.random.default_rng(99)
+    lens, offs, bs = [7, 3, 12], [2, 0, 5], 4
+    Ls, Lt, H, d, k = 5, 3, 2, 8, 3
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    nb = [(n + o + bs - 1) // bs for n, o in zip(lens, offs)]
+    pool = sum(nb)
+    perm = rng.permutation(pool).astype(np.int32)
+    table = np.full((3, max(nb)), -1, dtype=np.int32)
+    at = 0
+    for r in range(3):
+        table[r, :nb[r]] = perm[at:at + nb[r]]
+        at += nb[r]
+    src_k = rng.standard_normal((Ls, T, H, d))
+    src_v = rng.standard_normal((Ls, T, H, d))
+    idx = np.stack([rng.permutation(Ls)[:k] for _ in range(Lt)]).astype(np.int32)
+    w = rng.standard_normal((Lt, H, 2, k * d, d))
+    b = rng.standard_normal((Lt, H, 2, d))
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=w, b=b,
+                                 theta_src=1e4, theta_tgt=5e5, max_position=20,
+                                 cu_seqlens=cu, tgt_offset=offs, layout=oracle.PAGED,
+                                 block_size=bs, num_blocks=pool, block_table=table)
+    assert st == 0
+    nk, nv = _numpy_transfer(src_k, src_v, idx, w, b, 1e4, 5e5, cu, offs,
+                             oracle.PAGED, 0, bs, table, pool * bs)
+    np.testing.assert_allclose(dk, nk, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dv, nv, rtol=1e-12, atol=1e-12)
+
+
+def test_map_token_matches_transfer_row():
+    # The per-token entry point used for sampled checks at full size gives the
+    # same bits as the whole transfer.
+    rng = np.random.default_rng(3)
+    Ls, Lt, H, d, T, k = 4, 2, 2, 8, 6, 2
+    src_k = rng.standard_normal((Ls, T, H, d))
+    src_v = rng.standard_normal((Ls, T, H, d))
+    idx = np.array([[3, 1], [0, 3]], dtype=np.int32)
+    w = rng.standard_normal((Lt, H, 2, k * d, d))
+    b = rng.standard_normal((Lt, H, 2, d))
+    dk, dv, _ = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=w, b=b,
+                                theta_src=1e4, theta_tgt=1e6, max_position=T + 4,
+                                dst_capacity=T + 4, tgt_offset=[4])
+    for lt in range(Lt):
+        for h in range(H):
+            for t in range(T):
+                ok, ov = oracle.map_token(src_k[idx[lt], t, h], src_v[idx[lt], t, h],
+                                          w[lt, h, 0], w[lt, h, 1], b[lt, h, 0], b[lt, h, 1],
+                                          t, t + 4, 1e4, 1e6)
+                assert np.array_equal(ok, dk[lt, t + 4, h])
+                assert np.array_equal(ov, dv[lt, t + 4, h])
+
+
+# --------------------------------------------------------------------------
+# Ridge fit (Qwen3 article, linear bridge: the ridge demo)
+# --------------------------------------------------------------------------
+
+def test_ridge_worked_example_exact_fractions():
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "ridge_worked_example.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    x = np.array([float(v) for v in rows[0][1:]])
+    y = np.array([float(v) for v in rows[1][1:]])
+    for r in rows[2:]:
+        ln, ld, wn, wd, bn, bd = map(int, r[1:])
+        W, b = oracle.ridge_fit(x[:, None], y[:, None], lam=ln / ld)
+        assert W[0, 0] == pytest.approx(float(Fraction(wn, wd)), rel=1e-14)
+        assert b[0] == pytest.approx(float(Fraction(bn, bd)), rel=1e-14)
+
+
+def test_ridge_recovers_planted_map_as_lambda_vanishes():
+    n, p, q = 400, 12, 5
+    X = RNG.standard_normal((n, p)) * 3 + RNG.standard_normal(p)
+    Wstar = RNG.standard_normal((p, q))
+    bstar = RNG.standard_normal(q)
+    Y = X @ Wstar + bstar
+    W, b = oracle.ridge_fit(X, Y, lam=1e-10)
+    assert np.linalg.norm(W - Wstar) / np.linalg.norm(Wstar) < 1e-8
+    assert np.linalg.norm(b - bstar) / np.linalg.norm(bstar) < 1e-8
+
+
+def test_ridge_shrinkage_closed_form():
+    # Noiseless Y = X W* + b*: the centred fit is (XcT Xc + lam I)^-1 XcT Xc W*,
+    # solved here with LAPACK's LU (not the oracle's Cholesky).
+    n, p, q, lam = 300, 10, 4, 7.5
+    X = RNG.standard_normal((n, p)) + 2.0
+    Wstar = RNG.standard_normal((p, q))
+    Y = X @ Wstar + 0.5
+    Xc = X - X.mean(0)
+    G = Xc.T @ Xc
+    want = scipy.linalg.solve(G + lam * np.eye(p), G @ Wstar)
+    W, b = oracle.ridge_fit(X, Y, lam=lam)
+    np.testing.assert_allclose(W, want, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b, Y.mean(0) - X.mean(0) @ want, rtol=1e-10, atol=1e-12)
+
+
+def test_ridge_equals_augmented_least_squares():
+    # Ridge on centred data = least squares on [Xc; sqrt(lam) I] vs [Yc; 0]
+    # (numpy lstsq, an SVD solver).
+    n, p, q, lam = 200, 8, 3, 0.01
+    X = RNG.standard_normal((n, p)) * np.arange(1, p + 1)
+    Y = RNG.standard_normal((n, q)) + X[:, :q] * 2
+    Xc, Yc = X - X.mean(0), Y - Y.mean(0)
+    A = np.vstack([Xc, math.sqrt(lam) * np.eye(p)])
+    B = np.vstack([Yc, np.zeros((p, q))])
+    want = np.linalg.lstsq(A, B, rcond=None)[0]
+    W, b = oracle.ridge_fit(X, Y, lam=lam)
+    np.testing.assert_allclose(W, want, rtol=1e-9, atol=1e-11)
