@@ -1,0 +1,466 @@
+"""Benchmark of the cross-model KV-cache transfer on GB300.
+
+One step = one ``kvx_transfer`` (gather, un-rotate, concatenate, map, re-rotate,
+install) over every target layer, head and token of the workload.  The default
+workload is the Qwen3-14B -> 32B shape at 32,768 tokens (40 -> 64 layers, 8 KV
+heads, head_dim 128, k = 4, bf16 caches, fp32 W, bf16 b, theta 1e6), with
+synthetic inputs resident in HBM.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+
+Multi-GPU: launched under torchrun each rank runs an independent replica of the
+whole transfer on its own GPU (the transfer has no exchange step); the line
+reports the tokens of all ranks over the slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV-transfer tokens/s at 14B→32B shape, 32K tokens; % of HBM/tensor roofline"
+# Published context for this exact workload: the Qwen3 14B -> 32B mapper at
+# 32,768 tokens took 277.6 ms on an 8xH100 node (Qwen3 KV-transfer article,
+# section on what the headline number covers).
+PUBLISHED_MS = {"qwen3_14b_32b": 277.6}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
+    ap.add_argument("--workload", default="qwen3_14b_32b")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tcgen05"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(tokens_per_rank_step: int, ms_per_step_local: float, device=None):
+    """Whole-job throughput: all ranks' tokens over the slowest rank's time."""
+    import torch.distributed as dist
+    ws = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    ms = max_over_ranks(ms_per_step_local, device)
+    return ws * tokens_per_rank_step / (ms / 1e3), ms
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            ident = []
+        self.cmd = ["nvidia-smi", *ident, "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", "50"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# roofline
+# --------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha(kernel_name: str) -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "cross_model_kv_transfer_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn == KERNEL_FILES.get(kernel_name) or fn.endswith((".h", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            rows = json.load(f)
+    except Exception:
+        return None
+    sha = kernel_source_sha(kernel_name)
+    for r in rows:
+        if r.get("workload") == workload and r.get("kernel") == kernel_name \
+                and r.get("source_sha") == sha:
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+def roofline(wl, layer_idx, ms_per_launch, kernel_name, peaks, peak_kind):
+    alg_bytes = wl.algorithmic_bytes(layer_idx)
+    flops = wl.algorithmic_flops()
+    s = ms_per_launch / 1e3
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    traffic = measured_traffic(wl.name, kernel_name)
+    if kernel_name == "tcgen05" and t_tc >= t_hbm:
+        r = {"bound": "tensor", "achieved": flops / s / 1e12, "peak": peaks["bf16_tflops"],
+             "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": alg_bytes / s / 1e9, "peak": peaks["hbm_gbs"],
+             "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["traffic"] = traffic
+    r["peak_source"] = f"{peak_kind} (burst)"
+    r["algorithmic_bytes"] = alg_bytes
+    r["algorithmic_flops"] = flops
+    r["hbm_frac"] = (alg_bytes / s / 1e9) / peaks["hbm_gbs"]
+    r["tensor_frac"] = (flops / s / 1e12) / peaks["bf16_tflops"]
+    r["tighter_roofline_frac"] = max(t_hbm, t_tc) / s
+    return r
+
+
+# --------------------------------------------------------------------------
+# CPU oracle on a bounded sample
+# --------------------------------------------------------------------------
+
+def oracle_sample_inputs(wl, inp, ntok_sample: int):
+    """fp64 copies of the first ``ntok_sample`` source tokens (one request)."""
+    import torch
+    f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
+    return dict(src_k=f64(inp["src_k"][:, :ntok_sample]), src_v=f64(inp["src_v"][:, :ntok_sample]),
+                layer_idx=inp["layer_idx"].cpu().numpy(), w=f64(inp["w"]), b=f64(inp["b"]),
+                theta_src=wl.theta_src, theta_tgt=wl.theta_tgt, max_position=ntok_sample,
+                dst_capacity=ntok_sample)
+
+
+def time_oracle(wl, inp, target_seconds: float):
+    """Tokens/s of the fp64 oracle (one host thread) on a bounded sample."""
+    import oracle
+    probe = oracle_sample_inputs(wl, inp, 1)
+    t0 = time.perf_counter()
+    oracle.transfer(**probe)
+    per_tok = max(time.perf_counter() - t0, 1e-4)
+    n = int(max(1, min(wl.ntok, target_seconds / per_tok)))
+    sample = oracle_sample_inputs(wl, inp, n)
+    t0 = time.perf_counter()
+    oracle.transfer(**sample)
+    el = time.perf_counter() - t0
+    return n / el, n, el
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def kernel_code(name):
+    from cross_model_kv_transfer_gb300 import kvx
+    return {"auto": kvx.KVX_KERNEL_AUTO, "simt": kvx.KVX_KERNEL_SIMT,
+            "tcgen05": kvx.KVX_KERNEL_TCGEN05}[name]
+
+
+def transfer_kwargs(wl, inp, dst_k, dst_v, status):
+    from cross_model_kv_transfer_gb300.workloads import PAGED
+    kw = dict(src_k=inp["src_k"], src_v=inp["src_v"], layer_idx=inp["layer_idx"], w=inp["w"],
+              b=inp["b"], dst_k=dst_k, dst_v=dst_v, status=status)
+    if wl.num_requests > 1 or wl.layout == PAGED:
+        kw["cu_seqlens"] = inp["cu_seqlens"]
+    if any(wl.tgt_offsets):
+        kw["tgt_offset"] = inp["tgt_offset"]
+    if wl.layout == PAGED:
+        kw.update(block_table=inp["block_table"], num_blocks=wl.num_blocks)
+    else:
+        kw["dst_capacity"] = wl.dst_capacity
+    return kw
+
+
+def run_kvx(args):
+    import torch
+    from cross_model_kv_transfer_gb300 import kvx
+    from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
+
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, dev)
+    plan = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers, kv_heads=wl.kv_heads,
+                    head_dim=wl.head_dim, k=wl.k, rope_theta_src=wl.theta_src,
+                    rope_theta_tgt=wl.theta_tgt, max_position=wl.max_position,
+                    kv_dtype=wl.kv_dtype, w_dtype=torch.float32, b_dtype=wl.b_dtype,
+                    layout=wl.layout, block_size=wl.block_size if wl.layout == PAGED else 0,
+                    kernel=kernel_code(args.kernel))
+    kname = {kvx.KVX_KERNEL_SIMT: "simt", kvx.KVX_KERNEL_TCGEN05: "tcgen05"}[plan.kernel]
+    shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
+    dst_k = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
+    dst_v = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    targs = plan.make_args(**transfer_kwargs(wl, inp, dst_k, dst_v, status))
+    stream = torch.cuda.current_stream(dev)
+    sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
+
+    def step():
+        st = kvx.kvx_transfer(plan.handle, targs, sptr)
+        if st != kvx.KVX_OK:
+            raise kvx.KvxError(st, "kvx_transfer")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    value, ms = aggregate(wl.ntok, ms_local, dev)
+
+    peaks, peak_kind = load_peaks()
+    roof = roofline(wl, inp["layer_idx"], ms_local, kname, peaks, peak_kind)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tps, n, el = time_oracle(wl, inp, args.cpu_seconds)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n} source tokens of the workload through all "
+                         f"{wl.tgt_layers} target layers x {wl.kv_heads} heads x K|V "
+                         f"({el:.1f} s of fp64 CPU work, one thread)"}
+    pub = PUBLISHED_MS.get(wl.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / (wl.ntok / (pub / 1e3))) if pub else None,
+        "dtype": "bf16" if wl.kv_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded; shapes and value recipe of the pages' workloads)",
+        "config": {"workload": wl.name, "src_layers": wl.src_layers,
+                   "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
+                   "head_dim": wl.head_dim, "k": wl.k, "tokens": wl.ntok,
+                   "requests": wl.num_requests,
+                   "layout": "paged" if wl.layout == PAGED else "contiguous",
+                   "kernel": kname, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (source "
+                         f"{inp['src_k'].numel() * 2 * inp['src_k'].element_size() / 1e9:.2f} GB,"
+                         " no flush needed)"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * plan.launches_per_transfer,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+
+
+def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status):
+    """Same metric through the C ABI with HOST buffers: every step copies its
+    inputs from pinned host memory, transfers, and reads the target cache back."""
+    import torch
+    from cross_model_kv_transfer_gb300 import kvx
+    names = ["src_k", "src_v", "w", "b", "layer_idx", "cu_seqlens", "tgt_offset"]
+    if "block_table" in inp:
+        names.append("block_table")
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    hk = torch.empty(dst_k.shape, dtype=dst_k.dtype, pin_memory=True)
+    hv = torch.empty(dst_v.shape, dtype=dst_v.dtype, pin_memory=True)
+    dev_in = {n: torch.empty_like(inp[n]) for n in names}
+    targs = plan.make_args(**transfer_kwargs(wl, dev_in, dst_k, dst_v, status))
+    sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = hk.numel() * hk.element_size() * 2
+
+    def step():
+        for n in names:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        st = kvx.kvx_transfer(plan.handle, targs, sptr)
+        if st != kvx.KVX_OK:
+            raise kvx.KvxError(st, "kvx_transfer")
+        hk.copy_(dst_k, non_blocking=True)
+        hv.copy_(dst_v, non_blocking=True)
+
+    steps = max(1, min(args.steps, 20))
+    for _ in range(min(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms_local = ev0.elapsed_time(ev1) / steps
+    value, ms = aggregate(wl.ntok, ms_local, dev)
+    return {"value": value, "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_reference(args):
+    """The fp64 oracle, as it stands, on the machine's host cores: each step is a
+    bounded sample (a few source tokens through every target layer, head and
+    K|V) of the same workload."""
+    import torch
+    import oracle
+    from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    per_step = 2
+    small = wl.with_tokens([per_step], [0])
+    inp = make_inputs(small, "cpu")
+    sample = oracle_sample_inputs(small, inp, per_step)
+    for _ in range(args.warmup):
+        oracle.transfer(**sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.transfer(**sample)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "src_layers": wl.src_layers,
+                   "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
+                   "head_dim": wl.head_dim, "k": wl.k, "tokens": wl.ntok,
+                   "layout": "paged" if wl.layout == PAGED else "contiguous"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} source tokens per step through all "
+                                   f"{wl.tgt_layers} target layers x {wl.kv_heads} heads x K|V"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvx(args)
+
+
+if __name__ == "__main__":
+    main()

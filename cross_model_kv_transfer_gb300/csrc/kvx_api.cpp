@@ -1,0 +1,228 @@
+// kvx_api.cpp -- host side of the C ABI declared in include/kvx.h: argument
+// validation, plan creation (RoPE tables), kernel selection and launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kvx_internal.h"
+
+namespace {
+
+bool valid_dtype(int32_t t) { return t == KVX_F32 || t == KVX_BF16; }
+
+kvx_status validate_desc(const kvx_plan_desc *d) {
+  if (!d) return KVX_ERR_INVALID_ARG;
+  if (d->src_layers < 1 || d->tgt_layers < 1 || d->k < 1 || d->k > 64)
+    return KVX_ERR_INVALID_ARG;
+  if (d->src_kv_heads < 1 || d->tgt_kv_heads < 1) return KVX_ERR_INVALID_ARG;
+  if (d->src_head_dim < 2 || d->tgt_head_dim < 2 || d->src_head_dim > 256 ||
+      d->tgt_head_dim > 256 || (d->src_head_dim & 1) || (d->tgt_head_dim & 1))
+    return KVX_ERR_INVALID_ARG;
+  if (!(std::isfinite(d->rope_theta_src) && d->rope_theta_src > 0.0) ||
+      !(std::isfinite(d->rope_theta_tgt) && d->rope_theta_tgt > 0.0))
+    return KVX_ERR_INVALID_ARG;
+  if (!valid_dtype(d->kv_dtype) || !valid_dtype(d->w_dtype) || !valid_dtype(d->b_dtype))
+    return KVX_ERR_INVALID_ARG;
+  if (d->dst_layout != KVX_CONTIGUOUS && d->dst_layout != KVX_PAGED)
+    return KVX_ERR_INVALID_ARG;
+  if (d->dst_layout == KVX_PAGED && d->block_size < 1) return KVX_ERR_INVALID_ARG;
+  if (d->max_position < 1) return KVX_ERR_INVALID_ARG;
+  if (d->kernel != KVX_KERNEL_AUTO && d->kernel != KVX_KERNEL_SIMT &&
+      d->kernel != KVX_KERNEL_TCGEN05)
+    return KVX_ERR_INVALID_ARG;
+  // "Requirements": same number of KV heads and the same per-head dimension.
+  if (d->src_kv_heads != d->tgt_kv_heads || d->src_head_dim != d->tgt_head_dim)
+    return KVX_ERR_PAIR_MISMATCH;
+  return KVX_OK;
+}
+
+// cos/sin of p * theta^(-2i/d) for p in [0, max_position), i in [0, d/2):
+// angles and trigonometry in double precision, rounded once to fp32.
+std::vector<float2> rope_table(double theta, int d, int max_position) {
+  const int half = d / 2;
+  std::vector<float2> t((size_t)max_position * half);
+  for (int i = 0; i < half; ++i) {
+    const double w = std::pow(theta, -2.0 * (double)i / (double)d);
+    for (int p = 0; p < max_position; ++p) {
+      const double a = (double)p * w;
+      t[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  }
+  return t;
+}
+
+kvx_status upload(const std::vector<float2> &h, float2 **dptr) {
+  size_t bytes = h.size() * sizeof(float2);
+  cudaError_t e = cudaMalloc((void **)dptr, bytes);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    *dptr = nullptr;
+    return KVX_ERR_NO_MEMORY;
+  }
+  if (e != cudaSuccess) {
+    *dptr = nullptr;
+    return KVX_ERR_CUDA;
+  }
+  if (cudaMemcpy(*dptr, h.data(), bytes, cudaMemcpyHostToDevice) != cudaSuccess)
+    return KVX_ERR_CUDA;
+  return KVX_OK;
+}
+
+void free_tables(kvx_plan *p) {
+  if (p->rope_tgt && p->rope_tgt != p->rope_src) cudaFree(p->rope_tgt);
+  if (p->rope_src) cudaFree(p->rope_src);
+  p->rope_src = p->rope_tgt = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvx_status_string(kvx_status s) {
+  switch (s) {
+    case KVX_OK: return "ok";
+    case KVX_ERR_INVALID_ARG: return "invalid argument";
+    case KVX_ERR_PAIR_MISMATCH:
+      return "source and target differ in KV-head count or head dimension";
+    case KVX_ERR_UNSUPPORTED: return "unsupported device or configuration";
+    case KVX_ERR_CUDA: return "CUDA runtime error";
+    case KVX_ERR_NO_MEMORY: return "out of device memory";
+  }
+  return "unknown status";
+}
+
+kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
+  if (!out) return KVX_ERR_INVALID_ARG;
+  *out = nullptr;
+  kvx_status st = validate_desc(desc);
+  if (st != KVX_OK) return st;
+
+  int kernel = desc->kernel;
+  if (kernel == KVX_KERNEL_AUTO)
+    kernel = kvx_tc_supports(*desc) ? KVX_KERNEL_TCGEN05 : KVX_KERNEL_SIMT;
+  if (kernel == KVX_KERNEL_TCGEN05 && !kvx_tc_supports(*desc)) return KVX_ERR_UNSUPPORTED;
+  if (kernel == KVX_KERNEL_SIMT && !kvx_simt_supports(*desc)) return KVX_ERR_UNSUPPORTED;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) {
+    cudaGetLastError();
+    return KVX_ERR_UNSUPPORTED;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVX_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return KVX_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return KVX_ERR_UNSUPPORTED;  // sm_103 only
+
+  kvx_plan *p = new (std::nothrow) kvx_plan();
+  if (!p) return KVX_ERR_NO_MEMORY;
+  p->desc = *desc;
+  p->device = dev;
+  p->kernel = kernel;
+  p->num_sms = prop.multiProcessorCount;
+  p->half = desc->src_head_dim / 2;
+
+  st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
+              &p->rope_src);
+  if (st == KVX_OK) {
+    if (desc->rope_theta_tgt == desc->rope_theta_src)
+      p->rope_tgt = p->rope_src;
+    else
+      st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
+                  &p->rope_tgt);
+  }
+  if (st == KVX_OK) {
+    cudaError_t e = kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_prepare(p) : kvx_simt_prepare(p);
+    if (e != cudaSuccess) st = KVX_ERR_CUDA;
+  }
+  if (st != KVX_OK) {
+    free_tables(p);
+    delete p;
+    return st;
+  }
+  *out = p;
+  return KVX_OK;
+}
+
+kvx_status kvx_plan_destroy(kvx_plan *plan) {
+  if (!plan) return KVX_OK;
+  int cur = 0;
+  bool switched = false;
+  if (cudaGetDevice(&cur) == cudaSuccess && cur != plan->device) {
+    if (cudaSetDevice(plan->device) == cudaSuccess) switched = true;
+  }
+  cudaDeviceSynchronize();
+  free_tables(plan);
+  if (switched) cudaSetDevice(cur);
+  delete plan;
+  return KVX_OK;
+}
+
+int32_t kvx_plan_kernel(const kvx_plan *plan) { return plan ? plan->kernel : -1; }
+
+int32_t kvx_plan_launches(const kvx_plan *plan) { return plan ? 1 : -1; }
+
+kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *stream) {
+  if (!plan || !a) return KVX_ERR_INVALID_ARG;
+  const kvx_plan_desc &d = plan->desc;
+  if (a->ntok < 0 || a->ntok > INT32_MAX) return KVX_ERR_INVALID_ARG;
+  if (a->num_requests < 1) return KVX_ERR_INVALID_ARG;
+  if (!a->cu_seqlens && a->num_requests != 1) return KVX_ERR_INVALID_ARG;
+  if (!a->src_k || !a->src_v || !a->layer_idx || !a->w || !a->b || !a->dst_k || !a->dst_v)
+    return KVX_ERR_INVALID_ARG;
+  if (d.dst_layout == KVX_CONTIGUOUS) {
+    if (a->dst_capacity < 1) return KVX_ERR_INVALID_ARG;
+  } else {
+    if (a->num_blocks < 1 || !a->block_table || a->max_blocks_per_req < 1)
+      return KVX_ERR_INVALID_ARG;
+  }
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return KVX_ERR_CUDA;
+  if (cur != plan->device) return KVX_ERR_INVALID_ARG;
+  if (a->ntok == 0) return KVX_OK;  // nothing to transfer; status untouched
+
+  KvxParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.src_k = a->src_k;
+  p.src_v = a->src_v;
+  p.w = a->w;
+  p.b = a->b;
+  p.dst_k = a->dst_k;
+  p.dst_v = a->dst_v;
+  p.cu_seqlens = a->cu_seqlens;
+  p.layer_idx = a->layer_idx;
+  p.src_pos = a->src_pos;
+  p.tgt_pos = a->tgt_pos;
+  p.tgt_offset = a->tgt_offset;
+  p.block_table = a->block_table;
+  p.status = a->status;
+  p.rope_src = plan->rope_src;
+  p.rope_tgt = plan->rope_tgt;
+  p.ntok = a->ntok;
+  p.dst_capacity = a->dst_capacity;
+  p.num_blocks = a->num_blocks;
+  p.dst_rows = d.dst_layout == KVX_CONTIGUOUS
+                   ? (int64_t)a->num_requests * a->dst_capacity
+                   : a->num_blocks * (int64_t)d.block_size;
+  p.R = a->num_requests;
+  p.max_blocks = a->max_blocks_per_req;
+  p.Ls = d.src_layers;
+  p.Lt = d.tgt_layers;
+  p.H = d.src_kv_heads;
+  p.d = d.src_head_dim;
+  p.k = d.k;
+  p.layout = d.dst_layout;
+  p.block_size = d.block_size;
+  p.max_position = d.max_position;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = plan->kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_launch(plan, p, s)
+                                                     : kvx_simt_launch(plan, p, s);
+  return e == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// kvx_internal.h -- plan object and kernel parameter block shared by the
+// host API (kvx_api.cpp) and the kernels (kvx_simt.cu, kvx_tcgen05.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvx.h"
+
+struct kvx_plan {
+  kvx_plan_desc desc;
+  int device;
+  int kernel;            // KVX_KERNEL_SIMT or KVX_KERNEL_TCGEN05
+  int num_sms;
+  int half;              // head_dim / 2
+  // RoPE tables: rope[p * half + i] = (cos, sin)(p * theta^(-2i/d)),
+  // p in [0, max_position), computed in double on the host, stored fp32.
+  float2 *rope_src;
+  float2 *rope_tgt;      // aliases rope_src when the two thetas are equal
+};
+
+// Everything a kernel needs, passed by value.
+struct KvxParams {
+  const void *src_k, *src_v;
+  const void *w, *b;
+  void *dst_k, *dst_v;
+  const int32_t *cu_seqlens, *layer_idx, *src_pos, *tgt_pos, *tgt_offset;
+  const int32_t *block_table;
+  uint32_t *status;
+  const float2 *rope_src, *rope_tgt;
+  int64_t ntok, dst_capacity, num_blocks, dst_rows;
+  int32_t R, max_blocks;
+  int32_t Ls, Lt, H, d, k, layout, block_size, max_position;
+};
+
+// Per-kernel launchers; return cudaSuccess or the launch error.
+cudaError_t kvx_simt_prepare(const kvx_plan *plan);
+cudaError_t kvx_simt_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);
+bool kvx_simt_supports(const kvx_plan_desc &d);
+
+bool kvx_tc_supports(const kvx_plan_desc &d);
+cudaError_t kvx_tc_prepare(const kvx_plan *plan);
+cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);

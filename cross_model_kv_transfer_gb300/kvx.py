@@ -1,0 +1,258 @@
+"""ctypes binding of the kvx C ABI (``include/kvx.h``).
+
+Argument marshalling only: the functions below have the C names and pass
+device pointers straight through; every step of the transfer runs in the
+CUDA kernels of ``libkvx.so``.  There is no fallback: if the library cannot
+be loaded (or built with nvcc on first use), importing the symbols raises.
+
+Low level (same names as the C ABI): ``kvx_plan_create``, ``kvx_transfer``,
+``kvx_plan_destroy``, ``kvx_status_string``, ``kvx_plan_kernel`` taking the
+ctypes structures ``PlanDesc`` / ``TransferArgs``.
+
+Convenience: ``Plan`` (owns a plan handle) and ``Plan.transfer(...)`` which
+takes torch CUDA tensors, checks their shapes, dtypes and devices, and calls
+``kvx_transfer`` on the current torch stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+# --- constants mirrored from include/kvx.h ---------------------------------
+KVX_OK = 0
+KVX_ERR_INVALID_ARG = 1
+KVX_ERR_PAIR_MISMATCH = 2
+KVX_ERR_UNSUPPORTED = 3
+KVX_ERR_CUDA = 4
+KVX_ERR_NO_MEMORY = 5
+
+KVX_FLAG_BAD_LAYER_INDEX = 1
+KVX_FLAG_BAD_POSITION = 2
+KVX_FLAG_BAD_BLOCK = 4
+KVX_FLAG_BAD_ROW = 8
+KVX_FLAG_TIMEOUT = 16
+KVX_FLAG_BAD_SEQLENS = 32
+
+KVX_F32 = 0
+KVX_BF16 = 1
+KVX_CONTIGUOUS = 0
+KVX_PAGED = 1
+KVX_KERNEL_AUTO = 0
+KVX_KERNEL_SIMT = 1
+KVX_KERNEL_TCGEN05 = 2
+
+EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
+            "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches")
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [
+        ("src_layers", ctypes.c_int32), ("tgt_layers", ctypes.c_int32),
+        ("src_kv_heads", ctypes.c_int32), ("tgt_kv_heads", ctypes.c_int32),
+        ("src_head_dim", ctypes.c_int32), ("tgt_head_dim", ctypes.c_int32),
+        ("k", ctypes.c_int32),
+        ("rope_theta_src", ctypes.c_double), ("rope_theta_tgt", ctypes.c_double),
+        ("kv_dtype", ctypes.c_int32), ("w_dtype", ctypes.c_int32), ("b_dtype", ctypes.c_int32),
+        ("dst_layout", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("max_position", ctypes.c_int32), ("kernel", ctypes.c_int32),
+    ]
+
+
+class TransferArgs(ctypes.Structure):
+    _fields_ = [
+        ("src_k", ctypes.c_void_p), ("src_v", ctypes.c_void_p),
+        ("ntok", ctypes.c_int64), ("num_requests", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p), ("layer_idx", ctypes.c_void_p),
+        ("w", ctypes.c_void_p), ("b", ctypes.c_void_p),
+        ("src_pos", ctypes.c_void_p), ("tgt_pos", ctypes.c_void_p),
+        ("tgt_offset", ctypes.c_void_p),
+        ("dst_k", ctypes.c_void_p), ("dst_v", ctypes.c_void_p),
+        ("dst_capacity", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p), ("max_blocks_per_req", ctypes.c_int32),
+        ("status", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load ``libkvx.so`` (building it with nvcc if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"kvx CUDA library missing: {path}")
+            lib = ctypes.CDLL(path)
+            lib.kvx_plan_create.argtypes = [ctypes.POINTER(PlanDesc),
+                                            ctypes.POINTER(ctypes.c_void_p)]
+            lib.kvx_plan_create.restype = ctypes.c_int
+            lib.kvx_transfer.argtypes = [ctypes.c_void_p, ctypes.POINTER(TransferArgs),
+                                         ctypes.c_void_p]
+            lib.kvx_transfer.restype = ctypes.c_int
+            lib.kvx_plan_destroy.argtypes = [ctypes.c_void_p]
+            lib.kvx_plan_destroy.restype = ctypes.c_int
+            lib.kvx_status_string.argtypes = [ctypes.c_int]
+            lib.kvx_status_string.restype = ctypes.c_char_p
+            lib.kvx_plan_kernel.argtypes = [ctypes.c_void_p]
+            lib.kvx_plan_kernel.restype = ctypes.c_int32
+            lib.kvx_plan_launches.argtypes = [ctypes.c_void_p]
+            lib.kvx_plan_launches.restype = ctypes.c_int32
+            _lib = lib
+    return _lib
+
+
+def kvx_plan_create(desc: PlanDesc):
+    """Returns (status, plan handle or None)."""
+    h = ctypes.c_void_p()
+    st = load().kvx_plan_create(ctypes.byref(desc), ctypes.byref(h))
+    return st, (h.value if st == KVX_OK else None)
+
+
+def kvx_transfer(plan, args: TransferArgs, stream) -> int:
+    return load().kvx_transfer(plan, ctypes.byref(args), stream)
+
+
+def kvx_plan_destroy(plan) -> int:
+    return load().kvx_plan_destroy(plan)
+
+
+def kvx_status_string(status: int) -> str:
+    return load().kvx_status_string(int(status)).decode()
+
+
+def kvx_plan_kernel(plan) -> int:
+    return load().kvx_plan_kernel(plan)
+
+
+def kvx_plan_launches(plan) -> int:
+    return load().kvx_plan_launches(plan)
+
+
+class KvxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {kvx_status_string(status)} (status {status})")
+        self.status = status
+
+
+def _dtype_code(dt) -> int:
+    import torch
+    if dt == torch.float32:
+        return KVX_F32
+    if dt == torch.bfloat16:
+        return KVX_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+class Plan:
+    """A kvx plan for one (source, target) model pair on the current device."""
+
+    def __init__(self, *, src_layers, tgt_layers, kv_heads, head_dim, k, rope_theta_src,
+                 rope_theta_tgt, max_position, kv_dtype, w_dtype, b_dtype,
+                 layout=KVX_CONTIGUOUS, block_size=0, kernel=KVX_KERNEL_AUTO,
+                 tgt_kv_heads=None, tgt_head_dim=None):
+        self.desc = PlanDesc(
+            src_layers, tgt_layers, kv_heads,
+            kv_heads if tgt_kv_heads is None else tgt_kv_heads,
+            head_dim, head_dim if tgt_head_dim is None else tgt_head_dim, k,
+            float(rope_theta_src), float(rope_theta_tgt),
+            _dtype_code(kv_dtype), _dtype_code(w_dtype), _dtype_code(b_dtype),
+            int(layout), int(block_size), int(max_position), int(kernel))
+        self.kv_dtype, self.w_dtype, self.b_dtype = kv_dtype, w_dtype, b_dtype
+        st, h = kvx_plan_create(self.desc)
+        if st != KVX_OK:
+            raise KvxError(st, "kvx_plan_create")
+        self.handle = h
+
+    @property
+    def kernel(self) -> int:
+        return kvx_plan_kernel(self.handle)
+
+    @property
+    def launches_per_transfer(self) -> int:
+        return kvx_plan_launches(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            kvx_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def make_args(self, *, src_k, src_v, layer_idx, w, b, dst_k, dst_v, cu_seqlens=None,
+                  src_pos=None, tgt_pos=None, tgt_offset=None,
+                  dst_capacity=None, num_blocks=None, block_table=None,
+                  status=None) -> TransferArgs:
+        """Check tensors against the plan and pack a ``TransferArgs``."""
+        import torch
+        d = self.desc
+        Ls, Lt, H, hd, k = d.src_layers, d.tgt_layers, d.src_kv_heads, d.src_head_dim, d.k
+
+        def ptr(t, name, dtype, shape=None, ndim=None):
+            if t is None:
+                return None
+            if not isinstance(t, torch.Tensor) or not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor")
+            if t.dtype != dtype:
+                raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+            if shape is not None and tuple(t.shape) != tuple(shape):
+                raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+            if ndim is not None and t.dim() != ndim:
+                raise ValueError(f"{name} must have {ndim} dims")
+            return t.data_ptr()
+
+        ntok = src_k.shape[1]
+        R = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+        a = TransferArgs()
+        a.src_k = ptr(src_k, "src_k", self.kv_dtype, (Ls, ntok, H, hd))
+        a.src_v = ptr(src_v, "src_v", self.kv_dtype, (Ls, ntok, H, hd))
+        a.ntok = ntok
+        a.num_requests = R
+        a.cu_seqlens = ptr(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
+        a.layer_idx = ptr(layer_idx, "layer_idx", torch.int32, (Lt, k))
+        a.w = ptr(w, "w", self.w_dtype, (Lt, H, 2, k * hd, hd))
+        a.b = ptr(b, "b", self.b_dtype, (Lt, H, 2, hd))
+        a.src_pos = ptr(src_pos, "src_pos", torch.int32, (ntok,))
+        a.tgt_pos = ptr(tgt_pos, "tgt_pos", torch.int32, (ntok,))
+        a.tgt_offset = ptr(tgt_offset, "tgt_offset", torch.int32, (R,))
+        if d.dst_layout == KVX_CONTIGUOUS:
+            cap = int(dst_capacity) if dst_capacity is not None else dst_k.shape[1] // R
+            rows = R * cap
+            a.dst_capacity = cap
+        else:
+            nb = int(num_blocks) if num_blocks is not None else dst_k.shape[1] // d.block_size
+            rows = nb * d.block_size
+            a.num_blocks = nb
+            a.block_table = ptr(block_table, "block_table", torch.int32, ndim=2)
+            a.max_blocks_per_req = int(block_table.shape[1])
+        a.dst_k = ptr(dst_k, "dst_k", self.kv_dtype, (Lt, rows, H, hd))
+        a.dst_v = ptr(dst_v, "dst_v", self.kv_dtype, (Lt, rows, H, hd))
+        a.status = ptr(status, "status", torch.int32, (1,))
+        a._keep = (src_k, src_v, cu_seqlens, layer_idx, w, b, src_pos, tgt_pos, tgt_offset,
+                   dst_k, dst_v, block_table, status)
+        return a
+
+    def transfer(self, stream=None, **tensors) -> None:
+        """Enqueue one transfer on ``stream`` (default: torch's current stream)."""
+        import torch
+        args = self.make_args(**tensors)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        st = kvx_transfer(self.handle, args, ctypes.c_void_p(stream.cuda_stream))
+        if st != KVX_OK:
+            raise KvxError(st, "kvx_transfer")

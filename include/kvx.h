@@ -1,0 +1,189 @@
+/*
+ * kvx.h -- C ABI of the GB300 cross-model KV-cache transfer library.
+ *
+ * What it computes.  A pilot (source) model has filled its KV cache for a
+ * prompt; a larger target model of the same family is to continue from it
+ * without re-reading the prompt.  For every target layer lt, KV head h and
+ * token, the library
+ *   1. gathers the head-h key and value vectors of the k source layers
+ *      idx[lt][0..k-1] selected for lt,
+ *   2. un-rotates each key out of the source model's RoPE at its source
+ *      position p (half-split pairs (i, i + d/2), frequency
+ *      theta_src^(-2i/d)),
+ *   3. concatenates the k content vectors (width k*d, index-table order),
+ *   4. applies the per-(target layer, head) linear map y = x W + b, one map
+ *      for keys (m = 0) and one for values (m = 1),
+ *   5. re-rotates the mapped key into the target RoPE (theta_tgt) at the
+ *      position p' it will occupy in the target sequence,
+ *   6. stores both into the target cache, contiguous or paged.
+ * Sources: "Helm Intelligent Routing" (docs.iterate.ai), section "Why
+ * carrying the cache across is the hard part", steps 1-3 (un-rotate, map,
+ * re-rotate; re-rotation has no skip switch), section "Requirements" (the
+ * pair must share KV-head count and head dimension; layer counts may differ)
+ * and section "Current limitation" (install into the engine's paged cache);
+ * "Перенос KV-кэша между моделями Qwen3 вместо повторного префилла"
+ * (reactapp.top), section "Линейного моста, как ни странно, хватает"
+ * (selected source layers' features concatenated; one ridge map per target
+ * (layer, head), separately for keys and values; strip source RoPE, map,
+ * apply target RoPE); knlp.io routing page, the connector's inject step
+ * (writes into the paged cache through a block table).
+ *
+ * Execution model.  kvx_plan_create / kvx_plan_destroy may allocate, free
+ * and synchronise.  kvx_transfer only validates its arguments on the host
+ * and enqueues kernels on the given stream: it never synchronises and never
+ * allocates.  A plan is immutable after creation and may be used from
+ * several host threads and streams at once.  All tensors are owned by the
+ * caller; the plan owns only its RoPE tables.
+ *
+ * Errors.  Every call returns a kvx_status.  Host-detectable errors are
+ * returned before anything is enqueued, and nothing is written.  Errors only
+ * the device can see (an index-table entry outside [0, src_layers), a
+ * position outside [0, max_position), a block id outside [0, num_blocks), a
+ * contiguous row beyond the capacity, a malformed request table, a pipeline
+ * wait that gave up) never trap: the affected rows are skipped (all rows,
+ * for a malformed request table) and the matching KVX_FLAG_* bits are OR-ed
+ * into the caller's status word.  When
+ * that word is non-zero after the stream completes, the destination rows of
+ * this transfer are unspecified and the caller falls back to a normal
+ * prefill of the target ("What happens when a transfer cannot be used":
+ * every refusal falls back to prefill).
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVX_OK = 0,
+  KVX_ERR_INVALID_ARG = 1,    /* a NULL pointer, negative size, bad enum    */
+  KVX_ERR_PAIR_MISMATCH = 2,  /* source/target KV heads or head_dim differ  */
+  KVX_ERR_UNSUPPORTED = 3,    /* valid, but not supported by this build or
+                                 device (e.g. not sm_103, kernel forced onto
+                                 a shape it does not handle)                 */
+  KVX_ERR_CUDA = 4,           /* a CUDA runtime call failed                  */
+  KVX_ERR_NO_MEMORY = 5       /* plan tables could not be allocated          */
+} kvx_status;
+
+/* Bits OR-ed into kvx_transfer_args.status by the device. */
+#define KVX_FLAG_BAD_LAYER_INDEX 1u  /* idx[lt][j] outside [0, src_layers)    */
+#define KVX_FLAG_BAD_POSITION    2u  /* p or p' outside [0, max_position)     */
+#define KVX_FLAG_BAD_BLOCK       4u  /* p'/bs >= max_blocks_per_req, or the
+                                        block id outside [0, num_blocks)     */
+#define KVX_FLAG_BAD_ROW         8u  /* contiguous p' >= dst_capacity         */
+#define KVX_FLAG_TIMEOUT        16u  /* a pipeline wait gave up              */
+#define KVX_FLAG_BAD_SEQLENS    32u  /* cu_seqlens does not start at 0, runs
+                                        backwards or does not end at ntok:
+                                        nothing is written                   */
+
+typedef enum { KVX_F32 = 0, KVX_BF16 = 1 } kvx_dtype;
+typedef enum { KVX_CONTIGUOUS = 0, KVX_PAGED = 1 } kvx_layout;
+typedef enum {
+  KVX_KERNEL_AUTO = 0,        /* tensor-core path when the shape allows it  */
+  KVX_KERNEL_SIMT = 1,        /* fp32 FMA contraction (any even head_dim)   */
+  KVX_KERNEL_TCGEN05 = 2      /* tcgen05 tensor cores: bf16 K/V,
+                                 head_dim 128                                */
+} kvx_kernel;
+
+/* Plan descriptor.  The source and target KV-head counts and head
+ * dimensions are given separately so that an incompatible pair is refused
+ * with KVX_ERR_PAIR_MISMATCH ("Requirements": same number of KV heads and
+ * the same per-head dimension; layer counts may differ freely). */
+typedef struct {
+  int32_t src_layers;       /* Ls >= 1                                        */
+  int32_t tgt_layers;       /* Lt >= 1                                        */
+  int32_t src_kv_heads;     /* H, must equal tgt_kv_heads                     */
+  int32_t tgt_kv_heads;
+  int32_t src_head_dim;     /* d, even, 2..256; must equal tgt_head_dim       */
+  int32_t tgt_head_dim;
+  int32_t k;                /* selected source layers per target layer, >= 1 */
+  double rope_theta_src;    /* RoPE base of the source model, > 1             */
+  double rope_theta_tgt;    /* RoPE base of the target model, > 1             */
+  int32_t kv_dtype;         /* kvx_dtype of source and target K/V             */
+  int32_t w_dtype;          /* kvx_dtype of W                                 */
+  int32_t b_dtype;          /* kvx_dtype of b                                 */
+  int32_t dst_layout;       /* kvx_layout of the target cache                 */
+  int32_t block_size;       /* tokens per block, PAGED only (>= 1)            */
+  int32_t max_position;     /* every source and target position must lie in
+                               [0, max_position); sizes the RoPE tables      */
+  int32_t kernel;           /* kvx_kernel                                    */
+} kvx_plan_desc;
+
+typedef struct kvx_plan kvx_plan; /* opaque */
+
+/* Arguments of one transfer.  All pointers are DEVICE pointers to memory of
+ * the current device, except where noted; arrays are dense, row-major, with
+ * the element type fixed by the plan.  ntok = total source tokens of all
+ * requests, packed request after request. */
+typedef struct {
+  const void *src_k;          /* [Ls][ntok][H][d]  source keys (RoPE-rotated) */
+  const void *src_v;          /* [Ls][ntok][H][d]  source values              */
+  int64_t ntok;               /* >= 0 (0: nothing to do)                      */
+  int32_t num_requests;       /* R >= 1                                       */
+  const int32_t *cu_seqlens;  /* [R+1] request r owns source rows
+                                 [cu[r], cu[r+1]); must start at 0, never
+                                 decrease and end at ntok (else nothing is
+                                 written and KVX_FLAG_BAD_SEQLENS is set).
+                                 NULL means R == 1 and the single request
+                                 owns all ntok rows                          */
+  const int32_t *layer_idx;   /* [Lt][k] selected source layers, in
+                                 feature-concatenation order                 */
+  const void *w;              /* [Lt][H][2][k*d][d] map, m = 0 keys, 1 values;
+                                 rows follow the concatenation order         */
+  const void *b;              /* [Lt][H][2][d] bias                           */
+  const int32_t *src_pos;     /* [ntok] source positions, or NULL: 0..len-1
+                                 within each request                         */
+  const int32_t *tgt_pos;     /* [ntok] target positions, or NULL:
+                                 p' = p + tgt_offset[r]                      */
+  const int32_t *tgt_offset;  /* [R] or NULL (offset 0)                       */
+  void *dst_k;                /* CONTIGUOUS: [Lt][R*dst_capacity][H][d], row
+                                 r*dst_capacity + p';  PAGED:
+                                 [Lt][num_blocks*block_size][H][d], row
+                                 block_table[r][p'/bs]*bs + p' % bs          */
+  void *dst_v;                /* same layout as dst_k                         */
+  int64_t dst_capacity;       /* CONTIGUOUS: rows per request (>= 1)          */
+  int64_t num_blocks;         /* PAGED: blocks in the pool (>= 1)             */
+  const int32_t *block_table; /* PAGED: [R][max_blocks_per_req]               */
+  int32_t max_blocks_per_req; /* PAGED: >= 1                                  */
+  uint32_t *status;           /* optional device word; KVX_FLAG_* bits are
+                                 OR-ed in (never cleared by the library)     */
+} kvx_transfer_args;
+
+/* Validate the descriptor, build the RoPE tables (cos/sin of p * w_i for
+ * p in [0, max_position), computed in double precision on the host and
+ * stored as fp32) on the current device and return an opaque plan in *out.
+ * Returns KVX_ERR_INVALID_ARG / KVX_ERR_PAIR_MISMATCH for a bad descriptor
+ * (before touching the device), KVX_ERR_UNSUPPORTED if the current device
+ * is not sm_103 or the forced kernel cannot handle the shape, KVX_ERR_CUDA or
+ * KVX_ERR_NO_MEMORY if the device work fails.  On error *out is NULL. */
+kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out);
+
+/* Enqueue one transfer on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream).  Asynchronous: no host synchronisation, no allocation.
+ * Returns KVX_ERR_INVALID_ARG for a NULL plan/args or a missing required
+ * pointer or size, KVX_ERR_CUDA if a launch fails.  Device-detected errors
+ * are reported through args->status as described above. */
+kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *args,
+                        void *stream);
+
+/* Free the plan's tables (synchronises the device).  NULL is a no-op. */
+kvx_status kvx_plan_destroy(kvx_plan *plan);
+
+/* Static, NUL-terminated description of a status code. */
+const char *kvx_status_string(kvx_status status);
+
+/* Which kernel the plan runs (KVX_KERNEL_SIMT or KVX_KERNEL_TCGEN05), or -1
+ * for a NULL plan. */
+int32_t kvx_plan_kernel(const kvx_plan *plan);
+
+/* Number of kernel launches one kvx_transfer call enqueues with this plan
+ * (0 when ntok == 0), or -1 for a NULL plan. */
+int32_t kvx_plan_launches(const kvx_plan *plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVX_H */

@@ -107,6 +107,14 @@ int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
                            : P->num_blocks * P->block_size;
   int status = 0;
 
+  /* a malformed request table invalidates the whole transfer */
+  if (P->cu_seqlens) {
+    int ok = P->cu_seqlens[0] == 0 && P->cu_seqlens[P->num_requests] == ntok;
+    for (int64_t r = 0; r < P->num_requests; ++r)
+      if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;
+    if (!ok) return KVXO_BAD_SEQLENS;
+  }
+
   const double **krows = (const double **)malloc(sizeof(double *) * (size_t)k);
   const double **vrows = (const double **)malloc(sizeof(double *) * (size_t)k);
   double *ok = (double *)malloc(sizeof(double) * (size_t)d);
@@ -126,10 +134,6 @@ int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
   for (int64_t r = 0; r < P->num_requests; ++r) {
     int64_t beg = P->cu_seqlens ? P->cu_seqlens[r] : 0;
     int64_t end = P->cu_seqlens ? P->cu_seqlens[r + 1] : ntok;
-    if (beg < 0 || end < beg || end > ntok) {
-      status |= KVXO_BAD_SEQLENS;
-      continue;
-    }
     for (int64_t g = beg; g < end; ++g) {
       int64_t p = P->src_pos ? P->src_pos[g] : g - beg;
       int64_t off = P->tgt_offset ? P->tgt_offset[r] : 0;

@@ -34,8 +34,9 @@
  *  - The feature vector of target head h is the concatenation, in index-table
  *    order, of the k selected source layers' head-h vectors (width k*d);
  *    W[lt][h][m] is [k*d][d] row-major, m = 0 for K and 1 for V.
- *  - Request r owns source rows [cu_seqlens[r], cu_seqlens[r+1]); a request
- *    whose range is not inside [0, ntok] or runs backwards is skipped.
+ *  - Request r owns source rows [cu_seqlens[r], cu_seqlens[r+1]).  The
+ *    request table must start at 0, never decrease and end at ntok; if it
+ *    does not, nothing is written and only KVXO_BAD_SEQLENS is returned.
  *  - The target position p' sets both the re-rotation angle and the cache
  *    row.  p' = tgt_pos[g] if given, else p + tgt_offset[r] (0 if absent).
  *    Source and target positions must lie in [0, max_position).

@@ -1,0 +1,86 @@
+"""Parity at full workload sizes, in the launch configuration the benchmark
+times: the whole transfer runs on the GPU, and sampled output rows are
+recomputed one by one by the fp64 oracle (``oracle.map_token`` / ``dst_row``).
+Every row outside the transfer must keep its sentinel bits (checked on the
+device for the whole cache)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
+
+from parity import TOL, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SAMPLES = 48
+
+
+def _sample_rows(wl, inp, seed):
+    g = np.random.default_rng(seed)
+    cu = inp["cu_seqlens"].cpu().numpy()
+    offs = inp["tgt_offset"].cpu().numpy()
+    out = []
+    for _ in range(SAMPLES):
+        r = int(g.integers(wl.num_requests))
+        n = int(cu[r + 1] - cu[r])
+        pos = int(g.choice([0, n - 1, int(g.integers(n))]))
+        out.append((r, int(cu[r]) + pos, pos, pos + int(offs[r]),
+                    int(g.integers(wl.tgt_layers)), int(g.integers(wl.kv_heads))))
+    return out
+
+
+def _written_mask(wl, inp):
+    """[rows] bool on the device: rows some token of the transfer lands in."""
+    rows = torch.zeros(wl.dst_rows, dtype=torch.bool, device="cuda")
+    cu = inp["cu_seqlens"].long()
+    for r in range(wl.num_requests):
+        n = int(cu[r + 1] - cu[r])
+        pt = torch.arange(n, device="cuda") + int(inp["tgt_offset"][r])
+        if wl.layout == PAGED:
+            row = inp["block_table"][r].long()[pt // wl.block_size] * wl.block_size + pt % wl.block_size
+        else:
+            row = r * wl.dst_capacity + pt
+        rows[row] = True
+    return rows
+
+
+@pytest.mark.parametrize("name", ["qwen3_14b_32b", "llama31_8b_70b_paged"])
+def test_full_size_sampled_rows_match_oracle(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, "cuda")
+    gk, gv, st, plan = run_gpu(wl, inp)
+    assert st == 0
+    f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
+    num = {0: 0.0, 1: 0.0}
+    den = {0: 0.0, 1: 0.0}
+    table = inp["block_table"].cpu().numpy() if wl.layout == PAGED else None
+    for r, gtok, p, pt, lt, h in _sample_rows(wl, inp, 17):
+        idx = inp["layer_idx"][lt].long()
+        krows = f64(inp["src_k"][idx, gtok, h])
+        vrows = f64(inp["src_v"][idx, gtok, h])
+        w = f64(inp["w"][lt, h])
+        b = f64(inp["b"][lt, h])
+        ok, ov = oracle.map_token(krows, vrows, w[0], w[1], b[0], b[1], p, pt,
+                                  wl.theta_src, wl.theta_tgt)
+        if wl.layout == PAGED:
+            row, bad = oracle.dst_row(oracle.PAGED, r, pt, block_size=wl.block_size,
+                                      num_blocks=wl.num_blocks, block_table=table,
+                                      max_blocks_per_req=table.shape[1])
+        else:
+            row, bad = oracle.dst_row(oracle.CONTIGUOUS, r, pt, dst_capacity=wl.dst_capacity)
+        assert bad == 0
+        for m, (dst, ref) in enumerate(((gk, ok), (gv, ov))):
+            got = f64(dst[lt, row, h])
+            e = np.linalg.norm(got - ref)
+            assert e <= 3 * TOL[wl.kv_dtype] * np.linalg.norm(ref), (m, lt, h, gtok)
+            num[m] += e * e
+            den[m] += float(ref @ ref)
+    for m in (0, 1):
+        assert (num[m] / den[m]) ** 0.5 <= TOL[wl.kv_dtype]
+    written = _written_mask(wl, inp)
+    for dst in (gk, gv):
+        bits = dst.view(torch.int16)
+        assert bool((bits[:, ~written] == -1).all())
+        assert not bool((bits[:, written] == -1).all(dim=-1).any())

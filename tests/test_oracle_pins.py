@@ -330,11 +330,14 @@ def test_out_of_range_rows_are_skipped_and_flagged():
                                 tgt_offset=P["offs"], layer_idx=P["idx"], max_position=32,
                                 dst_capacity=8)
     assert st == oracle.BAD_ROW
-    # request ranges that run backwards
-    _, dv, st = oracle.transfer(src_k=P["src"], src_v=P["src"], w=P["w"], b=P["b"],
-                                theta_src=1e4, theta_tgt=1e4, cu_seqlens=[0, 5, 4, 15],
-                                layer_idx=P["idx"], max_position=32, dst_capacity=16)
-    assert st == oracle.BAD_SEQLENS
+    # a request table that runs backwards, or does not end at ntok, makes the
+    # whole transfer invalid: nothing is written
+    for cu in ([0, 5, 4, 15], [0, 5, 6, 14], [1, 5, 6, 15]):
+        dk, dv, st = oracle.transfer(src_k=P["src"], src_v=P["src"], w=P["w"], b=P["b"],
+                                     theta_src=1e4, theta_tgt=1e4, cu_seqlens=cu,
+                                     layer_idx=[[2], [3]], max_position=32, dst_capacity=16)
+        assert st == oracle.BAD_SEQLENS
+        assert np.isnan(dv).all() and np.isnan(dk).all()
 
 
 def test_dst_row_examples():
