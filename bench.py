@@ -44,6 +44,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
     ap.add_argument("--workload", default="qwen3_14b_32b")
     ap.add_argument("--kernel", choices=["auto", "simt", "tcgen05"], default="auto")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (profiling of small cases)")
+    ap.add_argument("--tiles-per-item", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -287,13 +290,15 @@ def run_kvx(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.with_tokens([args.tokens], [wl.tgt_offsets[0]], name=f"{wl.name}@{args.tokens}")
     inp = make_inputs(wl, dev)
     plan = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers, kv_heads=wl.kv_heads,
                     head_dim=wl.head_dim, k=wl.k, rope_theta_src=wl.theta_src,
                     rope_theta_tgt=wl.theta_tgt, max_position=wl.max_position,
                     kv_dtype=wl.kv_dtype, w_dtype=torch.float32, b_dtype=wl.b_dtype,
                     layout=wl.layout, block_size=wl.block_size if wl.layout == PAGED else 0,
-                    kernel=kernel_code(args.kernel))
+                    kernel=kernel_code(args.kernel), tiles_per_item=args.tiles_per_item)
     kname = {kvx.KVX_KERNEL_SIMT: "simt", kvx.KVX_KERNEL_TCGEN05: "tcgen05"}[plan.kernel]
     shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
     dst_k = torch.empty(shape, dtype=wl.kv_dtype, device=dev)

@@ -34,6 +34,8 @@ kvx_status validate_desc(const kvx_plan_desc *d) {
   if (d->kernel != KVX_KERNEL_AUTO && d->kernel != KVX_KERNEL_SIMT &&
       d->kernel != KVX_KERNEL_TCGEN05)
     return KVX_ERR_INVALID_ARG;
+  if (d->tiles_per_item < 0 || d->tiles_per_item > 4096) return KVX_ERR_INVALID_ARG;
+  if (d->flags & ~KVX_PLAN_TEST_STALL) return KVX_ERR_INVALID_ARG;
   // "Requirements": same number of KV heads and the same per-head dimension.
   if (d->src_kv_heads != d->tgt_kv_heads || d->src_head_dim != d->tgt_head_dim)
     return KVX_ERR_PAIR_MISMATCH;
@@ -75,7 +77,25 @@ kvx_status upload(const std::vector<float2> &h, float2 **dptr) {
 void free_tables(kvx_plan *p) {
   if (p->rope_tgt && p->rope_tgt != p->rope_src) cudaFree(p->rope_tgt);
   if (p->rope_src) cudaFree(p->rope_src);
+  if (p->workspace) cudaFree(p->workspace);
   p->rope_src = p->rope_tgt = nullptr;
+  p->workspace = nullptr;
+}
+
+kvx_status alloc_workspace(kvx_plan *p, size_t bytes) {
+  p->workspace_bytes = bytes;
+  if (bytes == 0) return KVX_OK;
+  cudaError_t e = cudaMalloc(&p->workspace, bytes);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    p->workspace = nullptr;
+    return KVX_ERR_NO_MEMORY;
+  }
+  if (e != cudaSuccess) {
+    p->workspace = nullptr;
+    return KVX_ERR_CUDA;
+  }
+  return KVX_OK;
 }
 
 }  // namespace
@@ -125,6 +145,8 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   p->kernel = kernel;
   p->num_sms = prop.multiProcessorCount;
   p->half = desc->src_head_dim / 2;
+  p->tiles_per_item = desc->tiles_per_item > 0 ? desc->tiles_per_item : 8;
+  p->stall_test = (desc->flags & KVX_PLAN_TEST_STALL) ? 1 : 0;
 
   st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
               &p->rope_src);
@@ -135,6 +157,8 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
       st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
                   &p->rope_tgt);
   }
+  if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05)
+    st = alloc_workspace(p, kvx_tc_workspace_bytes(*desc));
   if (st == KVX_OK) {
     cudaError_t e = kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_prepare(p) : kvx_simt_prepare(p);
     if (e != cudaSuccess) st = KVX_ERR_CUDA;
@@ -164,7 +188,10 @@ kvx_status kvx_plan_destroy(kvx_plan *plan) {
 
 int32_t kvx_plan_kernel(const kvx_plan *plan) { return plan ? plan->kernel : -1; }
 
-int32_t kvx_plan_launches(const kvx_plan *plan) { return plan ? 1 : -1; }
+int32_t kvx_plan_launches(const kvx_plan *plan) {
+  if (!plan) return -1;
+  return plan->kernel == KVX_KERNEL_TCGEN05 ? 2 : 1;  // W image + transfer, or transfer
+}
 
 kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *stream) {
   if (!plan || !a) return KVX_ERR_INVALID_ARG;

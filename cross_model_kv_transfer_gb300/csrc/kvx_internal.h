@@ -17,6 +17,12 @@ struct kvx_plan {
   // p in [0, max_position), computed in double on the host, stored fp32.
   float2 *rope_src;
   float2 *rope_tgt;      // aliases rope_src when the two thetas are equal
+  // tensor-core path only: bf16 W image written by every transfer before the
+  // main kernel reads it (transfers sharing a plan are stream-ordered on it)
+  void *workspace;
+  size_t workspace_bytes;
+  int tiles_per_item;    // 128-token tiles per work item of the persistent kernel
+  int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
 };
 
 // Everything a kernel needs, passed by value.
@@ -39,5 +45,6 @@ cudaError_t kvx_simt_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
 bool kvx_simt_supports(const kvx_plan_desc &d);
 
 bool kvx_tc_supports(const kvx_plan_desc &d);
+size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d);
 cudaError_t kvx_tc_prepare(const kvx_plan *plan);
 cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);

@@ -1,10 +1,629 @@
-// kvx_tcgen05.cu -- tensor-core (tcgen05) transfer kernel for bf16 caches.
+// kvx_tcgen05.cu -- the transfer on the 5th-generation tensor cores (sm_103a).
+//
+// The map ("Helm Intelligent Routing", "Why carrying the cache across is the
+// hard part", step 2; Qwen3 article, linear-bridge section: one ridge map per
+// target (layer, head), separately for K and V, applied to the concatenated
+// features of the selected source layers) is a dense contraction per
+// (target layer lt, head h, K|V):  Y[T x d] = X[T x k*d] . W[k*d x d] + b.
+// It runs as tcgen05.mma (kind::f16, bf16 operands, fp32 accumulation in
+// tensor memory), M = 128 tokens, N = d = 128, K = 16 per instruction.
+//
+// Data path of one CTA (persistent, one per SM), per work item
+// (h, lt, K|V, chunk of TILES_PER_ITEM 128-token tiles):
+//   * W producer warp: copies the item's bf16 W image (prepared by
+//     w_image_kernel, 2k chunks of 16 KB in the UMMA 128-byte-swizzled
+//     K-major layout) into shared memory with cp.async.bulk; W stays resident
+//     for all tiles of the item (the only operand read from shared memory).
+//   * 8 transform warps: every thread owns one token row and one half of the
+//     RoPE pairs.  For each selected source layer j it loads the row's head
+//     vector with 16-byte loads, un-rotates keys out of the source RoPE in
+//     fp32 (step 1, "strip source RoPE"), packs bf16 and writes it with
+//     tcgen05.st into tensor memory: that tensor-memory slot is operand A.
+//     Values are copied as stored.  Four slots of 64 columns form a ring.
+//   * MMA warp (one thread): 8 tcgen05.mma per selection, A from tensor
+//     memory, B = W from shared memory, accumulating into one of two
+//     128-column fp32 accumulators; tcgen05.commit frees A slots, W chunks and
+//     hands finished accumulators to the epilogue.
+//   * 4 epilogue warps: tcgen05.ld the accumulator row, add b, re-rotate keys
+//     into the target RoPE at p' (step 3), cast to bf16 and store the row to
+//     the contiguous or paged target cache.
+// Every mbarrier wait is bounded: after KVX_WAIT_NS of no progress the CTA
+// sets KVX_FLAG_TIMEOUT, all roles leave their loops, in-flight copies and
+// MMAs are drained (again with bounded waits) and tensor memory is freed.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
 
+#include "kvx_device.cuh"
 #include "kvx_internal.h"
 
-bool kvx_tc_supports(const kvx_plan_desc &) { return false; }
-cudaError_t kvx_tc_prepare(const kvx_plan *) { return cudaErrorNotSupported; }
-cudaError_t kvx_tc_launch(const kvx_plan *, const KvxParams &, cudaStream_t) {
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr int kD = 128;               // head_dim handled by this kernel
+constexpr int kHalf = kD / 2;
+constexpr int kTileM = 128;           // tokens per tile (MMA M)
+constexpr int kMaxK = 6;              // selected layers: W = k * 32 KB of smem
+constexpr int kSlots = 4;             // A ring slots (64 TMEM columns each)
+constexpr int kSlotCols = kD / 2;     // bf16 pairs per selection row
+constexpr int kDCol = kSlots * kSlotCols;  // first accumulator column (256)
+constexpr int kTmemCols = 512;
+constexpr int kChunkBytes = 16384;    // W chunk: 128 rows x 64 k x bf16
+constexpr int kTransformWarps = 8;
+constexpr int kEpilogueWarps = 4;
+constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 12
+constexpr int kProducerWarp = kMmaWarp + 1;                  // 13
+constexpr int kThreads = (kProducerWarp + 1) * 32;           // 448
+constexpr uint64_t kWaitNs = 2000000000ull;                  // 2 s without progress
+constexpr uint64_t kStallTestWaitNs = 20000000ull;           // 20 ms (stall test hook)
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// D[tmem] (+)= A[tmem] . B[smem desc]
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// UMMA shared-memory descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kD >> 3) << 17) |
+                            ((uint32_t)(kTileM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// Shared state of one CTA
+// ---------------------------------------------------------------------------
+struct Shared {
+  uint64_t a_full[kSlots], a_empty[kSlots];
+  uint64_t d_full[2], d_empty[2];
+  uint64_t w_full[2 * kMaxK], w_empty[2 * kMaxK];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+struct Waiter {
+  Shared *sh;
+  uint32_t *status;
+  uint64_t limit_ns;
+  // Bounded wait; false means the pipeline is being abandoned.
+  __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity) const {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      if (mbar_try_wait(a, parity)) return true;
+      if (sh->abort) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        sh->abort = 1;
+        if (status) atomicOr(status, KVX_FLAG_TIMEOUT);
+        return false;
+      }
+    }
+  }
+};
+
+// Bounded wait used while draining: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(a, parity) && globaltimer() - t0 < kWaitNs) {
+  }
+}
+
+struct ItemGeom {
+  int num_tiles, num_chunks, tiles_per_item;
+  long long num_items;
+};
+
+__device__ __forceinline__ void decode_item(const KvxParams &p, const ItemGeom &g, long long item,
+                                            int &h, int &chunk, int &lt, int &m) {
+  m = (int)(item & 1);
+  long long r = item >> 1;
+  lt = (int)(r % p.Lt);
+  r /= p.Lt;
+  chunk = (int)(r % g.num_chunks);
+  h = (int)(r / g.num_chunks);
+}
+
+// ---------------------------------------------------------------------------
+// The transfer kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_transfer_kernel(KvxParams p, const __nv_bfloat16 *__restrict__ w_img, ItemGeom geo,
+                       int stall_test) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // W chunks need 1024-byte alignment for the 128-byte swizzle atoms.
+  unsigned char *wbuf = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Shared *sh = reinterpret_cast<Shared *>(wbuf + (size_t)2 * p.k * kChunkBytes);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nchunks_w = 2 * p.k;
+
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_addr(&sh->a_full[s]), kTransformWarps);
+      mbar_init(smem_addr(&sh->a_empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&sh->d_full[b]), 1);
+      mbar_init(smem_addr(&sh->d_empty[b]), kEpilogueWarps);
+    }
+    for (int c = 0; c < nchunks_w; ++c) {
+      mbar_init(smem_addr(&sh->w_full[c]), 1);
+      mbar_init(smem_addr(&sh->w_empty[c]), 1);
+    }
+    mbar_init(smem_addr(&sh->drain), 1);
+    sh->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&sh->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  // The request table is validated by every CTA; a malformed one stops the
+  // whole transfer before any write.
+  const bool seq_ok = kvx::seqlens_ok(p, tid, kThreads);
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  const Waiter W{sh, p.status, stall_test ? kStallTestWaitNs : kWaitNs};
+
+  if (!seq_ok) {
+    if (blockIdx.x == 0 && tid == 0) kvx::report(p, KVX_FLAG_BAD_SEQLENS);
+  } else if (warp < kTransformWarps) {
+    // ------------------------------------------------------------------
+    // transform warps: X rows -> tensor memory (operand A)
+    // ------------------------------------------------------------------
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int ph = warp >> 2;                 // RoPE pair half: pairs [32 ph, 32 ph + 32)
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    uint32_t a_seq = 0;
+    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+      int h, chunk, lt, m;
+      decode_item(p, geo, item, h, chunk, lt, m);
+      if (!kvx::layer_row_ok(p, lt)) continue;
+      const __nv_bfloat16 *src =
+          reinterpret_cast<const __nv_bfloat16 *>(m == 0 ? p.src_k : p.src_v);
+      const int t_beg = chunk * geo.tiles_per_item;
+      const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+      for (int tile = t_beg; tile < t_end; ++tile) {
+        const int64_t g = (int64_t)tile * kTileM + row_in_tile;
+        int32_t ps = 0, pt = 0;
+        int64_t row = -1;
+        if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
+        const bool valid = row >= 0;
+        // cos/sin of the source RoPE at ps for this thread's 32 pairs
+        float cs[32], sn[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) cs[q] = sn[q] = 0.f;
+        if (m == 0 && valid) {
+          const float4 *t4 =
+              reinterpret_cast<const float4 *>(p.rope_src + (int64_t)ps * kHalf + 32 * ph);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float4 v = __ldg(t4 + q);
+            cs[2 * q] = v.x;
+            sn[2 * q] = v.y;
+            cs[2 * q + 1] = v.z;
+            sn[2 * q + 1] = v.w;
+          }
+        }
+        for (int j = 0; j < p.k; ++j) {
+          const int slot = a_seq % kSlots;
+          const uint32_t round = a_seq / kSlots;
+          uint4 lo[4], hi[4];
+          if (valid) {
+            const int sl = p.layer_idx[lt * p.k + j];
+            const uint4 *v4 = reinterpret_cast<const uint4 *>(
+                src + (((int64_t)sl * p.ntok + g) * p.H + h) * kD);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              lo[q] = __ldg(v4 + 4 * ph + q);      // dims [32 ph, 32 ph + 32)
+              hi[q] = __ldg(v4 + 8 + 4 * ph + q);  // dims [64 + 32 ph, ...)
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) lo[q] = hi[q] = make_uint4(0, 0, 0, 0);
+          }
+          uint32_t plo[16], phi[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t wl[4] = {lo[q].x, lo[q].y, lo[q].z, lo[q].w};
+            const uint32_t wh[4] = {hi[q].x, hi[q].y, hi[q].z, hi[q].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (m == 0) {
+                // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 32 ph + 8q + 2e (+1)
+                const int i0 = 8 * q + 2 * e;
+                const float a0 = bf_lo(wl[e]), a1 = bf_hi(wl[e]);
+                const float b0 = bf_lo(wh[e]), b1 = bf_hi(wh[e]);
+                const float x00 = fmaf(a0, cs[i0], b0 * sn[i0]);
+                const float x01 = fmaf(b0, cs[i0], -a0 * sn[i0]);
+                const float x10 = fmaf(a1, cs[i0 + 1], b1 * sn[i0 + 1]);
+                const float x11 = fmaf(b1, cs[i0 + 1], -a1 * sn[i0 + 1]);
+                plo[4 * q + e] = pack_bf16(x00, x10);
+                phi[4 * q + e] = pack_bf16(x01, x11);
+              } else {
+                plo[4 * q + e] = wl[e];
+                phi[4 * q + e] = wh[e];
+              }
+            }
+          }
+          if (!W.wait(&sh->a_empty[slot], (round & 1) ^ 1)) goto transform_done;
+          tc_fence_after();
+          {
+            const uint32_t col = (uint32_t)(slot * kSlotCols + 16 * ph);
+            tc_st16(tmem + lane_base + col, plo);
+            tc_st16(tmem + lane_base + col + 32, phi);
+          }
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && !stall_test) mbar_arrive(smem_addr(&sh->a_full[slot]));
+          ++a_seq;
+        }
+      }
+    }
+  transform_done:;
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------------
+    // epilogue warps: accumulator -> + b -> re-rotate (K) -> bf16 -> cache
+    // ------------------------------------------------------------------
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    uint32_t d_seq = 0;
+    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+      int h, chunk, lt, m;
+      decode_item(p, geo, item, h, chunk, lt, m);
+      const bool layer_ok = kvx::layer_row_ok(p, lt);
+      const bool reporter = h == 0 && m == 0;
+      if (!layer_ok && reporter && chunk == 0 && tid == kTransformWarps * 32)
+        kvx::report(p, KVX_FLAG_BAD_LAYER_INDEX);
+      const int t_beg = chunk * geo.tiles_per_item;
+      const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+      const __nv_bfloat16 *bias =
+          reinterpret_cast<const __nv_bfloat16 *>(p.b) + (((int64_t)lt * p.H + h) * 2 + m) * kD;
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(m == 0 ? p.dst_k : p.dst_v);
+      for (int tile = t_beg; tile < t_end; ++tile) {
+        const int64_t g = (int64_t)tile * kTileM + row_in_tile;
+        int32_t ps = 0, pt = 0;
+        int64_t row = -1;
+        uint32_t bad = 0;
+        if (g < p.ntok) bad = kvx::token_meta(p, g, ps, pt, row);
+        if (reporter) {
+          const uint32_t any = __reduce_or_sync(0xffffffffu, bad);
+          if (lane == 0) kvx::report(p, any);
+        }
+        if (!layer_ok) continue;
+        const int buf = d_seq & 1;
+        if (!W.wait(&sh->d_full[buf], (d_seq >> 1) & 1)) goto epilogue_done;
+        tc_fence_after();
+        {
+          const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
+          __nv_bfloat16 *orow = dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
+#pragma unroll 1
+          for (int pc = 0; pc < 4; ++pc) {
+            uint32_t vlo[16], vhi[16];
+            tc_ld16(dcol + 16 * pc, vlo);
+            tc_ld16(dcol + kHalf + 16 * pc, vhi);
+            tc_wait_ld();
+            if (row >= 0) {
+              const uint4 *b4 = reinterpret_cast<const uint4 *>(bias);
+              const uint4 bl0 = __ldg(b4 + 2 * pc), bl1 = __ldg(b4 + 2 * pc + 1);
+              const uint4 bh0 = __ldg(b4 + 8 + 2 * pc), bh1 = __ldg(b4 + 8 + 2 * pc + 1);
+              const uint32_t bl[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
+              const uint32_t bh[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+              uint32_t olo[8], ohi[8];
+              const float4 *t4 =
+                  reinterpret_cast<const float4 *>(p.rope_tgt + (int64_t)pt * kHalf + 16 * pc);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float y[2][2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                  const int c = 2 * e + u;
+                  const float bl_ = u ? bf_hi(bl[e]) : bf_lo(bl[e]);
+                  const float bh_ = u ? bf_hi(bh[e]) : bf_lo(bh[e]);
+                  float y0 = __uint_as_float(vlo[c]) + bl_;
+                  float y1 = __uint_as_float(vhi[c]) + bh_;
+                  if (m == 0) {
+                    const float4 t = __ldg(t4 + e);   // pairs c = 2e, 2e+1
+                    const float cc = u ? t.z : t.x, ss = u ? t.w : t.y;
+                    const float r0 = fmaf(y0, cc, -y1 * ss);  // (y0 + j y1) exp(+j p' w_i)
+                    const float r1 = fmaf(y0, ss, y1 * cc);
+                    y0 = r0;
+                    y1 = r1;
+                  }
+                  y[u][0] = y0;
+                  y[u][1] = y1;
+                }
+                olo[e] = pack_bf16(y[0][0], y[1][0]);
+                ohi[e] = pack_bf16(y[0][1], y[1][1]);
+              }
+              uint4 *o4 = reinterpret_cast<uint4 *>(orow);
+              o4[2 * pc] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+              o4[2 * pc + 1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+              o4[8 + 2 * pc] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+              o4[8 + 2 * pc + 1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
+        ++d_seq;
+      }
+    }
+  epilogue_done:;
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------
+    // MMA issuer (one thread)
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      uint32_t a_seq = 0, d_seq = 0, w_seq = 0;
+      bool issued = false;
+      for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+        int h, chunk, lt, m;
+        decode_item(p, geo, item, h, chunk, lt, m);
+        if (!kvx::layer_row_ok(p, lt)) continue;
+        const int t_beg = chunk * geo.tiles_per_item;
+        const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+        for (int tile = t_beg; tile < t_end; ++tile) {
+          const int buf = d_seq & 1;
+          if (!W.wait(&sh->d_empty[buf], ((d_seq >> 1) & 1) ^ 1)) goto mma_done;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + (uint32_t)(kDCol + buf * kD);
+          for (int j = 0; j < p.k; ++j) {
+            const int slot = a_seq % kSlots;
+            if (!W.wait(&sh->a_full[slot], (a_seq / kSlots) & 1)) goto mma_done;
+            if (tile == t_beg) {
+              if (!W.wait(&sh->w_full[2 * j], w_seq & 1)) goto mma_done;
+              if (!W.wait(&sh->w_full[2 * j + 1], w_seq & 1)) goto mma_done;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t wchunk = (uint32_t)(2 * j + (kk >> 2));
+              const uint64_t bdesc =
+                  sw128_desc(smem_addr(wbuf + wchunk * kChunkBytes + (kk & 3) * 32));
+              const uint32_t a_tmem = tmem + (uint32_t)(slot * kSlotCols + kk * 8);
+              tc_mma_ts(d_tmem, a_tmem, bdesc, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            issued = true;
+            tc_commit(smem_addr(&sh->a_empty[slot]));
+            if (tile == t_end - 1) {
+              tc_commit(smem_addr(&sh->w_empty[2 * j]));
+              tc_commit(smem_addr(&sh->w_empty[2 * j + 1]));
+            }
+            ++a_seq;
+          }
+          tc_commit(smem_addr(&sh->d_full[buf]));
+          ++d_seq;
+        }
+        ++w_seq;
+      }
+    mma_done:
+      // drain: every MMA issued so far has completed once `drain` flips
+      if (issued) {
+        tc_commit(smem_addr(&sh->drain));
+        drain_wait(&sh->drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------
+    // W producer (one thread): bf16 W image -> shared memory
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      uint32_t w_seq = 0;
+      uint32_t issued_rounds[2 * kMaxK];
+      for (int c = 0; c < 2 * kMaxK; ++c) issued_rounds[c] = 0;
+      for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+        int h, chunk, lt, m;
+        decode_item(p, geo, item, h, chunk, lt, m);
+        if (!kvx::layer_row_ok(p, lt)) continue;
+        const unsigned char *img = reinterpret_cast<const unsigned char *>(w_img) +
+                                   (((int64_t)lt * p.H + h) * 2 + m) * (int64_t)nchunks_w * kChunkBytes;
+        for (int c = 0; c < nchunks_w; ++c) {
+          if (!W.wait(&sh->w_empty[c], (w_seq & 1) ^ 1)) goto producer_done;
+          const uint32_t bar = smem_addr(&sh->w_full[c]);
+          mbar_expect_tx(bar, kChunkBytes);
+          bulk_g2s(smem_addr(wbuf + c * kChunkBytes), img + (int64_t)c * kChunkBytes, kChunkBytes,
+                   bar);
+          issued_rounds[c] = w_seq + 1;
+        }
+        ++w_seq;
+      }
+    producer_done:
+      // drain: wait (bounded) until every issued copy has landed
+      for (int c = 0; c < nchunks_w; ++c)
+        if (issued_rounds[c] != 0) drain_wait(&sh->w_full[c], (issued_rounds[c] - 1) & 1);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// W (fp32, [Lt][H][2][k*d][d]) -> bf16 image, per (lt, h, m) 2k chunks of
+// [128 rows n][64 k] in the 128-byte-swizzled K-major layout the MMA reads:
+// byte (n, kk) of a chunk = n*128 + ((kk/8) ^ (n%8))*16 + (kk%8)*2.
+// One CTA converts one chunk through a shared-memory transpose.
+// ---------------------------------------------------------------------------
+template <typename WT>
+__global__ void __launch_bounds__(256) w_image_kernel(const WT *__restrict__ w,
+                                                      uint4 *__restrict__ img) {
+  __shared__ float tile[64][kD + 1];
+  const int64_t chunk = blockIdx.x;          // over (lt, h, m, c)
+  const int nchunk = gridDim.y;              // chunks per (lt, h, m) = 2k
+  const int64_t lhm = chunk;                 // index of (lt, h, m)
+  const int c = blockIdx.y;
+  const WT *src = w + (lhm * nchunk * 64 + (int64_t)c * 64) * kD;   // rows k = 64c.., [64][128]
+  for (int e = threadIdx.x; e < 64 * kD; e += blockDim.x) {
+    const int kr = e / kD, n = e % kD;
+    tile[kr][n] = (float)src[(int64_t)kr * kD + n];
+  }
+  __syncthreads();
+  uint4 *out = img + (lhm * nchunk + c) * (kChunkBytes / 16);
+  for (int q = threadIdx.x; q < kChunkBytes / 16; q += blockDim.x) {
+    const int n = q >> 3, k8 = (q & 7) ^ (n & 7);
+    uint32_t v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      v[e] = pack_bf16(tile[k8 * 8 + 2 * e][n], tile[k8 * 8 + 2 * e + 1][n]);
+    out[q] = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+size_t smem_bytes(int k) { return 1024 + (size_t)2 * k * kChunkBytes + sizeof(Shared) + 64; }
+
+}  // namespace
+
+bool kvx_tc_supports(const kvx_plan_desc &d) {
+  return d.kv_dtype == KVX_BF16 && d.b_dtype == KVX_BF16 && d.src_head_dim == kD &&
+         d.k >= 1 && d.k <= kMaxK;
+}
+
+size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d) {
+  return (size_t)d.tgt_layers * d.src_kv_heads * 2 * (size_t)d.k * kD * kD * 2;
+}
+
+cudaError_t kvx_tc_prepare(const kvx_plan *plan) {
+  return cudaFuncSetAttribute(tc_transfer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes(plan->desc.k));
+}
+
+cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s) {
+  const kvx_plan_desc &d = plan->desc;
+  // 1. W -> bf16 image in the plan workspace
+  dim3 wgrid((unsigned)((int64_t)p.Lt * p.H * 2), (unsigned)(2 * p.k));
+  if (d.w_dtype == KVX_F32)
+    w_image_kernel<float><<<wgrid, 256, 0, s>>>(reinterpret_cast<const float *>(p.w),
+                                                reinterpret_cast<uint4 *>(plan->workspace));
+  else
+    w_image_kernel<__nv_bfloat16><<<wgrid, 256, 0, s>>>(
+        reinterpret_cast<const __nv_bfloat16 *>(p.w), reinterpret_cast<uint4 *>(plan->workspace));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // 2. the persistent transfer kernel
+  ItemGeom geo;
+  geo.num_tiles = (int)((p.ntok + kTileM - 1) / kTileM);
+  geo.tiles_per_item = plan->tiles_per_item;
+  geo.num_chunks = (geo.num_tiles + geo.tiles_per_item - 1) / geo.tiles_per_item;
+  geo.num_items = (long long)p.H * geo.num_chunks * p.Lt * 2;
+  const int grid = (int)(geo.num_items < plan->num_sms ? geo.num_items : plan->num_sms);
+  tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k), s>>>(
+      p, reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
+  return cudaGetLastError();
 }

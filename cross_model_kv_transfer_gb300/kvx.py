@@ -43,6 +43,7 @@ KVX_PAGED = 1
 KVX_KERNEL_AUTO = 0
 KVX_KERNEL_SIMT = 1
 KVX_KERNEL_TCGEN05 = 2
+KVX_PLAN_TEST_STALL = 1
 
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
             "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches")
@@ -58,6 +59,7 @@ class PlanDesc(ctypes.Structure):
         ("kv_dtype", ctypes.c_int32), ("w_dtype", ctypes.c_int32), ("b_dtype", ctypes.c_int32),
         ("dst_layout", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("max_position", ctypes.c_int32), ("kernel", ctypes.c_int32),
+        ("tiles_per_item", ctypes.c_int32), ("flags", ctypes.c_int32),
     ]
 
 
@@ -159,14 +161,15 @@ class Plan:
     def __init__(self, *, src_layers, tgt_layers, kv_heads, head_dim, k, rope_theta_src,
                  rope_theta_tgt, max_position, kv_dtype, w_dtype, b_dtype,
                  layout=KVX_CONTIGUOUS, block_size=0, kernel=KVX_KERNEL_AUTO,
-                 tgt_kv_heads=None, tgt_head_dim=None):
+                 tgt_kv_heads=None, tgt_head_dim=None, tiles_per_item=0, flags=0):
         self.desc = PlanDesc(
             src_layers, tgt_layers, kv_heads,
             kv_heads if tgt_kv_heads is None else tgt_kv_heads,
             head_dim, head_dim if tgt_head_dim is None else tgt_head_dim, k,
             float(rope_theta_src), float(rope_theta_tgt),
             _dtype_code(kv_dtype), _dtype_code(w_dtype), _dtype_code(b_dtype),
-            int(layout), int(block_size), int(max_position), int(kernel))
+            int(layout), int(block_size), int(max_position), int(kernel),
+            int(tiles_per_item), int(flags))
         self.kv_dtype, self.w_dtype, self.b_dtype = kv_dtype, w_dtype, b_dtype
         st, h = kvx_plan_create(self.desc)
         if st != KVX_OK:

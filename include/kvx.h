@@ -31,9 +31,11 @@
  * Execution model.  kvx_plan_create / kvx_plan_destroy may allocate, free
  * and synchronise.  kvx_transfer only validates its arguments on the host
  * and enqueues kernels on the given stream: it never synchronises and never
- * allocates.  A plan is immutable after creation and may be used from
- * several host threads and streams at once.  All tensors are owned by the
- * caller; the plan owns only its RoPE tables.
+ * allocates.  A plan is immutable after creation.  All tensors are owned by
+ * the caller; the plan owns its RoPE tables and, for the tensor-core path, a
+ * workspace that every transfer rewrites (the bf16 image of W): transfers
+ * with the same tensor-core plan must be ordered (same stream, or events);
+ * SIMT plans have no workspace and may run concurrently on several streams. 
  *
  * Errors.  Every call returns a kvx_status.  Host-detectable errors are
  * returned before anything is enqueued, and nothing is written.  Errors only
@@ -110,7 +112,16 @@ typedef struct {
   int32_t max_position;     /* every source and target position must lie in
                                [0, max_position); sizes the RoPE tables      */
   int32_t kernel;           /* kvx_kernel                                    */
+  int32_t tiles_per_item;   /* tensor-core path: 128-token tiles per work
+                               item (W is loaded once per item); 0 = default */
+  int32_t flags;            /* KVX_PLAN_* bits; 0 for normal use            */
 } kvx_plan_desc;
+
+/* Failure-detection test hook (tensor-core path): the warps that fill the
+ * MMA operand never signal it, so the pipeline waits run out (after 20 ms
+ * instead of 2 s) and the transfer reports KVX_FLAG_TIMEOUT.  Nothing faults
+ * or hangs; the kernel drains and exits.  Never set in production. */
+#define KVX_PLAN_TEST_STALL 1
 
 typedef struct kvx_plan kvx_plan; /* opaque */
 

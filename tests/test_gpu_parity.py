@@ -213,3 +213,43 @@ def test_host_rejects_missing_pointers_before_launch():
     assert st == kvx.KVX_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert bool((dk == 0).all())
+
+
+@pytest.mark.parametrize("k,tiles_per_item", [(1, 1), (3, 2), (5, 3), (6, 8)])
+def test_tcgen05_selection_counts_and_item_sizes(k, tiles_per_item):
+    # other k (ring wrap-around of the four operand slots, 2k W chunks) and
+    # other work-item sizes (W reloaded every 1, 2, 3 or 8 tiles)
+    base = WORKLOADS["qwen3_0p6b_1p7b_off37_2k"].with_tokens([700], [37])
+    wl = dataclasses.replace(base, k=k, tgt_layers=5)
+    inp = make_inputs(wl, "cuda")
+    plan = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers, kv_heads=wl.kv_heads,
+                    head_dim=wl.head_dim, k=k, rope_theta_src=wl.theta_src,
+                    rope_theta_tgt=5e5, max_position=wl.max_position, kv_dtype=wl.kv_dtype,
+                    w_dtype=torch.float32, b_dtype=wl.b_dtype,
+                    kernel=kvx.KVX_KERNEL_TCGEN05, tiles_per_item=tiles_per_item)
+    gk, gv, st, _ = run_gpu(wl, inp, plan=plan)
+    assert st == 0
+    rk, rv, _ = run_oracle(wl, inp, theta_tgt=5e5)
+    assert_parity(wl, gk, gv, rk, rv)
+
+
+def test_tcgen05_pipeline_wait_gives_up_and_reports_timeout():
+    # Failure detection without a GPU fault: the operand-filling warps never
+    # signal, every pipeline wait gives up after its limit, the kernel drains,
+    # frees tensor memory and reports KVX_FLAG_TIMEOUT; the context stays
+    # usable for the next (normal) transfer.
+    wl = WORKLOADS["qwen3_0p6b_1p7b"].with_tokens([256], [0])
+    wl = dataclasses.replace(wl, tgt_layers=2)
+    inp = make_inputs(wl, "cuda")
+    stalled = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers,
+                       kv_heads=wl.kv_heads, head_dim=wl.head_dim, k=wl.k,
+                       rope_theta_src=wl.theta_src, rope_theta_tgt=wl.theta_tgt,
+                       max_position=wl.max_position, kv_dtype=wl.kv_dtype,
+                       w_dtype=torch.float32, b_dtype=wl.b_dtype,
+                       kernel=kvx.KVX_KERNEL_TCGEN05, flags=kvx.KVX_PLAN_TEST_STALL)
+    _, _, st, _ = run_gpu(wl, inp, plan=stalled)
+    assert st & kvx.KVX_FLAG_TIMEOUT
+    gk, gv, st, _ = run_gpu(wl, inp, kvx.KVX_KERNEL_TCGEN05)
+    assert st == 0
+    rk, rv, _ = run_oracle(wl, inp)
+    assert_parity(wl, gk, gv, rk, rv)
