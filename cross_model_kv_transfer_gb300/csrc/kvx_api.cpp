@@ -157,8 +157,11 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
       st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
                   &p->rope_tgt);
   }
-  if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05)
-    st = alloc_workspace(p, kvx_tc_workspace_bytes(*desc));
+  if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05) {
+    p->encode_tiled = kvx_tc_encoder();
+    st = p->encode_tiled ? alloc_workspace(p, kvx_tc_workspace_bytes(*desc))
+                         : KVX_ERR_UNSUPPORTED;
+  }
   if (st == KVX_OK) {
     cudaError_t e = kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_prepare(p) : kvx_simt_prepare(p);
     if (e != cudaSuccess) st = KVX_ERR_CUDA;
@@ -200,6 +203,10 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   if (a->num_requests < 1) return KVX_ERR_INVALID_ARG;
   if (!a->cu_seqlens && a->num_requests != 1) return KVX_ERR_INVALID_ARG;
   if (!a->src_k || !a->src_v || !a->layer_idx || !a->w || !a->b || !a->dst_k || !a->dst_v)
+    return KVX_ERR_INVALID_ARG;
+  // the tensor-core path reads the source through TMA: 16-byte aligned bases
+  if (plan->kernel == KVX_KERNEL_TCGEN05 &&
+      (((uintptr_t)a->src_k | (uintptr_t)a->src_v) & 15u))
     return KVX_ERR_INVALID_ARG;
   if (d.dst_layout == KVX_CONTIGUOUS) {
     if (a->dst_capacity < 1) return KVX_ERR_INVALID_ARG;

@@ -22,6 +22,7 @@ struct kvx_plan {
   void *workspace;
   size_t workspace_bytes;
   int tiles_per_item;    // 128-token tiles per work item of the persistent kernel
+  void *encode_tiled;    // driver entry point cuTensorMapEncodeTiled
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
 };
 
@@ -46,5 +47,6 @@ bool kvx_simt_supports(const kvx_plan_desc &d);
 
 bool kvx_tc_supports(const kvx_plan_desc &d);
 size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d);
+void *kvx_tc_encoder();
 cudaError_t kvx_tc_prepare(const kvx_plan *plan);
 cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);

@@ -9,17 +9,21 @@
 // tensor memory), M = 128 tokens, N = d = 128, K = 16 per instruction.
 //
 // Data path of one CTA (persistent, one per SM), per work item
-// (h, lt, K|V, chunk of TILES_PER_ITEM 128-token tiles):
+// (h, lt, K|V, chunk of tiles_per_item 128-token tiles):
 //   * W producer warp: copies the item's bf16 W image (prepared by
 //     w_image_kernel, 2k chunks of 16 KB in the UMMA 128-byte-swizzled
 //     K-major layout) into shared memory with cp.async.bulk; W stays resident
-//     for all tiles of the item (the only operand read from shared memory).
+//     for all tiles of the item and is the only MMA operand read from shared
+//     memory.
+//   * X loader warp: TMA (cp.async.bulk.tensor, 4-D map over [Ls][T][H][d],
+//     128-byte swizzle) brings the 128 rows x d of one selected source layer
+//     for one tile into a ring of shared-memory stages, two boxes of 64 dims.
 //   * 8 transform warps: every thread owns one token row and one half of the
-//     RoPE pairs.  For each selected source layer j it loads the row's head
-//     vector with 16-byte loads, un-rotates keys out of the source RoPE in
-//     fp32 (step 1, "strip source RoPE"), packs bf16 and writes it with
-//     tcgen05.st into tensor memory: that tensor-memory slot is operand A.
-//     Values are copied as stored.  Four slots of 64 columns form a ring.
+//     RoPE pairs.  It reads its row from the stage (16-byte shared loads,
+//     conflict-free thanks to the swizzle), un-rotates keys out of the source
+//     RoPE in fp32 (step 1, "strip source RoPE"), packs bf16 and writes the
+//     row with tcgen05.st into tensor memory, which is operand A.  Values are
+//     copied as stored.  Four slots of 64 tensor-memory columns form a ring.
 //   * MMA warp (one thread): 8 tcgen05.mma per selection, A from tensor
 //     memory, B = W from shared memory, accumulating into one of two
 //     128-column fp32 accumulators; tcgen05.commit frees A slots, W chunks and
@@ -27,9 +31,10 @@
 //   * 4 epilogue warps: tcgen05.ld the accumulator row, add b, re-rotate keys
 //     into the target RoPE at p' (step 3), cast to bf16 and store the row to
 //     the contiguous or paged target cache.
-// Every mbarrier wait is bounded: after KVX_WAIT_NS of no progress the CTA
-// sets KVX_FLAG_TIMEOUT, all roles leave their loops, in-flight copies and
-// MMAs are drained (again with bounded waits) and tensor memory is freed.
+// Every mbarrier wait is bounded: after 2 s without progress the CTA sets
+// KVX_FLAG_TIMEOUT, all roles leave their loops, in-flight copies and MMAs
+// are drained (again with bounded waits) and tensor memory is freed.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -48,11 +53,15 @@ constexpr int kSlotCols = kD / 2;     // bf16 pairs per selection row
 constexpr int kDCol = kSlots * kSlotCols;  // first accumulator column (256)
 constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 16384;    // W chunk: 128 rows x 64 k x bf16
+constexpr int kStageBytes = 2 * kChunkBytes;  // one selection of one tile
+constexpr int kMaxStages = 4;
+constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
 constexpr int kTransformWarps = 8;
 constexpr int kEpilogueWarps = 4;
 constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 12
 constexpr int kProducerWarp = kMmaWarp + 1;                  // 13
-constexpr int kThreads = (kProducerWarp + 1) * 32;           // 448
+constexpr int kLoaderWarp = kProducerWarp + 1;               // 14
+constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 480
 constexpr uint64_t kWaitNs = 2000000000ull;                  // 2 s without progress
 constexpr uint64_t kStallTestWaitNs = 20000000ull;           // 20 ms (stall test hook)
 
@@ -94,6 +103,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// TMA tile load of a 4-D box into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -171,6 +189,7 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 // Shared state of one CTA
 // ---------------------------------------------------------------------------
 struct Shared {
+  uint64_t x_full[kMaxStages], x_empty[kMaxStages];
   uint64_t a_full[kSlots], a_empty[kSlots];
   uint64_t d_full[2], d_empty[2];
   uint64_t w_full[2 * kMaxK], w_empty[2 * kMaxK];
@@ -209,7 +228,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 struct ItemGeom {
-  int num_tiles, num_chunks, tiles_per_item;
+  int num_tiles, num_chunks, tiles_per_item, stages;
   long long num_items;
 };
 
@@ -227,19 +246,27 @@ __device__ __forceinline__ void decode_item(const KvxParams &p, const ItemGeom &
 // The transfer kernel
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_transfer_kernel(KvxParams p, const __nv_bfloat16 *__restrict__ w_img, ItemGeom geo,
-                       int stall_test) {
+    tc_transfer_kernel(const __grid_constant__ KvxParams p,
+                       const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v,
+                       const __nv_bfloat16 *__restrict__ w_img, const ItemGeom geo,
+                       const int stall_test) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // W chunks need 1024-byte alignment for the 128-byte swizzle atoms.
+  // W chunks and X stages need 1024-byte alignment (128-byte swizzle atoms).
   unsigned char *wbuf = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Shared *sh = reinterpret_cast<Shared *>(wbuf + (size_t)2 * p.k * kChunkBytes);
+  unsigned char *xbuf = wbuf + (size_t)2 * p.k * kChunkBytes;
+  Shared *sh = reinterpret_cast<Shared *>(xbuf + (size_t)geo.stages * kStageBytes);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int nchunks_w = 2 * p.k;
 
   if (tid == 0) {
+    for (int s = 0; s < geo.stages; ++s) {
+      mbar_init(smem_addr(&sh->x_full[s]), 1);
+      mbar_init(smem_addr(&sh->x_empty[s]), kTransformWarps * 32);
+    }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_addr(&sh->a_full[s]), kTransformWarps);
       mbar_init(smem_addr(&sh->a_empty[s]), 1);
@@ -281,13 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ph = warp >> 2;                 // RoPE pair half: pairs [32 ph, 32 ph + 32)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    uint32_t a_seq = 0;
+    uint32_t a_seq = 0, x_seq = 0;
+    const int sw = row_in_tile & 7;           // 128-byte swizzle phase of this row
     for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
       int h, chunk, lt, m;
       decode_item(p, geo, item, h, chunk, lt, m);
       if (!kvx::layer_row_ok(p, lt)) continue;
-      const __nv_bfloat16 *src =
-          reinterpret_cast<const __nv_bfloat16 *>(m == 0 ? p.src_k : p.src_v);
       const int t_beg = chunk * geo.tiles_per_item;
       const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
       for (int tile = t_beg; tile < t_end; ++tile) {
@@ -299,7 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // cos/sin of the source RoPE at ps for this thread's 32 pairs
         float cs[32], sn[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) cs[q] = sn[q] = 0.f;
+        for (int q = 0; q < 32; ++q) {
+          cs[q] = 1.f;
+          sn[q] = 0.f;
+        }
         if (m == 0 && valid) {
           const float4 *t4 =
               reinterpret_cast<const float4 *>(p.rope_src + (int64_t)ps * kHalf + 32 * ph);
@@ -313,22 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         for (int j = 0; j < p.k; ++j) {
+          const int stage = x_seq % geo.stages;
+          if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) goto transform_done;
+          // this row's dims [32 ph, 32 ph + 32) (box 0) and [64 + 32 ph, ...)
+          // (box 1): logical 16-byte chunks 4 ph .. 4 ph + 3 of a 128-byte row
+          const unsigned char *rb = xbuf + stage * kStageBytes + row_in_tile * 128;
+          uint4 lo[4], hi[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int pc = ((4 * ph + q) ^ sw) * 16;
+            lo[q] = *reinterpret_cast<const uint4 *>(rb + pc);
+            hi[q] = *reinterpret_cast<const uint4 *>(rb + kChunkBytes + pc);
+          }
+          mbar_arrive(smem_addr(&sh->x_empty[stage]));
+          ++x_seq;
           const int slot = a_seq % kSlots;
           const uint32_t round = a_seq / kSlots;
-          uint4 lo[4], hi[4];
-          if (valid) {
-            const int sl = p.layer_idx[lt * p.k + j];
-            const uint4 *v4 = reinterpret_cast<const uint4 *>(
-                src + (((int64_t)sl * p.ntok + g) * p.H + h) * kD);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              lo[q] = __ldg(v4 + 4 * ph + q);      // dims [32 ph, 32 ph + 32)
-              hi[q] = __ldg(v4 + 8 + 4 * ph + q);  // dims [64 + 32 ph, ...)
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) lo[q] = hi[q] = make_uint4(0, 0, 0, 0);
-          }
           uint32_t plo[16], phi[16];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -514,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(&sh->drain, 0);
       }
     }
-  } else {
+  } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------------
     // W producer (one thread): bf16 W image -> shared memory
     // ------------------------------------------------------------------
@@ -542,6 +571,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: wait (bounded) until every issued copy has landed
       for (int c = 0; c < nchunks_w; ++c)
         if (issued_rounds[c] != 0) drain_wait(&sh->w_full[c], (issued_rounds[c] - 1) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------------
+    // X loader (one thread): TMA boxes [128 tokens][64 dims] x 2 per
+    // (tile, selection) into the stage ring
+    // ------------------------------------------------------------------
+    if (lane == 0) {
+      uint32_t x_seq = 0;
+      for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+        int h, chunk, lt, m;
+        decode_item(p, geo, item, h, chunk, lt, m);
+        if (!kvx::layer_row_ok(p, lt)) continue;
+        const CUtensorMap *map = m == 0 ? &tmap_k : &tmap_v;
+        const int t_beg = chunk * geo.tiles_per_item;
+        const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+        for (int tile = t_beg; tile < t_end; ++tile) {
+          for (int j = 0; j < p.k; ++j) {
+            const int stage = x_seq % geo.stages;
+            if (!W.wait(&sh->x_empty[stage], ((x_seq / geo.stages) & 1) ^ 1)) goto loader_done;
+            const int sl = p.layer_idx[lt * p.k + j];
+            const uint32_t bar = smem_addr(&sh->x_full[stage]);
+            const uint32_t dst = smem_addr(xbuf + stage * kStageBytes);
+            mbar_expect_tx(bar, kStageBytes);
+            tma_load_4d(dst, map, 0, h, tile * kTileM, sl, bar);
+            tma_load_4d(dst + kChunkBytes, map, kHalf, h, tile * kTileM, sl, bar);
+            ++x_seq;
+          }
+        }
+      }
+    loader_done:
+      // drain: the last `stages` loads (at most) may still be in flight
+      for (uint32_t n = (x_seq > (uint32_t)geo.stages ? x_seq - geo.stages : 0); n < x_seq; ++n)
+        drain_wait(&sh->x_full[n % geo.stages], (n / geo.stages) & 1);
     }
   }
 
@@ -586,7 +648,35 @@ __global__ void __launch_bounds__(256) w_image_kernel(const WT *__restrict__ w,
   }
 }
 
-size_t smem_bytes(int k) { return 1024 + (size_t)2 * k * kChunkBytes + sizeof(Shared) + 64; }
+size_t smem_bytes(int k, int stages) {
+  return 1024 + (size_t)2 * k * kChunkBytes + (size_t)stages * kStageBytes + sizeof(Shared) + 64;
+}
+
+int max_stages(int k) {
+  int s = kMaxStages;
+  while (s > 1 && smem_bytes(k, s) > (size_t)kSmemLimit) --s;
+  return s;
+}
+
+// 4-D TMA map over a [Ls][ntok][H][128] bf16 cache: box [1][128][1][64],
+// 128-byte swizzle, out-of-range rows read as zero.
+bool encode_map(const kvx_plan *plan, CUtensorMap *map, const void *base, const KvxParams &p) {
+  typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                               const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                               const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  EncodeFn fn = reinterpret_cast<EncodeFn>(plan->encode_tiled);
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.H, (cuuint64_t)p.ntok,
+                              (cuuint64_t)p.Ls};
+  const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)p.H * kD * 2,
+                                 (cuuint64_t)p.ntok * p.H * kD * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)kHalf, 1u, (cuuint32_t)kTileM, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -599,9 +689,21 @@ size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d) {
   return (size_t)d.tgt_layers * d.src_kv_heads * 2 * (size_t)d.k * kD * kD * 2;
 }
 
+void *kvx_tc_encoder() {
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return fn;
+}
+
 cudaError_t kvx_tc_prepare(const kvx_plan *plan) {
+  if (!plan->encode_tiled) return cudaErrorNotSupported;
+  const int k = plan->desc.k;
   return cudaFuncSetAttribute(tc_transfer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes(plan->desc.k));
+                              (int)smem_bytes(k, max_stages(k)));
 }
 
 cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s) {
@@ -622,8 +724,12 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   geo.tiles_per_item = plan->tiles_per_item;
   geo.num_chunks = (geo.num_tiles + geo.tiles_per_item - 1) / geo.tiles_per_item;
   geo.num_items = (long long)p.H * geo.num_chunks * p.Lt * 2;
+  geo.stages = max_stages(p.k);
+  CUtensorMap mk, mv;
+  if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p))
+    return cudaErrorInvalidValue;
   const int grid = (int)(geo.num_items < plan->num_sms ? geo.num_items : plan->num_sms);
-  tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k), s>>>(
-      p, reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
+  tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k, geo.stages), s>>>(
+      p, mk, mv, reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
   return cudaGetLastError();
 }
