@@ -1,5 +1,6 @@
 // kvx_api.cpp -- host side of the C ABI declared in include/kvx.h: argument
-// validation, plan creation (RoPE tables), kernel selection and launch.
+// validation, plan creation (RoPE tables or fixed-point frequencies), kernel
+// selection and launch.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -55,6 +56,21 @@ std::vector<float2> rope_table(double theta, int d, int max_position) {
     }
   }
   return t;
+}
+
+// w_i / (2 pi) as a 64-bit binary fraction of a turn, in extended precision.
+void rope_turns(double theta, int d, unsigned long long *out) {
+  const long double two_pi = 6.283185307179586476925286766559005768L;
+  for (int i = 0; i < d / 2; ++i) {
+    const long double w = powl((long double)theta, -2.0L * (long double)i / (long double)d);
+    const long double f = w / two_pi;                  // turns per position
+    const long double x = ldexpl(f - floorl(f), 32);   // [0, 2^32)
+    const long double hi = floorl(x);
+    long double lo = roundl(ldexpl(x - hi, 32));       // [0, 2^32]
+    unsigned long long v = (unsigned long long)hi << 32;
+    v += (unsigned long long)lo;                       // a carry wraps mod 2^64 = mod 1 turn
+    out[i] = v;
+  }
 }
 
 kvx_status upload(const std::vector<float2> &h, float2 **dptr) {
@@ -148,14 +164,20 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   p->tiles_per_item = desc->tiles_per_item > 0 ? desc->tiles_per_item : 8;
   p->stall_test = (desc->flags & KVX_PLAN_TEST_STALL) ? 1 : 0;
 
-  st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
-              &p->rope_src);
-  if (st == KVX_OK) {
-    if (desc->rope_theta_tgt == desc->rope_theta_src)
-      p->rope_tgt = p->rope_src;
-    else
-      st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
-                  &p->rope_tgt);
+  if (kernel == KVX_KERNEL_SIMT) {
+    // fp32 tables from fp64 host trigonometry (the fp32 path's 1e-5 budget)
+    st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
+                &p->rope_src);
+    if (st == KVX_OK) {
+      if (desc->rope_theta_tgt == desc->rope_theta_src)
+        p->rope_tgt = p->rope_src;
+      else
+        st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
+                    &p->rope_tgt);
+    }
+  } else {
+    rope_turns(desc->rope_theta_src, desc->src_head_dim, p->turns_src);
+    rope_turns(desc->rope_theta_tgt, desc->tgt_head_dim, p->turns_tgt);
   }
   if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05) {
     p->encode_tiled = kvx_tc_encoder();

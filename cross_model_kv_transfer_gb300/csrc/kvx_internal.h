@@ -23,6 +23,9 @@ struct kvx_plan {
   size_t workspace_bytes;
   int tiles_per_item;    // 128-token tiles per work item of the persistent kernel
   void *encode_tiled;    // driver entry point cuTensorMapEncodeTiled
+  // RoPE frequencies in 64-bit fixed-point turns, round(w_i / 2pi * 2^64),
+  // for the tensor-core path (head_dim <= 256, so at most 128 pairs)
+  unsigned long long turns_src[128], turns_tgt[128];
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
 };
 

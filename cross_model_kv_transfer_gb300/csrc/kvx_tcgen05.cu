@@ -186,6 +186,24 @@ __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w <<
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
+// RoPE angles without tables.  For pair i the host stores the frequency in
+// turns, F_i = round(w_i / (2 pi) * 2^64), w_i = theta^(-2i/d).  The phase of
+// position p is then p * F_i mod 2^64 (an exact integer product), whose top
+// 32 bits are the angle in [-pi, pi) to 2^-32 of a turn; __sincosf is
+// accurate to about 4e-7 there.  This replaces per-row table gathers.
+// ---------------------------------------------------------------------------
+struct RopeTurns {
+  unsigned long long src[kHalf], tgt[kHalf];
+};
+
+__device__ __forceinline__ void rope_cs(uint32_t pos, unsigned long long turns, float &c,
+                                        float &s) {
+  const unsigned long long ph = (unsigned long long)pos * turns;
+  const float a = (float)(int32_t)(uint32_t)(ph >> 32) * 1.46291807926715968e-9f;  // 2 pi / 2^32
+  __sincosf(a, &s, &c);
+}
+
+// ---------------------------------------------------------------------------
 // Shared state of one CTA
 // ---------------------------------------------------------------------------
 struct Shared {
@@ -249,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_transfer_kernel(const __grid_constant__ KvxParams p,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v,
+                       const __grid_constant__ RopeTurns rope,
                        const __nv_bfloat16 *__restrict__ w_img, const ItemGeom geo,
                        const int stall_test) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -330,16 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           sn[q] = 0.f;
         }
         if (m == 0 && valid) {
-          const float4 *t4 =
-              reinterpret_cast<const float4 *>(p.rope_src + (int64_t)ps * kHalf + 32 * ph);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float4 v = __ldg(t4 + q);
-            cs[2 * q] = v.x;
-            sn[2 * q] = v.y;
-            cs[2 * q + 1] = v.z;
-            sn[2 * q + 1] = v.w;
-          }
+          for (int q = 0; q < 32; ++q) rope_cs((uint32_t)ps, rope.src[32 * ph + q], cs[q], sn[q]);
         }
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_seq % geo.stages;
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
           __nv_bfloat16 *orow = dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
-#pragma unroll 1
+#pragma unroll
           for (int pc = 0; pc < 4; ++pc) {
             uint32_t vlo[16], vhi[16];
             tc_ld16(dcol + 16 * pc, vlo);
@@ -448,8 +459,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t bl[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
               const uint32_t bh[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
               uint32_t olo[8], ohi[8];
-              const float4 *t4 =
-                  reinterpret_cast<const float4 *>(p.rope_tgt + (int64_t)pt * kHalf + 16 * pc);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 float y[2][2];
@@ -461,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float y0 = __uint_as_float(vlo[c]) + bl_;
                   float y1 = __uint_as_float(vhi[c]) + bh_;
                   if (m == 0) {
-                    const float4 t = __ldg(t4 + e);   // pairs c = 2e, 2e+1
-                    const float cc = u ? t.z : t.x, ss = u ? t.w : t.y;
+                    float cc, ss;
+                    rope_cs((uint32_t)pt, rope.tgt[16 * pc + c], cc, ss);
                     const float r0 = fmaf(y0, cc, -y1 * ss);  // (y0 + j y1) exp(+j p' w_i)
                     const float r1 = fmaf(y0, ss, y1 * cc);
                     y0 = r0;
@@ -729,7 +738,13 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p))
     return cudaErrorInvalidValue;
   const int grid = (int)(geo.num_items < plan->num_sms ? geo.num_items : plan->num_sms);
+  RopeTurns rope;
+  for (int i = 0; i < kHalf; ++i) {
+    rope.src[i] = plan->turns_src[i];
+    rope.tgt[i] = plan->turns_tgt[i];
+  }
   tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k, geo.stages), s>>>(
-      p, mk, mv, reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
+      p, mk, mv, rope, reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo,
+      plan->stall_test);
   return cudaGetLastError();
 }

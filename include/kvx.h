@@ -32,10 +32,11 @@
  * and synchronise.  kvx_transfer only validates its arguments on the host
  * and enqueues kernels on the given stream: it never synchronises and never
  * allocates.  A plan is immutable after creation.  All tensors are owned by
- * the caller; the plan owns its RoPE tables and, for the tensor-core path, a
- * workspace that every transfer rewrites (the bf16 image of W): transfers
- * with the same tensor-core plan must be ordered (same stream, or events);
- * SIMT plans have no workspace and may run concurrently on several streams. 
+ * the caller.  A SIMT plan owns RoPE tables (read only; its transfers may
+ * run concurrently on several streams).  A tensor-core plan computes RoPE
+ * angles on the fly and owns a workspace that every transfer rewrites (the
+ * bf16 image of W): transfers with the same tensor-core plan must be
+ * ordered (same stream, or events).
  *
  * Errors.  Every call returns a kvx_status.  Host-detectable errors are
  * returned before anything is enqueued, and nothing is written.  Errors only
@@ -110,7 +111,7 @@ typedef struct {
   int32_t dst_layout;       /* kvx_layout of the target cache                 */
   int32_t block_size;       /* tokens per block, PAGED only (>= 1)            */
   int32_t max_position;     /* every source and target position must lie in
-                               [0, max_position); sizes the RoPE tables      */
+                               [0, max_position); sizes the SIMT RoPE tables */
   int32_t kernel;           /* kvx_kernel                                    */
   int32_t tiles_per_item;   /* tensor-core path: 128-token tiles per work
                                item (W is loaded once per item); 0 = default */
@@ -163,9 +164,13 @@ typedef struct {
                                  OR-ed in (never cleared by the library)     */
 } kvx_transfer_args;
 
-/* Validate the descriptor, build the RoPE tables (cos/sin of p * w_i for
- * p in [0, max_position), computed in double precision on the host and
- * stored as fp32) on the current device and return an opaque plan in *out.
+/* Validate the descriptor and prepare the plan on the current device: for
+ * the SIMT kernel, RoPE tables (cos/sin of p * w_i for p in
+ * [0, max_position), computed in double precision on the host and stored as
+ * fp32); for the tensor-core kernel, the frequencies w_i / 2pi as 64-bit
+ * fixed-point fractions of a turn (the kernel reduces p * w_i exactly in
+ * integer arithmetic and evaluates sin/cos on [-pi, pi)) and the W-image
+ * workspace.  Returns an opaque plan in *out.
  * Returns KVX_ERR_INVALID_ARG / KVX_ERR_PAIR_MISMATCH for a bad descriptor
  * (before touching the device), KVX_ERR_UNSUPPORTED if the current device
  * is not sm_103 or the forced kernel cannot handle the shape, KVX_ERR_CUDA or
