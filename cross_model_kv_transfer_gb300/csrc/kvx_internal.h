@@ -23,9 +23,12 @@ struct kvx_plan {
   size_t workspace_bytes;
   int tiles_per_item;    // 128-token tiles per work item of the persistent kernel
   void *encode_tiled;    // driver entry point cuTensorMapEncodeTiled
-  // RoPE frequencies in 64-bit fixed-point turns, round(w_i / 2pi * 2^64),
-  // for the tensor-core path (head_dim <= 256, so at most 128 pairs)
-  unsigned long long turns_src[128], turns_tgt[128];
+  // tensor-core path RoPE tables, position-major per couple of pairs
+  // (i, i+1), i even: tc_rope_src[i/2][p] = bf16x2 (cos_i, cos_i+1) and
+  // (sin_i, sin_i+1) of the source RoPE; tc_rope_tgt[i/2][p] = fp32
+  // (cos_i, cos_i+1, sin_i, sin_i+1) of the target RoPE
+  void *tc_rope_src;
+  void *tc_rope_tgt;
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
 };
 

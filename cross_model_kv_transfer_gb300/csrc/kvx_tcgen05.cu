@@ -182,25 +182,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// ---------------------------------------------------------------------------
-// RoPE angles without tables.  For pair i the host stores the frequency in
-// turns, F_i = round(w_i / (2 pi) * 2^64), w_i = theta^(-2i/d).  The phase of
-// position p is then p * F_i mod 2^64 (an exact integer product), whose top
-// 32 bits are the angle in [-pi, pi) to 2^-32 of a turn; __sincosf is
-// accurate to about 4e-7 there.  This replaces per-row table gathers.
-// ---------------------------------------------------------------------------
-struct RopeTurns {
-  unsigned long long src[kHalf], tgt[kHalf];
-};
-
-__device__ __forceinline__ void rope_cs(uint32_t pos, unsigned long long turns, float &c,
-                                        float &s) {
-  const unsigned long long ph = (unsigned long long)pos * turns;
-  const float a = (float)(int32_t)(uint32_t)(ph >> 32) * 1.46291807926715968e-9f;  // 2 pi / 2^32
-  __sincosf(a, &s, &c);
+// bf16x2 helpers: un-rotation of two RoPE pairs at once in bf16x2 FMA
+// arithmetic.  a = (x_i, x_{i+1}) of the first half, b = (x_{i+d/2},
+// x_{i+1+d/2}), c/s the bf16 cos/sin couples, ns = -s.  Returns
+// a*c + b*s and b*c - a*s, each rounded to bf16 (the operand precision of
+// the MMA that consumes them).
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t v) {
+  return *reinterpret_cast<__nv_bfloat162 *>(&v);
+}
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 v) {
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void unrotate2(uint32_t a, uint32_t b, uint32_t c, uint32_t s,
+                                          uint32_t ns, uint32_t &x0, uint32_t &x1) {
+  x0 = as_u32(__hfma2(as_bf2(a), as_bf2(c), __hmul2(as_bf2(b), as_bf2(s))));
+  x1 = as_u32(__hfma2(as_bf2(b), as_bf2(c), __hmul2(as_bf2(a), as_bf2(ns))));
 }
 
 // ---------------------------------------------------------------------------
@@ -267,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_transfer_kernel(const __grid_constant__ KvxParams p,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v,
-                       const __grid_constant__ RopeTurns rope,
+                       const uint2 *__restrict__ rope_src2, const float4 *__restrict__ rope_tgt4,
+                       const float *__restrict__ bias_f32,
                        const __nv_bfloat16 *__restrict__ w_img, const ItemGeom geo,
                        const int stall_test) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -341,17 +339,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t row = -1;
         if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
         const bool valid = row >= 0;
-        // cos/sin of the source RoPE at ps for this thread's 32 pairs
-        float cs[32], sn[32];
+        // bf16x2 cos/sin couples of the source RoPE at ps for this thread's
+        // 32 pairs (couple q = pairs 32 ph + 2q, +1); position-major table,
+        // so a warp's 32 consecutive rows read contiguous memory
+        uint32_t c2[16], s2[16], n2[16];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          cs[q] = 1.f;
-          sn[q] = 0.f;
+        for (int q = 0; q < 16; ++q) {
+          c2[q] = 0x3F803F80u;   // (1, 1)
+          s2[q] = 0u;
         }
         if (m == 0 && valid) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) rope_cs((uint32_t)ps, rope.src[32 * ph + q], cs[q], sn[q]);
+          for (int q = 0; q < 16; ++q) {
+            const uint2 v = __ldg(rope_src2 + (int64_t)(16 * ph + q) * p.max_position + ps);
+            c2[q] = v.x;
+            s2[q] = v.y;
+          }
         }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) n2[q] = s2[q] ^ 0x80008000u;
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_seq % geo.stages;
           if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) goto transform_done;
@@ -378,15 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) {
               if (m == 0) {
                 // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 32 ph + 8q + 2e (+1)
-                const int i0 = 8 * q + 2 * e;
-                const float a0 = bf_lo(wl[e]), a1 = bf_hi(wl[e]);
-                const float b0 = bf_lo(wh[e]), b1 = bf_hi(wh[e]);
-                const float x00 = fmaf(a0, cs[i0], b0 * sn[i0]);
-                const float x01 = fmaf(b0, cs[i0], -a0 * sn[i0]);
-                const float x10 = fmaf(a1, cs[i0 + 1], b1 * sn[i0 + 1]);
-                const float x11 = fmaf(b1, cs[i0 + 1], -a1 * sn[i0 + 1]);
-                plo[4 * q + e] = pack_bf16(x00, x10);
-                phi[4 * q + e] = pack_bf16(x01, x11);
+                const int cq = 4 * q + e;
+                unrotate2(wl[e], wh[e], c2[cq], s2[cq], n2[cq], plo[cq], phi[cq]);
               } else {
                 plo[4 * q + e] = wl[e];
                 phi[4 * q + e] = wh[e];
@@ -426,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         kvx::report(p, KVX_FLAG_BAD_LAYER_INDEX);
       const int t_beg = chunk * geo.tiles_per_item;
       const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
-      const __nv_bfloat16 *bias =
-          reinterpret_cast<const __nv_bfloat16 *>(p.b) + (((int64_t)lt * p.H + h) * 2 + m) * kD;
+      const float4 *bias4 =
+          reinterpret_cast<const float4 *>(bias_f32 + (((int64_t)lt * p.H + h) * 2 + m) * kD);
       __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(m == 0 ? p.dst_k : p.dst_v);
       for (int tile = t_beg; tile < t_end; ++tile) {
         const int64_t g = (int64_t)tile * kTileM + row_in_tile;
@@ -453,35 +452,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_ld16(dcol + kHalf + 16 * pc, vhi);
             tc_wait_ld();
             if (row >= 0) {
-              const uint4 *b4 = reinterpret_cast<const uint4 *>(bias);
-              const uint4 bl0 = __ldg(b4 + 2 * pc), bl1 = __ldg(b4 + 2 * pc + 1);
-              const uint4 bh0 = __ldg(b4 + 8 + 2 * pc), bh1 = __ldg(b4 + 8 + 2 * pc + 1);
-              const uint32_t bl[8] = {bl0.x, bl0.y, bl0.z, bl0.w, bl1.x, bl1.y, bl1.z, bl1.w};
-              const uint32_t bh[8] = {bh0.x, bh0.y, bh0.z, bh0.w, bh1.x, bh1.y, bh1.z, bh1.w};
+              // b (fp32 image), columns [16 pc, 16 pc + 16) and [64 + 16 pc, ...)
+              float bl[16], bh[16];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 x = __ldg(bias4 + 4 * pc + q), y = __ldg(bias4 + 16 + 4 * pc + q);
+                bl[4 * q] = x.x; bl[4 * q + 1] = x.y; bl[4 * q + 2] = x.z; bl[4 * q + 3] = x.w;
+                bh[4 * q] = y.x; bh[4 * q + 1] = y.y; bh[4 * q + 2] = y.z; bh[4 * q + 3] = y.w;
+              }
               uint32_t olo[8], ohi[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                float y[2][2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                  const int c = 2 * e + u;
-                  const float bl_ = u ? bf_hi(bl[e]) : bf_lo(bl[e]);
-                  const float bh_ = u ? bf_hi(bh[e]) : bf_lo(bh[e]);
-                  float y0 = __uint_as_float(vlo[c]) + bl_;
-                  float y1 = __uint_as_float(vhi[c]) + bh_;
-                  if (m == 0) {
-                    float cc, ss;
-                    rope_cs((uint32_t)pt, rope.tgt[16 * pc + c], cc, ss);
-                    const float r0 = fmaf(y0, cc, -y1 * ss);  // (y0 + j y1) exp(+j p' w_i)
-                    const float r1 = fmaf(y0, ss, y1 * cc);
-                    y0 = r0;
-                    y1 = r1;
-                  }
-                  y[u][0] = y0;
-                  y[u][1] = y1;
+                float2 y0 = __fadd2_rn(make_float2(__uint_as_float(vlo[2 * e]), __uint_as_float(vlo[2 * e + 1])),
+                                       make_float2(bl[2 * e], bl[2 * e + 1]));
+                float2 y1 = __fadd2_rn(make_float2(__uint_as_float(vhi[2 * e]), __uint_as_float(vhi[2 * e + 1])),
+                                       make_float2(bh[2 * e], bh[2 * e + 1]));
+                if (m == 0) {
+                  // (y0 + j y1) exp(+j p' w_i) for pairs i = 16 pc + 2e, +1;
+                  // table couple = (cos_i, cos_i+1, sin_i, sin_i+1)
+                  const float4 t = __ldg(rope_tgt4 + (int64_t)(8 * pc + e) * p.max_position + pt);
+                  const float2 cc = make_float2(t.x, t.y), ss = make_float2(t.z, t.w);
+                  const float2 nss = make_float2(-t.z, -t.w);
+                  const float2 r0 = __ffma2_rn(y0, cc, __fmul2_rn(y1, nss));
+                  const float2 r1 = __ffma2_rn(y0, ss, __fmul2_rn(y1, cc));
+                  y0 = r0;
+                  y1 = r1;
                 }
-                olo[e] = pack_bf16(y[0][0], y[1][0]);
-                ohi[e] = pack_bf16(y[0][1], y[1][1]);
+                olo[e] = pack_bf16(y0.x, y0.y);
+                ohi[e] = pack_bf16(y1.x, y1.y);
               }
               uint4 *o4 = reinterpret_cast<uint4 *>(orow);
               o4[2 * pc] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
@@ -627,20 +625,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// W (fp32, [Lt][H][2][k*d][d]) -> bf16 image, per (lt, h, m) 2k chunks of
+// W ([Lt][H][2][k*d][d]) -> bf16 image, per (lt, h, m) 2k chunks of
 // [128 rows n][64 k] in the 128-byte-swizzled K-major layout the MMA reads:
 // byte (n, kk) of a chunk = n*128 + ((kk/8) ^ (n%8))*16 + (kk%8)*2.
-// One CTA converts one chunk through a shared-memory transpose.
+// One CTA converts one chunk through a shared-memory transpose; the first
+// chunk's CTA also writes b of its (lt, h, m) as fp32 (the epilogue's bias).
 // ---------------------------------------------------------------------------
-template <typename WT>
+template <typename WT, typename BT>
 __global__ void __launch_bounds__(256) w_image_kernel(const WT *__restrict__ w,
-                                                      uint4 *__restrict__ img) {
+                                                      uint4 *__restrict__ img,
+                                                      const BT *__restrict__ b,
+                                                      float *__restrict__ b_img) {
   __shared__ float tile[64][kD + 1];
   const int64_t chunk = blockIdx.x;          // over (lt, h, m, c)
   const int nchunk = gridDim.y;              // chunks per (lt, h, m) = 2k
   const int64_t lhm = chunk;                 // index of (lt, h, m)
   const int c = blockIdx.y;
   const WT *src = w + (lhm * nchunk * 64 + (int64_t)c * 64) * kD;   // rows k = 64c.., [64][128]
+  if (c == 0 && threadIdx.x < kD) b_img[lhm * kD + threadIdx.x] = (float)b[lhm * kD + threadIdx.x];
   for (int e = threadIdx.x; e < 64 * kD; e += blockDim.x) {
     const int kr = e / kD, n = e % kD;
     tile[kr][n] = (float)src[(int64_t)kr * kD + n];
@@ -689,13 +691,16 @@ bool encode_map(const kvx_plan *plan, CUtensorMap *map, const void *base, const 
 
 }  // namespace
 
+static size_t w_image_bytes(const kvx_plan_desc &d) {
+  return (size_t)d.tgt_layers * d.src_kv_heads * 2 * (size_t)d.k * kD * kD * 2;
+}
+
 bool kvx_tc_supports(const kvx_plan_desc &d) {
-  return d.kv_dtype == KVX_BF16 && d.b_dtype == KVX_BF16 && d.src_head_dim == kD &&
-         d.k >= 1 && d.k <= kMaxK;
+  return d.kv_dtype == KVX_BF16 && d.src_head_dim == kD && d.k >= 1 && d.k <= kMaxK;
 }
 
 size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d) {
-  return (size_t)d.tgt_layers * d.src_kv_heads * 2 * (size_t)d.k * kD * kD * 2;
+  return w_image_bytes(d) + (size_t)d.tgt_layers * d.src_kv_heads * 2 * kD * sizeof(float);
 }
 
 void *kvx_tc_encoder() {
@@ -719,12 +724,19 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   const kvx_plan_desc &d = plan->desc;
   // 1. W -> bf16 image in the plan workspace
   dim3 wgrid((unsigned)((int64_t)p.Lt * p.H * 2), (unsigned)(2 * p.k));
-  if (d.w_dtype == KVX_F32)
-    w_image_kernel<float><<<wgrid, 256, 0, s>>>(reinterpret_cast<const float *>(p.w),
-                                                reinterpret_cast<uint4 *>(plan->workspace));
+  uint4 *img = reinterpret_cast<uint4 *>(plan->workspace);
+  float *bimg = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(plan->workspace) +
+                                          w_image_bytes(d));
+  using bf = __nv_bfloat16;
+  const bool wf = d.w_dtype == KVX_F32, bfp = d.b_dtype == KVX_F32;
+  if (wf && bfp)
+    w_image_kernel<float, float><<<wgrid, 256, 0, s>>>((const float *)p.w, img, (const float *)p.b, bimg);
+  else if (wf)
+    w_image_kernel<float, bf><<<wgrid, 256, 0, s>>>((const float *)p.w, img, (const bf *)p.b, bimg);
+  else if (bfp)
+    w_image_kernel<bf, float><<<wgrid, 256, 0, s>>>((const bf *)p.w, img, (const float *)p.b, bimg);
   else
-    w_image_kernel<__nv_bfloat16><<<wgrid, 256, 0, s>>>(
-        reinterpret_cast<const __nv_bfloat16 *>(p.w), reinterpret_cast<uint4 *>(plan->workspace));
+    w_image_kernel<bf, bf><<<wgrid, 256, 0, s>>>((const bf *)p.w, img, (const bf *)p.b, bimg);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // 2. the persistent transfer kernel
@@ -738,13 +750,9 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p))
     return cudaErrorInvalidValue;
   const int grid = (int)(geo.num_items < plan->num_sms ? geo.num_items : plan->num_sms);
-  RopeTurns rope;
-  for (int i = 0; i < kHalf; ++i) {
-    rope.src[i] = plan->turns_src[i];
-    rope.tgt[i] = plan->turns_tgt[i];
-  }
   tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k, geo.stages), s>>>(
-      p, mk, mv, rope, reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo,
-      plan->stall_test);
+      p, mk, mv, reinterpret_cast<const uint2 *>(plan->tc_rope_src),
+      reinterpret_cast<const float4 *>(plan->tc_rope_tgt), bimg,
+      reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
   return cudaGetLastError();
 }
