@@ -70,29 +70,35 @@ uint16_t bf16_bits(double x) {
   return (uint16_t)(u >> 16);
 }
 
-// Tensor-core path tables: per couple of pairs (i, i+1) and position p,
-// src: bf16x2 (cos, cos), (sin, sin); tgt: fp32 (cos, cos, sin, sin).
-void tc_rope_tables(double theta_src, double theta_tgt, int d, int max_position,
-                    std::vector<uint32_t> &src, std::vector<float> &tgt) {
+// Tensor-core path source table: per couple of pairs (i, i+1) and position
+// p, bf16x2 (cos_i, cos_i+1), (sin_i, sin_i+1).
+void tc_rope_table(double theta, int d, int max_position, std::vector<uint32_t> &src) {
   const int couples = d / 4;
   src.assign((size_t)couples * max_position * 2, 0);
-  tgt.assign((size_t)couples * max_position * 4, 0.f);
   for (int q = 0; q < couples; ++q) {
-    const double ws0 = std::pow(theta_src, -2.0 * (2 * q) / d);
-    const double ws1 = std::pow(theta_src, -2.0 * (2 * q + 1) / d);
-    const double wt0 = std::pow(theta_tgt, -2.0 * (2 * q) / d);
-    const double wt1 = std::pow(theta_tgt, -2.0 * (2 * q + 1) / d);
+    const double w0 = std::pow(theta, -2.0 * (2 * q) / d);
+    const double w1 = std::pow(theta, -2.0 * (2 * q + 1) / d);
     for (int p = 0; p < max_position; ++p) {
       const size_t o = (size_t)q * max_position + p;
-      const double a0 = p * ws0, a1 = p * ws1;
+      const double a0 = p * w0, a1 = p * w1;
       src[2 * o] = (uint32_t)bf16_bits(std::cos(a0)) | ((uint32_t)bf16_bits(std::cos(a1)) << 16);
       src[2 * o + 1] = (uint32_t)bf16_bits(std::sin(a0)) | ((uint32_t)bf16_bits(std::sin(a1)) << 16);
-      const double b0 = p * wt0, b1 = p * wt1;
-      tgt[4 * o] = (float)std::cos(b0);
-      tgt[4 * o + 1] = (float)std::cos(b1);
-      tgt[4 * o + 2] = (float)std::sin(b0);
-      tgt[4 * o + 3] = (float)std::sin(b1);
     }
+  }
+}
+
+// w_i / (2 pi) as a 64-bit binary fraction of a turn, in extended precision.
+void rope_turns(double theta, int d, unsigned long long *out) {
+  const long double two_pi = 6.283185307179586476925286766559005768L;
+  for (int i = 0; i < d / 2; ++i) {
+    const long double w = powl((long double)theta, -2.0L * (long double)i / (long double)d);
+    const long double f = w / two_pi;                  // turns per position
+    const long double x = ldexpl(f - floorl(f), 32);   // [0, 2^32)
+    const long double hi = floorl(x);
+    const long double lo = roundl(ldexpl(x - hi, 32)); // [0, 2^32]
+    unsigned long long v = (unsigned long long)hi << 32;
+    v += (unsigned long long)lo;                       // a carry wraps mod 2^64 = mod 1 turn
+    out[i] = v;
   }
 }
 
@@ -133,9 +139,8 @@ void free_tables(kvx_plan *p) {
   if (p->rope_src) cudaFree(p->rope_src);
   if (p->workspace) cudaFree(p->workspace);
   if (p->tc_rope_src) cudaFree(p->tc_rope_src);
-  if (p->tc_rope_tgt) cudaFree(p->tc_rope_tgt);
   p->rope_src = p->rope_tgt = nullptr;
-  p->workspace = p->tc_rope_src = p->tc_rope_tgt = nullptr;
+  p->workspace = p->tc_rope_src = nullptr;
 }
 
 kvx_status alloc_workspace(kvx_plan *p, size_t bytes) {
@@ -217,11 +222,9 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
     }
   } else {
     std::vector<uint32_t> ts;
-    std::vector<float> tt;
-    tc_rope_tables(desc->rope_theta_src, desc->rope_theta_tgt, desc->src_head_dim,
-                   desc->max_position, ts, tt);
+    tc_rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position, ts);
     st = upload_bytes(ts.data(), ts.size() * sizeof(uint32_t), &p->tc_rope_src);
-    if (st == KVX_OK) st = upload_bytes(tt.data(), tt.size() * sizeof(float), &p->tc_rope_tgt);
+    rope_turns(desc->rope_theta_tgt, desc->tgt_head_dim, p->turns_tgt);
   }
   if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05) {
     p->encode_tiled = kvx_tc_encoder();

@@ -23,12 +23,12 @@ struct kvx_plan {
   size_t workspace_bytes;
   int tiles_per_item;    // 128-token tiles per work item of the persistent kernel
   void *encode_tiled;    // driver entry point cuTensorMapEncodeTiled
-  // tensor-core path RoPE tables, position-major per couple of pairs
-  // (i, i+1), i even: tc_rope_src[i/2][p] = bf16x2 (cos_i, cos_i+1) and
-  // (sin_i, sin_i+1) of the source RoPE; tc_rope_tgt[i/2][p] = fp32
-  // (cos_i, cos_i+1, sin_i, sin_i+1) of the target RoPE
+  // tensor-core path: source RoPE table, position-major per couple of pairs
+  // (i, i+1), i even: tc_rope_src[i/2][p] = bf16x2 (cos_i, cos_i+1),
+  // (sin_i, sin_i+1); target RoPE frequencies as 64-bit fractions of a turn,
+  // round(w_i / 2pi * 2^64)
   void *tc_rope_src;
-  void *tc_rope_tgt;
+  unsigned long long turns_tgt[128];
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
 };
 

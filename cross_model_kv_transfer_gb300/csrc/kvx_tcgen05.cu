@@ -57,11 +57,11 @@ constexpr int kStageBytes = 2 * kChunkBytes;  // one selection of one tile
 constexpr int kMaxStages = 4;
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
 constexpr int kTransformWarps = 8;
-constexpr int kEpilogueWarps = 4;
-constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 12
-constexpr int kProducerWarp = kMmaWarp + 1;                  // 13
-constexpr int kLoaderWarp = kProducerWarp + 1;               // 14
-constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 480
+constexpr int kEpilogueWarps = 8;
+constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 16
+constexpr int kProducerWarp = kMmaWarp + 1;                  // 17
+constexpr int kLoaderWarp = kProducerWarp + 1;               // 18
+constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 608
 constexpr uint64_t kWaitNs = 2000000000ull;                  // 2 s without progress
 constexpr uint64_t kStallTestWaitNs = 20000000ull;           // 20 ms (stall test hook)
 
@@ -183,6 +183,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Target RoPE angles without memory traffic.  The plan stores each pair's
+// frequency in turns as a 64-bit binary fraction, F_i = round(w_i / 2pi *
+// 2^64).  The phase of position p is p * F_i mod 2^64, an exact integer
+// product; its top 32 bits give the angle in [-pi, pi) to 2^-32 of a turn,
+// where __sincosf is accurate to about 4e-7.
+struct RopeTurns {
+  unsigned long long tgt[kHalf];
+};
+
+__device__ __forceinline__ void rope_cs(uint32_t pos, unsigned long long turns, float &c,
+                                        float &s) {
+  const uint32_t hi = (uint32_t)(turns >> 32), lo = (uint32_t)turns;
+  const uint32_t top = __umulhi(pos, lo) + pos * hi;    // bits 32..63 of pos * F mod 2^64
+  const float a = (float)(int32_t)top * 1.46291807926715968e-9f;  // 2 pi / 2^32
+  __sincosf(a, &s, &c);
+}
+
 // bf16x2 helpers: un-rotation of two RoPE pairs at once in bf16x2 FMA
 // arithmetic.  a = (x_i, x_{i+1}) of the first half, b = (x_{i+d/2},
 // x_{i+1+d/2}), c/s the bf16 cos/sin couples, ns = -s.  Returns
@@ -264,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_transfer_kernel(const __grid_constant__ KvxParams p,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v,
-                       const uint2 *__restrict__ rope_src2, const float4 *__restrict__ rope_tgt4,
+                       const uint2 *__restrict__ rope_src2,
+                       const __grid_constant__ RopeTurns rope,
                        const float *__restrict__ bias_f32,
                        const __nv_bfloat16 *__restrict__ w_img, const ItemGeom geo,
                        const int stall_test) {
@@ -342,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bf16x2 cos/sin couples of the source RoPE at ps for this thread's
         // 32 pairs (couple q = pairs 32 ph + 2q, +1); position-major table,
         // so a warp's 32 consecutive rows read contiguous memory
-        uint32_t c2[16], s2[16], n2[16];
+        uint32_t c2[16], s2[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           c2[q] = 0x3F803F80u;   // (1, 1)
@@ -356,8 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             s2[q] = v.y;
           }
         }
-#pragma unroll
-        for (int q = 0; q < 16; ++q) n2[q] = s2[q] ^ 0x80008000u;
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_seq % geo.stages;
           if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) goto transform_done;
@@ -385,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (m == 0) {
                 // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 32 ph + 8q + 2e (+1)
                 const int cq = 4 * q + e;
-                unrotate2(wl[e], wh[e], c2[cq], s2[cq], n2[cq], plo[cq], phi[cq]);
+                unrotate2(wl[e], wh[e], c2[cq], s2[cq], s2[cq] ^ 0x80008000u, plo[cq], phi[cq]);
               } else {
                 plo[4 * q + e] = wl[e];
                 phi[4 * q + e] = wh[e];
@@ -413,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue warps: accumulator -> + b -> re-rotate (K) -> bf16 -> cache
     // ------------------------------------------------------------------
     const int quad = warp & 3;
+    const int eh = (warp - kTransformWarps) >> 2;   // pairs [32 eh, 32 eh + 32)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint32_t d_seq = 0;
@@ -434,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t row = -1;
         uint32_t bad = 0;
         if (g < p.ntok) bad = kvx::token_meta(p, g, ps, pt, row);
-        if (reporter) {
+        if (reporter && eh == 0) {
           const uint32_t any = __reduce_or_sync(0xffffffffu, bad);
           if (lane == 0) kvx::report(p, any);
         }
@@ -446,7 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
           __nv_bfloat16 *orow = dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
 #pragma unroll
-          for (int pc = 0; pc < 4; ++pc) {
+          for (int pcl = 0; pcl < 2; ++pcl) {
+            const int pc = 2 * eh + pcl;         // 16-pair chunk of the row
             uint32_t vlo[16], vhi[16];
             tc_ld16(dcol + 16 * pc, vlo);
             tc_ld16(dcol + kHalf + 16 * pc, vhi);
@@ -468,11 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float2 y1 = __fadd2_rn(make_float2(__uint_as_float(vhi[2 * e]), __uint_as_float(vhi[2 * e + 1])),
                                        make_float2(bh[2 * e], bh[2 * e + 1]));
                 if (m == 0) {
-                  // (y0 + j y1) exp(+j p' w_i) for pairs i = 16 pc + 2e, +1;
-                  // table couple = (cos_i, cos_i+1, sin_i, sin_i+1)
-                  const float4 t = __ldg(rope_tgt4 + (int64_t)(8 * pc + e) * p.max_position + pt);
-                  const float2 cc = make_float2(t.x, t.y), ss = make_float2(t.z, t.w);
-                  const float2 nss = make_float2(-t.z, -t.w);
+                  // (y0 + j y1) exp(+j p' w_i) for pairs i = 16 pc + 2e, +1
+                  float c0, s0, c1, s1;
+                  rope_cs((uint32_t)pt, rope.tgt[16 * pc + 2 * e], c0, s0);
+                  rope_cs((uint32_t)pt, rope.tgt[16 * pc + 2 * e + 1], c1, s1);
+                  const float2 cc = make_float2(c0, c1), ss = make_float2(s0, s1);
+                  const float2 nss = make_float2(-s0, -s1);
                   const float2 r0 = __ffma2_rn(y0, cc, __fmul2_rn(y1, nss));
                   const float2 r1 = __ffma2_rn(y0, ss, __fmul2_rn(y1, cc));
                   y0 = r0;
@@ -750,9 +769,10 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p))
     return cudaErrorInvalidValue;
   const int grid = (int)(geo.num_items < plan->num_sms ? geo.num_items : plan->num_sms);
+  RopeTurns rope;
+  for (int i = 0; i < kHalf; ++i) rope.tgt[i] = plan->turns_tgt[i];
   tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k, geo.stages), s>>>(
-      p, mk, mv, reinterpret_cast<const uint2 *>(plan->tc_rope_src),
-      reinterpret_cast<const float4 *>(plan->tc_rope_tgt), bimg,
+      p, mk, mv, reinterpret_cast<const uint2 *>(plan->tc_rope_src), rope, bimg,
       reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
   return cudaGetLastError();
 }
