@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py: whole-job aggregation over ranks (world size
+2, gloo, CPU), clock-sample parsing and the roofline arithmetic."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from cross_model_kv_transfer_gb300.workloads import WORKLOADS
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    bench.init_dist("gloo")
+    ms_local = [4.0, 5.0][rank]
+    value, ms = bench.aggregate(1000, ms_local)
+    bench.barrier()
+    out[rank] = (value, ms)
+    dist.destroy_process_group()
+
+
+def test_aggregate_takes_slowest_rank_and_all_tokens():
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(2, port, out), nprocs=2, start_method="spawn", join=True)
+    for r in range(2):
+        value, ms = out[r]
+        assert ms == 5.0
+        assert value == pytest.approx(2 * 1000 / 5e-3)
+
+
+def test_single_process_aggregate_is_local():
+    value, ms = bench.aggregate(32768, 8.0)
+    assert ms == 8.0 and value == pytest.approx(32768 / 8e-3)
+
+
+def test_clock_summary_flags_throttle_reasons():
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.lines = ["1900, 2070, 900.0, Not Active, Not Active, Not Active, Active",
+               "2070, 2070, 1000.0, Not Active, Not Active, Not Active, Not Active",
+               "garbage"]
+    s = c.summary()
+    assert s["sm_mhz"] == pytest.approx(1985.0) and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def test_roofline_picks_the_tighter_bound():
+    wl = WORKLOADS["qwen3_14b_32b"]
+    idx = torch.stack([torch.arange(4) + i % 36 for i in range(64)]).to(torch.int32)
+    peaks = {"hbm_gbs": 6766.7, "bf16_tflops": 1908.0, "bf16_tflops_sustained": 1679.6}
+    r = bench.roofline(wl, idx, 4.398046511104, "tcgen05", peaks, "measured")
+    # 4.398 TFLOP in 4.398 ms = 1000 TFLOP/s; tensor time 2.31 ms > HBM time
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(1000.0, rel=1e-6)
+    assert r["frac"] == pytest.approx(1000.0 / 1908.0, rel=1e-6)
+    assert r["algorithmic_flops"] == 2 * 32768 * 512 * 128 * 64 * 8 * 2
+    small = wl.with_tokens([512], [0])
+    r = bench.roofline(small, idx, 1.0, "tcgen05", peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+
+
+def test_published_context_number_is_the_32k_mapper_latency():
+    # the Qwen3 article's 14B -> 32B mapper: 277.6 ms at 32,768 tokens
+    assert bench.PUBLISHED_MS["qwen3_14b_32b"] == 277.6
+    assert json.dumps(bench.METRIC)
