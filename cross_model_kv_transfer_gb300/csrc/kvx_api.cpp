@@ -172,6 +172,8 @@ const char *kvx_status_string(kvx_status s) {
     case KVX_ERR_UNSUPPORTED: return "unsupported device or configuration";
     case KVX_ERR_CUDA: return "CUDA runtime error";
     case KVX_ERR_NO_MEMORY: return "out of device memory";
+    case KVX_ERR_TOO_LARGE:
+      return "RoPE tables exceed the fixed device array of the allocation-free entry point";
   }
   return "unknown status";
 }

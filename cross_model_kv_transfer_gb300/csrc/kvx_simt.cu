@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "kvx_device.cuh"
 #include "kvx_internal.h"
 
@@ -203,4 +205,167 @@ cudaError_t kvx_simt_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   KvxParams pp = p;
   void *args[] = {&pp};
   return cudaLaunchKernel(fn, grid, block, args, bytes, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (kvx_transfer_static).
+//
+// Some callers cannot allocate device memory: serving engines that reserve
+// nearly all of the GPU for their own paged KV-cache pool and forbid later
+// cudaMalloc calls, and latency-critical paths where cudaMalloc/cudaFree
+// (which may synchronise the device) are not acceptable.  This entry point
+// runs the SIMT transfer kernel above without a plan: the RoPE tables it
+// needs live in one fixed file-scope device array, filled on the device by
+// every call.  The array holds kStaticRopeEntries (cos, sin) pairs, 8 MiB,
+// and stays allocated on every GPU that loads the library until the process
+// exits.  All calls share it, so calls whose kernels overlap on the GPU (for
+// example on two streams) race on it; order them.  Nothing in it has to
+// start at zero: each call rewrites the part it reads.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kStaticRopeEntries = (size_t)1 << 20;   // 8 MiB of float2
+static __device__ __align__(256) float2 g_static_rope[kStaticRopeEntries];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+float2 *g_static_ptr[kMaxDevices];    // device address of g_static_rope, per device
+
+// cos/sin(p * theta^(-2i/d)) for p in [0, max_position), i in [0, d/2), in
+// double precision on the device, rounded once to fp32; same layout as the
+// plan tables ([p][i]); the target table follows the source table.
+__global__ void static_rope_fill_kernel(float2 *dst, int d, int max_position, double theta_src,
+                                        double theta_tgt, int two_tables) {
+  const int half = d / 2;
+  const int64_t per = (int64_t)max_position * half;
+  const int64_t n = per * (two_tables ? 2 : 1);
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(e / per);
+    const int64_t r = e - t * per;
+    const int p = (int)(r / half), i = (int)(r % half);
+    const double w = pow(t ? theta_tgt : theta_src, -2.0 * (double)i / (double)d);
+    double s, c;
+    sincos((double)p * w, &s, &c);
+    dst[e] = make_float2((float)c, (float)s);
+  }
+}
+
+bool static_dtype_ok(int32_t t) { return t == KVX_F32 || t == KVX_BF16; }
+
+}  // namespace
+
+extern "C" kvx_status kvx_transfer_static(const kvx_plan_desc *desc,
+                                          const kvx_transfer_args *a, void *stream) {
+  // descriptor: the same rules as kvx_plan_create
+  if (!desc || !a) return KVX_ERR_INVALID_ARG;
+  const kvx_plan_desc &d = *desc;
+  if (d.src_layers < 1 || d.tgt_layers < 1 || d.k < 1 || d.k > 64 || d.src_kv_heads < 1 ||
+      d.tgt_kv_heads < 1 || d.src_head_dim < 2 || d.tgt_head_dim < 2 || d.src_head_dim > 256 ||
+      d.tgt_head_dim > 256 || (d.src_head_dim & 1) || (d.tgt_head_dim & 1) ||
+      !(d.rope_theta_src > 0.0 && d.rope_theta_src < 1e300) ||
+      !(d.rope_theta_tgt > 0.0 && d.rope_theta_tgt < 1e300) || !static_dtype_ok(d.kv_dtype) ||
+      !static_dtype_ok(d.w_dtype) || !static_dtype_ok(d.b_dtype) ||
+      (d.dst_layout != KVX_CONTIGUOUS && d.dst_layout != KVX_PAGED) ||
+      (d.dst_layout == KVX_PAGED && d.block_size < 1) || d.max_position < 1 ||
+      (d.kernel != KVX_KERNEL_AUTO && d.kernel != KVX_KERNEL_SIMT) || d.flags != 0)
+    return KVX_ERR_INVALID_ARG;
+  if (d.src_kv_heads != d.tgt_kv_heads || d.src_head_dim != d.tgt_head_dim)
+    return KVX_ERR_PAIR_MISMATCH;
+  if (!kvx_simt_supports(d)) return KVX_ERR_UNSUPPORTED;
+  const int half = d.src_head_dim / 2;
+  const bool two = d.rope_theta_tgt != d.rope_theta_src;
+  if ((size_t)d.max_position * half * (two ? 2 : 1) > kStaticRopeEntries) return KVX_ERR_TOO_LARGE;
+
+  // arguments: the same rules as kvx_transfer
+  if (a->ntok < 0 || a->ntok > INT32_MAX || a->num_requests < 1 ||
+      (!a->cu_seqlens && a->num_requests != 1) || !a->src_k || !a->src_v || !a->layer_idx ||
+      !a->w || !a->b || !a->dst_k || !a->dst_v)
+    return KVX_ERR_INVALID_ARG;
+  if (d.dst_layout == KVX_CONTIGUOUS ? a->dst_capacity < 1
+                                     : (a->num_blocks < 1 || !a->block_table ||
+                                        a->max_blocks_per_req < 1))
+    return KVX_ERR_INVALID_ARG;
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVX_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KVX_ERR_UNSUPPORTED;
+  {
+    // once per device, with that device current: the device address of the
+    // static array (its host-side name is only a stand-in for it)
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+      cudaDeviceProp prop;
+      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return KVX_ERR_CUDA;
+      if (prop.major != 10 || prop.minor != 3) return KVX_ERR_UNSUPPORTED;
+      void *ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_static_rope) != cudaSuccess || !ptr) return KVX_ERR_CUDA;
+      g_static_ptr[dev] = static_cast<float2 *>(ptr);
+    }
+  }
+  if (a->ntok == 0) return KVX_OK;
+
+  // the kernel's dynamic shared memory limit is raised, never lowered
+  void *fn = select_kernel(d);
+  const size_t bytes = smem_bytes(half, d.k * d.src_head_dim);
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return KVX_ERR_CUDA;
+  if ((size_t)fa.maxDynamicSharedSizeBytes < bytes &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+          cudaSuccess)
+    return KVX_ERR_CUDA;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  float2 *rope = g_static_ptr[dev];
+  const int64_t entries = (int64_t)d.max_position * half * (two ? 2 : 1);
+  const int fill_blocks = (int)((entries + 255) / 256 < 4096 ? (entries + 255) / 256 : 4096);
+  static_rope_fill_kernel<<<fill_blocks, 256, 0, s>>>(rope, d.src_head_dim, d.max_position,
+                                                      d.rope_theta_src, d.rope_theta_tgt,
+                                                      two ? 1 : 0);
+  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
+
+  kvx_plan tmp;                     // launch description only; owns nothing
+  std::memset(&tmp, 0, sizeof(tmp));
+  tmp.desc = d;
+  tmp.device = dev;
+  tmp.kernel = KVX_KERNEL_SIMT;
+  tmp.half = half;
+  tmp.rope_src = rope;
+  tmp.rope_tgt = two ? rope + (size_t)d.max_position * half : rope;
+
+  KvxParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.src_k = a->src_k;
+  p.src_v = a->src_v;
+  p.w = a->w;
+  p.b = a->b;
+  p.dst_k = a->dst_k;
+  p.dst_v = a->dst_v;
+  p.cu_seqlens = a->cu_seqlens;
+  p.layer_idx = a->layer_idx;
+  p.src_pos = a->src_pos;
+  p.tgt_pos = a->tgt_pos;
+  p.tgt_offset = a->tgt_offset;
+  p.block_table = a->block_table;
+  p.status = a->status;
+  p.rope_src = tmp.rope_src;
+  p.rope_tgt = tmp.rope_tgt;
+  p.ntok = a->ntok;
+  p.dst_capacity = a->dst_capacity;
+  p.num_blocks = a->num_blocks;
+  p.dst_rows = d.dst_layout == KVX_CONTIGUOUS ? (int64_t)a->num_requests * a->dst_capacity
+                                              : a->num_blocks * (int64_t)d.block_size;
+  p.R = a->num_requests;
+  p.max_blocks = a->max_blocks_per_req;
+  p.Ls = d.src_layers;
+  p.Lt = d.tgt_layers;
+  p.H = d.src_kv_heads;
+  p.d = d.src_head_dim;
+  p.k = d.k;
+  p.layout = d.dst_layout;
+  p.block_size = d.block_size;
+  p.max_position = d.max_position;
+  return kvx_simt_launch(&tmp, p, s) == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }

@@ -6,8 +6,9 @@ CUDA kernels of ``libkvx.so``.  There is no fallback: if the library cannot
 be loaded (or built with nvcc on first use), importing the symbols raises.
 
 Low level (same names as the C ABI): ``kvx_plan_create``, ``kvx_transfer``,
-``kvx_plan_destroy``, ``kvx_status_string``, ``kvx_plan_kernel`` taking the
-ctypes structures ``PlanDesc`` / ``TransferArgs``.
+``kvx_plan_destroy``, ``kvx_status_string``, ``kvx_plan_kernel``,
+``kvx_plan_launches``, ``kvx_transfer_static`` taking the ctypes structures
+``PlanDesc`` / ``TransferArgs``.
 
 Convenience: ``Plan`` (owns a plan handle) and ``Plan.transfer(...)`` which
 takes torch CUDA tensors, checks their shapes, dtypes and devices, and calls
@@ -28,6 +29,7 @@ KVX_ERR_PAIR_MISMATCH = 2
 KVX_ERR_UNSUPPORTED = 3
 KVX_ERR_CUDA = 4
 KVX_ERR_NO_MEMORY = 5
+KVX_ERR_TOO_LARGE = 6
 
 KVX_FLAG_BAD_LAYER_INDEX = 1
 KVX_FLAG_BAD_POSITION = 2
@@ -46,7 +48,8 @@ KVX_KERNEL_TCGEN05 = 2
 KVX_PLAN_TEST_STALL = 1
 
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
-            "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches")
+            "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches",
+            "kvx_transfer_static")
 
 
 class PlanDesc(ctypes.Structure):
@@ -109,6 +112,9 @@ def load():
             lib.kvx_plan_kernel.restype = ctypes.c_int32
             lib.kvx_plan_launches.argtypes = [ctypes.c_void_p]
             lib.kvx_plan_launches.restype = ctypes.c_int32
+            lib.kvx_transfer_static.argtypes = [ctypes.POINTER(PlanDesc),
+                                                ctypes.POINTER(TransferArgs), ctypes.c_void_p]
+            lib.kvx_transfer_static.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -138,6 +144,12 @@ def kvx_plan_kernel(plan) -> int:
 
 def kvx_plan_launches(plan) -> int:
     return load().kvx_plan_launches(plan)
+
+
+def kvx_transfer_static(desc: PlanDesc, args: TransferArgs, stream) -> int:
+    """Allocation-free transfer (SIMT kernel, RoPE tables in the library's
+    fixed device array); for callers that may not allocate device memory."""
+    return load().kvx_transfer_static(ctypes.byref(desc), ctypes.byref(args), stream)
 
 
 class KvxError(RuntimeError):

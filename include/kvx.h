@@ -68,7 +68,9 @@ typedef enum {
                                  device (e.g. not sm_103, kernel forced onto
                                  a shape it does not handle)                 */
   KVX_ERR_CUDA = 4,           /* a CUDA runtime call failed                  */
-  KVX_ERR_NO_MEMORY = 5       /* plan tables could not be allocated          */
+  KVX_ERR_NO_MEMORY = 5,      /* plan tables could not be allocated          */
+  KVX_ERR_TOO_LARGE = 6       /* kvx_transfer_static: the RoPE tables of this
+                                 descriptor do not fit its fixed device array */
 } kvx_status;
 
 /* Bits OR-ed into kvx_transfer_args.status by the device. */
@@ -198,6 +200,31 @@ int32_t kvx_plan_kernel(const kvx_plan *plan);
 /* Number of kernel launches one kvx_transfer call enqueues with this plan
  * (0 when ntok == 0), or -1 for a NULL plan. */
 int32_t kvx_plan_launches(const kvx_plan *plan);
+
+/* Allocation-free transfer.  The sources have no counterpart for this call:
+ * it exists for callers that may not allocate device memory -- engines that
+ * reserve nearly all of the GPU for their own paged KV-cache pool and forbid
+ * later cudaMalloc calls, and latency-critical paths where cudaMalloc or
+ * cudaFree (which may synchronise the device) are not acceptable.
+ *
+ * It performs the same transfer as a plan created from `desc` with
+ * kernel = KVX_KERNEL_SIMT (fp32 FMA contraction) and takes the same
+ * arguments, but needs no plan and calls no cudaMalloc, cudaFree or other
+ * allocating routine.  Its RoPE tables live in one fixed device array of
+ * 2^20 (cos, sin) pairs (8 MiB), compiled into the library and kept on every
+ * GPU that loads it until the process exits; each call refills it on the
+ * device before the transfer kernel runs.  Limits: max_position * head_dim/2
+ * table entries, doubled when the two RoPE bases differ, must not exceed
+ * 2^20, else KVX_ERR_TOO_LARGE is returned before anything is enqueued;
+ * desc->kernel must be AUTO or SIMT and desc->flags 0.
+ *
+ * All calls share the array: calls whose work overlaps on the GPU (two
+ * streams, for instance) race on it and must be ordered by the caller.  The
+ * first call on a device looks up the array's device address (once per
+ * device, under a lock); make that first call before any stream capture.
+ * Other errors as for kvx_transfer; `stream` as for kvx_transfer. */
+kvx_status kvx_transfer_static(const kvx_plan_desc *desc, const kvx_transfer_args *args,
+                               void *stream);
 
 #ifdef __cplusplus
 }

@@ -112,6 +112,6 @@ def test_transfer_and_destroy_reject_null():
 
 
 def test_status_strings():
-    for s in range(6):
+    for s in range(7):
         assert kvx.kvx_status_string(s) not in ("", "unknown status")
     assert kvx.kvx_status_string(99) == "unknown status"

@@ -1,0 +1,85 @@
+"""The allocation-free entry point, kvx_transfer_static.
+
+It is meant for callers that may not allocate device memory (engines that
+reserve nearly all of the GPU for their own KV-cache pool and forbid later
+cudaMalloc calls, latency-critical paths that cannot accept the device
+synchronisation cudaMalloc/cudaFree may cause).  It runs the SIMT transfer
+kernel with its RoPE tables in a fixed device array compiled into the library
+instead of plan-owned memory.  Here its output is checked against the plan
+path (kvx_plan_create + kvx_transfer with the SIMT kernel) on the same
+inputs, for two calls in a row, within the tolerances of the other parity
+tests.  This file is collected last on purpose.
+"""
+import ctypes
+import dataclasses
+
+import pytest
+import torch
+
+from cross_model_kv_transfer_gb300 import kvx
+from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_inputs, sentinel_like
+
+from parity import TOL, gpu_args, make_plan, run_gpu
+
+
+def _desc(**over):
+    base = dict(src_layers=4, tgt_layers=6, src_kv_heads=2, tgt_kv_heads=2, src_head_dim=64,
+                tgt_head_dim=64, k=2, rope_theta_src=1e4, rope_theta_tgt=1e4,
+                kv_dtype=kvx.KVX_F32, w_dtype=kvx.KVX_F32, b_dtype=kvx.KVX_F32,
+                dst_layout=kvx.KVX_CONTIGUOUS, block_size=0, max_position=128,
+                kernel=kvx.KVX_KERNEL_SIMT, tiles_per_item=0, flags=0)
+    base.update(over)
+    return kvx.PlanDesc(**base)
+
+
+def test_static_entry_point_refuses_tables_beyond_its_array():
+    # 2^20 (cos, sin) entries: 32768 positions x 64 pairs fit once, not twice
+    args = kvx.TransferArgs()
+    d = _desc(src_head_dim=128, tgt_head_dim=128, max_position=32768, rope_theta_tgt=5e5)
+    assert kvx.kvx_transfer_static(d, args, None) == kvx.KVX_ERR_TOO_LARGE
+    d = _desc(src_head_dim=128, tgt_head_dim=128, max_position=16385)
+    assert kvx.kvx_transfer_static(d, args, None) == kvx.KVX_ERR_TOO_LARGE
+    assert kvx.kvx_transfer_static(_desc(kernel=kvx.KVX_KERNEL_TCGEN05), args, None) \
+        == kvx.KVX_ERR_INVALID_ARG
+    assert "fixed device array" in kvx.kvx_status_string(kvx.KVX_ERR_TOO_LARGE)
+
+
+def _static_run(wl, inp, plan):
+    shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
+    dk = sentinel_like(shape, wl.kv_dtype, "cuda")
+    dv = sentinel_like(shape, wl.kv_dtype, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = plan.make_args(**gpu_args(wl, inp, dk, dv, status))
+    stream = torch.cuda.current_stream()
+    st = kvx.kvx_transfer_static(plan.desc, args, ctypes.c_void_p(stream.cuda_stream))
+    assert st == kvx.KVX_OK, kvx.kvx_status_string(st)
+    torch.cuda.synchronize()
+    return dk, dv, int(status.item())
+
+
+def _same(wl, a, b):
+    for x, y in zip(a, b):
+        bits = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
+        untouched = y.view(bits) == -1
+        assert torch.equal(x.view(bits)[untouched], y.view(bits)[untouched])
+        xf, yf = x.double()[~untouched], y.double()[~untouched]
+        err = (xf - yf).norm() / yf.norm()
+        assert err <= TOL[wl.kv_dtype], float(err)
+
+
+@pytest.mark.gpu
+def test_static_entry_point_matches_the_plan_path_on_two_calls():
+    tiny = WORKLOADS["tiny_fp32"]
+    paged = dataclasses.replace(
+        WORKLOADS["llama31_8b_70b_paged"].with_tokens([100, 37, 260], [5, 64, 0]), tgt_layers=6)
+    for wl, theta_tgt in ((tiny, None), (paged, 1e6)):
+        if theta_tgt is not None:
+            wl = dataclasses.replace(wl, theta_tgt=theta_tgt)   # two RoPE tables
+        inp = make_inputs(wl, "cuda")
+        plan = make_plan(wl, kvx.KVX_KERNEL_SIMT)
+        rk, rv, rst, _ = run_gpu(wl, inp, plan=plan)
+        assert rst == 0
+        for _ in range(2):
+            sk, sv, sst = _static_run(wl, inp, plan)
+            assert sst == 0
+            _same(wl, (sk, sv), (rk, rv))
