@@ -18,8 +18,8 @@
 //   * X loader warp: TMA (cp.async.bulk.tensor, 4-D map over [Ls][T][H][d],
 //     128-byte swizzle) brings the 128 rows x d of one selected source layer
 //     for one tile into a ring of shared-memory stages, two boxes of 64 dims.
-//   * 8 transform warps: every thread owns one token row and one half of the
-//     RoPE pairs.  It reads its row from the stage (16-byte shared loads,
+//   * 16 transform warps: every thread owns one token row and a quarter of
+//     the RoPE pairs.  It reads its row from the stage (16-byte shared loads,
 //     conflict-free thanks to the swizzle), un-rotates keys out of the source
 //     RoPE in fp32 (step 1, "strip source RoPE"), packs bf16 and writes the
 //     row with tcgen05.st into tensor memory, which is operand A.  Values are
@@ -56,12 +56,12 @@ constexpr int kChunkBytes = 16384;    // W chunk: 128 rows x 64 k x bf16
 constexpr int kStageBytes = 2 * kChunkBytes;  // one selection of one tile
 constexpr int kMaxStages = 4;
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
-constexpr int kTransformWarps = 8;
+constexpr int kTransformWarps = 16;
 constexpr int kEpilogueWarps = 8;
-constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 16
-constexpr int kProducerWarp = kMmaWarp + 1;                  // 17
-constexpr int kLoaderWarp = kProducerWarp + 1;               // 18
-constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 608
+constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 24
+constexpr int kProducerWarp = kMmaWarp + 1;                  // 25
+constexpr int kLoaderWarp = kProducerWarp + 1;               // 26
+constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 864
 constexpr uint64_t kWaitNs = 2000000000ull;                  // 2 s without progress
 constexpr uint64_t kStallTestWaitNs = 20000000ull;           // 20 ms (stall test hook)
 
@@ -142,6 +142,20 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16])
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr)
       : "memory");
 }
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -340,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // transform warps: X rows -> tensor memory (operand A)
     // ------------------------------------------------------------------
     const int quad = warp & 3;                // TMEM lane quadrant
-    const int ph = warp >> 2;                 // RoPE pair half: pairs [32 ph, 32 ph + 32)
+    const int tq = warp >> 2;                 // RoPE pair quarter: pairs [16 tq, 16 tq + 16)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint32_t a_seq = 0, x_seq = 0;
@@ -358,18 +372,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
         const bool valid = row >= 0;
         // bf16x2 cos/sin couples of the source RoPE at ps for this thread's
-        // 32 pairs (couple q = pairs 32 ph + 2q, +1); position-major table,
+        // 16 pairs (couple q = pairs 16 tq + 2q, +1); position-major table,
         // so a warp's 32 consecutive rows read contiguous memory
-        uint32_t c2[16], s2[16];
+        uint32_t c2[8], s2[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < 8; ++q) {
           c2[q] = 0x3F803F80u;   // (1, 1)
           s2[q] = 0u;
         }
         if (m == 0 && valid) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const uint2 v = __ldg(rope_src2 + (int64_t)(16 * ph + q) * p.max_position + ps);
+          for (int q = 0; q < 8; ++q) {
+            const uint2 v = __ldg(rope_src2 + (int64_t)(8 * tq + q) * p.max_position + ps);
             c2[q] = v.x;
             s2[q] = v.y;
           }
@@ -377,13 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_seq % geo.stages;
           if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) goto transform_done;
-          // this row's dims [32 ph, 32 ph + 32) (box 0) and [64 + 32 ph, ...)
-          // (box 1): logical 16-byte chunks 4 ph .. 4 ph + 3 of a 128-byte row
+          // this row's dims [16 tq, 16 tq + 16) (box 0) and [64 + 16 tq, ...)
+          // (box 1): logical 16-byte chunks 2 tq, 2 tq + 1 of a 128-byte row
           const unsigned char *rb = xbuf + stage * kStageBytes + row_in_tile * 128;
-          uint4 lo[4], hi[4];
+          uint4 lo[2], hi[2];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int pc = ((4 * ph + q) ^ sw) * 16;
+          for (int q = 0; q < 2; ++q) {
+            const int pc = ((2 * tq + q) ^ sw) * 16;
             lo[q] = *reinterpret_cast<const uint4 *>(rb + pc);
             hi[q] = *reinterpret_cast<const uint4 *>(rb + kChunkBytes + pc);
           }
@@ -391,15 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++x_seq;
           const int slot = a_seq % kSlots;
           const uint32_t round = a_seq / kSlots;
-          uint32_t plo[16], phi[16];
+          uint32_t plo[8], phi[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             const uint32_t wl[4] = {lo[q].x, lo[q].y, lo[q].z, lo[q].w};
             const uint32_t wh[4] = {hi[q].x, hi[q].y, hi[q].z, hi[q].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (m == 0) {
-                // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 32 ph + 8q + 2e (+1)
+                // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 16 tq + 8q + 2e (+1)
                 const int cq = 4 * q + e;
                 unrotate2(wl[e], wh[e], c2[cq], s2[cq], s2[cq] ^ 0x80008000u, plo[cq], phi[cq]);
               } else {
@@ -411,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!W.wait(&sh->a_empty[slot], (round & 1) ^ 1)) goto transform_done;
           tc_fence_after();
           {
-            const uint32_t col = (uint32_t)(slot * kSlotCols + 16 * ph);
-            tc_st16(tmem + lane_base + col, plo);
-            tc_st16(tmem + lane_base + col + 32, phi);
+            const uint32_t col = (uint32_t)(slot * kSlotCols + 8 * tq);
+            tc_st8(tmem + lane_base + col, plo);
+            tc_st8(tmem + lane_base + col + 32, phi);
           }
           tc_wait_st();
           tc_fence_before();
@@ -463,33 +477,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
           __nv_bfloat16 *orow = dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
 #pragma unroll
-          for (int pcl = 0; pcl < 2; ++pcl) {
-            const int pc = 2 * eh + pcl;         // 16-pair chunk of the row
-            uint32_t vlo[16], vhi[16];
-            tc_ld16(dcol + 16 * pc, vlo);
-            tc_ld16(dcol + kHalf + 16 * pc, vhi);
+          for (int pcl = 0; pcl < 4; ++pcl) {
+            const int pc = 4 * eh + pcl;         // 8-pair chunk of the row
+            uint32_t vlo[8], vhi[8];
+            tc_ld8(dcol + 8 * pc, vlo);
+            tc_ld8(dcol + kHalf + 8 * pc, vhi);
             tc_wait_ld();
             if (row >= 0) {
-              // b (fp32 image), columns [16 pc, 16 pc + 16) and [64 + 16 pc, ...)
-              float bl[16], bh[16];
+              // b (fp32 image), columns [8 pc, 8 pc + 8) and [64 + 8 pc, ...)
+              float bl[8], bh[8];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 x = __ldg(bias4 + 4 * pc + q), y = __ldg(bias4 + 16 + 4 * pc + q);
+              for (int q = 0; q < 2; ++q) {
+                const float4 x = __ldg(bias4 + 2 * pc + q), y = __ldg(bias4 + 16 + 2 * pc + q);
                 bl[4 * q] = x.x; bl[4 * q + 1] = x.y; bl[4 * q + 2] = x.z; bl[4 * q + 3] = x.w;
                 bh[4 * q] = y.x; bh[4 * q + 1] = y.y; bh[4 * q + 2] = y.z; bh[4 * q + 3] = y.w;
               }
-              uint32_t olo[8], ohi[8];
+              uint32_t olo[4], ohi[4];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
+              for (int e = 0; e < 4; ++e) {
                 float2 y0 = __fadd2_rn(make_float2(__uint_as_float(vlo[2 * e]), __uint_as_float(vlo[2 * e + 1])),
                                        make_float2(bl[2 * e], bl[2 * e + 1]));
                 float2 y1 = __fadd2_rn(make_float2(__uint_as_float(vhi[2 * e]), __uint_as_float(vhi[2 * e + 1])),
                                        make_float2(bh[2 * e], bh[2 * e + 1]));
                 if (m == 0) {
-                  // (y0 + j y1) exp(+j p' w_i) for pairs i = 16 pc + 2e, +1
+                  // (y0 + j y1) exp(+j p' w_i) for pairs i = 8 pc + 2e, +1
                   float c0, s0, c1, s1;
-                  rope_cs((uint32_t)pt, rope.tgt[16 * pc + 2 * e], c0, s0);
-                  rope_cs((uint32_t)pt, rope.tgt[16 * pc + 2 * e + 1], c1, s1);
+                  rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e], c0, s0);
+                  rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e + 1], c1, s1);
                   const float2 cc = make_float2(c0, c1), ss = make_float2(s0, s1);
                   const float2 nss = make_float2(-s0, -s1);
                   const float2 r0 = __ffma2_rn(y0, cc, __fmul2_rn(y1, nss));
@@ -501,10 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ohi[e] = pack_bf16(y1.x, y1.y);
               }
               uint4 *o4 = reinterpret_cast<uint4 *>(orow);
-              o4[2 * pc] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-              o4[2 * pc + 1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
-              o4[8 + 2 * pc] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-              o4[8 + 2 * pc + 1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+              o4[pc] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+              o4[8 + pc] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
             }
           }
         }
