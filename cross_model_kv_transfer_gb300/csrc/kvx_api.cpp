@@ -275,9 +275,11 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   if (!a->cu_seqlens && a->num_requests != 1) return KVX_ERR_INVALID_ARG;
   if (!a->src_k || !a->src_v || !a->layer_idx || !a->w || !a->b || !a->dst_k || !a->dst_v)
     return KVX_ERR_INVALID_ARG;
-  // the tensor-core path reads the source through TMA: 16-byte aligned bases
+  // the tensor-core path reads the source through TMA (16-byte aligned bases)
+  // and writes the cache in whole 32-byte sectors (32-byte aligned bases)
   if (plan->kernel == KVX_KERNEL_TCGEN05 &&
-      (((uintptr_t)a->src_k | (uintptr_t)a->src_v) & 15u))
+      ((((uintptr_t)a->src_k | (uintptr_t)a->src_v) & 15u) ||
+       (((uintptr_t)a->dst_k | (uintptr_t)a->dst_v) & 31u)))
     return KVX_ERR_INVALID_ARG;
   if (d.dst_layout == KVX_CONTIGUOUS) {
     if (a->dst_capacity < 1) return KVX_ERR_INVALID_ARG;

@@ -39,6 +39,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "kvx_device.cuh"
 #include "kvx_internal.h"
 
@@ -135,15 +137,6 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15])
-      : "memory");
-}
 __device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
@@ -158,15 +151,11 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
       : "r"(taddr)
       : "memory");
 }
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr)
-      : "memory");
+// 32-byte global store (one full sector); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -278,6 +267,32 @@ struct ItemGeom {
   long long num_items;
 };
 
+// Source-RoPE couples of row `row_in_tile` of `tile` for pairs
+// [16 tq, 16 tq + 16): couple q holds (cos, cos) and (sin, sin) in bf16x2 for
+// pairs 16 tq + 2q and +1 from the position-major table (a warp's 32
+// consecutive rows read contiguous memory).  Rows outside the transfer or
+// with an invalid position get the identity rotation.
+__device__ __forceinline__ void load_couples(const KvxParams &p, const uint2 *__restrict__ rope_src2,
+                                             int tile, int row_in_tile, int tq,
+                                             uint32_t (&c2)[8], uint32_t (&s2)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    c2[q] = 0x3F803F80u;   // (1, 1)
+    s2[q] = 0u;
+  }
+  const int64_t g = (int64_t)tile * kTileM + row_in_tile;
+  int32_t ps = 0, pt = 0;
+  int64_t row = -1;
+  if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
+  if (row < 0) return;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint2 v = __ldg(rope_src2 + (int64_t)(8 * tq + q) * p.max_position + ps);
+    c2[q] = v.x;
+    s2[q] = v.y;
+  }
+}
+
 __device__ __forceinline__ void decode_item(const KvxParams &p, const ItemGeom &g, long long item,
                                             int &h, int &chunk, int &lt, int &m) {
   m = (int)(item & 1);
@@ -359,70 +374,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint32_t a_seq = 0, x_seq = 0;
     const int sw = row_in_tile & 7;           // 128-byte swizzle phase of this row
-    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
-      int h, chunk, lt, m;
-      decode_item(p, geo, item, h, chunk, lt, m);
-      if (!kvx::layer_row_ok(p, lt)) continue;
-      const int t_beg = chunk * geo.tiles_per_item;
-      const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+    // The tiles of one item; keys (un-rotated out of the source RoPE) and
+    // values (copied as stored) are compiled as separate loops.  Returns
+    // false when the pipeline is being abandoned.
+    auto tiles = [&](auto key_c, int t_beg, int t_end) -> bool {
+      constexpr bool kKey = decltype(key_c)::value;
       for (int tile = t_beg; tile < t_end; ++tile) {
-        const int64_t g = (int64_t)tile * kTileM + row_in_tile;
-        int32_t ps = 0, pt = 0;
-        int64_t row = -1;
-        if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
-        const bool valid = row >= 0;
-        // bf16x2 cos/sin couples of the source RoPE at ps for this thread's
-        // 16 pairs (couple q = pairs 16 tq + 2q, +1); position-major table,
-        // so a warp's 32 consecutive rows read contiguous memory
+        // bf16x2 cos/sin couples of the source RoPE at this row's position
+        // for the thread's 16 pairs (couple q = pairs 16 tq + 2q, +1)
         uint32_t c2[8], s2[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          c2[q] = 0x3F803F80u;   // (1, 1)
-          s2[q] = 0u;
-        }
-        if (m == 0 && valid) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint2 v = __ldg(rope_src2 + (int64_t)(8 * tq + q) * p.max_position + ps);
-            c2[q] = v.x;
-            s2[q] = v.y;
-          }
-        }
+        if constexpr (kKey) load_couples(p, rope_src2, tile, row_in_tile, tq, c2, s2);
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_seq % geo.stages;
-          if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) goto transform_done;
+          if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) return false;
           // this row's dims [16 tq, 16 tq + 16) (box 0) and [64 + 16 tq, ...)
           // (box 1): logical 16-byte chunks 2 tq, 2 tq + 1 of a 128-byte row
           const unsigned char *rb = xbuf + stage * kStageBytes + row_in_tile * 128;
-          uint4 lo[2], hi[2];
+          uint32_t plo[8], phi[8];
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int pc = ((2 * tq + q) ^ sw) * 16;
-            lo[q] = *reinterpret_cast<const uint4 *>(rb + pc);
-            hi[q] = *reinterpret_cast<const uint4 *>(rb + kChunkBytes + pc);
+            const uint4 lo = *reinterpret_cast<const uint4 *>(rb + pc);
+            const uint4 hi = *reinterpret_cast<const uint4 *>(rb + kChunkBytes + pc);
+            plo[4 * q] = lo.x; plo[4 * q + 1] = lo.y; plo[4 * q + 2] = lo.z; plo[4 * q + 3] = lo.w;
+            phi[4 * q] = hi.x; phi[4 * q + 1] = hi.y; phi[4 * q + 2] = hi.z; phi[4 * q + 3] = hi.w;
           }
           mbar_arrive(smem_addr(&sh->x_empty[stage]));
           ++x_seq;
           const int slot = a_seq % kSlots;
           const uint32_t round = a_seq / kSlots;
-          uint32_t plo[8], phi[8];
+          if constexpr (kKey) {
+            // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 16 tq + 2q (+1)
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t wl[4] = {lo[q].x, lo[q].y, lo[q].z, lo[q].w};
-            const uint32_t wh[4] = {hi[q].x, hi[q].y, hi[q].z, hi[q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (m == 0) {
-                // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 16 tq + 8q + 2e (+1)
-                const int cq = 4 * q + e;
-                unrotate2(wl[e], wh[e], c2[cq], s2[cq], s2[cq] ^ 0x80008000u, plo[cq], phi[cq]);
-              } else {
-                plo[4 * q + e] = wl[e];
-                phi[4 * q + e] = wh[e];
-              }
-            }
+            for (int q = 0; q < 8; ++q)
+              unrotate2(plo[q], phi[q], c2[q], s2[q], s2[q] ^ 0x80008000u, plo[q], phi[q]);
           }
-          if (!W.wait(&sh->a_empty[slot], (round & 1) ^ 1)) goto transform_done;
+          if (!W.wait(&sh->a_empty[slot], (round & 1) ^ 1)) return false;
           tc_fence_after();
           {
             const uint32_t col = (uint32_t)(slot * kSlotCols + 8 * tq);
@@ -436,8 +423,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++a_seq;
         }
       }
+      return true;
+    };
+    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+      int h, chunk, lt, m;
+      decode_item(p, geo, item, h, chunk, lt, m);
+      if (!kvx::layer_row_ok(p, lt)) continue;
+      const int t_beg = chunk * geo.tiles_per_item;
+      const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+      const bool go = m == 0 ? tiles(std::true_type{}, t_beg, t_end)
+                             : tiles(std::false_type{}, t_beg, t_end);
+      if (!go) break;
     }
-  transform_done:;
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------------
     // epilogue warps: accumulator -> + b -> re-rotate (K) -> bf16 -> cache
@@ -447,6 +444,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint32_t d_seq = 0;
+    // The tiles of one item (keys re-rotated into the target RoPE, values
+    // not), compiled as separate loops.  Returns false when the pipeline is
+    // being abandoned.
+    auto tiles = [&](auto key_c, int lt, int h, int t_beg, int t_end, bool layer_ok,
+                     bool reporter) -> bool {
+      constexpr bool kKey = decltype(key_c)::value;
+      const float2 *bias2 = reinterpret_cast<const float2 *>(
+          bias_f32 + (((int64_t)lt * p.H + h) * 2 + (kKey ? 0 : 1)) * kD);
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(kKey ? p.dst_k : p.dst_v);
+      for (int tile = t_beg; tile < t_end; ++tile) {
+        const int64_t g = (int64_t)tile * kTileM + row_in_tile;
+        int32_t ps = 0, pt = 0;
+        int64_t row = -1;
+        uint32_t bad = 0;
+        if (g < p.ntok) bad = kvx::token_meta(p, g, ps, pt, row);
+        if (kKey && reporter && eh == 0) {
+          const uint32_t any = __reduce_or_sync(0xffffffffu, bad);
+          if (lane == 0) kvx::report(p, any);
+        }
+        if (!layer_ok) continue;
+        const int buf = d_seq & 1;
+        if (!W.wait(&sh->d_full[buf], (d_seq >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
+        __nv_bfloat16 *orow =
+            dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
+#pragma unroll 1
+        for (int pp = 0; pp < 2; ++pp) {
+          // two 8-pair chunks (pc0, pc0 + 1) make one 32-byte sector of the
+          // row's first half and one of its second half
+          const int pc0 = 4 * eh + 2 * pp;
+          uint32_t olo[8], ohi[8];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int pc = pc0 + c;
+            uint32_t vlo[8], vhi[8];
+            tc_ld8(dcol + 8 * pc, vlo);
+            tc_ld8(dcol + kHalf + 8 * pc, vhi);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // b (fp32 image) at columns 8 pc + 2e, +1 and 64 + 8 pc + 2e, +1
+              const float2 bl = __ldg(bias2 + 4 * pc + e), bh = __ldg(bias2 + 32 + 4 * pc + e);
+              float2 y0 = __fadd2_rn(make_float2(__uint_as_float(vlo[2 * e]), __uint_as_float(vlo[2 * e + 1])), bl);
+              float2 y1 = __fadd2_rn(make_float2(__uint_as_float(vhi[2 * e]), __uint_as_float(vhi[2 * e + 1])), bh);
+              if constexpr (kKey) {
+                // (y0 + j y1) exp(+j p' w_i) for pairs i = 8 pc + 2e, +1
+                float c0, s0, c1, s1;
+                rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e], c0, s0);
+                rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e + 1], c1, s1);
+                const float2 cc = make_float2(c0, c1), ss = make_float2(s0, s1);
+                const float2 nss = make_float2(-s0, -s1);
+                const float2 r0 = __ffma2_rn(y0, cc, __fmul2_rn(y1, nss));
+                const float2 r1 = __ffma2_rn(y0, ss, __fmul2_rn(y1, cc));
+                y0 = r0;
+                y1 = r1;
+              }
+              olo[4 * c + e] = pack_bf16(y0.x, y0.y);
+              ohi[4 * c + e] = pack_bf16(y1.x, y1.y);
+            }
+          }
+          if (row >= 0) {
+            st_global_v8(orow + 8 * pc0, olo);
+            st_global_v8(orow + kHalf + 8 * pc0, ohi);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
+        ++d_seq;
+      }
+      return true;
+    };
     for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
       int h, chunk, lt, m;
       decode_item(p, geo, item, h, chunk, lt, m);
@@ -456,77 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         kvx::report(p, KVX_FLAG_BAD_LAYER_INDEX);
       const int t_beg = chunk * geo.tiles_per_item;
       const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
-      const float4 *bias4 =
-          reinterpret_cast<const float4 *>(bias_f32 + (((int64_t)lt * p.H + h) * 2 + m) * kD);
-      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(m == 0 ? p.dst_k : p.dst_v);
-      for (int tile = t_beg; tile < t_end; ++tile) {
-        const int64_t g = (int64_t)tile * kTileM + row_in_tile;
-        int32_t ps = 0, pt = 0;
-        int64_t row = -1;
-        uint32_t bad = 0;
-        if (g < p.ntok) bad = kvx::token_meta(p, g, ps, pt, row);
-        if (reporter && eh == 0) {
-          const uint32_t any = __reduce_or_sync(0xffffffffu, bad);
-          if (lane == 0) kvx::report(p, any);
-        }
-        if (!layer_ok) continue;
-        const int buf = d_seq & 1;
-        if (!W.wait(&sh->d_full[buf], (d_seq >> 1) & 1)) goto epilogue_done;
-        tc_fence_after();
-        {
-          const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
-          __nv_bfloat16 *orow = dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
-#pragma unroll
-          for (int pcl = 0; pcl < 4; ++pcl) {
-            const int pc = 4 * eh + pcl;         // 8-pair chunk of the row
-            uint32_t vlo[8], vhi[8];
-            tc_ld8(dcol + 8 * pc, vlo);
-            tc_ld8(dcol + kHalf + 8 * pc, vhi);
-            tc_wait_ld();
-            if (row >= 0) {
-              // b (fp32 image), columns [8 pc, 8 pc + 8) and [64 + 8 pc, ...)
-              float bl[8], bh[8];
-#pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                const float4 x = __ldg(bias4 + 2 * pc + q), y = __ldg(bias4 + 16 + 2 * pc + q);
-                bl[4 * q] = x.x; bl[4 * q + 1] = x.y; bl[4 * q + 2] = x.z; bl[4 * q + 3] = x.w;
-                bh[4 * q] = y.x; bh[4 * q + 1] = y.y; bh[4 * q + 2] = y.z; bh[4 * q + 3] = y.w;
-              }
-              uint32_t olo[4], ohi[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                float2 y0 = __fadd2_rn(make_float2(__uint_as_float(vlo[2 * e]), __uint_as_float(vlo[2 * e + 1])),
-                                       make_float2(bl[2 * e], bl[2 * e + 1]));
-                float2 y1 = __fadd2_rn(make_float2(__uint_as_float(vhi[2 * e]), __uint_as_float(vhi[2 * e + 1])),
-                                       make_float2(bh[2 * e], bh[2 * e + 1]));
-                if (m == 0) {
-                  // (y0 + j y1) exp(+j p' w_i) for pairs i = 8 pc + 2e, +1
-                  float c0, s0, c1, s1;
-                  rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e], c0, s0);
-                  rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e + 1], c1, s1);
-                  const float2 cc = make_float2(c0, c1), ss = make_float2(s0, s1);
-                  const float2 nss = make_float2(-s0, -s1);
-                  const float2 r0 = __ffma2_rn(y0, cc, __fmul2_rn(y1, nss));
-                  const float2 r1 = __ffma2_rn(y0, ss, __fmul2_rn(y1, cc));
-                  y0 = r0;
-                  y1 = r1;
-                }
-                olo[e] = pack_bf16(y0.x, y0.y);
-                ohi[e] = pack_bf16(y1.x, y1.y);
-              }
-              uint4 *o4 = reinterpret_cast<uint4 *>(orow);
-              o4[pc] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-              o4[8 + pc] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
-        ++d_seq;
-      }
+      const bool go = m == 0 ? tiles(std::true_type{}, lt, h, t_beg, t_end, layer_ok, reporter)
+                             : tiles(std::false_type{}, lt, h, t_beg, t_end, layer_ok, reporter);
+      if (!go) break;
     }
-  epilogue_done:;
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------
     // MMA issuer (one thread)
@@ -586,29 +589,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // W producer (one thread): bf16 W image -> shared memory
     // ------------------------------------------------------------------
     if (lane == 0) {
+      // chunks [0, n_last) were last issued in round w_seq, chunks
+      // [n_last, nchunks_w) in round w_seq - 1 (rounds count from 1)
       uint32_t w_seq = 0;
-      uint32_t issued_rounds[2 * kMaxK];
-      for (int c = 0; c < 2 * kMaxK; ++c) issued_rounds[c] = 0;
+      int n_last = nchunks_w;
       for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
         int h, chunk, lt, m;
         decode_item(p, geo, item, h, chunk, lt, m);
         if (!kvx::layer_row_ok(p, lt)) continue;
         const unsigned char *img = reinterpret_cast<const unsigned char *>(w_img) +
                                    (((int64_t)lt * p.H + h) * 2 + m) * (int64_t)nchunks_w * kChunkBytes;
-        for (int c = 0; c < nchunks_w; ++c) {
-          if (!W.wait(&sh->w_empty[c], (w_seq & 1) ^ 1)) goto producer_done;
+        ++w_seq;
+        for (n_last = 0; n_last < nchunks_w; ++n_last) {
+          const int c = n_last;
+          if (!W.wait(&sh->w_empty[c], (w_seq & 1) ^ 0)) goto producer_done;
           const uint32_t bar = smem_addr(&sh->w_full[c]);
           mbar_expect_tx(bar, kChunkBytes);
           bulk_g2s(smem_addr(wbuf + c * kChunkBytes), img + (int64_t)c * kChunkBytes, kChunkBytes,
                    bar);
-          issued_rounds[c] = w_seq + 1;
         }
-        ++w_seq;
       }
     producer_done:
-      // drain: wait (bounded) until every issued copy has landed
-      for (int c = 0; c < nchunks_w; ++c)
-        if (issued_rounds[c] != 0) drain_wait(&sh->w_full[c], (issued_rounds[c] - 1) & 1);
+      // drain: wait (bounded) until every issued copy has landed; the copy of
+      // round r completes phase r - 1 of its chunk's w_full
+      for (int c = 0; c < nchunks_w; ++c) {
+        const uint32_t r = c < n_last ? w_seq : w_seq - 1;
+        if (r >= 1) drain_wait(&sh->w_full[c], (r - 1) & 1);
+      }
     }
   } else {
     // ------------------------------------------------------------------

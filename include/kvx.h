@@ -182,7 +182,9 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out);
 /* Enqueue one transfer on `stream` (a cudaStream_t; NULL is the legacy
  * default stream).  Asynchronous: no host synchronisation, no allocation.
  * Returns KVX_ERR_INVALID_ARG for a NULL plan/args or a missing required
- * pointer or size, KVX_ERR_CUDA if a launch fails.  Device-detected errors
+ * pointer or size, and, for a tensor-core plan, for source bases that are
+ * not 16-byte aligned or cache bases that are not 32-byte aligned;
+ * KVX_ERR_CUDA if a launch fails.  Device-detected errors
  * are reported through args->status as described above. */
 kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *args,
                         void *stream);
