@@ -293,14 +293,30 @@ __device__ __forceinline__ void load_couples(const KvxParams &p, const uint2 *__
   }
 }
 
+// Work items are (h, chunk, lt, m): Q = H * chunks * Lt groups (h, chunk,
+// lt), lt fastest, each with a key item (m = 0) and a value item (m = 1).
+// CTA b of G runs items b, b + G, b + 2G, ...; round r = item / G holds the
+// keys (r even) or the values (r odd) of groups [(r/2) G, (r/2) G + G), so
+// every CTA alternates keys and values (keys cost more: two RoPE passes).
+// Groups past the last whole pair of rounds alternate m item by item.
 __device__ __forceinline__ void decode_item(const KvxParams &p, const ItemGeom &g, long long item,
                                             int &h, int &chunk, int &lt, int &m) {
-  m = (int)(item & 1);
-  long long r = item >> 1;
-  lt = (int)(r % p.Lt);
-  r /= p.Lt;
-  chunk = (int)(r % g.num_chunks);
-  h = (int)(r / g.num_chunks);
+  const long long G = gridDim.x;
+  const long long full = (g.num_items >> 1) / G * G;   // groups in whole round pairs
+  long long q;
+  if (item < 2 * full) {
+    const long long r = item / G;
+    m = (int)(r & 1);
+    q = (r >> 1) * G + (item - r * G);
+  } else {
+    const long long t = item - 2 * full;
+    m = (int)(t & 1);
+    q = full + (t >> 1);
+  }
+  lt = (int)(q % p.Lt);
+  q /= p.Lt;
+  chunk = (int)(q % g.num_chunks);
+  h = (int)(q / g.num_chunks);
 }
 
 // ---------------------------------------------------------------------------
