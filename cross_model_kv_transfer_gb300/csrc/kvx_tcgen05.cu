@@ -122,19 +122,24 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-// D[tmem] (+)= A[tmem] . B[smem desc]
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] . B[smem desc], issued by one lane elected from the
+// (converged) warp; commit likewise.
+__device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n.reg .pred p;\n"
+      "{\n.reg .pred p, e;\n.reg .b32 r;\n"
+      "elect.sync r|e, 0xffffffff;\n"
       "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n.reg .pred e;\n.reg .b32 r;\n"
+      "elect.sync r|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+          bar)
       : "memory");
 }
 __device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&v)[8]) {
@@ -251,6 +256,12 @@ struct Waiter {
         return false;
       }
     }
+  }
+  // Lane 0 waits, the warp leaves together with lane 0's verdict.
+  __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane) const {
+    bool ok = true;
+    if (lane == 0) ok = wait(bar, parity);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   }
 };
 
@@ -548,57 +559,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------
-    // MMA issuer (one thread)
+    // MMA issuer: the whole warp runs the loop (its descriptors stay
+    // warp-uniform) and one elected lane issues each tcgen05 instruction.
     // ------------------------------------------------------------------
-    if (lane == 0) {
-      uint32_t a_seq = 0, d_seq = 0, w_seq = 0;
-      bool issued = false;
-      for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
-        int h, chunk, lt, m;
-        decode_item(p, geo, item, h, chunk, lt, m);
-        if (!kvx::layer_row_ok(p, lt)) continue;
-        const int t_beg = chunk * geo.tiles_per_item;
-        const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
-        for (int tile = t_beg; tile < t_end; ++tile) {
-          const int buf = d_seq & 1;
-          if (!W.wait(&sh->d_empty[buf], ((d_seq >> 1) & 1) ^ 1)) goto mma_done;
-          tc_fence_after();
-          const uint32_t d_tmem = tmem + (uint32_t)(kDCol + buf * kD);
-          for (int j = 0; j < p.k; ++j) {
-            const int slot = a_seq % kSlots;
-            if (!W.wait(&sh->a_full[slot], (a_seq / kSlots) & 1)) goto mma_done;
-            if (tile == t_beg) {
-              if (!W.wait(&sh->w_full[2 * j], w_seq & 1)) goto mma_done;
-              if (!W.wait(&sh->w_full[2 * j + 1], w_seq & 1)) goto mma_done;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t wchunk = (uint32_t)(2 * j + (kk >> 2));
-              const uint64_t bdesc =
-                  sw128_desc(smem_addr(wbuf + wchunk * kChunkBytes + (kk & 3) * 32));
-              const uint32_t a_tmem = tmem + (uint32_t)(slot * kSlotCols + kk * 8);
-              tc_mma_ts(d_tmem, a_tmem, bdesc, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-            issued = true;
-            tc_commit(smem_addr(&sh->a_empty[slot]));
-            if (tile == t_end - 1) {
-              tc_commit(smem_addr(&sh->w_empty[2 * j]));
-              tc_commit(smem_addr(&sh->w_empty[2 * j + 1]));
-            }
-            ++a_seq;
+    uint32_t a_seq = 0, d_seq = 0, w_seq = 0;
+    bool issued = false;
+    const uint64_t b0 = sw128_desc(smem_addr(wbuf));
+    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+      int h, chunk, lt, m;
+      decode_item(p, geo, item, h, chunk, lt, m);
+      if (!kvx::layer_row_ok(p, lt)) continue;
+      const int t_beg = chunk * geo.tiles_per_item;
+      const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+      for (int tile = t_beg; tile < t_end; ++tile) {
+        const int buf = d_seq & 1;
+        if (!W.warp_wait(&sh->d_empty[buf], ((d_seq >> 1) & 1) ^ 1, lane)) goto mma_done;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(kDCol + buf * kD);
+        for (int j = 0; j < p.k; ++j) {
+          const int slot = a_seq % kSlots;
+          if (!W.warp_wait(&sh->a_full[slot], (a_seq / kSlots) & 1, lane)) goto mma_done;
+          if (tile == t_beg) {
+            if (!W.warp_wait(&sh->w_full[2 * j], w_seq & 1, lane)) goto mma_done;
+            if (!W.warp_wait(&sh->w_full[2 * j + 1], w_seq & 1, lane)) goto mma_done;
           }
-          tc_commit(smem_addr(&sh->d_full[buf]));
-          ++d_seq;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            // W chunk 2j + kk/4, 32-byte K step kk%4 inside its 128-byte rows
+            const uint64_t bdesc =
+                b0 + (uint64_t)((((2 * j + (kk >> 2)) * kChunkBytes) + (kk & 3) * 32) >> 4);
+            const uint32_t a_tmem = tmem + (uint32_t)(slot * kSlotCols + kk * 8);
+            tc_mma_ts_elect(d_tmem, a_tmem, bdesc, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit_elect(smem_addr(&sh->a_empty[slot]));
+          if (tile == t_end - 1) {
+            tc_commit_elect(smem_addr(&sh->w_empty[2 * j]));
+            tc_commit_elect(smem_addr(&sh->w_empty[2 * j + 1]));
+          }
+          ++a_seq;
         }
-        ++w_seq;
+        tc_commit_elect(smem_addr(&sh->d_full[buf]));
+        ++d_seq;
       }
-    mma_done:
-      // drain: every MMA issued so far has completed once `drain` flips
-      if (issued) {
-        tc_commit(smem_addr(&sh->drain));
-        drain_wait(&sh->drain, 0);
-      }
+      ++w_seq;
+    }
+  mma_done:
+    // drain: every MMA issued so far has completed once `drain` flips
+    if (issued) {
+      tc_commit_elect(smem_addr(&sh->drain));
+      if (lane == 0) drain_wait(&sh->drain, 0);
+      __syncwarp();
     }
   } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------------
