@@ -257,11 +257,10 @@ struct Waiter {
       }
     }
   }
-  // Lane 0 waits, the warp leaves together with lane 0's verdict.
-  __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane) const {
-    bool ok = true;
-    if (lane == 0) ok = wait(bar, parity);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  // Every lane waits; the warp leaves together, with false if any lane gave up.
+  __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) const {
+    const bool ok = wait(bar, parity);
+    return __all_sync(0xffffffffu, ok) != 0;
   }
 };
 
@@ -573,15 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
       for (int tile = t_beg; tile < t_end; ++tile) {
         const int buf = d_seq & 1;
-        if (!W.warp_wait(&sh->d_empty[buf], ((d_seq >> 1) & 1) ^ 1, lane)) goto mma_done;
+        if (!W.warp_wait(&sh->d_empty[buf], ((d_seq >> 1) & 1) ^ 1)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(kDCol + buf * kD);
         for (int j = 0; j < p.k; ++j) {
           const int slot = a_seq % kSlots;
-          if (!W.warp_wait(&sh->a_full[slot], (a_seq / kSlots) & 1, lane)) goto mma_done;
+          if (!W.warp_wait(&sh->a_full[slot], (a_seq / kSlots) & 1)) goto mma_done;
           if (tile == t_beg) {
-            if (!W.warp_wait(&sh->w_full[2 * j], w_seq & 1, lane)) goto mma_done;
-            if (!W.warp_wait(&sh->w_full[2 * j + 1], w_seq & 1, lane)) goto mma_done;
+            if (!W.warp_wait(&sh->w_full[2 * j], w_seq & 1)) goto mma_done;
+            if (!W.warp_wait(&sh->w_full[2 * j + 1], w_seq & 1)) goto mma_done;
           }
           tc_fence_after();
 #pragma unroll
