@@ -156,9 +156,11 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
       : "r"(taddr)
       : "memory");
 }
-// 32-byte global store (one full sector); the address must be 32-byte aligned.
+// 32-byte global store (one full sector) that does not allocate in L1: the
+// cache rows are written once and never read back here, and L1 keeps the
+// bias and RoPE lines; the address must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8]) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
+  asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
@@ -425,6 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             plo[4 * q] = lo.x; plo[4 * q + 1] = lo.y; plo[4 * q + 2] = lo.z; plo[4 * q + 3] = lo.w;
             phi[4 * q] = hi.x; phi[4 * q + 1] = hi.y; phi[4 * q + 2] = hi.z; phi[4 * q + 3] = hi.w;
           }
+          // the stage's next contents arrive by TMA (async proxy): order
+          // these generic-proxy reads before it, then release the stage
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           mbar_arrive(smem_addr(&sh->x_empty[stage]));
           ++x_seq;
           const int slot = a_seq % kSlots;
@@ -658,11 +663,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap *map = m == 0 ? &tmap_k : &tmap_v;
         const int t_beg = chunk * geo.tiles_per_item;
         const int t_end = min(t_beg + geo.tiles_per_item, geo.num_tiles);
+        // the item's selected source layers, read once per item
+        int sl_all[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) sl_all[j] = j < p.k ? p.layer_idx[lt * p.k + j] : 0;
         for (int tile = t_beg; tile < t_end; ++tile) {
-          for (int j = 0; j < p.k; ++j) {
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j) {
+            if (j >= p.k) break;
             const int stage = x_seq % geo.stages;
             if (!W.wait(&sh->x_empty[stage], ((x_seq / geo.stages) & 1) ^ 1)) goto loader_done;
-            const int sl = p.layer_idx[lt * p.k + j];
+            const int sl = sl_all[j];
             const uint32_t bar = smem_addr(&sh->x_full[stage]);
             const uint32_t dst = smem_addr(xbuf + stage * kStageBytes);
             mbar_expect_tx(bar, kStageBytes);
