@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tq = warp >> 2;                 // RoPE pair quarter: pairs [16 tq, 16 tq + 16)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    uint32_t a_seq = 0, x_seq = 0;
+    uint32_t a_seq = 0;
+    int x_stage = 0;                          // X ring position, tracked incrementally
+    uint32_t x_par = 0;
     const int sw = row_in_tile & 7;           // 128-byte swizzle phase of this row
     // The tiles of one item; keys (un-rotated out of the source RoPE) and
     // values (copied as stored) are compiled as separate loops.  Returns
@@ -413,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t c2[8], s2[8];
         if constexpr (kKey) load_couples(p, rope_src2, tile, row_in_tile, tq, c2, s2);
         for (int j = 0; j < p.k; ++j) {
-          const int stage = x_seq % geo.stages;
-          if (!W.wait(&sh->x_full[stage], (x_seq / geo.stages) & 1)) return false;
+          const int stage = x_stage;
+          if (!W.wait(&sh->x_full[stage], x_par)) return false;
           // this row's dims [16 tq, 16 tq + 16) (box 0) and [64 + 16 tq, ...)
           // (box 1): logical 16-byte chunks 2 tq, 2 tq + 1 of a 128-byte row
           const unsigned char *rb = xbuf + stage * kStageBytes + row_in_tile * 128;
@@ -431,7 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // these generic-proxy reads before it, then release the stage
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           mbar_arrive(smem_addr(&sh->x_empty[stage]));
-          ++x_seq;
+          if (++x_stage == geo.stages) {
+            x_stage = 0;
+            x_par ^= 1;
+          }
           const int slot = a_seq % kSlots;
           const uint32_t round = a_seq / kSlots;
           if constexpr (kKey) {
