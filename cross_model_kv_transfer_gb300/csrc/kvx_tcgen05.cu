@@ -429,10 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             plo[4 * q] = lo.x; plo[4 * q + 1] = lo.y; plo[4 * q + 2] = lo.z; plo[4 * q + 3] = lo.w;
             phi[4 * q] = hi.x; phi[4 * q + 1] = hi.y; phi[4 * q + 2] = hi.z; phi[4 * q + 3] = hi.w;
           }
-          // the stage's next contents arrive by TMA (async proxy): order
-          // these generic-proxy reads before it, then release the stage
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(smem_addr(&sh->x_empty[stage]));
           if (++x_stage == geo.stages) {
             x_stage = 0;
             x_par ^= 1;
@@ -453,6 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_st8(tmem + lane_base + col + 32, phi);
           }
           tc_wait_st();
+          // release the X stage only now: its words went through registers
+          // into tensor memory (wait::st returned), so every read of the
+          // stage is complete before the loader's next TMA write lands there
+          mbar_arrive(smem_addr(&sh->x_empty[stage]));
           tc_fence_before();
           __syncwarp();
           if (lane == 0 && !stall_test) mbar_arrive(smem_addr(&sh->a_full[slot]));
