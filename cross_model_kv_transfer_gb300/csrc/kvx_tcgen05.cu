@@ -134,6 +134,31 @@ __device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The 8 MMAs of one selection (K = 128): A columns +8 per K step, B
+// descriptor +2 (32 bytes) per step inside a 16 KB chunk, next chunk +1024.
+__device__ __forceinline__ void tc_mma8_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred e, p, t;\n.reg .b32 r, a1, a2, a3, a4, a5, a6, a7;\n"
+      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"
+      "elect.sync r|e, 0xffffffff;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "setp.eq.u32 t, 0, 0;\n"
+      "add.u32 a1, %1, 8; add.u32 a2, %1, 16; add.u32 a3, %1, 24; add.u32 a4, %1, 32;\n"
+      "add.u32 a5, %1, 40; add.u32 a6, %1, 48; add.u32 a7, %1, 56;\n"
+      "add.u64 b1, %2, 2; add.u64 b2, %2, 4; add.u64 b3, %2, 6; add.u64 b4, %2, 1024;\n"
+      "add.u64 b5, %2, 1026; add.u64 b6, %2, 1028; add.u64 b7, %2, 1030;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n.reg .pred e;\n.reg .b32 r;\n"
@@ -593,14 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!W.warp_wait(&sh->w_full[2 * j + 1], w_seq & 1)) goto mma_done;
           }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            // W chunk 2j + kk/4, 32-byte K step kk%4 inside its 128-byte rows
-            const uint64_t bdesc =
-                b0 + (uint64_t)((((2 * j + (kk >> 2)) * kChunkBytes) + (kk & 3) * 32) >> 4);
-            const uint32_t a_tmem = tmem + (uint32_t)(slot * kSlotCols + kk * 8);
-            tc_mma_ts_elect(d_tmem, a_tmem, bdesc, kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
-          }
+          tc_mma8_elect(d_tmem, tmem + (uint32_t)(slot * kSlotCols),
+                        b0 + (uint64_t)((2 * j * kChunkBytes) >> 4), kIdesc, j > 0 ? 1u : 0u);
           issued = true;
           tc_commit_elect(smem_addr(&sh->a_empty[slot]));
           if (tile == t_end - 1) {
