@@ -47,6 +47,8 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (profiling of small cases)")
     ap.add_argument("--tiles-per-item", type=int, default=0)
+    ap.add_argument("--single-cta", action="store_true",
+                    help="tensor-core kernel on single CTAs instead of CTA pairs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -298,7 +300,8 @@ def run_kvx(args):
                     rope_theta_tgt=wl.theta_tgt, max_position=wl.max_position,
                     kv_dtype=wl.kv_dtype, w_dtype=torch.float32, b_dtype=wl.b_dtype,
                     layout=wl.layout, block_size=wl.block_size if wl.layout == PAGED else 0,
-                    kernel=kernel_code(args.kernel), tiles_per_item=args.tiles_per_item)
+                    kernel=kernel_code(args.kernel), tiles_per_item=args.tiles_per_item,
+                    flags=kvx.KVX_PLAN_TC_SINGLE_CTA if args.single_cta else 0)
     kname = {kvx.KVX_KERNEL_SIMT: "simt", kvx.KVX_KERNEL_TCGEN05: "tcgen05"}[plan.kernel]
     shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
     dst_k = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
@@ -359,7 +362,8 @@ def run_kvx(args):
                    "head_dim": wl.head_dim, "k": wl.k, "tokens": wl.ntok,
                    "requests": wl.num_requests,
                    "layout": "paged" if wl.layout == PAGED else "contiguous",
-                   "kernel": kname, "parallelism": f"replicas x{ws}",
+                   "kernel": kname, "cta_group": plan.cta_group,
+                   "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (source "
                          f"{inp['src_k'].numel() * 2 * inp['src_k'].element_size() / 1e9:.2f} GB,"
                          " no flush needed)"},

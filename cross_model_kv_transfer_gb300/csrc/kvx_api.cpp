@@ -35,7 +35,7 @@ kvx_status validate_desc(const kvx_plan_desc *d) {
       d->kernel != KVX_KERNEL_TCGEN05)
     return KVX_ERR_INVALID_ARG;
   if (d->tiles_per_item < 0 || d->tiles_per_item > 4096) return KVX_ERR_INVALID_ARG;
-  if (d->flags & ~KVX_PLAN_TEST_STALL) return KVX_ERR_INVALID_ARG;
+  if (d->flags & ~(KVX_PLAN_TEST_STALL | KVX_PLAN_TC_SINGLE_CTA)) return KVX_ERR_INVALID_ARG;
   // "Requirements": same number of KV heads and the same per-head dimension.
   if (d->src_kv_heads != d->tgt_kv_heads || d->src_head_dim != d->tgt_head_dim)
     return KVX_ERR_PAIR_MISMATCH;
@@ -265,6 +265,12 @@ int32_t kvx_plan_kernel(const kvx_plan *plan) { return plan ? plan->kernel : -1;
 int32_t kvx_plan_launches(const kvx_plan *plan) {
   if (!plan) return -1;
   return plan->kernel == KVX_KERNEL_TCGEN05 ? 2 : 1;  // W image + transfer, or transfer
+}
+
+int32_t kvx_plan_cta_group(const kvx_plan *plan) {
+  if (!plan) return -1;
+  if (plan->kernel != KVX_KERNEL_TCGEN05) return 0;
+  return plan->tc_pairs > 0 ? 2 : 1;
 }
 
 kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *stream) {

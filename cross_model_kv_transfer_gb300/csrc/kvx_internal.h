@@ -30,6 +30,7 @@ struct kvx_plan {
   void *tc_rope_src;
   unsigned long long turns_tgt[128];
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
+  int tc_pairs;          // tensor-core path: CTA pairs resident at once (0: single CTAs)
 };
 
 // Everything a kernel needs, passed by value.
@@ -54,5 +55,5 @@ bool kvx_simt_supports(const kvx_plan_desc &d);
 bool kvx_tc_supports(const kvx_plan_desc &d);
 size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d);
 void *kvx_tc_encoder();
-cudaError_t kvx_tc_prepare(const kvx_plan *plan);
+cudaError_t kvx_tc_prepare(kvx_plan *plan);
 cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);

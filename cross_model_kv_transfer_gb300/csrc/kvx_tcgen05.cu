@@ -56,7 +56,7 @@ constexpr int kDCol = kSlots * kSlotCols;  // first accumulator column (256)
 constexpr int kTmemCols = 512;
 constexpr int kChunkBytes = 16384;    // W chunk: 128 rows x 64 k x bf16
 constexpr int kStageBytes = 2 * kChunkBytes;  // one selection of one tile
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
 constexpr int kTransformWarps = 16;
 constexpr int kEpilogueWarps = 8;
@@ -83,6 +83,25 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the
+// cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
+  asm volatile(
+      "{\n.reg .b32 r;\n"
+      "mapa.shared::cluster.u32 r, %0, %1;\n"
+      "mbarrier.arrive.shared::cluster.b64 _, [r];\n}\n" ::"r"(bar),
+      "r"(rank)
+      : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -122,50 +141,61 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[tmem] . B[smem desc], issued by one lane elected from the
-// (converged) warp; commit likewise.
-__device__ __forceinline__ void tc_mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred p, e;\n.reg .b32 r;\n"
-      "elect.sync r|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // The 8 MMAs of one selection (K = 128): A columns +8 per K step, B
-// descriptor +2 (32 bytes) per step inside a 16 KB chunk, next chunk +1024.
+// descriptor +2 (32 bytes) per step inside a W chunk, then the next chunk
+// (this CTA's 16 KB / P of it).
+// P = 2: the CTA pair runs one M = 256 MMA (each CTA's 128 rows of A from its
+// own tensor memory, each CTA's half of B's N rows from its own shared memory
+// at the same offset, D in both CTAs' tensor memory); only rank 0 issues.
+template <int P>
 __device__ __forceinline__ void tc_mma8_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n.reg .pred e, p, t;\n.reg .b32 r, a1, a2, a3, a4, a5, a6, a7;\n"
-      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"
-      "elect.sync r|e, 0xffffffff;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "setp.eq.u32 t, 0, 0;\n"
-      "add.u32 a1, %1, 8; add.u32 a2, %1, 16; add.u32 a3, %1, 24; add.u32 a4, %1, 32;\n"
-      "add.u32 a5, %1, 40; add.u32 a6, %1, 48; add.u32 a7, %1, 56;\n"
-      "add.u64 b1, %2, 2; add.u64 b2, %2, 4; add.u64 b3, %2, 6; add.u64 b4, %2, 1024;\n"
-      "add.u64 b5, %2, 1026; add.u64 b6, %2, 1028; add.u64 b7, %2, 1030;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, t;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, t;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, t;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, t;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, t;\n"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, t;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+#define KVX_MMA8(G)                                                                            \
+  asm volatile(                                                                                \
+      "{\n.reg .pred e, p, t;\n.reg .b32 r, a1, a2, a3, a4, a5, a6, a7;\n"                     \
+      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n"                                                \
+      "elect.sync r|e, 0xffffffff;\n"                                                          \
+      "setp.ne.b32 p, %4, 0;\n"                                                                \
+      "setp.eq.u32 t, 0, 0;\n"                                                                 \
+      "add.u32 a1, %1, 8; add.u32 a2, %1, 16; add.u32 a3, %1, 24; add.u32 a4, %1, 32;\n"       \
+      "add.u32 a5, %1, 40; add.u32 a6, %1, 48; add.u32 a7, %1, 56;\n"                          \
+      "add.u64 b1, %2, 2; add.u64 b2, %2, 4; add.u64 b3, %2, 6; add.u64 b4, %2, %5;\n"        \
+      "add.u64 b5, b4, 2; add.u64 b6, b4, 4; add.u64 b7, b4, 6;\n"                              \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [%1], %2, %3, p;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a1], b1, %3, t;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a2], b2, %3, t;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a3], b3, %3, t;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a4], b4, %3, t;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a5], b5, %3, t;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a6], b6, %3, t;\n"                     \
+      "@e tcgen05.mma.cta_group::" G ".kind::f16 [%0], [a7], b7, %3, t;\n}\n" ::"r"(d_tmem),   \
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),                                    \
+      "l"((uint64_t)((kChunkBytes / P) >> 4))                                                   \
+      : "memory")
+  if constexpr (P == 1) KVX_MMA8("1");
+  else KVX_MMA8("2");
+#undef KVX_MMA8
 }
-__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
-  asm volatile(
-      "{\n.reg .pred e;\n.reg .b32 r;\n"
-      "elect.sync r|e, 0xffffffff;\n"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
-          bar)
-      : "memory");
+// Commit: the barrier (in every CTA of `mask` for P = 2) receives one arrival
+// once all MMAs issued so far by this thread are complete.
+template <int P>
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar, uint16_t mask = 3) {
+  if constexpr (P == 1) {
+    asm volatile(
+        "{\n.reg .pred e;\n.reg .b32 r;\n"
+        "elect.sync r|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+            bar)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n.reg .pred e;\n.reg .b32 r;\n"
+        "elect.sync r|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;\n}\n" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+  }
 }
 __device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile(
@@ -210,8 +240,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
 // N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kD >> 3) << 17) |
-                            ((uint32_t)(kTileM >> 4) << 24);
+template <int P>
+__host__ __device__ constexpr uint32_t idesc_for() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kD >> 3) << 17) |
+         ((uint32_t)((kTileM * P) >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -260,6 +293,7 @@ struct Shared {
   uint64_t a_full[kSlots], a_empty[kSlots];
   uint64_t d_full[2], d_empty[2];
   uint64_t w_full[2 * kMaxK], w_empty[2 * kMaxK];
+  uint64_t w_peer[2 * kMaxK];   // CTA pair: the peer's W half has landed (rank 0 only)
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort;
@@ -302,22 +336,24 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 struct ItemGeom {
   int num_tiles, num_chunks, tiles_per_item, stages;
   long long num_items;
+  long long stride;   // CTA groups (CTAs, or CTA pairs) running items concurrently
 };
 
-// Source-RoPE couples of row `row_in_tile` of `tile` for pairs
+// Source-RoPE couples of row `row_in_tile` of a tile starting at packed row
+// `row0`, for pairs
 // [16 tq, 16 tq + 16): couple q holds (cos, cos) and (sin, sin) in bf16x2 for
 // pairs 16 tq + 2q and +1 from the position-major table (a warp's 32
 // consecutive rows read contiguous memory).  Rows outside the transfer or
 // with an invalid position get the identity rotation.
 __device__ __forceinline__ void load_couples(const KvxParams &p, const uint2 *__restrict__ rope_src2,
-                                             int tile, int row_in_tile, int tq,
+                                             int64_t row0, int row_in_tile, int tq,
                                              uint32_t (&c2)[8], uint32_t (&s2)[8]) {
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     c2[q] = 0x3F803F80u;   // (1, 1)
     s2[q] = 0u;
   }
-  const int64_t g = (int64_t)tile * kTileM + row_in_tile;
+  const int64_t g = row0 + row_in_tile;
   int32_t ps = 0, pt = 0;
   int64_t row = -1;
   if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
@@ -332,13 +368,13 @@ __device__ __forceinline__ void load_couples(const KvxParams &p, const uint2 *__
 
 // Work items are (h, chunk, lt, m): Q = H * chunks * Lt groups (h, chunk,
 // lt), lt fastest, each with a key item (m = 0) and a value item (m = 1).
-// CTA b of G runs items b, b + G, b + 2G, ...; round r = item / G holds the
+// CTA group b of G runs items b, b + G, b + 2G, ...; round r = item / G holds the
 // keys (r even) or the values (r odd) of groups [(r/2) G, (r/2) G + G), so
 // every CTA alternates keys and values (keys cost more: two RoPE passes).
 // Groups past the last whole pair of rounds alternate m item by item.
 __device__ __forceinline__ void decode_item(const KvxParams &p, const ItemGeom &g, long long item,
                                             int &h, int &chunk, int &lt, int &m) {
-  const long long G = gridDim.x;
+  const long long G = g.stride;
   const long long full = (g.num_items >> 1) / G * G;   // groups in whole round pairs
   long long q;
   if (item < 2 * full) {
@@ -359,6 +395,7 @@ __device__ __forceinline__ void decode_item(const KvxParams &p, const ItemGeom &
 // ---------------------------------------------------------------------------
 // The transfer kernel
 // ---------------------------------------------------------------------------
+template <int P>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_transfer_kernel(const __grid_constant__ KvxParams p,
                        const __grid_constant__ CUtensorMap tmap_k,
@@ -372,12 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // W chunks and X stages need 1024-byte alignment (128-byte swizzle atoms).
   unsigned char *wbuf = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char *xbuf = wbuf + (size_t)2 * p.k * kChunkBytes;
+  constexpr int kWChunk = kChunkBytes / P;   // a CTA holds 128 / P rows n of each W chunk
+  unsigned char *xbuf = wbuf + (size_t)2 * p.k * kWChunk;
   Shared *sh = reinterpret_cast<Shared *>(xbuf + (size_t)geo.stages * kStageBytes);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int nchunks_w = 2 * p.k;
+  // CTA pair: rank 0 issues the MMAs and owns the barriers the pair shares
+  const uint32_t rank = P == 2 ? cluster_rank() : 0u;
+  const long long group = blockIdx.x / P;
+  const int tile_rows = kTileM * P;          // packed rows per tile of the group
 
   if (tid == 0) {
     for (int s = 0; s < geo.stages; ++s) {
@@ -385,32 +427,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&sh->x_empty[s]), kTransformWarps * 32);
     }
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(smem_addr(&sh->a_full[s]), kTransformWarps);
+      mbar_init(smem_addr(&sh->a_full[s]), kTransformWarps * P);
       mbar_init(smem_addr(&sh->a_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&sh->d_full[b]), 1);
-      mbar_init(smem_addr(&sh->d_empty[b]), kEpilogueWarps);
+      mbar_init(smem_addr(&sh->d_empty[b]), kEpilogueWarps * P);
     }
     for (int c = 0; c < nchunks_w; ++c) {
       mbar_init(smem_addr(&sh->w_full[c]), 1);
       mbar_init(smem_addr(&sh->w_empty[c]), 1);
+      mbar_init(smem_addr(&sh->w_peer[c]), 1);
     }
     mbar_init(smem_addr(&sh->drain), 1);
     sh->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(&sh->tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    // CTA pair: one warp in each CTA allocates collectively (same columns)
+    if constexpr (P == 1) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_addr(&sh->tmem_base)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_addr(&sh->tmem_base)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   // The request table is validated by every CTA; a malformed one stops the
   // whole transfer before any write.
   const bool seq_ok = kvx::seqlens_ok(p, tid, kThreads);
+  // CTA pair: the peer's barriers are initialised before any remote arrival
+  if constexpr (P == 2) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
   const Waiter W{sh, p.status, stall_test ? kStallTestWaitNs : kWaitNs};
@@ -438,7 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bf16x2 cos/sin couples of the source RoPE at this row's position
         // for the thread's 16 pairs (couple q = pairs 16 tq + 2q, +1)
         uint32_t c2[8], s2[8];
-        if constexpr (kKey) load_couples(p, rope_src2, tile, row_in_tile, tq, c2, s2);
+        if constexpr (kKey)
+          load_couples(p, rope_src2, (int64_t)tile * tile_rows + rank * kTileM, row_in_tile, tq,
+                       c2, s2);
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_stage;
           if (!W.wait(&sh->x_full[stage], x_par)) return false;
@@ -480,13 +536,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(smem_addr(&sh->x_empty[stage]));
           tc_fence_before();
           __syncwarp();
-          if (lane == 0 && !stall_test) mbar_arrive(smem_addr(&sh->a_full[slot]));
+          if (lane == 0 && !stall_test) {
+            if (P == 1 || rank == 0) mbar_arrive(smem_addr(&sh->a_full[slot]));
+            else mbar_arrive_cluster(smem_addr(&sh->a_full[slot]), 0);
+          }
           ++a_seq;
         }
       }
       return true;
     };
-    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+    for (long long item = group; item < geo.num_items; item += geo.stride) {
       int h, chunk, lt, m;
       decode_item(p, geo, item, h, chunk, lt, m);
       if (!kvx::layer_row_ok(p, lt)) continue;
@@ -515,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bias_f32 + (((int64_t)lt * p.H + h) * 2 + (kKey ? 0 : 1)) * kD);
       __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(kKey ? p.dst_k : p.dst_v);
       for (int tile = t_beg; tile < t_end; ++tile) {
-        const int64_t g = (int64_t)tile * kTileM + row_in_tile;
+        const int64_t g = (int64_t)tile * tile_rows + rank * kTileM + row_in_tile;
         int32_t ps = 0, pt = 0;
         int64_t row = -1;
         uint32_t bad = 0;
@@ -573,12 +632,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
+        if (lane == 0) {
+          if (P == 1 || rank == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
+          else mbar_arrive_cluster(smem_addr(&sh->d_empty[buf]), 0);
+        }
         ++d_seq;
       }
       return true;
     };
-    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+    for (long long item = group; item < geo.num_items; item += geo.stride) {
       int h, chunk, lt, m;
       decode_item(p, geo, item, h, chunk, lt, m);
       const bool layer_ok = kvx::layer_row_ok(p, lt);
@@ -599,7 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t a_seq = 0, d_seq = 0, w_seq = 0;
     bool issued = false;
     const uint64_t b0 = sw128_desc(smem_addr(wbuf));
-    for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+    constexpr uint32_t kIdesc = idesc_for<P>();
+    const long long first_item = (P == 1 || rank == 0) ? group : geo.num_items;   // the peer issues nothing
+    for (long long item = first_item; item < geo.num_items; item += geo.stride) {
       int h, chunk, lt, m;
       decode_item(p, geo, item, h, chunk, lt, m);
       if (!kvx::layer_row_ok(p, lt)) continue;
@@ -616,19 +680,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tile == t_beg) {
             if (!W.warp_wait(&sh->w_full[2 * j], w_seq & 1)) goto mma_done;
             if (!W.warp_wait(&sh->w_full[2 * j + 1], w_seq & 1)) goto mma_done;
+            if constexpr (P == 2) {   // the peer's halves of the same chunks
+              if (!W.warp_wait(&sh->w_peer[2 * j], w_seq & 1)) goto mma_done;
+              if (!W.warp_wait(&sh->w_peer[2 * j + 1], w_seq & 1)) goto mma_done;
+            }
           }
           tc_fence_after();
-          tc_mma8_elect(d_tmem, tmem + (uint32_t)(slot * kSlotCols),
-                        b0 + (uint64_t)((2 * j * kChunkBytes) >> 4), kIdesc, j > 0 ? 1u : 0u);
+          tc_mma8_elect<P>(d_tmem, tmem + (uint32_t)(slot * kSlotCols),
+                           b0 + (uint64_t)((2 * j * kWChunk) >> 4), kIdesc, j > 0 ? 1u : 0u);
           issued = true;
-          tc_commit_elect(smem_addr(&sh->a_empty[slot]));
+          tc_commit_elect<P>(smem_addr(&sh->a_empty[slot]));
           if (tile == t_end - 1) {
-            tc_commit_elect(smem_addr(&sh->w_empty[2 * j]));
-            tc_commit_elect(smem_addr(&sh->w_empty[2 * j + 1]));
+            tc_commit_elect<P>(smem_addr(&sh->w_empty[2 * j]));
+            tc_commit_elect<P>(smem_addr(&sh->w_empty[2 * j + 1]));
           }
           ++a_seq;
         }
-        tc_commit_elect(smem_addr(&sh->d_full[buf]));
+        tc_commit_elect<P>(smem_addr(&sh->d_full[buf]));
         ++d_seq;
       }
       ++w_seq;
@@ -636,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   mma_done:
     // drain: every MMA issued so far has completed once `drain` flips
     if (issued) {
-      tc_commit_elect(smem_addr(&sh->drain));
+      tc_commit_elect<P>(smem_addr(&sh->drain), (uint16_t)1);
       if (lane == 0) drain_wait(&sh->drain, 0);
       __syncwarp();
     }
@@ -649,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // [n_last, nchunks_w) in round w_seq - 1 (rounds count from 1)
       uint32_t w_seq = 0;
       int n_last = nchunks_w;
-      for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+      for (long long item = group; item < geo.num_items; item += geo.stride) {
         int h, chunk, lt, m;
         decode_item(p, geo, item, h, chunk, lt, m);
         if (!kvx::layer_row_ok(p, lt)) continue;
@@ -660,9 +728,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = n_last;
           if (!W.wait(&sh->w_empty[c], (w_seq & 1) ^ 0)) goto producer_done;
           const uint32_t bar = smem_addr(&sh->w_full[c]);
-          mbar_expect_tx(bar, kChunkBytes);
-          bulk_g2s(smem_addr(wbuf + c * kChunkBytes), img + (int64_t)c * kChunkBytes, kChunkBytes,
-                   bar);
+          mbar_expect_tx(bar, kWChunk);
+          // rows n of the chunk in [rank * 128 / P, ...): bytes [rank * kWChunk, +kWChunk)
+          bulk_g2s(smem_addr(wbuf + c * kWChunk),
+                   img + (int64_t)c * kChunkBytes + (int64_t)rank * kWChunk, kWChunk, bar);
+        }
+        if (P == 2 && rank != 0) {
+          // tell rank 0 (which issues the MMAs) that this CTA's halves landed
+          for (int c = 0; c < nchunks_w; ++c) {
+            if (!W.wait(&sh->w_full[c], (w_seq - 1) & 1)) goto producer_done;
+            mbar_arrive_cluster(smem_addr(&sh->w_peer[c]), 0);
+          }
         }
       }
     producer_done:
@@ -680,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------
     if (lane == 0) {
       uint32_t x_seq = 0;
-      for (long long item = blockIdx.x; item < geo.num_items; item += gridDim.x) {
+      for (long long item = group; item < geo.num_items; item += geo.stride) {
         int h, chunk, lt, m;
         decode_item(p, geo, item, h, chunk, lt, m);
         if (!kvx::layer_row_ok(p, lt)) continue;
@@ -701,8 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t bar = smem_addr(&sh->x_full[stage]);
             const uint32_t dst = smem_addr(xbuf + stage * kStageBytes);
             mbar_expect_tx(bar, kStageBytes);
-            tma_load_4d(dst, map, 0, h, tile * kTileM, sl, bar);
-            tma_load_4d(dst + kChunkBytes, map, kHalf, h, tile * kTileM, sl, bar);
+            const int r0 = tile * tile_rows + (int)rank * kTileM;
+            tma_load_4d(dst, map, 0, h, r0, sl, bar);
+            tma_load_4d(dst + kChunkBytes, map, kHalf, h, r0, sl, bar);
             ++x_seq;
           }
         }
@@ -715,12 +792,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // CTA pair: neither CTA leaves while the other may still arrive on its
+  // barriers or (rank 0's MMAs, drained above) use its memory
+  if constexpr (P == 2) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+    if constexpr (P == 1)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
   }
 }
 
@@ -759,13 +844,14 @@ __global__ void __launch_bounds__(256) w_image_kernel(const WT *__restrict__ w,
   }
 }
 
-size_t smem_bytes(int k, int stages) {
-  return 1024 + (size_t)2 * k * kChunkBytes + (size_t)stages * kStageBytes + sizeof(Shared) + 64;
+size_t smem_bytes(int k, int stages, int pair) {
+  return 1024 + (size_t)2 * k * (kChunkBytes / pair) + (size_t)stages * kStageBytes +
+         sizeof(Shared) + 64;
 }
 
-int max_stages(int k) {
+int max_stages(int k, int pair) {
   int s = kMaxStages;
-  while (s > 1 && smem_bytes(k, s) > (size_t)kSmemLimit) --s;
+  while (s > 1 && smem_bytes(k, s, pair) > (size_t)kSmemLimit) --s;
   return s;
 }
 
@@ -813,11 +899,37 @@ void *kvx_tc_encoder() {
   return fn;
 }
 
-cudaError_t kvx_tc_prepare(const kvx_plan *plan) {
+cudaError_t kvx_tc_prepare(kvx_plan *plan) {
   if (!plan->encode_tiled) return cudaErrorNotSupported;
   const int k = plan->desc.k;
-  return cudaFuncSetAttribute(tc_transfer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes(k, max_stages(k)));
+  cudaError_t e = cudaFuncSetAttribute(tc_transfer_kernel<1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes(k, max_stages(k, 1), 1));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_transfer_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes(k, max_stages(k, 2), 2));
+  if (e != cudaSuccess) return e;
+  // CTA pairs that can be resident at once (0: run single CTAs)
+  plan->tc_pairs = 0;
+  if (!(plan->desc.flags & KVX_PLAN_TC_SINGLE_CTA)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * plan->num_sms, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes(k, max_stages(k, 2), 2);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_transfer_kernel<2>, &cfg) == cudaSuccess)
+      plan->tc_pairs = n;
+    else
+      cudaGetLastError();
+  }
+  return cudaSuccess;
 }
 
 cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s) {
@@ -839,21 +951,42 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
     w_image_kernel<bf, bf><<<wgrid, 256, 0, s>>>((const bf *)p.w, img, (const bf *)p.b, bimg);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // 2. the persistent transfer kernel
+  // 2. the persistent transfer kernel: CTA pairs (one M = 256 MMA per K step
+  // over both CTAs' rows) when the device can co-schedule them, else single CTAs
+  const int P = plan->tc_pairs > 0 ? 2 : 1;
   ItemGeom geo;
-  geo.num_tiles = (int)((p.ntok + kTileM - 1) / kTileM);
+  geo.num_tiles = (int)((p.ntok + kTileM * P - 1) / (kTileM * P));
   geo.tiles_per_item = plan->tiles_per_item;
   geo.num_chunks = (geo.num_tiles + geo.tiles_per_item - 1) / geo.tiles_per_item;
   geo.num_items = (long long)p.H * geo.num_chunks * p.Lt * 2;
-  geo.stages = max_stages(p.k);
+  geo.stages = max_stages(p.k, P);
+  const long long slots = P == 2 ? plan->tc_pairs : plan->num_sms;
+  geo.stride = geo.num_items < slots ? geo.num_items : slots;
   CUtensorMap mk, mv;
   if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p))
     return cudaErrorInvalidValue;
-  const int grid = (int)(geo.num_items < plan->num_sms ? geo.num_items : plan->num_sms);
   RopeTurns rope;
   for (int i = 0; i < kHalf; ++i) rope.tgt[i] = plan->turns_tgt[i];
-  tc_transfer_kernel<<<grid, kThreads, smem_bytes(p.k, geo.stages), s>>>(
-      p, mk, mv, reinterpret_cast<const uint2 *>(plan->tc_rope_src), rope, bimg,
-      reinterpret_cast<const __nv_bfloat16 *>(plan->workspace), geo, plan->stall_test);
-  return cudaGetLastError();
+  const uint2 *rope_src2 = reinterpret_cast<const uint2 *>(plan->tc_rope_src);
+  const __nv_bfloat16 *wimg = reinterpret_cast<const __nv_bfloat16 *>(plan->workspace);
+  const size_t smem = smem_bytes(p.k, geo.stages, P);
+  if (P == 1) {
+    tc_transfer_kernel<1><<<(unsigned)geo.stride, kThreads, smem, s>>>(
+        p, mk, mv, rope_src2, rope, bimg, wimg, geo, plan->stall_test);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * geo.stride), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_transfer_kernel<2>, p, mk, mv, rope_src2, rope, bimg, wimg,
+                            geo, plan->stall_test);
 }

@@ -7,7 +7,7 @@ be loaded (or built with nvcc on first use), importing the symbols raises.
 
 Low level (same names as the C ABI): ``kvx_plan_create``, ``kvx_transfer``,
 ``kvx_plan_destroy``, ``kvx_status_string``, ``kvx_plan_kernel``,
-``kvx_plan_launches``, ``kvx_transfer_static`` taking the ctypes structures
+``kvx_plan_launches``, ``kvx_plan_cta_group``, ``kvx_transfer_static`` taking the ctypes structures
 ``PlanDesc`` / ``TransferArgs``.
 
 Convenience: ``Plan`` (owns a plan handle) and ``Plan.transfer(...)`` which
@@ -46,10 +46,11 @@ KVX_KERNEL_AUTO = 0
 KVX_KERNEL_SIMT = 1
 KVX_KERNEL_TCGEN05 = 2
 KVX_PLAN_TEST_STALL = 1
+KVX_PLAN_TC_SINGLE_CTA = 2
 
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
             "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches",
-            "kvx_transfer_static")
+            "kvx_plan_cta_group", "kvx_transfer_static")
 
 
 class PlanDesc(ctypes.Structure):
@@ -112,6 +113,8 @@ def load():
             lib.kvx_plan_kernel.restype = ctypes.c_int32
             lib.kvx_plan_launches.argtypes = [ctypes.c_void_p]
             lib.kvx_plan_launches.restype = ctypes.c_int32
+            lib.kvx_plan_cta_group.argtypes = [ctypes.c_void_p]
+            lib.kvx_plan_cta_group.restype = ctypes.c_int32
             lib.kvx_transfer_static.argtypes = [ctypes.POINTER(PlanDesc),
                                                 ctypes.POINTER(TransferArgs), ctypes.c_void_p]
             lib.kvx_transfer_static.restype = ctypes.c_int
@@ -144,6 +147,10 @@ def kvx_plan_kernel(plan) -> int:
 
 def kvx_plan_launches(plan) -> int:
     return load().kvx_plan_launches(plan)
+
+
+def kvx_plan_cta_group(plan) -> int:
+    return load().kvx_plan_cta_group(plan)
 
 
 def kvx_transfer_static(desc: PlanDesc, args: TransferArgs, stream) -> int:
@@ -191,6 +198,10 @@ class Plan:
     @property
     def kernel(self) -> int:
         return kvx_plan_kernel(self.handle)
+
+    @property
+    def cta_group(self) -> int:
+        return kvx_plan_cta_group(self.handle)
 
     @property
     def launches_per_transfer(self) -> int:

@@ -126,6 +126,11 @@ typedef struct {
  * or hangs; the kernel drains and exits.  Never set in production. */
 #define KVX_PLAN_TEST_STALL 1
 
+/* kvx_plan_desc.flags bit: run the tensor-core kernel on single CTAs even
+ * where the device can co-schedule CTA pairs (by default a pair shares each
+ * M = 256 MMA, every CTA holding half of W).  For testing both forms. */
+#define KVX_PLAN_TC_SINGLE_CTA 2
+
 typedef struct kvx_plan kvx_plan; /* opaque */
 
 /* Arguments of one transfer.  All pointers are DEVICE pointers to memory of
@@ -202,6 +207,12 @@ int32_t kvx_plan_kernel(const kvx_plan *plan);
 /* Number of kernel launches one kvx_transfer call enqueues with this plan
  * (0 when ntok == 0), or -1 for a NULL plan. */
 int32_t kvx_plan_launches(const kvx_plan *plan);
+
+/* CTAs that share each MMA in the plan's tensor-core kernel: 2 when the
+ * device co-schedules CTA pairs (one M = 256 MMA per K step, each CTA holding
+ * half of W), 1 for single CTAs (or KVX_PLAN_TC_SINGLE_CTA), 0 for a SIMT
+ * plan, -1 for a NULL plan. */
+int32_t kvx_plan_cta_group(const kvx_plan *plan);
 
 /* Allocation-free transfer.  The sources have no counterpart for this call:
  * it exists for callers that may not allocate device memory -- engines that

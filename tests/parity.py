@@ -16,6 +16,15 @@ from cross_model_kv_transfer_gb300.workloads import PAGED, Workload, make_inputs
 TOL = {torch.float32: 1e-5, torch.bfloat16: 1e-2}
 
 
+# Kernel choices of the tests: a kvx.KVX_KERNEL_* code, or TC_SINGLE for the
+# tensor-core kernel on single CTAs (the default runs it on CTA pairs).
+TC_SINGLE = "tcgen05_single_cta"
+
+
+def kernel_code(kernel) -> int:
+    return kvx.KVX_KERNEL_TCGEN05 if kernel == TC_SINGLE else kernel
+
+
 def make_plan(wl: Workload, kernel=kvx.KVX_KERNEL_AUTO, max_position=None):
     return kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers, kv_heads=wl.kv_heads,
                     head_dim=wl.head_dim, k=wl.k, rope_theta_src=wl.theta_src,
@@ -23,7 +32,8 @@ def make_plan(wl: Workload, kernel=kvx.KVX_KERNEL_AUTO, max_position=None):
                     max_position=wl.max_position if max_position is None else max_position,
                     kv_dtype=wl.kv_dtype, w_dtype=torch.float32, b_dtype=wl.b_dtype,
                     layout=wl.layout, block_size=wl.block_size if wl.layout == PAGED else 0,
-                    kernel=kernel)
+                    kernel=kernel_code(kernel),
+                    flags=kvx.KVX_PLAN_TC_SINGLE_CTA if kernel == TC_SINGLE else 0)
 
 
 def gpu_args(wl: Workload, inp: dict, dst_k, dst_v, status, **over):

@@ -15,12 +15,14 @@ import oracle
 from cross_model_kv_transfer_gb300 import kvx
 from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
 
-from parity import TOL, assert_parity, gpu_args, make_plan, run_gpu, run_oracle
+from parity import (TC_SINGLE, TOL, assert_parity, gpu_args, kernel_code, make_plan, run_gpu,
+                    run_oracle)
 
 pytestmark = pytest.mark.gpu
 
 BF16_KERNELS = [pytest.param(kvx.KVX_KERNEL_SIMT, id="simt"),
-                pytest.param(kvx.KVX_KERNEL_TCGEN05, id="tcgen05")]
+                pytest.param(kvx.KVX_KERNEL_TCGEN05, id="tcgen05"),
+                pytest.param(TC_SINGLE, id="tcgen05_single_cta")]
 
 
 def test_tiny_fp32_workload_matches_oracle():
@@ -38,7 +40,11 @@ def test_qwen3_0p6b_1p7b_512_tokens_matches_oracle(kernel):
     wl = WORKLOADS["qwen3_0p6b_1p7b"]
     inp = make_inputs(wl, "cuda")
     gk, gv, st, plan = run_gpu(wl, inp, kernel)
-    assert st == 0 and plan.kernel == kernel
+    assert st == 0 and plan.kernel == kernel_code(kernel)
+    if kernel == TC_SINGLE:
+        assert plan.cta_group == 1
+    elif kernel == kvx.KVX_KERNEL_TCGEN05:
+        assert plan.cta_group in (1, 2)
     rk, rv, _ = run_oracle(wl, inp)
     assert_parity(wl, gk, gv, rk, rv)
 
@@ -215,8 +221,10 @@ def test_host_rejects_missing_pointers_before_launch():
     assert bool((dk == 0).all())
 
 
+@pytest.mark.parametrize("flags", [pytest.param(0, id="pairs"),
+                                   pytest.param(kvx.KVX_PLAN_TC_SINGLE_CTA, id="single_cta")])
 @pytest.mark.parametrize("k,tiles_per_item", [(1, 1), (3, 2), (5, 3), (6, 8)])
-def test_tcgen05_selection_counts_and_item_sizes(k, tiles_per_item):
+def test_tcgen05_selection_counts_and_item_sizes(k, tiles_per_item, flags):
     # other k (ring wrap-around of the four operand slots, 2k W chunks) and
     # other work-item sizes (W reloaded every 1, 2, 3 or 8 tiles)
     base = WORKLOADS["qwen3_0p6b_1p7b_off37_2k"].with_tokens([700], [37])
@@ -226,14 +234,16 @@ def test_tcgen05_selection_counts_and_item_sizes(k, tiles_per_item):
                     head_dim=wl.head_dim, k=k, rope_theta_src=wl.theta_src,
                     rope_theta_tgt=5e5, max_position=wl.max_position, kv_dtype=wl.kv_dtype,
                     w_dtype=torch.float32, b_dtype=wl.b_dtype,
-                    kernel=kvx.KVX_KERNEL_TCGEN05, tiles_per_item=tiles_per_item)
+                    kernel=kvx.KVX_KERNEL_TCGEN05, tiles_per_item=tiles_per_item, flags=flags)
     gk, gv, st, _ = run_gpu(wl, inp, plan=plan)
     assert st == 0
     rk, rv, _ = run_oracle(wl, inp, theta_tgt=5e5)
     assert_parity(wl, gk, gv, rk, rv)
 
 
-def test_tcgen05_pipeline_wait_gives_up_and_reports_timeout():
+@pytest.mark.parametrize("flags", [pytest.param(0, id="pairs"),
+                                   pytest.param(kvx.KVX_PLAN_TC_SINGLE_CTA, id="single_cta")])
+def test_tcgen05_pipeline_wait_gives_up_and_reports_timeout(flags):
     # Failure detection without a GPU fault: the operand-filling warps never
     # signal, every pipeline wait gives up after its limit, the kernel drains,
     # frees tensor memory and reports KVX_FLAG_TIMEOUT; the context stays
@@ -246,7 +256,7 @@ def test_tcgen05_pipeline_wait_gives_up_and_reports_timeout():
                        rope_theta_src=wl.theta_src, rope_theta_tgt=wl.theta_tgt,
                        max_position=wl.max_position, kv_dtype=wl.kv_dtype,
                        w_dtype=torch.float32, b_dtype=wl.b_dtype,
-                       kernel=kvx.KVX_KERNEL_TCGEN05, flags=kvx.KVX_PLAN_TEST_STALL)
+                       kernel=kvx.KVX_KERNEL_TCGEN05, flags=kvx.KVX_PLAN_TEST_STALL | flags)
     _, _, st, _ = run_gpu(wl, inp, plan=stalled)
     assert st & kvx.KVX_FLAG_TIMEOUT
     gk, gv, st, _ = run_gpu(wl, inp, kvx.KVX_KERNEL_TCGEN05)
