@@ -70,19 +70,25 @@ uint16_t bf16_bits(double x) {
   return (uint16_t)(u >> 16);
 }
 
-// Tensor-core path source table: per couple of pairs (i, i+1) and position
-// p, bf16x2 (cos_i, cos_i+1), (sin_i, sin_i+1).
+// Tensor-core path source table, position-major per quad of pairs
+// (4u .. 4u + 3): element [u][p] is 16 bytes, bf16x2 (cos_4u, cos_4u+1),
+// (sin_4u, sin_4u+1), (cos_4u+2, cos_4u+3), (sin_4u+2, sin_4u+3) of p * w_i,
+// so one tile's 128 consecutive positions of all quads are a 2-D TMA box.
 void tc_rope_table(double theta, int d, int max_position, std::vector<uint32_t> &src) {
-  const int couples = d / 4;
-  src.assign((size_t)couples * max_position * 2, 0);
-  for (int q = 0; q < couples; ++q) {
-    const double w0 = std::pow(theta, -2.0 * (2 * q) / d);
-    const double w1 = std::pow(theta, -2.0 * (2 * q + 1) / d);
+  const int quads = d / 8;
+  src.assign((size_t)quads * max_position * 4, 0);
+  for (int u = 0; u < quads; ++u) {
+    double w[4];
+    for (int e = 0; e < 4; ++e) w[e] = std::pow(theta, -2.0 * (4 * u + e) / d);
     for (int p = 0; p < max_position; ++p) {
-      const size_t o = (size_t)q * max_position + p;
-      const double a0 = p * w0, a1 = p * w1;
-      src[2 * o] = (uint32_t)bf16_bits(std::cos(a0)) | ((uint32_t)bf16_bits(std::cos(a1)) << 16);
-      src[2 * o + 1] = (uint32_t)bf16_bits(std::sin(a0)) | ((uint32_t)bf16_bits(std::sin(a1)) << 16);
+      const size_t o = ((size_t)u * max_position + p) * 4;
+      for (int h = 0; h < 2; ++h) {
+        const double a0 = p * w[2 * h], a1 = p * w[2 * h + 1];
+        src[o + 2 * h] =
+            (uint32_t)bf16_bits(std::cos(a0)) | ((uint32_t)bf16_bits(std::cos(a1)) << 16);
+        src[o + 2 * h + 1] =
+            (uint32_t)bf16_bits(std::sin(a0)) | ((uint32_t)bf16_bits(std::sin(a1)) << 16);
+      }
     }
   }
 }

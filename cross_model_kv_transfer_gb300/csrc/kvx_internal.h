@@ -23,10 +23,10 @@ struct kvx_plan {
   size_t workspace_bytes;
   int tiles_per_item;    // 128-token tiles per work item of the persistent kernel
   void *encode_tiled;    // driver entry point cuTensorMapEncodeTiled
-  // tensor-core path: source RoPE table, position-major per couple of pairs
-  // (i, i+1), i even: tc_rope_src[i/2][p] = bf16x2 (cos_i, cos_i+1),
-  // (sin_i, sin_i+1); target RoPE frequencies as 64-bit fractions of a turn,
-  // round(w_i / 2pi * 2^64)
+  // tensor-core path: source RoPE table, position-major per quad of pairs
+  // (i .. i+3), i % 4 == 0: tc_rope_src[i/4][p] = bf16x2 (cos_i, cos_i+1),
+  // (sin_i, sin_i+1), (cos_i+2, cos_i+3), (sin_i+2, sin_i+3); target RoPE
+  // frequencies as 64-bit fractions of a turn, round(w_i / 2pi * 2^64)
   void *tc_rope_src;
   unsigned long long turns_tgt[128];
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook

@@ -58,6 +58,7 @@ constexpr int kChunkBytes = 16384;    // W chunk: 128 rows x 64 k x bf16
 constexpr int kStageBytes = 2 * kChunkBytes;  // one selection of one tile
 constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
+constexpr int kCplBytes = 16 * kTileM * 16;   // one tile's source-RoPE quads: [16][128 rows][16 B]
 constexpr int kTransformWarps = 16;
 constexpr int kEpilogueWarps = 8;
 constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 24
@@ -133,6 +134,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+// TMA tile load of a 2-D box into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -295,7 +305,9 @@ struct Shared {
   uint64_t w_full[2 * kMaxK], w_empty[2 * kMaxK];
   uint64_t w_peer[2 * kMaxK];   // CTA pair: the peer's W half has landed (rank 0 only)
   uint64_t drain;
+  uint64_t c_full, c_empty;   // CTA pairs: one K tile's source-RoPE quads in shared memory
   uint32_t tmem_base;
+  volatile int c_mode;        // 1: the quads of positions p0 .. p0 + 127 are staged; 2: use global
   volatile int abort;
 };
 
@@ -340,12 +352,11 @@ struct ItemGeom {
 };
 
 // Source-RoPE couples of row `row_in_tile` of a tile starting at packed row
-// `row0`, for pairs
-// [16 tq, 16 tq + 16): couple q holds (cos, cos) and (sin, sin) in bf16x2 for
-// pairs 16 tq + 2q and +1 from the position-major table (a warp's 32
-// consecutive rows read contiguous memory).  Rows outside the transfer or
-// with an invalid position get the identity rotation.
-__device__ __forceinline__ void load_couples(const KvxParams &p, const uint2 *__restrict__ rope_src2,
+// `row0`, for pairs [16 tq, 16 tq + 16): couple q holds (cos, cos) and (sin,
+// sin) in bf16x2 for pairs 16 tq + 2q and +1, read from the position-major
+// quad table (a warp's 32 consecutive rows read contiguous memory).  Rows
+// outside the transfer or with an invalid position get the identity rotation.
+__device__ __forceinline__ void load_couples(const KvxParams &p, const uint4 *__restrict__ rope_src4,
                                              int64_t row0, int row_in_tile, int tq,
                                              uint32_t (&c2)[8], uint32_t (&s2)[8]) {
 #pragma unroll
@@ -359,10 +370,12 @@ __device__ __forceinline__ void load_couples(const KvxParams &p, const uint2 *__
   if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
   if (row < 0) return;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint2 v = __ldg(rope_src2 + (int64_t)(8 * tq + q) * p.max_position + ps);
-    c2[q] = v.x;
-    s2[q] = v.y;
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = __ldg(rope_src4 + (int64_t)(4 * tq + i) * p.max_position + ps);
+    c2[2 * i] = v.x;
+    s2[2 * i] = v.y;
+    c2[2 * i + 1] = v.z;
+    s2[2 * i + 1] = v.w;
   }
 }
 
@@ -400,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_transfer_kernel(const __grid_constant__ KvxParams p,
                        const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v,
-                       const uint2 *__restrict__ rope_src2,
+                       const __grid_constant__ CUtensorMap tmap_cpl,
+                       const uint4 *__restrict__ rope_src4,
                        const __grid_constant__ RopeTurns rope,
                        const float *__restrict__ bias_f32,
                        const __nv_bfloat16 *__restrict__ w_img, const ItemGeom geo,
@@ -411,7 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kWChunk = kChunkBytes / P;   // a CTA holds 128 / P rows n of each W chunk
   unsigned char *xbuf = wbuf + (size_t)2 * p.k * kWChunk;
-  Shared *sh = reinterpret_cast<Shared *>(xbuf + (size_t)geo.stages * kStageBytes);
+  // CTA pairs have room to stage each K tile's source-RoPE quads by TMA
+  constexpr bool kStageCpl = P == 2;
+  unsigned char *cbuf = xbuf + (size_t)geo.stages * kStageBytes;
+  Shared *sh = reinterpret_cast<Shared *>(cbuf + (kStageCpl ? kCplBytes : 0));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -440,6 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&sh->w_peer[c]), 1);
     }
     mbar_init(smem_addr(&sh->drain), 1);
+    mbar_init(smem_addr(&sh->c_full), 1);
+    mbar_init(smem_addr(&sh->c_empty), kTransformWarps * 32);
     sh->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -482,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t a_seq = 0;
     int x_stage = 0;                          // X ring position, tracked incrementally
     uint32_t x_par = 0;
+    uint32_t c_par = 0;                       // staged-quads phase (K tiles, CTA pairs)
     const int sw = row_in_tile & 7;           // 128-byte swizzle phase of this row
     // The tiles of one item; keys (un-rotated out of the source RoPE) and
     // values (copied as stored) are compiled as separate loops.  Returns
@@ -492,9 +512,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bf16x2 cos/sin couples of the source RoPE at this row's position
         // for the thread's 16 pairs (couple q = pairs 16 tq + 2q, +1)
         uint32_t c2[8], s2[8];
-        if constexpr (kKey)
-          load_couples(p, rope_src2, (int64_t)tile * tile_rows + rank * kTileM, row_in_tile, tq,
-                       c2, s2);
+        if constexpr (kKey) {
+          bool from_global = true;
+          if constexpr (kStageCpl) {
+            // the loader staged this tile's quads (positions p0 + row) or
+            // left them to be read from the global table
+            if (!W.wait(&sh->c_full, c_par)) return false;
+            c_par ^= 1;
+            if (sh->c_mode == 1) {
+              from_global = false;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(
+                    cbuf + (4 * tq + i) * (kTileM * 16) + row_in_tile * 16);
+                c2[2 * i] = v.x;
+                s2[2 * i] = v.y;
+                c2[2 * i + 1] = v.z;
+                s2[2 * i + 1] = v.w;
+              }
+            }
+          }
+          if (from_global)
+            load_couples(p, rope_src4, (int64_t)tile * tile_rows + rank * kTileM, row_in_tile, tq,
+                         c2, s2);
+        }
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_stage;
           if (!W.wait(&sh->x_full[stage], x_par)) return false;
@@ -534,6 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // into tensor memory (wait::st returned), so every read of the
           // stage is complete before the loader's next TMA write lands there
           mbar_arrive(smem_addr(&sh->x_empty[stage]));
+          // likewise the staged quads, consumed by the first selection
+          if (kKey && kStageCpl && j == 0) mbar_arrive(smem_addr(&sh->c_empty));
           tc_fence_before();
           __syncwarp();
           if (lane == 0 && !stall_test) {
@@ -756,6 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------
     if (lane == 0) {
       uint32_t x_seq = 0;
+      uint32_t c_seq = 0;   // K tiles whose quads went through the staging buffer
       for (long long item = group; item < geo.num_items; item += geo.stride) {
         int h, chunk, lt, m;
         decode_item(p, geo, item, h, chunk, lt, m);
@@ -768,6 +812,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < kMaxK; ++j) sl_all[j] = j < p.k ? p.layer_idx[lt * p.k + j] : 0;
         for (int tile = t_beg; tile < t_end; ++tile) {
+          if (kStageCpl && m == 0) {
+            // a K tile: stage the source-RoPE quads of its positions when
+            // they are p0, p0 + 1, ... (one request, implicit positions),
+            // else let the transform warps read the global table
+            if (!W.wait(&sh->c_empty, (c_seq & 1) ^ 1)) goto loader_done;
+            const int64_t g0 = (int64_t)tile * tile_rows + rank * kTileM;
+            int mode = 2;
+            int64_t p0 = 0;
+            if (p.src_pos == nullptr && g0 < p.ntok) {
+              const int64_t g1 = g0 + kTileM - 1 < p.ntok ? g0 + kTileM - 1 : p.ntok - 1;
+              const int r0 = kvx::request_of(p, g0);
+              if (kvx::request_of(p, g1) == r0) {
+                p0 = g0 - (p.cu_seqlens ? (int64_t)p.cu_seqlens[r0] : 0);
+                mode = p0 < p.max_position ? 1 : 2;
+              }
+            }
+            sh->c_mode = mode;
+            const uint32_t cbar = smem_addr(&sh->c_full);
+            if (mode == 1) {
+              mbar_expect_tx(cbar, kCplBytes);
+              tma_load_2d(smem_addr(cbuf), &tmap_cpl, (int)(2 * p0), 0, cbar);
+            } else {
+              mbar_arrive(cbar);
+            }
+            ++c_seq;
+          }
 #pragma unroll
           for (int j = 0; j < kMaxK; ++j) {
             if (j >= p.k) break;
@@ -785,7 +855,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     loader_done:
-      // drain: the last `stages` loads (at most) may still be in flight
+      // drain: the last staged quads and the last `stages` loads (at most)
+      // may still be in flight
+      if (c_seq > 0) drain_wait(&sh->c_full, (c_seq - 1) & 1);
       for (uint32_t n = (x_seq > (uint32_t)geo.stages ? x_seq - geo.stages : 0); n < x_seq; ++n)
         drain_wait(&sh->x_full[n % geo.stages], (n / geo.stages) & 1);
     }
@@ -846,7 +918,7 @@ __global__ void __launch_bounds__(256) w_image_kernel(const WT *__restrict__ w,
 
 size_t smem_bytes(int k, int stages, int pair) {
   return 1024 + (size_t)2 * k * (kChunkBytes / pair) + (size_t)stages * kStageBytes +
-         sizeof(Shared) + 64;
+         (pair == 2 ? kCplBytes : 0) + sizeof(Shared) + 64;
 }
 
 int max_stages(int k, int pair) {
@@ -872,6 +944,24 @@ bool encode_map(const kvx_plan *plan, CUtensorMap *map, const void *base, const 
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D TMA map over the source-RoPE quad table [16][max_position] of 16-byte
+// elements, seen as 8-byte elements: box [16 quads][128 positions].
+bool encode_cpl_map(const kvx_plan *plan, CUtensorMap *map, const KvxParams &p) {
+  typedef CUresult (*EncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                               const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                               const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  EncodeFn fn = reinterpret_cast<EncodeFn>(plan->encode_tiled);
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)2 * p.max_position, (cuuint64_t)(kD / 8)};
+  const cuuint64_t strides[1] = {(cuuint64_t)p.max_position * 16};
+  const cuuint32_t box[2] = {(cuuint32_t)(2 * kTileM), (cuuint32_t)(kD / 8)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, plan->tc_rope_src, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -962,17 +1052,18 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   geo.stages = max_stages(p.k, P);
   const long long slots = P == 2 ? plan->tc_pairs : plan->num_sms;
   geo.stride = geo.num_items < slots ? geo.num_items : slots;
-  CUtensorMap mk, mv;
-  if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p))
+  CUtensorMap mk, mv, mc;
+  if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p) ||
+      !encode_cpl_map(plan, &mc, p))
     return cudaErrorInvalidValue;
   RopeTurns rope;
   for (int i = 0; i < kHalf; ++i) rope.tgt[i] = plan->turns_tgt[i];
-  const uint2 *rope_src2 = reinterpret_cast<const uint2 *>(plan->tc_rope_src);
+  const uint4 *rope_src4 = reinterpret_cast<const uint4 *>(plan->tc_rope_src);
   const __nv_bfloat16 *wimg = reinterpret_cast<const __nv_bfloat16 *>(plan->workspace);
   const size_t smem = smem_bytes(p.k, geo.stages, P);
   if (P == 1) {
     tc_transfer_kernel<1><<<(unsigned)geo.stride, kThreads, smem, s>>>(
-        p, mk, mv, rope_src2, rope, bimg, wimg, geo, plan->stall_test);
+        p, mk, mv, mc, rope_src4, rope, bimg, wimg, geo, plan->stall_test);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -987,6 +1078,6 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_transfer_kernel<2>, p, mk, mv, rope_src2, rope, bimg, wimg,
-                            geo, plan->stall_test);
+  return cudaLaunchKernelEx(&cfg, tc_transfer_kernel<2>, p, mk, mv, mc, rope_src4, rope, bimg,
+                            wimg, geo, plan->stall_test);
 }
