@@ -181,7 +181,9 @@ def kernel_source_sha(kernel_name: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "cross_model_kv_transfer_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        if fn == KERNEL_FILES.get(kernel_name) or fn.endswith((".h", ".cuh")):
+        # the kernel, its headers, and the host code that sets its launch
+        # shape (tiles per item, CTA pairs): all of them change its traffic
+        if fn in (KERNEL_FILES.get(kernel_name), "kvx_api.cpp") or fn.endswith((".h", ".cuh")):
             with open(os.path.join(csrc, fn), "rb") as f:
                 h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

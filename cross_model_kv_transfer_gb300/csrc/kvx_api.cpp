@@ -214,7 +214,7 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   p->kernel = kernel;
   p->num_sms = prop.multiProcessorCount;
   p->half = desc->src_head_dim / 2;
-  p->tiles_per_item = desc->tiles_per_item > 0 ? desc->tiles_per_item : 16;
+  p->tiles_per_item = desc->tiles_per_item > 0 ? desc->tiles_per_item : 32;
   p->stall_test = (desc->flags & KVX_PLAN_TEST_STALL) ? 1 : 0;
 
   if (kernel == KVX_KERNEL_SIMT) {

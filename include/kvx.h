@@ -115,8 +115,9 @@ typedef struct {
   int32_t max_position;     /* every source and target position must lie in
                                [0, max_position); sizes the SIMT RoPE tables */
   int32_t kernel;           /* kvx_kernel                                    */
-  int32_t tiles_per_item;   /* tensor-core path: 128-token tiles per work
-                               item (W is loaded once per item); 0 = default */
+  int32_t tiles_per_item;   /* tensor-core path: token tiles (128 rows, or
+                               256 for CTA pairs) per work item; W is loaded
+                               once per item; 0 = default (32)              */
   int32_t flags;            /* KVX_PLAN_* bits; 0 for normal use            */
 } kvx_plan_desc;
 
