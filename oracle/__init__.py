@@ -20,6 +20,11 @@ What each function computes, and the passages it follows, is documented in
 * ``transfer``    the whole transfer over all requests, tokens, layers, heads.
 * ``ridge_fit``   centred ridge regression with intercept (the Qwen3
                   article's ridge demo).
+* ``kv_diagnostics`` KV cosine ("Helm Intelligent Routing", "Reading the
+                  retention score") and explained variance (the Qwen3
+                  article's linear-structure analysis) of a mapped cache
+                  against the target's own, per (target layer, head, K|V);
+                  ``mean_cosine`` and ``explained_variance`` read them out.
 """
 from __future__ import annotations
 
@@ -110,6 +115,8 @@ def _load():
             lib.kvxo_ridge_fit.argtypes = [dp, dp, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_double, dp, dp]
             lib.kvxo_ridge_fit.restype = ctypes.c_int
+            lib.kvxo_kv_diagnostics.argtypes = [ctypes.POINTER(_Problem), dp, dp, dp, dp, dp]
+            lib.kvxo_kv_diagnostics.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -221,3 +228,53 @@ def ridge_fit(X, Y, lam: float = 0.01):
     if rc != 0:
         raise np.linalg.LinAlgError("ridge normal matrix is not positive definite")
     return W, b
+
+
+def kv_diagnostics(*, mapped_k, mapped_v, ref_k, ref_v, theta_tgt, max_position,
+                   ntok, cu_seqlens=None, src_pos=None, tgt_pos=None, tgt_offset=None,
+                   layout=CONTIGUOUS, dst_capacity=0, block_size=1, num_blocks=0,
+                   block_table=None):
+    """Per-(target layer, head, K|V) statistics [Lt][H][2][d + 4] of the
+    mapped cache against the target's own cache (both [Lt][rows][H][d]),
+    over the tokens a transfer with the same request table, positions and
+    layout writes; see ``kvx_oracle.h``.  Returns (stats, status bits)."""
+    mk, mv, rk, rv = _f64(mapped_k), _f64(mapped_v), _f64(ref_k), _f64(ref_v)
+    Lt, rows, H, d = rk.shape
+    assert mk.shape == mv.shape == rk.shape == rv.shape
+    cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    R = 1 if cu is None else cu.shape[0] - 1
+    sp = None if src_pos is None else np.ascontiguousarray(src_pos, dtype=np.int64)
+    tp = None if tgt_pos is None else np.ascontiguousarray(tgt_pos, dtype=np.int64)
+    to = None if tgt_offset is None else np.ascontiguousarray(tgt_offset, dtype=np.int64)
+    bt = None
+    mbpr = 0
+    if layout == PAGED:
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        mbpr = bt.shape[1]
+        assert rows == num_blocks * block_size
+    else:
+        assert rows == R * dst_capacity
+    P = _Problem(0, Lt, H, d, 0, 0.0, float(theta_tgt), int(max_position), R, int(ntok),
+                 _vp(cu), None, None, None, None, None, _vp(sp), _vp(tp), _vp(to),
+                 int(layout), int(dst_capacity), int(block_size), int(num_blocks), int(mbpr),
+                 _vp(bt))
+    stats = np.empty((Lt, H, 2, d + 4))
+    st = _load().kvxo_kv_diagnostics(ctypes.byref(P), _dp(mk), _dp(mv), _dp(rk), _dp(rv),
+                                     _dp(stats))
+    return stats, int(st)
+
+
+def mean_cosine(stats):
+    """Mean KV cosine per entry of ``stats[..., :]`` (NaN where n = 0)."""
+    s = np.asarray(stats, dtype=np.float64)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        return s[..., 1] / s[..., 0]
+
+
+def explained_variance(stats):
+    """Centred R^2 per entry of ``stats`` (content space, summed over d)."""
+    s = np.asarray(stats, dtype=np.float64)
+    n = s[..., 0]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        ss_tot = s[..., 3] - np.sum(s[..., 4:] ** 2, axis=-1) / n
+        return 1.0 - s[..., 2] / ss_tot

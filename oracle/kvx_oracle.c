@@ -180,6 +180,76 @@ int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
   return status;
 }
 
+/* KV cosine of [HIR] ("Reading the retention score") and explained variance
+ * of [QKV] ("Линейного моста, как ни странно, хватает"), accumulated over
+ * the tokens a transfer writes; definitions in kvx_oracle.h. */
+int kvxo_kv_diagnostics(const kvxo_problem *P, const double *mapped_k,
+                        const double *mapped_v, const double *ref_k,
+                        const double *ref_v, double *stats) {
+  const int64_t Lt = P->tgt_layers, H = P->kv_heads, d = P->head_dim;
+  const int64_t ntok = P->ntok, F = d + 4;
+  const int64_t rows = P->layout == KVXO_CONTIGUOUS
+                           ? (int64_t)P->num_requests * P->dst_capacity
+                           : P->num_blocks * P->block_size;
+  int status = 0;
+  for (int64_t i = 0; i < Lt * H * 2 * F; ++i) stats[i] = 0.0;
+  if (P->cu_seqlens) {
+    int ok = P->cu_seqlens[0] == 0 && P->cu_seqlens[P->num_requests] == ntok;
+    for (int64_t r = 0; r < P->num_requests; ++r)
+      if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;
+    if (!ok) return KVXO_BAD_SEQLENS;
+  }
+  double *content = (double *)malloc(sizeof(double) * (size_t)d);
+  for (int64_t r = 0; r < P->num_requests; ++r) {
+    int64_t beg = P->cu_seqlens ? P->cu_seqlens[r] : 0;
+    int64_t end = P->cu_seqlens ? P->cu_seqlens[r + 1] : ntok;
+    for (int64_t g = beg; g < end; ++g) {
+      int64_t p = P->src_pos ? P->src_pos[g] : g - beg;
+      int64_t off = P->tgt_offset ? P->tgt_offset[r] : 0;
+      int64_t pt = P->tgt_pos ? P->tgt_pos[g] : p + off;
+      if (p < 0 || p >= P->max_position || pt < 0 || pt >= P->max_position) {
+        status |= KVXO_BAD_POSITION;
+        continue;
+      }
+      int bad = 0;
+      int64_t row = kvxo_dst_row(P->layout, r, pt, P->dst_capacity,
+                                 P->block_size, P->num_blocks, P->block_table,
+                                 P->max_blocks_per_req, &bad);
+      if (row < 0) {
+        status |= bad;
+        continue;
+      }
+      for (int64_t lt = 0; lt < Lt; ++lt) {
+        for (int64_t h = 0; h < H; ++h) {
+          for (int m = 0; m < 2; ++m) {
+            const double *a = (m == 0 ? mapped_k : mapped_v) + ((lt * rows + row) * H + h) * d;
+            const double *y = (m == 0 ? ref_k : ref_v) + ((lt * rows + row) * H + h) * d;
+            double dot = 0.0, aa = 0.0, yy = 0.0, res = 0.0;
+            for (int64_t i = 0; i < d; ++i) {
+              dot += a[i] * y[i];
+              aa += a[i] * a[i];
+              yy += y[i] * y[i];
+              res += (y[i] - a[i]) * (y[i] - a[i]);
+            }
+            double *st = stats + ((lt * H + h) * 2 + m) * F;
+            st[0] += 1.0;
+            if (aa > 0.0 && yy > 0.0) st[1] += dot / sqrt(aa * yy);
+            st[2] += res;
+            st[3] += yy;
+            if (m == 0)
+              kvxo_rope(y, (int)d, (double)pt, P->theta_tgt, -1, content);
+            else
+              memcpy(content, y, sizeof(double) * (size_t)d);
+            for (int64_t i = 0; i < d; ++i) st[4 + i] += content[i];
+          }
+        }
+      }
+    }
+  }
+  free(content);
+  return status;
+}
+
 /* Ridge demo of [QKV] ("Линейного моста, как ни странно, хватает"): centre
  * X and Y on their column means, solve (XcT Xc + lam I) W = XcT Yc, and set
  * b = ybar - xbar W.  The solve is a plain Cholesky factorisation. */

@@ -117,6 +117,36 @@ typedef struct {
  * written keep their contents.  Returns the OR of KVXO_BAD_* bits. */
 int kvxo_transfer(const kvxo_problem *prob, double *dst_k, double *dst_v);
 
+/* Fidelity diagnostics of a transfer: how close the mapped cache is to the
+ * target model's own cache for the same tokens.
+ *  [HIR] section "Reading the retention score": "KV cosine" -- the closeness
+ *        of the mapped cache to the target's own, a diagnostic read beside
+ *        retention.
+ *  [QKV] section "Линейного моста, как ни странно, хватает": the share of
+ *        the target keys' / values' variance that the selected source layers
+ *        explain (one best layer ~56 % / 32 %, a set ~79 % / 65 %).
+ * Readings: the cosine is taken per (target layer, token, head) between the
+ * two d-vectors as stored (both keys carry the target RoPE at p', which a
+ * cosine does not see) and is 0 when either vector is zero; the explained
+ * variance is the centred R^2 of the mapped vectors as predictions of the
+ * target's, summed over the d dimensions, in content space: keys are
+ * un-rotated at p' (theta_tgt) before the mean is taken; the residual and
+ * the norms are the same in either space.
+ * For each (lt, h, m), m = 0 keys and 1 values, the d + 4 doubles at
+ * stats[((lt * H + h) * 2 + m) * (d + 4)] are set to
+ *   [0] n, tokens compared;          [1] sum of the cosines;
+ *   [2] sum |ref - mapped|^2;        [3] sum |ref|^2;
+ *   [4 + i] sum of ref_i in content space.
+ * Mean cosine = [1] / [0]; R^2 = 1 - [2] / ([3] - |[4..]|^2 / [0]).
+ * The tokens are the ones a transfer with the same problem writes: the same
+ * position and row rules (prob's source arrays, W and layer table are not
+ * used); caches are [Lt][rows][H][d] as for kvxo_transfer.  Returns the OR
+ * of the KVXO_BAD_* bits of the skipped tokens (KVXO_BAD_SEQLENS: nothing
+ * compared, all stats 0). */
+int kvxo_kv_diagnostics(const kvxo_problem *prob, const double *mapped_k,
+                        const double *mapped_v, const double *ref_k,
+                        const double *ref_v, double *stats);
+
 /* Centred ridge regression with intercept, as in the ridge demo of [QKV]:
  * X [n][p], Y [n][q] row-major; W [p][q] = (XcT Xc + lam I)^-1 XcT Yc,
  * b [q] = ybar - xbar W.  Solved by Cholesky.  Returns 0, or -1 if the

@@ -513,3 +513,148 @@ def test_ridge_equals_augmented_least_squares():
     want = np.linalg.lstsq(A, B, rcond=None)[0]
     W, b = oracle.ridge_fit(X, Y, lam=lam)
     np.testing.assert_allclose(W, want, rtol=1e-9, atol=1e-11)
+
+
+# --------------------------------------------------------------------------
+# Fidelity diagnostics: KV cosine ("Helm Intelligent Routing", "Reading the
+# retention score") and explained variance (the Qwen3 article, section on
+# the linear bridge: the share of target K / V variance the source explains)
+# --------------------------------------------------------------------------
+
+def _golden_rows(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *vals = line.split()
+            rows[key] = vals
+    return rows
+
+
+def _diag(mk, mv, rk, rv, **kw):
+    kw.setdefault("theta_tgt", 1e4)
+    kw.setdefault("max_position", 64)
+    return oracle.kv_diagnostics(mapped_k=mk, mapped_v=mv, ref_k=rk, ref_v=rv, **kw)
+
+
+def test_kv_diagnostics_worked_example():
+    g = _golden_rows("kv_diagnostics_worked_example.txt")
+    cache = lambda key: np.array([float(x) for x in g[key]]).reshape(1, 2, 1, 2)
+    stats, st = _diag(cache("mapped_k"), cache("mapped_v"), cache("ref_k"), cache("ref_v"),
+                      ntok=2, dst_capacity=2)
+    assert st == 0
+    frac = lambda v: float(Fraction(v))
+    k, v = stats[0, 0, 0], stats[0, 0, 1]
+    np.testing.assert_allclose(k[:4], [frac(x) for x in g["stats_k"]], rtol=1e-15)
+    # keys in content space: token 0 at p' = 0 as stored, token 1 at p' = 1
+    # un-rotated: (0 + 2j) e^{-j} = 2 sin 1 + 2j cos 1
+    ksum = [3 + 2 * math.sin(1.0), 4 + 2 * math.cos(1.0)]
+    np.testing.assert_allclose(k[4:], ksum, rtol=1e-15)
+    ss_tot = (29 - 12 * math.sin(1.0) - 16 * math.cos(1.0)) / 2
+    assert oracle.explained_variance(stats)[0, 0, 0] == pytest.approx(1 - 2 / ss_tot, rel=1e-14)
+    assert oracle.mean_cosine(stats)[0, 0, 0] == pytest.approx(49 / 50, rel=1e-15)
+    assert v[0] == 2 and v[1] == pytest.approx(1 / math.sqrt(2), rel=1e-15)
+    np.testing.assert_allclose(v[2:4], [frac(x) for x in g["stats_v"][2:]], rtol=1e-15)
+    np.testing.assert_allclose(v[4:], [frac(x) for x in g["sum_v"]], atol=0)
+    assert oracle.explained_variance(stats)[0, 0, 1] == pytest.approx(frac(g["r2_v"][0]), rel=1e-14)
+
+
+def _paged_case(rng, Lt=2, H=3, d=8):
+    # three requests, a permuted block pool, target offsets: every row a
+    # transfer writes is filled, every other row is NaN (never to be read)
+    cu = np.array([0, 5, 9, 16])
+    off = np.array([0, 3, 1])
+    bs, nblk, mbpr = 4, 12, 4
+    table = rng.permutation(nblk)[:3 * mbpr].reshape(3, mbpr).astype(np.int32)
+    rows = nblk * bs
+    ref_k = np.full((Lt, rows, H, d), np.nan)
+    ref_v = np.full((Lt, rows, H, d), np.nan)
+    pts, used = [], []
+    for r in range(3):
+        for g in range(cu[r], cu[r + 1]):
+            pt = g - cu[r] + off[r]
+            row = table[r][pt // bs] * bs + pt % bs
+            pts.append(pt)
+            used.append(row)
+    used = np.array(used)
+    ref_k[:, used] = rng.standard_normal((Lt, len(used), H, d))
+    ref_v[:, used] = rng.standard_normal((Lt, len(used), H, d))
+    kw = dict(ntok=16, cu_seqlens=cu, tgt_offset=off, layout=oracle.PAGED, block_size=bs,
+              num_blocks=nblk, block_table=table)
+    return ref_k, ref_v, np.array(pts), used, kw
+
+
+def test_kv_diagnostics_identity_negation_and_scale():
+    ref_k, ref_v, _, used, kw = _paged_case(np.random.default_rng(7))
+    s, st = _diag(ref_k, ref_v, ref_k, ref_v, **kw)
+    assert st == 0
+    assert np.all(s[..., 0] == 16)
+    np.testing.assert_allclose(oracle.mean_cosine(s), 1.0, rtol=1e-14)
+    assert np.all(s[..., 2] == 0)
+    np.testing.assert_allclose(oracle.explained_variance(s), 1.0, rtol=1e-14)
+    s, _ = _diag(-ref_k, 2.5 * ref_v, ref_k, ref_v, **kw)
+    np.testing.assert_allclose(oracle.mean_cosine(s)[..., 0], -1.0, rtol=1e-14)
+    np.testing.assert_allclose(oracle.mean_cosine(s)[..., 1], 1.0, rtol=1e-14)
+    # |y - 2.5 y|^2 = 2.25 |y|^2, summed over the compared tokens
+    np.testing.assert_allclose(s[..., 1, 2], 2.25 * s[..., 1, 3], rtol=1e-13)
+    yy = np.einsum("lthd,lthd->lh", ref_v[:, used], ref_v[:, used])
+    np.testing.assert_allclose(s[..., 1, 3], yy, rtol=1e-13)
+
+
+def test_kv_diagnostics_keys_are_averaged_in_content_space():
+    # every key is one content vector c rotated to its own p': un-rotating
+    # at p' with the target base gives back n * c (a wrong sign, base or
+    # pairing would not); the stored vectors themselves do not sum to n * c
+    rng = np.random.default_rng(11)
+    ref_k, ref_v, pts, used, kw = _paged_case(rng, Lt=1, H=2, d=8)
+    theta = 5e5
+    c = rng.standard_normal((2, 8))
+    for i, row in enumerate(used):
+        for h in range(2):
+            ref_k[0, row, h] = oracle.rope(c[h], pts[i], theta, +1)
+    s, st = _diag(ref_k, ref_v, ref_k, ref_v, theta_tgt=theta, **kw)
+    assert st == 0
+    np.testing.assert_allclose(s[0, :, 0, 4:], 16 * c, rtol=1e-12, atol=1e-12)
+    stored = ref_k[0, used].sum(axis=0)
+    assert np.max(np.abs(stored - 16 * c)) > 1.0
+
+
+def test_kv_diagnostics_mean_predictor_explains_nothing():
+    # predicting every token by the content-space mean (re-rotated to its p'
+    # for keys) gives R^2 = 0 exactly: the residual is the centred spread
+    rng = np.random.default_rng(5)
+    ref_k, ref_v, pts, used, kw = _paged_case(rng, Lt=1, H=2, d=6)
+    theta = 1e4
+    cont = np.stack([np.stack([oracle.rope(ref_k[0, row, h], pts[i], theta, -1)
+                               for h in range(2)]) for i, row in enumerate(used)])
+    mean_c = cont.mean(axis=0)
+    mk = np.full_like(ref_k, np.nan)
+    mv = np.full_like(ref_v, np.nan)
+    vmean = ref_v[0, used].mean(axis=0)
+    for i, row in enumerate(used):
+        for h in range(2):
+            mk[0, row, h] = oracle.rope(mean_c[h], pts[i], theta, +1)
+        mv[0, row] = vmean
+    s, _ = _diag(mk, mv, ref_k, ref_v, theta_tgt=theta, **kw)
+    np.testing.assert_allclose(oracle.explained_variance(s), 0.0, atol=1e-12)
+
+
+def test_kv_diagnostics_zero_vector_cosine_is_zero():
+    rk = np.ones((1, 1, 1, 4))
+    s, _ = _diag(np.zeros_like(rk), rk, rk, rk, ntok=1, dst_capacity=1)
+    assert s[0, 0, 0, 1] == 0.0 and s[0, 0, 0, 0] == 1
+    assert s[0, 0, 1, 1] == pytest.approx(1.0, rel=1e-15)
+
+
+def test_kv_diagnostics_skips_what_a_transfer_skips():
+    # the token at p' = 4 >= max_position is neither compared nor counted;
+    # a malformed request table compares nothing
+    rk = np.arange(2 * 5 * 1 * 2, dtype=np.float64).reshape(2, 5, 1, 2) + 1
+    s, st = _diag(rk, rk, rk, rk, ntok=5, dst_capacity=5, max_position=4)
+    assert st == oracle.BAD_POSITION
+    assert np.all(s[..., 0] == 4)
+    rk3 = np.ones((2, 15, 1, 2))
+    s, st = _diag(rk3, rk3, rk3, rk3, ntok=5, dst_capacity=5, cu_seqlens=[0, 3, 2, 5])
+    assert st == oracle.BAD_SEQLENS
+    assert np.all(s == 0)
