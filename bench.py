@@ -1,7 +1,10 @@
 """Benchmark of the cross-model KV-cache transfer on GB300.
 
 One step = one ``kvx_transfer`` (gather, un-rotate, concatenate, map, re-rotate,
-install) over every target layer, head and token of the workload.  The default
+install) over every target layer, head and token of the workload.  With
+``--op kv_diagnostics`` one step is instead one ``kvx_kv_diagnostics`` call
+(KV cosine and explained variance of the mapped cache against the target's
+own) over the same workload.  The default
 workload is the Qwen3-14B -> 32B shape at 32,768 tokens (40 -> 64 layers, 8 KV
 heads, head_dim 128, k = 4, bf16 caches, fp32 W, bf16 b, theta 1e6), with
 synthetic inputs resident in HBM.
@@ -33,7 +36,7 @@ METRIC = "KV-transfer tokens/s at 14B→32B shape, 32K tokens; % of HBM/tensor r
 # section on what the headline number covers).
 PUBLISHED_MS = {"qwen3_14b_32b": 277.6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu"}
+KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu", "diag": "kvx_diag.cu"}
 
 
 def parse_args(argv=None):
@@ -42,6 +45,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
+    ap.add_argument("--op", choices=["transfer", "kv_diagnostics"], default="transfer",
+                    help="transfer (the default step) or the fidelity diagnostics of a "
+                         "mapped cache against the target's own")
     ap.add_argument("--workload", default="qwen3_14b_32b")
     ap.add_argument("--kernel", choices=["auto", "simt", "tcgen05"], default="auto")
     ap.add_argument("--tokens", type=int, default=0,
@@ -312,6 +318,12 @@ def run_kvx(args):
     targs = plan.make_args(**transfer_kwargs(wl, inp, dst_k, dst_v, status))
     stream = torch.cuda.current_stream(dev)
     sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
+    if args.op == "kv_diagnostics":
+        if wl.layout != PAGED and any(wl.tgt_offsets):
+            raise SystemExit("kv_diagnostics bench: contiguous workloads with offset 0 only")
+        run_diag(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, ws, rank)
+        plan.close()
+        return
 
     def step():
         st = kvx.kvx_transfer(plan.handle, targs, sptr)
@@ -378,6 +390,158 @@ def run_kvx(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     plan.close()
+
+
+DIAG_METRIC = ("KV-diagnostics tokens/s (KV cosine + explained variance of a mapped cache "
+               "against the target's own) at 14B→32B shape, 32K tokens; % of HBM roofline")
+
+
+def diag_kwargs(wl, inp):
+    from cross_model_kv_transfer_gb300.workloads import PAGED
+    kw = dict(ntok=wl.ntok)
+    if wl.num_requests > 1 or wl.layout == PAGED:
+        kw["cu_seqlens"] = inp["cu_seqlens"]
+    if any(wl.tgt_offsets):
+        kw["tgt_offset"] = inp["tgt_offset"]
+    if wl.layout == PAGED:
+        kw.update(block_table=inp["block_table"], num_blocks=wl.num_blocks)
+    else:
+        kw["dst_capacity"] = wl.dst_capacity
+    return kw
+
+
+def run_diag(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, ws, rank):
+    """One step = one kvx_kv_diagnostics call over the whole mapped cache (the
+    output of one transfer) against a stand-in for the target's own cache.
+    HBM-bound: the algorithmic bytes are the two caches read once."""
+    import ctypes
+    import torch
+    from cross_model_kv_transfer_gb300 import kvx
+    from cross_model_kv_transfer_gb300.workloads import PAGED, perturbed_like
+
+    st = kvx.kvx_transfer(plan.handle, plan.make_args(**transfer_kwargs(wl, inp, dst_k, dst_v,
+                                                                        status)),
+                          ctypes.c_void_p(stream.cuda_stream))
+    if st != kvx.KVX_OK:
+        raise kvx.KvxError(st, "kvx_transfer")
+    ref_k, ref_v = perturbed_like(dst_k, 101), perturbed_like(dst_v, 102)
+    stats = torch.empty((wl.tgt_layers, wl.kv_heads, 2, wl.head_dim + 4), dtype=torch.float64,
+                        device=dev)
+    dargs = plan.make_diag_args(mapped_k=dst_k, mapped_v=dst_v, ref_k=ref_k, ref_v=ref_v,
+                                stats=stats, status=status, **diag_kwargs(wl, inp))
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        e = kvx.kvx_kv_diagnostics(plan.handle, dargs, sptr)
+        if e != kvx.KVX_OK:
+            raise kvx.KvxError(e, "kvx_kv_diagnostics")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    value, ms = aggregate(wl.ntok, ms_local, dev)
+
+    eb = dst_k.element_size()
+    alg_bytes = 4 * wl.tgt_layers * wl.ntok * wl.kv_heads * wl.head_dim * eb \
+        + stats.numel() * 8
+    peaks, peak_kind = load_peaks()
+    achieved = alg_bytes / (ms_local / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"],
+            "traffic": measured_traffic(wl.name, "diag"),
+            "peak_source": f"{peak_kind} (burst)", "algorithmic_bytes": alg_bytes}
+
+    e2e = None
+    if not args.no_e2e:
+        # host buffers: both caches copied in, the statistics read back, every step
+        hk, hv = dst_k.cpu().pin_memory(), dst_v.cpu().pin_memory()
+        hrk, hrv = ref_k.cpu().pin_memory(), ref_v.cpu().pin_memory()
+        hs = torch.empty(stats.shape, dtype=stats.dtype, pin_memory=True)
+        pairs = [(dst_k, hk), (dst_v, hv), (ref_k, hrk), (ref_v, hrv)]
+
+        def e2e_step():
+            for d_, h_ in pairs:
+                d_.copy_(h_, non_blocking=True)
+            step()
+            hs.copy_(stats, non_blocking=True)
+
+        n_e = max(1, min(args.steps, 3))
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        ev0.record(stream)
+        for _ in range(n_e):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_ms_local = ev0.elapsed_time(ev1) / n_e
+        e_val, e_ms = aggregate(wl.ntok, e_ms_local, dev)
+        e2e = {"value": e_val, "unit": "tokens/s", "ms_per_step": e_ms, "steps": n_e,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for _, h in pairs),
+               "d2h_bytes_per_step": hs.numel() * 8}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle_diag(wl, dst_k, dst_v, ref_k, ref_v, args.cpu_seconds)
+    line = {
+        "metric": DIAG_METRIC, "op": "kv_diagnostics", "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (mapped cache from one transfer of the seeded workload; the "
+                "target's own cache stood in by a seeded perturbation of it)",
+        "config": {"workload": wl.name, "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
+                   "head_dim": wl.head_dim, "tokens": wl.ntok, "requests": wl.num_requests,
+                   "layout": "paged" if wl.layout == PAGED else "contiguous",
+                   "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2 ({4 * dst_k.numel() * eb / 1e9:.2f} GB of "
+                         "caches read per step, no flush needed)"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def time_oracle_diag(wl, mk, mv, rk, rv, target_seconds: float):
+    """Tokens/s of the fp64 oracle's diagnostics (one host thread) on the
+    first n tokens of a contiguous, offset-0 cache."""
+    import torch
+    import oracle
+
+    def sample(n):
+        f64 = lambda t: t[:, :n].detach().cpu().to(torch.float64).numpy()
+        return dict(mapped_k=f64(mk), mapped_v=f64(mv), ref_k=f64(rk), ref_v=f64(rv),
+                    theta_tgt=wl.theta_tgt, max_position=n, ntok=n, dst_capacity=n)
+
+    s1 = sample(16)
+    t0 = time.perf_counter()
+    oracle.kv_diagnostics(**s1)
+    per_tok = max((time.perf_counter() - t0) / 16, 1e-6)
+    n = int(max(16, min(wl.ntok, target_seconds / per_tok)))
+    sn = sample(n)
+    t0 = time.perf_counter()
+    oracle.kv_diagnostics(**sn)
+    el = time.perf_counter() - t0
+    return {"value": n / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} tokens of the mapped and reference caches through all "
+                      f"{wl.tgt_layers} target layers x {wl.kv_heads} heads x K|V "
+                      f"({el:.1f} s of fp64 CPU work, one thread)"}
 
 
 def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status):

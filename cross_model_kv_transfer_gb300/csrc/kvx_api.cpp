@@ -232,8 +232,10 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
     std::vector<uint32_t> ts;
     tc_rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position, ts);
     st = upload_bytes(ts.data(), ts.size() * sizeof(uint32_t), &p->tc_rope_src);
-    rope_turns(desc->rope_theta_tgt, desc->tgt_head_dim, p->turns_tgt);
   }
+  // target frequencies in turns: the tensor-core epilogue and the
+  // diagnostics kernel (any plan) evaluate target RoPE angles from them
+  rope_turns(desc->rope_theta_tgt, desc->tgt_head_dim, p->turns_tgt);
   if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05) {
     p->encode_tiled = kvx_tc_encoder();
     st = p->encode_tiled ? alloc_workspace(p, kvx_tc_workspace_bytes(*desc))

@@ -27,6 +27,7 @@ struct kvx_plan {
   // (i .. i+3), i % 4 == 0: tc_rope_src[i/4][p] = bf16x2 (cos_i, cos_i+1),
   // (sin_i, sin_i+1), (cos_i+2, cos_i+3), (sin_i+2, sin_i+3); target RoPE
   // frequencies as 64-bit fractions of a turn, round(w_i / 2pi * 2^64)
+  // (set for every plan: the diagnostics kernel uses them too)
   void *tc_rope_src;
   unsigned long long turns_tgt[128];
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook

@@ -7,12 +7,14 @@ be loaded (or built with nvcc on first use), importing the symbols raises.
 
 Low level (same names as the C ABI): ``kvx_plan_create``, ``kvx_transfer``,
 ``kvx_plan_destroy``, ``kvx_status_string``, ``kvx_plan_kernel``,
-``kvx_plan_launches``, ``kvx_plan_cta_group``, ``kvx_transfer_static`` taking the ctypes structures
-``PlanDesc`` / ``TransferArgs``.
+``kvx_plan_launches``, ``kvx_plan_cta_group``, ``kvx_transfer_static``,
+``kvx_kv_diagnostics`` taking the ctypes structures ``PlanDesc`` /
+``TransferArgs`` / ``DiagArgs``.
 
-Convenience: ``Plan`` (owns a plan handle) and ``Plan.transfer(...)`` which
+Convenience: ``Plan`` (owns a plan handle), ``Plan.transfer(...)`` which
 takes torch CUDA tensors, checks their shapes, dtypes and devices, and calls
-``kvx_transfer`` on the current torch stream.
+``kvx_transfer`` on the current torch stream, and ``Plan.kv_diagnostics(...)``
+(fidelity statistics of a mapped cache against the target's own).
 """
 from __future__ import annotations
 
@@ -50,7 +52,7 @@ KVX_PLAN_TC_SINGLE_CTA = 2
 
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
             "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches",
-            "kvx_plan_cta_group", "kvx_transfer_static")
+            "kvx_plan_cta_group", "kvx_transfer_static", "kvx_kv_diagnostics")
 
 
 class PlanDesc(ctypes.Structure):
@@ -79,6 +81,20 @@ class TransferArgs(ctypes.Structure):
         ("dst_capacity", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
         ("block_table", ctypes.c_void_p), ("max_blocks_per_req", ctypes.c_int32),
         ("status", ctypes.c_void_p),
+    ]
+
+
+class DiagArgs(ctypes.Structure):
+    _fields_ = [
+        ("mapped_k", ctypes.c_void_p), ("mapped_v", ctypes.c_void_p),
+        ("ref_k", ctypes.c_void_p), ("ref_v", ctypes.c_void_p),
+        ("ntok", ctypes.c_int64), ("num_requests", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("src_pos", ctypes.c_void_p), ("tgt_pos", ctypes.c_void_p),
+        ("tgt_offset", ctypes.c_void_p),
+        ("dst_capacity", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p), ("max_blocks_per_req", ctypes.c_int32),
+        ("stats", ctypes.c_void_p), ("status", ctypes.c_void_p),
     ]
 
 
@@ -118,6 +134,9 @@ def load():
             lib.kvx_transfer_static.argtypes = [ctypes.POINTER(PlanDesc),
                                                 ctypes.POINTER(TransferArgs), ctypes.c_void_p]
             lib.kvx_transfer_static.restype = ctypes.c_int
+            lib.kvx_kv_diagnostics.argtypes = [ctypes.c_void_p, ctypes.POINTER(DiagArgs),
+                                               ctypes.c_void_p]
+            lib.kvx_kv_diagnostics.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -157,6 +176,10 @@ def kvx_transfer_static(desc: PlanDesc, args: TransferArgs, stream) -> int:
     """Allocation-free transfer (SIMT kernel, RoPE tables in the library's
     fixed device array); for callers that may not allocate device memory."""
     return load().kvx_transfer_static(ctypes.byref(desc), ctypes.byref(args), stream)
+
+
+def kvx_kv_diagnostics(plan, args: DiagArgs, stream) -> int:
+    return load().kvx_kv_diagnostics(plan, ctypes.byref(args), stream)
 
 
 class KvxError(RuntimeError):
@@ -282,3 +305,67 @@ class Plan:
         st = kvx_transfer(self.handle, args, ctypes.c_void_p(stream.cuda_stream))
         if st != KVX_OK:
             raise KvxError(st, "kvx_transfer")
+
+    def make_diag_args(self, *, mapped_k, mapped_v, ref_k, ref_v, stats, ntok, cu_seqlens=None,
+                       src_pos=None, tgt_pos=None, tgt_offset=None, dst_capacity=None,
+                       num_blocks=None, block_table=None, status=None) -> DiagArgs:
+        """Check tensors against the plan and pack a ``DiagArgs``."""
+        import torch
+        d = self.desc
+        Lt, H, hd = d.tgt_layers, d.tgt_kv_heads, d.tgt_head_dim
+        R = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+
+        def ptr(t, name, dtype, shape=None, ndim=None):
+            if t is None:
+                return None
+            if not isinstance(t, torch.Tensor) or not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor")
+            if t.dtype != dtype:
+                raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+            if shape is not None and tuple(t.shape) != tuple(shape):
+                raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+            if ndim is not None and t.dim() != ndim:
+                raise ValueError(f"{name} must have {ndim} dims")
+            return t.data_ptr()
+
+        a = DiagArgs()
+        a.ntok = int(ntok)
+        a.num_requests = R
+        a.cu_seqlens = ptr(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
+        a.src_pos = ptr(src_pos, "src_pos", torch.int32, (int(ntok),))
+        a.tgt_pos = ptr(tgt_pos, "tgt_pos", torch.int32, (int(ntok),))
+        a.tgt_offset = ptr(tgt_offset, "tgt_offset", torch.int32, (R,))
+        if d.dst_layout == KVX_CONTIGUOUS:
+            cap = int(dst_capacity) if dst_capacity is not None else ref_k.shape[1] // R
+            rows = R * cap
+            a.dst_capacity = cap
+        else:
+            nb = int(num_blocks) if num_blocks is not None else ref_k.shape[1] // d.block_size
+            rows = nb * d.block_size
+            a.num_blocks = nb
+            a.block_table = ptr(block_table, "block_table", torch.int32, ndim=2)
+            a.max_blocks_per_req = int(block_table.shape[1])
+        shape = (Lt, rows, H, hd)
+        a.mapped_k = ptr(mapped_k, "mapped_k", self.kv_dtype, shape)
+        a.mapped_v = ptr(mapped_v, "mapped_v", self.kv_dtype, shape)
+        a.ref_k = ptr(ref_k, "ref_k", self.kv_dtype, shape)
+        a.ref_v = ptr(ref_v, "ref_v", self.kv_dtype, shape)
+        a.stats = ptr(stats, "stats", torch.float64, (Lt, H, 2, hd + 4))
+        a.status = ptr(status, "status", torch.int32, (1,))
+        a._keep = (mapped_k, mapped_v, ref_k, ref_v, stats, cu_seqlens, src_pos, tgt_pos,
+                   tgt_offset, block_table, status)
+        return a
+
+    def kv_diagnostics(self, stream=None, **tensors) -> None:
+        """Enqueue the fidelity statistics [Lt][H][2][d + 4] (fp64, into
+        ``stats``) of a mapped cache against the target's own cache on
+        ``stream`` (default: torch's current stream)."""
+        import torch
+        args = self.make_diag_args(**tensors)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        st = kvx_kv_diagnostics(self.handle, args, ctypes.c_void_p(stream.cuda_stream))
+        if st != KVX_OK:
+            raise KvxError(st, "kvx_kv_diagnostics")

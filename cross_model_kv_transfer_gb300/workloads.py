@@ -237,6 +237,16 @@ def make_block_table(wl: Workload, seed: int) -> torch.Tensor:
     return table
 
 
+def perturbed_like(x: torch.Tensor, seed: int, scale: float = 0.3) -> torch.Tensor:
+    """A stand-in for the target model's own cache, to compare a mapped cache
+    against: 0.9 x plus seeded Gaussian noise of `scale` times the mean |x|
+    (entries that are NaN in x stay NaN), in x's dtype."""
+    g = _gen(x.device, seed)
+    noise = torch.randn(x.shape, generator=g, device=x.device, dtype=torch.float32)
+    xf = x.float()
+    return (0.9 * xf + scale * xf.abs().nanmean() * noise).to(x.dtype)
+
+
 def sentinel_like(shape, dtype, device="cpu") -> torch.Tensor:
     """A destination buffer filled with an all-ones bit pattern (a NaN in
     every float format), so untouched entries can be checked bit for bit."""

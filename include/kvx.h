@@ -215,6 +215,57 @@ int32_t kvx_plan_launches(const kvx_plan *plan);
  * plan, -1 for a NULL plan. */
 int32_t kvx_plan_cta_group(const kvx_plan *plan);
 
+/* Arguments of one fidelity-diagnostics call: a mapped cache (the output of a
+ * transfer) and the target model's own cache for the same tokens, in the
+ * plan's destination layout, plus the request table, positions and row
+ * rules of that transfer.  DEVICE pointers, as for kvx_transfer_args. */
+typedef struct {
+  const void *mapped_k;       /* [Lt][rows][H][d] mapped keys (kv dtype)      */
+  const void *mapped_v;       /* [Lt][rows][H][d] mapped values               */
+  const void *ref_k;          /* [Lt][rows][H][d] the target's own keys       */
+  const void *ref_v;          /* [Lt][rows][H][d] the target's own values     */
+  int64_t ntok;               /* source tokens of the transfer, >= 0          */
+  int32_t num_requests;       /* R >= 1                                       */
+  const int32_t *cu_seqlens;  /* [R+1] or NULL (R == 1), as for kvx_transfer  */
+  const int32_t *src_pos;     /* [ntok] or NULL, as for kvx_transfer          */
+  const int32_t *tgt_pos;     /* [ntok] or NULL                               */
+  const int32_t *tgt_offset;  /* [R] or NULL                                  */
+  int64_t dst_capacity;       /* CONTIGUOUS: rows per request                 */
+  int64_t num_blocks;         /* PAGED: blocks in the pool                    */
+  const int32_t *block_table; /* PAGED: [R][max_blocks_per_req]               */
+  int32_t max_blocks_per_req; /* PAGED                                        */
+  double *stats;              /* [Lt][H][2][d + 4] output, overwritten        */
+  uint32_t *status;           /* optional device word, KVX_FLAG_* OR-ed in    */
+} kvx_diag_args;
+
+/* Fidelity diagnostics of a transfer: how close the mapped cache is to the
+ * target model's own cache for the same tokens.  "Helm Intelligent Routing",
+ * section "Reading the retention score": the KV cosine between the mapped
+ * cache and the target's own is read beside retention as a diagnostic.
+ * "Перенос KV-кэша между моделями Qwen3 вместо повторного префилла", section
+ * "Линейного моста, как ни странно, хватает": the share of the target keys'
+ * and values' variance that the selected source layers explain.
+ *
+ * For each (target layer lt, head h, m), m = 0 keys and 1 values, the d + 4
+ * doubles at stats[((lt * H + h) * 2 + m) * (d + 4)] are set to
+ *   [0] n, the tokens compared;
+ *   [1] the sum over them of cos(mapped, ref) of the two d-vectors as stored
+ *       (0 for a token where either vector is zero);
+ *   [2] sum |ref - mapped|^2;   [3] sum |ref|^2;
+ *   [4 + i] sum of ref_i in content space (keys un-rotated at p' with the
+ *       target RoPE base, values as stored).
+ * Mean cosine = [1] / [0]; explained variance (centred R^2, summed over the
+ * d dimensions) = 1 - [2] / ([3] - |[4..]|^2 / [0]).  The tokens compared are
+ * the ones a transfer with the same arguments writes; rows it would skip are
+ * skipped with the same KVX_FLAG_* bits (a malformed request table: all stats
+ * 0 and KVX_FLAG_BAD_SEQLENS).  Sums are formed in fp32 per thread and
+ * combined in fp64; the order of the fp64 additions is not fixed.
+ * Asynchronous on `stream`, no allocation, two kernel launches (clear the
+ * stats, accumulate).  Returns KVX_ERR_INVALID_ARG for a NULL plan/args, a
+ * missing pointer or size, or a plan of another device; KVX_ERR_CUDA if a
+ * launch fails. */
+kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_args *args, void *stream);
+
 /* Allocation-free transfer.  The sources have no counterpart for this call:
  * it exists for callers that may not allocate device memory -- engines that
  * reserve nearly all of the GPU for their own paged KV-cache pool and forbid

@@ -17,7 +17,11 @@ What each function computes, and the passages it follows, is documented in
                   (same steps; the Qwen3 article's section on the linear
                   bridge for feature concatenation and the map).
 * ``dst_row``     contiguous / paged cache row of one token.
-* ``transfer``    the whole transfer over all requests, tokens, layers, heads.
+* ``transfer``    the whole transfer over all requests, tokens, layers, heads;
+                  ``wide=True`` for the wide-feature mapper (one dense map per
+                  target layer over all heads' keys and values of the
+                  selected layers: the Qwen3 article's mapper size, section
+                  on production limits); ``map_token_wide`` for one token.
 * ``ridge_fit``   centred ridge regression with intercept (the Qwen3
                   article's ridge demo).
 * ``kv_diagnostics`` KV cosine ("Helm Intelligent Routing", "Reading the
@@ -115,6 +119,13 @@ def _load():
             lib.kvxo_ridge_fit.argtypes = [dp, dp, ctypes.c_int64, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_double, dp, dp]
             lib.kvxo_ridge_fit.restype = ctypes.c_int
+            lib.kvxo_transfer_wide.argtypes = [ctypes.POINTER(_Problem), dp, dp]
+            lib.kvxo_transfer_wide.restype = ctypes.c_int
+            lib.kvxo_map_token_wide.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                ctypes.POINTER(dp), ctypes.POINTER(dp), dp, dp, ctypes.c_double,
+                ctypes.c_double, dp, dp]
+            lib.kvxo_map_token_wide.restype = None
             lib.kvxo_kv_diagnostics.argtypes = [ctypes.POINTER(_Problem), dp, dp, dp, dp, dp]
             lib.kvxo_kv_diagnostics.restype = ctypes.c_int
             _lib = lib
@@ -173,10 +184,13 @@ def dst_row(layout, r, p_tgt, dst_capacity=0, block_size=1, num_blocks=0,
 def transfer(*, src_k, src_v, layer_idx, w, b, theta_src, theta_tgt,
              max_position, cu_seqlens=None, src_pos=None, tgt_pos=None,
              tgt_offset=None, layout=CONTIGUOUS, dst_capacity=0,
-             block_size=1, num_blocks=0, block_table=None, dst_k=None, dst_v=None):
+             block_size=1, num_blocks=0, block_table=None, dst_k=None, dst_v=None,
+             wide=False):
     """The whole transfer in fp64.
 
-    src_k / src_v: [Ls][ntok][H][d]; layer_idx: [Lt][k]; w: [Lt][H][2][k*d][d];
+    src_k / src_v: [Ls][ntok][H][d]; layer_idx: [Lt][k]; w: [Lt][H][2][k*d][d]
+    (per-head maps) or, with ``wide``, [Lt][k*2*H*d][H*2*d] (one map per
+    target layer over all heads' keys and values, ``kvxo_transfer_wide``);
     b: [Lt][H][2][d].  dst_k / dst_v (optional, fp64) are the initial target
     cache [Lt][rows][H][d]; rows not written keep their values (NaN if the
     caller gives none).  Returns (dst_k, dst_v, status bits)."""
@@ -184,7 +198,10 @@ def transfer(*, src_k, src_v, layer_idx, w, b, theta_src, theta_tgt,
     Ls, ntok, H, d = src_k.shape
     idx = np.ascontiguousarray(layer_idx, dtype=np.int32)
     Lt, k = idx.shape
-    assert w.shape == (Lt, H, 2, k * d, d), w.shape
+    if wide:
+        assert w.shape == (Lt, k * 2 * H * d, H * 2 * d), w.shape
+    else:
+        assert w.shape == (Lt, H, 2, k * d, d), w.shape
     assert b.shape == (Lt, H, 2, d), b.shape
     cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int64)
     R = 1 if cu is None else cu.shape[0] - 1
@@ -212,8 +229,29 @@ def transfer(*, src_k, src_v, layer_idx, w, b, theta_src, theta_tgt,
                  int(max_position), R, ntok, _vp(cu), _vp(src_k), _vp(src_v),
                  _vp(idx), _vp(w), _vp(b), _vp(sp), _vp(tp), _vp(to), int(layout),
                  int(dst_capacity), int(block_size), int(num_blocks), int(mbpr), _vp(bt))
-    st = _load().kvxo_transfer(ctypes.byref(P), _dp(dst_k), _dp(dst_v))
+    fn = _load().kvxo_transfer_wide if wide else _load().kvxo_transfer
+    st = fn(ctypes.byref(P), _dp(dst_k), _dp(dst_v))
     return dst_k, dst_v, int(st)
+
+
+def map_token_wide(k_rows, v_rows, W, b, p_src, p_tgt, theta_src, theta_tgt):
+    """One token of one target layer with the wide-feature map.  k_rows /
+    v_rows: [k][H][d] (the selected source layers' head vectors, in
+    index-table order); W: [k*2*H*d][H*2*d]; b: [H][2][d].  Returns the
+    [H][d] key and value rows."""
+    k_rows, v_rows, W, b = _f64(k_rows), _f64(v_rows), _f64(W), _f64(b)
+    k, H, d = k_rows.shape
+    assert v_rows.shape == (k, H, d)
+    assert W.shape == (k * 2 * H * d, H * 2 * d) and b.shape == (H, 2, d)
+    dp = ctypes.POINTER(ctypes.c_double)
+    kptr = (dp * k)(*[_dp(k_rows[j]) for j in range(k)])
+    vptr = (dp * k)(*[_dp(v_rows[j]) for j in range(k)])
+    out_k = np.empty((H, d))
+    out_v = np.empty((H, d))
+    _load().kvxo_map_token_wide(H, d, k, float(theta_src), float(theta_tgt), kptr, vptr,
+                                _dp(W), _dp(b), float(p_src), float(p_tgt), _dp(out_k),
+                                _dp(out_v))
+    return out_k, out_v
 
 
 def ridge_fit(X, Y, lam: float = 0.01):

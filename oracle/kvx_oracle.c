@@ -180,6 +180,112 @@ int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
   return status;
 }
 
+/* Wide-feature mapper (definition in kvx_oracle.h): one dense map per
+ * target layer over all heads' keys and values of the selected layers. */
+void kvxo_map_token_wide(int H, int d, int k, double theta_src, double theta_tgt,
+                         const double *const *src_k_rows,
+                         const double *const *src_v_rows, const double *W,
+                         const double *b, double p_src, double p_tgt,
+                         double *out_k, double *out_v) {
+  int64_t F = (int64_t)k * 2 * H * d, N = (int64_t)H * 2 * d;
+  double *x = (double *)malloc(sizeof(double) * (size_t)F);
+  double *y = (double *)malloc(sizeof(double) * (size_t)N);
+
+  /* features in (j, m, h, i) order: un-rotated keys, then values as stored */
+  for (int j = 0; j < k; ++j)
+    for (int h = 0; h < H; ++h) {
+      kvxo_rope(src_k_rows[j] + (int64_t)h * d, d, p_src, theta_src, -1,
+                x + ((int64_t)(j * 2 + 0) * H + h) * d);
+      for (int i = 0; i < d; ++i)
+        x[((int64_t)(j * 2 + 1) * H + h) * d + i] = src_v_rows[j][(int64_t)h * d + i];
+    }
+  /* y = x W + b, summed in feature order */
+  for (int64_t n = 0; n < N; ++n) y[n] = b[n];
+  for (int64_t q = 0; q < F; ++q) {
+    const double *w_row = W + q * N;
+    for (int64_t n = 0; n < N; ++n) y[n] += x[q] * w_row[n];
+  }
+  /* outputs (h, m, i): keys re-rotated into the target position */
+  for (int h = 0; h < H; ++h) {
+    kvxo_rope(y + (int64_t)(h * 2 + 0) * d, d, p_tgt, theta_tgt, +1, out_k + (int64_t)h * d);
+    memcpy(out_v + (int64_t)h * d, y + (int64_t)(h * 2 + 1) * d, sizeof(double) * (size_t)d);
+  }
+  free(x);
+  free(y);
+}
+
+int kvxo_transfer_wide(const kvxo_problem *P, double *dst_k, double *dst_v) {
+  const int64_t Ls = P->src_layers, Lt = P->tgt_layers, H = P->kv_heads;
+  const int64_t d = P->head_dim, k = P->k, ntok = P->ntok;
+  const int64_t F = k * 2 * H * d, N = H * 2 * d;
+  const int64_t rows = P->layout == KVXO_CONTIGUOUS
+                           ? (int64_t)P->num_requests * P->dst_capacity
+                           : P->num_blocks * P->block_size;
+  int status = 0;
+
+  if (P->cu_seqlens) {
+    int ok = P->cu_seqlens[0] == 0 && P->cu_seqlens[P->num_requests] == ntok;
+    for (int64_t r = 0; r < P->num_requests; ++r)
+      if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;
+    if (!ok) return KVXO_BAD_SEQLENS;
+  }
+
+  const double **krows = (const double **)malloc(sizeof(double *) * (size_t)k);
+  const double **vrows = (const double **)malloc(sizeof(double *) * (size_t)k);
+  double *ok = (double *)malloc(sizeof(double) * (size_t)(H * d));
+  double *ov = (double *)malloc(sizeof(double) * (size_t)(H * d));
+  char *layer_ok = (char *)malloc((size_t)Lt);
+  for (int64_t lt = 0; lt < Lt; ++lt) {
+    layer_ok[lt] = 1;
+    for (int64_t j = 0; j < k; ++j) {
+      int32_t s = P->layer_idx[lt * k + j];
+      if (s < 0 || s >= Ls) layer_ok[lt] = 0;
+    }
+    if (!layer_ok[lt]) status |= KVXO_BAD_LAYER_INDEX;
+  }
+
+  for (int64_t r = 0; r < P->num_requests; ++r) {
+    int64_t beg = P->cu_seqlens ? P->cu_seqlens[r] : 0;
+    int64_t end = P->cu_seqlens ? P->cu_seqlens[r + 1] : ntok;
+    for (int64_t g = beg; g < end; ++g) {
+      int64_t p = P->src_pos ? P->src_pos[g] : g - beg;
+      int64_t off = P->tgt_offset ? P->tgt_offset[r] : 0;
+      int64_t pt = P->tgt_pos ? P->tgt_pos[g] : p + off;
+      if (p < 0 || p >= P->max_position || pt < 0 || pt >= P->max_position) {
+        status |= KVXO_BAD_POSITION;
+        continue;
+      }
+      int bad = 0;
+      int64_t row = kvxo_dst_row(P->layout, r, pt, P->dst_capacity,
+                                 P->block_size, P->num_blocks, P->block_table,
+                                 P->max_blocks_per_req, &bad);
+      if (row < 0) {
+        status |= bad;
+        continue;
+      }
+      for (int64_t lt = 0; lt < Lt; ++lt) {
+        if (!layer_ok[lt]) continue;
+        for (int64_t j = 0; j < k; ++j) {
+          int64_t s = P->layer_idx[lt * k + j];
+          krows[j] = P->src_k + (s * ntok + g) * H * d;
+          vrows[j] = P->src_v + (s * ntok + g) * H * d;
+        }
+        kvxo_map_token_wide((int)H, (int)d, (int)k, P->theta_src, P->theta_tgt,
+                            krows, vrows, P->w + lt * F * N, P->b + lt * N,
+                            (double)p, (double)pt, ok, ov);
+        memcpy(dst_k + (lt * rows + row) * H * d, ok, sizeof(double) * (size_t)(H * d));
+        memcpy(dst_v + (lt * rows + row) * H * d, ov, sizeof(double) * (size_t)(H * d));
+      }
+    }
+  }
+  free(layer_ok);
+  free(krows);
+  free(vrows);
+  free(ok);
+  free(ov);
+  return status;
+}
+
 /* KV cosine of [HIR] ("Reading the retention score") and explained variance
  * of [QKV] ("Линейного моста, как ни странно, хватает"), accumulated over
  * the tokens a transfer writes; definitions in kvx_oracle.h. */

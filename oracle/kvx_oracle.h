@@ -117,6 +117,36 @@ typedef struct {
  * written keep their contents.  Returns the OR of KVXO_BAD_* bits. */
 int kvxo_transfer(const kvxo_problem *prob, double *dst_k, double *dst_v);
 
+/* Wide-feature mapper: the reading of the 14B -> 32B mapper size in [QKV]
+ * section "Ограничения, важные в продакшене" (about 1.07e9 parameters, 4 GB
+ * per direction, which is 2^30 = Lt * F * N fp32 weights for Lt = 64,
+ * F = 8192, N = 2048): every target layer maps ALL heads' keys and values
+ * of its k selected source layers to all its heads' keys and values with
+ * one dense map.  Per token and target layer lt:
+ *   x (width F = k * 2 * H * d), feature (j, m, h, i) at
+ *     ((j * 2 + m) * H + h) * d + i:  m = 0 the key of source layer
+ *     idx[lt][j], head h, un-rotated at p (theta_src); m = 1 that layer's
+ *     value of head h as stored;
+ *   y = x W[lt] + b[lt], W[lt] [F][N] row-major, N = H * 2 * d, output
+ *     (h, m, i) at (h * 2 + m) * d + i, i.e. b keeps the per-head layout
+ *     [Lt][H][2][d];
+ *   key outputs (m = 0) re-rotated at p' (theta_tgt), then installed as in
+ *     kvxo_transfer.
+ * Each output element is summed as b[n] + x[0] W[0][n] + x[1] W[1][n] + ...
+ * in feature order.  With W[lt] zero outside the blocks (h, m) -> (h, m) it
+ * is the per-head transfer (same sums, same order).
+ * src_k_rows[j] / src_v_rows[j] point at the [H][d] head vectors of the
+ * j-th selected source layer; out_k / out_v are [H][d]. */
+void kvxo_map_token_wide(int H, int d, int k, double theta_src, double theta_tgt,
+                         const double *const *src_k_rows,
+                         const double *const *src_v_rows, const double *W,
+                         const double *b, double p_src, double p_tgt,
+                         double *out_k, double *out_v);
+
+/* Whole wide-feature transfer: as kvxo_transfer with prob->w read as
+ * [Lt][k * 2 * H * d][H * 2 * d]. */
+int kvxo_transfer_wide(const kvxo_problem *prob, double *dst_k, double *dst_v);
+
 /* Fidelity diagnostics of a transfer: how close the mapped cache is to the
  * target model's own cache for the same tokens.
  *  [HIR] section "Reading the retention score": "KV cosine" -- the closeness

@@ -38,7 +38,8 @@ def test_library_exports_every_declared_symbol():
 
 def test_ctypes_structs_match_the_c_layout(tmp_path):
     # Compile a probe against include/kvx.h that prints sizes and offsets.
-    fields = {"kvx_plan_desc": kvx.PlanDesc, "kvx_transfer_args": kvx.TransferArgs}
+    fields = {"kvx_plan_desc": kvx.PlanDesc, "kvx_transfer_args": kvx.TransferArgs,
+              "kvx_diag_args": kvx.DiagArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kvx.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -109,6 +110,8 @@ def test_transfer_and_destroy_reject_null():
     assert kvx.kvx_plan_destroy(None) == kvx.KVX_OK
     assert kvx.kvx_plan_kernel(None) == -1
     assert kvx.kvx_plan_launches(None) == -1
+    assert kvx.kvx_kv_diagnostics(None, kvx.DiagArgs(), None) == kvx.KVX_ERR_INVALID_ARG
+    assert kvx.load().kvx_kv_diagnostics(None, None, None) == kvx.KVX_ERR_INVALID_ARG
 
 
 def test_status_strings():

@@ -84,3 +84,28 @@ def test_full_size_sampled_rows_match_oracle(name):
         bits = dst.view(torch.int16)
         assert bool((bits[:, ~written] == -1).all())
         assert not bool((bits[:, written] == -1).all(dim=-1).any())
+
+
+def test_full_size_diagnostics_match_oracle_on_first_and_last_layer():
+    # the fidelity diagnostics at the 14B -> 32B shape, 32,768 tokens, in the
+    # launch configuration the benchmark times (all 64 target layers); the
+    # oracle recomputes target layers 0 and 63 over every token
+    from cross_model_kv_transfer_gb300.workloads import perturbed_like
+    from test_gpu_diagnostics import assert_stats_close, run_gpu_diag
+
+    wl = WORKLOADS["qwen3_14b_32b"]
+    inp = make_inputs(wl, "cuda")
+    mk, mv, st, plan = run_gpu(wl, inp)
+    assert st == 0
+    del inp
+    rk, rv = perturbed_like(mk, 101), perturbed_like(mv, 102)
+    g, st = run_gpu_diag(plan, mk, mv, rk, rv, ntok=wl.ntok, dst_capacity=wl.dst_capacity)
+    assert st == 0
+    layers = [0, wl.tgt_layers - 1]
+    f64 = lambda t: t[layers].cpu().to(torch.float64).numpy()
+    r, rst = oracle.kv_diagnostics(mapped_k=f64(mk), mapped_v=f64(mv), ref_k=f64(rk),
+                                   ref_v=f64(rv), theta_tgt=wl.theta_tgt,
+                                   max_position=wl.max_position, ntok=wl.ntok,
+                                   dst_capacity=wl.dst_capacity)
+    assert rst == 0
+    assert_stats_close(g[layers], r)
