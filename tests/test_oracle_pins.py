@@ -658,3 +658,200 @@ def test_kv_diagnostics_skips_what_a_transfer_skips():
     s, st = _diag(rk3, rk3, rk3, rk3, ntok=5, dst_capacity=5, cu_seqlens=[0, 3, 2, 5])
     assert st == oracle.BAD_SEQLENS
     assert np.all(s == 0)
+
+
+# --------------------------------------------------------------------------
+# Wide-feature mapper (Qwen3 article, production-limits section: a 14B ->
+# 32B mapper of about 1.07e9 parameters = 64 target layers x 8192 features
+# x 2048 outputs, i.e. all heads' keys and values of the selected layers
+# feed every head's key and value map)
+# --------------------------------------------------------------------------
+
+def _wide_case(rng, Ls=4, Lt=3, H=3, d=8, k=2, lens=(5, 9), offs=(0, 3)):
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    src_k = rng.standard_normal((Ls, T, H, d))
+    src_v = rng.standard_normal((Ls, T, H, d))
+    idx = np.stack([rng.permutation(Ls)[:k] for _ in range(Lt)]).astype(np.int32)
+    cap = max(n + o for n, o in zip(lens, offs))
+    kw = dict(theta_src=1e4, theta_tgt=5e5, max_position=cap, cu_seqlens=cu, tgt_offset=offs,
+              dst_capacity=cap)
+    return src_k, src_v, idx, kw
+
+
+def _wide_from_per_head(w_head, k, H, d):
+    """The wide map that is block-diagonal over (head, K|V): feature
+    (j, m, h, i) feeds output (h, m, i') through w_head[h][m][j*d + i][i']."""
+    Lt = w_head.shape[0]
+    F, N = k * 2 * H * d, H * 2 * d
+    W = np.zeros((Lt, F, N))
+    for lt in range(Lt):
+        for j in range(k):
+            for m in range(2):
+                for h in range(H):
+                    q0 = ((j * 2 + m) * H + h) * d
+                    n0 = (h * 2 + m) * d
+                    W[lt, q0:q0 + d, n0:n0 + d] = w_head[lt, h, m, j * d:(j + 1) * d]
+    return W
+
+
+def test_wide_block_diagonal_map_is_the_per_head_transfer_bit_for_bit():
+    # Zero weights add exact zeros and the non-zero terms are summed in the
+    # same (j, i) order, so the two oracles give the same bits.
+    rng = np.random.default_rng(31)
+    src_k, src_v, idx, kw = _wide_case(rng)
+    Lt, k = idx.shape
+    H, d = src_k.shape[2], src_k.shape[3]
+    w_head = rng.standard_normal((Lt, H, 2, k * d, d))
+    b = rng.standard_normal((Lt, H, 2, d))
+    hk, hv, hst = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=w_head, b=b, **kw)
+    wk, wv, wst = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx,
+                                  w=_wide_from_per_head(w_head, k, H, d), b=b, wide=True, **kw)
+    assert hst == wst == 0
+    assert np.array_equal(np.isnan(hk), np.isnan(wk))
+    written = ~np.isnan(hk)
+    assert np.array_equal(hk[written], wk[written]) and np.array_equal(hv[written], wv[written])
+
+
+def test_wide_selection_routes_across_heads_and_kinds():
+    # Every output (h, m, i) copies one feature chosen at random from the
+    # whole width (any selected layer, head, key or value).  Keys are stored
+    # as integer content rotated at p, so the expected features are written
+    # down here from the documented order without the oracle's gather:
+    # feature (j, m, h, i) = content key (m = 0) or value (m = 1) of source
+    # layer idx[lt][j], head h, dim i.  Key outputs come back re-rotated.
+    rng = np.random.default_rng(41)
+    Ls, Lt, H, d, k, T = 4, 2, 3, 6, 2, 5
+    th_s, th_t = 1e4, 1e6
+    content = rng.integers(-50, 50, size=(Ls, T, H, d)).astype(np.float64)
+    vals = rng.integers(-50, 50, size=(Ls, T, H, d)).astype(np.float64)
+    src_k = np.empty_like(content)
+    for s in range(Ls):
+        for t in range(T):
+            for h in range(H):
+                src_k[s, t, h] = oracle.rope(content[s, t, h], t, th_s, +1)
+    idx = np.array([[2, 0], [1, 3]], dtype=np.int32)
+    F, N = k * 2 * H * d, H * 2 * d
+    pick = rng.integers(0, F, size=(Lt, N))
+    W = np.zeros((Lt, F, N))
+    for lt in range(Lt):
+        W[lt, pick[lt], np.arange(N)] = 1.0
+    b = np.zeros((Lt, H, 2, d))
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=vals, layer_idx=idx, w=W, b=b,
+                                 theta_src=th_s, theta_tgt=th_t, max_position=T,
+                                 dst_capacity=T, wide=True)
+    assert st == 0
+    for lt in range(Lt):
+        for t in range(T):
+            feat = np.empty(F)
+            for q in range(F):
+                j, rest = divmod(q, 2 * H * d)
+                m, rest = divmod(rest, H * d)
+                h, i = divmod(rest, d)
+                s = idx[lt, j]
+                feat[q] = (content if m == 0 else vals)[s, t, h, i]
+            y = feat[pick[lt]].reshape(H, 2, d)
+            for h in range(H):
+                np.testing.assert_allclose(dv[lt, t, h], y[h, 1], rtol=0, atol=1e-12)
+                np.testing.assert_allclose(dk[lt, t, h], oracle.rope(y[h, 0], t, th_t, +1),
+                                           rtol=0, atol=1e-11)
+
+
+def test_wide_brute_force_numpy_phasors():
+    # An independent formulation: RoPE as complex phasors on (x_i + j x_{i+d/2}),
+    # the map as one matmul over the stacked features, the cache rows by a
+    # vectorised paged lookup.
+    rng = np.random.default_rng(53)
+    lens, offs, bs = [6, 11], [3, 0], 4
+    Ls, Lt, H, d, k = 5, 2, 2, 8, 3
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    nb = [(n + o + bs - 1) // bs for n, o in zip(lens, offs)]
+    pool = sum(nb)
+    perm = rng.permutation(pool).astype(np.int32)
+    table = np.full((2, max(nb)), -1, dtype=np.int32)
+    table[0, :nb[0]], table[1, :nb[1]] = perm[:nb[0]], perm[nb[0]:]
+    src_k = rng.standard_normal((Ls, T, H, d))
+    src_v = rng.standard_normal((Ls, T, H, d))
+    idx = np.stack([rng.permutation(Ls)[:k] for _ in range(Lt)]).astype(np.int32)
+    F, N = k * 2 * H * d, H * 2 * d
+    W = rng.standard_normal((Lt, F, N)) / math.sqrt(F)
+    b = rng.standard_normal((Lt, H, 2, d))
+    th_s, th_t = 1e4, 5e5
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=W, b=b,
+                                 theta_src=th_s, theta_tgt=th_t, max_position=20,
+                                 cu_seqlens=cu, tgt_offset=offs, layout=oracle.PAGED,
+                                 block_size=bs, num_blocks=pool, block_table=table, wide=True)
+    assert st == 0
+    half = d // 2
+    req = np.searchsorted(cu, np.arange(T), side="right") - 1
+    p = np.arange(T) - cu[req]
+    pt = p + np.asarray(offs)[req]
+    row = table[req, pt // bs] * bs + pt % bs
+
+    def phasor(theta, pos):
+        w = theta ** (-2.0 * np.arange(half) / d)
+        return np.exp(1j * np.outer(pos, w))                          # [T][half]
+
+    ck = src_k[..., :half] + 1j * src_k[..., half:]                  # [Ls][T][H][half]
+    ck = ck * np.conj(phasor(th_s, p))[None, :, None, :]
+    content = np.concatenate([ck.real, ck.imag], axis=-1)             # [Ls][T][H][d]
+    for lt in range(Lt):
+        X = np.stack([np.stack([content[idx[lt, j]], src_v[idx[lt, j]]], axis=1)
+                      for j in range(k)], axis=1)                     # [T][k][2][H][d]
+        Y = X.reshape(T, F) @ W[lt] + b[lt].reshape(N)                # [T][N]
+        Y = Y.reshape(T, H, 2, d)
+        yk = Y[:, :, 0, :half] + 1j * Y[:, :, 0, half:]
+        yk = yk * phasor(th_t, pt)[:, None, :]
+        np.testing.assert_allclose(dk[lt, row], np.concatenate([yk.real, yk.imag], -1),
+                                   rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dv[lt, row], Y[:, :, 1], rtol=1e-12, atol=1e-12)
+    untouched = np.ones(pool * bs, dtype=bool)
+    untouched[row] = False
+    assert np.isnan(dk[:, untouched]).all() and np.isnan(dv[:, untouched]).all()
+
+
+def test_wide_bias_only_and_skip_rules():
+    # W = 0: values are b, keys are b rotated to p' (closed form); a bad
+    # layer index skips its target layer, a position past the table its token
+    rng = np.random.default_rng(61)
+    src_k, src_v, idx, kw = _wide_case(rng, Lt=3)
+    Lt, k = idx.shape
+    H, d = src_k.shape[2], src_k.shape[3]
+    b = rng.standard_normal((Lt, H, 2, d))
+    W = np.zeros((Lt, k * 2 * H * d, H * 2 * d))
+    idx = idx.copy()
+    idx[1, 0] = 99
+    kw = dict(kw, max_position=kw["max_position"] - 1)
+    dk, dv, st = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=W, b=b, wide=True,
+                                 **kw)
+    assert st == oracle.BAD_LAYER_INDEX | oracle.BAD_POSITION
+    assert np.isnan(dk[1]).all() and np.isnan(dv[1]).all()
+    # request 1 (9 tokens, offset 3): p' = 3 .. 11, the last one is past the table
+    cap = kw["dst_capacity"]
+    for lt in (0, 2):
+        for pt in range(3, 11):
+            row = cap + pt
+            for h in range(H):
+                assert np.array_equal(dv[lt, row, h], b[lt, h, 1])
+                z = b[lt, h, 0, :d // 2] + 1j * b[lt, h, 0, d // 2:]
+                z = z * np.exp(1j * pt * 5e5 ** (-2.0 * np.arange(d // 2) / d))
+                np.testing.assert_allclose(dk[lt, row, h], np.concatenate([z.real, z.imag]),
+                                           rtol=0, atol=1e-13)
+        assert np.isnan(dk[lt, cap + 11]).all()
+
+
+def test_map_token_wide_matches_transfer_row():
+    rng = np.random.default_rng(71)
+    src_k, src_v, idx, kw = _wide_case(rng, lens=(7,), offs=(2,))
+    Lt, k = idx.shape
+    H, d = src_k.shape[2], src_k.shape[3]
+    W = rng.standard_normal((Lt, k * 2 * H * d, H * 2 * d))
+    b = rng.standard_normal((Lt, H, 2, d))
+    dk, dv, _ = oracle.transfer(src_k=src_k, src_v=src_v, layer_idx=idx, w=W, b=b, wide=True,
+                                **kw)
+    for lt in range(Lt):
+        for t in range(7):
+            ok, ov = oracle.map_token_wide(src_k[idx[lt], t], src_v[idx[lt], t], W[lt], b[lt],
+                                           t, t + 2, kw["theta_src"], kw["theta_tgt"])
+            assert np.array_equal(ok, dk[lt, t + 2]) and np.array_equal(ov, dv[lt, t + 2])
