@@ -31,12 +31,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KV-transfer tokens/s at 14B→32B shape, 32K tokens; % of HBM/tensor roofline"
+WIDE_METRIC = ("KV-transfer tokens/s at 14B→32B shape, 32K tokens, wide-feature mapper "
+               "(one 8192x2048 map per target layer, 1.07e9 parameters); % of tensor roofline")
 # Published context for this exact workload: the Qwen3 14B -> 32B mapper at
 # 32,768 tokens took 277.6 ms on an 8xH100 node (Qwen3 KV-transfer article,
 # section on what the headline number covers).
 PUBLISHED_MS = {"qwen3_14b_32b": 277.6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu", "diag": "kvx_diag.cu"}
+KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu", "diag": "kvx_diag.cu",
+                "wide": "kvx_wide.cu"}
 
 
 def parse_args(argv=None):
@@ -50,6 +53,10 @@ def parse_args(argv=None):
                          "mapped cache against the target's own")
     ap.add_argument("--workload", default="qwen3_14b_32b")
     ap.add_argument("--kernel", choices=["auto", "simt", "tcgen05"], default="auto")
+    ap.add_argument("--mapper", choices=["per_head", "wide"], default="per_head",
+                    help="per_head: one [k*d x d] map per (target layer, head, K|V); wide: one "
+                         "[k*2*H*d x H*2*d] map per target layer (the 1.07e9-parameter "
+                         "14B->32B mapper)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (profiling of small cases)")
     ap.add_argument("--tiles-per-item", type=int, default=0)
@@ -212,14 +219,14 @@ def measured_traffic(workload: str, kernel_name: str):
     return None
 
 
-def roofline(wl, layer_idx, ms_per_launch, kernel_name, peaks, peak_kind):
-    alg_bytes = wl.algorithmic_bytes(layer_idx)
-    flops = wl.algorithmic_flops()
+def roofline(wl, layer_idx, ms_per_launch, kernel_name, peaks, peak_kind, wide=False):
+    alg_bytes = wl.wide_algorithmic_bytes(layer_idx) if wide else wl.algorithmic_bytes(layer_idx)
+    flops = wl.wide_algorithmic_flops() if wide else wl.algorithmic_flops()
     s = ms_per_launch / 1e3
     t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks["bf16_tflops"] * 1e12)
     traffic = measured_traffic(wl.name, kernel_name)
-    if kernel_name == "tcgen05" and t_tc >= t_hbm:
+    if kernel_name in ("tcgen05", "wide") and t_tc >= t_hbm:
         r = {"bound": "tensor", "achieved": flops / s / 1e12, "peak": peaks["bf16_tflops"],
              "unit": "TFLOP/s"}
     else:
@@ -240,29 +247,35 @@ def roofline(wl, layer_idx, ms_per_launch, kernel_name, peaks, peak_kind):
 # CPU oracle on a bounded sample
 # --------------------------------------------------------------------------
 
-def oracle_sample_inputs(wl, inp, ntok_sample: int):
-    """fp64 copies of the first ``ntok_sample`` source tokens (one request)."""
+def oracle_sample_inputs(wl, inp, ntok_sample: int, layers=None, wide=False):
+    """fp64 copies of the first ``ntok_sample`` source tokens (one request),
+    for the first ``layers`` target layers (all by default)."""
     import torch
     f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
+    L = wl.tgt_layers if layers is None else layers
     return dict(src_k=f64(inp["src_k"][:, :ntok_sample]), src_v=f64(inp["src_v"][:, :ntok_sample]),
-                layer_idx=inp["layer_idx"].cpu().numpy(), w=f64(inp["w"]), b=f64(inp["b"]),
-                theta_src=wl.theta_src, theta_tgt=wl.theta_tgt, max_position=ntok_sample,
-                dst_capacity=ntok_sample)
+                layer_idx=inp["layer_idx"][:L].cpu().numpy(), w=f64(inp["w"][:L]),
+                b=f64(inp["b"][:L]), theta_src=wl.theta_src, theta_tgt=wl.theta_tgt,
+                max_position=ntok_sample, dst_capacity=ntok_sample, wide=wide)
 
 
-def time_oracle(wl, inp, target_seconds: float):
-    """Tokens/s of the fp64 oracle (one host thread) on a bounded sample."""
+def time_oracle(wl, inp, target_seconds: float, wide=False):
+    """Tokens/s of the fp64 oracle (one host thread) on a bounded sample:
+    the first n tokens through the first L target layers, scaled to all Lt
+    (the work is linear in the target layers).  Returns (tokens/s, n, L,
+    seconds)."""
     import oracle
-    probe = oracle_sample_inputs(wl, inp, 1)
+    L = min(wl.tgt_layers, 2) if wide else wl.tgt_layers
+    probe = oracle_sample_inputs(wl, inp, 1, L, wide)
     t0 = time.perf_counter()
     oracle.transfer(**probe)
     per_tok = max(time.perf_counter() - t0, 1e-4)
     n = int(max(1, min(wl.ntok, target_seconds / per_tok)))
-    sample = oracle_sample_inputs(wl, inp, n)
+    sample = oracle_sample_inputs(wl, inp, n, L, wide)
     t0 = time.perf_counter()
     oracle.transfer(**sample)
     el = time.perf_counter() - t0
-    return n / el, n, el
+    return n / (el * wl.tgt_layers / L), n, L, el
 
 
 # --------------------------------------------------------------------------
@@ -303,14 +316,21 @@ def run_kvx(args):
     if args.tokens:
         wl = wl.with_tokens([args.tokens], [wl.tgt_offsets[0]], name=f"{wl.name}@{args.tokens}")
     inp = make_inputs(wl, dev)
+    wide = args.mapper == "wide"
+    if wide:
+        from cross_model_kv_transfer_gb300.workloads import make_wide_weights
+        inp["w"] = make_wide_weights(wl, dev)
     plan = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers, kv_heads=wl.kv_heads,
                     head_dim=wl.head_dim, k=wl.k, rope_theta_src=wl.theta_src,
                     rope_theta_tgt=wl.theta_tgt, max_position=wl.max_position,
                     kv_dtype=wl.kv_dtype, w_dtype=torch.float32, b_dtype=wl.b_dtype,
                     layout=wl.layout, block_size=wl.block_size if wl.layout == PAGED else 0,
                     kernel=kernel_code(args.kernel), tiles_per_item=args.tiles_per_item,
-                    flags=kvx.KVX_PLAN_TC_SINGLE_CTA if args.single_cta else 0)
-    kname = {kvx.KVX_KERNEL_SIMT: "simt", kvx.KVX_KERNEL_TCGEN05: "tcgen05"}[plan.kernel]
+                    flags=kvx.KVX_PLAN_TC_SINGLE_CTA if args.single_cta else 0,
+                    mapper=kvx.KVX_MAPPER_WIDE if wide else kvx.KVX_MAPPER_PER_HEAD,
+                    max_tokens=wl.ntok if wide else 0)
+    kname = "wide" if wide else \
+        {kvx.KVX_KERNEL_SIMT: "simt", kvx.KVX_KERNEL_TCGEN05: "tcgen05"}[plan.kernel]
     shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
     dst_k = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
     dst_v = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
@@ -319,6 +339,8 @@ def run_kvx(args):
     stream = torch.cuda.current_stream(dev)
     sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
     if args.op == "kv_diagnostics":
+        if wide:
+            raise SystemExit("kv_diagnostics bench: per-head mapper only")
         if wl.layout != PAGED and any(wl.tgt_offsets):
             raise SystemExit("kv_diagnostics bench: contiguous workloads with offset 0 only")
         run_diag(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, ws, rank)
@@ -350,7 +372,7 @@ def run_kvx(args):
     value, ms = aggregate(wl.ntok, ms_local, dev)
 
     peaks, peak_kind = load_peaks()
-    roof = roofline(wl, inp["layer_idx"], ms_local, kname, peaks, peak_kind)
+    roof = roofline(wl, inp["layer_idx"], ms_local, kname, peaks, peak_kind, wide=wide)
 
     e2e = None
     if not args.no_e2e:
@@ -358,14 +380,17 @@ def run_kvx(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tps, n, el = time_oracle(wl, inp, args.cpu_seconds)
+        tps, n, L, el = time_oracle(wl, inp, args.cpu_seconds, wide=wide)
+        scaled = "" if L == wl.tgt_layers else \
+            f", timed on the first {L} target layers and scaled to all {wl.tgt_layers}"
         cpu = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {n} source tokens of the workload through all "
-                         f"{wl.tgt_layers} target layers x {wl.kv_heads} heads x K|V "
-                         f"({el:.1f} s of fp64 CPU work, one thread)"}
+               "sample": f"first {n} source tokens of the workload through "
+                         f"{L} target layers x {wl.kv_heads} heads x K|V "
+                         f"({el:.1f} s of fp64 CPU work, one thread{scaled})"}
     pub = PUBLISHED_MS.get(wl.name)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "metric": WIDE_METRIC if wide else METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / (wl.ntok / (pub / 1e3))) if pub else None,
@@ -377,6 +402,7 @@ def run_kvx(args):
                    "requests": wl.num_requests,
                    "layout": "paged" if wl.layout == PAGED else "contiguous",
                    "kernel": kname, "cta_group": plan.cta_group,
+                   "mapper": args.mapper,
                    "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (source "
                          f"{inp['src_k'].numel() * 2 * inp['src_k'].element_size() / 1e9:.2f} GB,"

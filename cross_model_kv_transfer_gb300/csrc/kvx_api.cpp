@@ -36,6 +36,8 @@ kvx_status validate_desc(const kvx_plan_desc *d) {
     return KVX_ERR_INVALID_ARG;
   if (d->tiles_per_item < 0 || d->tiles_per_item > 4096) return KVX_ERR_INVALID_ARG;
   if (d->flags & ~(KVX_PLAN_TEST_STALL | KVX_PLAN_TC_SINGLE_CTA)) return KVX_ERR_INVALID_ARG;
+  if (d->mapper != KVX_MAPPER_PER_HEAD && d->mapper != KVX_MAPPER_WIDE) return KVX_ERR_INVALID_ARG;
+  if (d->max_tokens < 0) return KVX_ERR_INVALID_ARG;
   // "Requirements": same number of KV heads and the same per-head dimension.
   if (d->src_kv_heads != d->tgt_kv_heads || d->src_head_dim != d->tgt_head_dim)
     return KVX_ERR_PAIR_MISMATCH;
@@ -190,10 +192,16 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   kvx_status st = validate_desc(desc);
   if (st != KVX_OK) return st;
 
+  const bool wide = desc->mapper == KVX_MAPPER_WIDE;
   int kernel = desc->kernel;
+  if (wide) {
+    // the wide map runs only as the tensor-core contraction
+    if (kernel == KVX_KERNEL_SIMT || !kvx_wide_supports(*desc)) return KVX_ERR_UNSUPPORTED;
+    kernel = KVX_KERNEL_TCGEN05;
+  }
   if (kernel == KVX_KERNEL_AUTO)
     kernel = kvx_tc_supports(*desc) ? KVX_KERNEL_TCGEN05 : KVX_KERNEL_SIMT;
-  if (kernel == KVX_KERNEL_TCGEN05 && !kvx_tc_supports(*desc)) return KVX_ERR_UNSUPPORTED;
+  if (!wide && kernel == KVX_KERNEL_TCGEN05 && !kvx_tc_supports(*desc)) return KVX_ERR_UNSUPPORTED;
   if (kernel == KVX_KERNEL_SIMT && !kvx_simt_supports(*desc)) return KVX_ERR_UNSUPPORTED;
 
   int ndev = 0;
@@ -217,7 +225,10 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   p->tiles_per_item = desc->tiles_per_item > 0 ? desc->tiles_per_item : 32;
   p->stall_test = (desc->flags & KVX_PLAN_TEST_STALL) ? 1 : 0;
 
-  if (kernel == KVX_KERNEL_SIMT) {
+  p->max_tokens = desc->max_tokens > 0 ? desc->max_tokens : desc->max_position;
+  if (wide) {
+    // no RoPE tables: both bases are evaluated from fixed-point phases
+  } else if (kernel == KVX_KERNEL_SIMT) {
     // fp32 tables from fp64 host trigonometry (the fp32 path's 1e-5 budget)
     st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
                 &p->rope_src);
@@ -236,14 +247,18 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   // target frequencies in turns: the tensor-core epilogue and the
   // diagnostics kernel (any plan) evaluate target RoPE angles from them
   rope_turns(desc->rope_theta_tgt, desc->tgt_head_dim, p->turns_tgt);
+  rope_turns(desc->rope_theta_src, desc->src_head_dim, p->turns_src);
   if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05) {
     p->encode_tiled = kvx_tc_encoder();
-    st = p->encode_tiled ? alloc_workspace(p, kvx_tc_workspace_bytes(*desc))
-                         : KVX_ERR_UNSUPPORTED;
+    st = !p->encode_tiled ? KVX_ERR_UNSUPPORTED
+         : alloc_workspace(p, wide ? kvx_wide_workspace_bytes(*desc, p->max_tokens)
+                                   : kvx_tc_workspace_bytes(*desc));
   }
   if (st == KVX_OK) {
-    cudaError_t e = kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_prepare(p) : kvx_simt_prepare(p);
-    if (e != cudaSuccess) st = KVX_ERR_CUDA;
+    cudaError_t e = wide ? kvx_wide_prepare(p)
+                         : kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_prepare(p) : kvx_simt_prepare(p);
+    if (e == cudaErrorNotSupported) st = KVX_ERR_UNSUPPORTED;
+    else if (e != cudaSuccess) st = KVX_ERR_CUDA;
   }
   if (st != KVX_OK) {
     free_tables(p);
@@ -272,6 +287,7 @@ int32_t kvx_plan_kernel(const kvx_plan *plan) { return plan ? plan->kernel : -1;
 
 int32_t kvx_plan_launches(const kvx_plan *plan) {
   if (!plan) return -1;
+  if (plan->desc.mapper == KVX_MAPPER_WIDE) return 3;  // un-rotated keys, W image, map
   return plan->kernel == KVX_KERNEL_TCGEN05 ? 2 : 1;  // W image + transfer, or transfer
 }
 
@@ -304,6 +320,8 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return KVX_ERR_CUDA;
   if (cur != plan->device) return KVX_ERR_INVALID_ARG;
+  const bool wide = d.mapper == KVX_MAPPER_WIDE;
+  if (wide && a->ntok > plan->max_tokens) return KVX_ERR_INVALID_ARG;
   if (a->ntok == 0) return KVX_OK;  // nothing to transfer; status untouched
 
   KvxParams p;
@@ -341,8 +359,9 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   p.max_position = d.max_position;
 
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = plan->kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_launch(plan, p, s)
-                                                     : kvx_simt_launch(plan, p, s);
+  cudaError_t e = wide ? kvx_wide_launch(plan, p, s)
+                  : plan->kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_launch(plan, p, s)
+                                                       : kvx_simt_launch(plan, p, s);
   return e == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }
 

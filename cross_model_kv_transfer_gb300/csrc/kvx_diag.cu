@@ -28,6 +28,7 @@
 
 #include "kvx_device.cuh"
 #include "kvx_internal.h"
+#include "kvx_ptx.cuh"
 
 namespace {
 
@@ -46,17 +47,6 @@ struct DiagParams {
   int32_t slot_groups;           // CTAs per (layer, chunk) along the lanes
   unsigned long long turns[128]; // target RoPE frequencies, 2^-64 turns
 };
-
-// Target RoPE (cos, sin) at position pos from the exact 64-bit fixed-point
-// phase pos * F mod 2^64 (F = w_i / 2pi in units of 2^-64 turns); its top 32
-// bits give the angle in [-pi, pi).
-__device__ __forceinline__ void phase_cs(uint32_t pos, unsigned long long turns, float &c,
-                                         float &s) {
-  const uint32_t hi = (uint32_t)(turns >> 32), lo = (uint32_t)turns;
-  const uint32_t top = __umulhi(pos, lo) + pos * hi;
-  const float a = (float)(int32_t)top * 1.46291807926715968e-9f;  // 2 pi / 2^32
-  __sincosf(a, &s, &c);
-}
 
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
@@ -200,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 3) kv_diag_kernel(const __grid_const
 #pragma unroll
         for (int j = 0; j < RL; ++j) {
           float c, s;
-          phase_cs(pt, F[e][j], c, s);
+          rope_cs(pt, F[e][j], c, s);   // exact fixed-point phase
           const float y0 = y[e][j], y1 = y[e][RL + j];
           csum[e][j] += fmaf(y0, c, y1 * s);
           csum[e][RL + j] += fmaf(y1, c, -y0 * s);

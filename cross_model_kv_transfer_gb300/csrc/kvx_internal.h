@@ -30,6 +30,12 @@ struct kvx_plan {
   // (set for every plan: the diagnostics kernel uses them too)
   void *tc_rope_src;
   unsigned long long turns_tgt[128];
+  // source RoPE frequencies in the same fixed point (the wide path's
+  // un-rotation pre-pass)
+  unsigned long long turns_src[128];
+  // wide-feature mapper: the workspace holds the bf16 W image, the fp32
+  // bias and the un-rotated source keys [Ls][max_tokens][H][d]
+  int64_t max_tokens;
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
   int tc_pairs;          // tensor-core path: CTA pairs resident at once (0: single CTAs)
 };
@@ -52,6 +58,11 @@ struct KvxParams {
 cudaError_t kvx_simt_prepare(const kvx_plan *plan);
 cudaError_t kvx_simt_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);
 bool kvx_simt_supports(const kvx_plan_desc &d);
+
+bool kvx_wide_supports(const kvx_plan_desc &d);
+size_t kvx_wide_workspace_bytes(const kvx_plan_desc &d, int64_t max_tokens);
+cudaError_t kvx_wide_prepare(kvx_plan *plan);
+cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);
 
 bool kvx_tc_supports(const kvx_plan_desc &d);
 size_t kvx_tc_workspace_bytes(const kvx_plan_desc &d);

@@ -270,7 +270,8 @@ extern "C" kvx_status kvx_transfer_static(const kvx_plan_desc *desc,
       !static_dtype_ok(d.w_dtype) || !static_dtype_ok(d.b_dtype) ||
       (d.dst_layout != KVX_CONTIGUOUS && d.dst_layout != KVX_PAGED) ||
       (d.dst_layout == KVX_PAGED && d.block_size < 1) || d.max_position < 1 ||
-      (d.kernel != KVX_KERNEL_AUTO && d.kernel != KVX_KERNEL_SIMT) || d.flags != 0)
+      (d.kernel != KVX_KERNEL_AUTO && d.kernel != KVX_KERNEL_SIMT) || d.flags != 0 ||
+      d.mapper != KVX_MAPPER_PER_HEAD)
     return KVX_ERR_INVALID_ARG;
   if (d.src_kv_heads != d.tgt_kv_heads || d.src_head_dim != d.tgt_head_dim)
     return KVX_ERR_PAIR_MISMATCH;

@@ -43,6 +43,7 @@
 
 #include "kvx_device.cuh"
 #include "kvx_internal.h"
+#include "kvx_ptx.cuh"
 
 namespace {
 
@@ -68,89 +69,9 @@ constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 864
 constexpr uint64_t kWaitNs = 2000000000ull;                  // 2 s without progress
 constexpr uint64_t kStallTestWaitNs = 20000000ull;           // 20 ms (stall test hook)
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// Arrive on the barrier at the same shared-memory offset in CTA `rank` of the
-// cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t rank) {
-  asm volatile(
-      "{\n.reg .b32 r;\n"
-      "mapa.shared::cluster.u32 r, %0, %1;\n"
-      "mbarrier.arrive.shared::cluster.b64 _, [r];\n}\n" ::"r"(bar),
-      "r"(rank)
-      : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      "selp.b32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-// TMA tile load of a 4-D box into shared memory, completing on an mbarrier.
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, int c3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-      : "memory");
-}
-// TMA tile load of a 2-D box into shared memory, completing on an mbarrier.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
+// PTX wrappers, the shared-memory descriptor, bf16 packing and the
+// fixed-point RoPE angle helper live in kvx_ptx.cuh.
+
 // The 8 MMAs of one selection (K = 128): A columns +8 per K step, B
 // descriptor +2 (32 bytes) per step inside a W chunk, then the next chunk
 // (this CTA's 16 KB / P of it).
@@ -186,68 +107,6 @@ __device__ __forceinline__ void tc_mma8_elect(uint32_t d_tmem, uint32_t a_tmem, 
   else KVX_MMA8("2");
 #undef KVX_MMA8
 }
-// Commit: the barrier (in every CTA of `mask` for P = 2) receives one arrival
-// once all MMAs issued so far by this thread are complete.
-template <int P>
-__device__ __forceinline__ void tc_commit_elect(uint32_t bar, uint16_t mask = 3) {
-  if constexpr (P == 1) {
-    asm volatile(
-        "{\n.reg .pred e;\n.reg .b32 r;\n"
-        "elect.sync r|e, 0xffffffff;\n"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
-            bar)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n.reg .pred e;\n.reg .b32 r;\n"
-        "elect.sync r|e, 0xffffffff;\n"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;\n}\n" ::"r"(bar),
-        "h"(mask)
-        : "memory");
-  }
-}
-__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-      : "memory");
-}
-__device__ __forceinline__ void tc_ld8(uint32_t taddr, uint32_t (&v)[8]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7])
-      : "r"(taddr)
-      : "memory");
-}
-// 32-byte global store (one full sector) that does not allocate in L1: the
-// cache rows are written once and never read back here, and L1 keeps the
-// bias and RoPE lines; the address must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t (&v)[8]) {
-  asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-__device__ __forceinline__ void tc_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// UMMA shared-memory descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for SW128 K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
-  d |= (uint64_t)1 << 46;                    // version
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
 // N = 128, M = 128.
 template <int P>
@@ -256,27 +115,10 @@ __host__ __device__ constexpr uint32_t idesc_for() {
          ((uint32_t)((kTileM * P) >> 4) << 24);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// Target RoPE angles without memory traffic.  The plan stores each pair's
-// frequency in turns as a 64-bit binary fraction, F_i = round(w_i / 2pi *
-// 2^64).  The phase of position p is p * F_i mod 2^64, an exact integer
-// product; its top 32 bits give the angle in [-pi, pi) to 2^-32 of a turn,
-// where __sincosf is accurate to about 4e-7.
 struct RopeTurns {
   unsigned long long tgt[kHalf];
 };
 
-__device__ __forceinline__ void rope_cs(uint32_t pos, unsigned long long turns, float &c,
-                                        float &s) {
-  const uint32_t hi = (uint32_t)(turns >> 32), lo = (uint32_t)turns;
-  const uint32_t top = __umulhi(pos, lo) + pos * hi;    // bits 32..63 of pos * F mod 2^64
-  const float a = (float)(int32_t)top * 1.46291807926715968e-9f;  // 2 pi / 2^32
-  __sincosf(a, &s, &c);
-}
 
 // bf16x2 helpers: un-rotation of two RoPE pairs at once in bf16x2 FMA
 // arithmetic.  a = (x_i, x_{i+1}) of the first half, b = (x_{i+d/2},

@@ -49,6 +49,8 @@ KVX_KERNEL_SIMT = 1
 KVX_KERNEL_TCGEN05 = 2
 KVX_PLAN_TEST_STALL = 1
 KVX_PLAN_TC_SINGLE_CTA = 2
+KVX_MAPPER_PER_HEAD = 0
+KVX_MAPPER_WIDE = 1
 
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
             "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches",
@@ -66,6 +68,7 @@ class PlanDesc(ctypes.Structure):
         ("dst_layout", ctypes.c_int32), ("block_size", ctypes.c_int32),
         ("max_position", ctypes.c_int32), ("kernel", ctypes.c_int32),
         ("tiles_per_item", ctypes.c_int32), ("flags", ctypes.c_int32),
+        ("mapper", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
     ]
 
 
@@ -203,7 +206,8 @@ class Plan:
     def __init__(self, *, src_layers, tgt_layers, kv_heads, head_dim, k, rope_theta_src,
                  rope_theta_tgt, max_position, kv_dtype, w_dtype, b_dtype,
                  layout=KVX_CONTIGUOUS, block_size=0, kernel=KVX_KERNEL_AUTO,
-                 tgt_kv_heads=None, tgt_head_dim=None, tiles_per_item=0, flags=0):
+                 tgt_kv_heads=None, tgt_head_dim=None, tiles_per_item=0, flags=0,
+                 mapper=KVX_MAPPER_PER_HEAD, max_tokens=0):
         self.desc = PlanDesc(
             src_layers, tgt_layers, kv_heads,
             kv_heads if tgt_kv_heads is None else tgt_kv_heads,
@@ -211,7 +215,7 @@ class Plan:
             float(rope_theta_src), float(rope_theta_tgt),
             _dtype_code(kv_dtype), _dtype_code(w_dtype), _dtype_code(b_dtype),
             int(layout), int(block_size), int(max_position), int(kernel),
-            int(tiles_per_item), int(flags))
+            int(tiles_per_item), int(flags), int(mapper), int(max_tokens))
         self.kv_dtype, self.w_dtype, self.b_dtype = kv_dtype, w_dtype, b_dtype
         st, h = kvx_plan_create(self.desc)
         if st != KVX_OK:
@@ -274,7 +278,10 @@ class Plan:
         a.num_requests = R
         a.cu_seqlens = ptr(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
         a.layer_idx = ptr(layer_idx, "layer_idx", torch.int32, (Lt, k))
-        a.w = ptr(w, "w", self.w_dtype, (Lt, H, 2, k * hd, hd))
+        if d.mapper == KVX_MAPPER_WIDE:
+            a.w = ptr(w, "w", self.w_dtype, (Lt, k * 2 * H * hd, H * 2 * hd))
+        else:
+            a.w = ptr(w, "w", self.w_dtype, (Lt, H, 2, k * hd, hd))
         a.b = ptr(b, "b", self.b_dtype, (Lt, H, 2, hd))
         a.src_pos = ptr(src_pos, "src_pos", torch.int32, (ntok,))
         a.tgt_pos = ptr(tgt_pos, "tgt_pos", torch.int32, (ntok,))

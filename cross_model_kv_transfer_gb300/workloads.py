@@ -130,6 +130,23 @@ class Workload:
         kd = self.k * self.head_dim
         return int(2 * self.ntok * kd * self.head_dim * self.tgt_layers * self.kv_heads * 2)
 
+    # ---- the wide-feature map: one [F x N] map per target layer ----------
+    def wide_algorithmic_bytes(self, layer_idx: torch.Tensor) -> int:
+        """As ``algorithmic_bytes`` with W [Lt][k*2*H*d][H*2*d] fp32."""
+        eb = torch.empty(0, dtype=self.kv_dtype).element_size()
+        row = self.kv_heads * self.head_dim * eb
+        src = 2 * self.unique_selected_layers(layer_idx) * self.ntok * row
+        dst = 2 * self.tgt_layers * self.ntok * row
+        F = self.k * 2 * self.kv_heads * self.head_dim
+        N = self.kv_heads * 2 * self.head_dim
+        bb = torch.empty(0, dtype=self.b_dtype).element_size()
+        return int(src + dst + self.tgt_layers * F * N * 4 + self.tgt_layers * N * bb)
+
+    def wide_algorithmic_flops(self) -> int:
+        F = self.k * 2 * self.kv_heads * self.head_dim
+        N = self.kv_heads * 2 * self.head_dim
+        return int(2 * self.ntok * F * N * self.tgt_layers)
+
 
 def _bf16(name, Ls, Lt, k, theta, seed, seqlens, offsets, **kw):
     return Workload(name=name, src_layers=Ls, tgt_layers=Lt, kv_heads=8, head_dim=128,
@@ -220,6 +237,20 @@ def make_inputs(wl: Workload, device="cpu", seed: Optional[int] = None) -> dict:
     if wl.layout == PAGED:
         out["block_table"] = make_block_table(wl, seed).to(dev)
     return out
+
+
+def make_wide_weights(wl: Workload, device="cpu", seed: Optional[int] = None) -> torch.Tensor:
+    """W of the wide-feature map, fp32 [Lt][F][N] with F = k*2*H*d features
+    and N = H*2*d outputs, drawn N(0, 1/F) (the per-head recipe's scale)."""
+    seed = (wl.seed if seed is None else seed) + 3000017
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    F = wl.k * 2 * wl.kv_heads * wl.head_dim
+    N = wl.kv_heads * 2 * wl.head_dim
+    w = torch.empty((wl.tgt_layers, F, N), dtype=torch.float32, device=dev)
+    for lt in range(wl.tgt_layers):
+        w[lt].copy_(torch.randn((F, N), generator=g, device=dev) / math.sqrt(F))
+    return w
 
 
 def make_block_table(wl: Workload, seed: int) -> torch.Tensor:

@@ -93,6 +93,20 @@ typedef enum {
                                  head_dim 128                                */
 } kvx_kernel;
 
+/* Which map the transfer applies.
+ * PER_HEAD: one map per (target layer, head, K|V) over that head's features
+ *   of the k selected layers (width k*d); W is [Lt][H][2][k*d][d].
+ * WIDE: one map per target layer over ALL heads' keys and values of the k
+ *   selected layers (width F = k*2*H*d) to all heads' keys and values
+ *   (N = H*2*d); W is [Lt][F][N], feature (j, m, h, i) at row
+ *   ((j*2 + m)*H + h)*d + i (m = 0 the un-rotated key, 1 the value, of
+ *   source layer idx[lt][j], head h), output (h, m, i) at column
+ *   (h*2 + m)*d + i; b keeps the [Lt][H][2][d] layout.  This is the reading
+ *   of the 14B -> 32B mapper size in "Перенос KV-кэша между моделями Qwen3
+ *   вместо повторного префилла", section "Ограничения, важные в продакшене"
+ *   (about 1.07e9 parameters, 4 GB: 64 x 8192 x 2048 fp32 weights). */
+typedef enum { KVX_MAPPER_PER_HEAD = 0, KVX_MAPPER_WIDE = 1 } kvx_mapper;
+
 /* Plan descriptor.  The source and target KV-head counts and head
  * dimensions are given separately so that an incompatible pair is refused
  * with KVX_ERR_PAIR_MISMATCH ("Requirements": same number of KV heads and
@@ -119,6 +133,12 @@ typedef struct {
                                256 for CTA pairs) per work item; W is loaded
                                once per item; 0 = default (32)              */
   int32_t flags;            /* KVX_PLAN_* bits; 0 for normal use            */
+  int32_t mapper;           /* kvx_mapper; WIDE needs the tensor-core kernel
+                               (bf16 K/V, head_dim 128)                     */
+  int32_t max_tokens;       /* WIDE: the most source tokens (ntok) one
+                               transfer may carry; sizes the plan's buffer of
+                               un-rotated source keys ([Ls][max_tokens][H][d]
+                               bf16); 0 = max_position.  Ignored otherwise  */
 } kvx_plan_desc;
 
 /* Failure-detection test hook (tensor-core path): the warps that fill the
@@ -151,8 +171,10 @@ typedef struct {
                                  owns all ntok rows                          */
   const int32_t *layer_idx;   /* [Lt][k] selected source layers, in
                                  feature-concatenation order                 */
-  const void *w;              /* [Lt][H][2][k*d][d] map, m = 0 keys, 1 values;
-                                 rows follow the concatenation order         */
+  const void *w;              /* PER_HEAD: [Lt][H][2][k*d][d] map, m = 0 keys,
+                                 1 values; rows follow the concatenation
+                                 order.  WIDE: [Lt][k*2*H*d][H*2*d] (see
+                                 kvx_mapper)                                 */
   const void *b;              /* [Lt][H][2][d] bias                           */
   const int32_t *src_pos;     /* [ntok] source positions, or NULL: 0..len-1
                                  within each request                         */
@@ -189,9 +211,13 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out);
  * default stream).  Asynchronous: no host synchronisation, no allocation.
  * Returns KVX_ERR_INVALID_ARG for a NULL plan/args or a missing required
  * pointer or size, and, for a tensor-core plan, for source bases that are
- * not 16-byte aligned or cache bases that are not 32-byte aligned;
- * KVX_ERR_CUDA if a launch fails.  Device-detected errors
- * are reported through args->status as described above. */
+ * not 16-byte aligned or cache bases that are not 32-byte aligned, and, for a
+ * WIDE plan, for ntok > max_tokens; KVX_ERR_CUDA if a launch fails.
+ * Device-detected errors are reported through args->status as described
+ * above.  A WIDE plan's transfer runs three kernels: the source keys of all
+ * layers un-rotated into the plan's buffer, W into a bf16 image, and the
+ * map as one tensor-core contraction per (target layer, 256 tokens, head)
+ * with bias, re-rotation and the cache install in its epilogue. */
 kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *args,
                         void *stream);
 
@@ -281,7 +307,7 @@ kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_args *args, v
  * device before the transfer kernel runs.  Limits: max_position * head_dim/2
  * table entries, doubled when the two RoPE bases differ, must not exceed
  * 2^20, else KVX_ERR_TOO_LARGE is returned before anything is enqueued;
- * desc->kernel must be AUTO or SIMT and desc->flags 0.
+ * desc->kernel must be AUTO or SIMT, desc->flags 0 and desc->mapper PER_HEAD.
  *
  * All calls share the array: calls whose work overlaps on the GPU (two
  * streams, for instance) race on it and must be ordered by the caller.  The
