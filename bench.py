@@ -233,6 +233,11 @@ def roofline(wl, layer_idx, ms_per_launch, kernel_name, peaks, peak_kind, wide=F
         r = {"bound": "hbm", "achieved": alg_bytes / s / 1e9, "peak": peaks["hbm_gbs"],
              "unit": "GB/s"}
     r["frac"] = r["achieved"] / r["peak"]
+    if r["bound"] == "tensor":
+        # a kernel timed over a long loop runs under the power cap: the
+        # sustained cuBLAS figure is its like-for-like denominator
+        r["sustained_peak"] = peaks["bf16_tflops_sustained"]
+        r["frac_of_sustained"] = r["achieved"] / peaks["bf16_tflops_sustained"]
     r["traffic"] = traffic
     r["peak_source"] = f"{peak_kind} (burst)"
     r["algorithmic_bytes"] = alg_bytes

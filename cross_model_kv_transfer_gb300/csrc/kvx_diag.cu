@@ -77,8 +77,16 @@ __device__ __forceinline__ void load_run(const T *src, float *out) {
   }
 }
 
+// The 16 / sizeof(T) elements of one 16-byte word as fp32.
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &u, float *out) {
+  const T *e = reinterpret_cast<const T *>(&u);
+#pragma unroll
+  for (int j = 0; j < 16 / (int)sizeof(T); ++j) out[j] = to_f<T>(e[j]);
+}
+
 template <typename T, int RL, int EMAX, bool VEC>
-__global__ void __launch_bounds__(kThreads, 3) kv_diag_kernel(const __grid_constant__ DiagParams P) {
+__global__ void __launch_bounds__(kThreads, 2) kv_diag_kernel(const __grid_constant__ DiagParams P) {
   __shared__ int64_t s_row[kMaxChunk];
   __shared__ int32_t s_pt[kMaxChunk];
   __shared__ uint32_t s_bits;
@@ -150,39 +158,21 @@ __global__ void __launch_bounds__(kThreads, 3) kv_diag_kernel(const __grid_const
 #pragma unroll
     for (int j = 0; j < 2 * RL; ++j) csum[e][j] = 0.f;
 
-  // Every lane runs every iteration (the shuffles below need the whole
-  // warp); lanes without a token or a row contribute zeros.
-  for (int base = 0; base < n; base += P.tok_par) {
-    const int i = base + tl;
-    const int64_t row = (lane_on && i < n) ? s_row[i] : -1;
-    const bool on = row >= 0;
-    const uint32_t pt = on ? (uint32_t)s_pt[i] : 0u;
+  // One token's row: fold the lane's runs into the per-token sums and the
+  // content-space sums.  a = mapped, y = reference, both [EMAX][2 RL] fp32.
+  auto fold = [&](const float (&a)[EMAX][2 * RL], const float (&y)[EMAX][2 * RL], bool on,
+                  uint32_t pt) {
     float dot = 0.f, aa = 0.f, yy = 0.f, res = 0.f;
-    float y[EMAX][2 * RL];
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-      const int r = q + e * P.G;
-      float a[2 * RL];
-      const bool run_on = on && r < P.NR;
-      if (run_on) {
-        const int64_t off = (((int64_t)lt * p.dst_rows + row) * p.H + h) * p.d + (int64_t)r * RL;
-        load_run<T, RL, VEC>(mapped + off, a);
-        load_run<T, RL, VEC>(mapped + off + half, a + RL);
-        load_run<T, RL, VEC>(ref + off, y[e]);
-        load_run<T, RL, VEC>(ref + off + half, y[e] + RL);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 2 * RL; ++j) a[j] = y[e][j] = 0.f;
-      }
+    for (int e = 0; e < EMAX; ++e)
 #pragma unroll
       for (int j = 0; j < 2 * RL; ++j) {
-        dot = fmaf(a[j], y[e][j], dot);
-        aa = fmaf(a[j], a[j], aa);
+        dot = fmaf(a[e][j], y[e][j], dot);
+        aa = fmaf(a[e][j], a[e][j], aa);
         yy = fmaf(y[e][j], y[e][j], yy);
-        const float df = y[e][j] - a[j];
+        const float df = y[e][j] - a[e][j];
         res = fmaf(df, df, res);
       }
-    }
     // content space: keys un-rotated at p' (multiply by exp(-j p' w_i))
     if (m == 0) {
 #pragma unroll
@@ -214,6 +204,73 @@ __global__ void __launch_bounds__(kThreads, 3) kv_diag_kernel(const __grid_const
       if (aa > 0.f && yy > 0.f) acc_cos += dot * rsqrtf(aa) * rsqrtf(yy);
       acc_res += res;
       acc_yy += yy;
+    }
+  };
+
+  // Every lane runs every iteration (the shuffles need the whole warp);
+  // lanes without a token or a row contribute zeros.
+  if constexpr (VEC && EMAX == 1) {
+    // two tokens per iteration, their 16-byte words loaded before either is
+    // used (twice the bytes in flight per thread)
+    constexpr int kNV = RL * (int)sizeof(T) / 16;   // 16-byte words per half run
+    for (int base = 0; base < n; base += 2 * P.tok_par) {
+      uint4 raw[2][4][kNV];                          // token, (a lo, a hi, y lo, y hi)
+      int64_t row[2];
+      uint32_t pt[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = base + u * P.tok_par + tl;
+        row[u] = (lane_on && i < n) ? s_row[i] : -1;
+        pt[u] = row[u] >= 0 ? (uint32_t)s_pt[i] : 0u;
+        const bool run_on = row[u] >= 0 && q < P.NR;
+        const int64_t off =
+            run_on ? (((int64_t)lt * p.dst_rows + row[u]) * p.H + h) * p.d + (int64_t)q * RL : 0;
+        const uint4 *src[4] = {reinterpret_cast<const uint4 *>(mapped + off),
+                               reinterpret_cast<const uint4 *>(mapped + off + half),
+                               reinterpret_cast<const uint4 *>(ref + off),
+                               reinterpret_cast<const uint4 *>(ref + off + half)};
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+          for (int v = 0; v < kNV; ++v)
+            raw[u][w][v] = run_on ? __ldcs(src[w] + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float a[1][2 * RL], y[1][2 * RL];
+#pragma unroll
+        for (int v = 0; v < kNV; ++v) {
+          constexpr int kPer = 16 / (int)sizeof(T);
+          unpack16<T>(raw[u][0][v], &a[0][v * kPer]);
+          unpack16<T>(raw[u][1][v], &a[0][RL + v * kPer]);
+          unpack16<T>(raw[u][2][v], &y[0][v * kPer]);
+          unpack16<T>(raw[u][3][v], &y[0][RL + v * kPer]);
+        }
+        fold(a, y, row[u] >= 0, pt[u]);
+      }
+    }
+  } else {
+    for (int base = 0; base < n; base += P.tok_par) {
+      const int i = base + tl;
+      const int64_t row = (lane_on && i < n) ? s_row[i] : -1;
+      const bool on = row >= 0;
+      const uint32_t pt = on ? (uint32_t)s_pt[i] : 0u;
+      float a[EMAX][2 * RL], y[EMAX][2 * RL];
+#pragma unroll
+      for (int e = 0; e < EMAX; ++e) {
+        const int r = q + e * P.G;
+        if (on && r < P.NR) {
+          const int64_t off = (((int64_t)lt * p.dst_rows + row) * p.H + h) * p.d + (int64_t)r * RL;
+          load_run<T, RL, VEC>(mapped + off, a[e]);
+          load_run<T, RL, VEC>(mapped + off + half, a[e] + RL);
+          load_run<T, RL, VEC>(ref + off, y[e]);
+          load_run<T, RL, VEC>(ref + off + half, y[e] + RL);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 2 * RL; ++j) a[e][j] = y[e][j] = 0.f;
+        }
+      }
+      fold(a, y, on, pt);
     }
   }
 

@@ -64,6 +64,8 @@ constexpr int kWEpiWarp0 = 2;
 constexpr int kWEpiWarps = 8;
 constexpr int kWThreads = (kWEpiWarp0 + kWEpiWarps) * 32;   // 320
 constexpr uint64_t kWWaitNs = 2000000000ull;   // 2 s without progress
+constexpr int kWSyncSteps = 16;                // feature steps per lockstep epoch
+constexpr int kWSyncLag = 2;                   // epochs a producer may run ahead of the mean
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
 // N = 256, M = 256 (CTA pair).
@@ -81,6 +83,13 @@ struct WideGeom {
   int stages;
   long long num_tiles;   // Lt * mt_count * nt_count
   long long stride;      // CTA pairs
+  // Loose lockstep of the producers (see wide_map_kernel): a counter of the
+  // epochs (kWSyncSteps feature steps each) every producer has issued,
+  // cleared by the W-image kernel; a producer issues epoch e only once the
+  // producers together have issued (e - kWSyncLag) epochs each on average.
+  unsigned int *sync;
+  int epochs_per_tile;
+  int max_epochs;        // epochs of a producer with the most tiles
 };
 
 struct WShared {
@@ -121,6 +130,17 @@ __device__ __forceinline__ void wdrain_wait(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(a, parity) && globaltimer() - t0 < kWWaitNs) {
   }
+}
+
+// The lockstep counter: relaxed loads and reductions at GPU scope (it paces
+// the producers and orders no data).
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_add_gpu(unsigned int *p, unsigned int v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // The four MMAs of one 64-feature stage: A and B descriptors advance by
@@ -208,10 +228,40 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // ------------------------------------------------------------------
     if (lane == 0) {
       uint32_t x_seq = 0;
+      // Loose lockstep: every producer streams K in the same order, so the
+      // 76 pairs together touch only the current feature slices of ~10 token
+      // blocks and 8 W blocks when they stay close; left alone they drift
+      // apart by whole tiles and the distinct operands of a wave (~70 MB)
+      // no longer stay in L2.  Epochs already counted for this producer:
+      uint32_t epochs = 0;
+      const unsigned long long producers = 2ull * (unsigned long long)geo.stride;
+      // true when epoch `epochs` may be issued; false if the pipeline is
+      // being abandoned (bounded like every other wait)
+      auto pace = [&]() -> bool {
+        const long long ahead = (long long)epochs - kWSyncLag;
+        if (ahead <= 0) return true;
+        const unsigned long long need = producers * (unsigned long long)ahead;
+        if (ld_relaxed_gpu(geo.sync) >= need) return true;
+        const uint64_t t0 = globaltimer();
+        while (ld_relaxed_gpu(geo.sync) < need) {
+          if (sh->abort) return false;
+          if (globaltimer() - t0 > kWWaitNs) {
+            sh->abort = 1;
+            if (p.status) atomicOr(p.status, KVX_FLAG_TIMEOUT);
+            return false;
+          }
+          __nanosleep(100);
+        }
+        return true;
+      };
       for (long long t = pair; t < geo.num_tiles; t += geo.stride) {
         int lt, mt, nt;
         decode_tile(geo, t, lt, mt, nt);
-        if (!kvx::layer_row_ok(p, lt)) continue;
+        if (!kvx::layer_row_ok(p, lt)) {
+          red_add_gpu(geo.sync, (unsigned)geo.epochs_per_tile);
+          epochs += geo.epochs_per_tile;
+          continue;
+        }
         const int tok0 = mt * 2 * kWRows + (int)rank * kWRows;
         const unsigned char *img = w_img +
                                    ((int64_t)lt * geo.nt_count + nt) * geo.kc_count * kWChunkBytes +
@@ -224,6 +274,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const CUtensorMap *map = m == 0 ? &map_key : &map_val;
             for (int h = 0; h < p.H; ++h) {
               for (int hf = 0; hf < 2; ++hf, ++kc) {
+                if (kc % kWSyncSteps == 0 && !pace()) goto producer_done;
                 const int stage = (int)(x_seq % (uint32_t)geo.stages);
                 if (!W.wait(&sh->empty[stage], ((x_seq / geo.stages) & 1) ^ 1)) goto producer_done;
                 const uint32_t bar = smem_addr(&sh->full[stage]);
@@ -232,12 +283,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 tma_load_4d(dst, map, hf * kWHalf, h, tok0, sl, bar);
                 bulk_g2s(dst + kWHalfBytes, img + (int64_t)kc * kWChunkBytes, kWHalfBytes, bar);
                 ++x_seq;
+                if (kc % kWSyncSteps == kWSyncSteps - 1 || kc == geo.kc_count - 1) {
+                  red_add_gpu(geo.sync, 1u);
+                  ++epochs;
+                }
               }
             }
           }
         }
       }
     producer_done:
+      // retire: count the epochs this producer will not issue, so that no
+      // other producer waits for them
+      if (epochs < (uint32_t)geo.max_epochs) red_add_gpu(geo.sync, (uint32_t)geo.max_epochs - epochs);
       // drain: the last `stages` loads (at most) may still be in flight
       for (uint32_t n = (x_seq > (uint32_t)geo.stages ? x_seq - geo.stages : 0); n < x_seq; ++n)
         wdrain_wait(&sh->full[n % geo.stages], (n / geo.stages) & 1);
@@ -455,9 +513,12 @@ __global__ void __launch_bounds__(256) wide_w_image_kernel(const WT *__restrict_
                                                            uint4 *__restrict__ img,
                                                            const BT *__restrict__ b,
                                                            float *__restrict__ b_img, int64_t F,
-                                                           int64_t N, int KC, int NT) {
+                                                           int64_t N, int KC, int NT,
+                                                           unsigned int *__restrict__ sync) {
   __shared__ float tile[kWKStep][kWRows + 1];
   const int kc = blockIdx.x, nt = blockIdx.y, lt = blockIdx.z;
+  // the map kernel's lockstep counter starts every transfer at zero
+  if (kc == 0 && nt == 0 && lt == 0 && threadIdx.x == 0) *sync = 0u;
   const WT *src = w + ((int64_t)lt * F + (int64_t)kc * kWKStep) * N + (int64_t)nt * kWN;
   uint4 *out = img + (((int64_t)lt * NT + nt) * KC + kc) * (kWChunkBytes / 16);
   for (int half = 0; half < 2; ++half) {
@@ -533,7 +594,7 @@ bool kvx_wide_supports(const kvx_plan_desc &d) {
 }
 
 size_t kvx_wide_workspace_bytes(const kvx_plan_desc &d, int64_t max_tokens) {
-  return align256(wide_img_bytes(d)) + align256(wide_bias_bytes(d)) +
+  return align256(wide_img_bytes(d)) + align256(wide_bias_bytes(d)) + 256 +
          (size_t)d.src_layers * (size_t)max_tokens * d.src_kv_heads * kWD * 2;
 }
 
@@ -569,8 +630,10 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   unsigned char *ws = reinterpret_cast<unsigned char *>(plan->workspace);
   uint4 *img = reinterpret_cast<uint4 *>(ws);
   float *bimg = reinterpret_cast<float *>(ws + align256(wide_img_bytes(d)));
+  unsigned int *sync = reinterpret_cast<unsigned int *>(ws + align256(wide_img_bytes(d)) +
+                                                        align256(wide_bias_bytes(d)));
   __nv_bfloat16 *content = reinterpret_cast<__nv_bfloat16 *>(
-      ws + align256(wide_img_bytes(d)) + align256(wide_bias_bytes(d)));
+      ws + align256(wide_img_bytes(d)) + align256(wide_bias_bytes(d)) + 256);
 
   // 1. un-rotated source keys
   WideTurns src_turns, tgt_turns;
@@ -591,16 +654,16 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   const bool wf = d.w_dtype == KVX_F32, bfp = d.b_dtype == KVX_F32;
   if (wf && bfp)
     wide_w_image_kernel<float, float><<<wgrid, 256, 0, s>>>((const float *)p.w, img,
-                                                           (const float *)p.b, bimg, F, N, KC, NT);
+                                                           (const float *)p.b, bimg, F, N, KC, NT, sync);
   else if (wf)
     wide_w_image_kernel<float, bf><<<wgrid, 256, 0, s>>>((const float *)p.w, img, (const bf *)p.b,
-                                                        bimg, F, N, KC, NT);
+                                                        bimg, F, N, KC, NT, sync);
   else if (bfp)
     wide_w_image_kernel<bf, float><<<wgrid, 256, 0, s>>>((const bf *)p.w, img, (const float *)p.b,
-                                                        bimg, F, N, KC, NT);
+                                                        bimg, F, N, KC, NT, sync);
   else
     wide_w_image_kernel<bf, bf><<<wgrid, 256, 0, s>>>((const bf *)p.w, img, (const bf *)p.b, bimg,
-                                                     F, N, KC, NT);
+                                                     F, N, KC, NT, sync);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -612,6 +675,9 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   geo.stages = wide_stages();
   geo.num_tiles = (long long)p.Lt * geo.mt_count * geo.nt_count;
   geo.stride = geo.num_tiles < plan->tc_pairs ? geo.num_tiles : plan->tc_pairs;
+  geo.sync = sync;
+  geo.epochs_per_tile = (KC + kWSyncSteps - 1) / kWSyncSteps;
+  geo.max_epochs = (int)((geo.num_tiles + geo.stride - 1) / geo.stride) * geo.epochs_per_tile;
   CUtensorMap mk, mv;
   if (!encode_wide_map(plan, &mk, content, p.ntok, plan->max_tokens, p.H, p.Ls) ||
       !encode_wide_map(plan, &mv, p.src_v, p.ntok, p.ntok, p.H, p.Ls))
@@ -621,6 +687,10 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   cfg.blockDim = dim3(kWThreads, 1, 1);
   cfg.dynamicSmemBytes = wide_smem_bytes(geo.stages);
   cfg.stream = s;
+  // The producers pace each other (loose lockstep), so all pairs must be
+  // resident together: the grid is the cluster occupancy of the device.  On
+  // a device shared with other work a pacing wait that cannot be satisfied
+  // gives up after 2 s and reports KVX_FLAG_TIMEOUT.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
