@@ -51,6 +51,7 @@ BAD_POSITION = 2
 BAD_BLOCK = 4
 BAD_ROW = 8
 BAD_SEQLENS = 32
+BAD_SRC_BLOCK = 64
 
 CONTIGUOUS = 0
 PAGED = 1
@@ -92,6 +93,10 @@ class _Problem(ctypes.Structure):
         ("block_size", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
         ("max_blocks_per_req", ctypes.c_int64),
         ("block_table", ctypes.c_void_p),
+        ("src_layout", ctypes.c_int32),
+        ("src_block_size", ctypes.c_int64), ("src_num_blocks", ctypes.c_int64),
+        ("src_max_blocks_per_req", ctypes.c_int64),
+        ("src_block_table", ctypes.c_void_p),
     ]
 
 
@@ -185,7 +190,8 @@ def transfer(*, src_k, src_v, layer_idx, w, b, theta_src, theta_tgt,
              max_position, cu_seqlens=None, src_pos=None, tgt_pos=None,
              tgt_offset=None, layout=CONTIGUOUS, dst_capacity=0,
              block_size=1, num_blocks=0, block_table=None, dst_k=None, dst_v=None,
-             wide=False):
+             wide=False, src_layout=CONTIGUOUS, src_block_size=1, src_block_table=None,
+             ntok=None):
     """The whole transfer in fp64.
 
     src_k / src_v: [Ls][ntok][H][d]; layer_idx: [Lt][k]; w: [Lt][H][2][k*d][d]
@@ -193,9 +199,21 @@ def transfer(*, src_k, src_v, layer_idx, w, b, theta_src, theta_tgt,
     target layer over all heads' keys and values, ``kvxo_transfer_wide``);
     b: [Lt][H][2][d].  dst_k / dst_v (optional, fp64) are the initial target
     cache [Lt][rows][H][d]; rows not written keep their values (NaN if the
-    caller gives none).  Returns (dst_k, dst_v, status bits)."""
+    caller gives none).  With ``src_layout=PAGED`` the source is the pilot's
+    paged cache [Ls][src_num_blocks*src_block_size][H][d] read through
+    ``src_block_table`` [R][max] (``kvxo_src_row``); ``ntok`` then defaults
+    to cu_seqlens[-1].  Returns (dst_k, dst_v, status bits)."""
     src_k, src_v, w, b = _f64(src_k), _f64(src_v), _f64(w), _f64(b)
-    Ls, ntok, H, d = src_k.shape
+    Ls, src_rows, H, d = src_k.shape
+    if src_layout == PAGED:
+        if ntok is None:
+            ntok = int(np.asarray(cu_seqlens)[-1]) if cu_seqlens is not None else None
+        assert ntok is not None and src_rows % src_block_size == 0
+        sbt = np.ascontiguousarray(src_block_table, dtype=np.int32)
+        src_nb, src_mb = src_rows // src_block_size, sbt.shape[1]
+    else:
+        ntok = src_rows
+        sbt, src_nb, src_mb = None, 0, 0
     idx = np.ascontiguousarray(layer_idx, dtype=np.int32)
     Lt, k = idx.shape
     if wide:
@@ -228,7 +246,8 @@ def transfer(*, src_k, src_v, layer_idx, w, b, theta_src, theta_tgt,
     P = _Problem(Ls, Lt, H, d, k, float(theta_src), float(theta_tgt),
                  int(max_position), R, ntok, _vp(cu), _vp(src_k), _vp(src_v),
                  _vp(idx), _vp(w), _vp(b), _vp(sp), _vp(tp), _vp(to), int(layout),
-                 int(dst_capacity), int(block_size), int(num_blocks), int(mbpr), _vp(bt))
+                 int(dst_capacity), int(block_size), int(num_blocks), int(mbpr), _vp(bt),
+                 int(src_layout), int(src_block_size), int(src_nb), int(src_mb), _vp(sbt))
     fn = _load().kvxo_transfer_wide if wide else _load().kvxo_transfer
     st = fn(ctypes.byref(P), _dp(dst_k), _dp(dst_v))
     return dst_k, dst_v, int(st)

@@ -98,10 +98,34 @@ int64_t kvxo_dst_row(int layout, int64_t r, int64_t p_tgt,
   return phys * block_size + p_tgt % block_size;
 }
 
+/* Reading the pilot's own paged cache: the same block-table rule as the
+ * target install, applied to the source position. */
+int64_t kvxo_src_row(int layout, int64_t g, int64_t r, int64_t p, int64_t block_size,
+                     int64_t num_blocks, const int32_t *block_table,
+                     int64_t max_blocks_per_req, int *bad) {
+  *bad = 0;
+  if (layout == KVXO_CONTIGUOUS) return g;
+  int64_t logical = p / block_size;
+  if (logical >= max_blocks_per_req) {
+    *bad = KVXO_BAD_SRC_BLOCK;
+    return -1;
+  }
+  int64_t phys = block_table[r * max_blocks_per_req + logical];
+  if (phys < 0 || phys >= num_blocks) {
+    *bad = KVXO_BAD_SRC_BLOCK;
+    return -1;
+  }
+  return phys * block_size + p % block_size;
+}
+
+static int64_t kvxo_src_rows(const kvxo_problem *P) {
+  return P->src_layout == KVXO_PAGED ? P->src_num_blocks * P->src_block_size : P->ntok;
+}
+
 int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
   const int64_t Ls = P->src_layers, Lt = P->tgt_layers, H = P->kv_heads;
   const int64_t d = P->head_dim, k = P->k, kd = k * d;
-  const int64_t ntok = P->ntok;
+  const int64_t ntok = P->ntok, src_rows = kvxo_src_rows(P);
   const int64_t rows = P->layout == KVXO_CONTIGUOUS
                            ? (int64_t)P->num_requests * P->dst_capacity
                            : P->num_blocks * P->block_size;
@@ -143,6 +167,13 @@ int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
         continue;
       }
       int bad = 0;
+      int64_t srow = kvxo_src_row(P->src_layout, g, r, p, P->src_block_size,
+                                  P->src_num_blocks, P->src_block_table,
+                                  P->src_max_blocks_per_req, &bad);
+      if (srow < 0) {
+        status |= bad;
+        continue;
+      }
       int64_t row = kvxo_dst_row(P->layout, r, pt, P->dst_capacity,
                                  P->block_size, P->num_blocks, P->block_table,
                                  P->max_blocks_per_req, &bad);
@@ -155,8 +186,8 @@ int kvxo_transfer(const kvxo_problem *P, double *dst_k, double *dst_v) {
         for (int64_t h = 0; h < H; ++h) {
           for (int64_t j = 0; j < k; ++j) {
             int64_t s = P->layer_idx[lt * k + j];
-            krows[j] = P->src_k + ((s * ntok + g) * H + h) * d;
-            vrows[j] = P->src_v + ((s * ntok + g) * H + h) * d;
+            krows[j] = P->src_k + ((s * src_rows + srow) * H + h) * d;
+            vrows[j] = P->src_v + ((s * src_rows + srow) * H + h) * d;
           }
           const double *Wk = P->w + ((lt * H + h) * 2 + 0) * kd * d;
           const double *Wv = P->w + ((lt * H + h) * 2 + 1) * kd * d;
@@ -216,7 +247,7 @@ void kvxo_map_token_wide(int H, int d, int k, double theta_src, double theta_tgt
 
 int kvxo_transfer_wide(const kvxo_problem *P, double *dst_k, double *dst_v) {
   const int64_t Ls = P->src_layers, Lt = P->tgt_layers, H = P->kv_heads;
-  const int64_t d = P->head_dim, k = P->k, ntok = P->ntok;
+  const int64_t d = P->head_dim, k = P->k, ntok = P->ntok, src_rows = kvxo_src_rows(P);
   const int64_t F = k * 2 * H * d, N = H * 2 * d;
   const int64_t rows = P->layout == KVXO_CONTIGUOUS
                            ? (int64_t)P->num_requests * P->dst_capacity
@@ -256,6 +287,13 @@ int kvxo_transfer_wide(const kvxo_problem *P, double *dst_k, double *dst_v) {
         continue;
       }
       int bad = 0;
+      int64_t srow = kvxo_src_row(P->src_layout, g, r, p, P->src_block_size,
+                                  P->src_num_blocks, P->src_block_table,
+                                  P->src_max_blocks_per_req, &bad);
+      if (srow < 0) {
+        status |= bad;
+        continue;
+      }
       int64_t row = kvxo_dst_row(P->layout, r, pt, P->dst_capacity,
                                  P->block_size, P->num_blocks, P->block_table,
                                  P->max_blocks_per_req, &bad);
@@ -267,8 +305,8 @@ int kvxo_transfer_wide(const kvxo_problem *P, double *dst_k, double *dst_v) {
         if (!layer_ok[lt]) continue;
         for (int64_t j = 0; j < k; ++j) {
           int64_t s = P->layer_idx[lt * k + j];
-          krows[j] = P->src_k + (s * ntok + g) * H * d;
-          vrows[j] = P->src_v + (s * ntok + g) * H * d;
+          krows[j] = P->src_k + (s * src_rows + srow) * H * d;
+          vrows[j] = P->src_v + (s * src_rows + srow) * H * d;
         }
         kvxo_map_token_wide((int)H, (int)d, (int)k, P->theta_src, P->theta_tgt,
                             krows, vrows, P->w + lt * F * N, P->b + lt * N,

@@ -61,6 +61,8 @@ extern "C" {
 #define KVXO_BAD_BLOCK       4
 #define KVXO_BAD_ROW         8
 #define KVXO_BAD_SEQLENS     32
+#define KVXO_BAD_SRC_BLOCK   64   /* paged source: p / bs beyond the table or a
+                                     block id outside the source pool */
 
 #define KVXO_CONTIGUOUS 0
 #define KVXO_PAGED      1
@@ -110,7 +112,25 @@ typedef struct {
   int64_t dst_capacity;        /* contiguous: rows per request */
   int64_t block_size, num_blocks, max_blocks_per_req;
   const int32_t *block_table;  /* [R][max_blocks_per_req] (paged) */
+  /* Source layout.  KVXO_CONTIGUOUS: src_k / src_v are [Ls][ntok][H][d] and
+   * token g is row g.  KVXO_PAGED: they are [Ls][src_num_blocks *
+   * src_block_size][H][d], the pilot's own paged cache, and token g of
+   * request r at source position p is row kvxo_src_row(...). */
+  int32_t src_layout;
+  int64_t src_block_size, src_num_blocks, src_max_blocks_per_req;
+  const int32_t *src_block_table;  /* [R][src_max_blocks_per_req] (paged) */
 } kvxo_problem;
+
+/* Source row of packed token g (request r, source position p): g for a
+ * contiguous source; src_block_table[r][p / bs] * bs + p % bs for a paged
+ * one (the pilot's cache holds its tokens at their positions, like the
+ * target cache of [KNLP]'s inject step), or -1 with *bad = KVXO_BAD_SRC_BLOCK
+ * when p / bs >= max_blocks_per_req or the block id is outside
+ * [0, num_blocks).  Per token the checks run in the order: positions, source
+ * row, destination row; the first that fails names the skip. */
+int64_t kvxo_src_row(int layout, int64_t g, int64_t r, int64_t p, int64_t block_size,
+                     int64_t num_blocks, const int32_t *block_table,
+                     int64_t max_blocks_per_req, int *bad);
 
 /* Whole transfer.  dst_k / dst_v are [Lt][rows][H][d] with rows =
  * R * dst_capacity (contiguous) or num_blocks * block_size (paged); rows not

@@ -855,3 +855,130 @@ def test_map_token_wide_matches_transfer_row():
             ok, ov = oracle.map_token_wide(src_k[idx[lt], t], src_v[idx[lt], t], W[lt], b[lt],
                                            t, t + 2, kw["theta_src"], kw["theta_tgt"])
             assert np.array_equal(ok, dk[lt, t + 2]) and np.array_equal(ov, dv[lt, t + 2])
+
+
+# --------------------------------------------------------------------------
+# Paged source: the pilot's own cache read through its block table (the
+# target install's block-table rule of the knlp.io inject step, applied to
+# the source position)
+# --------------------------------------------------------------------------
+
+def _scatter_paged_source(rng, src, cu, pos, bs, spare=3):
+    """Scatter the packed rows of ``src`` [Ls][ntok][H][d] into a permuted
+    pool of ``bs``-row blocks: request r's token at source position p goes to
+    slot table[r][p // bs] * bs + p % bs.  Written out here with numpy, apart
+    from the oracle's own row rule.  Unused slots are NaN."""
+    R = len(cu) - 1
+    Ls, _, H, d = src.shape
+    nblk = [int(pos[cu[r]:cu[r + 1]].max()) // bs + 1 for r in range(R)]
+    pool = sum(nblk) + spare
+    perm = rng.permutation(pool).astype(np.int32)
+    table = np.full((R, max(nblk) + 1), -1, dtype=np.int32)
+    at = 0
+    for r in range(R):
+        table[r, :nblk[r]] = perm[at:at + nblk[r]]
+        at += nblk[r]
+    paged = np.full((Ls, pool * bs, H, d), np.nan)
+    for r in range(R):
+        for g in range(cu[r], cu[r + 1]):
+            p = int(pos[g])
+            paged[:, table[r, p // bs] * bs + p % bs] = src[:, g]
+    return paged, table
+
+
+@pytest.mark.parametrize("wide", [False, True])
+def test_paged_source_equals_contiguous_source_bit_for_bit(wide):
+    rng = np.random.default_rng(81)
+    lens, offs, bs = [7, 12, 5], [0, 3, 9], 4
+    Ls, Lt, H, d, k = 4, 2, 2, 8, 2
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    pos = np.concatenate([np.arange(n) for n in lens])
+    src_k = rng.standard_normal((Ls, T, H, d))
+    src_v = rng.standard_normal((Ls, T, H, d))
+    idx = np.stack([rng.permutation(Ls)[:k] for _ in range(Lt)]).astype(np.int32)
+    if wide:
+        w = rng.standard_normal((Lt, k * 2 * H * d, H * 2 * d))
+    else:
+        w = rng.standard_normal((Lt, H, 2, k * d, d))
+    b = rng.standard_normal((Lt, H, 2, d))
+    kw = dict(layer_idx=idx, w=w, b=b, theta_src=1e4, theta_tgt=5e5, max_position=24,
+              cu_seqlens=cu, tgt_offset=offs, dst_capacity=24, wide=wide)
+    ck, cv, cst = oracle.transfer(src_k=src_k, src_v=src_v, **kw)
+    pk, table = _scatter_paged_source(rng, src_k, cu, pos, bs)
+    # values through the same table
+    pv = np.full_like(pk, np.nan)
+    for r in range(3):
+        for g in range(cu[r], cu[r + 1]):
+            p = int(pos[g])
+            pv[:, table[r, p // bs] * bs + p % bs] = src_v[:, g]
+    gk, gv, gst = oracle.transfer(src_k=pk, src_v=pv, src_layout=oracle.PAGED,
+                                  src_block_size=bs, src_block_table=table, **kw)
+    assert cst == gst == 0
+    assert np.array_equal(np.isnan(ck), np.isnan(gk))
+    m = ~np.isnan(ck)
+    assert np.array_equal(ck[m], gk[m]) and np.array_equal(cv[m], gv[m])
+
+
+def test_paged_source_follows_explicit_source_positions():
+    # the slot is chosen by the token's source position, not its packed index
+    rng = np.random.default_rng(83)
+    Ls, Lt, H, d, k, T, bs = 3, 2, 1, 4, 1, 6, 2
+    src_k = rng.standard_normal((Ls, T, H, d))
+    src_v = rng.standard_normal((Ls, T, H, d))
+    idx = np.array([[2], [0]], dtype=np.int32)
+    w = rng.standard_normal((Lt, H, 2, k * d, d))
+    b = np.zeros((Lt, H, 2, d))
+    src_pos = np.array([5, 0, 3, 1, 4, 2])
+    cu = np.array([0, T])
+    kw = dict(layer_idx=idx, w=w, b=b, theta_src=1e4, theta_tgt=1e4, max_position=8,
+              cu_seqlens=cu, src_pos=src_pos, dst_capacity=8)
+    ck, cv, _ = oracle.transfer(src_k=src_k, src_v=src_v, **kw)
+    pk, table = _scatter_paged_source(rng, src_k, cu, src_pos, bs)
+    pv = np.full_like(pk, np.nan)
+    for g in range(T):
+        p = int(src_pos[g])
+        pv[:, table[0, p // bs] * bs + p % bs] = src_v[:, g]
+    gk, gv, st = oracle.transfer(src_k=pk, src_v=pv, src_layout=oracle.PAGED, src_block_size=bs,
+                                 src_block_table=table, **kw)
+    assert st == 0
+    m = ~np.isnan(ck)
+    assert np.array_equal(ck[m], gk[m]) and np.array_equal(cv[m], gv[m])
+
+
+def test_paged_source_bad_blocks_skip_and_flag():
+    # a -1 entry and a position past the table's width: those tokens are
+    # skipped (destination rows keep their NaN) with BAD_SRC_BLOCK; the source
+    # check comes before the destination check
+    rng = np.random.default_rng(87)
+    lens, bs = [6, 5], 2
+    Ls, Lt, H, d, k = 2, 1, 1, 4, 1
+    cu = np.array([0, 6, 11])
+    pos = np.concatenate([np.arange(n) for n in lens])
+    src = rng.standard_normal((Ls, 11, H, d))
+    pk, table = _scatter_paged_source(rng, src, cu, pos, bs)
+    table = table[:, :3].copy()            # request 0 needs blocks 0..2, request 1 0..2
+    table[1, 1] = -1                       # request 1, positions 2 and 3
+    narrow = table[:, :2].copy()           # request 0 positions 4, 5 past the width
+    w = np.tile(np.eye(d), (Lt, H, 2, 1, 1))
+    b = np.zeros((Lt, H, 2, d))
+    kw = dict(layer_idx=np.array([[1]], dtype=np.int32), w=w, b=b, theta_src=1e4,
+              theta_tgt=1e4, max_position=8, cu_seqlens=cu, dst_capacity=8,
+              src_layout=oracle.PAGED, src_block_size=bs)
+    dk, dv, st = oracle.transfer(src_k=pk, src_v=pk, src_block_table=table, **kw)
+    assert st == oracle.BAD_SRC_BLOCK
+    assert np.isnan(dv[0, 8 + 2]).all() and np.isnan(dv[0, 8 + 3]).all()
+    assert np.array_equal(dv[0, 8 + 4], src[1, 6 + 4])
+    assert np.array_equal(dv[0, 5], src[1, 5])
+    dk, dv, st = oracle.transfer(src_k=pk, src_v=pk, src_block_table=narrow, **kw)
+    assert st == oracle.BAD_SRC_BLOCK
+    assert np.isnan(dv[0, 4]).all() and np.isnan(dv[0, 5]).all()
+    assert np.array_equal(dv[0, 3], src[1, 3])
+    # capacity 4: the tokens at p' = 4, 5 have a bad source block AND a bad
+    # row; the source check comes first, so only BAD_SRC_BLOCK is reported
+    kw2 = dict(kw, dst_capacity=4)
+    _, _, st = oracle.transfer(src_k=pk, src_v=pk, src_block_table=narrow, **kw2)
+    assert st == oracle.BAD_SRC_BLOCK
+    # with the full table the same rows only fail the row check
+    _, _, st = oracle.transfer(src_k=pk, src_v=pk, src_block_table=table[:, :3], **kw2)
+    assert st == oracle.BAD_SRC_BLOCK | oracle.BAD_ROW
