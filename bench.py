@@ -57,6 +57,9 @@ def parse_args(argv=None):
                     help="per_head: one [k*d x d] map per (target layer, head, K|V); wide: one "
                          "[k*2*H*d x H*2*d] map per target layer (the 1.07e9-parameter "
                          "14B->32B mapper)")
+    ap.add_argument("--src-block-size", type=int, default=0,
+                    help="read the source from a paged pilot cache with this block size "
+                         "(0: packed source rows)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (profiling of small cases)")
     ap.add_argument("--tiles-per-item", type=int, default=0)
@@ -293,10 +296,13 @@ def kernel_code(name):
             "tcgen05": kvx.KVX_KERNEL_TCGEN05}[name]
 
 
-def transfer_kwargs(wl, inp, dst_k, dst_v, status):
+def transfer_kwargs(wl, inp, dst_k, dst_v, status, paged_src=None):
     from cross_model_kv_transfer_gb300.workloads import PAGED
     kw = dict(src_k=inp["src_k"], src_v=inp["src_v"], layer_idx=inp["layer_idx"], w=inp["w"],
               b=inp["b"], dst_k=dst_k, dst_v=dst_v, status=status)
+    if paged_src is not None:
+        kw.update(src_k=paged_src[0], src_v=paged_src[1], src_block_table=paged_src[2],
+                  ntok=wl.ntok)
     if wl.num_requests > 1 or wl.layout == PAGED:
         kw["cu_seqlens"] = inp["cu_seqlens"]
     if any(wl.tgt_offsets):
@@ -333,19 +339,25 @@ def run_kvx(args):
                     kernel=kernel_code(args.kernel), tiles_per_item=args.tiles_per_item,
                     flags=kvx.KVX_PLAN_TC_SINGLE_CTA if args.single_cta else 0,
                     mapper=kvx.KVX_MAPPER_WIDE if wide else kvx.KVX_MAPPER_PER_HEAD,
-                    max_tokens=wl.ntok if wide else 0)
+                    max_tokens=wl.ntok if (wide or args.src_block_size) else 0,
+                    src_layout=kvx.KVX_PAGED if args.src_block_size else kvx.KVX_CONTIGUOUS,
+                    src_block_size=args.src_block_size)
     kname = "wide" if wide else \
         {kvx.KVX_KERNEL_SIMT: "simt", kvx.KVX_KERNEL_TCGEN05: "tcgen05"}[plan.kernel]
     shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
     dst_k = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
     dst_v = torch.empty(shape, dtype=wl.kv_dtype, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    targs = plan.make_args(**transfer_kwargs(wl, inp, dst_k, dst_v, status))
+    paged_src = None
+    if args.src_block_size:
+        from cross_model_kv_transfer_gb300.workloads import make_paged_source
+        paged_src = make_paged_source(wl, inp, args.src_block_size)
+    targs = plan.make_args(**transfer_kwargs(wl, inp, dst_k, dst_v, status, paged_src))
     stream = torch.cuda.current_stream(dev)
     sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
     if args.op == "kv_diagnostics":
-        if wide:
-            raise SystemExit("kv_diagnostics bench: per-head mapper only")
+        if wide or paged_src is not None:
+            raise SystemExit("kv_diagnostics bench: per-head mapper, packed source only")
         if wl.layout != PAGED and any(wl.tgt_offsets):
             raise SystemExit("kv_diagnostics bench: contiguous workloads with offset 0 only")
         run_diag(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, ws, rank)
@@ -381,7 +393,7 @@ def run_kvx(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status)
+        e2e = run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, paged_src)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -408,6 +420,8 @@ def run_kvx(args):
                    "layout": "paged" if wl.layout == PAGED else "contiguous",
                    "kernel": kname, "cta_group": plan.cta_group,
                    "mapper": args.mapper,
+                   "source": (f"paged, {args.src_block_size}-token blocks"
+                              if args.src_block_size else "packed rows"),
                    "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (source "
                          f"{inp['src_k'].numel() * 2 * inp['src_k'].element_size() / 1e9:.2f} GB,"
@@ -575,19 +589,24 @@ def time_oracle_diag(wl, mk, mv, rk, rv, target_seconds: float):
                       f"({el:.1f} s of fp64 CPU work, one thread)"}
 
 
-def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status):
+def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, paged_src=None):
     """Same metric through the C ABI with HOST buffers: every step copies its
     inputs from pinned host memory, transfers, and reads the target cache back."""
     import torch
     from cross_model_kv_transfer_gb300 import kvx
+    src = dict(inp)
+    if paged_src is not None:
+        src.update(src_k=paged_src[0], src_v=paged_src[1], src_block_table=paged_src[2])
     names = ["src_k", "src_v", "w", "b", "layer_idx", "cu_seqlens", "tgt_offset"]
-    if "block_table" in inp:
-        names.append("block_table")
-    host = {n: inp[n].cpu().pin_memory() for n in names}
+    names += [n for n in ("block_table", "src_block_table") if n in src]
+    host = {n: src[n].cpu().pin_memory() for n in names}
     hk = torch.empty(dst_k.shape, dtype=dst_k.dtype, pin_memory=True)
     hv = torch.empty(dst_v.shape, dtype=dst_v.dtype, pin_memory=True)
-    dev_in = {n: torch.empty_like(inp[n]) for n in names}
-    targs = plan.make_args(**transfer_kwargs(wl, dev_in, dst_k, dst_v, status))
+    dev_in = {n: torch.empty_like(src[n]) for n in names}
+    dev_paged = None
+    if paged_src is not None:
+        dev_paged = (dev_in["src_k"], dev_in["src_v"], dev_in["src_block_table"])
+    targs = plan.make_args(**transfer_kwargs(wl, dev_in, dst_k, dst_v, status, dev_paged))
     sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = hk.numel() * hk.element_size() * 2

@@ -38,6 +38,8 @@ kvx_status validate_desc(const kvx_plan_desc *d) {
   if (d->flags & ~(KVX_PLAN_TEST_STALL | KVX_PLAN_TC_SINGLE_CTA)) return KVX_ERR_INVALID_ARG;
   if (d->mapper != KVX_MAPPER_PER_HEAD && d->mapper != KVX_MAPPER_WIDE) return KVX_ERR_INVALID_ARG;
   if (d->max_tokens < 0) return KVX_ERR_INVALID_ARG;
+  if (d->src_layout != KVX_CONTIGUOUS && d->src_layout != KVX_PAGED) return KVX_ERR_INVALID_ARG;
+  if (d->src_layout == KVX_PAGED && d->src_block_size < 1) return KVX_ERR_INVALID_ARG;
   // "Requirements": same number of KV heads and the same per-head dimension.
   if (d->src_kv_heads != d->tgt_kv_heads || d->src_head_dim != d->tgt_head_dim)
     return KVX_ERR_PAIR_MISMATCH;
@@ -147,8 +149,27 @@ void free_tables(kvx_plan *p) {
   if (p->rope_src) cudaFree(p->rope_src);
   if (p->workspace) cudaFree(p->workspace);
   if (p->tc_rope_src) cudaFree(p->tc_rope_src);
+  if (p->packed_k) cudaFree(p->packed_k);
+  if (p->packed_v) cudaFree(p->packed_v);
   p->rope_src = p->rope_tgt = nullptr;
   p->workspace = p->tc_rope_src = nullptr;
+  p->packed_k = p->packed_v = nullptr;
+}
+
+kvx_status alloc_bytes(void **ptr, size_t bytes) {
+  *ptr = nullptr;
+  if (bytes == 0) return KVX_OK;
+  cudaError_t e = cudaMalloc(ptr, bytes);
+  if (e == cudaErrorMemoryAllocation) {
+    cudaGetLastError();
+    *ptr = nullptr;
+    return KVX_ERR_NO_MEMORY;
+  }
+  if (e != cudaSuccess) {
+    *ptr = nullptr;
+    return KVX_ERR_CUDA;
+  }
+  return KVX_OK;
 }
 
 kvx_status alloc_workspace(kvx_plan *p, size_t bytes) {
@@ -254,6 +275,14 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
          : alloc_workspace(p, wide ? kvx_wide_workspace_bytes(*desc, p->max_tokens)
                                    : kvx_tc_workspace_bytes(*desc));
   }
+  if (st == KVX_OK && kernel == KVX_KERNEL_TCGEN05 && desc->src_layout == KVX_PAGED) {
+    // packed rows of a paged source (values only for the wide map, whose
+    // workspace holds the un-rotated keys)
+    const size_t bytes = (size_t)desc->src_layers * (size_t)p->max_tokens *
+                         desc->src_kv_heads * desc->src_head_dim * 2;
+    st = alloc_bytes(&p->packed_v, bytes);
+    if (st == KVX_OK && !wide) st = alloc_bytes(&p->packed_k, bytes);
+  }
   if (st == KVX_OK) {
     cudaError_t e = wide ? kvx_wide_prepare(p)
                          : kernel == KVX_KERNEL_TCGEN05 ? kvx_tc_prepare(p) : kvx_simt_prepare(p);
@@ -287,8 +316,10 @@ int32_t kvx_plan_kernel(const kvx_plan *plan) { return plan ? plan->kernel : -1;
 
 int32_t kvx_plan_launches(const kvx_plan *plan) {
   if (!plan) return -1;
-  if (plan->desc.mapper == KVX_MAPPER_WIDE) return 3;  // un-rotated keys, W image, map
-  return plan->kernel == KVX_KERNEL_TCGEN05 ? 2 : 1;  // W image + transfer, or transfer
+  // a paged source adds the packing launch on the tensor-core paths
+  const int pack = plan->kernel == KVX_KERNEL_TCGEN05 && plan->desc.src_layout == KVX_PAGED;
+  if (plan->desc.mapper == KVX_MAPPER_WIDE) return 3 + pack;  // un-rotated keys, W image, map
+  return (plan->kernel == KVX_KERNEL_TCGEN05 ? 2 : 1) + pack;  // W image + transfer, or transfer
 }
 
 int32_t kvx_plan_cta_group(const kvx_plan *plan) {
@@ -321,7 +352,11 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   if (cudaGetDevice(&cur) != cudaSuccess) return KVX_ERR_CUDA;
   if (cur != plan->device) return KVX_ERR_INVALID_ARG;
   const bool wide = d.mapper == KVX_MAPPER_WIDE;
-  if (wide && a->ntok > plan->max_tokens) return KVX_ERR_INVALID_ARG;
+  const bool src_paged = d.src_layout == KVX_PAGED;
+  if (src_paged && (a->src_num_blocks < 1 || !a->src_block_table || a->max_src_blocks_per_req < 1))
+    return KVX_ERR_INVALID_ARG;
+  if ((wide || (src_paged && plan->kernel == KVX_KERNEL_TCGEN05)) && a->ntok > plan->max_tokens)
+    return KVX_ERR_INVALID_ARG;
   if (a->ntok == 0) return KVX_OK;  // nothing to transfer; status untouched
 
   KvxParams p;
@@ -357,6 +392,12 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   p.layout = d.dst_layout;
   p.block_size = d.block_size;
   p.max_position = d.max_position;
+  p.src_layout = d.src_layout;
+  p.src_block_size = src_paged ? d.src_block_size : 1;
+  p.src_max_blocks = src_paged ? a->max_src_blocks_per_req : 0;
+  p.src_num_blocks = src_paged ? a->src_num_blocks : 0;
+  p.src_block_table = src_paged ? a->src_block_table : nullptr;
+  p.src_rows = src_paged ? a->src_num_blocks * (int64_t)d.src_block_size : a->ntok;
 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = wide ? kvx_wide_launch(plan, p, s)

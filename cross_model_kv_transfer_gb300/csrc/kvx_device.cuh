@@ -45,9 +45,15 @@ __device__ __forceinline__ int request_of(const KvxParams &p, int64_t g) {
 // Source position p, target position p' and destination row of packed
 // source row g.  Returns 0 and sets row >= 0, or the KVX_FLAG_* reason with
 // row = -1.
+// Also sets srow, the row of token g in the source arrays: g for a
+// contiguous source, src_block_table[r][p / bs] * bs + p % bs for a paged one
+// (the pilot's own paged cache holds its tokens at their source positions).
+// The checks run in the order positions, source row, destination row; the
+// first that fails is returned (srow and row stay -1 from there on).
 __device__ __forceinline__ uint32_t token_meta(const KvxParams &p, int64_t g, int32_t &ps,
-                                               int32_t &pt, int64_t &row) {
+                                               int32_t &pt, int64_t &row, int64_t &srow) {
   row = -1;
+  srow = -1;
   const int r = request_of(p, g);
   const int64_t beg = p.cu_seqlens ? (int64_t)p.cu_seqlens[r] : 0;
   const int64_t sp = p.src_pos ? (int64_t)p.src_pos[g] : g - beg;
@@ -57,6 +63,15 @@ __device__ __forceinline__ uint32_t token_meta(const KvxParams &p, int64_t g, in
     return KVX_FLAG_BAD_POSITION;
   ps = (int32_t)sp;
   pt = (int32_t)tp;
+  if (p.src_layout == KVX_PAGED) {
+    const int64_t logical = sp / p.src_block_size;
+    if (logical >= p.src_max_blocks) return KVX_FLAG_BAD_SRC_BLOCK;
+    const int64_t phys = p.src_block_table[(int64_t)r * p.src_max_blocks + logical];
+    if (phys < 0 || phys >= p.src_num_blocks) return KVX_FLAG_BAD_SRC_BLOCK;
+    srow = phys * p.src_block_size + sp % p.src_block_size;
+  } else {
+    srow = g;
+  }
   if (p.layout == KVX_CONTIGUOUS) {
     if (tp >= p.dst_capacity) return KVX_FLAG_BAD_ROW;
     row = (int64_t)r * p.dst_capacity + tp;
@@ -68,6 +83,12 @@ __device__ __forceinline__ uint32_t token_meta(const KvxParams &p, int64_t g, in
   if (phys < 0 || phys >= p.num_blocks) return KVX_FLAG_BAD_BLOCK;
   row = phys * p.block_size + tp % p.block_size;
   return 0;
+}
+
+__device__ __forceinline__ uint32_t token_meta(const KvxParams &p, int64_t g, int32_t &ps,
+                                               int32_t &pt, int64_t &row) {
+  int64_t srow;
+  return token_meta(p, g, ps, pt, row, srow);
 }
 
 // True if every selected source layer of target layer lt lies in [0, Ls).

@@ -349,6 +349,8 @@ extern "C" kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_ar
   p.layout = d.dst_layout;
   p.block_size = d.block_size;
   p.max_position = d.max_position;
+  p.src_layout = KVX_CONTIGUOUS;   // the source is not read: target-side rules only
+  p.src_rows = a->ntok;
   P.mk = a->mapped_k;
   P.mv = a->mapped_v;
   P.rk = a->ref_k;

@@ -36,6 +36,10 @@ struct kvx_plan {
   // wide-feature mapper: the workspace holds the bf16 W image, the fp32
   // bias and the un-rotated source keys [Ls][max_tokens][H][d]
   int64_t max_tokens;
+  // tensor-core plans with a paged source: the rows the kernels read, packed
+  // into [Ls][max_tokens][H][d] buffers (keys and values; values only for
+  // the wide map, whose workspace already holds the un-rotated keys)
+  void *packed_k, *packed_v;
   int stall_test;        // KVX_PLAN_TEST_STALL: failure-detection test hook
   int tc_pairs;          // tensor-core path: CTA pairs resident at once (0: single CTAs)
 };
@@ -52,12 +56,23 @@ struct KvxParams {
   int64_t ntok, dst_capacity, num_blocks, dst_rows;
   int32_t R, max_blocks;
   int32_t Ls, Lt, H, d, k, layout, block_size, max_position;
+  // source layout: CONTIGUOUS (row g) or PAGED (through src_block_table);
+  // src_rows = rows per source layer of the arrays src_k / src_v point at
+  int32_t src_layout, src_block_size, src_max_blocks;
+  int64_t src_num_blocks, src_rows;
+  const int32_t *src_block_table;
 };
 
 // Per-kernel launchers; return cudaSuccess or the launch error.
 cudaError_t kvx_simt_prepare(const kvx_plan *plan);
 cudaError_t kvx_simt_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s);
 bool kvx_simt_supports(const kvx_plan_desc &d);
+
+// Packs the source rows of a paged source into [Ls][out_rows][H][d]
+// buffers (either may be NULL to skip it); rows whose position or source
+// block is out of range are written as zeros.
+cudaError_t kvx_pack_source(const KvxParams &p, void *out_k, void *out_v, int64_t out_rows,
+                            int elem_bytes, cudaStream_t s);
 
 bool kvx_wide_supports(const kvx_plan_desc &d);
 size_t kvx_wide_workspace_bytes(const kvx_plan_desc &d, int64_t max_tokens);

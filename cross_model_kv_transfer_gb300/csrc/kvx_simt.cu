@@ -38,7 +38,8 @@ int row_groups(int half) { return half >= kThreads ? 1 : kThreads / half; }
 
 size_t smem_bytes(int half, int kd) {
   const int tt = kRowsPerThread * row_groups(half);
-  return (size_t)tt * (kd + 1) * sizeof(float) + (size_t)tt * (sizeof(int64_t) + 2 * sizeof(int32_t));
+  return (size_t)tt * (kd + 1) * sizeof(float) +
+         (size_t)tt * (2 * sizeof(int64_t) + 2 * sizeof(int32_t));
 }
 
 template <typename KT, typename WT, typename BT>
@@ -51,7 +52,8 @@ __global__ void __launch_bounds__(kThreads) simt_transfer_kernel(KvxParams p) {
   const int ldx = kd + 1;
   float *X = reinterpret_cast<float *>(smem_raw);
   int64_t *s_row = reinterpret_cast<int64_t *>(X + (size_t)TT * ldx);
-  int32_t *s_ps = reinterpret_cast<int32_t *>(s_row + TT);
+  int64_t *s_srow = s_row + TT;                  // row of the token in the source arrays
+  int32_t *s_ps = reinterpret_cast<int32_t *>(s_srow + TT);
   int32_t *s_pt = s_ps + TT;
   __shared__ uint32_t s_bits;
   __shared__ int s_layer_ok;
@@ -77,12 +79,13 @@ __global__ void __launch_bounds__(kThreads) simt_transfer_kernel(KvxParams p) {
   if (tid < TT) {
     const int64_t g = t0 + tid;
     int32_t ps = 0, pt = 0;
-    int64_t row = -1;
+    int64_t row = -1, srow = -1;
     if (g < p.ntok) {
-      const uint32_t bad = kvx::token_meta(p, g, ps, pt, row);
+      const uint32_t bad = kvx::token_meta(p, g, ps, pt, row, srow);
       if (bad) atomicOr(&s_bits, bad);
     }
     s_row[tid] = row;
+    s_srow[tid] = srow;
     s_ps[tid] = ps;
     s_pt[tid] = pt;
   }
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) simt_transfer_kernel(KvxParams p) {
   const KT *src = reinterpret_cast<const KT *>(m == 0 ? p.src_k : p.src_v);
   for (int q = ty; q < TT; q += G) {
     if (s_row[q] < 0) continue;
-    const int64_t g = t0 + q;
+    const int64_t srow = s_srow[q];
     for (int i = tx; i < half; i += blockDim.x) {
       float c = 1.f, s = 0.f;
       if (m == 0) {
@@ -110,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) simt_transfer_kernel(KvxParams p) {
       }
       for (int j = 0; j < p.k; ++j) {
         const int sl = p.layer_idx[lt * p.k + j];
-        const KT *v = src + (((int64_t)sl * p.ntok + g) * p.H + h) * p.d;
+        const KT *v = src + (((int64_t)sl * p.src_rows + srow) * p.H + h) * p.d;
         const float x0 = ldf(v + i), x1 = ldf(v + i + half);
         // un-rotate: multiply (x0 + j x1) by exp(-j p w_i)
         X[q * ldx + j * p.d + i] = m == 0 ? fmaf(x0, c, x1 * s) : x0;
@@ -271,7 +274,9 @@ extern "C" kvx_status kvx_transfer_static(const kvx_plan_desc *desc,
       (d.dst_layout != KVX_CONTIGUOUS && d.dst_layout != KVX_PAGED) ||
       (d.dst_layout == KVX_PAGED && d.block_size < 1) || d.max_position < 1 ||
       (d.kernel != KVX_KERNEL_AUTO && d.kernel != KVX_KERNEL_SIMT) || d.flags != 0 ||
-      d.mapper != KVX_MAPPER_PER_HEAD)
+      d.mapper != KVX_MAPPER_PER_HEAD ||
+      (d.src_layout != KVX_CONTIGUOUS && d.src_layout != KVX_PAGED) ||
+      (d.src_layout == KVX_PAGED && d.src_block_size < 1))
     return KVX_ERR_INVALID_ARG;
   if (d.src_kv_heads != d.tgt_kv_heads || d.src_head_dim != d.tgt_head_dim)
     return KVX_ERR_PAIR_MISMATCH;
@@ -288,6 +293,9 @@ extern "C" kvx_status kvx_transfer_static(const kvx_plan_desc *desc,
   if (d.dst_layout == KVX_CONTIGUOUS ? a->dst_capacity < 1
                                      : (a->num_blocks < 1 || !a->block_table ||
                                         a->max_blocks_per_req < 1))
+    return KVX_ERR_INVALID_ARG;
+  const bool src_paged = d.src_layout == KVX_PAGED;
+  if (src_paged && (a->src_num_blocks < 1 || !a->src_block_table || a->max_src_blocks_per_req < 1))
     return KVX_ERR_INVALID_ARG;
 
   int dev = -1;
@@ -368,5 +376,11 @@ extern "C" kvx_status kvx_transfer_static(const kvx_plan_desc *desc,
   p.layout = d.dst_layout;
   p.block_size = d.block_size;
   p.max_position = d.max_position;
+  p.src_layout = d.src_layout;
+  p.src_block_size = src_paged ? d.src_block_size : 1;
+  p.src_max_blocks = src_paged ? a->max_src_blocks_per_req : 0;
+  p.src_num_blocks = src_paged ? a->src_num_blocks : 0;
+  p.src_block_table = src_paged ? a->src_block_table : nullptr;
+  p.src_rows = src_paged ? a->src_num_blocks * (int64_t)d.src_block_size : a->ntok;
   return kvx_simt_launch(&tmp, p, s) == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }

@@ -781,7 +781,7 @@ bool encode_map(const kvx_plan *plan, CUtensorMap *map, const void *base, const 
   const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)p.H, (cuuint64_t)p.ntok,
                               (cuuint64_t)p.Ls};
   const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)p.H * kD * 2,
-                                 (cuuint64_t)p.ntok * p.H * kD * 2};
+                                 (cuuint64_t)p.src_rows * p.H * kD * 2};
   const cuuint32_t box[4] = {(cuuint32_t)kHalf, 1u, (cuuint32_t)kTileM, 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
@@ -864,8 +864,19 @@ cudaError_t kvx_tc_prepare(kvx_plan *plan) {
   return cudaSuccess;
 }
 
-cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p, cudaStream_t s) {
+cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p_in, cudaStream_t s) {
   const kvx_plan_desc &d = plan->desc;
+  // 0. a paged source: its rows gathered into packed order first (the TMA
+  // boxes read 128 consecutive rows); the kernel still applies the source
+  // block checks to skip and flag the tokens it cannot read
+  KvxParams p = p_in;
+  if (p.src_layout == KVX_PAGED) {
+    cudaError_t pe = kvx_pack_source(p, plan->packed_k, plan->packed_v, plan->max_tokens, 2, s);
+    if (pe != cudaSuccess) return pe;
+    p.src_k = plan->packed_k;
+    p.src_v = plan->packed_v;
+    p.src_rows = plan->max_tokens;
+  }
   // 1. W -> bf16 image in the plan workspace
   dim3 wgrid((unsigned)((int64_t)p.Lt * p.H * 2), (unsigned)(2 * p.k));
   uint4 *img = reinterpret_cast<uint4 *>(plan->workspace);

@@ -472,10 +472,11 @@ __global__ void __launch_bounds__(256) wide_unrotate_kernel(const __grid_constan
   const int h = rem >> 3, q = rem & 7;
   const int s = blockIdx.y;
   int32_t ps = 0, pt = 0;
-  int64_t row = -1;
-  const bool pos_ok = kvx::token_meta(p, g, ps, pt, row) != KVX_FLAG_BAD_POSITION;
-  const __nv_bfloat16 *src =
-      reinterpret_cast<const __nv_bfloat16 *>(p.src_k) + (((int64_t)s * p.ntok + g) * p.H + h) * kWD;
+  int64_t row = -1, srow = -1;
+  kvx::token_meta(p, g, ps, pt, row, srow);
+  const bool pos_ok = srow >= 0;   // a valid position and, if paged, source block
+  const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(p.src_k) +
+                             (((int64_t)s * p.src_rows + (pos_ok ? srow : 0)) * p.H + h) * kWD;
   __nv_bfloat16 *dst = out + (((int64_t)s * out_tokens + g) * p.H + h) * kWD;
   uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
   if (pos_ok) {
@@ -678,9 +679,19 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   geo.sync = sync;
   geo.epochs_per_tile = (KC + kWSyncSteps - 1) / kWSyncSteps;
   geo.max_epochs = (int)((geo.num_tiles + geo.stride - 1) / geo.stride) * geo.epochs_per_tile;
+  // values: read in place, or (paged source) packed first into the plan's
+  // buffer; the keys' pre-pass above read a paged source directly
+  const void *vals = p.src_v;
+  int64_t val_rows = p.src_rows;
+  if (p.src_layout == KVX_PAGED) {
+    e = kvx_pack_source(p, nullptr, plan->packed_v, plan->max_tokens, 2, s);
+    if (e != cudaSuccess) return e;
+    vals = plan->packed_v;
+    val_rows = plan->max_tokens;
+  }
   CUtensorMap mk, mv;
   if (!encode_wide_map(plan, &mk, content, p.ntok, plan->max_tokens, p.H, p.Ls) ||
-      !encode_wide_map(plan, &mv, p.src_v, p.ntok, p.ntok, p.H, p.Ls))
+      !encode_wide_map(plan, &mv, vals, p.ntok, val_rows, p.H, p.Ls))
     return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * geo.stride), 1, 1);

@@ -39,6 +39,7 @@ KVX_FLAG_BAD_BLOCK = 4
 KVX_FLAG_BAD_ROW = 8
 KVX_FLAG_TIMEOUT = 16
 KVX_FLAG_BAD_SEQLENS = 32
+KVX_FLAG_BAD_SRC_BLOCK = 64
 
 KVX_F32 = 0
 KVX_BF16 = 1
@@ -69,6 +70,7 @@ class PlanDesc(ctypes.Structure):
         ("max_position", ctypes.c_int32), ("kernel", ctypes.c_int32),
         ("tiles_per_item", ctypes.c_int32), ("flags", ctypes.c_int32),
         ("mapper", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+        ("src_layout", ctypes.c_int32), ("src_block_size", ctypes.c_int32),
     ]
 
 
@@ -84,6 +86,8 @@ class TransferArgs(ctypes.Structure):
         ("dst_capacity", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
         ("block_table", ctypes.c_void_p), ("max_blocks_per_req", ctypes.c_int32),
         ("status", ctypes.c_void_p),
+        ("src_num_blocks", ctypes.c_int64), ("src_block_table", ctypes.c_void_p),
+        ("max_src_blocks_per_req", ctypes.c_int32),
     ]
 
 
@@ -207,7 +211,8 @@ class Plan:
                  rope_theta_tgt, max_position, kv_dtype, w_dtype, b_dtype,
                  layout=KVX_CONTIGUOUS, block_size=0, kernel=KVX_KERNEL_AUTO,
                  tgt_kv_heads=None, tgt_head_dim=None, tiles_per_item=0, flags=0,
-                 mapper=KVX_MAPPER_PER_HEAD, max_tokens=0):
+                 mapper=KVX_MAPPER_PER_HEAD, max_tokens=0, src_layout=KVX_CONTIGUOUS,
+                 src_block_size=0):
         self.desc = PlanDesc(
             src_layers, tgt_layers, kv_heads,
             kv_heads if tgt_kv_heads is None else tgt_kv_heads,
@@ -215,7 +220,8 @@ class Plan:
             float(rope_theta_src), float(rope_theta_tgt),
             _dtype_code(kv_dtype), _dtype_code(w_dtype), _dtype_code(b_dtype),
             int(layout), int(block_size), int(max_position), int(kernel),
-            int(tiles_per_item), int(flags), int(mapper), int(max_tokens))
+            int(tiles_per_item), int(flags), int(mapper), int(max_tokens), int(src_layout),
+            int(src_block_size))
         self.kv_dtype, self.w_dtype, self.b_dtype = kv_dtype, w_dtype, b_dtype
         st, h = kvx_plan_create(self.desc)
         if st != KVX_OK:
@@ -248,8 +254,10 @@ class Plan:
     def make_args(self, *, src_k, src_v, layer_idx, w, b, dst_k, dst_v, cu_seqlens=None,
                   src_pos=None, tgt_pos=None, tgt_offset=None,
                   dst_capacity=None, num_blocks=None, block_table=None,
-                  status=None) -> TransferArgs:
-        """Check tensors against the plan and pack a ``TransferArgs``."""
+                  status=None, ntok=None, src_block_table=None) -> TransferArgs:
+        """Check tensors against the plan and pack a ``TransferArgs``.  A
+        paged source ([Ls][src_num_blocks*src_block_size][H][d]) needs
+        ``src_block_table`` [R][max] and ``ntok`` (the packed token count)."""
         import torch
         d = self.desc
         Ls, Lt, H, hd, k = d.src_layers, d.tgt_layers, d.src_kv_heads, d.src_head_dim, d.k
@@ -269,11 +277,22 @@ class Plan:
                 raise ValueError(f"{name} must have {ndim} dims")
             return t.data_ptr()
 
-        ntok = src_k.shape[1]
         R = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
         a = TransferArgs()
-        a.src_k = ptr(src_k, "src_k", self.kv_dtype, (Ls, ntok, H, hd))
-        a.src_v = ptr(src_v, "src_v", self.kv_dtype, (Ls, ntok, H, hd))
+        if d.src_layout == KVX_PAGED:
+            if ntok is None or src_block_table is None:
+                raise ValueError("a paged source needs ntok and src_block_table")
+            src_rows = src_k.shape[1]
+            if src_rows % d.src_block_size:
+                raise ValueError("source rows must be whole blocks")
+            a.src_num_blocks = src_rows // d.src_block_size
+            a.src_block_table = ptr(src_block_table, "src_block_table", torch.int32, ndim=2)
+            a.max_src_blocks_per_req = int(src_block_table.shape[1])
+        else:
+            ntok = src_k.shape[1] if ntok is None else int(ntok)
+            src_rows = ntok
+        a.src_k = ptr(src_k, "src_k", self.kv_dtype, (Ls, src_rows, H, hd))
+        a.src_v = ptr(src_v, "src_v", self.kv_dtype, (Ls, src_rows, H, hd))
         a.ntok = ntok
         a.num_requests = R
         a.cu_seqlens = ptr(cu_seqlens, "cu_seqlens", torch.int32, (R + 1,))
@@ -300,7 +319,7 @@ class Plan:
         a.dst_v = ptr(dst_v, "dst_v", self.kv_dtype, (Lt, rows, H, hd))
         a.status = ptr(status, "status", torch.int32, (1,))
         a._keep = (src_k, src_v, cu_seqlens, layer_idx, w, b, src_pos, tgt_pos, tgt_offset,
-                   dst_k, dst_v, block_table, status)
+                   dst_k, dst_v, block_table, status, src_block_table)
         return a
 
     def transfer(self, stream=None, **tensors) -> None:

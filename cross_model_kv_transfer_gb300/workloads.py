@@ -253,6 +253,38 @@ def make_wide_weights(wl: Workload, device="cpu", seed: Optional[int] = None) ->
     return w
 
 
+def make_paged_source(wl: Workload, inp: dict, block_size: int, seed: Optional[int] = None,
+                      spare_blocks: int = 3):
+    """The pilot's own paged cache holding the same tokens as the packed
+    source of ``inp``: each request's blocks are dealt from a seeded random
+    permutation of a shared pool (plus ``spare_blocks`` unused ones), and the
+    token at position p of request r sits in slot p % block_size of its
+    request's block p // block_size.  Unused slots hold the all-ones bit
+    pattern.  Returns (src_k, src_v, src_block_table [R][max], -1 padded)."""
+    seed = (wl.seed if seed is None else seed) + 4000037
+    g = _gen("cpu", seed)
+    nb = [(n + block_size - 1) // block_size for n in wl.seqlens]
+    pool = int(sum(nb)) + spare_blocks
+    perm = torch.randperm(pool, generator=g).to(torch.int32)
+    table = torch.full((wl.num_requests, max(nb) + 1), -1, dtype=torch.int32)
+    at = 0
+    rows = []
+    for r, n in enumerate(wl.seqlens):
+        table[r, :nb[r]] = perm[at: at + nb[r]]
+        at += nb[r]
+        pos = torch.arange(n)
+        rows.append(table[r, pos // block_size].long() * block_size + pos % block_size)
+    dev = inp["src_k"].device
+    rows = torch.cat(rows).to(dev)
+    out = []
+    for src in (inp["src_k"], inp["src_v"]):
+        paged = sentinel_like((src.shape[0], pool * block_size) + tuple(src.shape[2:]), src.dtype,
+                              dev)
+        paged[:, rows] = src
+        out.append(paged)
+    return out[0], out[1], table.to(dev)
+
+
 def make_block_table(wl: Workload, seed: int) -> torch.Tensor:
     """Per-request block tables dealt, in request order, from a seeded random
     permutation of the shared pool of ``wl.num_blocks`` blocks; unused

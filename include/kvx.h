@@ -83,6 +83,9 @@ typedef enum {
 #define KVX_FLAG_BAD_SEQLENS    32u  /* cu_seqlens does not start at 0, runs
                                         backwards or does not end at ntok:
                                         nothing is written                   */
+#define KVX_FLAG_BAD_SRC_BLOCK  64u  /* paged source: p/src_bs >=
+                                        max_src_blocks_per_req, or the block
+                                        id outside [0, src_num_blocks)       */
 
 typedef enum { KVX_F32 = 0, KVX_BF16 = 1 } kvx_dtype;
 typedef enum { KVX_CONTIGUOUS = 0, KVX_PAGED = 1 } kvx_layout;
@@ -135,10 +138,16 @@ typedef struct {
   int32_t flags;            /* KVX_PLAN_* bits; 0 for normal use            */
   int32_t mapper;           /* kvx_mapper; WIDE needs the tensor-core kernel
                                (bf16 K/V, head_dim 128)                     */
-  int32_t max_tokens;       /* WIDE: the most source tokens (ntok) one
-                               transfer may carry; sizes the plan's buffer of
-                               un-rotated source keys ([Ls][max_tokens][H][d]
-                               bf16); 0 = max_position.  Ignored otherwise  */
+  int32_t max_tokens;       /* WIDE, or a PAGED source on the tensor-core
+                               kernel: the most source tokens (ntok) one
+                               transfer may carry; sizes the plan's buffers
+                               of packed / un-rotated source rows
+                               ([Ls][max_tokens][H][d] each); 0 =
+                               max_position.  Ignored otherwise             */
+  int32_t src_layout;       /* kvx_layout of the SOURCE cache: CONTIGUOUS
+                               (packed rows) or PAGED (the pilot's own paged
+                               cache, read through a source block table)    */
+  int32_t src_block_size;   /* tokens per source block, PAGED source only   */
 } kvx_plan_desc;
 
 /* Failure-detection test hook (tensor-core path): the warps that fill the
@@ -159,8 +168,13 @@ typedef struct kvx_plan kvx_plan; /* opaque */
  * the element type fixed by the plan.  ntok = total source tokens of all
  * requests, packed request after request. */
 typedef struct {
-  const void *src_k;          /* [Ls][ntok][H][d]  source keys (RoPE-rotated) */
-  const void *src_v;          /* [Ls][ntok][H][d]  source values              */
+  const void *src_k;          /* CONTIGUOUS source: [Ls][ntok][H][d] source keys
+                                 (RoPE-rotated), token g at row g.  PAGED
+                                 source: [Ls][src_num_blocks*src_bs][H][d],
+                                 token g of request r at source position p at
+                                 row src_block_table[r][p/src_bs]*src_bs +
+                                 p % src_bs (the pilot's paged cache)        */
+  const void *src_v;          /* source values, same layout as src_k          */
   int64_t ntok;               /* >= 0 (0: nothing to do)                      */
   int32_t num_requests;       /* R >= 1                                       */
   const int32_t *cu_seqlens;  /* [R+1] request r owns source rows
@@ -192,6 +206,9 @@ typedef struct {
   int32_t max_blocks_per_req; /* PAGED: >= 1                                  */
   uint32_t *status;           /* optional device word; KVX_FLAG_* bits are
                                  OR-ed in (never cleared by the library)     */
+  int64_t src_num_blocks;     /* PAGED source: blocks in the source pool      */
+  const int32_t *src_block_table; /* PAGED source: [R][max_src_blocks_per_req] */
+  int32_t max_src_blocks_per_req; /* PAGED source: >= 1                        */
 } kvx_transfer_args;
 
 /* Validate the descriptor and prepare the plan on the current device: for
@@ -212,12 +229,18 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out);
  * Returns KVX_ERR_INVALID_ARG for a NULL plan/args or a missing required
  * pointer or size, and, for a tensor-core plan, for source bases that are
  * not 16-byte aligned or cache bases that are not 32-byte aligned, and, for a
- * WIDE plan, for ntok > max_tokens; KVX_ERR_CUDA if a launch fails.
+ * WIDE plan or a tensor-core plan with a PAGED source, for ntok >
+ * max_tokens; KVX_ERR_CUDA if a launch fails.
  * Device-detected errors are reported through args->status as described
  * above.  A WIDE plan's transfer runs three kernels: the source keys of all
  * layers un-rotated into the plan's buffer, W into a bf16 image, and the
  * map as one tensor-core contraction per (target layer, 256 tokens, head)
- * with bias, re-rotation and the cache install in its epilogue. */
+ * with bias, re-rotation and the cache install in its epilogue.  With a
+ * PAGED source the SIMT kernel reads the source rows through the source
+ * block table directly; the tensor-core kernels first pack the rows they
+ * read (every layer's keys and values, or the values for WIDE, whose key
+ * pre-pass reads the paged keys itself) into the plan's buffers, one more
+ * launch. */
 kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *args,
                         void *stream);
 
@@ -282,9 +305,11 @@ typedef struct {
  *       target RoPE base, values as stored).
  * Mean cosine = [1] / [0]; explained variance (centred R^2, summed over the
  * d dimensions) = 1 - [2] / ([3] - |[4..]|^2 / [0]).  The tokens compared are
- * the ones a transfer with the same arguments writes; rows it would skip are
- * skipped with the same KVX_FLAG_* bits (a malformed request table: all stats
- * 0 and KVX_FLAG_BAD_SEQLENS).  Sums are formed in fp32 per thread and
+ * the ones a transfer with the same request table, positions and destination
+ * layout writes; rows it would skip for those reasons are skipped with the
+ * same KVX_FLAG_* bits (a malformed request table: all stats 0 and
+ * KVX_FLAG_BAD_SEQLENS).  The source side is not read (a paged source's block
+ * table plays no part).  Sums are formed in fp32 per thread and
  * combined in fp64; the order of the fp64 additions is not fixed.
  * Asynchronous on `stream`, no allocation, two kernel launches (clear the
  * stats, accumulate).  Returns KVX_ERR_INVALID_ARG for a NULL plan/args, a

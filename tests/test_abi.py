@@ -82,6 +82,10 @@ def _desc(**over):
     (dict(dst_layout=kvx.KVX_PAGED, block_size=0), kvx.KVX_ERR_INVALID_ARG),
     (dict(max_position=0), kvx.KVX_ERR_INVALID_ARG),
     (dict(kernel=9), kvx.KVX_ERR_INVALID_ARG),
+    (dict(mapper=2), kvx.KVX_ERR_INVALID_ARG),
+    (dict(max_tokens=-1), kvx.KVX_ERR_INVALID_ARG),
+    (dict(src_layout=2), kvx.KVX_ERR_INVALID_ARG),
+    (dict(src_layout=kvx.KVX_PAGED, src_block_size=0), kvx.KVX_ERR_INVALID_ARG),
     # "Requirements": same number of KV heads and the same head dimension
     (dict(tgt_kv_heads=4), kvx.KVX_ERR_PAIR_MISMATCH),
     (dict(tgt_head_dim=128), kvx.KVX_ERR_PAIR_MISMATCH),
