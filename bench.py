@@ -406,7 +406,10 @@ def run_kvx(args):
                          f"({el:.1f} s of fp64 CPU work, one thread{scaled})"}
     pub = PUBLISHED_MS.get(wl.name)
     line = {
-        "metric": WIDE_METRIC if wide else METRIC, "value": value, "unit": "tokens/s",
+        "metric": (WIDE_METRIC if wide else METRIC) if wl.name == "qwen3_14b_32b" else
+                  f"KV-transfer tokens/s, {wl.name} shape"
+                  f"{', wide-feature mapper' if wide else ''}; % of HBM/tensor roofline",
+        "value": value, "unit": "tokens/s",
         "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak",
