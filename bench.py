@@ -39,7 +39,7 @@ WIDE_METRIC = ("KV-transfer tokens/s at 14B→32B shape, 32K tokens, wide-featur
 PUBLISHED_MS = {"qwen3_14b_32b": 277.6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu", "diag": "kvx_diag.cu",
-                "wide": "kvx_wide.cu"}
+                "wide": "kvx_wide.cu", "ridge": "kvx_ridge.cu"}
 
 
 def parse_args(argv=None):
@@ -48,9 +48,13 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
-    ap.add_argument("--op", choices=["transfer", "kv_diagnostics"], default="transfer",
-                    help="transfer (the default step) or the fidelity diagnostics of a "
-                         "mapped cache against the target's own")
+    ap.add_argument("--op", choices=["transfer", "kv_diagnostics", "ridge_fit"],
+                    default="transfer",
+                    help="transfer (the default step), the fidelity diagnostics of a "
+                         "mapped cache against the target's own, or a batch of ridge fits "
+                         "of the per-head maps (calibration)")
+    ap.add_argument("--ridge-batch", type=int, default=16, help="ridge fits per step")
+    ap.add_argument("--ridge-n", type=int, default=131072, help="observations per ridge fit")
     ap.add_argument("--workload", default="qwen3_14b_32b")
     ap.add_argument("--kernel", choices=["auto", "simt", "tcgen05"], default="auto")
     ap.add_argument("--mapper", choices=["per_head", "wide"], default="per_head",
@@ -312,6 +316,138 @@ def transfer_kwargs(wl, inp, dst_k, dst_v, status, paged_src=None):
     else:
         kw["dst_capacity"] = wl.dst_capacity
     return kw
+
+
+RIDGE_METRIC = ("ridge fits/s of the 14B→32B per-head maps (512 features → 128 outputs, "
+                "131,072 observations each); % of fp32 ALU roofline")
+
+
+def fp32_alu_peak_tflops():
+    """fp32 FMA rate from unit counts and the maximum SM clock: SMs x 128
+    fp32 lanes x 2 flops x clock."""
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f)["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def run_ridge(args):
+    """One step = one kvx_ridge_fit call: a batch of ridge fits of the
+    per-head map shape from synthetic paired observations."""
+    import ctypes
+    import torch
+    from cross_model_kv_transfer_gb300 import kvx
+    from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_ridge_inputs
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]
+    B, n = args.ridge_batch, args.ridge_n
+    x, y = make_ridge_inputs(wl, B, n, dev)
+    p, q = x.shape[2], y.shape[2]
+    w = torch.empty((B, p, q), dtype=torch.float32, device=dev)
+    b = torch.empty((B, q), dtype=torch.float32, device=dev)
+    scratch = torch.empty(kvx.kvx_ridge_workspace_bytes(B, p, q), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    a = kvx.RidgeArgs(B, n, p, q, 0.01, kvx.KVX_F32, x.data_ptr(), y.data_ptr(), w.data_ptr(),
+                      b.data_ptr(), scratch.data_ptr(), scratch.numel(), status.data_ptr())
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        e = kvx.kvx_ridge_fit(a, sptr)
+        if e != kvx.KVX_OK:
+            raise kvx.KvxError(e, "kvx_ridge_fit")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    value, ms = aggregate(B, ms_local, dev)
+    # useful flops: the symmetric Gram block once, the cross block, per fit
+    flops = B * 2.0 * n * (p * (p + 1) / 2 + p * q)
+    peak = fp32_alu_peak_tflops()
+    achieved = flops / (ms_local / 1e3) / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": measured_traffic(wl.name, "ridge"),
+            "peak_source": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
+            "algorithmic_flops": flops}
+
+    e2e = None
+    if not args.no_e2e:
+        hx, hy = x.cpu().pin_memory(), y.cpu().pin_memory()
+        hw = torch.empty(w.shape, dtype=w.dtype, pin_memory=True)
+        hb = torch.empty(b.shape, dtype=b.dtype, pin_memory=True)
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            y.copy_(hy, non_blocking=True)
+            step()
+            hw.copy_(w, non_blocking=True)
+            hb.copy_(b, non_blocking=True)
+
+        n_e = max(1, min(args.steps, 5))
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        ev0.record(stream)
+        for _ in range(n_e):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_val, e_ms = aggregate(B, ev0.elapsed_time(ev1) / n_e, dev)
+        e2e = {"value": e_val, "unit": "fits/s", "ms_per_step": e_ms, "steps": n_e,
+               "h2d_bytes_per_step": (hx.numel() + hy.numel()) * 4,
+               "d2h_bytes_per_step": (hw.numel() + hb.numel()) * 4}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        xs, ys = x[0].double().cpu().numpy(), y[0].double().cpu().numpy()
+        m = 256
+        t0 = time.perf_counter()
+        oracle.ridge_fit(xs[:m], ys[:m], 0.01)
+        per_obs = max((time.perf_counter() - t0) / m, 1e-7)
+        m = int(max(256, min(n, args.cpu_seconds / per_obs)))
+        t0 = time.perf_counter()
+        oracle.ridge_fit(xs[:m], ys[:m], 0.01)
+        el = time.perf_counter() - t0
+        cpu = {"value": 1.0 / (el * n / m), "unit": "fits/s", "cores": 1, "kind": "oracle",
+               "sample": f"one fit on its first {m} of {n} observations ({el:.1f} s of fp64 "
+                         f"CPU work, one thread), scaled to {n} observations"}
+    line = {
+        "metric": RIDGE_METRIC, "op": "ridge_fit", "value": value, "unit": "fits/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded paired observations with a planted map)",
+        "config": {"workload": f"{wl.name} per-head maps", "fits": B, "observations": n,
+                   "features": p, "outputs": q, "lambda": 0.01,
+                   "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2 ({(x.numel() + y.numel()) * 4 / 1e9:.2f} GB "
+                         "read per step, no flush needed)"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def run_kvx(args):
@@ -686,6 +822,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "ridge_fit":
+        run_ridge(args)
     else:
         run_kvx(args)
 

@@ -1,0 +1,319 @@
+// kvx_ridge.cu -- the ridge fit of the maps (kvx_ridge_fit), on the GPU.
+//
+// The Qwen3 14B -> 32B article, section "Линейного моста, как ни странно,
+// хватает", fits one ridge regression per target (layer, head), one for
+// keys and one for values, on paired source / target cache observations; its
+// ridge demo centres X and Y on their column means, solves
+// (XcT Xc + lam I) W = XcT Yc and sets b = ybar - xbar W.  For a batch of
+// independent fits (X [n][p], Y [n][q] each) this runs as four launches:
+//   1. clear the fp64 workspace;
+//   2. column means of X and Y (fp32 partial sums over 256 rows, fp64 across
+//      them, chunks of rows in parallel with fp64 atomics);
+//   3. the centred Gram blocks G = XcT Xc (upper triangle of 64 x 64 tiles)
+//      and C = XcT Yc: a register-tiled fp32 FMA contraction over the
+//      observations (each thread 4 x 4 outputs), fp32 partial sums over 256
+//      observations added into fp64, observation chunks in parallel with fp64
+//      atomics;
+//   4. per fit, one CTA: G + lam I mirrored to full, Cholesky factorisation
+//      in fp64 (left-looking, one warp per row), forward and back
+//      substitution for the q columns of C in fp64, b = ybar - xbar W; W and b
+//      stored as fp32.  A non-positive pivot leaves W and b NaN and sets
+//      KVX_FLAG_NOT_SPD.
+// The contraction is a dense Gram product, but it runs on the CUDA cores in
+// fp32: bf16 or tf32 tensor-core operands would round the centred features
+// to 8 or 11 significant bits, and the solve amplifies Gram errors by the
+// condition number of G + lam I.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cmath>
+
+#include "../../include/kvx.h"
+
+namespace {
+
+constexpr int kTile = 64;           // Gram tile (features x features or outputs)
+constexpr int kChunkObs = 32;       // observations staged in shared memory per step
+constexpr int kFlushObs = 256;      // fp32 partial sums are added into fp64 this often
+constexpr int64_t kRowsPerSlice = 16384;   // observations per CTA of the Gram / means
+
+template <typename T>
+__device__ __forceinline__ float ldv(const T *p);
+template <>
+__device__ __forceinline__ float ldv<float>(const float *p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float ldv<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  return __bfloat162float(*p);
+}
+
+__global__ void clear_kernel(double *x, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    x[i] = 0.0;
+}
+
+// sums[b][c] += column c of [X | Y] over this CTA's slice of observations
+template <typename T>
+__global__ void __launch_bounds__(256) mean_kernel(const T *__restrict__ x, const T *__restrict__ y,
+                                                   double *__restrict__ sums, int64_t n, int p,
+                                                   int q) {
+  const int b = blockIdx.z;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= p + q) return;
+  const int64_t t0 = (int64_t)blockIdx.y * kRowsPerSlice;
+  const int64_t t1 = t0 + kRowsPerSlice < n ? t0 + kRowsPerSlice : n;
+  const T *col = c < p ? x + (int64_t)b * n * p + c : y + (int64_t)b * n * q + (c - p);
+  const int ld = c < p ? p : q;
+  double acc = 0.0;
+  for (int64_t t = t0; t < t1; t += kFlushObs) {
+    float part = 0.f;
+    const int64_t te = t + kFlushObs < t1 ? t + kFlushObs : t1;
+    for (int64_t u = t; u < te; ++u) part += ldv<T>(col + u * ld);
+    acc += (double)part;
+  }
+  atomicAdd(sums + (int64_t)b * (p + q) + c, acc);
+}
+
+// One 64 x 64 tile of Z = Xc^T [Xc | Yc] over a slice of observations.
+// Tile (ti, tj): rows are features 64 ti.., columns are features (tj <
+// tiles_p, upper triangle only) or outputs 64 (tj - tiles_p)...
+template <typename T>
+__global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, const T *__restrict__ y,
+                                                   const double *__restrict__ sums,
+                                                   double *__restrict__ G, double *__restrict__ C,
+                                                   int64_t n, int p, int q, int tiles_p,
+                                                   int tiles_q) {
+  __shared__ float sa[kChunkObs][kTile];
+  __shared__ float sb[kChunkObs][kTile];
+  __shared__ float mean_a[kTile], mean_b[kTile];
+  const int b = blockIdx.z;
+  // decode the tile: upper-triangle G tiles first, then the C tiles
+  int ti, tj;
+  {
+    int t = blockIdx.x;
+    const int n_upper = tiles_p * (tiles_p + 1) / 2;
+    if (t < n_upper) {
+      ti = 0;
+      while (t >= tiles_p - ti) {
+        t -= tiles_p - ti;
+        ++ti;
+      }
+      tj = ti + t;
+    } else {
+      t -= n_upper;
+      ti = t / tiles_q;
+      tj = tiles_p + t % tiles_q;
+    }
+  }
+  const bool is_c = tj >= tiles_p;
+  const int i0 = ti * kTile;
+  const int j0 = (is_c ? tj - tiles_p : tj) * kTile;
+  const int ncols = is_c ? q : p;
+  const T *xa = x + (int64_t)b * n * p;
+  const T *xb = is_c ? y + (int64_t)b * n * q : xa;
+  const double inv_n = 1.0 / (double)n;
+  const int tid = threadIdx.x;
+  if (tid < kTile) {
+    const int i = i0 + tid;
+    mean_a[tid] = i < p ? (float)(sums[(int64_t)b * (p + q) + i] * inv_n) : 0.f;
+  } else if (tid < 2 * kTile) {
+    const int j = j0 + tid - kTile;
+    mean_b[tid - kTile] =
+        j < ncols ? (float)(sums[(int64_t)b * (p + q) + (is_c ? p : 0) + j] * inv_n) : 0.f;
+  }
+  const int tx = tid & 15, ty = tid >> 4;   // thread's 4 x 4 block: rows 4 ty.., cols 4 tx..
+  const int64_t t0 = (int64_t)blockIdx.y * kRowsPerSlice;
+  const int64_t t1 = t0 + kRowsPerSlice < n ? t0 + kRowsPerSlice : n;
+  double acc[4][4];
+  float part[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0, part[r][c] = 0.f;
+  __syncthreads();
+  int since_flush = 0;
+  for (int64_t t = t0; t < t1; t += kChunkObs) {
+    // stage 32 observations x 64 columns of each operand, centred, fp32
+    for (int e = tid; e < kChunkObs * kTile; e += blockDim.x) {
+      const int o = e / kTile, c = e % kTile;
+      const int64_t u = t + o;
+      const int i = i0 + c, j = j0 + c;
+      sa[o][c] = (u < t1 && i < p) ? ldv<T>(xa + u * p + i) - mean_a[c] : 0.f;
+      sb[o][c] = (u < t1 && j < ncols) ? ldv<T>(xb + u * ncols + j) - mean_b[c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int o = 0; o < kChunkObs; ++o) {
+      const float4 a4 = *reinterpret_cast<const float4 *>(&sa[o][4 * ty]);
+      const float4 b4 = *reinterpret_cast<const float4 *>(&sb[o][4 * tx]);
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) part[r][c] = fmaf(av[r], bv[c], part[r][c]);
+    }
+    __syncthreads();
+    since_flush += kChunkObs;
+    if (since_flush >= kFlushObs) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] += (double)part[r][c], part[r][c] = 0.f;
+      since_flush = 0;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = i0 + 4 * ty + r, j = j0 + 4 * tx + c;
+      if (i >= p || j >= ncols) continue;
+      const double v = acc[r][c] + (double)part[r][c];
+      if (is_c)
+        atomicAdd(C + ((int64_t)b * p + i) * q + j, v);
+      else
+        atomicAdd(G + ((int64_t)b * p + i) * p + j, v);
+    }
+}
+
+// Per fit: Cholesky of G + lam I and the two triangular solves, in fp64.
+__global__ void __launch_bounds__(256) solve_kernel(double *__restrict__ G, double *__restrict__ C,
+                                                    const double *__restrict__ sums, int64_t n,
+                                                    int p, int q, double lam,
+                                                    float *__restrict__ W, float *__restrict__ bias,
+                                                    uint32_t *status) {
+  __shared__ double s_pivot;
+  __shared__ int s_fail;
+  const int b = blockIdx.x;
+  double *A = G + (int64_t)b * p * p;
+  double *Z = C + (int64_t)b * p * q;
+  const double *mx = sums + (int64_t)b * (p + q);
+  const double inv_n = 1.0 / (double)n;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  // the Gram kernel filled the upper triangle (and whole diagonal tiles):
+  // mirror it, add lam on the diagonal
+  for (int64_t e = tid; e < (int64_t)p * p; e += blockDim.x) {
+    const int i = (int)(e / p), j = (int)(e % p);
+    if (i > j) A[e] = A[(int64_t)j * p + i];
+  }
+  __syncthreads();
+  for (int i = tid; i < p; i += blockDim.x) A[(int64_t)i * p + i] += lam;
+  if (tid == 0) s_fail = 0;
+  __syncthreads();
+  // left-looking Cholesky: column j from the finished columns m < j; L in
+  // the lower triangle of A
+  for (int j = 0; j < p; ++j) {
+    const double *rj = A + (int64_t)j * p;
+    if (warp == 0) {
+      double s = 0.0;
+      for (int m = lane; m < j; m += 32) s = fma(rj[m], rj[m], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) {
+        const double d = rj[j] - s;
+        if (!(d > 0.0)) s_fail = 1;
+        s_pivot = d > 0.0 ? sqrt(d) : 1.0;
+        A[(int64_t)j * p + j] = s_pivot;
+      }
+    }
+    __syncthreads();
+    if (s_fail) break;
+    const double ljj = s_pivot;
+    for (int i = j + 1 + warp; i < p; i += nwarps) {
+      const double *ri = A + (int64_t)i * p;
+      double s = 0.0;
+      for (int m = lane; m < j; m += 32) s = fma(ri[m], rj[m], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) A[(int64_t)i * p + j] = (ri[j] - s) / ljj;
+    }
+    __syncthreads();
+  }
+  if (s_fail) {
+    for (int e = tid; e < p * q; e += blockDim.x) W[(int64_t)b * p * q + e] = nanf("");
+    for (int c = tid; c < q; c += blockDim.x) bias[(int64_t)b * q + c] = nanf("");
+    if (tid == 0 && status) atomicOr(status, KVX_FLAG_NOT_SPD);
+    return;
+  }
+  // forward L Z = C, back L^T W = Z, one thread per output column
+  for (int c = tid; c < q; c += blockDim.x) {
+    for (int i = 0; i < p; ++i) {
+      const double *ri = A + (int64_t)i * p;
+      double v = Z[(int64_t)i * q + c];
+      for (int m = 0; m < i; ++m) v = fma(-ri[m], Z[(int64_t)m * q + c], v);
+      Z[(int64_t)i * q + c] = v / ri[i];
+    }
+    for (int i = p - 1; i >= 0; --i) {
+      double v = Z[(int64_t)i * q + c];
+      for (int m = i + 1; m < p; ++m) v = fma(-A[(int64_t)m * p + i], Z[(int64_t)m * q + c], v);
+      Z[(int64_t)i * q + c] = v / A[(int64_t)i * p + i];
+    }
+    double bc = mx[p + c] * inv_n;
+    for (int i = 0; i < p; ++i) {
+      const double w = Z[(int64_t)i * q + c];
+      W[((int64_t)b * p + i) * q + c] = (float)w;
+      bc = fma(-mx[i] * inv_n, w, bc);
+    }
+    bias[(int64_t)b * q + c] = (float)bc;
+  }
+}
+
+constexpr int kMaxDim = 4096;
+
+size_t ws_sums(int batch, int p, int q) { return (size_t)batch * (p + q) * sizeof(double); }
+size_t ws_gram(int batch, int p) { return (size_t)batch * p * p * sizeof(double); }
+size_t ws_cross(int batch, int p, int q) { return (size_t)batch * p * q * sizeof(double); }
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q) {
+  if (batch < 1 || p < 1 || q < 1 || p > kMaxDim || q > kMaxDim) return 0;
+  return round256(ws_sums(batch, p, q)) + round256(ws_gram(batch, p)) + ws_cross(batch, p, q);
+}
+
+extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
+  if (!a) return KVX_ERR_INVALID_ARG;
+  if (a->batch < 1 || a->batch > 65535 || a->n < 1 || a->p < 1 || a->q < 1 ||
+      a->p > kMaxDim || a->q > kMaxDim || !std::isfinite(a->lambda) || !a->x || !a->y ||
+      !a->w || !a->b || !a->workspace ||
+      (a->x_dtype != KVX_F32 && a->x_dtype != KVX_BF16))
+    return KVX_ERR_INVALID_ARG;
+  if (a->workspace_bytes < kvx_ridge_workspace_bytes(a->batch, a->p, a->q))
+    return KVX_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int batch = a->batch, p = a->p, q = a->q;
+  const int64_t n = a->n;
+  unsigned char *ws = reinterpret_cast<unsigned char *>(a->workspace);
+  double *sums = reinterpret_cast<double *>(ws);
+  double *G = reinterpret_cast<double *>(ws + round256(ws_sums(batch, p, q)));
+  double *C = reinterpret_cast<double *>(ws + round256(ws_sums(batch, p, q)) +
+                                         round256(ws_gram(batch, p)));
+  const int64_t words = (int64_t)(round256(ws_sums(batch, p, q)) + round256(ws_gram(batch, p)) +
+                                  ws_cross(batch, p, q)) / 8;
+  clear_kernel<<<1024, 256, 0, s>>>(sums, words);
+  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
+
+  const int slices = (int)((n + kRowsPerSlice - 1) / kRowsPerSlice);
+  if (slices > 65535) return KVX_ERR_INVALID_ARG;
+  dim3 mgrid((unsigned)((p + q + 255) / 256), (unsigned)slices, (unsigned)batch);
+  const int tiles_p = (p + kTile - 1) / kTile, tiles_q = (q + kTile - 1) / kTile;
+  dim3 ggrid((unsigned)(tiles_p * (tiles_p + 1) / 2 + tiles_p * tiles_q), (unsigned)slices,
+             (unsigned)batch);
+  if (a->x_dtype == KVX_F32) {
+    const float *x = reinterpret_cast<const float *>(a->x);
+    const float *y = reinterpret_cast<const float *>(a->y);
+    mean_kernel<float><<<mgrid, 256, 0, s>>>(x, y, sums, n, p, q);
+    gram_kernel<float><<<ggrid, 256, 0, s>>>(x, y, sums, G, C, n, p, q, tiles_p, tiles_q);
+  } else {
+    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a->x);
+    const __nv_bfloat16 *y = reinterpret_cast<const __nv_bfloat16 *>(a->y);
+    mean_kernel<__nv_bfloat16><<<mgrid, 256, 0, s>>>(x, y, sums, n, p, q);
+    gram_kernel<__nv_bfloat16><<<ggrid, 256, 0, s>>>(x, y, sums, G, C, n, p, q, tiles_p, tiles_q);
+  }
+  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
+  solve_kernel<<<batch, 256, 0, s>>>(G, C, sums, n, p, q, a->lambda, a->w, a->b, a->status);
+  return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
+}

@@ -40,6 +40,7 @@ KVX_FLAG_BAD_ROW = 8
 KVX_FLAG_TIMEOUT = 16
 KVX_FLAG_BAD_SEQLENS = 32
 KVX_FLAG_BAD_SRC_BLOCK = 64
+KVX_FLAG_NOT_SPD = 128
 
 KVX_F32 = 0
 KVX_BF16 = 1
@@ -55,7 +56,8 @@ KVX_MAPPER_WIDE = 1
 
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
             "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches",
-            "kvx_plan_cta_group", "kvx_transfer_static", "kvx_kv_diagnostics")
+            "kvx_plan_cta_group", "kvx_transfer_static", "kvx_kv_diagnostics",
+            "kvx_ridge_workspace_bytes", "kvx_ridge_fit")
 
 
 class PlanDesc(ctypes.Structure):
@@ -105,6 +107,18 @@ class DiagArgs(ctypes.Structure):
     ]
 
 
+class RidgeArgs(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("n", ctypes.c_int64),
+        ("p", ctypes.c_int32), ("q", ctypes.c_int32),
+        ("lambda", ctypes.c_double), ("x_dtype", ctypes.c_int32),
+        ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+        ("w", ctypes.c_void_p), ("b", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -144,6 +158,11 @@ def load():
             lib.kvx_kv_diagnostics.argtypes = [ctypes.c_void_p, ctypes.POINTER(DiagArgs),
                                                ctypes.c_void_p]
             lib.kvx_kv_diagnostics.restype = ctypes.c_int
+            lib.kvx_ridge_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32,
+                                                      ctypes.c_int32]
+            lib.kvx_ridge_workspace_bytes.restype = ctypes.c_size_t
+            lib.kvx_ridge_fit.argtypes = [ctypes.POINTER(RidgeArgs), ctypes.c_void_p]
+            lib.kvx_ridge_fit.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -187,6 +206,50 @@ def kvx_transfer_static(desc: PlanDesc, args: TransferArgs, stream) -> int:
 
 def kvx_kv_diagnostics(plan, args: DiagArgs, stream) -> int:
     return load().kvx_kv_diagnostics(plan, ctypes.byref(args), stream)
+
+
+def kvx_ridge_workspace_bytes(batch: int, p: int, q: int) -> int:
+    return int(load().kvx_ridge_workspace_bytes(int(batch), int(p), int(q)))
+
+
+def kvx_ridge_fit(args: RidgeArgs, stream) -> int:
+    return load().kvx_ridge_fit(ctypes.byref(args), stream)
+
+
+def ridge_fit(x, y, lam: float = 0.01, w=None, b=None, workspace=None, status=None,
+              stream=None):
+    """Batched ridge fit of torch CUDA tensors x [batch][n][p], y
+    [batch][n][q] (fp32 or bf16, or 2-D for one fit): returns fp32 (w
+    [batch][p][q], b [batch][q]), enqueued on ``stream`` (default: torch's
+    current stream).  Scratch is allocated here unless ``workspace`` (a
+    uint8 CUDA tensor) is given."""
+    import torch
+    squeeze = x.dim() == 2
+    if squeeze:
+        x, y = x.unsqueeze(0), y.unsqueeze(0)
+    if not (x.is_cuda and y.is_cuda and x.is_contiguous() and y.is_contiguous()):
+        raise ValueError("x and y must be contiguous CUDA tensors")
+    if x.dtype != y.dtype:
+        raise ValueError("x and y must have the same dtype")
+    batch, n, p = x.shape
+    if tuple(y.shape[:2]) != (batch, n):
+        raise ValueError("x and y must have the same batch and observation counts")
+    q = y.shape[2]
+    dev = x.device
+    w = torch.empty((batch, p, q), dtype=torch.float32, device=dev) if w is None else w
+    b = torch.empty((batch, q), dtype=torch.float32, device=dev) if b is None else b
+    need = kvx_ridge_workspace_bytes(batch, p, q)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    a = RidgeArgs(int(batch), int(n), int(p), int(q), float(lam), _dtype_code(x.dtype),
+                  x.data_ptr(), y.data_ptr(), w.data_ptr(), b.data_ptr(), workspace.data_ptr(),
+                  workspace.numel(), None if status is None else status.data_ptr())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    st = kvx_ridge_fit(a, ctypes.c_void_p(stream.cuda_stream))
+    if st != KVX_OK:
+        raise KvxError(st, "kvx_ridge_fit")
+    return (w[0], b[0]) if squeeze else (w, b)
 
 
 class KvxError(RuntimeError):

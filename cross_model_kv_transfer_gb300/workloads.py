@@ -285,6 +285,31 @@ def make_paged_source(wl: Workload, inp: dict, block_size: int, seed: Optional[i
     return out[0], out[1], table.to(dev)
 
 
+def make_ridge_inputs(wl: Workload, batch: int, n: int, device="cpu",
+                      seed: Optional[int] = None):
+    """Stand-in for the paired observations one calibration batch fits on:
+    ``batch`` fits of the per-head map shape (p = k*d features, q = d
+    outputs), ``n`` observations each.  Features: N(0, 1) times a
+    per-(fit, feature) log-normal (sigma = 0.5) scale plus a per-feature
+    offset; targets: the features through a planted N(0, 1/p) map plus an
+    offset and N(0, 0.1^2) noise.  fp32 [batch][n][p] and [batch][n][q]."""
+    seed = (wl.seed if seed is None else seed) + 5000011
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    p, q = wl.k * wl.head_dim, wl.head_dim
+    x = torch.empty((batch, n, p), dtype=torch.float32, device=dev)
+    y = torch.empty((batch, n, q), dtype=torch.float32, device=dev)
+    for i in range(batch):
+        scale = torch.exp(0.5 * torch.randn((1, p), generator=g, device=dev))
+        xi = torch.randn((n, p), generator=g, device=dev) * scale + \
+            torch.randn((1, p), generator=g, device=dev)
+        wi = torch.randn((p, q), generator=g, device=dev) / math.sqrt(p)
+        y[i].copy_(xi @ wi + torch.randn((1, q), generator=g, device=dev) +
+                   0.1 * torch.randn((n, q), generator=g, device=dev))
+        x[i].copy_(xi)
+    return x, y
+
+
 def make_block_table(wl: Workload, seed: int) -> torch.Tensor:
     """Per-request block tables dealt, in request order, from a seeded random
     permutation of the shared pool of ``wl.num_blocks`` blocks; unused

@@ -54,6 +54,7 @@
 #ifndef KVX_H
 #define KVX_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -86,6 +87,8 @@ typedef enum {
 #define KVX_FLAG_BAD_SRC_BLOCK  64u  /* paged source: p/src_bs >=
                                         max_src_blocks_per_req, or the block
                                         id outside [0, src_num_blocks)       */
+#define KVX_FLAG_NOT_SPD       128u  /* kvx_ridge_fit: XcT Xc + lam I has a
+                                        non-positive pivot (W, b left NaN)   */
 
 typedef enum { KVX_F32 = 0, KVX_BF16 = 1 } kvx_dtype;
 typedef enum { KVX_CONTIGUOUS = 0, KVX_PAGED = 1 } kvx_layout;
@@ -316,6 +319,47 @@ typedef struct {
  * missing pointer or size, or a plan of another device; KVX_ERR_CUDA if a
  * launch fails. */
 kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_args *args, void *stream);
+
+/* Arguments of a batch of independent ridge fits (kvx_ridge_fit).  DEVICE
+ * pointers; arrays dense and row-major. */
+typedef struct {
+  int32_t batch;            /* independent fits, 1..65535                     */
+  int64_t n;                /* observations per fit, >= 1                     */
+  int32_t p;                /* features per observation, 1..4096              */
+  int32_t q;                /* outputs per observation, 1..4096               */
+  double lambda;            /* ridge strength, added unscaled to the diagonal */
+  int32_t x_dtype;          /* kvx_dtype of x and y                           */
+  const void *x;            /* [batch][n][p] features                         */
+  const void *y;            /* [batch][n][q] targets                          */
+  float *w;                 /* [batch][p][q] output: the map                  */
+  float *b;                 /* [batch][q] output: the bias                    */
+  void *workspace;          /* scratch of at least kvx_ridge_workspace_bytes() */
+  size_t workspace_bytes;
+  uint32_t *status;         /* optional device word, KVX_FLAG_NOT_SPD OR-ed in */
+} kvx_ridge_args;
+
+/* Bytes of scratch a kvx_ridge_fit call with these sizes needs (fp64 column
+ * sums, Gram blocks and cross products: 8 * batch * (p + q + p*p + p*q),
+ * rounded up), or 0 for sizes outside the limits above. */
+size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
+
+/* Fit the maps: for each fit, W = (XcT Xc + lambda I)^-1 XcT Yc and
+ * b = ybar - xbar W, with Xc, Yc the observations centred on their column
+ * means.  "Перенос KV-кэша между моделями Qwen3 вместо повторного префилла",
+ * section "Линейного моста, как ни странно, хватает": one ridge regression per
+ * target (layer, head), one for keys and one for values, fitted on paired
+ * source / target observations; its ridge demo centres X and Y and adds
+ * lambda I unscaled (0.01 there).  A batch ordered (target layer, head, K|V)
+ * with p = k*d and q = d writes W and b in exactly the layouts kvx_transfer
+ * reads for a per-head plan with fp32 W and b.  The centred Gram blocks are
+ * accumulated from fp32 products in fp64, the Cholesky factorisation and
+ * both triangular solves run in fp64, W and b are stored as fp32.
+ * Asynchronous on `stream`; no allocation (the caller passes the scratch);
+ * four kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL pointer,
+ * sizes outside the limits, a non-finite lambda or a workspace that is too
+ * small; KVX_ERR_CUDA if a launch fails.  A fit whose matrix is not positive
+ * definite gets NaN W and b and sets KVX_FLAG_NOT_SPD. */
+kvx_status kvx_ridge_fit(const kvx_ridge_args *args, void *stream);
 
 /* Allocation-free transfer.  The sources have no counterpart for this call:
  * it exists for callers that may not allocate device memory -- engines that

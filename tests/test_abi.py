@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol():
 def test_ctypes_structs_match_the_c_layout(tmp_path):
     # Compile a probe against include/kvx.h that prints sizes and offsets.
     fields = {"kvx_plan_desc": kvx.PlanDesc, "kvx_transfer_args": kvx.TransferArgs,
-              "kvx_diag_args": kvx.DiagArgs}
+              "kvx_diag_args": kvx.DiagArgs, "kvx_ridge_args": kvx.RidgeArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kvx.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -122,3 +122,17 @@ def test_status_strings():
     for s in range(7):
         assert kvx.kvx_status_string(s) not in ("", "unknown status")
     assert kvx.kvx_status_string(99) == "unknown status"
+
+
+def test_ridge_workspace_size_and_host_validation():
+    # 8 bytes per column sum, Gram entry and cross product, each block
+    # rounded up to 256 bytes
+    r = lambda x: (x + 255) // 256 * 256
+    assert kvx.kvx_ridge_workspace_bytes(3, 10, 4) == r(8 * 3 * 14) + r(8 * 3 * 100) + 8 * 3 * 40
+    assert kvx.kvx_ridge_workspace_bytes(0, 10, 4) == 0
+    assert kvx.kvx_ridge_workspace_bytes(1, 5000, 4) == 0
+    assert kvx.load().kvx_ridge_fit(None, None) == kvx.KVX_ERR_INVALID_ARG
+    a = kvx.RidgeArgs(1, 10, 4, 2, 0.01, kvx.KVX_F32, 16, 16, 16, 16, 16, 0, None)
+    assert kvx.kvx_ridge_fit(a, None) == kvx.KVX_ERR_INVALID_ARG      # workspace too small
+    a = kvx.RidgeArgs(1, 10, 4, 2, float("inf"), kvx.KVX_F32, 16, 16, 16, 16, 16, 1 << 20, None)
+    assert kvx.kvx_ridge_fit(a, None) == kvx.KVX_ERR_INVALID_ARG      # lambda not finite
