@@ -5,19 +5,20 @@
 // keys and one for values, on paired source / target cache observations; its
 // ridge demo centres X and Y on their column means, solves
 // (XcT Xc + lam I) W = XcT Yc and sets b = ybar - xbar W.  For a batch of
-// independent fits (X [n][p], Y [n][q] each) this runs as four launches:
+// independent fits (X [n][p], Y [n][q] each) this runs as five launches:
 //   1. clear the fp64 workspace;
 //   2. column means of X and Y (fp32 partial sums over 256 rows, fp64 across
 //      them, chunks of rows in parallel with fp64 atomics);
 //   3. the centred Gram blocks G = XcT Xc (upper triangle of 64 x 64 tiles)
 //      and C = XcT Yc: a register-tiled fp32 FMA contraction over the
 //      observations (each thread 4 x 4 outputs), fp32 partial sums over 256
-//      observations added into fp64, observation chunks in parallel with fp64
-//      atomics;
+//      observations summed in fp32 over a slice of 16,384, slices in parallel
+//      and added in fp64 with atomics;
 //   4. per fit, one CTA: G + lam I mirrored to full, Cholesky factorisation
-//      in fp64 (left-looking, one warp per row), forward and back
-//      substitution for the q columns of C in fp64, b = ybar - xbar W; W and b
-//      stored as fp32.  A non-positive pivot leaves W and b NaN and sets
+//      in fp64 (left-looking, one warp per row);
+//   5. per (fit, 16 output columns), one CTA: forward and back substitution
+//      in fp64 (one warp per column), b = ybar - xbar W; W and b stored as
+//      fp32.  A non-positive pivot leaves W and b NaN and sets
 //      KVX_FLAG_NOT_SPD.
 // The contraction is a dense Gram product, but it runs on the CUDA cores in
 // fp32: bf16 or tf32 tensor-core operands would round the centred features
@@ -125,12 +126,15 @@ __global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, cons
   const int tx = tid & 15, ty = tid >> 4;   // thread's 4 x 4 block: rows 4 ty.., cols 4 tx..
   const int64_t t0 = (int64_t)blockIdx.y * kRowsPerSlice;
   const int64_t t1 = t0 + kRowsPerSlice < n ? t0 + kRowsPerSlice : n;
-  double acc[4][4];
+  // two fp32 levels: 256-observation partial sums, summed over the slice
+  // (at most 64 of them); slices meet in fp64 (FP64 adds are ~64x slower
+  // than FP32 FMAs here, so none sit in the inner loops)
+  float acc[4][4];
   float part[4][4];
 #pragma unroll
   for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0, part[r][c] = 0.f;
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f, part[r][c] = 0.f;
   __syncthreads();
   int since_flush = 0;
   for (int64_t t = t0; t < t1; t += kChunkObs) {
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, cons
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] += (double)part[r][c], part[r][c] = 0.f;
+        for (int c = 0; c < 4; ++c) acc[r][c] += part[r][c], part[r][c] = 0.f;
       since_flush = 0;
     }
   }
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, cons
     for (int c = 0; c < 4; ++c) {
       const int i = i0 + 4 * ty + r, j = j0 + 4 * tx + c;
       if (i >= p || j >= ncols) continue;
-      const double v = acc[r][c] + (double)part[r][c];
+      const double v = (double)acc[r][c] + (double)part[r][c];
       if (is_c)
         atomicAdd(C + ((int64_t)b * p + i) * q + j, v);
       else
@@ -178,22 +182,18 @@ __global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, cons
     }
 }
 
-// Per fit: Cholesky of G + lam I and the two triangular solves, in fp64.
-__global__ void __launch_bounds__(256) solve_kernel(double *__restrict__ G, double *__restrict__ C,
-                                                    const double *__restrict__ sums, int64_t n,
-                                                    int p, int q, double lam,
-                                                    float *__restrict__ W, float *__restrict__ bias,
-                                                    uint32_t *status) {
+// Per fit, one CTA: G + lam I mirrored to full and factorised in fp64,
+// A = L L^T with L in the lower triangle (left-looking: column j from the
+// finished columns m < j, one warp per row).  A non-positive pivot marks the
+// fit by a NaN in A[0][0] and sets KVX_FLAG_NOT_SPD.
+__global__ void __launch_bounds__(256) chol_kernel(double *__restrict__ G, int p, double lam,
+                                                   uint32_t *status) {
   __shared__ double s_pivot;
   __shared__ int s_fail;
   const int b = blockIdx.x;
   double *A = G + (int64_t)b * p * p;
-  double *Z = C + (int64_t)b * p * q;
-  const double *mx = sums + (int64_t)b * (p + q);
-  const double inv_n = 1.0 / (double)n;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  // the Gram kernel filled the upper triangle (and whole diagonal tiles):
-  // mirror it, add lam on the diagonal
+  // the Gram kernel filled the upper triangle (and whole diagonal tiles)
   for (int64_t e = tid; e < (int64_t)p * p; e += blockDim.x) {
     const int i = (int)(e / p), j = (int)(e % p);
     if (i > j) A[e] = A[(int64_t)j * p + i];
@@ -202,8 +202,6 @@ __global__ void __launch_bounds__(256) solve_kernel(double *__restrict__ G, doub
   for (int i = tid; i < p; i += blockDim.x) A[(int64_t)i * p + i] += lam;
   if (tid == 0) s_fail = 0;
   __syncthreads();
-  // left-looking Cholesky: column j from the finished columns m < j; L in
-  // the lower triangle of A
   for (int j = 0; j < p; ++j) {
     const double *rj = A + (int64_t)j * p;
     if (warp == 0) {
@@ -231,32 +229,63 @@ __global__ void __launch_bounds__(256) solve_kernel(double *__restrict__ G, doub
     }
     __syncthreads();
   }
-  if (s_fail) {
-    for (int e = tid; e < p * q; e += blockDim.x) W[(int64_t)b * p * q + e] = nanf("");
-    for (int c = tid; c < q; c += blockDim.x) bias[(int64_t)b * q + c] = nanf("");
-    if (tid == 0 && status) atomicOr(status, KVX_FLAG_NOT_SPD);
-    return;
+  if (s_fail && tid == 0) {
+    A[0] = nan("");
+    if (status) atomicOr(status, KVX_FLAG_NOT_SPD);
   }
-  // forward L Z = C, back L^T W = Z, one thread per output column
-  for (int c = tid; c < q; c += blockDim.x) {
+}
+
+constexpr int kSolveCols = 16;   // output columns per CTA of the solve
+
+// Per (fit, 16 output columns): forward L Z = C and back L^T W = Z in fp64,
+// one warp per column (lanes split each dot product), then
+// b = ybar - xbar W; W and b stored as fp32 (NaN for a failed fit).
+__global__ void __launch_bounds__(256) trsm_kernel(const double *__restrict__ G,
+                                                   double *__restrict__ C,
+                                                   const double *__restrict__ sums, int64_t n,
+                                                   int p, int q, float *__restrict__ W,
+                                                   float *__restrict__ bias) {
+  const int b = blockIdx.x;
+  const double *A = G + (int64_t)b * p * p;
+  double *Z = C + (int64_t)b * p * q;
+  const double *mx = sums + (int64_t)b * (p + q);
+  const double inv_n = 1.0 / (double)n;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const bool failed = isnan(A[0]);
+  for (int c = blockIdx.y * kSolveCols + warp; c < q && c < (blockIdx.y + 1) * kSolveCols;
+       c += nwarps) {
+    if (failed) {
+      for (int i = lane; i < p; i += 32) W[((int64_t)b * p + i) * q + c] = nanf("");
+      if (lane == 0) bias[(int64_t)b * q + c] = nanf("");
+      continue;
+    }
     for (int i = 0; i < p; ++i) {
       const double *ri = A + (int64_t)i * p;
-      double v = Z[(int64_t)i * q + c];
-      for (int m = 0; m < i; ++m) v = fma(-ri[m], Z[(int64_t)m * q + c], v);
-      Z[(int64_t)i * q + c] = v / ri[i];
+      double s = 0.0;
+      for (int m = lane; m < i; m += 32) s = fma(ri[m], Z[(int64_t)m * q + c], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) Z[(int64_t)i * q + c] = (Z[(int64_t)i * q + c] - s) / ri[i];
+      __syncwarp();
     }
     for (int i = p - 1; i >= 0; --i) {
-      double v = Z[(int64_t)i * q + c];
-      for (int m = i + 1; m < p; ++m) v = fma(-A[(int64_t)m * p + i], Z[(int64_t)m * q + c], v);
-      Z[(int64_t)i * q + c] = v / A[(int64_t)i * p + i];
+      double s = 0.0;
+      for (int m = i + 1 + lane; m < p; m += 32)
+        s = fma(A[(int64_t)m * p + i], Z[(int64_t)m * q + c], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) Z[(int64_t)i * q + c] = (Z[(int64_t)i * q + c] - s) / A[(int64_t)i * p + i];
+      __syncwarp();
     }
-    double bc = mx[p + c] * inv_n;
-    for (int i = 0; i < p; ++i) {
+    double s = 0.0;
+    for (int i = lane; i < p; i += 32) {
       const double w = Z[(int64_t)i * q + c];
       W[((int64_t)b * p + i) * q + c] = (float)w;
-      bc = fma(-mx[i] * inv_n, w, bc);
+      s = fma(mx[i] * inv_n, w, s);
     }
-    bias[(int64_t)b * q + c] = (float)bc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) bias[(int64_t)b * q + c] = (float)(mx[p + c] * inv_n - s);
   }
 }
 
@@ -314,6 +343,10 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
     gram_kernel<__nv_bfloat16><<<ggrid, 256, 0, s>>>(x, y, sums, G, C, n, p, q, tiles_p, tiles_q);
   }
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
-  solve_kernel<<<batch, 256, 0, s>>>(G, C, sums, n, p, q, a->lambda, a->w, a->b, a->status);
+  chol_kernel<<<batch, 256, 0, s>>>(G, p, a->lambda, a->status);
+  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
+  dim3 tgrid((unsigned)batch, (unsigned)((q + kSolveCols - 1) / kSolveCols));
+  trsm_kernel<<<tgrid, kSolveCols * 32 < 256 ? kSolveCols * 32 : 256, 0, s>>>(G, C, sums, n, p, q,
+                                                                           a->w, a->b);
   return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }

@@ -352,10 +352,11 @@ size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
  * lambda I unscaled (0.01 there).  A batch ordered (target layer, head, K|V)
  * with p = k*d and q = d writes W and b in exactly the layouts kvx_transfer
  * reads for a per-head plan with fp32 W and b.  The centred Gram blocks are
- * accumulated from fp32 products in fp64, the Cholesky factorisation and
- * both triangular solves run in fp64, W and b are stored as fp32.
- * Asynchronous on `stream`; no allocation (the caller passes the scratch);
- * four kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL pointer,
+ * formed from fp32 products (fp32 partial sums over 256 observations, summed
+ * in fp32 over slices of 16,384, slices added in fp64), the Cholesky
+ * factorisation and both triangular solves run in fp64, W and b are stored as
+ * fp32.  Asynchronous on `stream`; no allocation (the caller passes the
+ * scratch); five kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL pointer,
  * sizes outside the limits, a non-finite lambda or a workspace that is too
  * small; KVX_ERR_CUDA if a launch fails.  A fit whose matrix is not positive
  * definite gets NaN W and b and sets KVX_FLAG_NOT_SPD. */

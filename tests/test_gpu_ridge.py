@@ -4,8 +4,9 @@ lam I) W = XcT Yc by Cholesky, b = ybar - xbar W; the Qwen3 article's
 linear-bridge section).
 
 Tolerances.  The GPU forms the centred Gram blocks from fp32 products (fp32
-partial sums over 256 observations, fp64 across them) and solves in fp64, so
-its Gram blocks carry a relative error of ~1e-6; the solve amplifies that by
+partial sums over 256 observations, summed in fp32 over slices of 16,384,
+slices added in fp64) and solves in fp64, so its Gram blocks carry a relative
+error of ~1e-6; the solve amplifies that by
 at most the condition number kappa of XcT Xc + lam I.  The tests draw
 features with moderate scale spread (kappa below ~1e3, computed and checked
 in each test) and require, per fit, a relative Frobenius error of W and of
