@@ -66,6 +66,8 @@ def parse_args(argv=None):
                          "(0: packed source rows)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (profiling of small cases)")
+    ap.add_argument("--tgt-layers", type=int, default=0,
+                    help="override the workload's target-layer count (profiling of small cases)")
     ap.add_argument("--tiles-per-item", type=int, default=0)
     ap.add_argument("--single-cta", action="store_true",
                     help="tensor-core kernel on single CTAs instead of CTA pairs")
@@ -462,6 +464,10 @@ def run_kvx(args):
     wl = WORKLOADS[args.workload]
     if args.tokens:
         wl = wl.with_tokens([args.tokens], [wl.tgt_offsets[0]], name=f"{wl.name}@{args.tokens}")
+    if args.tgt_layers:
+        import dataclasses
+        wl = dataclasses.replace(wl, tgt_layers=args.tgt_layers,
+                                 name=f"{wl.name}/Lt{args.tgt_layers}")
     inp = make_inputs(wl, dev)
     wide = args.mapper == "wide"
     if wide:
