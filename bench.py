@@ -445,7 +445,8 @@ def run_ridge(args):
                    "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2 ({(x.numel() + y.numel()) * 4 / 1e9:.2f} GB "
                          "read per step, no flush needed)"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 5 * args.steps,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": (4 + 3 * ((p + 63) // 64) - 1) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:

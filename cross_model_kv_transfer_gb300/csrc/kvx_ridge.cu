@@ -5,7 +5,8 @@
 // keys and one for values, on paired source / target cache observations; its
 // ridge demo centres X and Y on their column means, solves
 // (XcT Xc + lam I) W = XcT Yc and sets b = ybar - xbar W.  For a batch of
-// independent fits (X [n][p], Y [n][q] each) this runs as five launches:
+// independent fits (X [n][p], Y [n][q] each) this runs as 4 + 3 ceil(p / 64) - 1
+// launches:
 //   1. clear the fp64 workspace;
 //   2. column means of X and Y (fp32 partial sums over 256 rows, fp64 across
 //      them, chunks of rows in parallel with fp64 atomics);
@@ -14,12 +15,13 @@
 //      observations (each thread 4 x 4 outputs), fp32 partial sums over 256
 //      observations summed in fp32 over a slice of 16,384, slices in parallel
 //      and added in fp64 with atomics;
-//   4. per fit, one CTA: G + lam I mirrored to full, Cholesky factorisation
-//      in fp64 (left-looking, one warp per row);
-//   5. per (fit, 16 output columns), one CTA: forward and back substitution
-//      in fp64 (one warp per column), b = ybar - xbar W; W and b stored as
-//      fp32.  A non-positive pivot leaves W and b NaN and sets
-//      KVX_FLAG_NOT_SPD.
+//   4. G + lam I mirrored to full, then a Cholesky factorisation in fp64
+//      blocked by 64 (per diagonal block: factor it, solve the panel below,
+//      update the trailing blocks, each step spread over CTAs);
+//   5. per (fit, up to 8 output columns), one CTA: forward and back
+//      substitution in fp64 (one warp per column, the column in shared
+//      memory), b = ybar - xbar W; W and b stored as fp32.  A non-positive
+//      pivot leaves W and b NaN and sets KVX_FLAG_NOT_SPD.
 // The contraction is a dense Gram product, but it runs on the CUDA cores in
 // fp32: bf16 or tf32 tensor-core operands would round the centred features
 // to 8 or 11 significant bits, and the solve amplifies Gram errors by the
@@ -182,111 +184,230 @@ __global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, cons
     }
 }
 
-// Per fit, one CTA: G + lam I mirrored to full and factorised in fp64,
-// A = L L^T with L in the lower triangle (left-looking: column j from the
-// finished columns m < j, one warp per row).  A non-positive pivot marks the
-// fit by a NaN in A[0][0] and sets KVX_FLAG_NOT_SPD.
-__global__ void __launch_bounds__(256) chol_kernel(double *__restrict__ G, int p, double lam,
-                                                   uint32_t *status) {
-  __shared__ double s_pivot;
-  __shared__ int s_fail;
-  const int b = blockIdx.x;
-  double *A = G + (int64_t)b * p * p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  // the Gram kernel filled the upper triangle (and whole diagonal tiles)
-  for (int64_t e = tid; e < (int64_t)p * p; e += blockDim.x) {
-    const int i = (int)(e / p), j = (int)(e % p);
-    if (i > j) A[e] = A[(int64_t)j * p + i];
+// ---------------------------------------------------------------------------
+// fp64 Cholesky, blocked by 64 (right-looking): for each diagonal block kb,
+// factor it (one CTA per fit), solve the panel below it (one CTA per block
+// row), and update the trailing lower triangle (one CTA per 64 x 64 block).
+// The fp64 pipe of one SM is the limit of a one-CTA factorisation; the
+// blocked form spreads the update, which is most of the work, over the GPU.
+// A fit that meets a non-positive pivot is marked by a NaN in A[0][0]
+// (later steps of that fit do nothing) and sets KVX_FLAG_NOT_SPD.
+// ---------------------------------------------------------------------------
+constexpr int kB = 64;   // block of the factorisation
+
+// G + lam I mirrored to full: row block blockIdx.y of fit blockIdx.x.
+__global__ void __launch_bounds__(256) chol_prep_kernel(double *__restrict__ G, int p, double lam) {
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  const int r0 = blockIdx.y * kB;
+  for (int e = threadIdx.x; e < kB * p; e += blockDim.x) {
+    const int i = r0 + e / p, j = e % p;
+    if (i >= p) break;
+    if (i > j) A[(int64_t)i * p + j] = A[(int64_t)j * p + i];
+    else if (i == j) A[(int64_t)i * p + j] += lam;
   }
-  __syncthreads();
-  for (int i = tid; i < p; i += blockDim.x) A[(int64_t)i * p + i] += lam;
+}
+
+__device__ __forceinline__ int blk_len(int p, int kb) { return p - kb * kB < kB ? p - kb * kB : kB; }
+
+// Factor the diagonal block kb of each fit in shared memory (left-looking,
+// one warp per row); the update of earlier blocks is already applied.
+__global__ void __launch_bounds__(256) chol_diag_kernel(double *__restrict__ G, int p, int kb,
+                                                        uint32_t *status) {
+  __shared__ double L[kB][kB + 1];
+  __shared__ int s_fail;
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  if (isnan(A[0])) return;
+  const int o = kb * kB, nb = blk_len(p, kb);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  for (int e = tid; e < nb * nb; e += blockDim.x) {
+    const int i = e / nb, j = e % nb;
+    L[i][j] = A[(int64_t)(o + i) * p + o + j];
+  }
   if (tid == 0) s_fail = 0;
   __syncthreads();
-  for (int j = 0; j < p; ++j) {
-    const double *rj = A + (int64_t)j * p;
+  for (int j = 0; j < nb; ++j) {
     if (warp == 0) {
-      double s = 0.0;
-      for (int m = lane; m < j; m += 32) s = fma(rj[m], rj[m], s);
+      double sum = 0.0;
+      for (int m = lane; m < j; m += 32) sum = fma(L[j][m], L[j][m], sum);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      for (int w = 16; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
       if (lane == 0) {
-        const double d = rj[j] - s;
+        const double d = L[j][j] - sum;
         if (!(d > 0.0)) s_fail = 1;
-        s_pivot = d > 0.0 ? sqrt(d) : 1.0;
-        A[(int64_t)j * p + j] = s_pivot;
+        L[j][j] = d > 0.0 ? sqrt(d) : 1.0;
       }
     }
     __syncthreads();
     if (s_fail) break;
-    const double ljj = s_pivot;
-    for (int i = j + 1 + warp; i < p; i += nwarps) {
-      const double *ri = A + (int64_t)i * p;
-      double s = 0.0;
-      for (int m = lane; m < j; m += 32) s = fma(ri[m], rj[m], s);
+    for (int i = j + 1 + warp; i < nb; i += nwarps) {
+      double sum = 0.0;
+      for (int m = lane; m < j; m += 32) sum = fma(L[i][m], L[j][m], sum);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) A[(int64_t)i * p + j] = (ri[j] - s) / ljj;
+      for (int w = 16; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
+      if (lane == 0) L[i][j] = (L[i][j] - sum) / L[j][j];
     }
     __syncthreads();
   }
-  if (s_fail && tid == 0) {
-    A[0] = nan("");
-    if (status) atomicOr(status, KVX_FLAG_NOT_SPD);
+  if (s_fail) {
+    if (tid == 0) {
+      A[0] = nan("");
+      if (status) atomicOr(status, KVX_FLAG_NOT_SPD);
+    }
+    return;
+  }
+  // L in the lower triangle, L^T in the upper (rows of L^T are what the
+  // back substitution reads)
+  for (int e = tid; e < nb * nb; e += blockDim.x) {
+    const int i = e / nb, j = e % nb;
+    A[(int64_t)(o + i) * p + o + j] = i >= j ? L[i][j] : L[j][i];
   }
 }
 
-constexpr int kSolveCols = 16;   // output columns per CTA of the solve
+// Panel: block row ib = kb + 1 + blockIdx.y of fit blockIdx.x solves
+// X L_kb^T = A[ib][kb] (rows independent: one thread per row).
+__global__ void __launch_bounds__(64) chol_panel_kernel(double *__restrict__ G, int p, int kb) {
+  __shared__ double L[kB][kB + 1];
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  if (isnan(A[0])) return;
+  const int o = kb * kB, nb = blk_len(p, kb);
+  const int ib = kb + 1 + blockIdx.y;
+  const int r0 = ib * kB, nr = blk_len(p, ib);
+  for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
+    const int i = e / nb, j = e % nb;
+    L[i][j] = i >= j ? A[(int64_t)(o + i) * p + o + j] : 0.0;
+  }
+  __syncthreads();
+  const int r = threadIdx.x;
+  if (r >= nr) return;
+  double *row = A + (int64_t)(r0 + r) * p + o;
+  double x[kB];
+#pragma unroll
+  for (int j = 0; j < kB; ++j) x[j] = j < nb ? row[j] : 0.0;
+#pragma unroll
+  for (int j = 0; j < kB; ++j) {
+    if (j >= nb) break;
+    double v = x[j];
+#pragma unroll
+    for (int m = 0; m < j; ++m) v = fma(-x[m], L[j][m], v);
+    x[j] = v / L[j][j];
+  }
+#pragma unroll
+  for (int j = 0; j < kB; ++j)
+    if (j < nb) {
+      row[j] = x[j];                                   // L[r0 + r][o + j]
+      A[(int64_t)(o + j) * p + r0 + r] = x[j];         // and L^T
+    }
+}
 
-// Per (fit, 16 output columns): forward L Z = C and back L^T W = Z in fp64,
-// one warp per column (lanes split each dot product), then
-// b = ybar - xbar W; W and b stored as fp32 (NaN for a failed fit).
+// Trailing update: lower-triangle block (ib, jb), ib >= jb > kb, of fit
+// blockIdx.x: A[ib][jb] -= A[ib][kb] A[jb][kb]^T; 256 threads, 4 x 4 each.
+__global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ G, int p, int kb) {
+  __shared__ double Pa[kB][kB / 2 + 1];
+  __shared__ double Pb[kB][kB / 2 + 1];
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  if (isnan(A[0])) return;
+  // decode (ib, jb) from the lower triangle of the trailing blocks
+  int t = blockIdx.y, ib = kb + 1, jb = kb + 1;
+  while (t > ib - (kb + 1)) {
+    t -= ib - kb;
+    ++ib;
+  }
+  jb = kb + 1 + t;
+  const int o = kb * kB, nk = blk_len(p, kb);
+  const int ri = ib * kB, rj = jb * kB, ni = blk_len(p, ib), nj = blk_len(p, jb);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  double acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.0;
+  for (int k0 = 0; k0 < nk; k0 += kB / 2) {
+    for (int e = threadIdx.x; e < kB * (kB / 2); e += blockDim.x) {
+      const int r = e / (kB / 2), k = e % (kB / 2);
+      const bool kin = k0 + k < nk;
+      Pa[r][k] = (r < ni && kin) ? A[(int64_t)(ri + r) * p + o + k0 + k] : 0.0;
+      Pb[r][k] = (r < nj && kin) ? A[(int64_t)(rj + r) * p + o + k0 + k] : 0.0;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < kB / 2; ++k) {
+      double av[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = Pa[4 * ty + a][k];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bv[c] = Pb[4 * tx + c][k];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = fma(av[a], bv[c], acc[a][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = 4 * ty + a, j = 4 * tx + c;
+      if (i < ni && j < nj && (ib != jb || i >= j))
+        A[(int64_t)(ri + i) * p + rj + j] -= acc[a][c];
+    }
+}
+
+// Per (fit, group of output columns): forward L Z = C and back L^T W = Z in
+// fp64, one warp per column, the column kept in shared memory (the lanes
+// split each dot product over a row of L, or of L^T from the upper triangle,
+// read coalesced from global memory);
+// then b = ybar - xbar W.  W and b are stored as fp32 (NaN for a failed
+// fit).
 __global__ void __launch_bounds__(256) trsm_kernel(const double *__restrict__ G,
                                                    double *__restrict__ C,
                                                    const double *__restrict__ sums, int64_t n,
-                                                   int p, int q, float *__restrict__ W,
+                                                   int p, int q, int cols_per_cta,
+                                                   float *__restrict__ W,
                                                    float *__restrict__ bias) {
+  extern __shared__ double zs[];   // [cols_per_cta][p]
   const int b = blockIdx.x;
   const double *A = G + (int64_t)b * p * p;
   double *Z = C + (int64_t)b * p * q;
   const double *mx = sums + (int64_t)b * (p + q);
   const double inv_n = 1.0 / (double)n;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const bool failed = isnan(A[0]);
-  for (int c = blockIdx.y * kSolveCols + warp; c < q && c < (blockIdx.y + 1) * kSolveCols;
-       c += nwarps) {
-    if (failed) {
-      for (int i = lane; i < p; i += 32) W[((int64_t)b * p + i) * q + c] = nanf("");
-      if (lane == 0) bias[(int64_t)b * q + c] = nanf("");
-      continue;
-    }
-    for (int i = 0; i < p; ++i) {
-      const double *ri = A + (int64_t)i * p;
-      double s = 0.0;
-      for (int m = lane; m < i; m += 32) s = fma(ri[m], Z[(int64_t)m * q + c], s);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) Z[(int64_t)i * q + c] = (Z[(int64_t)i * q + c] - s) / ri[i];
-      __syncwarp();
-    }
-    for (int i = p - 1; i >= 0; --i) {
-      double s = 0.0;
-      for (int m = i + 1 + lane; m < p; m += 32)
-        s = fma(A[(int64_t)m * p + i], Z[(int64_t)m * q + c], s);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) Z[(int64_t)i * q + c] = (Z[(int64_t)i * q + c] - s) / A[(int64_t)i * p + i];
-      __syncwarp();
-    }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.y * cols_per_cta + warp;
+  if (warp >= cols_per_cta || c >= q) return;
+  double *z = zs + (size_t)warp * p;
+  if (isnan(A[0])) {
+    for (int i = lane; i < p; i += 32) W[((int64_t)b * p + i) * q + c] = nanf("");
+    if (lane == 0) bias[(int64_t)b * q + c] = nanf("");
+    return;
+  }
+  for (int i = lane; i < p; i += 32) z[i] = Z[(int64_t)i * q + c];
+  __syncwarp();
+  for (int i = 0; i < p; ++i) {
+    const double *ri = A + (int64_t)i * p;
     double s = 0.0;
-    for (int i = lane; i < p; i += 32) {
-      const double w = Z[(int64_t)i * q + c];
-      W[((int64_t)b * p + i) * q + c] = (float)w;
-      s = fma(mx[i] * inv_n, w, s);
-    }
+    for (int m = lane; m < i; m += 32) s = fma(ri[m], z[m], s);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) bias[(int64_t)b * q + c] = (float)(mx[p + c] * inv_n - s);
+    if (lane == 0) z[i] = (z[i] - s) / ri[i];
+    __syncwarp();
   }
+  for (int i = p - 1; i >= 0; --i) {
+    const double *ri = A + (int64_t)i * p;           // row i of L^T (upper triangle)
+    double s = 0.0;
+    for (int m = i + 1 + lane; m < p; m += 32) s = fma(ri[m], z[m], s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) z[i] = (z[i] - s) / ri[i];
+    __syncwarp();
+  }
+  double s = 0.0;
+  for (int i = lane; i < p; i += 32) {
+    W[((int64_t)b * p + i) * q + c] = (float)z[i];
+    s = fma(mx[i] * inv_n, z[i], s);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) bias[(int64_t)b * q + c] = (float)(mx[p + c] * inv_n - s);
 }
 
 constexpr int kMaxDim = 4096;
@@ -343,10 +464,26 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
     gram_kernel<__nv_bfloat16><<<ggrid, 256, 0, s>>>(x, y, sums, G, C, n, p, q, tiles_p, tiles_q);
   }
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
-  chol_kernel<<<batch, 256, 0, s>>>(G, p, a->lambda, a->status);
+  // blocked fp64 Cholesky
+  const int nblk = (p + kB - 1) / kB;
+  chol_prep_kernel<<<dim3((unsigned)batch, (unsigned)nblk), 256, 0, s>>>(G, p, a->lambda);
+  for (int kb = 0; kb < nblk; ++kb) {
+    chol_diag_kernel<<<batch, 256, 0, s>>>(G, p, kb, a->status);
+    const int rest = nblk - 1 - kb;
+    if (rest > 0) {
+      chol_panel_kernel<<<dim3((unsigned)batch, (unsigned)rest), 64, 0, s>>>(G, p, kb);
+      chol_update_kernel<<<dim3((unsigned)batch, (unsigned)(rest * (rest + 1) / 2)), 256, 0, s>>>(
+          G, p, kb);
+    }
+  }
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
-  dim3 tgrid((unsigned)batch, (unsigned)((q + kSolveCols - 1) / kSolveCols));
-  trsm_kernel<<<tgrid, kSolveCols * 32 < 256 ? kSolveCols * 32 : 256, 0, s>>>(G, C, sums, n, p, q,
-                                                                           a->w, a->b);
+  // triangular solves: one warp per output column, columns in shared memory
+  const int cols = (int)(48 * 1024 / ((size_t)p * sizeof(double))) < 8
+                       ? (int)(48 * 1024 / ((size_t)p * sizeof(double)))
+                       : 8;
+  const int cpc = cols < 1 ? 1 : cols;
+  dim3 tgrid((unsigned)batch, (unsigned)((q + cpc - 1) / cpc));
+  trsm_kernel<<<tgrid, cpc * 32, (size_t)cpc * p * sizeof(double), s>>>(G, C, sums, n, p, q, cpc,
+                                                                          a->w, a->b);
   return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }

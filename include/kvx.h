@@ -355,8 +355,9 @@ size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
  * formed from fp32 products (fp32 partial sums over 256 observations, summed
  * in fp32 over slices of 16,384, slices added in fp64), the Cholesky
  * factorisation and both triangular solves run in fp64, W and b are stored as
- * fp32.  Asynchronous on `stream`; no allocation (the caller passes the
- * scratch); five kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL pointer,
+ * fp32; the factorisation is blocked by 64 and spread over CTAs.
+ * Asynchronous on `stream`; no allocation (the caller passes the scratch);
+ * 4 + 3 ceil(p / 64) - 1 kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL pointer,
  * sizes outside the limits, a non-finite lambda or a workspace that is too
  * small; KVX_ERR_CUDA if a launch fails.  A fit whose matrix is not positive
  * definite gets NaN W and b and sets KVX_FLAG_NOT_SPD. */
