@@ -1,6 +1,10 @@
 """Parity at full workload sizes, in the launch configuration the benchmark
 times: the whole transfer runs on the GPU, and sampled output rows are
 recomputed one by one by the fp64 oracle (``oracle.map_token`` / ``dst_row``).
+Covers the 14B -> 32B shape at 32,768 tokens, the 8B -> 70B batched paged
+recipe, and the 0.6B -> 1.7B pair at 2,048 and 8,192 tokens with the target
+shifted by +37 (the 512-token pair is compared in full in
+test_gpu_parity.py).
 Every row outside the transfer must keep its sentinel bits (checked on the
 device for the whole cache)."""
 import numpy as np
@@ -46,7 +50,8 @@ def _written_mask(wl, inp):
     return rows
 
 
-@pytest.mark.parametrize("name", ["qwen3_14b_32b", "llama31_8b_70b_paged"])
+@pytest.mark.parametrize("name", ["qwen3_14b_32b", "llama31_8b_70b_paged",
+                                  "qwen3_0p6b_1p7b_off37_2k", "qwen3_0p6b_1p7b_off37_8k"])
 def test_full_size_sampled_rows_match_oracle(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl, "cuda")
