@@ -77,6 +77,33 @@ __device__ __forceinline__ void load_run(const T *src, float *out) {
   }
 }
 
+// cp.async of 16 bytes global -> shared, bypassing L1; src_bytes = 0 writes
+// zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src,
+                                           uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem_dst)),
+               "l"(gmem_src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Stages of the cp.async ring (96 KB of shared memory at 256 threads).
+template <typename T>
+constexpr int kStages = 6;
+template <>
+constexpr int kStages<float> = 3;
+
+template <typename T>
+constexpr size_t ring_bytes(int nthreads) {
+  return (size_t)kStages<T> * 4 * (8 * sizeof(T) / 16) * nthreads * 16;
+}
+
 // The 16 / sizeof(T) elements of one 16-byte word as fp32.
 template <typename T>
 __device__ __forceinline__ void unpack16(const uint4 &u, float *out) {
@@ -210,45 +237,56 @@ __global__ void __launch_bounds__(kThreads, 2) kv_diag_kernel(const __grid_const
   // Every lane runs every iteration (the shuffles need the whole warp);
   // lanes without a token or a row contribute zeros.
   if constexpr (VEC && EMAX == 1) {
-    // two tokens per iteration, their 16-byte words loaded before either is
-    // used (twice the bytes in flight per thread)
+    // Each thread streams its own 16-byte words into a ring of kStages
+    // shared-memory stages with cp.async (kStages - 1 tokens in flight per
+    // thread, no registers held by loads in flight), reading back the
+    // oldest stage; no barrier is needed, every thread reads only what it
+    // copied.  Tokens past the chunk and rows that are skipped copy zeros.
     constexpr int kNV = RL * (int)sizeof(T) / 16;   // 16-byte words per half run
-    for (int base = 0; base < n; base += 2 * P.tok_par) {
-      uint4 raw[2][4][kNV];                          // token, (a lo, a hi, y lo, y hi)
-      int64_t row[2];
-      uint32_t pt[2];
+    constexpr int kW = 4 * kNV;                      // words per token: a lo, a hi, y lo, y hi
+    constexpr int kS = kStages<T>;
+    extern __shared__ uint4 ring[];                  // [kS][kW][blockDim.x]
+    const int nt = blockDim.x;
+    const int iters = (n + P.tok_par - 1) / P.tok_par;
+    auto issue = [&](int it) {
+      const int i = it * P.tok_par + tl;
+      const int64_t row = (lane_on && i < n) ? s_row[i] : -1;
+      const bool run_on = row >= 0 && q < P.NR;
+      const int64_t off =
+          run_on ? (((int64_t)lt * p.dst_rows + row) * p.H + h) * p.d + (int64_t)q * RL : 0;
+      const uint4 *src[4] = {reinterpret_cast<const uint4 *>(mapped + off),
+                             reinterpret_cast<const uint4 *>(mapped + off + half),
+                             reinterpret_cast<const uint4 *>(ref + off),
+                             reinterpret_cast<const uint4 *>(ref + off + half)};
+      uint4 *dst = ring + (size_t)(it % kS) * kW * nt + tid;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = base + u * P.tok_par + tl;
-        row[u] = (lane_on && i < n) ? s_row[i] : -1;
-        pt[u] = row[u] >= 0 ? (uint32_t)s_pt[i] : 0u;
-        const bool run_on = row[u] >= 0 && q < P.NR;
-        const int64_t off =
-            run_on ? (((int64_t)lt * p.dst_rows + row[u]) * p.H + h) * p.d + (int64_t)q * RL : 0;
-        const uint4 *src[4] = {reinterpret_cast<const uint4 *>(mapped + off),
-                               reinterpret_cast<const uint4 *>(mapped + off + half),
-                               reinterpret_cast<const uint4 *>(ref + off),
-                               reinterpret_cast<const uint4 *>(ref + off + half)};
+      for (int w = 0; w < 4; ++w)
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
+        for (int v = 0; v < kNV; ++v)
+          cp_async16(dst + (size_t)(w * kNV + v) * nt, src[w] + v, run_on ? 16u : 0u);
+      cp_async_commit();
+    };
+#pragma unroll 1
+    for (int it = 0; it < kS - 1; ++it) issue(it);
+#pragma unroll 1
+    for (int it = 0; it < iters; ++it) {
+      issue(it + kS - 1);
+      cp_async_wait<kS - 1>();
+      const uint4 *src = ring + (size_t)(it % kS) * kW * nt + tid;
+      float a[1][2 * RL], y[1][2 * RL];
 #pragma unroll
-          for (int v = 0; v < kNV; ++v)
-            raw[u][w][v] = run_on ? __ldcs(src[w] + v) : make_uint4(0u, 0u, 0u, 0u);
+      for (int v = 0; v < kNV; ++v) {
+        constexpr int kPer = 16 / (int)sizeof(T);
+        unpack16<T>(src[(size_t)(0 * kNV + v) * nt], &a[0][v * kPer]);
+        unpack16<T>(src[(size_t)(1 * kNV + v) * nt], &a[0][RL + v * kPer]);
+        unpack16<T>(src[(size_t)(2 * kNV + v) * nt], &y[0][v * kPer]);
+        unpack16<T>(src[(size_t)(3 * kNV + v) * nt], &y[0][RL + v * kPer]);
       }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        float a[1][2 * RL], y[1][2 * RL];
-#pragma unroll
-        for (int v = 0; v < kNV; ++v) {
-          constexpr int kPer = 16 / (int)sizeof(T);
-          unpack16<T>(raw[u][0][v], &a[0][v * kPer]);
-          unpack16<T>(raw[u][1][v], &a[0][RL + v * kPer]);
-          unpack16<T>(raw[u][2][v], &y[0][v * kPer]);
-          unpack16<T>(raw[u][3][v], &y[0][RL + v * kPer]);
-        }
-        fold(a, y, row[u] >= 0, pt[u]);
-      }
+      const int i = it * P.tok_par + tl;
+      const int64_t row = (lane_on && i < n) ? s_row[i] : -1;
+      fold(a, y, row >= 0, row >= 0 ? (uint32_t)s_pt[i] : 0u);
     }
+    cp_async_wait<0>();
   } else {
     for (int base = 0; base < n; base += P.tok_par) {
       const int i = base + tl;
@@ -411,7 +449,16 @@ extern "C" kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_ar
     fn = bf ? (void *)&kv_diag_kernel<bf16, 1, 4, false>
             : (void *)&kv_diag_kernel<float, 1, 4, false>;
   }
+  // the 16-byte-word instances stream through a cp.async ring in dynamic
+  // shared memory
+  size_t dyn = 0;
+  if (runs8 && aligned) {
+    dyn = bf ? ring_bytes<bf16>(nthreads) : ring_bytes<float>(nthreads);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) !=
+        cudaSuccess)
+      return KVX_ERR_CUDA;
+  }
   void *args[] = {&P};
-  return cudaLaunchKernel(fn, grid, dim3(nthreads), args, 0, s) == cudaSuccess ? KVX_OK
-                                                                               : KVX_ERR_CUDA;
+  return cudaLaunchKernel(fn, grid, dim3(nthreads), args, dyn, s) == cudaSuccess ? KVX_OK
+                                                                                 : KVX_ERR_CUDA;
 }
