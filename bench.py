@@ -737,7 +737,15 @@ def time_oracle_diag(wl, mk, mv, rk, rv, target_seconds: float):
 
 def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, paged_src=None):
     """Same metric through the C ABI with HOST buffers: every step copies its
-    inputs from pinned host memory, transfers, and reads the target cache back."""
+    inputs from pinned host memory, transfers, and reads the whole target
+    cache back to pinned host memory.  Steps are pipelined the way a serving
+    loop would run them: host-to-device copies on one stream, the transfer on
+    another, device-to-host copies on a third, with two device buffer sets
+    so that step i's input copy and step i-1's output copy overlap step i's
+    neighbours (events order every reuse of a buffer).  The timed region runs
+    from before the first step's input copy to after the last step's output
+    copy."""
+    import ctypes
     import torch
     from cross_model_kv_transfer_gb300 import kvx
     src = dict(inp)
@@ -746,42 +754,68 @@ def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, paged_src=No
     names = ["src_k", "src_v", "w", "b", "layer_idx", "cu_seqlens", "tgt_offset"]
     names += [n for n in ("block_table", "src_block_table") if n in src]
     host = {n: src[n].cpu().pin_memory() for n in names}
-    hk = torch.empty(dst_k.shape, dtype=dst_k.dtype, pin_memory=True)
-    hv = torch.empty(dst_v.shape, dtype=dst_v.dtype, pin_memory=True)
-    dev_in = {n: torch.empty_like(src[n]) for n in names}
-    dev_paged = None
-    if paged_src is not None:
-        dev_paged = (dev_in["src_k"], dev_in["src_v"], dev_in["src_block_table"])
-    targs = plan.make_args(**transfer_kwargs(wl, dev_in, dst_k, dst_v, status, dev_paged))
-    sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = hk.numel() * hk.element_size() * 2
+    d2h = dst_k.numel() * dst_k.element_size() * 2
+    nbuf = 2
+    dev_in = [{n: torch.empty_like(src[n]) for n in names} for _ in range(nbuf)]
+    dev_out = [(dst_k, dst_v)] + [(torch.empty_like(dst_k), torch.empty_like(dst_v))
+                                  for _ in range(nbuf - 1)]
+    host_out = [(torch.empty(dst_k.shape, dtype=dst_k.dtype, pin_memory=True),
+                 torch.empty(dst_v.shape, dtype=dst_v.dtype, pin_memory=True))
+                for _ in range(nbuf)]
+    targs = []
+    for i in range(nbuf):
+        dp = None
+        if paged_src is not None:
+            dp = (dev_in[i]["src_k"], dev_in[i]["src_v"], dev_in[i]["src_block_table"])
+        targs.append(plan.make_args(**transfer_kwargs(wl, dev_in[i], dev_out[i][0],
+                                                      dev_out[i][1], status, dp)))
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cmp_ptr = ctypes.c_void_p(s_cmp.cuda_stream)
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    issued = [0]
 
     def step():
-        for n in names:
-            dev_in[n].copy_(host[n], non_blocking=True)
-        st = kvx.kvx_transfer(plan.handle, targs, sptr)
+        i = issued[0] % nbuf
+        if issued[0] >= nbuf:
+            s_in.wait_event(ev_cmp[i])         # the transfer that read these inputs is done
+        with torch.cuda.stream(s_in):
+            for n in names:
+                dev_in[i][n].copy_(host[n], non_blocking=True)
+        ev_in[i].record(s_in)
+        s_cmp.wait_event(ev_in[i])
+        if issued[0] >= nbuf:
+            s_cmp.wait_event(ev_out[i])        # the read-back of this cache is done
+        st = kvx.kvx_transfer(plan.handle, targs[i], cmp_ptr)
         if st != kvx.KVX_OK:
             raise kvx.KvxError(st, "kvx_transfer")
-        hk.copy_(dst_k, non_blocking=True)
-        hv.copy_(dst_v, non_blocking=True)
+        ev_cmp[i].record(s_cmp)
+        s_out.wait_event(ev_cmp[i])
+        with torch.cuda.stream(s_out):
+            host_out[i][0].copy_(dev_out[i][0], non_blocking=True)
+            host_out[i][1].copy_(dev_out[i][1], non_blocking=True)
+        ev_out[i].record(s_out)
+        issued[0] += 1
 
     steps = max(1, min(args.steps, 20))
     for _ in range(min(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    ev0.record(stream)
+    t0.record(s_in)
     for _ in range(steps):
         step()
-    ev1.record(stream)
+    t1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier()
-    ms_local = ev0.elapsed_time(ev1) / steps
+    ms_local = t0.elapsed_time(t1) / steps
     value, ms = aggregate(wl.ntok, ms_local, dev)
     return {"value": value, "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelining": "input copy, transfer and read-back on three streams, two buffer sets"}
 
 
 def run_reference(args):
