@@ -200,14 +200,23 @@ def load_peaks():
 
 
 def kernel_source_sha(kernel_name: str) -> str:
-    h = hashlib.sha256()
+    """Hash of what decides a kernel's DRAM traffic: its source file, the
+    library headers it includes (transitively), and the host code that sets
+    its launch shape (tiles per item, CTA pairs)."""
+    import re
     csrc = os.path.join(ROOT, "cross_model_kv_transfer_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        # the kernel, its headers, and the host code that sets its launch
-        # shape (tiles per item, CTA pairs): all of them change its traffic
-        if fn in (KERNEL_FILES.get(kernel_name), "kvx_api.cpp") or fn.endswith((".h", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + b"\0" + f.read())
+    seen, todo = [], [KERNEL_FILES.get(kernel_name), "kvx_api.cpp"]
+    while todo:
+        fn = todo.pop(0)
+        if not fn or fn in seen or not os.path.exists(os.path.join(csrc, fn)):
+            continue
+        seen.append(fn)
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            todo += re.findall(r'#include\s+"([^"/]+)"', f.read())
+    h = hashlib.sha256()
+    for fn in sorted(seen):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 

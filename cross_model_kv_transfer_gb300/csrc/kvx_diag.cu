@@ -28,6 +28,7 @@
 
 #include "kvx_device.cuh"
 #include "kvx_internal.h"
+#include "kvx_async.cuh"
 #include "kvx_ptx.cuh"
 
 namespace {
@@ -75,22 +76,6 @@ __device__ __forceinline__ void load_run(const T *src, float *out) {
 #pragma unroll
     for (int j = 0; j < RL; ++j) out[j] = to_f<T>(src[j]);
   }
-}
-
-// cp.async of 16 bytes global -> shared, bypassing L1; src_bytes = 0 writes
-// zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src,
-                                           uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(smem_dst)),
-               "l"(gmem_src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Stages of the cp.async ring (96 KB of shared memory at 256 threads).

@@ -12,9 +12,10 @@
 //      them, chunks of rows in parallel with fp64 atomics);
 //   3. the centred Gram blocks G = XcT Xc (upper triangle of 64 x 64 tiles)
 //      and C = XcT Yc: a register-tiled fp32 FMA contraction over the
-//      observations (each thread 4 x 4 outputs), fp32 partial sums over 256
-//      observations summed in fp32 over a slice of 16,384, slices in parallel
-//      and added in fp64 with atomics;
+//      observations (each thread 4 x 4 outputs; fp32 observations with p
+//      and q multiples of 4 are staged through a 4-stage cp.async ring),
+//      fp32 partial sums over 256 observations summed in fp32 over a slice
+//      of 16,384, slices in parallel and added in fp64 with atomics;
 //   4. G + lam I mirrored to full, then a Cholesky factorisation in fp64
 //      blocked by 64 (per diagonal block: factor it, solve the panel below,
 //      update the trailing blocks, each step spread over CTAs);
@@ -33,6 +34,7 @@
 #include <cmath>
 
 #include "../../include/kvx.h"
+#include "kvx_async.cuh"
 
 namespace {
 
@@ -177,6 +179,149 @@ __global__ void __launch_bounds__(256) gram_kernel(const T *__restrict__ x, cons
       const int i = i0 + 4 * ty + r, j = j0 + 4 * tx + c;
       if (i >= p || j >= ncols) continue;
       const double v = (double)acc[r][c] + (double)part[r][c];
+      if (is_c)
+        atomicAdd(C + ((int64_t)b * p + i) * q + j, v);
+      else
+        atomicAdd(G + ((int64_t)b * p + i) * p + j, v);
+    }
+}
+
+// The same tile with the observations staged asynchronously (fp32 inputs, p
+// and q multiples of 4, 16-byte aligned bases): every thread copies its own
+// 16-byte words of the next kGramStages - 1 chunks into a ring with
+// cp.async, so global latency overlaps the FMAs; once a chunk has landed the
+// thread centres the words it copied in place (padding stays zero) and the
+// CTA computes on it.
+constexpr int kGramStages = 4;
+constexpr size_t kGramRingBytes = (size_t)kGramStages * 2 * kChunkObs * kTile * sizeof(float);
+
+__global__ void __launch_bounds__(256) gram_async_kernel(const float *__restrict__ x,
+                                                         const float *__restrict__ y,
+                                                         const double *__restrict__ sums,
+                                                         double *__restrict__ G,
+                                                         double *__restrict__ C, int64_t n, int p,
+                                                         int q, int tiles_p, int tiles_q) {
+  extern __shared__ __align__(16) float ring_s[];   // [stage][operand a|b][32][64]
+  __shared__ __align__(16) float mean_a[kTile], mean_b[kTile];
+  const int b = blockIdx.z;
+  int ti, tj;
+  {
+    int t = blockIdx.x;
+    const int n_upper = tiles_p * (tiles_p + 1) / 2;
+    if (t < n_upper) {
+      ti = 0;
+      while (t >= tiles_p - ti) {
+        t -= tiles_p - ti;
+        ++ti;
+      }
+      tj = ti + t;
+    } else {
+      t -= n_upper;
+      ti = t / tiles_q;
+      tj = tiles_p + t % tiles_q;
+    }
+  }
+  const bool is_c = tj >= tiles_p;
+  const int i0 = ti * kTile;
+  const int j0 = (is_c ? tj - tiles_p : tj) * kTile;
+  const int ncols = is_c ? q : p;
+  const float *xa = x + (int64_t)b * n * p;
+  const float *xb = is_c ? y + (int64_t)b * n * q : xa;
+  const double inv_n = 1.0 / (double)n;
+  const int tid = threadIdx.x;
+  if (tid < kTile) {
+    const int i = i0 + tid;
+    mean_a[tid] = i < p ? (float)(sums[(int64_t)b * (p + q) + i] * inv_n) : 0.f;
+  } else if (tid < 2 * kTile) {
+    const int j = j0 + tid - kTile;
+    mean_b[tid - kTile] =
+        j < ncols ? (float)(sums[(int64_t)b * (p + q) + (is_c ? p : 0) + j] * inv_n) : 0.f;
+  }
+  const int64_t t0 = (int64_t)blockIdx.y * kRowsPerSlice;
+  const int64_t t1 = t0 + kRowsPerSlice < n ? t0 + kRowsPerSlice : n;
+  const int chunks = (int)((t1 - t0 + kChunkObs - 1) / kChunkObs);
+  constexpr int kStage = 2 * kChunkObs * kTile;      // floats per stage
+  constexpr int kWords = kChunkObs * kTile / 4;      // 16-byte words per operand per chunk
+  // this thread's words: w = tid + 256 k, k = 0, 1 -> row w / 16, columns 4 (w % 16)..
+  auto issue = [&](int c) {
+    float *st = ring_s + (c % kGramStages) * kStage;
+#pragma unroll
+    for (int k = 0; k < kWords / 256; ++k) {
+      const int w = tid + 256 * k, o = w / (kTile / 4), c4 = 4 * (w % (kTile / 4));
+      const int64_t u = t0 + (int64_t)c * kChunkObs + o;
+      const bool ra = c < chunks && u < t1 && i0 + c4 < p;
+      const bool rb = c < chunks && u < t1 && j0 + c4 < ncols;
+      cp_async16(st + o * kTile + c4, ra ? xa + u * p + i0 + c4 : xa, ra ? 16u : 0u);
+      cp_async16(st + kChunkObs * kTile + o * kTile + c4, rb ? xb + u * ncols + j0 + c4 : xb,
+                 rb ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  const int tx = tid & 15, ty = tid >> 4;
+  float acc[4][4], part[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f, part[r][c] = 0.f;
+  for (int c = 0; c < kGramStages - 1; ++c) issue(c);
+  __syncthreads();   // the means are in place
+  int since_flush = 0;
+  for (int c = 0; c < chunks; ++c) {
+    issue(c + kGramStages - 1);
+    cp_async_wait<kGramStages - 1>();
+    float *st = ring_s + (c % kGramStages) * kStage;
+    // centre the words this thread copied (rows and columns past the data
+    // stay zero)
+#pragma unroll
+    for (int k = 0; k < kWords / 256; ++k) {
+      const int w = tid + 256 * k, o = w / (kTile / 4), c4 = 4 * (w % (kTile / 4));
+      const int64_t u = t0 + (int64_t)c * kChunkObs + o;
+      if (u < t1 && i0 + c4 < p) {
+        float4 *v = reinterpret_cast<float4 *>(st + o * kTile + c4);
+        const float4 m = *reinterpret_cast<const float4 *>(mean_a + c4);
+        float4 a = *v;
+        a.x -= m.x, a.y -= m.y, a.z -= m.z, a.w -= m.w;
+        *v = a;
+      }
+      if (u < t1 && j0 + c4 < ncols) {
+        float4 *v = reinterpret_cast<float4 *>(st + kChunkObs * kTile + o * kTile + c4);
+        const float4 m = *reinterpret_cast<const float4 *>(mean_b + c4);
+        float4 a = *v;
+        a.x -= m.x, a.y -= m.y, a.z -= m.z, a.w -= m.w;
+        *v = a;
+      }
+    }
+    __syncthreads();
+    const float *sa = st, *sb = st + kChunkObs * kTile;
+#pragma unroll 8
+    for (int o = 0; o < kChunkObs; ++o) {
+      const float4 a4 = *reinterpret_cast<const float4 *>(sa + o * kTile + 4 * ty);
+      const float4 b4 = *reinterpret_cast<const float4 *>(sb + o * kTile + 4 * tx);
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) part[r][cc] = fmaf(av[r], bv[cc], part[r][cc]);
+    }
+    __syncthreads();   // the stage is free for the copy issued next
+    since_flush += kChunkObs;
+    if (since_flush >= kFlushObs) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) acc[r][cc] += part[r][cc], part[r][cc] = 0.f;
+      since_flush = 0;
+    }
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int i = i0 + 4 * ty + r, j = j0 + 4 * tx + cc;
+      if (i >= p || j >= ncols) continue;
+      const double v = (double)acc[r][cc] + (double)part[r][cc];
       if (is_c)
         atomicAdd(C + ((int64_t)b * p + i) * q + j, v);
       else
@@ -456,7 +601,17 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
     const float *x = reinterpret_cast<const float *>(a->x);
     const float *y = reinterpret_cast<const float *>(a->y);
     mean_kernel<float><<<mgrid, 256, 0, s>>>(x, y, sums, n, p, q);
-    gram_kernel<float><<<ggrid, 256, 0, s>>>(x, y, sums, G, C, n, p, q, tiles_p, tiles_q);
+    const bool async_ok = p % 4 == 0 && q % 4 == 0 &&
+                          ((((uintptr_t)x) | ((uintptr_t)y)) & 15u) == 0;
+    if (async_ok) {
+      if (cudaFuncSetAttribute(gram_async_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kGramRingBytes) != cudaSuccess)
+        return KVX_ERR_CUDA;
+      gram_async_kernel<<<ggrid, 256, kGramRingBytes, s>>>(x, y, sums, G, C, n, p, q, tiles_p,
+                                                           tiles_q);
+    } else {
+      gram_kernel<float><<<ggrid, 256, 0, s>>>(x, y, sums, G, C, n, p, q, tiles_p, tiles_q);
+    }
   } else {
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a->x);
     const __nv_bfloat16 *y = reinterpret_cast<const __nv_bfloat16 *>(a->y);
