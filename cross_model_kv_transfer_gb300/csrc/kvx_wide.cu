@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       bool pacing = true;
       auto pace = [&]() -> bool {
         const long long ahead = (long long)epochs - kWSyncLag;
-        if (!pacing || ahead <= 0) return true;
+        if (!pacing || geo.sync == nullptr || ahead <= 0) return true;
         const unsigned long long need = producers * (unsigned long long)ahead;
         if (ld_relaxed_gpu(geo.sync) >= need) return true;
         const uint64_t t0 = globaltimer();
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         int lt, mt, nt;
         decode_tile(geo, t, lt, mt, nt);
         if (!kvx::layer_row_ok(p, lt)) {
-          red_add_gpu(geo.sync, (unsigned)geo.epochs_per_tile);
+          if (geo.sync) red_add_gpu(geo.sync, (unsigned)geo.epochs_per_tile);
           epochs += geo.epochs_per_tile;
           continue;
         }
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 bulk_g2s(dst + kWHalfBytes, img + (int64_t)kc * kWChunkBytes, kWHalfBytes, bar);
                 ++x_seq;
                 if (kc % kWSyncSteps == kWSyncSteps - 1 || kc == geo.kc_count - 1) {
-                  red_add_gpu(geo.sync, 1u);
+                  if (geo.sync) red_add_gpu(geo.sync, 1u);
                   ++epochs;
                 }
               }
@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
     producer_done:
       // retire: count the epochs this producer will not issue, so that no
       // other producer waits for them
-      if (epochs < (uint32_t)geo.max_epochs) red_add_gpu(geo.sync, (uint32_t)geo.max_epochs - epochs);
+      if (geo.sync && epochs < (uint32_t)geo.max_epochs)
+        red_add_gpu(geo.sync, (uint32_t)geo.max_epochs - epochs);
       // drain: the last `stages` loads (at most) may still be in flight
       for (uint32_t n = (x_seq > (uint32_t)geo.stages ? x_seq - geo.stages : 0); n < x_seq; ++n)
         wdrain_wait(&sh->full[n % geo.stages], (n / geo.stages) & 1);
@@ -680,9 +681,14 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   geo.stages = wide_stages();
   geo.num_tiles = (long long)p.Lt * geo.mt_count * geo.nt_count;
   geo.stride = geo.num_tiles < plan->tc_pairs ? geo.num_tiles : plan->tc_pairs;
-  geo.sync = sync;
   geo.epochs_per_tile = (KC + kWSyncSteps - 1) / kWSyncSteps;
-  geo.max_epochs = (int)((geo.num_tiles + geo.stride - 1) / geo.stride) * geo.epochs_per_tile;
+  const long long max_epochs =
+      (geo.num_tiles + geo.stride - 1) / geo.stride * (long long)geo.epochs_per_tile;
+  // the 32-bit counter must hold every producer's epochs; past that the
+  // kernel runs unpaced
+  const bool paced = 2 * geo.stride * max_epochs < (1ll << 31);
+  geo.sync = paced ? sync : nullptr;
+  geo.max_epochs = paced ? (int)max_epochs : 0;
   // values: read in place, or (paged source) packed first into the plan's
   // buffer; the keys' pre-pass above read a paged source directly
   const void *vals = p.src_v;
