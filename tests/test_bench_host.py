@@ -75,3 +75,37 @@ def test_published_context_number_is_the_32k_mapper_latency():
     # the Qwen3 article's 14B -> 32B mapper: 277.6 ms at 32,768 tokens
     assert bench.PUBLISHED_MS["qwen3_14b_32b"] == 277.6
     assert json.dumps(bench.METRIC)
+
+
+def test_wide_roofline_uses_the_wide_map_accounting():
+    # one [8192 x 2048] map per target layer: 70.37 TFLOP per 32K transfer,
+    # W counted as stored (fp32, 4.3 GB)
+    wl = WORKLOADS["qwen3_14b_32b"]
+    idx = torch.stack([torch.arange(4) + i % 36 for i in range(64)]).to(torch.int32)
+    assert wl.wide_algorithmic_flops() == 2 * 32768 * 8192 * 2048 * 64
+    peaks = {"hbm_gbs": 6766.7, "bf16_tflops": 1908.0, "bf16_tflops_sustained": 1679.6}
+    r = bench.roofline(wl, idx, 46.0, "wide", peaks, "measured", wide=True)
+    assert r["bound"] == "tensor"
+    assert r["frac_of_sustained"] == pytest.approx(r["achieved"] / 1679.6)
+    w_bytes = 64 * 8192 * 2048 * 4
+    assert r["algorithmic_bytes"] - wl.algorithmic_bytes(idx) == pytest.approx(
+        w_bytes - 64 * 8 * 2 * 512 * 128 * 4, rel=0, abs=64 * 2048 * 2)
+
+
+def test_kernel_source_hash_follows_includes_only():
+    # a kernel's hash covers its file, the csrc headers it includes
+    # (transitively) and the host launch code, not unrelated headers
+    h1 = bench.kernel_source_sha("diag")
+    assert h1 == bench.kernel_source_sha("diag") and len(h1) == 16
+    assert bench.kernel_source_sha("tcgen05") != h1
+    csrc = os.path.join(bench.ROOT, "cross_model_kv_transfer_gb300", "csrc")
+    tc = open(os.path.join(csrc, "kvx_tcgen05.cu")).read()
+    assert '#include "kvx_async.cuh"' not in tc     # so kvx_async.cuh cannot move its hash
+
+
+def test_dram_records_name_known_kernels_and_commands():
+    rows = json.load(open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")))
+    for r in rows:
+        assert r["kernel"] in bench.KERNEL_FILES
+        assert r["dram_bytes_per_launch"] == r["dram_bytes_read"] + r["dram_bytes_write"]
+        assert r["command"].startswith("ncu ") and "--clock-control none" in r["command"]
