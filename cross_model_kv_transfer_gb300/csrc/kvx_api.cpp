@@ -247,23 +247,38 @@ kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out) {
   p->stall_test = (desc->flags & KVX_PLAN_TEST_STALL) ? 1 : 0;
 
   p->max_tokens = desc->max_tokens > 0 ? desc->max_tokens : desc->max_position;
-  if (wide) {
-    // no RoPE tables: both bases are evaluated from fixed-point phases
-  } else if (kernel == KVX_KERNEL_SIMT) {
-    // fp32 tables from fp64 host trigonometry (the fp32 path's 1e-5 budget)
-    st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
-                &p->rope_src);
-    if (st == KVX_OK) {
-      if (desc->rope_theta_tgt == desc->rope_theta_src)
-        p->rope_tgt = p->rope_src;
-      else
-        st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
-                    &p->rope_tgt);
+  // RoPE tables: one device copy each, built on the host first.  Tables
+  // larger than the device are refused before the host buffer is made, and
+  // a failed host allocation is reported rather than thrown across the C ABI.
+  const size_t positions = (size_t)desc->max_position;
+  const size_t table_bytes =
+      wide ? 0
+      : kernel == KVX_KERNEL_SIMT
+          ? positions * (size_t)p->half * sizeof(float2) *
+                (desc->rope_theta_tgt == desc->rope_theta_src ? 1 : 2)
+          : positions * (size_t)(desc->src_head_dim / 8) * 16;
+  if (table_bytes > prop.totalGlobalMem) st = KVX_ERR_NO_MEMORY;
+  try {
+    if (st != KVX_OK || wide) {
+      // wide: no RoPE tables, both bases are evaluated from fixed-point phases
+    } else if (kernel == KVX_KERNEL_SIMT) {
+      // fp32 tables from fp64 host trigonometry (the fp32 path's 1e-5 budget)
+      st = upload(rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position),
+                  &p->rope_src);
+      if (st == KVX_OK) {
+        if (desc->rope_theta_tgt == desc->rope_theta_src)
+          p->rope_tgt = p->rope_src;
+        else
+          st = upload(rope_table(desc->rope_theta_tgt, desc->tgt_head_dim, desc->max_position),
+                      &p->rope_tgt);
+      }
+    } else {
+      std::vector<uint32_t> ts;
+      tc_rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position, ts);
+      st = upload_bytes(ts.data(), ts.size() * sizeof(uint32_t), &p->tc_rope_src);
     }
-  } else {
-    std::vector<uint32_t> ts;
-    tc_rope_table(desc->rope_theta_src, desc->src_head_dim, desc->max_position, ts);
-    st = upload_bytes(ts.data(), ts.size() * sizeof(uint32_t), &p->tc_rope_src);
+  } catch (...) {
+    st = KVX_ERR_NO_MEMORY;
   }
   // target frequencies in turns: the tensor-core epilogue and the
   // diagnostics kernel (any plan) evaluate target RoPE angles from them

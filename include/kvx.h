@@ -125,8 +125,8 @@ typedef struct {
   int32_t src_head_dim;     /* d, even, 2..256; must equal tgt_head_dim       */
   int32_t tgt_head_dim;
   int32_t k;                /* selected source layers per target layer, >= 1 */
-  double rope_theta_src;    /* RoPE base of the source model, > 1             */
-  double rope_theta_tgt;    /* RoPE base of the target model, > 1             */
+  double rope_theta_src;    /* RoPE base of the source model, finite, > 0     */
+  double rope_theta_tgt;    /* RoPE base of the target model, finite, > 0     */
   int32_t kv_dtype;         /* kvx_dtype of source and target K/V             */
   int32_t w_dtype;          /* kvx_dtype of W                                 */
   int32_t b_dtype;          /* kvx_dtype of b                                 */
@@ -224,7 +224,9 @@ typedef struct {
  * Returns KVX_ERR_INVALID_ARG / KVX_ERR_PAIR_MISMATCH for a bad descriptor
  * (before touching the device), KVX_ERR_UNSUPPORTED if the current device
  * is not sm_103 or the forced kernel cannot handle the shape, KVX_ERR_CUDA or
- * KVX_ERR_NO_MEMORY if the device work fails.  On error *out is NULL. */
+ * KVX_ERR_NO_MEMORY if the device work fails (KVX_ERR_NO_MEMORY also when
+ * the RoPE tables of max_position would not fit the device, or their host
+ * staging buffer cannot be allocated).  On error *out is NULL. */
 kvx_status kvx_plan_create(const kvx_plan_desc *desc, kvx_plan **out);
 
 /* Enqueue one transfer on `stream` (a cudaStream_t; NULL is the legacy
