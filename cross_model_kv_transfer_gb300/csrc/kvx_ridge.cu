@@ -578,9 +578,12 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
     return KVX_ERR_INVALID_ARG;
   if (a->workspace_bytes < kvx_ridge_workspace_bytes(a->batch, a->p, a->q))
     return KVX_ERR_INVALID_ARG;
+  const int64_t n = a->n;
+  const int64_t slices64 = (n + kRowsPerSlice - 1) / kRowsPerSlice;
+  if (slices64 > 65535) return KVX_ERR_INVALID_ARG;  // grid y; checked before any launch
+  const int slices = (int)slices64;
   cudaStream_t s = (cudaStream_t)stream;
   const int batch = a->batch, p = a->p, q = a->q;
-  const int64_t n = a->n;
   unsigned char *ws = reinterpret_cast<unsigned char *>(a->workspace);
   double *sums = reinterpret_cast<double *>(ws);
   double *G = reinterpret_cast<double *>(ws + round256(ws_sums(batch, p, q)));
@@ -591,8 +594,6 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   clear_kernel<<<1024, 256, 0, s>>>(sums, words);
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
 
-  const int slices = (int)((n + kRowsPerSlice - 1) / kRowsPerSlice);
-  if (slices > 65535) return KVX_ERR_INVALID_ARG;
   dim3 mgrid((unsigned)((p + q + 255) / 256), (unsigned)slices, (unsigned)batch);
   const int tiles_p = (p + kTile - 1) / kTile, tiles_q = (q + kTile - 1) / kTile;
   dim3 ggrid((unsigned)(tiles_p * (tiles_p + 1) / 2 + tiles_p * tiles_q), (unsigned)slices,

@@ -326,7 +326,7 @@ kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_args *args, v
  * pointers; arrays dense and row-major. */
 typedef struct {
   int32_t batch;            /* independent fits, 1..65535                     */
-  int64_t n;                /* observations per fit, >= 1                     */
+  int64_t n;                /* observations per fit, 1..65535*16384           */
   int32_t p;                /* features per observation, 1..4096              */
   int32_t q;                /* outputs per observation, 1..4096               */
   double lambda;            /* ridge strength, added unscaled to the diagonal */

@@ -136,3 +136,7 @@ def test_ridge_workspace_size_and_host_validation():
     assert kvx.kvx_ridge_fit(a, None) == kvx.KVX_ERR_INVALID_ARG      # workspace too small
     a = kvx.RidgeArgs(1, 10, 4, 2, float("inf"), kvx.KVX_F32, 16, 16, 16, 16, 16, 1 << 20, None)
     assert kvx.kvx_ridge_fit(a, None) == kvx.KVX_ERR_INVALID_ARG      # lambda not finite
+    # more observations than 65,535 slices of 16,384 is refused before any launch
+    a = kvx.RidgeArgs(1, 65535 * 16384 + 1, 4, 2, 0.01, kvx.KVX_F32, 16, 16, 16, 16, 16, 1 << 20,
+                      None)
+    assert kvx.kvx_ridge_fit(a, None) == kvx.KVX_ERR_INVALID_ARG
