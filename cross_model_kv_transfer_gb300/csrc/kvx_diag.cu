@@ -385,9 +385,6 @@ extern "C" kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_ar
   const int half = p.d / 2;
   const int64_t nstats = (int64_t)p.Lt * p.H * 2 * (p.d + 4);
   const int zb = (int)((nstats + 255) / 256 < 1024 ? (nstats + 255) / 256 : 1024);
-  zero_kernel<<<zb, 256, 0, s>>>(a->stats, nstats);
-  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
-  if (a->ntok == 0) return KVX_OK;
 
   // lanes: runs of 8 pairs when half is a multiple of 8 (16- or 32-byte
   // loads), else single pairs, up to 32 lanes per row and EMAX runs a lane
@@ -419,8 +416,12 @@ extern "C" kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_ar
   P.chunk = chunk;
   const int64_t gy = (int64_t)p.Lt * P.slot_groups;
   const int64_t gx = (p.ntok + chunk - 1) / chunk;
-  if (gy > 65535 || gx > INT32_MAX) return KVX_ERR_UNSUPPORTED;
+  if (gy > 65535 || gx > INT32_MAX) return KVX_ERR_UNSUPPORTED;  // before any launch
   dim3 grid((unsigned)gx, (unsigned)gy);
+
+  zero_kernel<<<zb, 256, 0, s>>>(a->stats, nstats);
+  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
+  if (a->ntok == 0) return KVX_OK;
 
   void *fn;
   using bf16 = __nv_bfloat16;

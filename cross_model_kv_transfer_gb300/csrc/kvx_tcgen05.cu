@@ -870,12 +870,22 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p_in, cudaStrea
   // boxes read 128 consecutive rows); the kernel still applies the source
   // block checks to skip and flag the tokens it cannot read
   KvxParams p = p_in;
-  if (p.src_layout == KVX_PAGED) {
-    cudaError_t pe = kvx_pack_source(p, plan->packed_k, plan->packed_v, plan->max_tokens, 2, s);
-    if (pe != cudaSuccess) return pe;
+  const bool paged_src = p.src_layout == KVX_PAGED;
+  if (paged_src) {
     p.src_k = plan->packed_k;
     p.src_v = plan->packed_v;
     p.src_rows = plan->max_tokens;
+  }
+  // the tensor maps before any launch: a map the driver refuses is reported
+  // with nothing enqueued
+  CUtensorMap mk, mv, mc;
+  if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p) ||
+      !encode_cpl_map(plan, &mc, p))
+    return cudaErrorInvalidValue;
+  if (paged_src) {
+    cudaError_t pe =
+        kvx_pack_source(p_in, plan->packed_k, plan->packed_v, plan->max_tokens, 2, s);
+    if (pe != cudaSuccess) return pe;
   }
   // 1. W -> bf16 image in the plan workspace
   dim3 wgrid((unsigned)((int64_t)p.Lt * p.H * 2), (unsigned)(2 * p.k));
@@ -905,10 +915,6 @@ cudaError_t kvx_tc_launch(const kvx_plan *plan, const KvxParams &p_in, cudaStrea
   geo.stages = max_stages(p.k, P);
   const long long slots = P == 2 ? plan->tc_pairs : plan->num_sms;
   geo.stride = geo.num_items < slots ? geo.num_items : slots;
-  CUtensorMap mk, mv, mc;
-  if (!encode_map(plan, &mk, p.src_k, p) || !encode_map(plan, &mv, p.src_v, p) ||
-      !encode_cpl_map(plan, &mc, p))
-    return cudaErrorInvalidValue;
   RopeTurns rope;
   for (int i = 0; i < kHalf; ++i) rope.tgt[i] = plan->turns_tgt[i];
   const uint4 *rope_src4 = reinterpret_cast<const uint4 *>(plan->tc_rope_src);

@@ -641,6 +641,17 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   __nv_bfloat16 *content = reinterpret_cast<__nv_bfloat16 *>(
       ws + align256(wide_img_bytes(d)) + align256(wide_bias_bytes(d)) + 256);
 
+  // values: read in place, or (paged source) packed first into the plan's
+  // buffer; the keys' pre-pass below reads a paged source directly
+  const void *vals = p.src_layout == KVX_PAGED ? plan->packed_v : p.src_v;
+  const int64_t val_rows = p.src_layout == KVX_PAGED ? plan->max_tokens : p.src_rows;
+  // the tensor maps before any launch: a map the driver refuses is reported
+  // with nothing enqueued
+  CUtensorMap mk, mv;
+  if (!encode_wide_map(plan, &mk, content, p.ntok, plan->max_tokens, p.H, p.Ls) ||
+      !encode_wide_map(plan, &mv, vals, p.ntok, val_rows, p.H, p.Ls))
+    return cudaErrorInvalidValue;
+
   // 1. un-rotated source keys
   WideTurns src_turns, tgt_turns;
   for (int i = 0; i < kWHalf; ++i) {
@@ -689,20 +700,10 @@ cudaError_t kvx_wide_launch(const kvx_plan *plan, const KvxParams &p, cudaStream
   const bool paced = 2 * geo.stride * max_epochs < (1ll << 31);
   geo.sync = paced ? sync : nullptr;
   geo.max_epochs = paced ? (int)max_epochs : 0;
-  // values: read in place, or (paged source) packed first into the plan's
-  // buffer; the keys' pre-pass above read a paged source directly
-  const void *vals = p.src_v;
-  int64_t val_rows = p.src_rows;
   if (p.src_layout == KVX_PAGED) {
     e = kvx_pack_source(p, nullptr, plan->packed_v, plan->max_tokens, 2, s);
     if (e != cudaSuccess) return e;
-    vals = plan->packed_v;
-    val_rows = plan->max_tokens;
   }
-  CUtensorMap mk, mv;
-  if (!encode_wide_map(plan, &mk, content, p.ntok, plan->max_tokens, p.H, p.Ls) ||
-      !encode_wide_map(plan, &mv, vals, p.ntok, val_rows, p.H, p.Ls))
-    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * geo.stride), 1, 1);
   cfg.blockDim = dim3(kWThreads, 1, 1);

@@ -318,8 +318,9 @@ typedef struct {
  * combined in fp64; the order of the fp64 additions is not fixed.
  * Asynchronous on `stream`, no allocation, two kernel launches (clear the
  * stats, accumulate).  Returns KVX_ERR_INVALID_ARG for a NULL plan/args, a
- * missing pointer or size, or a plan of another device; KVX_ERR_CUDA if a
- * launch fails. */
+ * missing pointer or size, or a plan of another device; KVX_ERR_UNSUPPORTED
+ * when target layers x row groups exceed 65,535 CTAs in the grid's y
+ * dimension (nothing enqueued); KVX_ERR_CUDA if a launch fails. */
 kvx_status kvx_kv_diagnostics(const kvx_plan *plan, const kvx_diag_args *args, void *stream);
 
 /* Arguments of a batch of independent ridge fits (kvx_ridge_fit).  DEVICE
