@@ -305,6 +305,53 @@ def time_oracle(wl, inp, target_seconds: float, wide=False):
 # arms
 # --------------------------------------------------------------------------
 
+def select_workload(args):
+    """The transfer workload both arms run: the named one, with the
+    profiling overrides of token count and target layers applied."""
+    import dataclasses
+    from cross_model_kv_transfer_gb300.workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.with_tokens([args.tokens], [wl.tgt_offsets[0]], name=f"{wl.name}@{args.tokens}")
+    if args.tgt_layers:
+        wl = dataclasses.replace(wl, tgt_layers=args.tgt_layers,
+                                 name=f"{wl.name}/Lt{args.tgt_layers}")
+    return wl
+
+
+def transfer_metric(wl, wide: bool) -> str:
+    if wl.name == "qwen3_14b_32b":
+        return WIDE_METRIC if wide else METRIC
+    return (f"KV-transfer tokens/s, {wl.name} shape"
+            f"{', wide-feature mapper' if wide else ''}; % of HBM/tensor roofline")
+
+
+def transfer_config(wl, args) -> dict:
+    """Workload keys of a transfer line, the same in both arms."""
+    from cross_model_kv_transfer_gb300.workloads import PAGED
+    return {"workload": wl.name, "src_layers": wl.src_layers, "tgt_layers": wl.tgt_layers,
+            "kv_heads": wl.kv_heads, "head_dim": wl.head_dim, "k": wl.k, "tokens": wl.ntok,
+            "requests": wl.num_requests,
+            "layout": "paged" if wl.layout == PAGED else "contiguous",
+            "mapper": args.mapper,
+            "source": (f"paged, {args.src_block_size}-token blocks"
+                       if args.src_block_size else "packed rows")}
+
+
+def diag_config(wl) -> dict:
+    """Workload keys of a diagnostics line, the same in both arms."""
+    from cross_model_kv_transfer_gb300.workloads import PAGED
+    return {"workload": wl.name, "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
+            "head_dim": wl.head_dim, "tokens": wl.ntok, "requests": wl.num_requests,
+            "layout": "paged" if wl.layout == PAGED else "contiguous"}
+
+
+def ridge_config(wl, batch: int, n: int) -> dict:
+    """Workload keys of a ridge-fit line, the same in both arms."""
+    return {"workload": f"{wl.name} per-head maps", "fits": batch, "observations": n,
+            "features": wl.k * wl.head_dim, "outputs": wl.head_dim, "lambda": 0.01}
+
+
 def kernel_code(name):
     from cross_model_kv_transfer_gb300 import kvx
     return {"auto": kvx.KVX_KERNEL_AUTO, "simt": kvx.KVX_KERNEL_SIMT,
@@ -449,8 +496,7 @@ def run_ridge(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded paired observations with a planted map)",
-        "config": {"workload": f"{wl.name} per-head maps", "fits": B, "observations": n,
-                   "features": p, "outputs": q, "lambda": 0.01,
+        "config": {**ridge_config(wl, B, n),
                    "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2 ({(x.numel() + y.numel()) * 4 / 1e9:.2f} GB "
                          "read per step, no flush needed)"},
@@ -471,13 +517,7 @@ def run_kvx(args):
     _, _, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = WORKLOADS[args.workload]
-    if args.tokens:
-        wl = wl.with_tokens([args.tokens], [wl.tgt_offsets[0]], name=f"{wl.name}@{args.tokens}")
-    if args.tgt_layers:
-        import dataclasses
-        wl = dataclasses.replace(wl, tgt_layers=args.tgt_layers,
-                                 name=f"{wl.name}/Lt{args.tgt_layers}")
+    wl = select_workload(args)
     inp = make_inputs(wl, dev)
     wide = args.mapper == "wide"
     if wide:
@@ -558,9 +598,7 @@ def run_kvx(args):
                          f"({el:.1f} s of fp64 CPU work, one thread{scaled})"}
     pub = PUBLISHED_MS.get(wl.name)
     line = {
-        "metric": (WIDE_METRIC if wide else METRIC) if wl.name == "qwen3_14b_32b" else
-                  f"KV-transfer tokens/s, {wl.name} shape"
-                  f"{', wide-feature mapper' if wide else ''}; % of HBM/tensor roofline",
+        "metric": transfer_metric(wl, wide),
         "value": value, "unit": "tokens/s",
         "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -568,15 +606,8 @@ def run_kvx(args):
         "vs_baseline": (value / (wl.ntok / (pub / 1e3))) if pub else None,
         "dtype": "bf16" if wl.kv_dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded; shapes and value recipe of the pages' workloads)",
-        "config": {"workload": wl.name, "src_layers": wl.src_layers,
-                   "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
-                   "head_dim": wl.head_dim, "k": wl.k, "tokens": wl.ntok,
-                   "requests": wl.num_requests,
-                   "layout": "paged" if wl.layout == PAGED else "contiguous",
+        "config": {**transfer_config(wl, args),
                    "kernel": kname, "cta_group": plan.cta_group,
-                   "mapper": args.mapper,
-                   "source": (f"paged, {args.src_block_size}-token blocks"
-                              if args.src_block_size else "packed rows"),
                    "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (source "
                          f"{inp['src_k'].numel() * 2 * inp['src_k'].element_size() / 1e9:.2f} GB,"
@@ -704,9 +735,7 @@ def run_diag(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, ws, rank):
         "dtype": "bf16" if wl.kv_dtype == torch.bfloat16 else "f32",
         "data": "synthetic (mapped cache from one transfer of the seeded workload; the "
                 "target's own cache stood in by a seeded perturbation of it)",
-        "config": {"workload": wl.name, "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
-                   "head_dim": wl.head_dim, "tokens": wl.ntok, "requests": wl.num_requests,
-                   "layout": "paged" if wl.layout == PAGED else "contiguous",
+        "config": {**diag_config(wl),
                    "parallelism": f"replicas x{ws}",
                    "l2": f"inputs larger than L2 ({4 * dst_k.numel() * eb / 1e9:.2f} GB of "
                          "caches read per step, no flush needed)"},
@@ -832,43 +861,93 @@ def run_e2e(args, wl, inp, plan, dev, stream, dst_k, dst_v, status, paged_src=No
 
 
 def run_reference(args):
-    """The fp64 oracle, as it stands, on the machine's host cores: each step is a
-    bounded sample (a few source tokens through every target layer, head and
-    K|V) of the same workload."""
+    """The fp64 oracle, as it stands, on the machine's host cores (one thread),
+    for the same op, workload, metric and config as the GPU arm.  Each step
+    is a bounded sample of that workload, stated in ``cpu_baseline.sample``:
+    a few source tokens through every target layer, head and K|V (through
+    two target layers for the wide map, scaled to all: the work is linear in
+    the target layers), a few tokens of the two caches for the diagnostics,
+    one fit on its first observations for the ridge fit (scaled to all
+    observations)."""
     import torch
     import oracle
-    from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
+    from cross_model_kv_transfer_gb300 import workloads as W
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]
-    per_step = 2
-    small = wl.with_tokens([per_step], [0])
-    inp = make_inputs(small, "cpu")
-    sample = oracle_sample_inputs(small, inp, per_step)
+    f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
+    if args.op == "ridge_fit":
+        wl = W.WORKLOADS[args.workload]
+        m = 256
+        x, y = W.make_ridge_inputs(wl, 1, m, "cpu")
+        xs, ys = f64(x[0]), f64(y[0])
+        run = lambda: oracle.ridge_fit(xs, ys, 0.01)
+        scale = args.ridge_n / m                    # one fit = n / m samples
+        metric, unit, config = RIDGE_METRIC, "fits/s", ridge_config(wl, args.ridge_batch,
+                                                                    args.ridge_n)
+        units = 1.0
+        sample = (f"one fit on its first {m} of {args.ridge_n} observations per step, "
+                  f"scaled to {args.ridge_n} observations")
+    elif args.op == "kv_diagnostics":
+        wl = select_workload(args)
+        n = 16
+        small = wl.with_tokens([n], [0])
+        inp = W.make_inputs(small, "cpu")
+        mk, mv, _ = oracle.transfer(**oracle_sample_inputs(small, inp, n))
+        rk = f64(W.perturbed_like(torch.from_numpy(mk), 101))
+        rv = f64(W.perturbed_like(torch.from_numpy(mv), 102))
+        run = lambda: oracle.kv_diagnostics(mapped_k=mk, mapped_v=mv, ref_k=rk, ref_v=rv,
+                                            theta_tgt=wl.theta_tgt, max_position=n, ntok=n,
+                                            dst_capacity=n)
+        scale, units = 1.0, float(n)
+        metric, unit, config = DIAG_METRIC, "tokens/s", diag_config(wl)
+        sample = (f"{n} tokens of a mapped cache and a perturbed copy per step through all "
+                  f"{wl.tgt_layers} target layers x {wl.kv_heads} heads x K|V")
+    else:
+        import dataclasses
+        wl = select_workload(args)
+        wide = args.mapper == "wide"
+        n = 1 if wide else 2
+        L = min(wl.tgt_layers, 2) if wide else wl.tgt_layers
+        small = dataclasses.replace(wl.with_tokens([n], [0]), tgt_layers=L)
+        inp = W.make_inputs(small, "cpu")
+        if wide:
+            inp["w"] = W.make_wide_weights(small, "cpu")
+        kw = oracle_sample_inputs(small, inp, n, wide=wide)
+        if args.src_block_size:
+            pk, pv, table = W.make_paged_source(small, inp, args.src_block_size)
+            kw.update(src_k=f64(pk), src_v=f64(pv), src_layout=oracle.PAGED,
+                      src_block_size=args.src_block_size,
+                      src_block_table=table.numpy(), ntok=n)
+        run = lambda: oracle.transfer(**kw)
+        scale, units = wl.tgt_layers / L, float(n)
+        metric, unit, config = transfer_metric(wl, wide), "tokens/s", transfer_config(wl, args)
+        sample = (f"{n} source token{'s' if n > 1 else ''} per step through {L} target layers"
+                  f" x {wl.kv_heads} heads x K|V"
+                  + (f", scaled to all {wl.tgt_layers}" if L < wl.tgt_layers else "")
+                  + (f", read through {args.src_block_size}-token source blocks"
+                     if args.src_block_size else ""))
     for _ in range(args.warmup):
-        oracle.transfer(**sample)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.transfer(**sample)
-    el = time.perf_counter() - t0
-    value = per_step * args.steps / el
+        run()
+    el = (time.perf_counter() - t0) * scale
+    value = units * args.steps / el
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "src_layers": wl.src_layers,
-                   "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
-                   "head_dim": wl.head_dim, "k": wl.k, "tokens": wl.ntok,
-                   "layout": "paged" if wl.layout == PAGED else "contiguous"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{per_step} source tokens per step through all "
-                                   f"{wl.tgt_layers} target layers x {wl.kv_heads} heads x K|V"},
-        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+        "config": config,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
+    if args.op != "transfer":
+        line["op"] = args.op                      # as the GPU arm's line for this op
     print(json.dumps(line), flush=True)
 
 
