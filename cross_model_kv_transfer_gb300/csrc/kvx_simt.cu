@@ -76,18 +76,20 @@ __global__ void __launch_bounds__(kThreads) simt_transfer_kernel(KvxParams p) {
     s_layer_ok = kvx::layer_row_ok(p, lt);
   }
   __syncthreads();
-  if (tid < TT) {
-    const int64_t g = t0 + tid;
+  // one entry per tile row; for head dims below 16 a tile has more rows
+  // (8 G) than the CTA has threads (d/2 x G), so the threads stride over them
+  for (int q = tid; q < TT; q += blockDim.x * blockDim.y) {
+    const int64_t g = t0 + q;
     int32_t ps = 0, pt = 0;
     int64_t row = -1, srow = -1;
     if (g < p.ntok) {
       const uint32_t bad = kvx::token_meta(p, g, ps, pt, row, srow);
       if (bad) atomicOr(&s_bits, bad);
     }
-    s_row[tid] = row;
-    s_srow[tid] = srow;
-    s_ps[tid] = ps;
-    s_pt[tid] = pt;
+    s_row[q] = row;
+    s_srow[q] = srow;
+    s_ps[q] = ps;
+    s_pt[q] = pt;
   }
   __syncthreads();
   if (tid == 0) {

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from cross_model_kv_transfer_gb300 import kvx
-from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
+from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs, sentinel_like
 
 from parity import (TC_SINGLE, TOL, assert_parity, gpu_args, kernel_code, make_plan, run_gpu,
                     run_oracle)
@@ -263,3 +263,53 @@ def test_tcgen05_pipeline_wait_gives_up_and_reports_timeout(flags):
     assert st == 0
     rk, rv, _ = run_oracle(wl, inp)
     assert_parity(wl, gk, gv, rk, rv)
+
+
+@pytest.mark.parametrize("d,k", [(2, 1), (4, 3), (6, 2), (10, 2), (14, 1), (256, 3)])
+def test_simt_head_dims_at_the_limits_match_oracle(d, k):
+    # Below d = 16 a SIMT tile holds more rows (8 G) than its CTA has threads
+    # (d/2 x G), so the row bookkeeping is strided; d = 2 is a single RoPE
+    # pair, 256 the largest head dim.  Three requests with target offsets
+    # leave ragged tails across several tiles.
+    seqlens = (700, 3, 333) if d < 256 else (300, 3, 33)
+    wl = dataclasses.replace(WORKLOADS["tiny_fp32"], name=f"tiny_fp32_d{d}_k{k}", head_dim=d,
+                             k=k, seqlens=seqlens, tgt_offsets=(0, 5, 2))
+    inp = make_inputs(wl, "cuda")
+    gk, gv, st, plan = run_gpu(wl, inp, kvx.KVX_KERNEL_SIMT)
+    assert st == 0 and plan.kernel == kvx.KVX_KERNEL_SIMT
+    rk, rv, rst = run_oracle(wl, inp)
+    assert rst == 0
+    assert_parity(wl, gk, gv, rk, rv)
+
+
+@pytest.mark.parametrize("kernel", BF16_KERNELS)
+def test_empty_transfer_enqueues_nothing(kernel):
+    # ntok = 0 through the C ABI (valid buffers, zero tokens): the call
+    # succeeds, the status word and both caches keep their bits
+    wl = WORKLOADS["qwen3_0p6b_1p7b"]
+    inp = make_inputs(wl, "cuda")
+    plan = make_plan(wl, kernel)
+    shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
+    dk = sentinel_like(shape, wl.kv_dtype, "cuda")
+    dv = sentinel_like(shape, wl.kv_dtype, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    args = plan.make_args(**gpu_args(wl, inp, dk, dv, status))
+    args.ntok = 0
+    assert kvx.kvx_transfer(plan.handle, args, None) == kvx.KVX_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert bool((dk.view(torch.int16) == -1).all()) and bool((dv.view(torch.int16) == -1).all())
+
+
+def test_empty_diagnostics_clear_the_statistics():
+    wl = WORKLOADS["qwen3_0p6b_1p7b"]
+    plan = make_plan(wl, kvx.KVX_KERNEL_TCGEN05)
+    shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
+    cache = torch.ones(shape, dtype=wl.kv_dtype, device="cuda")
+    stats = torch.full((wl.tgt_layers, wl.kv_heads, 2, wl.head_dim + 4), 7.0,
+                       dtype=torch.float64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    plan.kv_diagnostics(mapped_k=cache, mapped_v=cache, ref_k=cache, ref_v=cache, stats=stats,
+                        status=status, ntok=0, dst_capacity=wl.dst_capacity)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and bool((stats == 0).all())
