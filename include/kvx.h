@@ -96,7 +96,9 @@ typedef enum {
   KVX_KERNEL_AUTO = 0,        /* tensor-core path when the shape allows it  */
   KVX_KERNEL_SIMT = 1,        /* fp32 FMA contraction (any even head_dim)   */
   KVX_KERNEL_TCGEN05 = 2      /* tcgen05 tensor cores: bf16 K/V,
-                                 head_dim 128                                */
+                                 head_dim 128, k <= 6 for the per-head map
+                                 (W takes k x 32 KB of shared memory; AUTO
+                                 picks SIMT beyond)                          */
 } kvx_kernel;
 
 /* Which map the transfer applies.
