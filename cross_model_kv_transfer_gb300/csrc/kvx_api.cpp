@@ -349,7 +349,10 @@ kvx_status kvx_transfer(const kvx_plan *plan, const kvx_transfer_args *a, void *
   if (a->ntok < 0 || a->ntok > INT32_MAX) return KVX_ERR_INVALID_ARG;
   if (a->num_requests < 1) return KVX_ERR_INVALID_ARG;
   if (!a->cu_seqlens && a->num_requests != 1) return KVX_ERR_INVALID_ARG;
-  if (!a->src_k || !a->src_v || !a->layer_idx || !a->w || !a->b || !a->dst_k || !a->dst_v)
+  // with no tokens nothing is read from the source: its pointers may be NULL
+  // (zero-row arrays have no storage)
+  if ((a->ntok > 0 && (!a->src_k || !a->src_v)) || !a->layer_idx || !a->w || !a->b ||
+      !a->dst_k || !a->dst_v)
     return KVX_ERR_INVALID_ARG;
   // the tensor-core path reads the source through TMA (16-byte aligned bases)
   // and writes the cache in whole 32-byte sectors (32-byte aligned bases)

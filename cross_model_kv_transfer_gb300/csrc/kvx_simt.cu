@@ -237,6 +237,40 @@ static __device__ __align__(256) float2 g_static_rope[kStaticRopeEntries];
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mu;
 float2 *g_static_ptr[kMaxDevices];    // device address of g_static_rope, per device
+unsigned long long g_static_ctx[kMaxDevices];   // id of the context it was looked up in
+
+// Unique id of the calling thread's current CUDA context (never reused within
+// a process), 0 if there is none or the driver does not report it.  A device
+// reset destroys the primary context and the module with it, so an address
+// looked up in an earlier context is stale; the id tells the two apart.
+unsigned long long current_context_id() {
+  typedef int (*GetCurrentFn)(void **);
+  typedef int (*GetIdFn)(void *, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void *f = nullptr, *g = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &g, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+      get_id = reinterpret_cast<GetIdFn>(g);
+    } else {
+      cudaGetLastError();
+    }
+    looked_up = true;
+  }
+  if (!get_current || !get_id) return 0;
+  void *ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
 
 // cos/sin(p * theta^(-2i/d)) for p in [0, max_position), i in [0, d/2), in
 // double precision on the device, rounded once to fp32; same layout as the
@@ -304,16 +338,20 @@ extern "C" kvx_status kvx_transfer_static(const kvx_plan_desc *desc,
   if (cudaGetDevice(&dev) != cudaSuccess) return KVX_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return KVX_ERR_UNSUPPORTED;
   {
-    // once per device, with that device current: the device address of the
-    // static array (its host-side name is only a stand-in for it)
+    // once per device and context, with that device current: the device
+    // address of the static array (its host-side name is only a stand-in for
+    // it).  The lookup is repeated when the device's context has been
+    // recreated (cudaDeviceReset), since the old address no longer holds.
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_static_ptr[dev] || ctx == 0 || ctx != g_static_ctx[dev]) {
       cudaDeviceProp prop;
       if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return KVX_ERR_CUDA;
       if (prop.major != 10 || prop.minor != 3) return KVX_ERR_UNSUPPORTED;
       void *ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_static_rope) != cudaSuccess || !ptr) return KVX_ERR_CUDA;
       g_static_ptr[dev] = static_cast<float2 *>(ptr);
+      g_static_ctx[dev] = current_context_id();   // the lookup made the context current
     }
   }
   if (a->ntok == 0) return KVX_OK;

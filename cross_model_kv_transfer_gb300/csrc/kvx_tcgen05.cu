@@ -6,31 +6,39 @@
 // features of the selected source layers) is a dense contraction per
 // (target layer lt, head h, K|V):  Y[T x d] = X[T x k*d] . W[k*d x d] + b.
 // It runs as tcgen05.mma (kind::f16, bf16 operands, fp32 accumulation in
-// tensor memory), M = 128 tokens, N = d = 128, K = 16 per instruction.
+// tensor memory), M = 128 tokens per CTA (256 per CTA pair), N = d = 128,
+// K = 16 per instruction.
 //
-// Data path of one CTA (persistent, one per SM), per work item
-// (h, lt, K|V, chunk of tiles_per_item 128-token tiles):
-//   * W producer warp: copies the item's bf16 W image (prepared by
-//     w_image_kernel, 2k chunks of 16 KB in the UMMA 128-byte-swizzled
-//     K-major layout) into shared memory with cp.async.bulk; W stays resident
-//     for all tiles of the item and is the only MMA operand read from shared
-//     memory.
-//   * X loader warp: TMA (cp.async.bulk.tensor, 4-D map over [Ls][T][H][d],
-//     128-byte swizzle) brings the 128 rows x d of one selected source layer
-//     for one tile into a ring of shared-memory stages, two boxes of 64 dims.
-//   * 16 transform warps: every thread owns one token row and a quarter of
-//     the RoPE pairs.  It reads its row from the stage (16-byte shared loads,
-//     conflict-free thanks to the swizzle), un-rotates keys out of the source
-//     RoPE in fp32 (step 1, "strip source RoPE"), packs bf16 and writes the
-//     row with tcgen05.st into tensor memory, which is operand A.  Values are
-//     copied as stored.  Four slots of 64 tensor-memory columns form a ring.
-//   * MMA warp (one thread): 8 tcgen05.mma per selection, A from tensor
-//     memory, B = W from shared memory, accumulating into one of two
-//     128-column fp32 accumulators; tcgen05.commit frees A slots, W chunks and
-//     hands finished accumulators to the epilogue.
-//   * 4 epilogue warps: tcgen05.ld the accumulator row, add b, re-rotate keys
-//     into the target RoPE at p' (step 3), cast to bf16 and store the row to
-//     the contiguous or paged target cache.
+// Data path of one CTA (persistent, one per SM; by default CTA pairs share
+// each M = 256 MMA), per work item (h, lt, K|V, chunk of 128-token tiles):
+//   * W producer (one thread): copies the item's bf16 W image (prepared by
+//     w_image_kernel: 2k chunks of 16 KB in the UMMA 128-byte-swizzled
+//     K-major layout, output channels in the epilogue's column order) into
+//     shared memory with cp.async.bulk; W stays resident for all tiles of
+//     the item and is the MMA's B operand.
+//   * X loader (one thread): TMA (cp.async.bulk.tensor, 4-D map over
+//     [Ls][T][H][d], 128-byte swizzle) brings the 128 rows x d of one
+//     selected source layer for one tile into a ring of shared-memory stages,
+//     two boxes of 64 dims; for key tiles of one request it also stages the
+//     source-RoPE cos/sin couples of the tile's positions.
+//   * 8 transform warps (two per tensor-memory lane quadrant): every thread
+//     owns one token row and half of the RoPE pairs.  It reads its row from
+//     the stage (16-byte shared loads, conflict-free thanks to the swizzle),
+//     un-rotates keys out of the source RoPE (step 1, "strip source RoPE")
+//     with bf16x2 FMAs, and writes the row with tcgen05.st into tensor
+//     memory, operand A (a ring of four 64-column slots).  Values are copied
+//     as stored.
+//   * MMA warp: 8 tcgen05.mma per selection (one elected lane issues), A from
+//     tensor memory, B = W from shared memory, into one of two 128-column
+//     fp32 accumulators; tcgen05.commit frees A slots and W chunks and hands
+//     finished accumulators to the epilogue.
+//   * 8 epilogue warps (two per lane quadrant, 16 rows each): tcgen05.ld of
+//     the 16x256b shape gives each thread two rows and, thanks to the W
+//     image's column order, 16 whole RoPE pairs (channels 16q..16q+15 and
+//     their partners 64 + 16q.., q = lane % 4); the accumulator is released
+//     as soon as it is in registers.  Then + b, re-rotation of keys into the
+//     target RoPE at p' (step 3), bf16 cast, and 32-byte stores in which the
+//     four threads of a row write one whole 128-byte line.
 // Every mbarrier wait is bounded: after 2 s without progress the CTA sets
 // KVX_FLAG_TIMEOUT, all roles leave their loops, in-flight copies and MMAs
 // are drained (again with bounded waits) and tensor memory is freed.
@@ -60,12 +68,12 @@ constexpr int kStageBytes = 2 * kChunkBytes;  // one selection of one tile
 constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
 constexpr int kCplBytes = 16 * kTileM * 16;   // one tile's source-RoPE quads: [16][128 rows][16 B]
-constexpr int kTransformWarps = 16;
+constexpr int kTransformWarps = 8;
 constexpr int kEpilogueWarps = 8;
-constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 24
-constexpr int kProducerWarp = kMmaWarp + 1;                  // 25
-constexpr int kLoaderWarp = kProducerWarp + 1;               // 26
-constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 864
+constexpr int kMmaWarp = kTransformWarps + kEpilogueWarps;   // 16
+constexpr int kProducerWarp = kMmaWarp + 1;                  // 17
+constexpr int kLoaderWarp = kProducerWarp + 1;               // 18
+constexpr int kThreads = (kLoaderWarp + 1) * 32;             // 608
 constexpr uint64_t kWaitNs = 2000000000ull;                  // 2 s without progress
 constexpr uint64_t kStallTestWaitNs = 20000000ull;           // 20 ms (stall test hook)
 
@@ -119,6 +127,23 @@ struct RopeTurns {
   unsigned long long tgt[kHalf];
 };
 
+// Output channel held by accumulator column c of a per-head map.  The W
+// image puts channel chan_of_col(c) in B's row c, so that a 16x256b
+// tensor-memory load of the 64-column half H (thread t: columns 8i +
+// 2(t%4) + e, i < 8) hands thread q = t%4 the channels 32H + 8q + v (v =
+// 2i + e < 8) and their RoPE partners 64 + 32H + 8q + (v - 8) (v >= 8):
+// the four threads of a row hold 32 consecutive channels and their partners.
+__host__ __device__ constexpr int chan_of_col(int c) {
+  return ((((c & 63) >> 3) << 1) | (c & 1)) < 8
+             ? 32 * (c >> 6) + 8 * ((c >> 1) & 3) + ((((c & 63) >> 3) << 1) | (c & 1))
+             : 64 + 32 * (c >> 6) + 8 * ((c >> 1) & 3) + ((((c & 63) >> 3) << 1) | (c & 1)) - 8;
+}
+
+// Padded shared-memory slots of the target-RoPE frequencies: the epilogue's
+// four q groups read their runs of 8 from distinct banks.
+__device__ __forceinline__ int pad_turn(int i) { return i + 2 * (i >> 4); }
+constexpr int kTurnSlots = kHalf + 2 * 4;     // 64-bit entries
+
 
 // bf16x2 helpers: un-rotation of two RoPE pairs at once in bf16x2 FMA
 // arithmetic.  a = (x_i, x_{i+1}) of the first half, b = (x_{i+d/2},
@@ -151,6 +176,7 @@ struct Shared {
   uint32_t tmem_base;
   volatile int c_mode;        // 1: the quads of positions p0 .. p0 + 127 are staged; 2: use global
   volatile int abort;
+  __align__(16) unsigned long long turns[kTurnSlots];   // target-RoPE frequencies (padded)
 };
 
 struct Waiter {
@@ -194,17 +220,17 @@ struct ItemGeom {
 };
 
 // Source-RoPE couples of row `row_in_tile` of a tile starting at packed row
-// `row0`, for pairs [16 tq, 16 tq + 16): couple q holds (cos, cos) and (sin,
-// sin) in bf16x2 for pairs 16 tq + 2q and +1, read from the position-major
+// `row0`, for pairs [32 th, 32 th + 32): couple u holds (cos, cos) and (sin,
+// sin) in bf16x2 for pairs 32 th + 2u and +1, read from the position-major
 // quad table (a warp's 32 consecutive rows read contiguous memory).  Rows
 // outside the transfer or with an invalid position get the identity rotation.
 __device__ __forceinline__ void load_couples(const KvxParams &p, const uint4 *__restrict__ rope_src4,
-                                             int64_t row0, int row_in_tile, int tq,
-                                             uint32_t (&c2)[8], uint32_t (&s2)[8]) {
+                                             int64_t row0, int row_in_tile, int th,
+                                             uint32_t (&c2)[16], uint32_t (&s2)[16]) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    c2[q] = 0x3F803F80u;   // (1, 1)
-    s2[q] = 0u;
+  for (int u = 0; u < 16; ++u) {
+    c2[u] = 0x3F803F80u;   // (1, 1)
+    s2[u] = 0u;
   }
   const int64_t g = row0 + row_in_tile;
   int32_t ps = 0, pt = 0;
@@ -212,8 +238,8 @@ __device__ __forceinline__ void load_couples(const KvxParams &p, const uint4 *__
   if (g < p.ntok) kvx::token_meta(p, g, ps, pt, row);
   if (row < 0) return;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 v = __ldg(rope_src4 + (int64_t)(4 * tq + i) * p.max_position + ps);
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = __ldg(rope_src4 + (int64_t)(8 * th + i) * p.max_position + ps);
     c2[2 * i] = v.x;
     s2[2 * i] = v.y;
     c2[2 * i + 1] = v.z;
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < geo.stages; ++s) {
       mbar_init(smem_addr(&sh->x_full[s]), 1);
-      mbar_init(smem_addr(&sh->x_empty[s]), kTransformWarps * 32);
+      mbar_init(smem_addr(&sh->x_empty[s]), kTransformWarps);
     }
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_addr(&sh->a_full[s]), kTransformWarps * P);
@@ -300,10 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_addr(&sh->drain), 1);
     mbar_init(smem_addr(&sh->c_full), 1);
-    mbar_init(smem_addr(&sh->c_empty), kTransformWarps * 32);
+    mbar_init(smem_addr(&sh->c_empty), kTransformWarps);
     sh->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // the target-RoPE frequencies for the epilogue (visible after the barrier
+  // inside seqlens_ok below)
+  if (tid < kHalf) sh->turns[pad_turn(tid)] = rope.tgt[tid];
   if (warp == kMmaWarp) {
     // CTA pair: one warp in each CTA allocates collectively (same columns)
     if constexpr (P == 1) {
@@ -337,14 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // transform warps: X rows -> tensor memory (operand A)
     // ------------------------------------------------------------------
     const int quad = warp & 3;                // TMEM lane quadrant
-    const int tq = warp >> 2;                 // RoPE pair quarter: pairs [16 tq, 16 tq + 16)
+    const int th = warp >> 2;                 // RoPE pair half: pairs [32 th, 32 th + 32)
     const int row_in_tile = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     uint32_t a_seq = 0;
     int x_stage = 0;                          // X ring position, tracked incrementally
     uint32_t x_par = 0;
     uint32_t c_par = 0;                       // staged-quads phase (K tiles, CTA pairs)
-    const int sw = row_in_tile & 7;           // 128-byte swizzle phase of this row
+    // byte offsets in a swizzled 128-byte row of the thread's four 16-byte
+    // chunks (dims 32 th .. 32 th + 31 of each 64-dim box)
+    uint32_t choff[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) choff[q] = (uint32_t)(((4 * th + q) ^ (row_in_tile & 7)) * 16);
     // The tiles of one item; keys (un-rotated out of the source RoPE) and
     // values (copied as stored) are compiled as separate loops.  Returns
     // false when the pipeline is being abandoned.
@@ -352,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr bool kKey = decltype(key_c)::value;
       for (int tile = t_beg; tile < t_end; ++tile) {
         // bf16x2 cos/sin couples of the source RoPE at this row's position
-        // for the thread's 16 pairs (couple q = pairs 16 tq + 2q, +1)
-        uint32_t c2[8], s2[8];
+        // for the thread's 32 pairs (couple u = pairs 32 th + 2u, +1)
+        uint32_t c2[16], s2[16];
         if constexpr (kKey) {
           bool from_global = true;
           if constexpr (kStageCpl) {
@@ -364,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sh->c_mode == 1) {
               from_global = false;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
+              for (int i = 0; i < 8; ++i) {
                 const uint4 v = *reinterpret_cast<const uint4 *>(
-                    cbuf + (4 * tq + i) * (kTileM * 16) + row_in_tile * 16);
+                    cbuf + (8 * th + i) * (kTileM * 16) + row_in_tile * 16);
                 c2[2 * i] = v.x;
                 s2[2 * i] = v.y;
                 c2[2 * i + 1] = v.z;
@@ -375,21 +408,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (from_global)
-            load_couples(p, rope_src4, (int64_t)tile * tile_rows + rank * kTileM, row_in_tile, tq,
+            load_couples(p, rope_src4, (int64_t)tile * tile_rows + rank * kTileM, row_in_tile, th,
                          c2, s2);
         }
         for (int j = 0; j < p.k; ++j) {
           const int stage = x_stage;
           if (!W.wait(&sh->x_full[stage], x_par)) return false;
-          // this row's dims [16 tq, 16 tq + 16) (box 0) and [64 + 16 tq, ...)
-          // (box 1): logical 16-byte chunks 2 tq, 2 tq + 1 of a 128-byte row
+          // this row's dims [32 th, 32 th + 32) (box 0) and [64 + 32 th, ...)
+          // (box 1)
           const unsigned char *rb = xbuf + stage * kStageBytes + row_in_tile * 128;
-          uint32_t plo[8], phi[8];
+          uint32_t plo[16], phi[16];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int pc = ((2 * tq + q) ^ sw) * 16;
-            const uint4 lo = *reinterpret_cast<const uint4 *>(rb + pc);
-            const uint4 hi = *reinterpret_cast<const uint4 *>(rb + kChunkBytes + pc);
+          for (int q = 0; q < 4; ++q) {
+            const uint4 lo = *reinterpret_cast<const uint4 *>(rb + choff[q]);
+            const uint4 hi = *reinterpret_cast<const uint4 *>(rb + kChunkBytes + choff[q]);
             plo[4 * q] = lo.x; plo[4 * q + 1] = lo.y; plo[4 * q + 2] = lo.z; plo[4 * q + 3] = lo.w;
             phi[4 * q] = hi.x; phi[4 * q + 1] = hi.y; phi[4 * q + 2] = hi.z; phi[4 * q + 3] = hi.w;
           }
@@ -400,30 +432,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = a_seq % kSlots;
           const uint32_t round = a_seq / kSlots;
           if constexpr (kKey) {
-            // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 16 tq + 2q (+1)
+            // un-rotate: (x0 + j x1) * exp(-j p w_i), pairs i = 32 th + 2u (+1)
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              unrotate2(plo[q], phi[q], c2[q], s2[q], s2[q] ^ 0x80008000u, plo[q], phi[q]);
+            for (int u = 0; u < 16; ++u)
+              unrotate2(plo[u], phi[u], c2[u], s2[u], s2[u] ^ 0x80008000u, plo[u], phi[u]);
           }
           if (!W.wait(&sh->a_empty[slot], (round & 1) ^ 1)) return false;
           tc_fence_after();
           {
-            const uint32_t col = (uint32_t)(slot * kSlotCols + 8 * tq);
-            tc_st8(tmem + lane_base + col, plo);
-            tc_st8(tmem + lane_base + col + 32, phi);
+            // A column slot * 64 + f / 2 holds features (f, f + 1)
+            const uint32_t col = (uint32_t)(slot * kSlotCols + 16 * th);
+            tc_st16(tmem + lane_base + col, plo);
+            tc_st16(tmem + lane_base + col + 32, phi);
           }
           tc_wait_st();
           // release the X stage only now: its words went through registers
-          // into tensor memory (wait::st returned), so every read of the
-          // stage is complete before the loader's next TMA write lands there
-          mbar_arrive(smem_addr(&sh->x_empty[stage]));
-          // likewise the staged quads, consumed by the first selection
-          if (kKey && kStageCpl && j == 0) mbar_arrive(smem_addr(&sh->c_empty));
+          // into tensor memory (wait::st returned for the whole warp), so
+          // every read of the stage is complete before the loader's next TMA
+          // write lands there
           tc_fence_before();
           __syncwarp();
-          if (lane == 0 && !stall_test) {
-            if (P == 1 || rank == 0) mbar_arrive(smem_addr(&sh->a_full[slot]));
-            else mbar_arrive_cluster(smem_addr(&sh->a_full[slot]), 0);
+          if (lane == 0) {
+            mbar_arrive(smem_addr(&sh->x_empty[stage]));
+            // likewise the staged quads, consumed by the first selection
+            if (kKey && kStageCpl && j == 0) mbar_arrive(smem_addr(&sh->c_empty));
+            if (!stall_test) {
+              if (P == 1 || rank == 0) mbar_arrive(smem_addr(&sh->a_full[slot]));
+              else mbar_arrive_cluster(smem_addr(&sh->a_full[slot]), 0);
+            }
           }
           ++a_seq;
         }
@@ -444,10 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------
     // epilogue warps: accumulator -> + b -> re-rotate (K) -> bf16 -> cache
     // ------------------------------------------------------------------
+    const int ew = warp - kTransformWarps;
     const int quad = warp & 3;
-    const int eh = (warp - kTransformWarps) >> 2;   // pairs [32 eh, 32 eh + 32)
-    const int row_in_tile = quad * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int eh = ew >> 2;                          // rows 32 quad + 16 eh .. + 16
+    const int q = lane & 3;                          // channels 16q.. and 64 + 16q..
+    const uint32_t lane_base = (uint32_t)(quad * 32 + 16 * eh) << 16;
+    const int meta_row = quad * 32 + 16 * eh + (lane & 15);   // resolved by lanes 0..15
     uint32_t d_seq = 0;
     // The tiles of one item (keys re-rotated into the target RoPE, values
     // not), compiled as separate loops.  Returns false when the pipeline is
@@ -455,71 +493,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tiles = [&](auto key_c, int lt, int h, int t_beg, int t_end, bool layer_ok,
                      bool reporter) -> bool {
       constexpr bool kKey = decltype(key_c)::value;
+      // the item's bias (fp32 image, natural channel order; L1-resident)
       const float2 *bias2 = reinterpret_cast<const float2 *>(
           bias_f32 + (((int64_t)lt * p.H + h) * 2 + (kKey ? 0 : 1)) * kD);
       __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(kKey ? p.dst_k : p.dst_v);
       for (int tile = t_beg; tile < t_end; ++tile) {
-        const int64_t g = (int64_t)tile * tile_rows + rank * kTileM + row_in_tile;
-        int32_t ps = 0, pt = 0;
-        int64_t row = -1;
+        // lanes 0..15 resolve the positions and cache rows of the warp's 16
+        // rows; every thread then takes its rows t/4 and t/4 + 8
+        int32_t pt_l = 0;
+        long long row_l = -1;
         uint32_t bad = 0;
-        if (g < p.ntok) bad = kvx::token_meta(p, g, ps, pt, row);
-        if (kKey && reporter && eh == 0) {
+        if (lane < 16) {
+          const int64_t g = (int64_t)tile * tile_rows + rank * kTileM + meta_row;
+          int32_t ps = 0, pt = 0;
+          int64_t row = -1;
+          if (g < p.ntok) bad = kvx::token_meta(p, g, ps, pt, row);
+          pt_l = pt;
+          row_l = row;
+        }
+        if (kKey && reporter) {
           const uint32_t any = __reduce_or_sync(0xffffffffu, bad);
           if (lane == 0) kvx::report(p, any);
         }
         if (!layer_ok) continue;
+        const int32_t pt0 = __shfl_sync(0xffffffffu, pt_l, lane >> 2);
+        const int32_t pt1 = __shfl_sync(0xffffffffu, pt_l, (lane >> 2) + 8);
+        const long long row0 = __shfl_sync(0xffffffffu, row_l, lane >> 2);
+        const long long row1 = __shfl_sync(0xffffffffu, row_l, (lane >> 2) + 8);
         const int buf = d_seq & 1;
         if (!W.wait(&sh->d_full[buf], (d_seq >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t dcol = tmem + lane_base + (uint32_t)(kDCol + buf * kD);
-        __nv_bfloat16 *orow =
-            dst + (((int64_t)lt * p.dst_rows + (row < 0 ? 0 : row)) * p.H + h) * kD;
-#pragma unroll 1
-        for (int pp = 0; pp < 2; ++pp) {
-          // two 8-pair chunks (pc0, pc0 + 1) make one 32-byte sector of the
-          // row's first half and one of its second half
-          const int pc0 = 4 * eh + 2 * pp;
-          uint32_t olo[8], ohi[8];
+        __nv_bfloat16 *o0 = row0 >= 0 ? dst + (((int64_t)lt * p.dst_rows + row0) * p.H + h) * kD
+                                      : nullptr;
+        __nv_bfloat16 *o1 = row1 >= 0 ? dst + (((int64_t)lt * p.dst_rows + row1) * p.H + h) * kD
+                                      : nullptr;
+        // register 4i + 2rs + e of half H holds (row rs, channel 32H + 8q +
+        // 2i + e) for i < 4 and its RoPE partner (+64) for i = 4..7; the two
+        // 64-column halves are loaded, processed and stored one after the other
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int pc = pc0 + c;
-            uint32_t vlo[8], vhi[8];
-            tc_ld8(dcol + 8 * pc, vlo);
-            tc_ld8(dcol + kHalf + 8 * pc, vhi);
-            tc_wait_ld();
+        for (int H = 0; H < 2; ++H) {
+          uint32_t v[32];
+          tc_ld16x256_x8(dcol + 64 * H, v);
+          tc_wait_ld();
+          if (H == 1) {
+            // the accumulator is in registers: hand it back to the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if (P == 1 || rank == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
+              else mbar_arrive_cluster(smem_addr(&sh->d_empty[buf]), 0);
+            }
+          }
+          uint32_t olo[2][4], ohi[2][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              // b (fp32 image) at columns 8 pc + 2e, +1 and 64 + 8 pc + 2e, +1
-              const float2 bl = __ldg(bias2 + 4 * pc + e), bh = __ldg(bias2 + 32 + 4 * pc + e);
-              float2 y0 = __fadd2_rn(make_float2(__uint_as_float(vlo[2 * e]), __uint_as_float(vlo[2 * e + 1])), bl);
-              float2 y1 = __fadd2_rn(make_float2(__uint_as_float(vhi[2 * e]), __uint_as_float(vhi[2 * e + 1])), bh);
+          for (int i = 0; i < 4; ++i) {
+            const int n = 32 * H + 8 * q + 2 * i;    // channels n, n + 1 and n + 64, n + 65
+            const float2 bl = __ldg(bias2 + (n >> 1));
+            const float2 bh = __ldg(bias2 + ((64 + n) >> 1));
+            float c0 = 1.f, s0 = 0.f, c1 = 1.f, s1 = 0.f, c2 = 1.f, s2 = 0.f, c3 = 1.f, s3 = 0.f;
+            if constexpr (kKey) {
+              const ulonglong2 f = *reinterpret_cast<const ulonglong2 *>(sh->turns + pad_turn(n));
+              rope_cs((uint32_t)pt0, f.x, c0, s0);
+              rope_cs((uint32_t)pt0, f.y, c1, s1);
+              rope_cs((uint32_t)pt1, f.x, c2, s2);
+              rope_cs((uint32_t)pt1, f.y, c3, s3);
+            }
+#pragma unroll
+            for (int rs = 0; rs < 2; ++rs) {
+              float2 y0 = __fadd2_rn(make_float2(__uint_as_float(v[4 * i + 2 * rs]),
+                                                 __uint_as_float(v[4 * i + 2 * rs + 1])), bl);
+              float2 y1 = __fadd2_rn(make_float2(__uint_as_float(v[4 * (i + 4) + 2 * rs]),
+                                                 __uint_as_float(v[4 * (i + 4) + 2 * rs + 1])), bh);
               if constexpr (kKey) {
-                // (y0 + j y1) exp(+j p' w_i) for pairs i = 8 pc + 2e, +1
-                float c0, s0, c1, s1;
-                rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e], c0, s0);
-                rope_cs((uint32_t)pt, rope.tgt[8 * pc + 2 * e + 1], c1, s1);
-                const float2 cc = make_float2(c0, c1), ss = make_float2(s0, s1);
-                const float2 nss = make_float2(-s0, -s1);
+                // (y0 + j y1) exp(+j p' w_i), pairs i = n, n + 1
+                const float2 cc = rs ? make_float2(c2, c3) : make_float2(c0, c1);
+                const float2 ss = rs ? make_float2(s2, s3) : make_float2(s0, s1);
+                const float2 nss = make_float2(-ss.x, -ss.y);
                 const float2 r0 = __ffma2_rn(y0, cc, __fmul2_rn(y1, nss));
                 const float2 r1 = __ffma2_rn(y0, ss, __fmul2_rn(y1, cc));
                 y0 = r0;
                 y1 = r1;
               }
-              olo[4 * c + e] = pack_bf16(y0.x, y0.y);
-              ohi[4 * c + e] = pack_bf16(y1.x, y1.y);
+              olo[rs][i] = pack_bf16(y0.x, y0.y);
+              ohi[rs][i] = pack_bf16(y1.x, y1.y);
             }
           }
-          if (row >= 0) {
-            st_global_v8(orow + 8 * pc0, olo);
-            st_global_v8(orow + kHalf + 8 * pc0, ohi);
+          // the four threads of a row write 64 consecutive bytes of each half
+          const int c0 = 32 * H + 8 * q;
+          if (o0) {
+            st_global_v4(o0 + c0, olo[0]);
+            st_global_v4(o0 + kHalf + c0, ohi[0]);
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (P == 1 || rank == 0) mbar_arrive(smem_addr(&sh->d_empty[buf]));
-          else mbar_arrive_cluster(smem_addr(&sh->d_empty[buf]), 0);
+          if (o1) {
+            st_global_v4(o1 + c0, olo[1]);
+            st_global_v4(o1 + kHalf + c0, ohi[1]);
+          }
         }
         ++d_seq;
       }
@@ -726,7 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // W ([Lt][H][2][k*d][d]) -> bf16 image, per (lt, h, m) 2k chunks of
 // [128 rows n][64 k] in the 128-byte-swizzled K-major layout the MMA reads:
-// byte (n, kk) of a chunk = n*128 + ((kk/8) ^ (n%8))*16 + (kk%8)*2.
+// byte (n, kk) of a chunk = n*128 + ((kk/8) ^ (n%8))*16 + (kk%8)*2; row n
+// holds output channel chan_of_col(n) (the epilogue's column order).
 // One CTA converts one chunk through a shared-memory transpose; the first
 // chunk's CTA also writes b of its (lt, h, m) as fp32 (the epilogue's bias).
 // ---------------------------------------------------------------------------
@@ -750,10 +820,11 @@ __global__ void __launch_bounds__(256) w_image_kernel(const WT *__restrict__ w,
   uint4 *out = img + (lhm * nchunk + c) * (kChunkBytes / 16);
   for (int q = threadIdx.x; q < kChunkBytes / 16; q += blockDim.x) {
     const int n = q >> 3, k8 = (q & 7) ^ (n & 7);
+    const int ch = chan_of_col(n);   // the epilogue's column order
     uint32_t v[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      v[e] = pack_bf16(tile[k8 * 8 + 2 * e][n], tile[k8 * 8 + 2 * e + 1][n]);
+      v[e] = pack_bf16(tile[k8 * 8 + 2 * e][ch], tile[k8 * 8 + 2 * e + 1][ch]);
     out[q] = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }

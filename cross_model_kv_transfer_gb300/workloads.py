@@ -1,9 +1,11 @@
 """Seeded synthetic inputs for the cross-model KV-cache transfer.
 
 This module draws random inputs and nothing else: it holds none of the
-transfer's arithmetic (no RoPE at a position, no map, no cache routing).  The
-CUDA library and the fp64 oracle both consume what it returns; neither is
-imported here.
+transfer's arithmetic (no un-rotation, no map, no re-rotation, no cache
+routing).  The one rotation here is the pilot model's own RoPE, applied once
+when the synthetic pilot cache is drawn, as a real pilot cache stores its
+keys.  The CUDA library and the fp64 oracle both consume what it returns;
+neither is imported here.
 
 Workloads (shapes of the pairs the pages measure; no model weights or
 datasets are used -- every tensor is synthetic):
@@ -27,12 +29,13 @@ Value recipe:
 * content vectors: N(0, 1) times a per-(layer, head, channel) log-normal
   (sigma = 1) scale; in the bf16 workloads 4 channels per (layer, head) are
   further scaled x10 (outliers).
-* keys are stored as RoPE-rotated content.  A rotated half-split pair is the
-  content pair turned by some angle, so the stored pair (i, i + d/2) is drawn
-  as the content pair turned by a seeded uniform angle.  Both the kernel and
-  the oracle un-rotate exactly the stored bytes, so parity does not depend on
-  which angle was used; the draw only gives the stored keys the magnitudes
-  and pair mixing of real rotated keys.
+* keys are stored as the pilot model would have cached them: the drawn
+  content turned by its RoPE at the token's source position p (0 .. len - 1
+  within its request), half-split pairs (i, i + d/2) turned by the angle
+  p * theta_src^(-2i/d), the angle formed and its cosine and sine taken in
+  fp64.  This is part of synthesising a pilot cache, like the value
+  distribution; the CUDA library and the oracle each un-rotate the stored
+  bytes with their own code and share nothing with this module.
 * values are stored as drawn.
 * W ~ N(0, 1/(k d)) stored fp32; b ~ N(0, 0.01^2) stored fp32 (tiny) or bf16.
 * the layer-index table draws, for each target layer, k distinct source
@@ -203,6 +206,13 @@ def make_inputs(wl: Workload, device="cpu", seed: Optional[int] = None) -> dict:
 
     src_k = torch.empty((Ls, T, H, d), dtype=wl.kv_dtype, device=dev)
     src_v = torch.empty((Ls, T, H, d), dtype=wl.kv_dtype, device=dev)
+    # the pilot's RoPE at each token's source position, angles in fp64
+    pos = torch.cat([torch.arange(n, dtype=torch.float64) for n in wl.seqlens]).to(dev)
+    freq = wl.theta_src ** (-2.0 * torch.arange(half, dtype=torch.float64) / d)
+    phi = pos[:, None] * freq.to(dev)[None, :]                       # [T][half]
+    cos_p = torch.cos(phi).to(torch.float32)[:, None, :]
+    sin_p = torch.sin(phi).to(torch.float32)[:, None, :]
+    del phi
     for s in range(Ls):
         for dst, is_key in ((src_k, True), (src_v, False)):
             scale = torch.exp(torch.randn((1, H, d), generator=g, device=dev))
@@ -212,10 +222,8 @@ def make_inputs(wl: Workload, device="cpu", seed: Optional[int] = None) -> dict:
                     scale[0, h, ch] *= 10.0
             x = torch.randn((T, H, d), generator=g, device=dev) * scale
             if is_key:
-                phi = torch.rand((T, H, half), generator=g, device=dev) * (2.0 * math.pi)
-                c, sn = torch.cos(phi), torch.sin(phi)
                 x0, x1 = x[..., :half], x[..., half:]
-                x = torch.cat((x0 * c - x1 * sn, x0 * sn + x1 * c), dim=-1)
+                x = torch.cat((x0 * cos_p - x1 * sin_p, x0 * sin_p + x1 * cos_p), dim=-1)
             dst[s].copy_(x.to(wl.kv_dtype))
             del x
 

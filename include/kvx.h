@@ -179,7 +179,8 @@ typedef struct {
                                  token g of request r at source position p at
                                  row src_block_table[r][p/src_bs]*src_bs +
                                  p % src_bs (the pilot's paged cache)        */
-  const void *src_v;          /* source values, same layout as src_k          */
+  const void *src_v;          /* source values, same layout as src_k; src_k
+                                 and src_v may be NULL when ntok == 0        */
   int64_t ntok;               /* >= 0 (0: nothing to do)                      */
   int32_t num_requests;       /* R >= 1                                       */
   const int32_t *cu_seqlens;  /* [R+1] request r owns source rows
@@ -388,7 +389,9 @@ kvx_status kvx_ridge_fit(const kvx_ridge_args *args, void *stream);
  * All calls share the array: calls whose work overlaps on the GPU (two
  * streams, for instance) race on it and must be ordered by the caller.  The
  * first call on a device looks up the array's device address (once per
- * device, under a lock); make that first call before any stream capture.
+ * device and CUDA context, under a lock; a call after cudaDeviceReset looks
+ * it up again in the new context); make that first call before any stream
+ * capture.
  * Other errors as for kvx_transfer; `stream` as for kvx_transfer. */
 kvx_status kvx_transfer_static(const kvx_plan_desc *desc, const kvx_transfer_args *args,
                                void *stream);

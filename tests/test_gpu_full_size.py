@@ -1,12 +1,19 @@
 """Parity at full workload sizes, in the launch configuration the benchmark
-times: the whole transfer runs on the GPU, and sampled output rows are
-recomputed one by one by the fp64 oracle (``oracle.map_token`` / ``dst_row``).
-Covers the 14B -> 32B shape at 32,768 tokens, the 8B -> 70B batched paged
-recipe, and the 0.6B -> 1.7B pair at 2,048 and 8,192 tokens with the target
-shifted by +37 (the 512-token pair is compared in full in
-test_gpu_parity.py).
-Every row outside the transfer must keep its sentinel bits (checked on the
-device for the whole cache)."""
+times: the whole transfer runs on the GPU, and the fp64 oracle recomputes a
+stratified set of tokens for every (target layer, head, K|V) map.  Each map
+must be within the plain tolerance (relative Frobenius error over the chosen
+tokens, 1e-2 for bf16 caches with fp32 accumulation) -- no per-row slack.
+
+* 0.6B -> 1.7B pair at 2,048 and 8,192 tokens, target shifted by +37: every
+  token (the 512-token pair is compared in full in test_gpu_parity.py).
+* 14B -> 32B shape at 32,768 tokens and the 8B -> 70B batched paged recipe:
+  windows of consecutive tokens (256 and 128) at the start and end of every
+  request, on both sides of every 8,192-token boundary of the packed batch
+  (the kernel's work items cover multiples of 256 packed rows), at the
+  batch's end, and at seeded random places.
+Every row outside the transfer must keep its sentinel bits and every row
+inside it must have been written (checked on the device for the whole
+cache).  The worst map error is printed."""
 import numpy as np
 import pytest
 import torch
@@ -14,25 +21,27 @@ import torch
 import oracle
 from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs
 
-from parity import TOL, run_gpu
+from parity import assert_token_parity, dst_rows_of, oracle_tokens, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-SAMPLES = 48
 
-
-def _sample_rows(wl, inp, seed):
+def stratified_tokens(wl, inp, seed, window, boundary=8192, random_windows=4):
+    """Packed tokens: windows of ``window`` tokens at both ends of every
+    request, on both sides of every multiple of ``boundary``, at the batch's
+    end, and ``random_windows`` seeded random windows."""
+    cu = inp["cu_seqlens"].cpu().numpy().astype(np.int64)
+    n = wl.ntok
+    starts = []
+    for r in range(wl.num_requests):
+        starts += [cu[r], cu[r + 1] - window]
+    starts += [b - window for b in range(boundary, n, boundary)]
+    starts += list(range(boundary, n, boundary))
+    starts += [n - window]
     g = np.random.default_rng(seed)
-    cu = inp["cu_seqlens"].cpu().numpy()
-    offs = inp["tgt_offset"].cpu().numpy()
-    out = []
-    for _ in range(SAMPLES):
-        r = int(g.integers(wl.num_requests))
-        n = int(cu[r + 1] - cu[r])
-        pos = int(g.choice([0, n - 1, int(g.integers(n))]))
-        out.append((r, int(cu[r]) + pos, pos, pos + int(offs[r]),
-                    int(g.integers(wl.tgt_layers)), int(g.integers(wl.kv_heads))))
-    return out
+    starts += list(g.integers(0, max(1, n - window), random_windows))
+    toks = np.concatenate([np.arange(max(0, s), min(n, s + window)) for s in starts])
+    return np.unique(toks)
 
 
 def _written_mask(wl, inp):
@@ -50,45 +59,39 @@ def _written_mask(wl, inp):
     return rows
 
 
-@pytest.mark.parametrize("name", ["qwen3_14b_32b", "llama31_8b_70b_paged",
-                                  "qwen3_0p6b_1p7b_off37_2k", "qwen3_0p6b_1p7b_off37_8k"])
-def test_full_size_sampled_rows_match_oracle(name):
+def check_sentinels(wl, inp, gk, gv):
+    written = _written_mask(wl, inp)
+    for dst in (gk, gv):
+        bits = dst.view(torch.int16)
+        assert bool((bits[:, ~written] == -1).all()), "rows outside the transfer were written"
+        assert not bool((bits[:, written] == -1).all(dim=-1).any()), "a row was not written"
+
+
+@pytest.mark.parametrize("name", ["qwen3_0p6b_1p7b_off37_2k", "qwen3_0p6b_1p7b_off37_8k"])
+def test_full_size_every_token_matches_oracle(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl, "cuda")
     gk, gv, st, plan = run_gpu(wl, inp)
     assert st == 0
-    f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
-    num = {0: 0.0, 1: 0.0}
-    den = {0: 0.0, 1: 0.0}
-    table = inp["block_table"].cpu().numpy() if wl.layout == PAGED else None
-    for r, gtok, p, pt, lt, h in _sample_rows(wl, inp, 17):
-        idx = inp["layer_idx"][lt].long()
-        krows = f64(inp["src_k"][idx, gtok, h])
-        vrows = f64(inp["src_v"][idx, gtok, h])
-        w = f64(inp["w"][lt, h])
-        b = f64(inp["b"][lt, h])
-        ok, ov = oracle.map_token(krows, vrows, w[0], w[1], b[0], b[1], p, pt,
-                                  wl.theta_src, wl.theta_tgt)
-        if wl.layout == PAGED:
-            row, bad = oracle.dst_row(oracle.PAGED, r, pt, block_size=wl.block_size,
-                                      num_blocks=wl.num_blocks, block_table=table,
-                                      max_blocks_per_req=table.shape[1])
-        else:
-            row, bad = oracle.dst_row(oracle.CONTIGUOUS, r, pt, dst_capacity=wl.dst_capacity)
-        assert bad == 0
-        for m, (dst, ref) in enumerate(((gk, ok), (gv, ov))):
-            got = f64(dst[lt, row, h])
-            e = np.linalg.norm(got - ref)
-            assert e <= 3 * TOL[wl.kv_dtype] * np.linalg.norm(ref), (m, lt, h, gtok)
-            num[m] += e * e
-            den[m] += float(ref @ ref)
-    for m in (0, 1):
-        assert (num[m] / den[m]) ** 0.5 <= TOL[wl.kv_dtype]
-    written = _written_mask(wl, inp)
-    for dst in (gk, gv):
-        bits = dst.view(torch.int16)
-        assert bool((bits[:, ~written] == -1).all())
-        assert not bool((bits[:, written] == -1).all(dim=-1).any())
+    check_sentinels(wl, inp, gk, gv)
+    tokens = np.arange(wl.ntok)
+    ok, ov, toks = oracle_tokens(wl, inp, tokens)
+    worst = assert_token_parity(wl, gk, gv, ok, ov, dst_rows_of(wl, inp, toks))
+    print(f"{name}: kernel {plan.kernel}, every token, worst map {worst[0]:.3e} at {worst[1]}")
+
+
+@pytest.mark.parametrize("name,window", [("qwen3_14b_32b", 256), ("llama31_8b_70b_paged", 128)])
+def test_full_size_stratified_tokens_match_oracle(name, window):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, "cuda")
+    gk, gv, st, plan = run_gpu(wl, inp)
+    assert st == 0
+    check_sentinels(wl, inp, gk, gv)
+    tokens = stratified_tokens(wl, inp, seed=17, window=window)
+    ok, ov, toks = oracle_tokens(wl, inp, tokens)
+    worst = assert_token_parity(wl, gk, gv, ok, ov, dst_rows_of(wl, inp, toks))
+    print(f"{name}: kernel {plan.kernel}, {len(toks)} tokens, worst map {worst[0]:.3e} "
+          f"at {worst[1]}")
 
 
 def test_full_size_diagnostics_match_oracle_on_first_and_last_layer():

@@ -299,6 +299,15 @@ def test_empty_transfer_enqueues_nothing(kernel):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert bool((dk.view(torch.int16) == -1).all()) and bool((dv.view(torch.int16) == -1).all())
+    # the same through the Python binding with zero-row source tensors (no
+    # storage: NULL data pointers)
+    empty = torch.empty((wl.src_layers, 0, wl.kv_heads, wl.head_dim), dtype=wl.kv_dtype,
+                        device="cuda")
+    plan.transfer(**gpu_args(wl, dict(inp, src_k=empty, src_v=empty.clone()), dk, dv, status,
+                             cu_seqlens=torch.zeros(2, dtype=torch.int32, device="cuda")))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert bool((dk.view(torch.int16) == -1).all()) and bool((dv.view(torch.int16) == -1).all())
 
 
 def test_empty_diagnostics_clear_the_statistics():

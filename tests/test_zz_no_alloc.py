@@ -1,14 +1,17 @@
 """The allocation-free entry point, kvx_transfer_static.
 
-It is meant for callers that may not allocate device memory (engines that
-reserve nearly all of the GPU for their own KV-cache pool and forbid later
-cudaMalloc calls, latency-critical paths that cannot accept the device
-synchronisation cudaMalloc/cudaFree may cause).  It runs the SIMT transfer
-kernel with its RoPE tables in a fixed device array compiled into the library
-instead of plan-owned memory.  Here its output is checked against the plan
-path (kvx_plan_create + kvx_transfer with the SIMT kernel) on the same
-inputs, for two calls in a row, within the tolerances of the other parity
-tests.  This file is collected last on purpose.
+It is meant for callers that may not allocate device memory: serving engines
+that reserve nearly all of the GPU for their own KV-cache pool and forbid
+later cudaMalloc calls, and latency-critical paths that cannot accept the
+device synchronisation cudaMalloc/cudaFree may cause.  It runs the SIMT
+transfer kernel with its RoPE tables in a fixed device array compiled into
+the library instead of plan-owned memory.  The tables are filled on the device
+(fp64 math, rounded once to fp32), a different source from the plan path's
+host-built tables, so each call is checked on its own against the fp64 oracle,
+per (target layer, head, K|V), for two calls in a row: on the tiny fp32
+workload and on a ragged paged batch whose target RoPE base differs from the
+source's (two tables in the array).  This file is collected last on purpose:
+if it fails, a run that stops at the first failure has run every other test.
 """
 import ctypes
 import dataclasses
@@ -19,7 +22,7 @@ import torch
 from cross_model_kv_transfer_gb300 import kvx
 from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_inputs, sentinel_like
 
-from parity import TOL, gpu_args, make_plan, run_gpu
+from parity import assert_parity, gpu_args, make_plan, run_oracle
 
 
 def _desc(**over):
@@ -45,6 +48,8 @@ def test_static_entry_point_refuses_tables_beyond_its_array():
 
 
 def _static_run(wl, inp, plan):
+    """One kvx_transfer_static call into sentinel-filled destinations (the
+    plan object only builds the descriptor and argument structures)."""
     shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
     dk = sentinel_like(shape, wl.kv_dtype, "cuda")
     dv = sentinel_like(shape, wl.kv_dtype, "cuda")
@@ -57,29 +62,19 @@ def _static_run(wl, inp, plan):
     return dk, dv, int(status.item())
 
 
-def _same(wl, a, b):
-    for x, y in zip(a, b):
-        bits = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
-        untouched = y.view(bits) == -1
-        assert torch.equal(x.view(bits)[untouched], y.view(bits)[untouched])
-        xf, yf = x.double()[~untouched], y.double()[~untouched]
-        err = (xf - yf).norm() / yf.norm()
-        assert err <= TOL[wl.kv_dtype], float(err)
-
-
 @pytest.mark.gpu
-def test_static_entry_point_matches_the_plan_path_on_two_calls():
+def test_static_entry_point_matches_the_oracle_on_two_calls():
     tiny = WORKLOADS["tiny_fp32"]
     paged = dataclasses.replace(
-        WORKLOADS["llama31_8b_70b_paged"].with_tokens([100, 37, 260], [5, 64, 0]), tgt_layers=6)
-    for wl, theta_tgt in ((tiny, None), (paged, 1e6)):
-        if theta_tgt is not None:
-            wl = dataclasses.replace(wl, theta_tgt=theta_tgt)   # two RoPE tables
+        WORKLOADS["llama31_8b_70b_paged"].with_tokens([100, 37, 260], [5, 64, 0]), tgt_layers=6,
+        theta_tgt=1e6)   # a target base unlike the source's: two tables in the array
+    for wl in (tiny, paged):
         inp = make_inputs(wl, "cuda")
-        plan = make_plan(wl, kvx.KVX_KERNEL_SIMT)
-        rk, rv, rst, _ = run_gpu(wl, inp, plan=plan)
+        rk, rv, rst = run_oracle(wl, inp)
         assert rst == 0
-        for _ in range(2):
+        plan = make_plan(wl, kvx.KVX_KERNEL_SIMT)
+        for call in range(2):
             sk, sv, sst = _static_run(wl, inp, plan)
-            assert sst == 0
-            _same(wl, (sk, sv), (rk, rv))
+            assert sst == 0, f"{wl.name} call {call}: device status {sst}"
+            err = assert_parity(wl, sk, sv, rk, rv)
+            print(f"{wl.name} static call {call}: worst rel Frobenius {err:.2e}")
