@@ -71,6 +71,24 @@ def test_roofline_picks_the_tighter_bound():
     assert r["bound"] == "hbm" and r["unit"] == "GB/s"
 
 
+def test_roofline_compares_a_power_capped_run_with_the_sustained_peak():
+    # the timed region ran under the power cap: the sustained cuBLAS figure
+    # (measured in the same regime) is the denominator; both fractions and
+    # the nominal one (SMs x 8192 flops/clk x sampled clock) are reported
+    wl = WORKLOADS["qwen3_14b_32b"]
+    idx = torch.stack([torch.arange(4) + i % 36 for i in range(64)]).to(torch.int32)
+    peaks = {"hbm_gbs": 6766.7, "bf16_tflops": 1908.0, "bf16_tflops_sustained": 1679.6}
+    capped = {"sm_mhz": 1740.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    r = bench.roofline(wl, idx, 4.398046511104, "tcgen05", peaks, "measured", clocks=capped)
+    assert r["peak"] == 1679.6 and r["frac"] == pytest.approx(1000.0 / 1679.6, rel=1e-6)
+    assert "sustained" in r["peak_source"]
+    assert r["frac_of_burst"] == pytest.approx(1000.0 / 1908.0, rel=1e-6)
+    assert r["nominal_peak"] == pytest.approx(152 * 8192 * 1740e6 / 1e12)
+    free = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    r = bench.roofline(wl, idx, 4.398046511104, "tcgen05", peaks, "measured", clocks=free)
+    assert r["peak"] == 1908.0 and "burst" in r["peak_source"]
+
+
 def test_published_context_number_is_the_32k_mapper_latency():
     # the Qwen3 article's 14B -> 32B mapper: 277.6 ms at 32,768 tokens
     assert bench.PUBLISHED_MS["qwen3_14b_32b"] == 277.6
