@@ -133,6 +133,7 @@ def test_tensor_core_plan_rejects_more_tokens_than_its_buffers():
     wl = dataclasses.replace(WORKLOADS["qwen3_0p6b_1p7b"].with_tokens([300], [0]), tgt_layers=2)
     inp, pk, pv, table = paged_inputs(wl, kvx.KVX_KERNEL_TCGEN05)
     plan = paged_plan(wl, kvx.KVX_KERNEL_TCGEN05, max_tokens=299)
+    assert plan.launches_per_transfer == 3     # pack, W image, transfer
     shape = (wl.tgt_layers, wl.dst_rows, wl.kv_heads, wl.head_dim)
     dk = torch.zeros(shape, dtype=wl.kv_dtype, device="cuda")
     dv = torch.zeros(shape, dtype=wl.kv_dtype, device="cuda")
