@@ -24,6 +24,10 @@ What each function computes, and the passages it follows, is documented in
                   on production limits); ``map_token_wide`` for one token.
 * ``ridge_fit``   centred ridge regression with intercept (the Qwen3
                   article's ridge demo).
+* ``layer_scores`` explained variance of each target (layer, head, K|V) by
+                  the ridge fit on one source layer, or on a set (the Qwen3
+                  article's linear-bridge section: layer choice by predictive
+                  power).
 * ``kv_diagnostics`` KV cosine ("Helm Intelligent Routing", "Reading the
                   retention score") and explained variance (the Qwen3
                   article's linear-structure analysis) of a mapped cache
@@ -133,6 +137,9 @@ def _load():
             lib.kvxo_map_token_wide.restype = None
             lib.kvxo_kv_diagnostics.argtypes = [ctypes.POINTER(_Problem), dp, dp, dp, dp, dp]
             lib.kvxo_kv_diagnostics.restype = ctypes.c_int
+            lib.kvxo_layer_scores.argtypes = [ctypes.POINTER(_Problem), dp, dp, ctypes.c_double,
+                                              dp, ctypes.c_void_p]
+            lib.kvxo_layer_scores.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -319,6 +326,33 @@ def kv_diagnostics(*, mapped_k, mapped_v, ref_k, ref_v, theta_tgt, max_position,
     st = _load().kvxo_kv_diagnostics(ctypes.byref(P), _dp(mk), _dp(mv), _dp(rk), _dp(rv),
                                      _dp(stats))
     return stats, int(st)
+
+
+def layer_scores(*, src_k, src_v, tgt_k, tgt_v, theta_src, theta_tgt, max_position,
+                 lam=0.01, cu_seqlens=None, src_pos=None, layer_idx=None):
+    """Layer-selection scores (``kvxo_layer_scores``): in-sample explained
+    variance of each target (layer, head, K|V) by the ridge fit on one source
+    layer, r2 [Lt][Ls][H][2], and, with ``layer_idx`` [Lt][k], on the set of
+    that table row, r2_set [Lt][H][2] (else None).  src_k / src_v
+    [Ls][ntok][H][d] and tgt_k / tgt_v [Lt][ntok][H][d] hold the same tokens
+    in the same order.  Returns (r2, r2_set, status bits)."""
+    sk, sv, tk, tv = _f64(src_k), _f64(src_v), _f64(tgt_k), _f64(tgt_v)
+    Ls, ntok, H, d = sk.shape
+    Lt = tk.shape[0]
+    assert sv.shape == sk.shape and tk.shape == tv.shape == (Lt, ntok, H, d)
+    cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    R = 1 if cu is None else cu.shape[0] - 1
+    sp = None if src_pos is None else np.ascontiguousarray(src_pos, dtype=np.int64)
+    idx = None if layer_idx is None else np.ascontiguousarray(layer_idx, dtype=np.int32)
+    k = 0 if idx is None else idx.shape[1]
+    P = _Problem(Ls, Lt, H, d, k, float(theta_src), float(theta_tgt), int(max_position), R,
+                 int(ntok), _vp(cu), _vp(sk), _vp(sv), _vp(idx), None, None, _vp(sp), None,
+                 None, CONTIGUOUS, 0, 1, 0, 0, None)
+    r2 = np.empty((Lt, Ls, H, 2))
+    r2_set = None if idx is None else np.empty((Lt, H, 2))
+    st = _load().kvxo_layer_scores(ctypes.byref(P), _dp(tk), _dp(tv), float(lam), _dp(r2),
+                                   None if r2_set is None else r2_set.ctypes.data)
+    return r2, r2_set, int(st)
 
 
 def mean_cosine(stats):

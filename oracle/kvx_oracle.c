@@ -464,3 +464,117 @@ int kvxo_ridge_fit(const double *X, const double *Y, int64_t n, int p, int q,
   free(B);
   return rc;
 }
+
+/* Layer-selection scores (definition and readings in kvx_oracle.h): for
+ * every (target layer, head, K|V) the content-space target vectors are
+ * regressed with the ridge demo on one source layer's (or a set's) content
+ * vectors, and the in-sample explained variance is summed over dimensions. */
+static double kvxo_score_fit(const double *X, const double *Y, int64_t n, int p, int d,
+                             double lam) {
+  double *W = (double *)malloc(sizeof(double) * (size_t)p * d);
+  double *b = (double *)malloc(sizeof(double) * (size_t)d);
+  double *ym = (double *)calloc((size_t)d, sizeof(double));
+  double r2 = NAN;
+  if (kvxo_ridge_fit(X, Y, n, p, d, lam, W, b) == 0) {
+    for (int64_t g = 0; g < n; ++g)
+      for (int i = 0; i < d; ++i) ym[i] += Y[g * d + i];
+    for (int i = 0; i < d; ++i) ym[i] /= (double)n;
+    double ss_res = 0.0, ss_tot = 0.0;
+    for (int64_t g = 0; g < n; ++g) {
+      for (int i = 0; i < d; ++i) {
+        double pred = b[i];
+        for (int f = 0; f < p; ++f) pred += X[g * p + f] * W[(int64_t)f * d + i];
+        double e = Y[g * d + i] - pred;
+        double c = Y[g * d + i] - ym[i];
+        ss_res += e * e;
+        ss_tot += c * c;
+      }
+    }
+    if (ss_tot > 0.0) r2 = 1.0 - ss_res / ss_tot;
+  }
+  free(W);
+  free(b);
+  free(ym);
+  return r2;
+}
+
+int kvxo_layer_scores(const kvxo_problem *P, const double *tgt_k, const double *tgt_v,
+                      double lam, double *r2, double *r2_set) {
+  const int64_t Ls = P->src_layers, Lt = P->tgt_layers, H = P->kv_heads, d = P->head_dim;
+  const int64_t ntok = P->ntok, k = P->k;
+  const int want_set = r2_set != NULL && P->layer_idx != NULL;
+  for (int64_t i = 0; i < Lt * Ls * H * 2; ++i) r2[i] = NAN;
+  if (want_set)
+    for (int64_t i = 0; i < Lt * H * 2; ++i) r2_set[i] = NAN;
+  if (P->cu_seqlens) {
+    int ok = P->cu_seqlens[0] == 0 && P->cu_seqlens[P->num_requests] == ntok;
+    for (int64_t r = 0; r < P->num_requests; ++r)
+      if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;
+    if (!ok) return KVXO_BAD_SEQLENS;
+  }
+  /* every token's position */
+  int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(ntok > 0 ? ntok : 1));
+  for (int64_t r = 0; r < P->num_requests; ++r) {
+    int64_t beg = P->cu_seqlens ? P->cu_seqlens[r] : 0;
+    int64_t end = P->cu_seqlens ? P->cu_seqlens[r + 1] : ntok;
+    for (int64_t g = beg; g < end; ++g) {
+      pos[g] = P->src_pos ? P->src_pos[g] : g - beg;
+      if (pos[g] < 0 || pos[g] >= P->max_position) {
+        free(pos);
+        return KVXO_BAD_POSITION;
+      }
+    }
+  }
+  int status = 0;
+  double *Y = (double *)malloc(sizeof(double) * (size_t)(ntok * d + 1));
+  double *X = (double *)malloc(sizeof(double) * (size_t)(ntok * d + 1));
+  double *Xs = want_set ? (double *)malloc(sizeof(double) * (size_t)(ntok * k * d + 1)) : NULL;
+  for (int64_t lt = 0; lt < Lt; ++lt) {
+    for (int64_t h = 0; h < H; ++h) {
+      for (int m = 0; m < 2; ++m) {
+        /* the target's content vectors of (lt, h, m) */
+        for (int64_t g = 0; g < ntok; ++g) {
+          const double *y = (m == 0 ? tgt_k : tgt_v) + ((lt * ntok + g) * H + h) * d;
+          if (m == 0) kvxo_rope(y, (int)d, (double)pos[g], P->theta_tgt, -1, Y + g * d);
+          else memcpy(Y + g * d, y, sizeof(double) * (size_t)d);
+        }
+        /* one source layer at a time */
+        for (int64_t s = 0; s < Ls; ++s) {
+          for (int64_t g = 0; g < ntok; ++g) {
+            const double *x = (m == 0 ? P->src_k : P->src_v) + ((s * ntok + g) * H + h) * d;
+            if (m == 0) kvxo_rope(x, (int)d, (double)pos[g], P->theta_src, -1, X + g * d);
+            else memcpy(X + g * d, x, sizeof(double) * (size_t)d);
+          }
+          r2[((lt * Ls + s) * H + h) * 2 + m] = kvxo_score_fit(X, Y, ntok, (int)d, (int)d, lam);
+        }
+        /* the set of the layer table, concatenated in table order */
+        if (want_set) {
+          int ok = 1;
+          for (int64_t j = 0; j < k; ++j) {
+            int32_t s = P->layer_idx[lt * k + j];
+            if (s < 0 || s >= Ls) ok = 0;
+          }
+          if (!ok) {
+            status |= KVXO_BAD_LAYER_INDEX;
+            continue;
+          }
+          for (int64_t g = 0; g < ntok; ++g) {
+            for (int64_t j = 0; j < k; ++j) {
+              int64_t s = P->layer_idx[lt * k + j];
+              const double *x = (m == 0 ? P->src_k : P->src_v) + ((s * ntok + g) * H + h) * d;
+              double *dst = Xs + (g * k + j) * d;
+              if (m == 0) kvxo_rope(x, (int)d, (double)pos[g], P->theta_src, -1, dst);
+              else memcpy(dst, x, sizeof(double) * (size_t)d);
+            }
+          }
+          r2_set[(lt * H + h) * 2 + m] = kvxo_score_fit(Xs, Y, ntok, (int)(k * d), (int)d, lam);
+        }
+      }
+    }
+  }
+  free(pos);
+  free(Y);
+  free(X);
+  free(Xs);
+  return status;
+}

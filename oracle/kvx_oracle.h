@@ -204,6 +204,38 @@ int kvxo_kv_diagnostics(const kvxo_problem *prob, const double *mapped_k,
 int kvxo_ridge_fit(const double *X, const double *Y, int64_t n, int p, int q,
                    double lam, double *W, double *b);
 
+/* Layer-selection scores: how much of a target layer's key / value variance
+ * one source layer, or a set of source layers, explains through the ridge
+ * bridge.  [QKV] section "Линейного моста, как ни странно, хватает": the
+ * method picks, per target layer, the source layers whose KV states best
+ * predict it; for Qwen3 14B -> 32B the best single layer explains about 56 %
+ * of the target keys' variance and 32 % of the values', a set about 79 % and
+ * 65 %.  Readings:
+ *  - Both caches hold the same tokens (calibration prefills both models on
+ *    the same text), packed the same way: token g is row g of src_k / src_v
+ *    ([Ls][ntok][H][d]) and of tgt_k / tgt_v ([Lt][ntok][H][d]), at the
+ *    same position p (src_pos[g], else g - cu_seqlens[r]).
+ *  - Keys are compared in content space: source keys un-rotated at p with
+ *    theta_src, target keys at p with theta_tgt; values as stored.
+ *  - The predictor of target (lt, h, m) from source layer s is the ridge
+ *    demo's fit (kvxo_ridge_fit, centred, intercept, lam unscaled) of the
+ *    target head-h vectors on the source head-h vectors of layer s; the set
+ *    predictor concatenates the k layers of layer_idx[lt] in table order
+ *    (the transfer's feature vector).
+ *  - The score is the in-sample explained variance summed over the d
+ *    dimensions: R^2 = 1 - sum_g |y_g - (x_g W + b)|^2 / sum_g |y_g - ybar|^2.
+ * r2 [Lt][Ls][H][2] (m = 0 keys, 1 values); r2_set [Lt][H][2], computed when
+ * both it and prob->layer_idx are given.  Every token must have a position
+ * in [0, max_position): otherwise nothing is scored, every output is NaN and
+ * KVXO_BAD_POSITION is returned (KVXO_BAD_SEQLENS likewise for a malformed
+ * request table).  A set row with a layer index outside [0, Ls) gives NaN
+ * scores for that target layer and KVXO_BAD_LAYER_INDEX; a fit whose normal
+ * matrix is not positive definite, or a target with no variance, gives NaN.
+ * prob's transfer-only fields (W, b, target positions, layouts) are unused;
+ * the source must be packed (KVXO_CONTIGUOUS). */
+int kvxo_layer_scores(const kvxo_problem *prob, const double *tgt_k,
+                      const double *tgt_v, double lam, double *r2, double *r2_set);
+
 #ifdef __cplusplus
 }
 #endif

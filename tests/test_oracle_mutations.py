@@ -83,7 +83,7 @@ MUTATIONS = {
          "int64_t p = P->src_pos ? P->src_pos[g] : g;", 3)],
     "backwards_request_table_accepted": [
         (C, "if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;",
-         "if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = ok + 0;", 3)],
+         "if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = ok + 0;", 4)],
     "contiguous_row_ignores_request_slab": [
         (C, "return r * dst_capacity + p_tgt;", "return 0 * r * dst_capacity + p_tgt;", 1)],
     "paged_target_slot_off_by_one": [
@@ -138,6 +138,20 @@ MUTATIONS = {
         (C, "v -= xm[i] * W[i * q + c];", "v += xm[i] * W[i * q + c];", 1)],
     "ridge_back_solve_with_L_not_LT": [
         (C, "v -= A[m * p + i] * W[m * q + c];", "v -= A[i * p + m] * W[m * q + c];", 1)],
+    # layer-selection scores
+    "scores_target_keys_not_unrotated": [
+        (C, "if (m == 0) kvxo_rope(y, (int)d, (double)pos[g], P->theta_tgt, -1, Y + g * d);",
+         "if (m == 0) memcpy(Y + g * d, y, sizeof(double) * (size_t)d);", 1)],
+    "scores_source_keys_unrotated_with_target_base": [
+        (C, "if (m == 0) kvxo_rope(x, (int)d, (double)pos[g], P->theta_src, -1, X + g * d);",
+         "if (m == 0) kvxo_rope(x, (int)d, (double)pos[g], P->theta_tgt, -1, X + g * d);", 1)],
+    "scores_total_uncentred": [
+        (C, "double c = Y[g * d + i] - ym[i];", "double c = Y[g * d + i];", 1)],
+    "scores_prediction_without_intercept": [
+        (C, "double pred = b[i];", "double pred = 0.0 * b[i];", 1)],
+    "scores_set_from_first_layer_only": [
+        (C, "int64_t s = P->layer_idx[lt * k + j];\n              const double *x",
+         "int64_t s = P->layer_idx[lt * k + 0];\n              const double *x", 1)],
 }
 
 # runs every pin function of test_oracle_pins (parametrized ones once per

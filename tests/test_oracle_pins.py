@@ -982,3 +982,135 @@ def test_paged_source_bad_blocks_skip_and_flag():
     # with the full table the same rows only fail the row check
     _, _, st = oracle.transfer(src_k=pk, src_v=pk, src_block_table=table[:, :3], **kw2)
     assert st == oracle.BAD_SRC_BLOCK | oracle.BAD_ROW
+
+
+# ---------------------------------------------------------------------------
+# Layer-selection scores (kvxo_layer_scores)
+# ---------------------------------------------------------------------------
+def _rotate_np(x, pos, theta):
+    """Half-split RoPE written out here with numpy (test input preparation)."""
+    d = x.shape[-1]
+    half = d // 2
+    w = theta ** (-2.0 * np.arange(half) / d)
+    a = np.asarray(pos, dtype=np.float64)[:, None] * w[None, :]
+    x0, x1 = x[..., :half], x[..., half:]
+    c, s = np.cos(a), np.sin(a)
+    if x.ndim == 3:        # [n][H][d]
+        c, s = c[:, None, :], s[:, None, :]
+    return np.concatenate((x0 * c - x1 * s, x0 * s + x1 * c), axis=-1)
+
+
+def test_layer_scores_worked_example_exact_fractions():
+    g = _golden_rows("layer_scores_worked_example.txt")
+    a = np.array([float(v) for v in g["a"]])
+    b = np.array([float(v) for v in g["b"]])
+    lam = float(g["lam"][0]) / float(g["lam"][1])
+    ts, tt = float(g["theta_src"][0]), float(g["theta_tgt"][0])
+    n = len(a)
+    xc = np.zeros((n, 4)); xc[:, 1] = a
+    yc = np.zeros((n, 4)); yc[:, 1] = b
+    pos = np.arange(n)
+    src_v = xc[None, :, None, :]
+    tgt_v = yc[None, :, None, :]
+    src_k = _rotate_np(xc, pos, ts)[None, :, None, :]
+    tgt_k = _rotate_np(yc, pos, tt)[None, :, None, :]
+    r2, r2s, st = oracle.layer_scores(src_k=src_k, src_v=src_v, tgt_k=tgt_k, tgt_v=tgt_v,
+                                      theta_src=ts, theta_tgt=tt, max_position=n, lam=lam,
+                                      layer_idx=np.array([[0]]))
+    assert st == 0
+    frac = lambda key: float(g[key][0]) / float(g[key][1])
+    assert r2[0, 0, 0, 1] == pytest.approx(frac("r2_values"), abs=1e-13)
+    assert r2[0, 0, 0, 0] == pytest.approx(frac("r2_keys"), abs=1e-12)
+    assert r2s[0, 0, 1] == pytest.approx(frac("r2_set"), abs=1e-13)
+    assert r2s[0, 0, 0] == pytest.approx(frac("r2_set"), abs=1e-12)
+
+
+def _score_case(seed, Ls=3, Lt=2, H=2, d=8, n=40, noise=0.3):
+    rng = np.random.default_rng(seed)
+    xs_k = rng.normal(size=(Ls, n, H, d)) * np.exp(rng.normal(size=(Ls, 1, H, d)))
+    xs_v = rng.normal(size=(Ls, n, H, d))
+    # target layer lt is a linear function of source layer lt (+ noise)
+    yk = np.empty((Lt, n, H, d)); yv = np.empty((Lt, n, H, d))
+    for lt in range(Lt):
+        for h in range(H):
+            A = rng.normal(size=(d, d)); B = rng.normal(size=(d, d))
+            yk[lt, :, h] = xs_k[lt, :, h] @ A + 0.5 + noise * rng.normal(size=(n, d))
+            yv[lt, :, h] = xs_v[lt, :, h] @ B - 0.2 + noise * rng.normal(size=(n, d))
+    return xs_k, xs_v, yk, yv
+
+
+def test_layer_scores_equal_least_squares_r2_as_lambda_vanishes():
+    # lam -> 0: the ridge fit is the least-squares fit with intercept, whose
+    # in-sample R^2 (summed over outputs) LAPACK's lstsq gives independently
+    xk, xv, yk, yv = _score_case(3)
+    Ls, n, H, d = xv.shape
+    r2, _, st = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv, theta_src=1.0,
+                                    theta_tgt=1.0, max_position=n, lam=1e-10)
+    assert st == 0
+    pos = np.arange(n)
+    for lt in range(yk.shape[0]):
+        for s in range(Ls):
+            for h in range(H):
+                for m, (X, Y) in enumerate(((xk, yk), (xv, yv))):
+                    x = X[s, :, h]; y = Y[lt, :, h]
+                    if m == 0:   # content space: un-rotate at p with base 1
+                        x = _rotate_np(x, -pos, 1.0); y = _rotate_np(y, -pos, 1.0)
+                    A = np.hstack([x, np.ones((n, 1))])
+                    coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+                    res = y - A @ coef
+                    ref = 1 - (res ** 2).sum() / ((y - y.mean(0)) ** 2).sum()
+                    assert r2[lt, s, h, m] == pytest.approx(ref, abs=1e-8)
+
+
+def test_layer_scores_see_content_only_through_each_models_rope():
+    # keys stored rotated, with different bases on the two sides, related
+    # exactly (linear, noiseless) in content space: the matched layer scores
+    # 1 - O(lam); un-rotating with the wrong base or skipping it would not
+    xk, xv, yk, yv = _score_case(5, noise=0.0)
+    Ls, n, H, d = xk.shape
+    pos = np.arange(n)
+    sk = np.stack([_rotate_np(xk[s], pos, 1e4) for s in range(Ls)])
+    tk = np.stack([_rotate_np(yk[lt], pos, 5e5) for lt in range(yk.shape[0])])
+    r2, _, st = oracle.layer_scores(src_k=sk, src_v=xv, tgt_k=tk, tgt_v=yv, theta_src=1e4,
+                                    theta_tgt=5e5, max_position=n, lam=1e-9)
+    assert st == 0
+    for lt in range(yk.shape[0]):
+        assert np.all(r2[lt, lt] > 1 - 1e-6)
+    # the same stored keys read with swapped bases lose the linear relation
+    r2w, _, _ = oracle.layer_scores(src_k=sk, src_v=xv, tgt_k=tk, tgt_v=yv, theta_src=5e5,
+                                    theta_tgt=1e4, max_position=n, lam=1e-9)
+    assert np.all(r2w[0, 0, :, 0] < 0.99)
+
+
+def test_layer_scores_invariances_and_set_bounds():
+    xk, xv, yk, yv = _score_case(7)
+    Ls, n, H, d = xk.shape
+    kw = dict(theta_src=1e4, theta_tgt=1e4, max_position=n, lam=0.01)
+    r2, r2s, st = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv,
+                                      layer_idx=np.array([[0, 2], [1, 0]]), **kw)
+    assert st == 0 and np.all(r2 <= 1) and np.all(r2s <= 1)
+    # scaling the target changes nothing for values; for keys the scale
+    # commutes with the rotation
+    r2b, _, _ = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=3 * yk, tgt_v=3 * yv, **kw)
+    # ridge with the same lam on a scaled target: identical fit up to scale
+    assert np.allclose(r2b, r2, atol=1e-12)
+    # a set of one layer is that layer's fit
+    r21, r2s1, _ = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv,
+                                       layer_idx=np.array([[2], [1]]), **kw)
+    assert np.allclose(r2s1[0], r21[0, 2]) and np.allclose(r2s1[1], r21[1, 1])
+    # more features never fit worse in sample (tiny lam); the layer each
+    # target was drawn from is listed second, so a set that read only its
+    # first layer would fall short of it
+    kw["lam"] = 1e-10
+    r2t, r2st, _ = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv,
+                                       layer_idx=np.array([[2, 0], [0, 1]]), **kw)
+    assert np.all(r2st[0] >= np.maximum(r2t[0, 0], r2t[0, 2]) - 1e-9)
+    assert np.all(r2st[1] >= np.maximum(r2t[1, 1], r2t[1, 0]) - 1e-9)
+    # the score of a set does not depend on the order of its layers
+    _, r2sr, _ = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv,
+                                     layer_idx=np.array([[0, 2], [1, 0]]), **kw)
+    assert np.allclose(r2sr, r2st, atol=1e-9)
+    # a bad position scores nothing
+    r2e, _, ste = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv,
+                                      theta_src=1e4, theta_tgt=1e4, max_position=n - 1)
+    assert ste == oracle.BAD_POSITION and np.all(np.isnan(r2e))
