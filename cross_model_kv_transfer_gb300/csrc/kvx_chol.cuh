@@ -1,0 +1,193 @@
+// kvx_chol.cuh -- batched fp64 Cholesky factorisation of G + lam I, blocked
+// by 64, shared by the ridge fit (kvx_ridge.cu) and the layer-selection
+// scores (kvx_scores.cu).  G is [batch][p][p] fp64 in global memory holding
+// the upper triangle of a symmetric matrix; after chol_factor it holds L in
+// its lower triangle and L^T in its upper one.  A fit whose pivot is not
+// positive gets G[0] = NaN and KVX_FLAG_NOT_SPD in *status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvx.h"
+
+namespace {
+
+constexpr int kB = 64;   // block of the factorisation
+
+// G + lam I mirrored to full: row block blockIdx.y of fit blockIdx.x.
+__global__ void __launch_bounds__(256) chol_prep_kernel(double *__restrict__ G, int p, double lam) {
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  const int r0 = blockIdx.y * kB;
+  for (int e = threadIdx.x; e < kB * p; e += blockDim.x) {
+    const int i = r0 + e / p, j = e % p;
+    if (i >= p) break;
+    if (i > j) A[(int64_t)i * p + j] = A[(int64_t)j * p + i];
+    else if (i == j) A[(int64_t)i * p + j] += lam;
+  }
+}
+
+__device__ __forceinline__ int blk_len(int p, int kb) { return p - kb * kB < kB ? p - kb * kB : kB; }
+
+// Factor the diagonal block kb of each fit in shared memory (left-looking,
+// one warp per row); the update of earlier blocks is already applied.
+__global__ void __launch_bounds__(256) chol_diag_kernel(double *__restrict__ G, int p, int kb,
+                                                        uint32_t *status) {
+  __shared__ double L[kB][kB + 1];
+  __shared__ int s_fail;
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  if (isnan(A[0])) return;
+  const int o = kb * kB, nb = blk_len(p, kb);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+  for (int e = tid; e < nb * nb; e += blockDim.x) {
+    const int i = e / nb, j = e % nb;
+    L[i][j] = A[(int64_t)(o + i) * p + o + j];
+  }
+  if (tid == 0) s_fail = 0;
+  __syncthreads();
+  for (int j = 0; j < nb; ++j) {
+    if (warp == 0) {
+      double sum = 0.0;
+      for (int m = lane; m < j; m += 32) sum = fma(L[j][m], L[j][m], sum);
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
+      if (lane == 0) {
+        const double d = L[j][j] - sum;
+        if (!(d > 0.0)) s_fail = 1;
+        L[j][j] = d > 0.0 ? sqrt(d) : 1.0;
+      }
+    }
+    __syncthreads();
+    if (s_fail) break;
+    for (int i = j + 1 + warp; i < nb; i += nwarps) {
+      double sum = 0.0;
+      for (int m = lane; m < j; m += 32) sum = fma(L[i][m], L[j][m], sum);
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
+      if (lane == 0) L[i][j] = (L[i][j] - sum) / L[j][j];
+    }
+    __syncthreads();
+  }
+  if (s_fail) {
+    if (tid == 0) {
+      A[0] = nan("");
+      if (status) atomicOr(status, KVX_FLAG_NOT_SPD);
+    }
+    return;
+  }
+  // L in the lower triangle, L^T in the upper (rows of L^T are what the
+  // back substitution reads)
+  for (int e = tid; e < nb * nb; e += blockDim.x) {
+    const int i = e / nb, j = e % nb;
+    A[(int64_t)(o + i) * p + o + j] = i >= j ? L[i][j] : L[j][i];
+  }
+}
+
+// Panel: block row ib = kb + 1 + blockIdx.y of fit blockIdx.x solves
+// X L_kb^T = A[ib][kb] (rows independent: one thread per row).
+__global__ void __launch_bounds__(64) chol_panel_kernel(double *__restrict__ G, int p, int kb) {
+  __shared__ double L[kB][kB + 1];
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  if (isnan(A[0])) return;
+  const int o = kb * kB, nb = blk_len(p, kb);
+  const int ib = kb + 1 + blockIdx.y;
+  const int r0 = ib * kB, nr = blk_len(p, ib);
+  for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
+    const int i = e / nb, j = e % nb;
+    L[i][j] = i >= j ? A[(int64_t)(o + i) * p + o + j] : 0.0;
+  }
+  __syncthreads();
+  const int r = threadIdx.x;
+  if (r >= nr) return;
+  double *row = A + (int64_t)(r0 + r) * p + o;
+  double x[kB];
+#pragma unroll
+  for (int j = 0; j < kB; ++j) x[j] = j < nb ? row[j] : 0.0;
+#pragma unroll
+  for (int j = 0; j < kB; ++j) {
+    if (j >= nb) break;
+    double v = x[j];
+#pragma unroll
+    for (int m = 0; m < j; ++m) v = fma(-x[m], L[j][m], v);
+    x[j] = v / L[j][j];
+  }
+#pragma unroll
+  for (int j = 0; j < kB; ++j)
+    if (j < nb) {
+      row[j] = x[j];                                   // L[r0 + r][o + j]
+      A[(int64_t)(o + j) * p + r0 + r] = x[j];         // and L^T
+    }
+}
+
+// Trailing update: lower-triangle block (ib, jb), ib >= jb > kb, of fit
+// blockIdx.x: A[ib][jb] -= A[ib][kb] A[jb][kb]^T; 256 threads, 4 x 4 each.
+__global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ G, int p, int kb) {
+  __shared__ double Pa[kB][kB / 2 + 1];
+  __shared__ double Pb[kB][kB / 2 + 1];
+  double *A = G + (int64_t)blockIdx.x * p * p;
+  if (isnan(A[0])) return;
+  // decode (ib, jb) from the lower triangle of the trailing blocks
+  int t = blockIdx.y, ib = kb + 1, jb = kb + 1;
+  while (t > ib - (kb + 1)) {
+    t -= ib - kb;
+    ++ib;
+  }
+  jb = kb + 1 + t;
+  const int o = kb * kB, nk = blk_len(p, kb);
+  const int ri = ib * kB, rj = jb * kB, ni = blk_len(p, ib), nj = blk_len(p, jb);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  double acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.0;
+  for (int k0 = 0; k0 < nk; k0 += kB / 2) {
+    for (int e = threadIdx.x; e < kB * (kB / 2); e += blockDim.x) {
+      const int r = e / (kB / 2), k = e % (kB / 2);
+      const bool kin = k0 + k < nk;
+      Pa[r][k] = (r < ni && kin) ? A[(int64_t)(ri + r) * p + o + k0 + k] : 0.0;
+      Pb[r][k] = (r < nj && kin) ? A[(int64_t)(rj + r) * p + o + k0 + k] : 0.0;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < kB / 2; ++k) {
+      double av[4], bv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) av[a] = Pa[4 * ty + a][k];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bv[c] = Pb[4 * tx + c][k];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = fma(av[a], bv[c], acc[a][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = 4 * ty + a, j = 4 * tx + c;
+      if (i < ni && j < nj && (ib != jb || i >= j))
+        A[(int64_t)(ri + i) * p + rj + j] -= acc[a][c];
+    }
+}
+
+// Launch the whole factorisation (4 + 3 (p / 64 rounded up) - 1 launches).
+inline cudaError_t chol_factor(double *G, int batch, int p, double lam, uint32_t *status,
+                               cudaStream_t s) {
+  const int nblk = (p + kB - 1) / kB;
+  chol_prep_kernel<<<dim3((unsigned)batch, (unsigned)nblk), 256, 0, s>>>(G, p, lam);
+  for (int kb = 0; kb < nblk; ++kb) {
+    chol_diag_kernel<<<batch, 256, 0, s>>>(G, p, kb, status);
+    const int rest = nblk - 1 - kb;
+    if (rest > 0) {
+      chol_panel_kernel<<<dim3((unsigned)batch, (unsigned)rest), 64, 0, s>>>(G, p, kb);
+      chol_update_kernel<<<dim3((unsigned)batch, (unsigned)(rest * (rest + 1) / 2)), 256, 0, s>>>(
+          G, p, kb);
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace

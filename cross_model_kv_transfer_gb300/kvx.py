@@ -57,7 +57,8 @@ KVX_MAPPER_WIDE = 1
 EXPORTED = ("kvx_plan_create", "kvx_transfer", "kvx_plan_destroy",
             "kvx_status_string", "kvx_plan_kernel", "kvx_plan_launches",
             "kvx_plan_cta_group", "kvx_transfer_static", "kvx_kv_diagnostics",
-            "kvx_ridge_workspace_bytes", "kvx_ridge_fit")
+            "kvx_ridge_workspace_bytes", "kvx_ridge_fit",
+            "kvx_layer_scores_workspace_bytes", "kvx_layer_scores")
 
 
 class PlanDesc(ctypes.Structure):
@@ -119,6 +120,19 @@ class RidgeArgs(ctypes.Structure):
     ]
 
 
+class ScoreArgs(ctypes.Structure):
+    _fields_ = [
+        ("src_k", ctypes.c_void_p), ("src_v", ctypes.c_void_p),
+        ("tgt_k", ctypes.c_void_p), ("tgt_v", ctypes.c_void_p),
+        ("ntok", ctypes.c_int64), ("num_requests", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p), ("src_pos", ctypes.c_void_p),
+        ("layer_idx", ctypes.c_void_p), ("lambda", ctypes.c_double),
+        ("r2", ctypes.c_void_p), ("r2_set", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -163,6 +177,11 @@ def load():
             lib.kvx_ridge_workspace_bytes.restype = ctypes.c_size_t
             lib.kvx_ridge_fit.argtypes = [ctypes.POINTER(RidgeArgs), ctypes.c_void_p]
             lib.kvx_ridge_fit.restype = ctypes.c_int
+            lib.kvx_layer_scores_workspace_bytes.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+            lib.kvx_layer_scores_workspace_bytes.restype = ctypes.c_size_t
+            lib.kvx_layer_scores.argtypes = [ctypes.c_void_p, ctypes.POINTER(ScoreArgs),
+                                             ctypes.c_void_p]
+            lib.kvx_layer_scores.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -214,6 +233,14 @@ def kvx_ridge_workspace_bytes(batch: int, p: int, q: int) -> int:
 
 def kvx_ridge_fit(args: RidgeArgs, stream) -> int:
     return load().kvx_ridge_fit(ctypes.byref(args), stream)
+
+
+def kvx_layer_scores_workspace_bytes(plan, ntok: int) -> int:
+    return load().kvx_layer_scores_workspace_bytes(plan, int(ntok))
+
+
+def kvx_layer_scores(plan, args: ScoreArgs, stream) -> int:
+    return load().kvx_layer_scores(plan, ctypes.byref(args), stream)
 
 
 def ridge_fit(x, y, lam: float = 0.01, w=None, b=None, workspace=None, status=None,
@@ -446,6 +473,55 @@ class Plan:
         a._keep = (mapped_k, mapped_v, ref_k, ref_v, stats, cu_seqlens, src_pos, tgt_pos,
                    tgt_offset, block_table, status)
         return a
+
+    def layer_scores(self, *, src_k, src_v, tgt_k, tgt_v, lam=0.01, cu_seqlens=None,
+                     src_pos=None, layer_idx=None, r2=None, r2_set=None, workspace=None,
+                     status=None, stream=None):
+        """Layer-selection scores (``kvx_layer_scores``) of CUDA tensors:
+        src_k / src_v [Ls][ntok][H][d] and tgt_k / tgt_v [Lt][ntok][H][d] of
+        the same tokens; returns fp64 r2 [Lt][Ls][H][2] and, with
+        ``layer_idx`` [Lt][k], r2_set [Lt][H][2] (else None), enqueued on
+        ``stream``.  Scratch is allocated here unless ``workspace`` (a uint8
+        CUDA tensor) is given."""
+        import torch
+        d = self.desc
+        Ls, Lt, H, hd = d.src_layers, d.tgt_layers, d.src_kv_heads, d.src_head_dim
+        for name, t, L in (("src_k", src_k, Ls), ("src_v", src_v, Ls), ("tgt_k", tgt_k, Lt),
+                           ("tgt_v", tgt_v, Lt)):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA tensor")
+            if t.dtype != self.kv_dtype or t.dim() != 4 or t.shape[0] != L or \
+                    tuple(t.shape[2:]) != (H, hd):
+                raise ValueError(f"{name}: expected [{L}][ntok][{H}][{hd}] {self.kv_dtype}")
+        ntok = src_k.shape[1]
+        if any(t.shape[1] != ntok for t in (src_v, tgt_k, tgt_v)):
+            raise ValueError("the four caches must hold the same tokens")
+        dev = src_k.device
+        R = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+        r2 = torch.empty((Lt, Ls, H, 2), dtype=torch.float64, device=dev) if r2 is None else r2
+        if layer_idx is not None and r2_set is None:
+            r2_set = torch.empty((Lt, H, 2), dtype=torch.float64, device=dev)
+        need = kvx_layer_scores_workspace_bytes(self.handle, ntok)
+        if need == 0:
+            raise KvxError(KVX_ERR_UNSUPPORTED, "kvx_layer_scores_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        for name, t, shape in (("cu_seqlens", cu_seqlens, (R + 1,)), ("src_pos", src_pos, (ntok,)),
+                               ("layer_idx", layer_idx, (Lt, d.k))):
+            if t is not None and (t.dtype != torch.int32 or tuple(t.shape) != shape or
+                                  not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous int32 CUDA tensor {shape}")
+        a = ScoreArgs(src_k.data_ptr(), src_v.data_ptr(), tgt_k.data_ptr(), tgt_v.data_ptr(),
+                      int(ntok), int(R), ptr(cu_seqlens), ptr(src_pos), ptr(layer_idx),
+                      float(lam), r2.data_ptr(), ptr(r2_set), workspace.data_ptr(),
+                      workspace.numel(), ptr(status))
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        st = kvx_layer_scores(self.handle, a, ctypes.c_void_p(stream.cuda_stream))
+        if st != KVX_OK:
+            raise KvxError(st, "kvx_layer_scores")
+        return r2, r2_set
 
     def kv_diagnostics(self, stream=None, **tensors) -> None:
         """Enqueue the fidelity statistics [Lt][H][2][d + 4] (fp64, into

@@ -369,6 +369,66 @@ size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
  * definite gets NaN W and b and sets KVX_FLAG_NOT_SPD. */
 kvx_status kvx_ridge_fit(const kvx_ridge_args *args, void *stream);
 
+/* Arguments of the layer-selection scores (kvx_layer_scores).  DEVICE
+ * pointers unless noted; shapes come from the plan (Ls, Lt, H, d, k, the two
+ * RoPE bases, max_position, the cache dtype).  Both caches hold the same
+ * tokens in the same packed order (calibration prefills both models on the
+ * same text): token g is row g of the source and of the target arrays. */
+typedef struct {
+  const void *src_k, *src_v;  /* [Ls][ntok][H][d] the pilot's cache (keys
+                                 RoPE-rotated with rope_theta_src)           */
+  const void *tgt_k, *tgt_v;  /* [Lt][ntok][H][d] the target's own cache of
+                                 the same tokens (keys with rope_theta_tgt)  */
+  int64_t ntok;               /* tokens, >= 2                                 */
+  int32_t num_requests;       /* R >= 1                                       */
+  const int32_t *cu_seqlens;  /* [R+1] or NULL (R == 1), as for kvx_transfer  */
+  const int32_t *src_pos;     /* [ntok] positions, or NULL: 0..len-1 per
+                                 request; both caches are at these positions */
+  const int32_t *layer_idx;   /* [Lt][k] or NULL: also score each row's set  */
+  double lambda;              /* ridge strength (> 0), added unscaled         */
+  double *r2;                 /* [Lt][Ls][H][2] output, m = 0 keys, 1 values  */
+  double *r2_set;             /* [Lt][H][2] output, or NULL (needs layer_idx) */
+  void *workspace;            /* kvx_layer_scores_workspace_bytes(plan, ntok) */
+  size_t workspace_bytes;
+  uint32_t *status;           /* optional device word; KVX_FLAG_* OR-ed in    */
+} kvx_score_args;
+
+/* Bytes of scratch kvx_layer_scores needs for `ntok` tokens (content
+ * features of one (head, K|V) at a time, fp64 sums, Gram and cross blocks),
+ * or 0 if the plan cannot score (head_dim not a multiple of 16 or above 128,
+ * ntok < 2). */
+size_t kvx_layer_scores_workspace_bytes(const kvx_plan *plan, int64_t ntok);
+
+/* Layer-selection scores: how much of each target layer's key / value
+ * variance one source layer, or the set of a layer-table row, explains
+ * through the ridge bridge.  "Перенос KV-кэша между моделями Qwen3 вместо
+ * повторного префилла", section "Линейного моста, как ни странно, хватает":
+ * the method picks, per target layer, the source layers whose KV states best
+ * predict it (for 14B -> 32B the best single layer explains ~56 % of the
+ * keys' variance and ~32 % of the values', a set ~79 % and ~65 %), and fits
+ * one ridge regression per target (layer, head), one for keys, one for
+ * values.  For every (target layer lt, source layer s, head h, K|V): keys are
+ * taken in content space (source keys un-rotated at their position with
+ * rope_theta_src, target keys with rope_theta_tgt), the ridge demo's
+ * centred fit of the target vectors on the source vectors is formed, and
+ * r2 = 1 - sum |y - (x W + b)|^2 / sum |y - ybar|^2, summed over the d
+ * dimensions (in-sample).  With layer_idx the set of row lt (its k layers
+ * concatenated in table order, the transfer's feature vector) is scored the
+ * same way into r2_set.  Computed from fp32 content features with fp32
+ * products accumulated in fp64 (centred Gram and cross blocks), an fp64
+ * Cholesky of G + lambda I and fp64 triangular solves:
+ * r2 = (|L^-1 C|^2 + lambda |W|^2) / sum |y - ybar|^2.  Asynchronous on
+ * `stream`; no allocation (the caller passes the scratch).  Returns
+ * KVX_ERR_INVALID_ARG for a NULL pointer, lambda <= 0 or non-finite, ntok < 2
+ * or a workspace that is too small; KVX_ERR_UNSUPPORTED for a head_dim the
+ * scorer does not handle; KVX_ERR_CUDA if a launch fails.  Device-detected:
+ * a token position outside [0, max_position) or a malformed request table
+ * makes every score NaN (KVX_FLAG_BAD_POSITION / KVX_FLAG_BAD_SEQLENS); a
+ * set row with a layer index outside [0, Ls) gives NaN set scores
+ * (KVX_FLAG_BAD_LAYER_INDEX); a fit that is not positive definite or a
+ * target without variance gives NaN (KVX_FLAG_NOT_SPD for the former). */
+kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_args *args, void *stream);
+
 /* Allocation-free transfer.  The sources have no counterpart for this call:
  * it exists for callers that may not allocate device memory -- engines that
  * reserve nearly all of the GPU for their own paged KV-cache pool and forbid
