@@ -39,7 +39,7 @@ WIDE_METRIC = ("KV-transfer tokens/s at 14B→32B shape, 32K tokens, wide-featur
 PUBLISHED_MS = {"qwen3_14b_32b": 277.6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu", "diag": "kvx_diag.cu",
-                "wide": "kvx_wide.cu", "ridge": "kvx_ridge.cu"}
+                "wide": "kvx_wide.cu", "ridge": "kvx_ridge.cu", "scores": "kvx_scores.cu"}
 
 
 def parse_args(argv=None):
@@ -48,11 +48,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
-    ap.add_argument("--op", choices=["transfer", "kv_diagnostics", "ridge_fit"],
+    ap.add_argument("--op", choices=["transfer", "kv_diagnostics", "ridge_fit", "layer_scores"],
                     default="transfer",
                     help="transfer (the default step), the fidelity diagnostics of a "
-                         "mapped cache against the target's own, or a batch of ridge fits "
-                         "of the per-head maps (calibration)")
+                         "mapped cache against the target's own, a batch of ridge fits "
+                         "of the per-head maps (calibration), or the layer-selection "
+                         "scores of paired calibration caches")
+    ap.add_argument("--score-tokens", type=int, default=4096,
+                    help="calibration tokens of the layer-selection scores")
     ap.add_argument("--ridge-batch", type=int, default=16, help="ridge fits per step")
     ap.add_argument("--ridge-n", type=int, default=131072, help="observations per ridge fit")
     ap.add_argument("--workload", default="qwen3_14b_32b")
@@ -530,6 +533,181 @@ def run_ridge(args):
         print(json.dumps(line), flush=True)
 
 
+SCORE_METRIC = ("layer-selection scores: calibration tokens/s through every (target layer, "
+                "source layer, head, K|V) fit and every target layer's set fit at the 14B→32B "
+                "shape, 4,096 tokens; % of fp32 ALU roofline")
+
+
+def score_config(wl, n: int) -> dict:
+    """Workload keys of a layer-selection score line, the same in both arms."""
+    return {"workload": f"{wl.name} layer-selection scores", "tokens": n,
+            "src_layers": wl.src_layers, "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
+            "head_dim": wl.head_dim, "k": wl.k, "lambda": 0.01}
+
+
+def score_flops(Ls, Lt, H, d, k, n) -> float:
+    """Useful flops of one scoring pass: per (head, K|V) the centred Gram
+    (symmetric, counted once) and cross moments of every source layer
+    against every target layer's d columns, and of every target layer's set
+    of k source layers against its own d columns."""
+    per = Ls * (d * (d + 1) / 2 + d * Lt * d) + Lt * (k * d * (k * d + 1) / 2 + k * d * d)
+    return 2.0 * n * per * 2 * H
+
+
+def score_launches(Ls, Lt, H, d, k, sets=True) -> int:
+    """Kernels one kvx_layer_scores call launches: three table checks, then
+    per (head, K|V) clear, content, Gram, Cholesky (prep + per 64-column
+    block: diagonal, panel, update), solve, the set fits' Gram, Cholesky and
+    solve, and the final ratios."""
+    chol = lambda p: 1 + 3 * ((p + 63) // 64) - 2
+    per = 3 + chol(d) + 1 + (2 + chol(k * d) if sets else 0) + 1
+    return 2 + (1 if sets else 0) + H * 2 * per
+
+
+def run_scores(args):
+    """One step = one kvx_layer_scores call on seeded paired calibration
+    caches (the pilot's and the target's caches of the same tokens)."""
+    import torch
+    from cross_model_kv_transfer_gb300 import kvx
+    from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_score_inputs
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload].with_tokens([args.score_tokens], [0])
+    n = wl.ntok
+    inp = make_score_inputs(wl, dev)
+    plan = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers, kv_heads=wl.kv_heads,
+                    head_dim=wl.head_dim, k=wl.k, rope_theta_src=wl.theta_src,
+                    rope_theta_tgt=wl.theta_tgt, max_position=wl.max_position,
+                    kv_dtype=wl.kv_dtype, w_dtype=torch.float32, b_dtype=wl.b_dtype,
+                    kernel=kvx.KVX_KERNEL_SIMT)
+    Ls, Lt, H, d, k = wl.src_layers, wl.tgt_layers, wl.kv_heads, wl.head_dim, wl.k
+    r2 = torch.empty((Lt, Ls, H, 2), dtype=torch.float64, device=dev)
+    r2s = torch.empty((Lt, H, 2), dtype=torch.float64, device=dev)
+    scratch = torch.empty(kvx.kvx_layer_scores_workspace_bytes(plan.handle, n), dtype=torch.uint8,
+                          device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(lam=0.01, layer_idx=inp["layer_idx"], r2=r2, r2_set=r2s, workspace=scratch,
+              status=status, stream=stream)
+    cache = ("src_k", "src_v", "tgt_k", "tgt_v")
+
+    def step():
+        plan.layer_scores(**{c: inp[c] for c in cache}, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    value, ms = aggregate(n, ms_local, dev)
+    flops = score_flops(Ls, Lt, H, d, k, n)
+    peak = fp32_alu_peak_tflops()
+    achieved = flops / (ms_local / 1e3) / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": measured_traffic(wl.name, "scores"),
+            "peak_source": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
+            "algorithmic_flops": flops, "scope": "whole call (every kernel of the pass)"}
+    in_bytes = sum(inp[c].numel() * inp[c].element_size() for c in cache)
+
+    e2e = None
+    if not args.no_e2e:
+        host = {c: inp[c].cpu().pin_memory() for c in cache}
+        hr, hs = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (r2, r2s))
+
+        def e2e_step():
+            for c in cache:
+                inp[c].copy_(host[c], non_blocking=True)
+            step()
+            hr.copy_(r2, non_blocking=True)
+            hs.copy_(r2s, non_blocking=True)
+
+        n_e = max(1, min(args.steps, 3))
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        ev0.record(stream)
+        for _ in range(n_e):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_val, e_ms = aggregate(n, ev0.elapsed_time(ev1) / n_e, dev)
+        e2e = {"value": e_val, "unit": "tokens/s", "ms_per_step": e_ms, "steps": n_e,
+               "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": (hr.numel() + hs.numel()) * 8}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle_scores(wl, args.cpu_seconds)
+    line = {
+        "metric": SCORE_METRIC, "op": "layer_scores", "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded paired caches with planted source layers)",
+        "config": {**score_config(wl, n), "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of caches read per "
+                         "step, no flush needed)"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": score_launches(Ls, Lt, H, d, k) * args.steps,
+        "clocks": clk.summary(),
+        "mean_best_single_layer_r2": [float(x) for x in
+                                      r2.max(dim=1).values.mean(dim=(0, 1)).cpu()],
+        "mean_set_r2": [float(x) for x in r2s.mean(dim=(0, 1)).cpu()],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def score_sample(wl, n: int, lt: int = 2, heads: int = 1):
+    """A bounded slice of the scoring workload for the oracle: n tokens,
+    every source layer, ``lt`` target layers, ``heads`` heads; returns
+    (kwargs of oracle.layer_scores, the slice's useful flops)."""
+    import dataclasses
+    import torch
+    from cross_model_kv_transfer_gb300.workloads import make_score_inputs
+    small = dataclasses.replace(wl.with_tokens([n], [0]), tgt_layers=lt, kv_heads=heads)
+    inp = make_score_inputs(small, "cpu")
+    f64 = lambda t: t.to(torch.float64).numpy()
+    kw = dict(src_k=f64(inp["src_k"]), src_v=f64(inp["src_v"]), tgt_k=f64(inp["tgt_k"]),
+              tgt_v=f64(inp["tgt_v"]), theta_src=wl.theta_src, theta_tgt=wl.theta_tgt,
+              max_position=n, lam=0.01, layer_idx=inp["layer_idx"].numpy())
+    return kw, score_flops(wl.src_layers, lt, heads, wl.head_dim, wl.k, n)
+
+
+def time_oracle_scores(wl, target_seconds: float):
+    """The oracle on a growing slice until it takes about ``target_seconds``,
+    scaled to the whole workload by useful flops."""
+    import oracle
+    full = score_flops(wl.src_layers, wl.tgt_layers, wl.kv_heads, wl.head_dim, wl.k, wl.ntok)
+    n = 256
+    while True:
+        kw, f = score_sample(wl, n)
+        t0 = time.perf_counter()
+        oracle.layer_scores(**kw)
+        el = time.perf_counter() - t0
+        if el * 2 > target_seconds or n * 2 > wl.ntok:
+            break
+        n *= 2
+    return {"value": wl.ntok / (el * full / f), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} tokens x all {wl.src_layers} source layers x 2 target layers x 1 "
+                      f"head x K|V ({el:.1f} s of fp64 CPU work, one thread), scaled to the "
+                      "whole workload by useful flops"}
+
+
 def run_kvx(args):
     import torch
     from cross_model_kv_transfer_gb300 import kvx
@@ -899,7 +1077,17 @@ def run_reference(args):
     if rank != 0:
         return
     f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
-    if args.op == "ridge_fit":
+    if args.op == "layer_scores":
+        wl = W.WORKLOADS[args.workload].with_tokens([args.score_tokens], [0])
+        m = 512
+        kw, f = score_sample(wl, m)
+        run = lambda: oracle.layer_scores(**kw)
+        full = score_flops(wl.src_layers, wl.tgt_layers, wl.kv_heads, wl.head_dim, wl.k, wl.ntok)
+        scale, units = full / f, float(wl.ntok)
+        metric, unit, config = SCORE_METRIC, "tokens/s", score_config(wl, wl.ntok)
+        sample = (f"{m} tokens x all {wl.src_layers} source layers x 2 target layers x 1 head "
+                  "x K|V per step, scaled to the whole workload by useful flops")
+    elif args.op == "ridge_fit":
         wl = W.WORKLOADS[args.workload]
         m = 256
         x, y = W.make_ridge_inputs(wl, 1, m, "cpu")
@@ -980,6 +1168,8 @@ def main(argv=None):
         run_reference(args)
     elif args.op == "ridge_fit":
         run_ridge(args)
+    elif args.op == "layer_scores":
+        run_scores(args)
     else:
         run_kvx(args)
 

@@ -40,6 +40,8 @@ Value recipe:
 * W ~ N(0, 1/(k d)) stored fp32; b ~ N(0, 0.01^2) stored fp32 (tiny) or bf16.
 * the layer-index table draws, for each target layer, k distinct source
   layers uniformly without replacement.
+* paired calibration caches for layer-selection scoring: see
+  ``make_score_inputs``.
 """
 from __future__ import annotations
 
@@ -316,6 +318,74 @@ def make_ridge_inputs(wl: Workload, batch: int, n: int, device="cpu",
                    0.1 * torch.randn((n, q), generator=g, device=dev))
         x[i].copy_(xi)
     return x, y
+
+
+def make_score_inputs(wl: Workload, device="cpu", seed: Optional[int] = None) -> dict:
+    """Stand-in for the paired calibration caches layer selection scores:
+    the pilot's and the target model's caches of the same tokens
+    (``wl.seqlens`` requests, positions 0 .. len - 1 in each).
+
+    Source content: as ``make_inputs`` (N(0, 1) times a per-(layer, head,
+    channel) log-normal scale, outlier channels where the workload has them).
+    Target content of layer lt, head h, K|V: the content of its k planted
+    source layers ``layer_idx[lt]`` (drawn as in ``make_inputs``) through
+    seeded N(0, 1/(k d)) maps, plus N(0, 0.5^2) noise per channel times a
+    per-(layer, head, channel) log-normal (sigma = 0.5) scale.  Keys are
+    stored turned by each model's own RoPE (theta_src, theta_tgt) at the
+    token's position, angles in fp64; values as drawn.  Returns src_k, src_v
+    [Ls][ntok][H][d], tgt_k, tgt_v [Lt][ntok][H][d] (kv dtype), layer_idx
+    int32 [Lt][k] and cu_seqlens int32 [R+1]."""
+    seed = (wl.seed if seed is None else seed) + 7000003
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    gc = _gen("cpu", seed + 1)
+    Ls, Lt, H, d, k = wl.src_layers, wl.tgt_layers, wl.kv_heads, wl.head_dim, wl.k
+    T, half = wl.ntok, wl.head_dim // 2
+    pos = torch.cat([torch.arange(n, dtype=torch.float64) for n in wl.seqlens]).to(dev)
+
+    def turned(x, theta):
+        freq = theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / d)
+        phi = pos[:, None] * freq.to(dev)[None, :]
+        c = torch.cos(phi).to(torch.float32)[:, None, :]
+        s = torch.sin(phi).to(torch.float32)[:, None, :]
+        x0, x1 = x[..., :half], x[..., half:]
+        return torch.cat((x0 * c - x1 * s, x0 * s + x1 * c), dim=-1)
+
+    content = torch.empty((2, Ls, T, H, d), dtype=torch.float32, device=dev)
+    for s in range(Ls):
+        for m in range(2):
+            scale = torch.exp(torch.randn((1, H, d), generator=g, device=dev))
+            if wl.outliers:
+                for h in range(H):
+                    ch = torch.randperm(d, generator=gc)[: wl.outliers].to(dev)
+                    scale[0, h, ch] *= 10.0
+            content[m, s] = torch.randn((T, H, d), generator=g, device=dev) * scale
+    layer_idx = torch.stack([torch.randperm(Ls, generator=gc)[:k] for _ in range(Lt)])
+    out = {}
+    for m, name, theta, L in ((0, "src_k", wl.theta_src, Ls), (1, "src_v", 0, Ls)):
+        t = torch.empty((L, T, H, d), dtype=wl.kv_dtype, device=dev)
+        for s in range(L):
+            t[s] = (turned(content[m, s], theta) if m == 0 else content[m, s]).to(wl.kv_dtype)
+        out[name] = t
+    std = 1.0 / math.sqrt(k * d)
+    for m, name in ((0, "tgt_k"), (1, "tgt_v")):
+        t = torch.empty((Lt, T, H, d), dtype=wl.kv_dtype, device=dev)
+        for lt in range(Lt):
+            y = 0.5 * torch.randn((T, H, d), generator=g, device=dev) * \
+                torch.exp(0.5 * torch.randn((1, H, d), generator=g, device=dev))
+            for s in layer_idx[lt].tolist():
+                a = torch.randn((H, d, d), generator=g, device=dev) * std
+                y += torch.einsum("thi,hij->thj", content[m, s], a)
+            t[lt] = (turned(y, wl.theta_tgt) if m == 0 else y).to(wl.kv_dtype)
+            del y
+        out[name] = t
+    del content
+    lens = torch.tensor(wl.seqlens, dtype=torch.int64)
+    cu = torch.zeros(wl.num_requests + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lens, 0)
+    out["layer_idx"] = layer_idx.to(torch.int32).to(dev)
+    out["cu_seqlens"] = cu.to(torch.int32).to(dev)
+    return out
 
 
 def make_block_table(wl: Workload, seed: int) -> torch.Tensor:
