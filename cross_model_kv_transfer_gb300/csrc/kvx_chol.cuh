@@ -2,8 +2,13 @@
 // by 64, shared by the ridge fit (kvx_ridge.cu) and the layer-selection
 // scores (kvx_scores.cu).  G is [batch][p][p] fp64 in global memory holding
 // the upper triangle of a symmetric matrix; after chol_factor it holds L in
-// its lower triangle and L^T in its upper one.  A fit whose pivot is not
-// positive gets G[0] = NaN and KVX_FLAG_NOT_SPD in *status.
+// its lower triangle and L^T in its upper one.  Right-looking: per diagonal
+// block, factor it (one CTA per fit), solve the panel below it (one CTA per
+// block row) and update the trailing lower triangle (one CTA per 64 x 64
+// block), so that the update, most of the work, is spread over the GPU.  A
+// fit whose pivot is not positive gets G[0] = NaN (later steps skip it) and
+// KVX_FLAG_NOT_SPD in *status.  chol_solve_cols then solves columns against
+// the factor.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -174,6 +179,60 @@ __global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ G
 }
 
 // Launch the whole factorisation (4 + 3 (p / 64 rounded up) - 1 launches).
+constexpr int kSolveThreads = 128;   // threads per CTA of the column solves
+
+// Columns one CTA of a triangular solve holds in shared memory: the largest
+// power of two <= 32 with p x nc <= 4096 doubles (32 KB).
+inline int solve_cols_per_cta(int p) {
+  int nc = 32;
+  while (nc > 1 && (int64_t)p * nc > 4096) nc >>= 1;
+  return nc;
+}
+inline size_t solve_smem_bytes(int p, int nc) { return ((size_t)p * nc + p) * sizeof(double); }
+
+// Forward L z = c, then back L^T w = z, in fp64, for the nc columns a CTA of
+// kSolveThreads threads holds in shared memory (col[i * nc + j] is row i of
+// column j; rd is p doubles of scratch), where A is a factor left by
+// chol_factor.  Right-looking: once z_k = c_k / L_kk is known every later
+// row takes c_i -= L_ik z_k (L_ik = A[k][i], row k of the upper triangle,
+// contiguous), and the back solve does the same from the bottom with row i
+// of the lower triangle.  Thread t works on column t % nc and, in each
+// update, on the rows congruent to t / nc modulo kSolveThreads / nc, so that
+// the fp64 pipe sees many independent multiply-adds per step; one barrier
+// ends each step.  The pivots' reciprocals are taken once, so a step costs a
+// multiply, not a division.  On return col holds w, and the threads t < nc
+// hold |z|^2 and |w|^2 of column t (0 in the other threads).
+__device__ inline void chol_solve_cols(const double *__restrict__ A, int p, double *col,
+                                       double *rd, int nc, double &zn, double &wn) {
+  const int t = threadIdx.x, rpc = kSolveThreads / nc, cl = t % nc, r0 = t / nc;
+  for (int i = t; i < p; i += kSolveThreads) rd[i] = 1.0 / A[(int64_t)i * p + i];
+  zn = 0.0;
+  wn = 0.0;
+  __syncthreads();
+  // row k is final once step k - 1 has ended and is not written in step k
+  for (int k = 0; k < p; ++k) {
+    const double *lk = A + (int64_t)k * p;
+    const double zk = col[k * nc + cl] * rd[k];
+    if (r0 == 0) zn = fma(zk, zk, zn);
+#pragma unroll 4
+    for (int i = k + 1 + r0; i < p; i += rpc)
+      col[i * nc + cl] = fma(-__ldg(lk + i), zk, col[i * nc + cl]);
+    __syncthreads();
+  }
+  for (int e = t; e < p * nc; e += kSolveThreads) col[e] *= rd[e / nc];   // col = z
+  __syncthreads();
+  for (int i = p - 1; i >= 0; --i) {
+    const double *li = A + (int64_t)i * p;
+    const double wi = col[i * nc + cl] * rd[i];
+    if (r0 == 0) wn = fma(wi, wi, wn);
+#pragma unroll 4
+    for (int m = r0; m < i; m += rpc) col[m * nc + cl] = fma(-__ldg(li + m), wi, col[m * nc + cl]);
+    __syncthreads();
+  }
+  for (int e = t; e < p * nc; e += kSolveThreads) col[e] *= rd[e / nc];   // col = w
+  __syncthreads();
+}
+
 inline cudaError_t chol_factor(double *G, int batch, int p, double lam, uint32_t *status,
                                cudaStream_t s) {
   const int nblk = (p + kB - 1) / kB;

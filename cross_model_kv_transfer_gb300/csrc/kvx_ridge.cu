@@ -19,9 +19,10 @@
 //   4. G + lam I mirrored to full, then a Cholesky factorisation in fp64
 //      blocked by 64 (per diagonal block: factor it, solve the panel below,
 //      update the trailing blocks, each step spread over CTAs);
-//   5. per (fit, up to 8 output columns), one CTA: forward and back
-//      substitution in fp64 (one warp per column, the column in shared
-//      memory), b = ybar - xbar W; W and b stored as fp32.  A non-positive
+//   5. per (fit, nc output columns), one CTA: forward and back
+//      substitution in fp64 (the columns in shared memory, the threads
+//      split over the columns and the rows of each right-looking update),
+//      b = ybar - xbar W; W and b stored as fp32.  A non-positive
 //      pivot leaves W and b NaN and sets KVX_FLAG_NOT_SPD.
 // The contraction is a dense Gram product, but it runs on the CUDA cores in
 // fp32: bf16 or tf32 tensor-core operands would round the centred features
@@ -330,70 +331,39 @@ __global__ void __launch_bounds__(256) gram_async_kernel(const float *__restrict
     }
 }
 
-// ---------------------------------------------------------------------------
-// fp64 Cholesky, blocked by 64 (right-looking): for each diagonal block kb,
-// factor it (one CTA per fit), solve the panel below it (one CTA per block
-// row), and update the trailing lower triangle (one CTA per 64 x 64 block).
-// The fp64 pipe of one SM is the limit of a one-CTA factorisation; the
-// blocked form spreads the update, which is most of the work, over the GPU.
-// A fit that meets a non-positive pivot is marked by a NaN in A[0][0]
-// (later steps of that fit do nothing) and sets KVX_FLAG_NOT_SPD.
-// ---------------------------------------------------------------------------
-// Per (fit, group of output columns): forward L Z = C and back L^T W = Z in
-// fp64, one warp per column, the column kept in shared memory (the lanes
-// split each dot product over a row of L, or of L^T from the upper triangle,
-// read coalesced from global memory);
-// then b = ybar - xbar W.  W and b are stored as fp32 (NaN for a failed
-// fit).
-__global__ void __launch_bounds__(256) trsm_kernel(const double *__restrict__ G,
-                                                   double *__restrict__ C,
-                                                   const double *__restrict__ sums, int64_t n,
-                                                   int p, int q, int cols_per_cta,
-                                                   float *__restrict__ W,
-                                                   float *__restrict__ bias) {
-  extern __shared__ double zs[];   // [cols_per_cta][p]
+// Per (fit, nc output columns): forward L Z = C and back L^T W = Z in fp64
+// (chol_solve_cols: the columns in shared memory, right-looking updates with
+// the threads split over columns and rows), then b = ybar - xbar W.  W and b
+// are stored as fp32 (NaN for a failed fit).
+__global__ void __launch_bounds__(kSolveThreads) trsm_kernel(
+    const double *__restrict__ G, const double *__restrict__ C, const double *__restrict__ sums,
+    int64_t n, int p, int q, int nc, float *__restrict__ W, float *__restrict__ bias) {
+  extern __shared__ double cols[];   // [p][nc], then p reciprocals
   const int b = blockIdx.x;
   const double *A = G + (int64_t)b * p * p;
-  double *Z = C + (int64_t)b * p * q;
+  const double *Z = C + (int64_t)b * p * q;
   const double *mx = sums + (int64_t)b * (p + q);
   const double inv_n = 1.0 / (double)n;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.y * cols_per_cta + warp;
-  if (warp >= cols_per_cta || c >= q) return;
-  double *z = zs + (size_t)warp * p;
+  const int t = threadIdx.x, c0 = blockIdx.y * nc;
   if (isnan(A[0])) {
-    for (int i = lane; i < p; i += 32) W[((int64_t)b * p + i) * q + c] = nanf("");
-    if (lane == 0) bias[(int64_t)b * q + c] = nanf("");
+    for (int e = t; e < p * nc; e += kSolveThreads)
+      if (c0 + e % nc < q) W[((int64_t)b * p + e / nc) * q + c0 + e % nc] = nanf("");
+    if (t < nc && c0 + t < q) bias[(int64_t)b * q + c0 + t] = nanf("");
     return;
   }
-  for (int i = lane; i < p; i += 32) z[i] = Z[(int64_t)i * q + c];
-  __syncwarp();
-  for (int i = 0; i < p; ++i) {
-    const double *ri = A + (int64_t)i * p;
+  for (int e = t; e < p * nc; e += kSolveThreads) {
+    const int i = e / nc, j = e % nc;
+    cols[e] = c0 + j < q ? Z[(int64_t)i * q + c0 + j] : 0.0;
+  }
+  double zn, wn;
+  chol_solve_cols(A, p, cols, cols + (size_t)p * nc, nc, zn, wn);
+  for (int e = t; e < p * nc; e += kSolveThreads)
+    if (c0 + e % nc < q) W[((int64_t)b * p + e / nc) * q + c0 + e % nc] = (float)cols[e];
+  if (t < nc && c0 + t < q) {
     double s = 0.0;
-    for (int m = lane; m < i; m += 32) s = fma(ri[m], z[m], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) z[i] = (z[i] - s) / ri[i];
-    __syncwarp();
+    for (int i = 0; i < p; ++i) s = fma(mx[i] * inv_n, cols[i * nc + t], s);
+    bias[(int64_t)b * q + c0 + t] = (float)(mx[p + c0 + t] * inv_n - s);
   }
-  for (int i = p - 1; i >= 0; --i) {
-    const double *ri = A + (int64_t)i * p;           // row i of L^T (upper triangle)
-    double s = 0.0;
-    for (int m = i + 1 + lane; m < p; m += 32) s = fma(ri[m], z[m], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) z[i] = (z[i] - s) / ri[i];
-    __syncwarp();
-  }
-  double s = 0.0;
-  for (int i = lane; i < p; i += 32) {
-    W[((int64_t)b * p + i) * q + c] = (float)z[i];
-    s = fma(mx[i] * inv_n, z[i], s);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) bias[(int64_t)b * q + c] = (float)(mx[p + c] * inv_n - s);
 }
 
 constexpr int kMaxDim = 4096;
@@ -463,13 +433,14 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
   // blocked fp64 Cholesky
   if (chol_factor(G, batch, p, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
-  // triangular solves: one warp per output column, columns in shared memory
-  const int cols = (int)(48 * 1024 / ((size_t)p * sizeof(double))) < 8
-                       ? (int)(48 * 1024 / ((size_t)p * sizeof(double)))
-                       : 8;
-  const int cpc = cols < 1 ? 1 : cols;
-  dim3 tgrid((unsigned)batch, (unsigned)((q + cpc - 1) / cpc));
-  trsm_kernel<<<tgrid, cpc * 32, (size_t)cpc * p * sizeof(double), s>>>(G, C, sums, n, p, q, cpc,
-                                                                          a->w, a->b);
+  // triangular solves: nc output columns per CTA, in shared memory
+  const int nc = solve_cols_per_cta(p);
+  if (solve_smem_bytes(p, nc) > 48 * 1024 &&
+      cudaFuncSetAttribute(trsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)solve_smem_bytes(p, nc)) != cudaSuccess)
+    return KVX_ERR_CUDA;
+  dim3 tgrid((unsigned)batch, (unsigned)((q + nc - 1) / nc));
+  trsm_kernel<<<tgrid, kSolveThreads, solve_smem_bytes(p, nc), s>>>(G, C, sums, n, p, q, nc,
+                                                                    a->w, a->b);
   return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }

@@ -355,52 +355,27 @@ __global__ void __launch_bounds__(256) gram_kernel(
     }
 }
 
-// 4. Per (fit b, group of columns): forward L z = c and back L^T w = z in
-// fp64, one warp per column (the column in shared memory), then |z|^2 and
-// |w|^2 added into zz / ww [b][column / d] (the target layer of the column
-// for the per-layer fits, the single output group for the sets).
-__global__ void __launch_bounds__(256) solve_norms_kernel(const double *__restrict__ G,
-                                                          const double *__restrict__ C, int p,
-                                                          int q, int d, int cols_per_cta,
-                                                          double *__restrict__ zz,
-                                                          double *__restrict__ ww, int groups) {
-  extern __shared__ double zs[];   // [cols_per_cta][p]
+// 4. Per (fit b, nc columns): forward L z = c and back L^T w = z in fp64
+// (chol_solve_cols), then |z|^2 and |w|^2 added into zz / ww
+// [b][column / d] (the target layer of the column for the per-layer fits,
+// the single output group for the sets).
+__global__ void __launch_bounds__(kSolveThreads) solve_norms_kernel(
+    const double *__restrict__ G, const double *__restrict__ C, int p, int q, int d, int nc,
+    double *__restrict__ zz, double *__restrict__ ww, int groups) {
+  extern __shared__ double cols[];   // [p][nc], then p reciprocals
   const int b = blockIdx.x;
   const double *A = G + (int64_t)b * p * p;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = blockIdx.y * cols_per_cta + warp;
-  if (warp >= cols_per_cta || c >= q) return;
   if (isnan(A[0])) return;    // not positive definite: the scores stay NaN
-  double *z = zs + (size_t)warp * p;
-  for (int i = lane; i < p; i += 32) z[i] = C[((int64_t)b * p + i) * q + c];
-  __syncwarp();
-  double zn = 0.0;
-  for (int i = 0; i < p; ++i) {
-    const double *ri = A + (int64_t)i * p;
-    double s = 0.0;
-    for (int m = lane; m < i; m += 32) s = fma(ri[m], z[m], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) {
-      z[i] = (z[i] - s) / ri[i];
-      zn = fma(z[i], z[i], zn);
-    }
-    __syncwarp();
+  const int c0 = blockIdx.y * nc;
+  const double *src = C + (int64_t)b * p * q;
+  for (int e = threadIdx.x; e < p * nc; e += kSolveThreads) {
+    const int i = e / nc, j = e % nc;
+    cols[e] = c0 + j < q ? src[(int64_t)i * q + c0 + j] : 0.0;
   }
-  double wn = 0.0;
-  for (int i = p - 1; i >= 0; --i) {
-    const double *ri = A + (int64_t)i * p;           // row i of L^T
-    double s = 0.0;
-    for (int m = i + 1 + lane; m < p; m += 32) s = fma(ri[m], z[m], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) {
-      z[i] = (z[i] - s) / ri[i];
-      wn = fma(z[i], z[i], wn);
-    }
-    __syncwarp();
-  }
-  if (lane == 0) {
+  double zn, wn;
+  chol_solve_cols(A, p, cols, cols + (size_t)p * nc, nc, zn, wn);
+  const int c = c0 + threadIdx.x;
+  if (threadIdx.x < nc && c < q) {
     const int grp = groups > 1 ? c / d : 0;
     atomicAdd(zz + (int64_t)b * groups + grp, zn);
     atomicAdd(ww + (int64_t)b * groups + grp, wn);
@@ -537,8 +512,7 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   const int64_t clear_words = (int64_t)(lay.bad - lay.xs) / 8;
   const int per_tok = D / 16, tpb = 256 / per_tok;
   dim3 cgrid((unsigned)((n + tpb - 1) / tpb), (unsigned)(Ls + Lt));
-  const int cols1 = (int)(48 * 1024 / ((size_t)D * 8)) < 8 ? (int)(48 * 1024 / ((size_t)D * 8)) : 8;
-  const int colsk = (int)(48 * 1024 / ((size_t)pk * 8)) < 8 ? (int)(48 * 1024 / ((size_t)pk * 8)) : 8;
+  const int cols1 = solve_cols_per_cta(D), colsk = solve_cols_per_cta(pk);
   for (int h = 0; h < H; ++h) {
     for (int m = 0; m < 2; ++m) {
       clear_kernel<<<1024, 256, 0, s>>>(clear_from, clear_words);
@@ -560,9 +534,9 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
                     256, 0, s>>>(ps.X, ps.Y, ps.xs, ps.ys, ident, 1, D, Lt, n, q1, 0, 0, ps.G,
                                  ps.C, tiles_d, tiles_q1);
       if (chol_factor(ps.G, Ls, D, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
-      solve_norms_kernel<<<dim3((unsigned)Ls, (unsigned)((q1 + cols1 - 1) / cols1)), cols1 * 32,
-                           (size_t)cols1 * D * 8, s>>>(ps.G, ps.C, D, q1, D, cols1, ps.zz, ps.ww,
-                                                       Lt);
+      solve_norms_kernel<<<dim3((unsigned)Ls, (unsigned)((q1 + cols1 - 1) / cols1)), kSolveThreads,
+                           solve_smem_bytes(D, cols1), s>>>(ps.G, ps.C, D, q1, D, cols1, ps.zz,
+                                                            ps.ww, Lt);
       if (sets) {
         // set fits: batch lt, features = the row's k layers, targets = lt
         gram_kernel<<<dim3((unsigned)(tiles_pk * (tiles_pk + 1) / 2 + tiles_pk * tiles_d),
@@ -571,9 +545,9 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
                                    ps.Gs, ps.Cs, tiles_pk, tiles_d);
         if (chol_factor(ps.Gs, Lt, pk, a->lambda, a->status, s) != cudaSuccess)
           return KVX_ERR_CUDA;
-        solve_norms_kernel<<<dim3((unsigned)Lt, (unsigned)((D + colsk - 1) / colsk)), colsk * 32,
-                             (size_t)colsk * pk * 8, s>>>(ps.Gs, ps.Cs, pk, D, D, colsk, ps.zzs,
-                                                          ps.wws, 1);
+        solve_norms_kernel<<<dim3((unsigned)Lt, (unsigned)((D + colsk - 1) / colsk)),
+                             kSolveThreads, solve_smem_bytes(pk, colsk), s>>>(
+            ps.Gs, ps.Cs, pk, D, D, colsk, ps.zzs, ps.wws, 1);
       }
       finalize_kernel<<<(Ls * Lt + 255) / 256 + 1, 256, 0, s>>>(
           ps, Ls, Lt, H, D, h, m, n, a->lambda, a->r2, a->r2_set, a->layer_idx, k, a->status);

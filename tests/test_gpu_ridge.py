@@ -127,3 +127,25 @@ def test_host_rejects_a_small_workspace():
     ws = torch.empty(need - 8, dtype=torch.uint8, device="cuda")
     with pytest.raises(kvx.KvxError):
         kvx.ridge_fit(x, y, workspace=ws)
+
+
+def test_ridge_fit_wide_feature_block_solves_in_large_shared_memory():
+    # p = 3,100 features: one output column per solve CTA, whose columns and
+    # pivot reciprocals take more than 48 KB of shared memory.  The fp64
+    # reference here is the normal equations solved by LAPACK on the same
+    # observations (a plain library solve of the ridge problem).
+    x, y = _data(1, 6500, 3100, 3, seed=23, spread=0.2)
+    w, b = kvx.ridge_fit(x, y, lam=0.01)
+    torch.cuda.synchronize()
+    xs, ys = x[0].double().cpu().numpy(), y[0].double().cpu().numpy()
+    xm, ym = xs.mean(axis=0), ys.mean(axis=0)
+    xc, yc = xs - xm, ys - ym
+    g = xc.T @ xc + 0.01 * np.eye(xs.shape[1])
+    wr = np.linalg.solve(g, xc.T @ yc)
+    br = ym - xm @ wr
+    kappa = np.linalg.cond(g)
+    wg, bg = w[0].double().cpu().numpy(), b[0].double().cpu().numpy()
+    assert np.linalg.norm(wg - wr) / np.linalg.norm(wr) <= max(1e-5, 1e-6 * kappa)
+    assert np.linalg.norm(bg - br) / np.linalg.norm(br) <= max(1e-5, 1e-6 * kappa)
+    pg, pr = xs @ wg + bg, xs @ wr + br
+    assert np.linalg.norm(pg - pr) / np.linalg.norm(pr) <= 1e-5
