@@ -33,12 +33,14 @@
 //     fp32 accumulators; tcgen05.commit frees A slots and W chunks and hands
 //     finished accumulators to the epilogue.
 //   * 8 epilogue warps (two per lane quadrant, 16 rows each): tcgen05.ld of
-//     the 16x256b shape gives each thread two rows and, thanks to the W
-//     image's column order, 16 whole RoPE pairs (channels 16q..16q+15 and
-//     their partners 64 + 16q.., q = lane % 4); the accumulator is released
-//     as soon as it is in registers.  Then + b, re-rotation of keys into the
-//     target RoPE at p' (step 3), bf16 cast, and 32-byte stores in which the
-//     four threads of a row write one whole 128-byte line.
+//     the 16x256b shape, one 64-column half at a time, gives each thread two
+//     rows and, thanks to the W image's column order, 8 whole RoPE pairs per
+//     half (channels 32H + 8q .. 32H + 8q + 7 and their partners at +64,
+//     q = lane % 4); the accumulator is released as soon as the second half
+//     is in registers.  Then + b, re-rotation of keys into the target RoPE at
+//     p' (step 3), bf16 cast, and 16-byte stores: per half, the four threads
+//     of a row write 64 consecutive bytes of the row's first 64 channels and
+//     64 of its last 64.
 // Every mbarrier wait is bounded: after 2 s without progress the CTA sets
 // KVX_FLAG_TIMEOUT, all roles leave their loops, in-flight copies and MMAs
 // are drained (again with bounded waits) and tensor memory is freed.

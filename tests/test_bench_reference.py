@@ -21,6 +21,7 @@ MODES = {
     "paged_source": ["--src-block-size", "16"],
     "kv_diagnostics": ["--op", "kv_diagnostics"],
     "ridge_fit": ["--op", "ridge_fit"],
+    "layer_scores": ["--op", "layer_scores"],
     "small_override": ["--tokens", "4096", "--tgt-layers", "8"],
 }
 
@@ -48,6 +49,10 @@ def test_reference_line_matches_the_gpu_arm_contract(mode):
         wl = WORKLOADS[args.workload]
         metric, unit = bench.RIDGE_METRIC, "fits/s"
         config = bench.ridge_config(wl, args.ridge_batch, args.ridge_n)
+    elif args.op == "layer_scores":
+        wl = WORKLOADS[args.workload].with_tokens([args.score_tokens], [0])
+        metric, unit = bench.SCORE_METRIC, "tokens/s"
+        config = bench.score_config(wl, args.score_tokens)
     elif args.op == "kv_diagnostics":
         wl = bench.select_workload(args)
         metric, unit, config = bench.DIAG_METRIC, "tokens/s", bench.diag_config(wl)
