@@ -339,14 +339,17 @@ typedef struct {
   const void *y;            /* [batch][n][q] targets                          */
   float *w;                 /* [batch][p][q] output: the map                  */
   float *b;                 /* [batch][q] output: the bias                    */
-  void *workspace;          /* scratch of at least kvx_ridge_workspace_bytes() */
+  void *workspace;          /* scratch of at least kvx_ridge_workspace_bytes(),
+                               16-byte aligned                                */
   size_t workspace_bytes;
   uint32_t *status;         /* optional device word, KVX_FLAG_NOT_SPD OR-ed in */
 } kvx_ridge_args;
 
-/* Bytes of scratch a kvx_ridge_fit call with these sizes needs (fp64 column
- * sums, Gram blocks and cross products: 8 * batch * (p + q + p*p + p*q),
- * rounded up), or 0 for sizes outside the limits above. */
+/* Bytes of scratch a kvx_ridge_fit call with these sizes needs: fp64 column
+ * sums, Gram blocks and cross products (8 * batch * (p + q + p*p + p*q),
+ * each part rounded up to 256 bytes) and the split-precision planes of one
+ * chunk of 16,384 observations (2 * 4 * batch * (p + q) * 16384 bytes); 0 for
+ * sizes outside the limits above. */
 size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
 
 /* Fit the maps: for each fit, W = (XcT Xc + lambda I)^-1 XcT Yc and
@@ -358,14 +361,16 @@ size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
  * lambda I unscaled (0.01 there).  A batch ordered (target layer, head, K|V)
  * with p = k*d and q = d writes W and b in exactly the layouts kvx_transfer
  * reads for a per-head plan with fp32 W and b.  The centred Gram blocks are
- * formed from fp32 products (fp32 partial sums over 256 observations, summed
- * in fp32 over slices of 16,384, slices added in fp64), the Cholesky
- * factorisation and both triangular solves run in fp64, W and b are stored as
- * fp32; the factorisation is blocked by 64 and spread over CTAs.
- * Asynchronous on `stream`; no allocation (the caller passes the scratch);
- * 4 + 3 ceil(p / 64) - 1 kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL pointer,
- * sizes outside the limits, a non-finite lambda or a workspace that is too
- * small; KVX_ERR_CUDA if a launch fails.  A fit whose matrix is not positive
+ * formed on the tensor cores with each centred fp32 value split into two tf32
+ * values (products hi*hi + hi*lo + lo*hi, about 22 significant bits; fp32
+ * partial sums over 256 observations, summed in fp32 over slices of 4,096,
+ * slices added in fp64), the Cholesky factorisation and both triangular
+ * solves run in fp64, W and b are stored as fp32; the factorisation is
+ * blocked by 64 and spread over CTAs.  Asynchronous on `stream`; no
+ * allocation (the caller passes the scratch); 3 + 2 ceil(n / 16384) +
+ * 3 ceil(p / 64) - 1 kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL
+ * pointer, sizes outside the limits, a non-finite lambda, or a workspace that
+ * is too small or not 16-byte aligned; KVX_ERR_CUDA if a launch fails.  A fit whose matrix is not positive
  * definite gets NaN W and b and sets KVX_FLAG_NOT_SPD. */
 kvx_status kvx_ridge_fit(const kvx_ridge_args *args, void *stream);
 
