@@ -526,7 +526,7 @@ def run_ridge(args):
                    "l2": f"inputs larger than L2 ({(x.numel() + y.numel()) * 4 / 1e9:.2f} GB "
                          "read per step, no flush needed)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": (4 + 3 * ((p + 63) // 64) - 1) * args.steps,
+        "gpu_launches": (3 + 2 * ((n + 16383) // 16384) + 3 * ((p + 63) // 64) - 1) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -554,14 +554,17 @@ def score_flops(Ls, Lt, H, d, k, n) -> float:
     return 2.0 * n * per * 2 * H
 
 
-def score_launches(Ls, Lt, H, d, k, sets=True) -> int:
-    """Kernels one kvx_layer_scores call launches: three table checks, then
-    per (head, K|V) clear, content, Gram, Cholesky (prep + per 64-column
-    block: diagonal, panel, update), solve, the set fits' Gram, Cholesky and
-    solve, and the final ratios."""
+def score_launches(Ls, Lt, H, d, k, n, sets=True) -> int:
+    """Kernels one kvx_layer_scores call launches: the request-table check,
+    with a table the clamped table and the row check, then per (head, K|V)
+    clear, content, per chunk of 16,384 tokens the split and the tensor-core
+    moments, the Cholesky (prep + per 64-column block: diagonal, panel,
+    update) and solve of the per-layer fits, those of the set fits, and the
+    final ratios."""
     chol = lambda p: 1 + 3 * ((p + 63) // 64) - 2
-    per = 3 + chol(d) + 1 + (2 + chol(k * d) if sets else 0) + 1
-    return 2 + (1 if sets else 0) + H * 2 * per
+    chunks = (n + 16383) // 16384
+    per = 2 + 2 * chunks + chol(d) + 1 + (chol(k * d) + 1 if sets else 0) + 1
+    return 1 + (2 if sets else 0) + H * 2 * per
 
 
 def run_scores(args):
@@ -662,7 +665,7 @@ def run_scores(args):
                    "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of caches read per "
                          "step, no flush needed)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": score_launches(Ls, Lt, H, d, k) * args.steps,
+        "gpu_launches": score_launches(Ls, Lt, H, d, k, n) * args.steps,
         "clocks": clk.summary(),
         "mean_best_single_layer_r2": [float(x) for x in
                                       r2.max(dim=1).values.mean(dim=(0, 1)).cpu()],

@@ -17,13 +17,16 @@
 // Per (head, K|V) one pass of launches:
 //   1. content features (keys un-rotated at the token's position with each
 //      model's base, values as stored) of every source and target layer,
-//      fp32, with fp64 column sums and the targets' sums of squares;
-//   2. centred Gram blocks G (upper triangle) and cross blocks C: fp32
-//      products in register tiles, fp32 partial sums over 256 tokens, slices
-//      of tokens added in fp64 with atomics; one batch per source layer (G
-//      of that layer, C against every target layer at once), and with a
-//      layer table one batch per target layer (its row's layers gathered as
-//      the features, C against that target layer);
+//      fp32 [Ls + Lt][n][d], with fp64 column sums and the targets' sums of
+//      squares;
+//   2. per chunk of 16,384 tokens: the centred features split into tf32 hi
+//      and lo planes (kvx_moments.cuh), then on the tensor cores (products
+//      hi*hi + hi*lo + lo*hi) the centred Gram blocks G of every source layer
+//      and its cross blocks C against every target layer's columns, and with
+//      a layer table the Gram blocks of each row's set (its layers gathered
+//      as 128-row blocks) and their cross blocks against that target layer;
+//      fp32 partial sums over 256 tokens, summed in fp32 per slice of 4,096,
+//      added in fp64;
 //   3. fp64 Cholesky of G + lam I, blocked by 64 (kvx_chol.cuh);
 //   4. fp64 forward and back substitution per column, keeping only the
 //      column's |z|^2 and |w|^2, summed per target layer;
@@ -35,14 +38,11 @@
 #include <cmath>
 
 #include "kvx_chol.cuh"
+#include "kvx_moments.cuh"
 #include "kvx_internal.h"
 
 namespace {
 
-constexpr int kTile = 64;              // Gram tile
-constexpr int kChunkObs = 32;          // tokens staged per step
-constexpr int kFlushObs = 256;         // fp32 partials flushed this often
-constexpr int64_t kRowsPerSlice = 8192;  // tokens per CTA of the Gram kernel
 constexpr int kMaxD = 128;
 constexpr int kMaxK = 8;
 
@@ -56,9 +56,9 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return _
 // Per-pass scratch (one head h and one of K|V), carved from the caller's
 // workspace.
 struct Pass {
-  float *X;          // [Ls][n][d] source content
-  float *Y;          // [n][Lt][d] target content (all target layers per token)
-  double *xs;        // [Ls][d] column sums
+  float *X;          // [Ls + Lt][n][d] content: source layers, then target layers
+  float *planes;     // [2][(Ls + Lt) d][np] tf32 hi and lo of one chunk
+  double *xs;        // [Ls][d] column sums (followed by ys)
   double *ys;        // [Lt][d]
   double *yss;       // [Lt] sums of squares
   double *G;         // [Ls][d][d]
@@ -73,17 +73,25 @@ struct Pass {
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t X, Y, xs, ys, yss, G, C, zz, ww, Gs, Cs, zzs, wws, bad, total;
+  size_t X, planes, xs, ys, yss, G, C, zz, ww, Gs, Cs, zzs, wws, bad, total;
 };
+
+// Tokens per plane chunk, padded to the tensor-core block.
+int64_t chunk_np(int64_t n) {
+  const int64_t len = n < kMomChunk ? n : kMomChunk;
+  return (len + kMomKB - 1) / kMomKB * kMomKB;
+}
 
 Layout layout_of(int64_t Ls, int64_t Lt, int64_t d, int64_t k, int64_t n) {
   Layout L;
   size_t at = 0;
   auto take = [&](size_t bytes) { const size_t o = at; at += round256(bytes); return o; };
-  L.X = take((size_t)Ls * n * d * 4);
-  L.Y = take((size_t)n * Lt * d * 4);
-  L.xs = take((size_t)Ls * d * 8);
-  L.ys = take((size_t)Lt * d * 8);
+  L.X = take((size_t)(Ls + Lt) * n * d * 4);
+  L.planes = take((size_t)2 * (Ls + Lt) * d * chunk_np(n) * 4);
+  L.xs = (size_t)at;
+  at += (size_t)Ls * d * 8;                       // xs and ys adjacent: [Ls + Lt][d]
+  L.ys = at;
+  at += round256((size_t)Lt * d * 8);
   L.yss = take((size_t)Lt * 8);
   L.G = take((size_t)Ls * d * d * 8);
   L.C = take((size_t)Ls * d * Lt * d * 8);
@@ -207,8 +215,7 @@ __global__ void __launch_bounds__(256) content_kernel(
         if (status) atomicOr(status, KVX_FLAG_BAD_POSITION);
       }
     }
-    float *out = is_src ? ps.X + ((int64_t)layer * n + g) * d
-                        : ps.Y + (g * Lt + layer) * d;
+    float *out = ps.X + ((int64_t)L * n + g) * d;
     float sq = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -226,134 +233,96 @@ __global__ void __launch_bounds__(256) content_kernel(
   if (!is_src && tid == 0) atomicAdd(ps.yss + layer, (double)sss);
 }
 
-// 2. Centred Gram (upper-triangle tiles) and cross blocks of a batch of
-// fits.  Fit b has p = nsel * d features: feature j * d + i is dim i of
-// source layer xl[b * nsel + j] (content X), and q target columns starting
-// at column y0 + b * y_step of the [n][Lt * d] target content Y.
-__global__ void __launch_bounds__(256) gram_kernel(
-    const float *__restrict__ X, const float *__restrict__ Y, const double *__restrict__ xs,
-    const double *__restrict__ ys, const int32_t *__restrict__ xl, int nsel, int d, int Lt,
-    int64_t n, int q, int y0, int y_step, double *__restrict__ G, double *__restrict__ C,
-    int tiles_p, int tiles_q) {
-  __shared__ float sa[kChunkObs][kTile];
-  __shared__ float sb[kChunkObs][kTile];
-  __shared__ float mean_a[kTile], mean_b[kTile];
-  __shared__ int src_a[kTile];                      // source layer of each a column
-  __shared__ int src_b[kTile];                      // (Gram tiles) of each b column
-  const int b = blockIdx.z;
-  const int p = nsel * d;
-  int ti, tj;
-  {
-    int t = blockIdx.x;
-    const int n_upper = tiles_p * (tiles_p + 1) / 2;
-    if (t < n_upper) {
-      ti = 0;
-      while (t >= tiles_p - ti) {
-        t -= tiles_p - ti;
-        ++ti;
-      }
-      tj = ti + t;
-    } else {
-      t -= n_upper;
-      ti = t / tiles_q;
-      tj = tiles_p + t % tiles_q;
-    }
-  }
-  const bool is_c = tj >= tiles_p;
-  const int i0 = ti * kTile;
-  const int j0 = (is_c ? tj - tiles_p : tj) * kTile;
-  const int ncols = is_c ? q : p;
-  const int ycol0 = y0 + b * y_step;
-  const double inv_n = 1.0 / (double)n;
-  const int tid = threadIdx.x;
-  if (tid < kTile) {
-    const int f = i0 + tid;
-    if (f < p) {
-      const int s = xl[b * nsel + f / d];
-      src_a[tid] = s;
-      mean_a[tid] = (float)(xs[(int64_t)s * d + f % d] * inv_n);
-    } else {
-      src_a[tid] = -1;
-      mean_a[tid] = 0.f;
-    }
-  } else if (tid < 2 * kTile) {
-    const int c = tid - kTile;
-    const int f = j0 + c;
-    if (f < ncols) {
-      if (is_c) {
-        src_b[c] = -1;
-        mean_b[c] = (float)(ys[(int64_t)(ycol0 + f)] * inv_n);   // ys is [Lt][d] = [Lt*d]
-      } else {
-        const int s = xl[b * nsel + f / d];
-        src_b[c] = s;
-        mean_b[c] = (float)(xs[(int64_t)s * d + f % d] * inv_n);
-      }
-    } else {
-      src_b[c] = -2;
-      mean_b[c] = 0.f;
-    }
-  }
-  const int tx = tid & 15, ty = tid >> 4;
-  const int64_t t0 = (int64_t)blockIdx.y * kRowsPerSlice;
-  const int64_t t1 = t0 + kRowsPerSlice < n ? t0 + kRowsPerSlice : n;
-  float acc[4][4], part[4][4];
+// 2. Per chunk [n0, n0 + np): the centred content of plane row f (= layer
+// f / d, dimension f % d, source layers first) as tf32 hi and lo planes,
+// column t - n0 (tokens beyond n are zero); a CTA transposes a 32 x 32 block
+// through shared memory.
+__global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ X,
+                                                    const double *__restrict__ sums, int64_t n,
+                                                    int rows, int d, int64_t n0, int64_t np,
+                                                    float *__restrict__ planes) {
+  __shared__ float blk[32][33];
+  const int f0 = blockIdx.y * 32;
+  const int64_t c0 = (int64_t)blockIdx.x * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int f = f0 + tx;
+  float mean = 0.f;
+  if (f < rows) mean = (float)(sums[f] / (double)n);
+  const float *col = X + (int64_t)(f / d) * n * d + f % d;
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.f, part[r][c] = 0.f;
+  for (int i = 0; i < 4; ++i) {
+    const int r = ty + 8 * i;
+    const int64_t t = n0 + c0 + r;
+    blk[r][tx] = f < rows && t < n ? col[t * d] - mean : 0.f;
+  }
   __syncthreads();
-  int since_flush = 0;
-  const int64_t yrow = (int64_t)Lt * d;
-  for (int64_t t = t0; t < t1; t += kChunkObs) {
-    for (int e = tid; e < kChunkObs * kTile; e += blockDim.x) {
-      const int o = e / kTile, c = e % kTile;
-      const int64_t u = t + o;
-      const bool in = u < t1;
-      const int fa = i0 + c, fb = j0 + c;
-      sa[o][c] = (in && src_a[c] >= 0)
-                     ? X[((int64_t)src_a[c] * n + u) * d + fa % d] - mean_a[c]
-                     : 0.f;
-      float vb = 0.f;
-      if (in && src_b[c] != -2)
-        vb = (is_c ? Y[u * yrow + ycol0 + fb] : X[((int64_t)src_b[c] * n + u) * d + fb % d]) -
-             mean_b[c];
-      sb[o][c] = vb;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int o = 0; o < kChunkObs; ++o) {
-      const float4 a4 = *reinterpret_cast<const float4 *>(&sa[o][4 * ty]);
-      const float4 b4 = *reinterpret_cast<const float4 *>(&sb[o][4 * tx]);
-      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-      const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) part[r][c] = fmaf(av[r], bv[c], part[r][c]);
-    }
-    __syncthreads();
-    since_flush += kChunkObs;
-    if (since_flush >= kFlushObs) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] += part[r][c], part[r][c] = 0.f;
-      since_flush = 0;
-    }
+  for (int i = 0; i < 4; ++i) {
+    const int fr = f0 + ty + 8 * i;
+    if (fr < rows) mom_put(planes, rows, np, fr, c0 + tx, blk[tx][ty + 8 * i]);
   }
-#pragma unroll
-  for (int r = 0; r < 4; ++r)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int i = i0 + 4 * ty + r, j = j0 + 4 * tx + c;
-      if (i >= p || j >= ncols) continue;
-      const double v = (double)acc[r][c] + (double)part[r][c];
-      if (is_c)
-        atomicAdd(C + ((int64_t)b * p + i) * q + j, v);
-      else
-        atomicAdd(G + ((int64_t)b * p + i) * p + j, v);
-    }
 }
+
+// The tensor-core tiles of one pass.  Per source layer s: its Gram block
+// (A = B = layer s) and ceil(Lt d / 128) cross tiles against the target
+// columns.  Per target layer lt (with a table): the Gram blocks (j1 <= j2)
+// of its set, A = layer sets[lt][j1], B = layer sets[lt][j2], and its k cross
+// blocks against layer lt's d columns.  Plane row of layer L, dim i: L d + i
+// (target layer lt is L = Ls + lt).  With d < 128 a block's extra rows are
+// other layers' and are not stored.
+struct ScoreTiles {
+  int Ls, Lt, d, k, nq, layer_tiles;
+  const int32_t *sets;
+  double *G, *C, *Gs, *Cs;
+  __device__ MomTile tile(int t) const {
+    MomTile m;
+    m.m_valid = d;
+    if (t < layer_tiles) {
+      const int s = t / (1 + nq), j = t % (1 + nq);
+      m.a_row = s * d;
+      if (j == 0) {
+        m.b_row = s * d;
+        m.n_split = m.n_valid = d;
+        m.out0 = m.out1 = G + (int64_t)s * d * d;
+        m.ld0 = m.ld1 = d;
+      } else {
+        const int c0 = (j - 1) * kMomRows;
+        m.b_row = Ls * d + c0;
+        m.n_split = 0;
+        m.n_valid = min(kMomRows, Lt * d - c0);
+        m.out0 = m.out1 = C + (int64_t)s * d * Lt * d + c0;
+        m.ld0 = m.ld1 = (int64_t)Lt * d;
+      }
+      return m;
+    }
+    const int pairs = k * (k + 1) / 2, per = pairs + k, p = k * d;
+    int r = t - layer_tiles;
+    const int lt = r / per;
+    r -= lt * per;
+    if (r < pairs) {
+      int j1 = 0;
+      while (r >= k - j1) {
+        r -= k - j1;
+        ++j1;
+      }
+      const int j2 = j1 + r;
+      m.a_row = sets[lt * k + j1] * d;
+      m.b_row = sets[lt * k + j2] * d;
+      m.n_split = m.n_valid = d;
+      m.out0 = m.out1 = Gs + (int64_t)lt * p * p + (int64_t)j1 * d * p + j2 * d;
+      m.ld0 = m.ld1 = p;
+    } else {
+      const int j = r - pairs;
+      m.a_row = sets[lt * k + j] * d;
+      m.b_row = (Ls + lt) * d;
+      m.n_split = 0;
+      m.n_valid = d;
+      m.out0 = m.out1 = Cs + (int64_t)lt * p * d + (int64_t)j * d * d;
+      m.ld0 = m.ld1 = d;
+    }
+    return m;
+  }
+};
 
 // 4. Per (fit b, nc columns): forward L z = c and back L^T w = z in fp64
 // (chol_solve_cols), then |z|^2 and |w|^2 added into zz / ww
@@ -421,12 +390,10 @@ __global__ void check_rows_kernel(const int32_t *idx, int Lt, int k, int Ls, uin
     atomicOr(status, KVX_FLAG_BAD_LAYER_INDEX);
 }
 
-// Identity list 0..Ls-1 for the per-layer fits; the set fits read the
-// table, with out-of-range indices clamped (their scores are NaN anyway).
-__global__ void layer_lists_kernel(int32_t *ident, int Ls, int32_t *sets, const int32_t *idx,
-                                   int n_idx) {
+// The layer table with entries outside [0, Ls) clamped (their rows are
+// flagged and get NaN scores); the tiles read layers through it.
+__global__ void layer_lists_kernel(int32_t *sets, const int32_t *idx, int n_idx, int Ls) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e < Ls) ident[e] = e;
   if (e < n_idx) {
     const int v = idx[e];
     sets[e] = v < 0 ? 0 : (v >= Ls ? Ls - 1 : v);
@@ -439,9 +406,7 @@ bool plan_ok(const kvx_plan_desc &d) {
          (d.kv_dtype == KVX_F32 || d.kv_dtype == KVX_BF16);
 }
 
-size_t lists_bytes(const kvx_plan_desc &d) {
-  return round256((size_t)d.src_layers * 4) + round256((size_t)d.tgt_layers * d.k * 4);
-}
+size_t lists_bytes(const kvx_plan_desc &d) { return round256((size_t)d.tgt_layers * d.k * 4); }
 
 }  // namespace
 
@@ -462,8 +427,8 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
     return KVX_ERR_INVALID_ARG;
   const int64_t n = a->ntok;
   if (a->workspace_bytes < kvx_layer_scores_workspace_bytes(plan, n)) return KVX_ERR_INVALID_ARG;
-  const int64_t slices64 = (n + kRowsPerSlice - 1) / kRowsPerSlice;
-  if (slices64 > 65535 || n > INT32_MAX) return KVX_ERR_INVALID_ARG;
+  if (n > INT32_MAX || (reinterpret_cast<uintptr_t>(a->workspace) & 15u) != 0)
+    return KVX_ERR_INVALID_ARG;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return KVX_ERR_CUDA;
   if (cur != plan->device) return KVX_ERR_INVALID_ARG;
@@ -475,7 +440,7 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   unsigned char *ws = reinterpret_cast<unsigned char *>(a->workspace);
   Pass ps;
   ps.X = reinterpret_cast<float *>(ws + lay.X);
-  ps.Y = reinterpret_cast<float *>(ws + lay.Y);
+  ps.planes = reinterpret_cast<float *>(ws + lay.planes);
   ps.xs = reinterpret_cast<double *>(ws + lay.xs);
   ps.ys = reinterpret_cast<double *>(ws + lay.ys);
   ps.yss = reinterpret_cast<double *>(ws + lay.yss);
@@ -488,8 +453,7 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   ps.zzs = reinterpret_cast<double *>(ws + lay.zzs);
   ps.wws = reinterpret_cast<double *>(ws + lay.wws);
   ps.bad = reinterpret_cast<int *>(ws + lay.bad);
-  int32_t *ident = reinterpret_cast<int32_t *>(ws + lay.total);
-  int32_t *set_list = reinterpret_cast<int32_t *>(ws + lay.total + round256((size_t)Ls * 4));
+  int32_t *set_list = reinterpret_cast<int32_t *>(ws + lay.total);
 
   Turns turns;
   for (int i = 0; i < D / 2; ++i) {
@@ -498,15 +462,17 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   }
   check_table_kernel<<<1, 256, 0, s>>>(a->cu_seqlens, a->num_requests, n, ps.bad, a->status);
   const int n_idx = sets ? Lt * k : 0;
-  layer_lists_kernel<<<(Ls + n_idx + 255) / 256 + 1, 256, 0, s>>>(ident, Ls, set_list,
-                                                                 a->layer_idx, n_idx);
+  if (sets)
+    layer_lists_kernel<<<(n_idx + 255) / 256, 256, 0, s>>>(set_list, a->layer_idx, n_idx, Ls);
   if (sets) check_rows_kernel<<<(Lt * k + 255) / 256, 256, 0, s>>>(a->layer_idx, Lt, k, Ls, a->status);
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
 
-  const int tiles_d = (D + kTile - 1) / kTile;
   const int q1 = Lt * D;
-  const int tiles_q1 = (q1 + kTile - 1) / kTile;
-  const int pk = k * D, tiles_pk = (pk + kTile - 1) / kTile;
+  const int pk = k * D;
+  const int rows = (Ls + Lt) * D;
+  const int nq = (q1 + kMomRows - 1) / kMomRows;
+  const ScoreTiles tiles{Ls, Lt, D, k, nq, Ls * (1 + nq), set_list, ps.G, ps.C, ps.Gs, ps.Cs};
+  const int num_tiles = tiles.layer_tiles + (sets ? Lt * (k * (k + 1) / 2 + k) : 0);
   // the per-pass fp64 region: sums, yss, G, C, zz, ww, Gs, Cs, zzs, wws
   double *clear_from = ps.xs;
   const int64_t clear_words = (int64_t)(lay.bad - lay.xs) / 8;
@@ -527,22 +493,21 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
             reinterpret_cast<const float *>(m ? a->src_v : a->src_k),
             reinterpret_cast<const float *>(m ? a->tgt_v : a->tgt_k), Ls, Lt, H, D, h, m == 0, n,
             a->cu_seqlens, a->num_requests, a->src_pos, d.max_position, turns, ps, a->status);
-      // per-layer fits: batch s, features = source layer s, targets = every
-      // target layer's columns
-      gram_kernel<<<dim3((unsigned)(tiles_d * (tiles_d + 1) / 2 + tiles_d * tiles_q1),
-                         (unsigned)slices64, (unsigned)Ls),
-                    256, 0, s>>>(ps.X, ps.Y, ps.xs, ps.ys, ident, 1, D, Lt, n, q1, 0, 0, ps.G,
-                                 ps.C, tiles_d, tiles_q1);
+      // Gram and cross blocks of the per-layer and set fits, chunk by chunk
+      for (int64_t n0 = 0; n0 < n; n0 += kMomChunk) {
+        const int64_t len = n - n0 < kMomChunk ? n - n0 : kMomChunk;
+        const int64_t np = (len + kMomKB - 1) / kMomKB * kMomKB;
+        split_kernel<<<dim3((unsigned)(np / 32), (unsigned)((rows + 31) / 32)), 256, 0, s>>>(
+            ps.X, ps.xs, n, rows, D, n0, np, ps.planes);
+        if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
+        if (mom_launch(ps.planes, rows, np, tiles, num_tiles, a->status, s) != cudaSuccess)
+          return KVX_ERR_CUDA;
+      }
       if (chol_factor(ps.G, Ls, D, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
       solve_norms_kernel<<<dim3((unsigned)Ls, (unsigned)((q1 + cols1 - 1) / cols1)), kSolveThreads,
                            solve_smem_bytes(D, cols1), s>>>(ps.G, ps.C, D, q1, D, cols1, ps.zz,
                                                             ps.ww, Lt);
       if (sets) {
-        // set fits: batch lt, features = the row's k layers, targets = lt
-        gram_kernel<<<dim3((unsigned)(tiles_pk * (tiles_pk + 1) / 2 + tiles_pk * tiles_d),
-                           (unsigned)slices64, (unsigned)Lt),
-                      256, 0, s>>>(ps.X, ps.Y, ps.xs, ps.ys, set_list, k, D, Lt, n, D, 0, D,
-                                   ps.Gs, ps.Cs, tiles_pk, tiles_d);
         if (chol_factor(ps.Gs, Lt, pk, a->lambda, a->status, s) != cudaSuccess)
           return KVX_ERR_CUDA;
         solve_norms_kernel<<<dim3((unsigned)Lt, (unsigned)((D + colsk - 1) / colsk)),

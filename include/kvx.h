@@ -370,8 +370,9 @@ size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
  * allocation (the caller passes the scratch); 3 + 2 ceil(n / 16384) +
  * 3 ceil(p / 64) - 1 kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL
  * pointer, sizes outside the limits, a non-finite lambda, or a workspace that
- * is too small or not 16-byte aligned; KVX_ERR_CUDA if a launch fails.  A fit whose matrix is not positive
- * definite gets NaN W and b and sets KVX_FLAG_NOT_SPD. */
+ * is too small or not 16-byte aligned; KVX_ERR_CUDA if a launch fails.  A fit
+ * whose matrix is not positive definite gets NaN W and b and sets
+ * KVX_FLAG_NOT_SPD. */
 kvx_status kvx_ridge_fit(const kvx_ridge_args *args, void *stream);
 
 /* Arguments of the layer-selection scores (kvx_layer_scores).  DEVICE
@@ -393,14 +394,16 @@ typedef struct {
   double lambda;              /* ridge strength (> 0), added unscaled         */
   double *r2;                 /* [Lt][Ls][H][2] output, m = 0 keys, 1 values  */
   double *r2_set;             /* [Lt][H][2] output, or NULL (needs layer_idx) */
-  void *workspace;            /* kvx_layer_scores_workspace_bytes(plan, ntok) */
+  void *workspace;            /* kvx_layer_scores_workspace_bytes(plan, ntok)
+                                 bytes, 16-byte aligned                      */
   size_t workspace_bytes;
   uint32_t *status;           /* optional device word; KVX_FLAG_* OR-ed in    */
 } kvx_score_args;
 
 /* Bytes of scratch kvx_layer_scores needs for `ntok` tokens (content
- * features of one (head, K|V) at a time, fp64 sums, Gram and cross blocks),
- * or 0 if the plan cannot score (head_dim not a multiple of 16 or above 128,
+ * features of one (head, K|V) at a time, the split-precision planes of one
+ * chunk of up to 16,384 tokens, fp64 sums, Gram and cross blocks), or 0 if
+ * the plan cannot score (head_dim not a multiple of 16 or above 128,
  * ntok < 2). */
 size_t kvx_layer_scores_workspace_bytes(const kvx_plan *plan, int64_t ntok);
 
@@ -419,13 +422,15 @@ size_t kvx_layer_scores_workspace_bytes(const kvx_plan *plan, int64_t ntok);
  * r2 = 1 - sum |y - (x W + b)|^2 / sum |y - ybar|^2, summed over the d
  * dimensions (in-sample).  With layer_idx the set of row lt (its k layers
  * concatenated in table order, the transfer's feature vector) is scored the
- * same way into r2_set.  Computed from fp32 content features with fp32
- * products accumulated in fp64 (centred Gram and cross blocks), an fp64
- * Cholesky of G + lambda I and fp64 triangular solves:
- * r2 = (|L^-1 C|^2 + lambda |W|^2) / sum |y - ybar|^2.  Asynchronous on
- * `stream`; no allocation (the caller passes the scratch).  Returns
- * KVX_ERR_INVALID_ARG for a NULL pointer, lambda <= 0 or non-finite, ntok < 2
- * or a workspace that is too small; KVX_ERR_UNSUPPORTED for a head_dim the
+ * same way into r2_set.  Computed from fp32 content features: the centred
+ * Gram and cross blocks on the tensor cores with each centred value split
+ * into two tf32 values (products hi*hi + hi*lo + lo*hi, fp32 partial sums
+ * over 256 tokens added in fp64), an fp64 Cholesky of G + lambda I and fp64
+ * triangular solves: r2 = (|L^-1 C|^2 + lambda |W|^2) / sum |y - ybar|^2.
+ * Asynchronous on `stream`; no allocation (the caller passes the scratch).
+ * Returns KVX_ERR_INVALID_ARG for a NULL pointer, lambda <= 0 or non-finite,
+ * ntok < 2, or a workspace that is too small or not 16-byte aligned;
+ * KVX_ERR_UNSUPPORTED for a head_dim the
  * scorer does not handle; KVX_ERR_CUDA if a launch fails.  Device-detected:
  * a token position outside [0, max_position) or a malformed request table
  * makes every score NaN (KVX_FLAG_BAD_POSITION / KVX_FLAG_BAD_SEQLENS); a
