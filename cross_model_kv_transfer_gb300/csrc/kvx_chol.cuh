@@ -34,42 +34,46 @@ __global__ void __launch_bounds__(256) chol_prep_kernel(double *__restrict__ G, 
 
 __device__ __forceinline__ int blk_len(int p, int kb) { return p - kb * kB < kB ? p - kb * kB : kB; }
 
-// Factor the diagonal block kb of each fit in shared memory (left-looking,
-// one warp per row); the update of earlier blocks is already applied.
+// Factor the diagonal block kb of each fit in shared memory, right-looking
+// over all threads: per column, the pivot's square root (one thread, with
+// its reciprocal), the column below it scaled, then the trailing lower
+// triangle updated; the update of earlier blocks is already applied.
 __global__ void __launch_bounds__(256) chol_diag_kernel(double *__restrict__ G, int p, int kb,
                                                         uint32_t *status) {
   __shared__ double L[kB][kB + 1];
+  __shared__ double s_rpiv;
   __shared__ int s_fail;
   double *A = G + (int64_t)blockIdx.x * p * p;
   if (isnan(A[0])) return;
   const int o = kb * kB, nb = blk_len(p, kb);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
-  for (int e = tid; e < nb * nb; e += blockDim.x) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  for (int e = tid; e < nb * nb; e += nthreads) {
     const int i = e / nb, j = e % nb;
     L[i][j] = A[(int64_t)(o + i) * p + o + j];
   }
   if (tid == 0) s_fail = 0;
   __syncthreads();
   for (int j = 0; j < nb; ++j) {
-    if (warp == 0) {
-      double sum = 0.0;
-      for (int m = lane; m < j; m += 32) sum = fma(L[j][m], L[j][m], sum);
-#pragma unroll
-      for (int w = 16; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
-      if (lane == 0) {
-        const double d = L[j][j] - sum;
-        if (!(d > 0.0)) s_fail = 1;
-        L[j][j] = d > 0.0 ? sqrt(d) : 1.0;
+    if (tid == 0) {
+      const double d = L[j][j];
+      if (!(d > 0.0)) {
+        s_fail = 1;
+        s_rpiv = 1.0;
+      } else {
+        const double r = sqrt(d);
+        L[j][j] = r;
+        s_rpiv = 1.0 / r;
       }
     }
     __syncthreads();
     if (s_fail) break;
-    for (int i = j + 1 + warp; i < nb; i += nwarps) {
-      double sum = 0.0;
-      for (int m = lane; m < j; m += 32) sum = fma(L[i][m], L[j][m], sum);
-#pragma unroll
-      for (int w = 16; w > 0; w >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, w);
-      if (lane == 0) L[i][j] = (L[i][j] - sum) / L[j][j];
+    const double rp = s_rpiv;
+    for (int i = j + 1 + tid; i < nb; i += nthreads) L[i][j] *= rp;
+    __syncthreads();
+    const int w = nb - j - 1;                  // trailing block: rows and columns j + 1 ..
+    for (int e = tid; e < w * w; e += nthreads) {
+      const int i = j + 1 + e / w, m = j + 1 + e % w;
+      if (m <= i) L[i][m] = fma(-L[i][j], L[m][j], L[i][m]);
     }
     __syncthreads();
   }
@@ -182,10 +186,20 @@ __global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ G
 constexpr int kSolveThreads = 128;   // threads per CTA of the column solves
 
 // Columns one CTA of a triangular solve holds in shared memory: the largest
-// power of two <= 32 with p x nc <= 4096 doubles (32 KB).
-inline int solve_cols_per_cta(int p) {
+// power of two <= 32 with p x nc <= 4096 doubles (32 KB), halved while the
+// `batch` fits of q columns would give fewer than four CTAs per SM (the
+// steps of one CTA are a chain of latencies; more CTAs hide them).
+inline int solve_cols_per_cta(int p, int batch, int q) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
   int nc = 32;
   while (nc > 1 && (int64_t)p * nc > 4096) nc >>= 1;
+  while (nc > 1 && (int64_t)batch * ((q + nc - 1) / nc) < 4LL * sms) nc >>= 1;
   return nc;
 }
 inline size_t solve_smem_bytes(int p, int nc) { return ((size_t)p * nc + p) * sizeof(double); }

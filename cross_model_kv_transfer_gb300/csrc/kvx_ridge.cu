@@ -41,7 +41,8 @@
 namespace {
 
 constexpr int kFlushObs = 256;      // fp32 partial sums of the means go into fp64 this often
-constexpr int64_t kRowsPerSlice = 16384;   // observations per CTA of the means
+constexpr int64_t kMeanRows = 4096;  // observations per CTA of the means
+constexpr int kSplitObs = 128;       // observations per CTA of the split pass
 
 template <typename T>
 __device__ __forceinline__ float ldv(const T *p);
@@ -59,59 +60,74 @@ __global__ void clear_kernel(double *x, int64_t n) {
 }
 
 // sums[b][c] += column c of [X | Y] over this CTA's slice of observations
+// (blockIdx.x: slice of kMeanRows, blockIdx.y: 256 columns); four
+// independent fp32 partial sums per 256 rows keep four loads in flight.
 template <typename T>
 __global__ void __launch_bounds__(256) mean_kernel(const T *__restrict__ x, const T *__restrict__ y,
                                                    double *__restrict__ sums, int64_t n, int p,
                                                    int q) {
   const int b = blockIdx.z;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
   if (c >= p + q) return;
-  const int64_t t0 = (int64_t)blockIdx.y * kRowsPerSlice;
-  const int64_t t1 = t0 + kRowsPerSlice < n ? t0 + kRowsPerSlice : n;
+  const int64_t t0 = (int64_t)blockIdx.x * kMeanRows;
+  const int64_t t1 = t0 + kMeanRows < n ? t0 + kMeanRows : n;
   const T *col = c < p ? x + (int64_t)b * n * p + c : y + (int64_t)b * n * q + (c - p);
-  const int ld = c < p ? p : q;
+  const int64_t ld = c < p ? p : q;
   double acc = 0.0;
   for (int64_t t = t0; t < t1; t += kFlushObs) {
-    float part = 0.f;
     const int64_t te = t + kFlushObs < t1 ? t + kFlushObs : t1;
-    for (int64_t u = t; u < te; ++u) part += ldv<T>(col + u * ld);
-    acc += (double)part;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    int64_t u = t;
+    for (; u + 3 < te; u += 4) {
+      s0 += ldv<T>(col + u * ld);
+      s1 += ldv<T>(col + (u + 1) * ld);
+      s2 += ldv<T>(col + (u + 2) * ld);
+      s3 += ldv<T>(col + (u + 3) * ld);
+    }
+    for (; u < te; ++u) s0 += ldv<T>(col + u * ld);
+    acc += (double)((s0 + s1) + (s2 + s3));
   }
   atomicAdd(sums + (int64_t)b * (p + q) + c, acc);
 }
 
 // Per chunk [n0, n0 + np): the centred values of [X | Y] of fit b as tf32 hi
 // and lo planes, plane row b (p + q) + f, column t - n0 (observations beyond
-// n are zero).  A CTA transposes a 32 x 32 block through shared memory:
-// loads run along the features, stores along the observations.
+// n are zero).  A CTA transposes 32 features x 128 observations through
+// shared memory: loads run along the features (16 per thread in flight),
+// stores along the observations.
 template <typename T>
 __global__ void __launch_bounds__(256) split_kernel(const T *__restrict__ x, const T *__restrict__ y,
                                                     const double *__restrict__ sums, int64_t n,
                                                     int p, int q, int64_t n0, int64_t np,
                                                     int64_t R, float *__restrict__ planes) {
-  __shared__ float blk[32][33];
+  __shared__ float blk[kSplitObs][33];
   const int b = blockIdx.z, pq = p + q;
   const int f0 = blockIdx.y * 32;
-  const int64_t c0 = (int64_t)blockIdx.x * 32;
+  const int64_t c0 = (int64_t)blockIdx.x * kSplitObs;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int f = f0 + tx;
   float mean = 0.f;
   if (f < pq) mean = (float)(sums[(int64_t)b * pq + f] / (double)n);
+  const T *base = f < p ? x + (int64_t)b * n * p + f : y + (int64_t)b * n * q + (f - p);
+  const int64_t ld = f < p ? p : q;
+  float v[kSplitObs / 8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty + 8 * i;
-    const int64_t t = n0 + c0 + r;
-    float v = 0.f;
-    if (f < pq && t < n)
-      v = (f < p ? ldv<T>(x + ((int64_t)b * n + t) * p + f)
-                 : ldv<T>(y + ((int64_t)b * n + t) * q + (f - p))) - mean;
-    blk[r][tx] = v;
+  for (int i = 0; i < kSplitObs / 8; ++i) {
+    const int64_t t = n0 + c0 + ty + 8 * i;
+    v[i] = f < pq && t < n ? ldv<T>(base + t * ld) - mean : 0.f;
   }
+#pragma unroll
+  for (int i = 0; i < kSplitObs / 8; ++i) blk[ty + 8 * i][tx] = v[i];
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int fr = f0 + ty + 8 * i;
-    if (fr < pq) mom_put(planes, R, np, (int64_t)b * pq + fr, c0 + tx, blk[tx][ty + 8 * i]);
+    if (fr >= pq) continue;
+#pragma unroll
+    for (int j = 0; j < kSplitObs / 32; ++j) {
+      const int64_t col = c0 + tx + 32 * j;
+      if (col < np) mom_put(planes, R, np, (int64_t)b * pq + fr, col, blk[tx + 32 * j][ty + 8 * i]);
+    }
   }
 }
 
@@ -207,8 +223,8 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
       (reinterpret_cast<uintptr_t>(a->workspace) & 15u) != 0)
     return KVX_ERR_INVALID_ARG;
   const int64_t n = a->n;
-  const int64_t slices64 = (n + kRowsPerSlice - 1) / kRowsPerSlice;
-  if (slices64 > 65535) return KVX_ERR_INVALID_ARG;  // grid y; checked before any launch
+  const int64_t slices64 = (n + kMeanRows - 1) / kMeanRows;
+  if (n > 65535LL * 16384) return KVX_ERR_INVALID_ARG;   // the documented limit
   const int slices = (int)slices64;
   cudaStream_t s = (cudaStream_t)stream;
   const int batch = a->batch, p = a->p, q = a->q;
@@ -225,7 +241,7 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   clear_kernel<<<1024, 256, 0, s>>>(sums, words);
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
 
-  dim3 mgrid((unsigned)((p + q + 255) / 256), (unsigned)slices, (unsigned)batch);
+  dim3 mgrid((unsigned)slices, (unsigned)((p + q + 255) / 256), (unsigned)batch);
   if (a->x_dtype == KVX_F32)
     mean_kernel<float><<<mgrid, 256, 0, s>>>(reinterpret_cast<const float *>(a->x),
                                              reinterpret_cast<const float *>(a->y), sums, n, p, q);
@@ -241,7 +257,8 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   for (int64_t n0 = 0; n0 < n; n0 += kMomChunk) {
     const int64_t len = n - n0 < kMomChunk ? n - n0 : kMomChunk;
     const int64_t np = (len + kMomKB - 1) / kMomKB * kMomKB;
-    dim3 sgrid((unsigned)(np / 32), (unsigned)((p + q + 31) / 32), (unsigned)batch);
+    dim3 sgrid((unsigned)((np + kSplitObs - 1) / kSplitObs), (unsigned)((p + q + 31) / 32),
+               (unsigned)batch);
     if (a->x_dtype == KVX_F32)
       split_kernel<float><<<sgrid, 256, 0, s>>>(reinterpret_cast<const float *>(a->x),
                                                 reinterpret_cast<const float *>(a->y), sums, n, p,
@@ -257,7 +274,7 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   // blocked fp64 Cholesky
   if (chol_factor(G, batch, p, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
   // triangular solves: nc output columns per CTA, in shared memory
-  const int nc = solve_cols_per_cta(p);
+  const int nc = solve_cols_per_cta(p, batch, q);
   if (solve_smem_bytes(p, nc) > 48 * 1024 &&
       cudaFuncSetAttribute(trsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)solve_smem_bytes(p, nc)) != cudaSuccess)

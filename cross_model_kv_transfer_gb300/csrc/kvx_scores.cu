@@ -235,31 +235,39 @@ __global__ void __launch_bounds__(256) content_kernel(
 
 // 2. Per chunk [n0, n0 + np): the centred content of plane row f (= layer
 // f / d, dimension f % d, source layers first) as tf32 hi and lo planes,
-// column t - n0 (tokens beyond n are zero); a CTA transposes a 32 x 32 block
-// through shared memory.
+// column t - n0 (tokens beyond n are zero); a CTA transposes 32 rows x 128
+// tokens through shared memory (16 loads per thread in flight).
+constexpr int kSplitObs = 128;
 __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ X,
                                                     const double *__restrict__ sums, int64_t n,
                                                     int rows, int d, int64_t n0, int64_t np,
                                                     float *__restrict__ planes) {
-  __shared__ float blk[32][33];
+  __shared__ float blk[kSplitObs][33];
   const int f0 = blockIdx.y * 32;
-  const int64_t c0 = (int64_t)blockIdx.x * 32;
+  const int64_t c0 = (int64_t)blockIdx.x * kSplitObs;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int f = f0 + tx;
   float mean = 0.f;
   if (f < rows) mean = (float)(sums[f] / (double)n);
   const float *col = X + (int64_t)(f / d) * n * d + f % d;
+  float v[kSplitObs / 8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty + 8 * i;
-    const int64_t t = n0 + c0 + r;
-    blk[r][tx] = f < rows && t < n ? col[t * d] - mean : 0.f;
+  for (int i = 0; i < kSplitObs / 8; ++i) {
+    const int64_t t = n0 + c0 + ty + 8 * i;
+    v[i] = f < rows && t < n ? col[t * d] - mean : 0.f;
   }
+#pragma unroll
+  for (int i = 0; i < kSplitObs / 8; ++i) blk[ty + 8 * i][tx] = v[i];
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int fr = f0 + ty + 8 * i;
-    if (fr < rows) mom_put(planes, rows, np, fr, c0 + tx, blk[tx][ty + 8 * i]);
+    if (fr >= rows) continue;
+#pragma unroll
+    for (int j = 0; j < kSplitObs / 32; ++j) {
+      const int64_t c = c0 + tx + 32 * j;
+      if (c < np) mom_put(planes, rows, np, fr, c, blk[tx + 32 * j][ty + 8 * i]);
+    }
   }
 }
 
@@ -478,7 +486,7 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   const int64_t clear_words = (int64_t)(lay.bad - lay.xs) / 8;
   const int per_tok = D / 16, tpb = 256 / per_tok;
   dim3 cgrid((unsigned)((n + tpb - 1) / tpb), (unsigned)(Ls + Lt));
-  const int cols1 = solve_cols_per_cta(D), colsk = solve_cols_per_cta(pk);
+  const int cols1 = solve_cols_per_cta(D, Ls, q1), colsk = solve_cols_per_cta(pk, Lt, D);
   for (int h = 0; h < H; ++h) {
     for (int m = 0; m < 2; ++m) {
       clear_kernel<<<1024, 256, 0, s>>>(clear_from, clear_words);
@@ -497,7 +505,9 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
       for (int64_t n0 = 0; n0 < n; n0 += kMomChunk) {
         const int64_t len = n - n0 < kMomChunk ? n - n0 : kMomChunk;
         const int64_t np = (len + kMomKB - 1) / kMomKB * kMomKB;
-        split_kernel<<<dim3((unsigned)(np / 32), (unsigned)((rows + 31) / 32)), 256, 0, s>>>(
+        split_kernel<<<dim3((unsigned)((np + kSplitObs - 1) / kSplitObs),
+                            (unsigned)((rows + 31) / 32)),
+                       256, 0, s>>>(
             ps.X, ps.xs, n, rows, D, n0, np, ps.planes);
         if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
         if (mom_launch(ps.planes, rows, np, tiles, num_tiles, a->status, s) != cudaSuccess)
