@@ -402,20 +402,43 @@ def transfer_kwargs(wl, inp, dst_k, dst_v, status, paged_src=None):
 
 
 RIDGE_METRIC = ("ridge fits/s of the 14B→32B per-head maps (512 features → 128 outputs, "
-                "131,072 observations each); % of fp32 ALU roofline")
+                "131,072 observations each); % of the roofline of the call's dominant phase")
 
 
-def fp32_alu_peak_tflops():
-    """fp32 FMA rate from unit counts and the maximum SM clock: SMs x 128
-    fp32 lanes x 2 flops x clock."""
-    import torch
-    props = torch.cuda.get_device_properties(torch.cuda.current_device())
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            mhz = float(json.load(f)["sm_max_mhz"])
-    except Exception:
-        mhz = 2070.0
-    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+# Nominal dense rates for the phases the measured peaks do not cover: tf32
+# tensor 1.1 and fp64 1.25 PFLOP/s / TFLOP/s against bf16's 2.25 PFLOP/s.
+TF32_PER_BF16 = 1.1 / 2.25
+NOMINAL_FP64_TFLOPS = 1.25
+
+
+def phase_roofline(call_ms, tensor_flops, fp64_flops, hbm_bytes, kernel_name, workload):
+    """Roofline of a call made of phases that run one after another (the
+    ridge fit, the layer scores): the ideal time of each phase at its own
+    peak -- the split-precision products on the tensor cores (tf32 peak =
+    measured bf16 burst x the nominal tf32/bf16 ratio), the fp64
+    factorisations and solves (nominal fp64 rate), the algorithmic bytes at
+    the measured HBM copy bandwidth -- and, as `bound`, the phase with the
+    largest ideal time, its work over the whole call's time."""
+    peaks, src = load_peaks()
+    tf32 = peaks["bf16_tflops"] * TF32_PER_BF16
+    ideal = {"tensor": tensor_flops / (tf32 * 1e12) * 1e3,
+             "alu": fp64_flops / (NOMINAL_FP64_TFLOPS * 1e12) * 1e3,
+             "hbm": hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3}
+    bound = max(ideal, key=ideal.get)
+    work = {"tensor": tensor_flops, "alu": fp64_flops, "hbm": hbm_bytes}[bound]
+    peak = {"tensor": tf32, "alu": NOMINAL_FP64_TFLOPS, "hbm": peaks["hbm_gbs"]}[bound]
+    scale = 1e12 if bound != "hbm" else 1e9
+    achieved = work / (call_ms / 1e3) / scale
+    return {"bound": bound, "achieved": achieved, "peak": peak,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
+            "traffic": measured_traffic(workload, kernel_name),
+            "peak_source": {"tensor": f"tf32: {src} bf16 burst peak x 1.1/2.25 (nominal ratio)",
+                            "alu": "nominal fp64 rate (1.25 TFLOP/s; no measured fp64 peak)",
+                            "hbm": f"{src} HBM copy bandwidth"}[bound],
+            "ideal_ms": {k: round(v, 4) for k, v in ideal.items()},
+            "frac_of_ideal_sum": sum(ideal.values()) / call_ms,
+            "tensor_flops": tensor_flops, "fp64_flops": fp64_flops, "algorithmic_bytes": hbm_bytes,
+            "scope": "whole call; its phases run one after another"}
 
 
 def run_ridge(args):
@@ -464,14 +487,14 @@ def run_ridge(args):
         barrier()
     ms_local = ev0.elapsed_time(ev1) / args.steps
     value, ms = aggregate(B, ms_local, dev)
-    # useful flops: the symmetric Gram block once, the cross block, per fit
+    # useful flops: the symmetric Gram block once, the cross block, per fit;
+    # each is three tf32 products on the tensor cores.  fp64: the Cholesky
+    # (p^3 / 3 multiply-adds) and the two triangular solves (p^2 q) per fit.
     flops = B * 2.0 * n * (p * (p + 1) / 2 + p * q)
-    peak = fp32_alu_peak_tflops()
-    achieved = flops / (ms_local / 1e3) / 1e12
-    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": measured_traffic(wl.name, "ridge"),
-            "peak_source": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
-            "algorithmic_flops": flops}
+    fp64 = B * (2.0 * p ** 3 / 3 + 2.0 * p * p * q)
+    roof = phase_roofline(ms_local, 3 * flops, fp64, (x.numel() + y.numel()) * 4, "ridge",
+                          wl.name)
+    roof["useful_gram_flops"] = flops
 
     e2e = None
     if not args.no_e2e:
@@ -535,7 +558,7 @@ def run_ridge(args):
 
 SCORE_METRIC = ("layer-selection scores: calibration tokens/s through every (target layer, "
                 "source layer, head, K|V) fit and every target layer's set fit at the 14B→32B "
-                "shape, 4,096 tokens; % of fp32 ALU roofline")
+                "shape, 4,096 tokens; % of the roofline of the call's dominant phase")
 
 
 def score_config(wl, n: int) -> dict:
@@ -552,6 +575,15 @@ def score_flops(Ls, Lt, H, d, k, n) -> float:
     of k source layers against its own d columns."""
     per = Ls * (d * (d + 1) / 2 + d * Lt * d) + Lt * (k * d * (k * d + 1) / 2 + k * d * d)
     return 2.0 * n * per * 2 * H
+
+
+def score_fp64_flops(Ls, Lt, H, d, k) -> float:
+    """fp64 flops of one scoring call: per (head, K|V) the Cholesky of every
+    per-layer Gram block (d^3 / 3 multiply-adds) and the two solves of its
+    Lt d columns (d^2 each), and with a table those of every set (k d)."""
+    kd = k * d
+    per = Ls * (d ** 3 / 3 + d * d * Lt * d) + Lt * (kd ** 3 / 3 + kd * kd * d)
+    return 2.0 * per * 2 * H
 
 
 def score_launches(Ls, Lt, H, d, k, n, sets=True) -> int:
@@ -617,13 +649,10 @@ def run_scores(args):
     ms_local = ev0.elapsed_time(ev1) / args.steps
     value, ms = aggregate(n, ms_local, dev)
     flops = score_flops(Ls, Lt, H, d, k, n)
-    peak = fp32_alu_peak_tflops()
-    achieved = flops / (ms_local / 1e3) / 1e12
-    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": measured_traffic(wl.name, "scores"),
-            "peak_source": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
-            "algorithmic_flops": flops, "scope": "whole call (every kernel of the pass)"}
     in_bytes = sum(inp[c].numel() * inp[c].element_size() for c in cache)
+    roof = phase_roofline(ms_local, 3 * flops, score_fp64_flops(Ls, Lt, H, d, k), in_bytes,
+                          "scores", wl.name)
+    roof["useful_gram_flops"] = flops
 
     e2e = None
     if not args.no_e2e:

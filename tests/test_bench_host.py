@@ -127,3 +127,16 @@ def test_dram_records_name_known_kernels_and_commands():
         assert r["kernel"] in bench.KERNEL_FILES
         assert r["dram_bytes_per_launch"] == r["dram_bytes_read"] + r["dram_bytes_write"]
         assert r["command"].startswith("ncu ") and "--clock-control none" in r["command"]
+
+
+def test_phase_roofline_picks_the_phase_with_the_largest_ideal_time():
+    peaks, _ = bench.load_peaks()
+    tf32 = peaks["bf16_tflops"] * bench.TF32_PER_BF16
+    # 1 ms of tensor work, 3 ms of fp64 work, 0.5 ms of HBM traffic, 10 ms call
+    r = bench.phase_roofline(10.0, tf32 * 1e9, bench.NOMINAL_FP64_TFLOPS * 3e9,
+                             peaks["hbm_gbs"] * 0.5e6, "ridge", "none")
+    assert r["bound"] == "alu" and r["unit"] == "TFLOP/s"
+    assert abs(r["ideal_ms"]["tensor"] - 1.0) < 1e-3 and abs(r["ideal_ms"]["alu"] - 3.0) < 1e-3
+    assert abs(r["frac"] - 0.3) < 1e-9 and abs(r["frac_of_ideal_sum"] - 0.45) < 1e-6
+    r = bench.phase_roofline(2.0, tf32 * 1e9, 0.0, 0.0, "ridge", "none")
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-9 and r["traffic"] is None
