@@ -40,8 +40,7 @@
 
 namespace {
 
-constexpr int kFlushObs = 256;      // fp32 partial sums of the means go into fp64 this often
-constexpr int64_t kMeanRows = 4096;  // observations per CTA of the means
+constexpr int64_t kMeanRows = 2048;  // observations per CTA of the means (256 per thread)
 constexpr int kSplitObs = 128;       // observations per CTA of the split pass
 
 template <typename T>
@@ -59,35 +58,45 @@ __global__ void clear_kernel(double *x, int64_t n) {
     x[i] = 0.0;
 }
 
-// sums[b][c] += column c of [X | Y] over this CTA's slice of observations
-// (blockIdx.x: slice of kMeanRows, blockIdx.y: 256 columns); four
-// independent fp32 partial sums per 256 rows keep four loads in flight.
+// sums[b][c] += column c of [X | Y] over this CTA's kMeanRows observations.
+// A CTA covers 32 columns (one per lane, so a warp's loads are one line per
+// row) and 8 row groups; each thread keeps 8 fp32 partial sums over its 256
+// rows (8 loads in flight), the CTA adds its groups in fp64 and one atomic
+// per column goes to the output.
 template <typename T>
 __global__ void __launch_bounds__(256) mean_kernel(const T *__restrict__ x, const T *__restrict__ y,
                                                    double *__restrict__ sums, int64_t n, int p,
                                                    int q) {
-  const int b = blockIdx.z;
-  const int c = blockIdx.y * blockDim.x + threadIdx.x;
-  if (c >= p + q) return;
+  __shared__ double red[8][32];
+  const int b = blockIdx.z, pq = p + q;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c = blockIdx.y * 32 + tx;
   const int64_t t0 = (int64_t)blockIdx.x * kMeanRows;
   const int64_t t1 = t0 + kMeanRows < n ? t0 + kMeanRows : n;
-  const T *col = c < p ? x + (int64_t)b * n * p + c : y + (int64_t)b * n * q + (c - p);
-  const int64_t ld = c < p ? p : q;
   double acc = 0.0;
-  for (int64_t t = t0; t < t1; t += kFlushObs) {
-    const int64_t te = t + kFlushObs < t1 ? t + kFlushObs : t1;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    int64_t u = t;
-    for (; u + 3 < te; u += 4) {
-      s0 += ldv<T>(col + u * ld);
-      s1 += ldv<T>(col + (u + 1) * ld);
-      s2 += ldv<T>(col + (u + 2) * ld);
-      s3 += ldv<T>(col + (u + 3) * ld);
+  if (c < pq) {
+    const T *col = c < p ? x + (int64_t)b * n * p + c : y + (int64_t)b * n * q + (c - p);
+    const int64_t ld = c < p ? p : q;
+    float part[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) part[u] = 0.f;
+    int64_t t = t0 + ty;
+    for (; t + 56 < t1; t += 64) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) part[u] += ldv<T>(col + (t + 8 * u) * ld);
     }
-    for (; u < te; ++u) s0 += ldv<T>(col + u * ld);
-    acc += (double)((s0 + s1) + (s2 + s3));
+    for (; t < t1; t += 8) part[0] += ldv<T>(col + t * ld);
+    acc = (double)(((part[0] + part[1]) + (part[2] + part[3])) +
+                   ((part[4] + part[5]) + (part[6] + part[7])));
   }
-  atomicAdd(sums + (int64_t)b * (p + q) + c, acc);
+  red[ty][tx] = acc;
+  __syncthreads();
+  if (ty == 0 && c < pq) {
+    double sum = 0.0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) sum += red[g][tx];
+    atomicAdd(sums + (int64_t)b * pq + c, sum);
+  }
 }
 
 // Per chunk [n0, n0 + np): the centred values of [X | Y] of fit b as tf32 hi
@@ -241,7 +250,7 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   clear_kernel<<<1024, 256, 0, s>>>(sums, words);
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
 
-  dim3 mgrid((unsigned)slices, (unsigned)((p + q + 255) / 256), (unsigned)batch);
+  dim3 mgrid((unsigned)slices, (unsigned)((p + q + 31) / 32), (unsigned)batch);
   if (a->x_dtype == KVX_F32)
     mean_kernel<float><<<mgrid, 256, 0, s>>>(reinterpret_cast<const float *>(a->x),
                                              reinterpret_cast<const float *>(a->y), sums, n, p, q);
