@@ -578,11 +578,13 @@ def score_flops(Ls, Lt, H, d, k, n) -> float:
 
 
 def score_fp64_flops(Ls, Lt, H, d, k) -> float:
-    """fp64 flops of one scoring call: per (head, K|V) the Cholesky of every
-    per-layer Gram block (d^3 / 3 multiply-adds) and the two solves of its
-    Lt d columns (d^2 each), and with a table those of every set (k d)."""
+    """fp64 flops of one scoring call: per (head, K|V) and source layer the
+    Cholesky of G + lam I (d^3 / 3 multiply-adds), the inverse (d^3), N =
+    M + lam M M (d^3), its Cholesky (d^3 / 3) and R^T C over the Lt d target
+    columns (d^2 / 2 each); with a table, per set the Cholesky ((k d)^3 / 3)
+    and the two solves of its d columns ((k d)^2 each)."""
     kd = k * d
-    per = Ls * (d ** 3 / 3 + d * d * Lt * d) + Lt * (kd ** 3 / 3 + kd * kd * d)
+    per = Ls * (d ** 3 * (2 / 3 + 2) + d * d / 2 * Lt * d) + Lt * (kd ** 3 / 3 + kd * kd * d)
     return 2.0 * per * 2 * H
 
 
@@ -590,12 +592,13 @@ def score_launches(Ls, Lt, H, d, k, n, sets=True) -> int:
     """Kernels one kvx_layer_scores call launches: the request-table check,
     with a table the clamped table and the row check, then per (head, K|V)
     clear, content, per chunk of 16,384 tokens the split and the tensor-core
-    moments, the Cholesky (prep + per 64-column block: diagonal, panel,
-    update) and solve of the per-layer fits, those of the set fits, and the
-    final ratios."""
+    moments; for the per-layer fits the Cholesky of G + lam I (prep + per
+    64-column block: diagonal, panel, update), the inverse, N, its Cholesky
+    and the triangular norms; for the set fits the Cholesky and the solves;
+    and the final ratios."""
     chol = lambda p: 1 + 3 * ((p + 63) // 64) - 2
     chunks = (n + 16383) // 16384
-    per = 2 + 2 * chunks + chol(d) + 1 + (chol(k * d) + 1 if sets else 0) + 1
+    per = 2 + 2 * chunks + 2 * chol(d) + 3 + (chol(k * d) + 1 if sets else 0) + 1
     return 1 + (2 if sets else 0) + H * 2 * per
 
 

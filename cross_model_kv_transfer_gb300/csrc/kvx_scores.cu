@@ -17,19 +17,22 @@
 // Per (head, K|V) one pass of launches:
 //   1. content features (keys un-rotated at the token's position with each
 //      model's base, values as stored) of every source and target layer,
-//      fp32 [Ls + Lt][n][d], with fp64 column sums and the targets' sums of
-//      squares;
+//      fp32 [Ls + Lt][n][d], with fp64 column sums;
 //   2. per chunk of 16,384 tokens: the centred features split into tf32 hi
 //      and lo planes (kvx_moments.cuh), then on the tensor cores (products
 //      hi*hi + hi*lo + lo*hi) the centred Gram blocks G of every source layer
-//      and its cross blocks C against every target layer's columns, and with
-//      a layer table the Gram blocks of each row's set (its layers gathered
-//      as 128-row blocks) and their cross blocks against that target layer;
+//      and its cross blocks C against every target layer's columns, each
+//      target layer's own Gram block (its trace is sum |Yc|^2), and with a
+//      layer table the Gram blocks of each row's set (its layers gathered as
+//      128-row blocks) and their cross blocks against that target layer;
 //      fp32 partial sums over 256 tokens, summed in fp32 per slice of 4,096,
 //      added in fp64;
-//   3. fp64 Cholesky of G + lam I, blocked by 64 (kvx_chol.cuh);
-//   4. fp64 forward and back substitution per column, keeping only the
-//      column's |z|^2 and |w|^2, summed per target layer;
+//   3. per-layer fits: the fp64 Cholesky of G + lam I (kvx_chol.cuh), then
+//      M = (G + lam I)^-1, N = M + lam M M = R R^T (a second Cholesky), and
+//      |Z|^2 + lam |W|^2 = |R^T C|^2 per target layer as one triangular
+//      product per source layer;
+//   4. set fits: the Cholesky of each set's Gram block and fp64 forward and
+//      back substitution per column, keeping only |z|^2 and |w|^2;
 //   5. the scores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -60,9 +63,11 @@ struct Pass {
   float *planes;     // [2][(Ls + Lt) d][np] tf32 hi and lo of one chunk
   double *xs;        // [Ls][d] column sums (followed by ys)
   double *ys;        // [Lt][d]
-  double *yss;       // [Lt] sums of squares
   double *G;         // [Ls][d][d]
   double *C;         // [Ls][d][Lt*d]
+  double *M;         // [Ls][d][d]  (G + lam I)^-1
+  double *N;         // [Ls][d][d]  M + lam M M, then its Cholesky factor R
+  double *Gy;        // [Lt][d][d]  centred Gram of each target layer (its trace: SS_tot)
   double *zz, *ww;   // [Ls][Lt]
   double *Gs;        // [Lt][k*d][k*d]   (sets)
   double *Cs;        // [Lt][k*d][d]
@@ -73,7 +78,7 @@ struct Pass {
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t X, planes, xs, ys, yss, G, C, zz, ww, Gs, Cs, zzs, wws, bad, total;
+  size_t X, planes, xs, ys, G, C, M, N, Gy, zz, ww, Gs, Cs, zzs, wws, bad, total;
 };
 
 // Tokens per plane chunk, padded to the tensor-core block.
@@ -92,9 +97,11 @@ Layout layout_of(int64_t Ls, int64_t Lt, int64_t d, int64_t k, int64_t n) {
   at += (size_t)Ls * d * 8;                       // xs and ys adjacent: [Ls + Lt][d]
   L.ys = at;
   at += round256((size_t)Lt * d * 8);
-  L.yss = take((size_t)Lt * 8);
   L.G = take((size_t)Ls * d * d * 8);
   L.C = take((size_t)Ls * d * Lt * d * 8);
+  L.M = take((size_t)Ls * d * d * 8);
+  L.N = take((size_t)Ls * d * d * 8);
+  L.Gy = take((size_t)Lt * d * d * 8);
   L.zz = take((size_t)Ls * Lt * 8);
   L.ww = take((size_t)Ls * Lt * 8);
   L.Gs = take((size_t)Lt * k * d * k * d * 8);
@@ -163,7 +170,6 @@ __global__ void __launch_bounds__(256) content_kernel(
     const int32_t *__restrict__ src_pos, int max_position, const __grid_constant__ Turns turns,
     Pass ps, uint32_t *status) {
   __shared__ float ssum[kMaxD];
-  __shared__ float sss;
   const int L = blockIdx.y;
   const bool is_src = L < Ls;
   const int layer = is_src ? L : L - Ls;
@@ -171,7 +177,6 @@ __global__ void __launch_bounds__(256) content_kernel(
   const int tpb = 256 / per_tok;                   // tokens per block
   const int tid = threadIdx.x;
   for (int i = tid; i < d; i += blockDim.x) ssum[i] = 0.f;
-  if (tid == 0) sss = 0.f;
   __syncthreads();
   const int q = tid % per_tok;
   const int64_t g = (int64_t)blockIdx.x * tpb + tid / per_tok;
@@ -216,21 +221,17 @@ __global__ void __launch_bounds__(256) content_kernel(
       }
     }
     float *out = ps.X + ((int64_t)L * n + g) * d;
-    float sq = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       out[8 * q + e] = lo[e];
       out[half + 8 * q + e] = hi[e];
       atomicAdd(&ssum[8 * q + e], lo[e]);
       atomicAdd(&ssum[half + 8 * q + e], hi[e]);
-      sq += lo[e] * lo[e] + hi[e] * hi[e];
     }
-    if (!is_src) atomicAdd(&sss, sq);
   }
   __syncthreads();
   double *sums = is_src ? ps.xs + (int64_t)layer * d : ps.ys + (int64_t)layer * d;
   for (int i = tid; i < d; i += blockDim.x) atomicAdd(sums + i, (double)ssum[i]);
-  if (!is_src && tid == 0) atomicAdd(ps.yss + layer, (double)sss);
 }
 
 // 2. Per chunk [n0, n0 + np): the centred content of plane row f (= layer
@@ -273,7 +274,8 @@ __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ X,
 
 // The tensor-core tiles of one pass.  Per source layer s: its Gram block
 // (A = B = layer s) and ceil(Lt d / 128) cross tiles against the target
-// columns.  Per target layer lt (with a table): the Gram blocks (j1 <= j2)
+// columns.  Per target layer: its own Gram block (the trace is the centred
+// total sum of squares).  Per target layer lt (with a table): the Gram blocks (j1 <= j2)
 // of its set, A = layer sets[lt][j1], B = layer sets[lt][j2], and its k cross
 // blocks against layer lt's d columns.  Plane row of layer L, dim i: L d + i
 // (target layer lt is L = Ls + lt).  With d < 128 a block's extra rows are
@@ -281,10 +283,19 @@ __global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ X,
 struct ScoreTiles {
   int Ls, Lt, d, k, nq, layer_tiles;
   const int32_t *sets;
-  double *G, *C, *Gs, *Cs;
+  double *G, *C, *Gy, *Gs, *Cs;
   __device__ MomTile tile(int t) const {
     MomTile m;
     m.m_valid = d;
+    if (t >= layer_tiles && t < layer_tiles + Lt) {   // a target layer's own Gram block
+      const int lt = t - layer_tiles;
+      m.a_row = m.b_row = (Ls + lt) * d;
+      m.n_split = m.n_valid = d;
+      m.out0 = m.out1 = Gy + (int64_t)lt * d * d;
+      m.ld0 = m.ld1 = d;
+      return m;
+    }
+    if (t >= layer_tiles) t -= Lt;
     if (t < layer_tiles) {
       const int s = t / (1 + nq), j = t % (1 + nq);
       m.a_row = s * d;
@@ -359,6 +370,147 @@ __global__ void __launch_bounds__(kSolveThreads) solve_norms_kernel(
   }
 }
 
+// 4'. The per-layer fits without per-column solves.  With G_lam = G + lam I,
+// M = G_lam^-1 and W = M C, the explained sum of squares of a target block
+// C is |L^-1 C|^2 + lam |W|^2 = tr(C^T (M + lam M M) C) = |R^T C|^2 for
+// N = M + lam M M = R R^T.  Per source layer: M from the factor of G_lam
+// (column solves against the identity), N, the Cholesky factor R of N, and
+// then one triangular product R^T C over all Lt d target columns: half the
+// multiply-adds of the forward and back solves, and no chain of dependent
+// steps per column.
+
+// a. Per (source layer s, nc columns): columns of M = G_lam^-1.
+__global__ void __launch_bounds__(kSolveThreads) inverse_kernel(const double *__restrict__ G,
+                                                                int d, int nc,
+                                                                double *__restrict__ Minv) {
+  extern __shared__ double cols[];   // [d][nc], then d reciprocals
+  const int s = blockIdx.x, c0 = blockIdx.y * nc;
+  const double *A = G + (int64_t)s * d * d;
+  double *M = Minv + (int64_t)s * d * d;
+  if (isnan(A[0])) {
+    if (blockIdx.y == 0 && threadIdx.x == 0) M[0] = nan("");
+    return;
+  }
+  for (int e = threadIdx.x; e < d * nc; e += kSolveThreads)
+    cols[e] = e / nc == c0 + e % nc ? 1.0 : 0.0;
+  double zn, wn;
+  chol_solve_cols(A, d, cols, cols + (size_t)d * nc, nc, zn, wn);
+  for (int e = threadIdx.x; e < d * nc; e += kSolveThreads)
+    if (c0 + e % nc < d) M[(int64_t)(e / nc) * d + c0 + e % nc] = cols[e];
+}
+
+// b. N = M + lam M M per source layer, the full symmetric matrix, 64 x 64
+// output tiles (4 x 4 per thread, 16 rows of K per step).
+__global__ void __launch_bounds__(256) bridge_n_kernel(const double *__restrict__ Minv, int d,
+                                                       double lam, double *__restrict__ N) {
+  __shared__ double sa[16][65], sb[16][65];
+  const int s = blockIdx.z, i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  const double *M = Minv + (int64_t)s * d * d;
+  double *O = N + (int64_t)s * d * d;
+  if (isnan(M[0])) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) O[0] = nan("");
+    return;
+  }
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  double acc[4][4] = {};
+  for (int k0 = 0; k0 < d; k0 += 16) {
+    for (int e = tid; e < 16 * 64; e += 256) {
+      const int kk = e / 64, ii = e % 64;
+      sa[kk][ii] = i0 + ii < d ? M[(int64_t)(i0 + ii) * d + k0 + kk] : 0.0;   // M symmetric
+      sb[kk][ii] = j0 + ii < d ? M[(int64_t)(k0 + kk) * d + j0 + ii] : 0.0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      double a[4], b[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = sa[kk][4 * ty + r], b[r] = sb[kk][4 * tx + r];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fma(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = i0 + 4 * ty + r, j = j0 + 4 * tx + c;
+      if (i < d && j < d) O[(int64_t)i * d + j] = fma(lam, acc[r][c], M[(int64_t)i * d + j]);
+    }
+}
+
+// c. Per (source layer s, 64 target columns), after the factorisation of N:
+// Q = R^T C for the columns (row i of R^T = row i of the factor's upper
+// triangle, k >= i), and |Q|^2 of each column added into zz[s][column / d].
+// Warp w owns rows 16 w .. 16 w + 15 (a lane: 4 rows x 8 columns) and skips
+// the blocks of K below its rows.
+__global__ void __launch_bounds__(256) bridge_norms_kernel(const double *__restrict__ Nf,
+                                                           const double *__restrict__ C, int d,
+                                                           int q, int Lt,
+                                                           double *__restrict__ zz) {
+  __shared__ double sr[kMaxD][17];
+  __shared__ double sc[16][64];
+  __shared__ double red[8][64];
+  const int s = blockIdx.y, c0 = blockIdx.x * 64;
+  const double *A = Nf + (int64_t)s * d * d;
+  if (isnan(A[0])) return;
+  const double *Cs = C + (int64_t)s * d * q;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rq = lane >> 3, cg = lane & 7;
+  const int i0 = warp * 16 + rq * 4;           // rows i0 .. i0 + 3 (d is a multiple of 16)
+  const bool rows_ok = warp * 16 < d;
+  double acc[4][8] = {};
+  for (int k0 = 0; k0 < d; k0 += 16) {
+    for (int e = tid; e < d * 16; e += 256) {
+      const int i = e >> 4, k = k0 + (e & 15);
+      sr[i][e & 15] = k >= i ? A[(int64_t)i * d + k] : 0.0;
+    }
+    for (int e = tid; e < 16 * 64; e += 256) {
+      const int kk = e >> 6, j = e & 63;
+      sc[kk][j] = c0 + j < q ? Cs[(int64_t)(k0 + kk) * q + c0 + j] : 0.0;
+    }
+    __syncthreads();
+    if (rows_ok && k0 + 15 >= warp * 16) {
+#pragma unroll 4
+      for (int kk = 0; kk < 16; ++kk) {
+        double r[4], cv[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) r[a] = sr[i0 + a][kk];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) cv[c] = sc[kk][8 * cg + c];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) acc[a][c] = fma(r[a], cv[c], acc[a][c]);
+      }
+    }
+    __syncthreads();
+  }
+  double part[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    double v = 0.0;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) v = fma(acc[a][c], acc[a][c], v);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 16);
+    part[c] = rows_ok ? v : 0.0;
+  }
+  if (rq == 0) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) red[warp][8 * cg + c] = part[c];
+  }
+  __syncthreads();
+  if (tid < 64 && c0 + tid < q) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += red[w][tid];
+    atomicAdd(zz + (int64_t)s * Lt + (c0 + tid) / d, t);
+  }
+}
+
 // 5. The scores of one pass: r2 = (|Z|^2 + lam |W|^2) / sum |Yc|^2.
 __global__ void finalize_kernel(const Pass ps, int Ls, int Lt, int H, int d, int h, int m,
                                 int64_t n, double lam, double *__restrict__ r2,
@@ -371,8 +523,8 @@ __global__ void finalize_kernel(const Pass ps, int Ls, int Lt, int H, int d, int
     if (r2_set) {
       bool ok = !bad;
       for (int j = 0; j < k; ++j) ok = ok && idx[e * k + j] >= 0 && idx[e * k + j] < Ls;
-      double tot = ps.yss[e];
-      for (int i = 0; i < d; ++i) tot -= ps.ys[(int64_t)e * d + i] * ps.ys[(int64_t)e * d + i] / (double)n;
+      double tot = 0.0;
+      for (int i = 0; i < d; ++i) tot += ps.Gy[((int64_t)e * d + i) * d + i];
       const bool spd = !isnan(ps.Gs[(int64_t)e * k * d * k * d]);
       double v = nan("");
       if (ok && spd && tot > 0.0) v = (ps.zzs[e] + lam * ps.wws[e]) / tot;
@@ -381,9 +533,9 @@ __global__ void finalize_kernel(const Pass ps, int Ls, int Lt, int H, int d, int
   }
   if (e < Ls * Lt) {
     const int s = e / Lt, lt = e % Lt;
-    double tot = ps.yss[lt];
-    for (int i = 0; i < d; ++i) tot -= ps.ys[(int64_t)lt * d + i] * ps.ys[(int64_t)lt * d + i] / (double)n;
-    const bool spd = !isnan(ps.G[(int64_t)s * d * d]);
+    double tot = 0.0;
+    for (int i = 0; i < d; ++i) tot += ps.Gy[((int64_t)lt * d + i) * d + i];
+    const bool spd = !isnan(ps.G[(int64_t)s * d * d]) && !isnan(ps.N[(int64_t)s * d * d]);
     double v = nan("");
     if (!bad && spd && tot > 0.0) v = (ps.zz[(int64_t)s * Lt + lt] + lam * ps.ww[(int64_t)s * Lt + lt]) / tot;
     r2[(((int64_t)lt * Ls + s) * H + h) * 2 + m] = v;
@@ -451,9 +603,11 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   ps.planes = reinterpret_cast<float *>(ws + lay.planes);
   ps.xs = reinterpret_cast<double *>(ws + lay.xs);
   ps.ys = reinterpret_cast<double *>(ws + lay.ys);
-  ps.yss = reinterpret_cast<double *>(ws + lay.yss);
   ps.G = reinterpret_cast<double *>(ws + lay.G);
   ps.C = reinterpret_cast<double *>(ws + lay.C);
+  ps.M = reinterpret_cast<double *>(ws + lay.M);
+  ps.N = reinterpret_cast<double *>(ws + lay.N);
+  ps.Gy = reinterpret_cast<double *>(ws + lay.Gy);
   ps.zz = reinterpret_cast<double *>(ws + lay.zz);
   ps.ww = reinterpret_cast<double *>(ws + lay.ww);
   ps.Gs = reinterpret_cast<double *>(ws + lay.Gs);
@@ -479,14 +633,15 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   const int pk = k * D;
   const int rows = (Ls + Lt) * D;
   const int nq = (q1 + kMomRows - 1) / kMomRows;
-  const ScoreTiles tiles{Ls, Lt, D, k, nq, Ls * (1 + nq), set_list, ps.G, ps.C, ps.Gs, ps.Cs};
-  const int num_tiles = tiles.layer_tiles + (sets ? Lt * (k * (k + 1) / 2 + k) : 0);
-  // the per-pass fp64 region: sums, yss, G, C, zz, ww, Gs, Cs, zzs, wws
+  const ScoreTiles tiles{Ls, Lt, D, k, nq, Ls * (1 + nq), set_list, ps.G, ps.C, ps.Gy, ps.Gs,
+                         ps.Cs};
+  const int num_tiles = tiles.layer_tiles + Lt + (sets ? Lt * (k * (k + 1) / 2 + k) : 0);
+  // the per-pass fp64 region: sums, G, C, M, N, Gy, zz, ww, Gs, Cs, zzs, wws
   double *clear_from = ps.xs;
   const int64_t clear_words = (int64_t)(lay.bad - lay.xs) / 8;
   const int per_tok = D / 16, tpb = 256 / per_tok;
   dim3 cgrid((unsigned)((n + tpb - 1) / tpb), (unsigned)(Ls + Lt));
-  const int cols1 = solve_cols_per_cta(D, Ls, q1), colsk = solve_cols_per_cta(pk, Lt, D);
+  const int cols1 = solve_cols_per_cta(D, Ls, D), colsk = solve_cols_per_cta(pk, Lt, D);
   for (int h = 0; h < H; ++h) {
     for (int m = 0; m < 2; ++m) {
       clear_kernel<<<1024, 256, 0, s>>>(clear_from, clear_words);
@@ -513,10 +668,15 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
         if (mom_launch(ps.planes, rows, np, tiles, num_tiles, a->status, s) != cudaSuccess)
           return KVX_ERR_CUDA;
       }
+      // per-layer fits: |R^T C|^2 with R R^T = M + lam M M, M = (G + lam I)^-1
       if (chol_factor(ps.G, Ls, D, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
-      solve_norms_kernel<<<dim3((unsigned)Ls, (unsigned)((q1 + cols1 - 1) / cols1)), kSolveThreads,
-                           solve_smem_bytes(D, cols1), s>>>(ps.G, ps.C, D, q1, D, cols1, ps.zz,
-                                                            ps.ww, Lt);
+      inverse_kernel<<<dim3((unsigned)Ls, (unsigned)((D + cols1 - 1) / cols1)), kSolveThreads,
+                       solve_smem_bytes(D, cols1), s>>>(ps.G, D, cols1, ps.M);
+      bridge_n_kernel<<<dim3((unsigned)((D + 63) / 64), (unsigned)((D + 63) / 64), (unsigned)Ls),
+                        256, 0, s>>>(ps.M, D, a->lambda, ps.N);
+      if (chol_factor(ps.N, Ls, D, 0.0, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
+      bridge_norms_kernel<<<dim3((unsigned)((q1 + 63) / 64), (unsigned)Ls), 256, 0, s>>>(
+          ps.N, ps.C, D, q1, Lt, ps.zz);
       if (sets) {
         if (chol_factor(ps.Gs, Lt, pk, a->lambda, a->status, s) != cudaSuccess)
           return KVX_ERR_CUDA;
