@@ -183,6 +183,165 @@ __global__ void __launch_bounds__(256) chol_update_kernel(double *__restrict__ G
 }
 
 // Launch the whole factorisation (4 + 3 (p / 64 rounded up) - 1 launches).
+// ---------------------------------------------------------------------------
+// Blocked column solves (p <= kBlkMaxP): forward L Z = C and back L^T W = Z
+// by 64-row blocks.  Per block, the right-hand side minus the product of the
+// factor's panel with the rows already solved (a GEMM from shared memory),
+// then the block's inverse diagonal block (chol_block_inverse_kernel); so
+// nearly all of the fp64 work is GEMM-shaped and the fp64 pipe stays busy.
+// ---------------------------------------------------------------------------
+constexpr int kBlkCols = 16;      // columns per CTA
+constexpr int kBlkThreads = 256;  // 16 row groups of 4 rows x 16 columns
+constexpr int kBlkMaxP = 1024;
+
+inline size_t blk_solve_smem_bytes(int p) {
+  return ((size_t)p * kBlkCols + (size_t)kB * kBlkCols + (size_t)kB * 33) * sizeof(double);
+}
+
+// Inverse of each 64 x 64 diagonal block of L: Dinv[fit][blk] (row-major,
+// lower triangular; rows beyond p read as the identity).  One thread per
+// column j of the inverse X, in fp64: X[j][j] = 1 / L[j][j] and, for i > j,
+// X[i][j] = -(sum_{j <= k < i} L[i][k] X[k][j]) / L[i][i].  S holds L's
+// strictly lower part and X's strictly lower part transposed (X[i][j] at
+// S[j][i]); r holds the reciprocals of L's diagonal.
+__global__ void __launch_bounds__(kB) chol_block_inverse_kernel(const double *__restrict__ G,
+                                                                int p,
+                                                                double *__restrict__ Dinv) {
+  __shared__ double S[kB][kB + 1];
+  __shared__ double r[kB];
+  const int b = blockIdx.x, blk = blockIdx.y, nblk = (p + kB - 1) / kB;
+  const double *A = G + (int64_t)b * p * p;
+  if (isnan(A[0])) return;
+  const int o = blk * kB, nb = blk_len(p, blk), j = threadIdx.x;
+  for (int i = j + 1; i < kB; ++i)
+    S[i][j] = i < nb ? A[(int64_t)(o + i) * p + o + j] : 0.0;
+  r[j] = j < nb ? 1.0 / A[(int64_t)(o + j) * p + o + j] : 1.0;
+  __syncthreads();
+  for (int i = j + 1; i < kB; ++i) {
+    double acc = S[i][j] * r[j];                  // k = j: L[i][j] X[j][j]
+    for (int k = j + 1; k < i; ++k) acc = fma(S[i][k], S[j][k], acc);
+    S[j][i] = -acc * r[i];
+  }
+  __syncthreads();
+  double *D = Dinv + ((int64_t)b * nblk + blk) * kB * kB;
+  for (int i = 0; i < kB; ++i) D[i * kB + j] = i > j ? S[j][i] : (i == j ? r[i] : 0.0);
+}
+
+// Per (fit b, kBlkCols columns of C [p][q]): Z and W in shared memory, then
+// epi(b, c0, col, zn, wn): col holds W ([p][kBlkCols]); zn and wn are the
+// column's |z|^2 and |w|^2 in threads t < kBlkCols.  A fit whose factor
+// failed gets epi.failed(b, c0).
+template <typename Epi>
+__global__ void __launch_bounds__(kBlkThreads) chol_solve_blocked_kernel(
+    const double *__restrict__ G, const double *__restrict__ Dinv, const double *__restrict__ C,
+    int p, int q, Epi epi) {
+  extern __shared__ double sm[];
+  double *Z = sm;                                   // [p][kBlkCols]
+  double *T = Z + (size_t)p * kBlkCols;             // [64][kBlkCols]
+  double *Lp = T + (size_t)kB * kBlkCols;           // [64][33] panel tile
+  __shared__ double red[16][kBlkCols + 1];
+  const int b = blockIdx.x, c0 = blockIdx.y * kBlkCols, nblk = (p + kB - 1) / kB;
+  const double *A = G + (int64_t)b * p * p;
+  if (isnan(A[0])) {
+    epi.failed(b, c0);
+    return;
+  }
+  const double *Cb = C + (int64_t)b * p * q;
+  const int t = threadIdx.x, j = t & (kBlkCols - 1), g = t >> 4;
+  for (int e = t; e < p * kBlkCols; e += kBlkThreads) {
+    const int i = e / kBlkCols, c = e % kBlkCols;
+    Z[e] = c0 + c < q ? Cb[(int64_t)i * q + c0 + c] : 0.0;
+  }
+  __syncthreads();
+  double zsq = 0.0, wsq = 0.0;
+  // forward: Z_blk = Dinv_blk (C_blk - L[blk][< blk] Z[< blk])
+  for (int blk = 0; blk < nblk; ++blk) {
+    const int r0 = blk * kB, nr = blk_len(p, blk);
+    double acc[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) acc[a] = 4 * g + a < nr ? Z[(r0 + 4 * g + a) * kBlkCols + j] : 0.0;
+    for (int k0 = 0; k0 < r0; k0 += 32) {
+      for (int e = t; e < kB * 32; e += kBlkThreads) {
+        const int i = e >> 5, kk = e & 31;
+        Lp[i * 33 + kk] = i < nr ? A[(int64_t)(r0 + i) * p + k0 + kk] : 0.0;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) {
+        const double z = Z[(k0 + kk) * kBlkCols + j];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = fma(-Lp[(4 * g + a) * 33 + kk], z, acc[a]);
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) T[(4 * g + a) * kBlkCols + j] = acc[a];
+    __syncthreads();
+    const double *D = Dinv + ((int64_t)b * nblk + blk) * kB * kB;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = 4 * g + a;
+      double v = 0.0;
+      for (int k = 0; k <= i; ++k) v = fma(__ldg(D + i * kB + k), T[k * kBlkCols + j], v);
+      if (i < nr) {
+        Z[(r0 + i) * kBlkCols + j] = v;
+        zsq = fma(v, v, zsq);
+      }
+    }
+    __syncthreads();
+  }
+  // back: W_blk = Dinv_blk^T (Z_blk - L[> blk][blk]^T W[> blk]); row r0 + i of
+  // L^T is row r0 + i of the factor's upper triangle
+  for (int blk = nblk - 1; blk >= 0; --blk) {
+    const int r0 = blk * kB, nr = blk_len(p, blk);
+    double acc[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) acc[a] = 4 * g + a < nr ? Z[(r0 + 4 * g + a) * kBlkCols + j] : 0.0;
+    for (int k0 = r0 + kB; k0 < p; k0 += 32) {
+      for (int e = t; e < kB * 32; e += kBlkThreads) {
+        const int i = e >> 5, kk = e & 31;
+        Lp[i * 33 + kk] = i < nr && k0 + kk < p ? A[(int64_t)(r0 + i) * p + k0 + kk] : 0.0;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < 32; ++kk) {
+        const double w = k0 + kk < p ? Z[(k0 + kk) * kBlkCols + j] : 0.0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = fma(-Lp[(4 * g + a) * 33 + kk], w, acc[a]);
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) T[(4 * g + a) * kBlkCols + j] = acc[a];
+    __syncthreads();
+    const double *D = Dinv + ((int64_t)b * nblk + blk) * kB * kB;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = 4 * g + a;
+      double v = 0.0;
+      for (int k = i; k < nr; ++k) v = fma(__ldg(D + k * kB + i), T[k * kBlkCols + j], v);
+      if (i < nr) {
+        Z[(r0 + i) * kBlkCols + j] = v;
+        wsq = fma(v, v, wsq);
+      }
+    }
+    __syncthreads();
+  }
+  red[g][j] = zsq;
+  __syncthreads();
+  double zn = 0.0, wn = 0.0;
+  if (t < kBlkCols) {
+    for (int r = 0; r < 16; ++r) zn += red[r][t];
+  }
+  __syncthreads();
+  red[g][j] = wsq;
+  __syncthreads();
+  if (t < kBlkCols) {
+    for (int r = 0; r < 16; ++r) wn += red[r][t];
+  }
+  epi(b, c0, Z, zn, wn);
+}
+
 constexpr int kSolveThreads = 128;   // threads per CTA of the column solves
 
 // Columns one CTA of a triangular solve holds in shared memory: the largest

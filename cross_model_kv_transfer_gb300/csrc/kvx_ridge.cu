@@ -203,12 +203,43 @@ __global__ void __launch_bounds__(kSolveThreads) trsm_kernel(
   }
 }
 
+// Epilogue of the blocked solves: W (fp32) and b = ybar - xbar W of the
+// CTA's columns.
+struct RidgeEpi {
+  const double *sums;
+  int64_t n;
+  int p, q;
+  float *W, *bias;
+  __device__ void operator()(int b, int c0, const double *col, double, double) const {
+    for (int e = threadIdx.x; e < p * kBlkCols; e += blockDim.x) {
+      const int i = e / kBlkCols, c = e % kBlkCols;
+      if (c0 + c < q) W[((int64_t)b * p + i) * q + c0 + c] = (float)col[e];
+    }
+    if (threadIdx.x < kBlkCols && c0 + (int)threadIdx.x < q) {
+      const double *mx = sums + (int64_t)b * (p + q);
+      const double inv_n = 1.0 / (double)n;
+      double s = 0.0;
+      for (int i = 0; i < p; ++i) s = fma(mx[i] * inv_n, col[i * kBlkCols + threadIdx.x], s);
+      bias[(int64_t)b * q + c0 + threadIdx.x] = (float)(mx[p + c0 + threadIdx.x] * inv_n - s);
+    }
+  }
+  __device__ void failed(int b, int c0) const {
+    for (int e = threadIdx.x; e < p * kBlkCols; e += blockDim.x) {
+      const int i = e / kBlkCols, c = e % kBlkCols;
+      if (c0 + c < q) W[((int64_t)b * p + i) * q + c0 + c] = nanf("");
+    }
+    if (threadIdx.x < kBlkCols && c0 + (int)threadIdx.x < q)
+      bias[(int64_t)b * q + c0 + threadIdx.x] = nanf("");
+  }
+};
+
 constexpr int kMaxDim = 4096;
 
 size_t ws_sums(int batch, int p, int q) { return (size_t)batch * (p + q) * sizeof(double); }
 size_t ws_gram(int batch, int p) { return (size_t)batch * p * p * sizeof(double); }
 size_t ws_cross(int batch, int p, int q) { return (size_t)batch * p * q * sizeof(double); }
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t ws_dinv(int batch, int p) { return (size_t)batch * ((p + 63) / 64) * 64 * 64 * 8; }
 size_t ws_planes(int batch, int p, int q) {
   return (size_t)2 * batch * (p + q) * kMomChunk * sizeof(float);
 }
@@ -218,7 +249,7 @@ size_t ws_planes(int batch, int p, int q) {
 extern "C" size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q) {
   if (batch < 1 || p < 1 || q < 1 || p > kMaxDim || q > kMaxDim) return 0;
   return round256(ws_sums(batch, p, q)) + round256(ws_gram(batch, p)) +
-         round256(ws_cross(batch, p, q)) + ws_planes(batch, p, q);
+         round256(ws_cross(batch, p, q)) + round256(ws_planes(batch, p, q)) + ws_dinv(batch, p);
 }
 
 extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
@@ -282,14 +313,29 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   }
   // blocked fp64 Cholesky
   if (chol_factor(G, batch, p, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
-  // triangular solves: nc output columns per CTA, in shared memory
-  const int nc = solve_cols_per_cta(p, batch, q);
-  if (solve_smem_bytes(p, nc) > 48 * 1024 &&
-      cudaFuncSetAttribute(trsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)solve_smem_bytes(p, nc)) != cudaSuccess)
-    return KVX_ERR_CUDA;
-  dim3 tgrid((unsigned)batch, (unsigned)((q + nc - 1) / nc));
-  trsm_kernel<<<tgrid, kSolveThreads, solve_smem_bytes(p, nc), s>>>(G, C, sums, n, p, q, nc,
-                                                                    a->w, a->b);
+  // triangular solves: by 64-row blocks (p <= 1024), else right-looking
+  // with nc output columns per CTA in shared memory
+  if (p <= kBlkMaxP) {
+    double *dinv = reinterpret_cast<double *>(reinterpret_cast<unsigned char *>(planes) +
+                                              round256(ws_planes(batch, p, q)));
+    chol_block_inverse_kernel<<<dim3((unsigned)batch, (unsigned)((p + 63) / 64)), 64, 0, s>>>(
+        G, p, dinv);
+    if (cudaFuncSetAttribute(chol_solve_blocked_kernel<RidgeEpi>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)blk_solve_smem_bytes(p)) != cudaSuccess)
+      return KVX_ERR_CUDA;
+    chol_solve_blocked_kernel<RidgeEpi>
+        <<<dim3((unsigned)batch, (unsigned)((q + kBlkCols - 1) / kBlkCols)), kBlkThreads,
+           blk_solve_smem_bytes(p), s>>>(G, dinv, C, p, q, RidgeEpi{sums, n, p, q, a->w, a->b});
+  } else {
+    const int nc = solve_cols_per_cta(p, batch, q);
+    if (solve_smem_bytes(p, nc) > 48 * 1024 &&
+        cudaFuncSetAttribute(trsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)solve_smem_bytes(p, nc)) != cudaSuccess)
+      return KVX_ERR_CUDA;
+    dim3 tgrid((unsigned)batch, (unsigned)((q + nc - 1) / nc));
+    trsm_kernel<<<tgrid, kSolveThreads, solve_smem_bytes(p, nc), s>>>(G, C, sums, n, p, q, nc,
+                                                                      a->w, a->b);
+  }
   return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;
 }

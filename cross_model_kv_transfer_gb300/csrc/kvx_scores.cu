@@ -31,8 +31,9 @@
 //      M = (G + lam I)^-1, N = M + lam M M = R R^T (a second Cholesky), and
 //      |Z|^2 + lam |W|^2 = |R^T C|^2 per target layer as one triangular
 //      product per source layer;
-//   4. set fits: the Cholesky of each set's Gram block and fp64 forward and
-//      back substitution per column, keeping only |z|^2 and |w|^2;
+//   4. set fits: the Cholesky of each set's Gram block, the inverses of its
+//      64 x 64 diagonal blocks, and fp64 forward and back substitution by
+//      64-row blocks (kvx_chol.cuh), keeping only |z|^2 and |w|^2;
 //   5. the scores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -72,13 +73,14 @@ struct Pass {
   double *Gs;        // [Lt][k*d][k*d]   (sets)
   double *Cs;        // [Lt][k*d][d]
   double *zzs, *wws; // [Lt]
+  double *Dinv;      // [Lt][k d / 64][64][64] inverse diagonal blocks of the sets' factors
   int *bad;          // [1]: the transfer-wide validity (positions, request table)
 };
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t X, planes, xs, ys, G, C, M, N, Gy, zz, ww, Gs, Cs, zzs, wws, bad, total;
+  size_t X, planes, xs, ys, G, C, M, N, Gy, zz, ww, Gs, Cs, zzs, wws, Dinv, bad, total;
 };
 
 // Tokens per plane chunk, padded to the tensor-core block.
@@ -108,6 +110,7 @@ Layout layout_of(int64_t Ls, int64_t Lt, int64_t d, int64_t k, int64_t n) {
   L.Cs = take((size_t)Lt * k * d * d * 8);
   L.zzs = take((size_t)Lt * 8);
   L.wws = take((size_t)Lt * 8);
+  L.Dinv = take((size_t)Lt * ((k * d + 63) / 64) * 64 * 64 * 8);
   L.bad = take(16);
   L.total = at;
   return L;
@@ -511,6 +514,19 @@ __global__ void __launch_bounds__(256) bridge_norms_kernel(const double *__restr
   }
 }
 
+// Epilogue of the blocked set solves: |z|^2 and |w|^2 of each column.
+struct NormsEpi {
+  double *zz, *ww;
+  int q;
+  __device__ void operator()(int b, int c0, const double *, double zn, double wn) const {
+    if (threadIdx.x < kBlkCols && c0 + (int)threadIdx.x < q) {
+      atomicAdd(zz + b, zn);
+      atomicAdd(ww + b, wn);
+    }
+  }
+  __device__ void failed(int, int) const {}
+};
+
 // 5. The scores of one pass: r2 = (|Z|^2 + lam |W|^2) / sum |Yc|^2.
 __global__ void finalize_kernel(const Pass ps, int Ls, int Lt, int H, int d, int h, int m,
                                 int64_t n, double lam, double *__restrict__ r2,
@@ -614,6 +630,7 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   ps.Cs = reinterpret_cast<double *>(ws + lay.Cs);
   ps.zzs = reinterpret_cast<double *>(ws + lay.zzs);
   ps.wws = reinterpret_cast<double *>(ws + lay.wws);
+  ps.Dinv = reinterpret_cast<double *>(ws + lay.Dinv);
   ps.bad = reinterpret_cast<int *>(ws + lay.bad);
   int32_t *set_list = reinterpret_cast<int32_t *>(ws + lay.total);
 
@@ -642,6 +659,11 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
   const int per_tok = D / 16, tpb = 256 / per_tok;
   dim3 cgrid((unsigned)((n + tpb - 1) / tpb), (unsigned)(Ls + Lt));
   const int cols1 = solve_cols_per_cta(D, Ls, D), colsk = solve_cols_per_cta(pk, Lt, D);
+  if (sets && pk <= kBlkMaxP &&
+      cudaFuncSetAttribute(chol_solve_blocked_kernel<NormsEpi>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)blk_solve_smem_bytes(pk)) != cudaSuccess)
+    return KVX_ERR_CUDA;
   for (int h = 0; h < H; ++h) {
     for (int m = 0; m < 2; ++m) {
       clear_kernel<<<1024, 256, 0, s>>>(clear_from, clear_words);
@@ -680,9 +702,18 @@ extern "C" kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_arg
       if (sets) {
         if (chol_factor(ps.Gs, Lt, pk, a->lambda, a->status, s) != cudaSuccess)
           return KVX_ERR_CUDA;
-        solve_norms_kernel<<<dim3((unsigned)Lt, (unsigned)((D + colsk - 1) / colsk)),
-                             kSolveThreads, solve_smem_bytes(pk, colsk), s>>>(
-            ps.Gs, ps.Cs, pk, D, D, colsk, ps.zzs, ps.wws, 1);
+        if (pk <= kBlkMaxP) {
+          chol_block_inverse_kernel<<<dim3((unsigned)Lt, (unsigned)((pk + 63) / 64)), 64, 0, s>>>(
+              ps.Gs, pk, ps.Dinv);
+          chol_solve_blocked_kernel<NormsEpi>
+              <<<dim3((unsigned)Lt, (unsigned)((D + kBlkCols - 1) / kBlkCols)), kBlkThreads,
+                 blk_solve_smem_bytes(pk), s>>>(ps.Gs, ps.Dinv, ps.Cs, pk, D,
+                                                NormsEpi{ps.zzs, ps.wws, D});
+        } else {
+          solve_norms_kernel<<<dim3((unsigned)Lt, (unsigned)((D + colsk - 1) / colsk)),
+                               kSolveThreads, solve_smem_bytes(pk, colsk), s>>>(
+              ps.Gs, ps.Cs, pk, D, D, colsk, ps.zzs, ps.wws, 1);
+        }
       }
       finalize_kernel<<<(Ls * Lt + 255) / 256 + 1, 256, 0, s>>>(
           ps, Ls, Lt, H, D, h, m, n, a->lambda, a->r2, a->r2_set, a->layer_idx, k, a->status);

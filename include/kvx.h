@@ -346,10 +346,11 @@ typedef struct {
 } kvx_ridge_args;
 
 /* Bytes of scratch a kvx_ridge_fit call with these sizes needs: fp64 column
- * sums, Gram blocks and cross products (8 * batch * (p + q + p*p + p*q),
- * each part rounded up to 256 bytes) and the split-precision planes of one
- * chunk of 16,384 observations (2 * 4 * batch * (p + q) * 16384 bytes); 0 for
- * sizes outside the limits above. */
+ * sums, Gram blocks and cross products (8 * batch * (p + q + p*p + p*q)),
+ * the split-precision planes of one chunk of 16,384 observations
+ * (2 * 4 * batch * (p + q) * 16384 bytes) and the inverses of the factor's
+ * 64 x 64 diagonal blocks (8 * batch * ceil(p / 64) * 4096), each part but the
+ * last rounded up to 256 bytes; 0 for sizes outside the limits above. */
 size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
 
 /* Fit the maps: for each fit, W = (XcT Xc + lambda I)^-1 XcT Yc and
