@@ -131,6 +131,16 @@ def test_scores_match_oracle_head_dim_128_with_explicit_positions():
     assert np.abs(gs - rs).max() <= ATOL, np.abs(gs - rs).max()
 
 
+def test_scores_over_several_token_chunks_match_oracle():
+    # 20,000 + 13,001 tokens: the tensor-core moments run over three chunks
+    # of up to 16,384 tokens (the last one ragged), summed in fp64
+    c = Case(Ls=3, Lt=2, H=1, d=16, k=2, lens=(20000, 13001), dtype=torch.bfloat16)
+    g, gs, st, r, rs, rst = run_both(c, make_case(c, 15))
+    assert st == 0 and rst == 0
+    assert np.abs(g - r).max() <= ATOL, np.abs(g - r).max()
+    assert np.abs(gs - rs).max() <= ATOL, np.abs(gs - rs).max()
+
+
 def test_scores_nan_and_flags_for_bad_inputs():
     c = Case(Ls=3, Lt=2, H=1, d=16, k=2, lens=(40, 24))
     inp = make_case(c, 13)
