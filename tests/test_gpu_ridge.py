@@ -149,3 +149,20 @@ def test_ridge_fit_wide_feature_block_solves_in_large_shared_memory():
     assert np.linalg.norm(bg - br) / np.linalg.norm(br) <= max(1e-5, 1e-6 * kappa)
     pg, pr = xs @ wg + bg, xs @ wr + br
     assert np.linalg.norm(pg - pr) / np.linalg.norm(pr) <= 1e-5
+
+
+def test_ridge_fit_centres_before_the_products_large_offsets():
+    # features and targets whose means are ~100x their spread: the Gram
+    # blocks are formed from centred values, so no cancellation eats the
+    # split-precision products (an uncentred XtX - n mu mu^T would lose ~4
+    # digits here)
+    g = torch.Generator(device="cuda").manual_seed(31)
+    n, p, q = 6000, 64, 16
+    x = torch.randn((1, n, p), generator=g, device="cuda") + \
+        100.0 * (1.0 + torch.rand((1, 1, p), generator=g, device="cuda"))
+    w = torch.randn((p, q), generator=g, device="cuda") / p ** 0.5
+    y = (x - x.mean(dim=1, keepdim=True)) @ w + 300.0 + \
+        0.1 * torch.randn((1, n, q), generator=g, device="cuda")
+    wg, bg = kvx.ridge_fit(x.contiguous(), y.contiguous(), lam=0.01)
+    torch.cuda.synchronize()
+    _check(x, y, wg, bg, 0.01)

@@ -248,3 +248,17 @@ def test_scores_full_size_sampled_entries_match_oracle():
         assert err <= ATOL, (lt, h, err)
     print(f"layer scores at 4,096 tokens: worst sampled |r2 - oracle| {worst:.2e}; "
           f"mean best single layer {g.max(axis=1).mean(axis=(0, 1))}, mean set {gs.mean(axis=(0, 1))}")
+
+
+def test_scores_with_large_means_match_oracle():
+    # caches whose content means are ~50x their spread (values only, keys
+    # carry the same offsets before rotation): the totals and moments come
+    # from centred values
+    c = Case(Ls=3, Lt=2, H=2, d=32, k=2, lens=(900,), dtype=torch.float32)
+    inp = make_case(c, 16)
+    for name in ("src_v", "tgt_v"):
+        inp[name] = inp[name] + 50.0
+    g, gs, st, r, rs, rst = run_both(c, inp)
+    assert st == 0 and rst == 0
+    assert np.abs(g - r).max() <= ATOL, np.abs(g - r).max()
+    assert np.abs(gs - rs).max() <= ATOL, np.abs(gs - rs).max()
