@@ -194,8 +194,11 @@ constexpr int kBlkCols = 16;      // columns per CTA
 constexpr int kBlkThreads = 256;  // 16 row groups of 4 rows x 16 columns
 constexpr int kBlkMaxP = 1024;
 
+// Shared memory of a blocked solve: the columns [p][kBlkCols], T [64][kBlkCols]
+// and one buffer that holds either a [64][33] panel tile or a [64][65]
+// inverse diagonal block (rows padded against bank conflicts).
 inline size_t blk_solve_smem_bytes(int p) {
-  return ((size_t)p * kBlkCols + (size_t)kB * kBlkCols + (size_t)kB * 33) * sizeof(double);
+  return ((size_t)p * kBlkCols + (size_t)kB * kBlkCols + (size_t)kB * (kB + 1)) * sizeof(double);
 }
 
 // Inverse of each 64 x 64 diagonal block of L: Dinv[fit][blk] (row-major,
@@ -238,7 +241,8 @@ __global__ void __launch_bounds__(kBlkThreads) chol_solve_blocked_kernel(
   extern __shared__ double sm[];
   double *Z = sm;                                   // [p][kBlkCols]
   double *T = Z + (size_t)p * kBlkCols;             // [64][kBlkCols]
-  double *Lp = T + (size_t)kB * kBlkCols;           // [64][33] panel tile
+  double *Lp = T + (size_t)kB * kBlkCols;           // [64][33] panel tile, or
+  double *Ds = Lp;                                  // [64][65] inverse diagonal block
   __shared__ double red[16][kBlkCols + 1];
   const int b = blockIdx.x, c0 = blockIdx.y * kBlkCols, nblk = (p + kB - 1) / kB;
   const double *A = G + (int64_t)b * p * p;
@@ -278,11 +282,13 @@ __global__ void __launch_bounds__(kBlkThreads) chol_solve_blocked_kernel(
     for (int a = 0; a < 4; ++a) T[(4 * g + a) * kBlkCols + j] = acc[a];
     __syncthreads();
     const double *D = Dinv + ((int64_t)b * nblk + blk) * kB * kB;
+    for (int e = t; e < kB * kB; e += kBlkThreads) Ds[(e >> 6) * (kB + 1) + (e & 63)] = D[e];
+    __syncthreads();
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const int i = 4 * g + a;
       double v = 0.0;
-      for (int k = 0; k <= i; ++k) v = fma(__ldg(D + i * kB + k), T[k * kBlkCols + j], v);
+      for (int k = 0; k <= i; ++k) v = fma(Ds[i * (kB + 1) + k], T[k * kBlkCols + j], v);
       if (i < nr) {
         Z[(r0 + i) * kBlkCols + j] = v;
         zsq = fma(v, v, zsq);
@@ -315,11 +321,13 @@ __global__ void __launch_bounds__(kBlkThreads) chol_solve_blocked_kernel(
     for (int a = 0; a < 4; ++a) T[(4 * g + a) * kBlkCols + j] = acc[a];
     __syncthreads();
     const double *D = Dinv + ((int64_t)b * nblk + blk) * kB * kB;
+    for (int e = t; e < kB * kB; e += kBlkThreads) Ds[(e >> 6) * (kB + 1) + (e & 63)] = D[e];
+    __syncthreads();
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const int i = 4 * g + a;
       double v = 0.0;
-      for (int k = i; k < nr; ++k) v = fma(__ldg(D + k * kB + i), T[k * kBlkCols + j], v);
+      for (int k = i; k < nr; ++k) v = fma(Ds[k * (kB + 1) + i], T[k * kBlkCols + j], v);
       if (i < nr) {
         Z[(r0 + i) * kBlkCols + j] = v;
         wsq = fma(v, v, wsq);
