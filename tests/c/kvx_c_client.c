@@ -64,6 +64,9 @@ int main(void) {
     return 8;
   memset(&r, 0, sizeof r);
   if (kvx_ridge_fit(&r, NULL) != KVX_ERR_INVALID_ARG) return 9;
+  if (kvx_layer_scores(NULL, NULL, NULL) != KVX_ERR_INVALID_ARG ||
+      kvx_layer_scores_workspace_bytes(NULL, 4096) != 0)
+    return 13;
   memset(&g, 0, sizeof g);
   if (kvx_kv_diagnostics(NULL, &g, NULL) != KVX_ERR_INVALID_ARG) return 10;
 

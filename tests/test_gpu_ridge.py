@@ -127,6 +127,11 @@ def test_host_rejects_a_small_workspace():
     ws = torch.empty(need - 8, dtype=torch.uint8, device="cuda")
     with pytest.raises(kvx.KvxError):
         kvx.ridge_fit(x, y, workspace=ws)
+    # large enough but not 16-byte aligned (the split-precision planes are
+    # read by TMA)
+    ws = torch.empty(need + 8, dtype=torch.uint8, device="cuda")[8:]
+    with pytest.raises(kvx.KvxError):
+        kvx.ridge_fit(x, y, workspace=ws)
 
 
 def test_ridge_fit_wide_feature_block_solves_in_large_shared_memory():

@@ -185,6 +185,9 @@ def test_scores_refuse_bad_arguments_before_launch():
     a.r2_set = r2.data_ptr()                       # a set output without a table
     assert kvx.kvx_layer_scores(plan.handle, a, None) == kvx.KVX_ERR_INVALID_ARG
     a.r2_set = None
+    ws3 = torch.empty(need + 8, dtype=torch.uint8, device="cuda")
+    a.workspace, a.workspace_bytes = ws3.data_ptr() + 8, need    # not 16-byte aligned
+    assert kvx.kvx_layer_scores(plan.handle, a, None) == kvx.KVX_ERR_INVALID_ARG
     a.workspace_bytes = need
     ws2 = torch.empty(need, dtype=torch.uint8, device="cuda")
     a.workspace = ws2.data_ptr()
