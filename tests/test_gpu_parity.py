@@ -243,6 +243,31 @@ def test_tcgen05_selection_counts_and_item_sizes(k, tiles_per_item, flags):
 
 @pytest.mark.parametrize("flags", [pytest.param(0, id="pairs"),
                                    pytest.param(kvx.KVX_PLAN_TC_SINGLE_CTA, id="single_cta")])
+def test_tcgen05_schedules_agree_bit_for_bit(flags):
+    # the pipeline's scheduling must not touch the arithmetic: work items of
+    # 1, 3 and 32 tiles (W reloaded every tile, every 3 tiles, once; the
+    # stage and operand rings wrap at different points) give the same bytes
+    base = WORKLOADS["llama31_8b_70b_paged"].with_tokens([900, 130, 2200], [3, 64, 0])
+    wl = dataclasses.replace(base, tgt_layers=6)
+    inp = make_inputs(wl, "cuda")
+    outs = []
+    for tpi in (1, 3, 32):
+        plan = kvx.Plan(src_layers=wl.src_layers, tgt_layers=wl.tgt_layers,
+                        kv_heads=wl.kv_heads, head_dim=wl.head_dim, k=wl.k,
+                        rope_theta_src=wl.theta_src, rope_theta_tgt=wl.theta_tgt,
+                        max_position=wl.max_position, kv_dtype=wl.kv_dtype,
+                        w_dtype=torch.float32, b_dtype=wl.b_dtype, layout=wl.layout,
+                        block_size=wl.block_size, kernel=kvx.KVX_KERNEL_TCGEN05,
+                        tiles_per_item=tpi, flags=flags)
+        gk, gv, st, _ = run_gpu(wl, inp, plan=plan)
+        assert st == 0
+        outs.append((gk.view(torch.int16), gv.view(torch.int16)))
+    for gk, gv in outs[1:]:
+        assert torch.equal(gk, outs[0][0]) and torch.equal(gv, outs[0][1])
+
+
+@pytest.mark.parametrize("flags", [pytest.param(0, id="pairs"),
+                                   pytest.param(kvx.KVX_PLAN_TC_SINGLE_CTA, id="single_cta")])
 def test_tcgen05_pipeline_wait_gives_up_and_reports_timeout(flags):
     # Failure detection without a GPU fault: the operand-filling warps never
     # signal, every pipeline wait gives up after its limit, the kernel drains,
