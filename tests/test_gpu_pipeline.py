@@ -11,7 +11,6 @@ the chosen table (both are the R^2 of the same centred ridge fit on the same
 tokens), up to the rounding of the transfer's bf16 output (measured 1.4e-5;
 the test allows 1e-4)."""
 import dataclasses
-import math
 
 import numpy as np
 import pytest
