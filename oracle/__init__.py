@@ -28,6 +28,10 @@ What each function computes, and the passages it follows, is documented in
                   the ridge fit on one source layer, or on a set (the Qwen3
                   article's linear-bridge section: layer choice by predictive
                   power).
+* ``ridge_features`` the inputs of those ridge fits in content space: the
+                  table row's source layers side by side (keys un-rotated)
+                  and the target layer's content, per (target layer, head,
+                  K|V) (the same section).
 * ``kv_diagnostics`` KV cosine ("Helm Intelligent Routing", "Reading the
                   retention score") and explained variance (the Qwen3
                   article's linear-structure analysis) of a mapped cache
@@ -140,6 +144,8 @@ def _load():
             lib.kvxo_layer_scores.argtypes = [ctypes.POINTER(_Problem), dp, dp, ctypes.c_double,
                                               dp, ctypes.c_void_p]
             lib.kvxo_layer_scores.restype = ctypes.c_int
+            lib.kvxo_ridge_features.argtypes = [ctypes.POINTER(_Problem), dp, dp, dp, dp]
+            lib.kvxo_ridge_features.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -353,6 +359,34 @@ def layer_scores(*, src_k, src_v, tgt_k, tgt_v, theta_src, theta_tgt, max_positi
     st = _load().kvxo_layer_scores(ctypes.byref(P), _dp(tk), _dp(tv), float(lam), _dp(r2),
                                    None if r2_set is None else r2_set.ctypes.data)
     return r2, r2_set, int(st)
+
+
+def ridge_features(*, src_k, src_v, theta_src, theta_tgt, max_position, layer_idx,
+                   tgt_k=None, tgt_v=None, cu_seqlens=None, src_pos=None):
+    """Content-space inputs of the ridge fits (``kvxo_ridge_features``):
+    x [Lt][H][2][ntok][k d] (the table row's source layers concatenated,
+    keys un-rotated with theta_src) and, with the target caches, y
+    [Lt][H][2][ntok][d] (keys un-rotated with theta_tgt), at every token's
+    position.  src_k / src_v [Ls][ntok][H][d], tgt_k / tgt_v [Lt][ntok][H][d].
+    Returns (x, y or None, status bits)."""
+    sk, sv = _f64(src_k), _f64(src_v)
+    Ls, ntok, H, d = sk.shape
+    idx = np.ascontiguousarray(layer_idx, dtype=np.int32)
+    Lt, k = idx.shape
+    tk = None if tgt_k is None else _f64(tgt_k)
+    tv = None if tgt_v is None else _f64(tgt_v)
+    cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    R = 1 if cu is None else cu.shape[0] - 1
+    sp = None if src_pos is None else np.ascontiguousarray(src_pos, dtype=np.int64)
+    P = _Problem(Ls, Lt, H, d, k, float(theta_src), float(theta_tgt), int(max_position), R,
+                 int(ntok), _vp(cu), _vp(sk), _vp(sv), _vp(idx), None, None, _vp(sp), None,
+                 None, CONTIGUOUS, 0, 1, 0, 0, None)
+    x = np.empty((Lt, H, 2, ntok, k * d))
+    y = None if tk is None else np.empty((Lt, H, 2, ntok, d))
+    st = _load().kvxo_ridge_features(ctypes.byref(P), None if tk is None else _dp(tk),
+                                     None if tv is None else _dp(tv), _dp(x),
+                                     None if y is None else _dp(y))
+    return x, y, int(st)
 
 
 def mean_cosine(stats):

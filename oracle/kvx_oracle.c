@@ -578,3 +578,61 @@ int kvxo_layer_scores(const kvxo_problem *P, const double *tgt_k, const double *
   free(Xs);
   return status;
 }
+
+int kvxo_ridge_features(const kvxo_problem *P, const double *tgt_k, const double *tgt_v,
+                        double *x, double *y) {
+  const int64_t Ls = P->src_layers, Lt = P->tgt_layers, H = P->kv_heads, d = P->head_dim;
+  const int64_t ntok = P->ntok, k = P->k;
+  const int64_t B = Lt * H * 2;
+  const int want_y = y != NULL && tgt_k != NULL && tgt_v != NULL;
+  for (int64_t e = 0; e < B * ntok * k * d; ++e) x[e] = 0.0;
+  if (want_y)
+    for (int64_t e = 0; e < B * ntok * d; ++e) y[e] = 0.0;
+  if (P->cu_seqlens) {
+    int ok = P->cu_seqlens[0] == 0 && P->cu_seqlens[P->num_requests] == ntok;
+    for (int64_t r = 0; r < P->num_requests; ++r)
+      if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;
+    if (!ok) return KVXO_BAD_SEQLENS;
+  }
+  int status = 0;
+  for (int64_t r = 0; r < P->num_requests; ++r) {
+    const int64_t beg = P->cu_seqlens ? P->cu_seqlens[r] : 0;
+    const int64_t end = P->cu_seqlens ? P->cu_seqlens[r + 1] : ntok;
+    for (int64_t g = beg; g < end; ++g) {
+      const int64_t p = P->src_pos ? P->src_pos[g] : g - beg;
+      if (p < 0 || p >= P->max_position) {
+        status |= KVXO_BAD_POSITION;
+        continue;                               /* the token's rows stay zero */
+      }
+      for (int64_t lt = 0; lt < Lt; ++lt) {
+        int row_ok = 1;
+        for (int64_t j = 0; j < k; ++j) {
+          const int32_t s = P->layer_idx[lt * k + j];
+          if (s < 0 || s >= Ls) row_ok = 0;
+        }
+        if (!row_ok) status |= KVXO_BAD_LAYER_INDEX;
+        for (int64_t h = 0; h < H; ++h) {
+          for (int m = 0; m < 2; ++m) {
+            const int64_t b = (lt * H + h) * 2 + m;
+            /* the selected layers' content, concatenated in table order */
+            for (int64_t j = 0; row_ok && j < k; ++j) {
+              const int64_t s = P->layer_idx[lt * k + j];
+              const double *v = (m == 0 ? P->src_k : P->src_v) + ((s * ntok + g) * H + h) * d;
+              double *o = x + (b * ntok + g) * k * d + j * d;
+              if (m == 0) kvxo_rope(v, (int)d, (double)p, P->theta_src, -1, o);
+              else memcpy(o, v, sizeof(double) * (size_t)d);
+            }
+            /* the target layer's content at the same position */
+            if (want_y) {
+              const double *v = (m == 0 ? tgt_k : tgt_v) + ((lt * ntok + g) * H + h) * d;
+              double *o = y + (b * ntok + g) * d;
+              if (m == 0) kvxo_rope(v, (int)d, (double)p, P->theta_tgt, -1, o);
+              else memcpy(o, v, sizeof(double) * (size_t)d);
+            }
+          }
+        }
+      }
+    }
+  }
+  return status;
+}

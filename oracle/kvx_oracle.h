@@ -236,6 +236,27 @@ int kvxo_ridge_fit(const double *X, const double *Y, int64_t n, int p, int q,
 int kvxo_layer_scores(const kvxo_problem *prob, const double *tgt_k,
                       const double *tgt_v, double lam, double *r2, double *r2_set);
 
+/* The inputs of the ridge fits of the maps, in content space ("Перенос
+ * KV-кэша между моделями Qwen3 вместо повторного префилла", section
+ * "Линейного моста, как ни странно, хватает": strip the source RoPE,
+ * concatenate the selected layers' features, fit one ridge map per target
+ * (layer, head), one for keys and one for values).  For every target layer
+ * lt, head h and m (0 keys, 1 values), batch b = (lt H + h) 2 + m:
+ *   x[b][g][j d + i] = dim i of source layer layer_idx[lt][j], head h, token
+ *                      g; keys un-rotated at the token's position with
+ *                      theta_src, values as stored;
+ *   y[b][g][i]       = dim i of target layer lt, head h, token g; keys
+ *                      un-rotated at the same position with theta_tgt.
+ * x is [Lt][H][2][ntok][k d], y [Lt][H][2][ntok][d] (y and the target caches
+ * may be NULL).  Positions come from the request table or src_pos as for the
+ * transfer.  A token whose position lies outside [0, max_position) gets zero
+ * rows (KVXO_BAD_POSITION); a table row with a layer outside [0, Ls) leaves
+ * that target layer's x rows zero (KVXO_BAD_LAYER_INDEX); a malformed request
+ * table leaves everything zero (KVXO_BAD_SEQLENS).  The source must be packed
+ * (KVXO_CONTIGUOUS); W, b, target positions and layouts are unused. */
+int kvxo_ridge_features(const kvxo_problem *prob, const double *tgt_k, const double *tgt_v,
+                        double *x, double *y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,10 +80,10 @@ MUTATIONS = {
          "int64_t pt = P->tgt_pos ? P->tgt_pos[g] : p + 0 * off;", 3)],
     "source_position_counted_from_batch_start": [
         (C, "int64_t p = P->src_pos ? P->src_pos[g] : g - beg;",
-         "int64_t p = P->src_pos ? P->src_pos[g] : g;", 3)],
+         "int64_t p = P->src_pos ? P->src_pos[g] : g;", 4)],
     "backwards_request_table_accepted": [
         (C, "if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = 0;",
-         "if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = ok + 0;", 4)],
+         "if (P->cu_seqlens[r + 1] < P->cu_seqlens[r]) ok = ok + 0;", 5)],
     "contiguous_row_ignores_request_slab": [
         (C, "return r * dst_capacity + p_tgt;", "return 0 * r * dst_capacity + p_tgt;", 1)],
     "paged_target_slot_off_by_one": [
@@ -152,6 +152,19 @@ MUTATIONS = {
     "scores_set_from_first_layer_only": [
         (C, "int64_t s = P->layer_idx[lt * k + j];\n              const double *x",
          "int64_t s = P->layer_idx[lt * k + 0];\n              const double *x", 1)],
+    # ridge-fit inputs
+    "features_keys_unrotated_with_target_base": [
+        (C, "if (m == 0) kvxo_rope(v, (int)d, (double)p, P->theta_src, -1, o);",
+         "if (m == 0) kvxo_rope(v, (int)d, (double)p, P->theta_tgt, -1, o);", 1)],
+    "features_target_keys_left_rotated": [
+        (C, "if (m == 0) kvxo_rope(v, (int)d, (double)p, P->theta_tgt, -1, o);",
+         "if (m == 0) memcpy(o, v, sizeof(double) * (size_t)d);", 1)],
+    "features_layers_side_by_side_in_reverse": [
+        (C, "double *o = x + (b * ntok + g) * k * d + j * d;",
+         "double *o = x + (b * ntok + g) * k * d + (k - 1 - j) * d;", 1)],
+    "features_bad_layer_row_still_written": [
+        (C, "for (int64_t j = 0; row_ok && j < k; ++j) {",
+         "for (int64_t j = 0; (row_ok || P->layer_idx[lt * k + j] < Ls) && j < k; ++j) {", 1)],
 }
 
 # runs every pin function of test_oracle_pins (parametrized ones once per

@@ -1114,3 +1114,94 @@ def test_layer_scores_invariances_and_set_bounds():
     r2e, _, ste = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv,
                                       theta_src=1e4, theta_tgt=1e4, max_position=n - 1)
     assert ste == oracle.BAD_POSITION and np.all(np.isnan(r2e))
+
+
+# ---------------------------------------------------------------------------
+# Ridge-fit inputs in content space (kvxo_ridge_features)
+# ---------------------------------------------------------------------------
+def test_ridge_features_recover_planted_content_in_table_order():
+    # keys stored as content turned at each token's own position (ragged
+    # requests, explicit positions), with different bases on the two sides;
+    # the features must give the content back, the table's layers side by
+    # side in the table's order, values as stored
+    rng = np.random.default_rng(11)
+    Ls, Lt, H, d, n = 4, 3, 2, 8, 23
+    cs_k = rng.normal(size=(Ls, n, H, d)); cs_v = rng.normal(size=(Ls, n, H, d))
+    ct_k = rng.normal(size=(Lt, n, H, d)); ct_v = rng.normal(size=(Lt, n, H, d))
+    cu = np.array([0, 9, 9, 23])
+    pos = rng.integers(0, 500, size=n)
+    sk = np.stack([_rotate_np(cs_k[s], pos, 1e4) for s in range(Ls)])
+    tk = np.stack([_rotate_np(ct_k[t], pos, 1e6) for t in range(Lt)])
+    table = np.array([[3, 0], [1, 1], [2, 3]])
+    x, y, st = oracle.ridge_features(src_k=sk, src_v=cs_v, tgt_k=tk, tgt_v=ct_v, theta_src=1e4,
+                                     theta_tgt=1e6, max_position=500, layer_idx=table,
+                                     cu_seqlens=cu, src_pos=pos)
+    assert st == 0 and x.shape == (Lt, H, 2, n, 2 * d) and y.shape == (Lt, H, 2, n, d)
+    for lt in range(Lt):
+        for h in range(H):
+            for j, s in enumerate(table[lt]):
+                np.testing.assert_allclose(x[lt, h, 0, :, j * d:(j + 1) * d], cs_k[s, :, h],
+                                           atol=1e-12)
+                np.testing.assert_array_equal(x[lt, h, 1, :, j * d:(j + 1) * d], cs_v[s, :, h])
+            np.testing.assert_allclose(y[lt, h, 0], ct_k[lt, :, h], atol=1e-12)
+            np.testing.assert_array_equal(y[lt, h, 1], ct_v[lt, :, h])
+    # without the target caches only x is produced, and it is the same
+    x2, y2, st2 = oracle.ridge_features(src_k=sk, src_v=cs_v, theta_src=1e4, theta_tgt=1e6,
+                                        max_position=500, layer_idx=table, cu_seqlens=cu,
+                                        src_pos=pos)
+    assert st2 == 0 and y2 is None and np.array_equal(x2, x)
+    # positions restart at 0 in every request when none are given
+    x3, _, _ = oracle.ridge_features(src_k=sk, src_v=cs_v, theta_src=1e4, theta_tgt=1e6,
+                                     max_position=500, layer_idx=table, cu_seqlens=cu)
+    own = np.concatenate([np.arange(9), np.arange(14)])
+    want = _rotate_np(sk[table[0, 0]][:, 1], -own, 1e4)
+    np.testing.assert_allclose(x3[0, 1, 0, :, :d], want, atol=1e-12)
+
+
+def test_ridge_features_fit_reproduces_the_set_score():
+    # the set score of a table is the in-sample R^2 of the centred ridge fit
+    # on exactly these features; with lam -> 0 that is least squares with an
+    # intercept, which LAPACK's lstsq gives independently of both functions
+    xk, xv, yk, yv = _score_case(9)
+    Ls, n, H, d = xk.shape
+    table = np.array([[2, 0], [1, 2]])
+    kw = dict(theta_src=1e4, theta_tgt=5e5, max_position=n)
+    _, r2s, st = oracle.layer_scores(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv, lam=1e-10,
+                                     layer_idx=table, **kw)
+    x, y, st2 = oracle.ridge_features(src_k=xk, src_v=xv, tgt_k=yk, tgt_v=yv, layer_idx=table,
+                                      **kw)
+    assert st == 0 and st2 == 0
+    for lt in range(2):
+        for h in range(H):
+            for m in range(2):
+                A = np.hstack([x[lt, h, m], np.ones((n, 1))])
+                coef, *_ = np.linalg.lstsq(A, y[lt, h, m], rcond=None)
+                res = y[lt, h, m] - A @ coef
+                yy = y[lt, h, m]
+                ref = 1 - (res ** 2).sum() / ((yy - yy.mean(0)) ** 2).sum()
+                assert r2s[lt, h, m] == pytest.approx(ref, abs=1e-8)
+
+
+def test_ridge_features_flag_bad_inputs_and_zero_their_rows():
+    rng = np.random.default_rng(12)
+    Ls, Lt, H, d, n = 3, 2, 1, 4, 6
+    sk = rng.normal(size=(Ls, n, H, d)); sv = rng.normal(size=(Ls, n, H, d))
+    tk = rng.normal(size=(Lt, n, H, d)); tv = rng.normal(size=(Lt, n, H, d))
+    kw = dict(src_k=sk, src_v=sv, tgt_k=tk, tgt_v=tv, theta_src=1e4, theta_tgt=1e4)
+    # a position past the limit: that token's rows are zero, the rest intact
+    pos = np.arange(n); pos[4] = 50
+    x, y, st = oracle.ridge_features(max_position=10, layer_idx=np.array([[0], [2]]),
+                                     src_pos=pos, **kw)
+    assert st == oracle.BAD_POSITION
+    assert not x[:, :, :, 4].any() and not y[:, :, :, 4].any()
+    np.testing.assert_array_equal(x[1, 0, 1, 5], sv[2, 5, 0])
+    # a table row naming a missing layer: that target layer's x is zero, its
+    # y and the other layer's rows are intact
+    x, y, st = oracle.ridge_features(max_position=10, layer_idx=np.array([[0, 1], [2, 3]]), **kw)
+    assert st == oracle.BAD_LAYER_INDEX
+    assert not x[1].any() and x[0].all()
+    np.testing.assert_array_equal(y[1, 0, 1], tv[1, :, 0])
+    # a malformed request table: nothing is written but zeros
+    x, y, st = oracle.ridge_features(max_position=10, layer_idx=np.array([[0, 1], [1, 2]]),
+                                     cu_seqlens=np.array([0, 4, 3, 6]), **kw)
+    assert st == oracle.BAD_SEQLENS and not x.any() and not y.any()
