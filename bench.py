@@ -39,7 +39,8 @@ WIDE_METRIC = ("KV-transfer tokens/s at 14B→32B shape, 32K tokens, wide-featur
 PUBLISHED_MS = {"qwen3_14b_32b": 277.6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_FILES = {"tcgen05": "kvx_tcgen05.cu", "simt": "kvx_simt.cu", "diag": "kvx_diag.cu",
-                "wide": "kvx_wide.cu", "ridge": "kvx_ridge.cu", "scores": "kvx_scores.cu"}
+                "wide": "kvx_wide.cu", "ridge": "kvx_ridge.cu", "scores": "kvx_scores.cu",
+                "features": "kvx_features.cu"}
 
 
 def parse_args(argv=None):
@@ -48,12 +49,14 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
-    ap.add_argument("--op", choices=["transfer", "kv_diagnostics", "ridge_fit", "layer_scores"],
+    ap.add_argument("--op", choices=["transfer", "kv_diagnostics", "ridge_fit", "layer_scores",
+                                     "ridge_features"],
                     default="transfer",
                     help="transfer (the default step), the fidelity diagnostics of a "
                          "mapped cache against the target's own, a batch of ridge fits "
-                         "of the per-head maps (calibration), or the layer-selection "
-                         "scores of paired calibration caches")
+                         "of the per-head maps (calibration), the layer-selection "
+                         "scores of paired calibration caches, or the content-space "
+                         "observations of the maps' ridge fits")
     ap.add_argument("--score-tokens", type=int, default=4096,
                     help="calibration tokens of the layer-selection scores")
     ap.add_argument("--ridge-batch", type=int, default=16, help="ridge fits per step")
@@ -743,6 +746,144 @@ def time_oracle_scores(wl, target_seconds: float):
                       "whole workload by useful flops"}
 
 
+FEATURE_METRIC = ("ridge-fit observations: calibration tokens/s of content-space features (each "
+                  "target layer's k source layers side by side, keys un-rotated) and targets "
+                  "for every (target layer, head, K|V) at the 14B→32B shape, 32K tokens, fp32 "
+                  "out; % of HBM roofline")
+
+
+def feature_config(wl) -> dict:
+    """Workload keys of a ridge-features line, the same in both arms."""
+    return {"workload": f"{wl.name} ridge-fit observations", "tokens": wl.ntok,
+            "src_layers": wl.src_layers, "tgt_layers": wl.tgt_layers, "kv_heads": wl.kv_heads,
+            "head_dim": wl.head_dim, "k": wl.k, "out_dtype": "f32"}
+
+
+def feature_bytes(wl, layer_idx, elem_bytes: int, out_bytes: int = 4) -> int:
+    """Algorithmic bytes of one kvx_ridge_features call: the source layers the
+    table names and every target layer read once (K and V), x and y written."""
+    used = len(set(int(v) for v in layer_idx.flatten().tolist()))
+    row = wl.ntok * wl.kv_heads * wl.head_dim * 2 * elem_bytes
+    B = wl.tgt_layers * wl.kv_heads * 2
+    return (used + wl.tgt_layers) * row + B * wl.ntok * (wl.k + 1) * wl.head_dim * out_bytes
+
+
+def run_features(args):
+    """One step = one kvx_ridge_features call on seeded paired calibration
+    caches: x [Lt H 2][ntok][k d] and y [Lt H 2][ntok][d] in fp32, the inputs
+    of the per-head maps' ridge fits.  HBM-bound (writes dominate)."""
+    import ctypes
+    import torch
+    from cross_model_kv_transfer_gb300 import kvx
+    from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_score_inputs
+    ws, rank = init_dist("nccl")
+    _, _, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.with_tokens([args.tokens], [0])
+    inp = make_score_inputs(wl, dev)
+    Ls, Lt, H, d, k, n = wl.src_layers, wl.tgt_layers, wl.kv_heads, wl.head_dim, wl.k, wl.ntok
+    plan = kvx.Plan(src_layers=Ls, tgt_layers=Lt, kv_heads=H, head_dim=d, k=k,
+                    rope_theta_src=wl.theta_src, rope_theta_tgt=wl.theta_tgt,
+                    max_position=wl.max_position, kv_dtype=wl.kv_dtype, w_dtype=torch.float32,
+                    b_dtype=torch.float32, kernel=kvx.KVX_KERNEL_SIMT)
+    B = Lt * H * 2
+    x = torch.empty((B, n, k * d), dtype=torch.float32, device=dev)
+    y = torch.empty((B, n, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fa = kvx.FeatureArgs(inp["src_k"].data_ptr(), inp["src_v"].data_ptr(),
+                         inp["tgt_k"].data_ptr(), inp["tgt_v"].data_ptr(), n, 1, None, None,
+                         inp["layer_idx"].data_ptr(), kvx.KVX_F32, x.data_ptr(), y.data_ptr(),
+                         status.data_ptr())
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def step():
+        e = kvx.kvx_ridge_features(plan.handle, fa, sptr)
+        if e != kvx.KVX_OK:
+            raise kvx.KvxError(e, "kvx_ridge_features")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    value, ms = aggregate(n, ms_local, dev)
+    alg = feature_bytes(wl, inp["layer_idx"], inp["src_k"].element_size())
+    peaks, peak_kind = load_peaks()
+    achieved = alg / (ms_local / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(wl.name, "features"),
+            "peak_source": f"{peak_kind} (burst)", "algorithmic_bytes": alg}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle_features(wl, args.cpu_seconds)
+    in_bytes = sum(inp[c].numel() * inp[c].element_size()
+                   for c in ("src_k", "src_v", "tgt_k", "tgt_v"))
+    line = {
+        "metric": FEATURE_METRIC, "op": "ridge_features", "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded paired caches with planted source layers)",
+        "config": {**feature_config(wl), "parallelism": f"replicas x{ws}",
+                   "l2": f"inputs and outputs larger than L2 ({in_bytes / 1e9:.2f} GB read, "
+                         f"{(x.numel() + y.numel()) * 4 / 1e9:.1f} GB written per step, no "
+                         "flush needed)"},
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": None,
+        "e2e_note": "x and y are the device-side inputs of the ridge fit that follows; a read-"
+                    "back of them to the host is not part of their use",
+        "gpu_launches": args.steps, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    plan.close()
+
+
+def feature_sample(wl, n: int):
+    """The first n tokens of the features workload for the oracle (all target
+    layers, heads and K|V): kwargs of oracle.ridge_features."""
+    import torch
+    from cross_model_kv_transfer_gb300.workloads import make_score_inputs
+    inp = make_score_inputs(wl.with_tokens([n], [0]), "cpu")
+    f64 = lambda t: t.to(torch.float64).numpy()
+    return dict(src_k=f64(inp["src_k"]), src_v=f64(inp["src_v"]), tgt_k=f64(inp["tgt_k"]),
+                tgt_v=f64(inp["tgt_v"]), theta_src=wl.theta_src, theta_tgt=wl.theta_tgt,
+                max_position=n, layer_idx=inp["layer_idx"].numpy())
+
+
+def time_oracle_features(wl, target_seconds: float):
+    """The oracle on a growing prefix of tokens until it takes about
+    ``target_seconds``; tokens/s (the work is linear in the tokens)."""
+    import oracle
+    n = 16
+    while True:
+        kw = feature_sample(wl, n)
+        t0 = time.perf_counter()
+        oracle.ridge_features(**kw)
+        el = time.perf_counter() - t0
+        if el * 2 > target_seconds or n * 2 > wl.ntok:
+            break
+        n *= 2
+    return {"value": n / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} tokens x all {wl.tgt_layers} target layers x "
+                      f"{wl.kv_heads} heads x K|V ({el:.1f} s of fp64 CPU work, one thread)"}
+
+
 def run_kvx(args):
     import torch
     from cross_model_kv_transfer_gb300 import kvx
@@ -1112,7 +1253,18 @@ def run_reference(args):
     if rank != 0:
         return
     f64 = lambda t: t.detach().cpu().to(torch.float64).numpy()
-    if args.op == "layer_scores":
+    if args.op == "ridge_features":
+        wl = W.WORKLOADS[args.workload]
+        if args.tokens:
+            wl = wl.with_tokens([args.tokens], [0])
+        m = 64
+        kw = feature_sample(wl, m)
+        run = lambda: oracle.ridge_features(**kw)
+        scale, units = 1.0, float(m)
+        metric, unit, config = FEATURE_METRIC, "tokens/s", feature_config(wl)
+        sample = (f"{m} tokens per step through all {wl.tgt_layers} target layers x "
+                  f"{wl.kv_heads} heads x K|V")
+    elif args.op == "layer_scores":
         wl = W.WORKLOADS[args.workload].with_tokens([args.score_tokens], [0])
         m = 512
         kw, f = score_sample(wl, m)
@@ -1205,6 +1357,8 @@ def main(argv=None):
         run_ridge(args)
     elif args.op == "layer_scores":
         run_scores(args)
+    elif args.op == "ridge_features":
+        run_features(args)
     else:
         run_kvx(args)
 

@@ -133,6 +133,18 @@ class ScoreArgs(ctypes.Structure):
     ]
 
 
+class FeatureArgs(ctypes.Structure):
+    _fields_ = [
+        ("src_k", ctypes.c_void_p), ("src_v", ctypes.c_void_p),
+        ("tgt_k", ctypes.c_void_p), ("tgt_v", ctypes.c_void_p),
+        ("ntok", ctypes.c_int64), ("num_requests", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p), ("src_pos", ctypes.c_void_p),
+        ("layer_idx", ctypes.c_void_p), ("out_dtype", ctypes.c_int32),
+        ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -182,6 +194,9 @@ def load():
             lib.kvx_layer_scores.argtypes = [ctypes.c_void_p, ctypes.POINTER(ScoreArgs),
                                              ctypes.c_void_p]
             lib.kvx_layer_scores.restype = ctypes.c_int
+            lib.kvx_ridge_features.argtypes = [ctypes.c_void_p, ctypes.POINTER(FeatureArgs),
+                                               ctypes.c_void_p]
+            lib.kvx_ridge_features.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -241,6 +256,10 @@ def kvx_layer_scores_workspace_bytes(plan, ntok: int) -> int:
 
 def kvx_layer_scores(plan, args: ScoreArgs, stream) -> int:
     return load().kvx_layer_scores(plan, ctypes.byref(args), stream)
+
+
+def kvx_ridge_features(plan, args: FeatureArgs, stream) -> int:
+    return load().kvx_ridge_features(plan, ctypes.byref(args), stream)
 
 
 def ridge_fit(x, y, lam: float = 0.01, w=None, b=None, workspace=None, status=None,
@@ -522,6 +541,63 @@ class Plan:
         if st != KVX_OK:
             raise KvxError(st, "kvx_layer_scores")
         return r2, r2_set
+
+    def ridge_features(self, *, src_k, src_v, layer_idx, tgt_k=None, tgt_v=None,
+                       cu_seqlens=None, src_pos=None, out_dtype=None, x=None, y=None,
+                       status=None, stream=None):
+        """Content-space observations of the maps' ridge fits
+        (``kvx_ridge_features``) from CUDA caches src_k / src_v
+        [Ls][ntok][H][d] and, for y, tgt_k / tgt_v [Lt][ntok][H][d] of the
+        same tokens: returns x [Lt*H*2][ntok][k*d] and y [Lt*H*2][ntok][d]
+        (None without the target caches) in ``out_dtype`` (default fp32),
+        enqueued on ``stream`` -- the x and y of one ``ridge_fit`` whose W
+        and b this plan's transfer reads."""
+        import torch
+        d = self.desc
+        Ls, Lt, H, hd, k = d.src_layers, d.tgt_layers, d.src_kv_heads, d.src_head_dim, d.k
+        if layer_idx is None:
+            raise ValueError("layer_idx [Lt][k] is required")
+        with_y = tgt_k is not None or tgt_v is not None
+        caches = [("src_k", src_k, Ls), ("src_v", src_v, Ls)]
+        if with_y:
+            caches += [("tgt_k", tgt_k, Lt), ("tgt_v", tgt_v, Lt)]
+        for name, t, L in caches:
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA tensor")
+            if t.dtype != self.kv_dtype or t.dim() != 4 or t.shape[0] != L or \
+                    tuple(t.shape[2:]) != (H, hd):
+                raise ValueError(f"{name}: expected [{L}][ntok][{H}][{hd}] {self.kv_dtype}")
+        ntok = src_k.shape[1]
+        if any(t.shape[1] != ntok for _, t, _ in caches):
+            raise ValueError("the caches must hold the same tokens")
+        R = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+        for name, t, shape in (("cu_seqlens", cu_seqlens, (R + 1,)), ("src_pos", src_pos, (ntok,)),
+                               ("layer_idx", layer_idx, (Lt, k))):
+            if t is not None and (t.dtype != torch.int32 or tuple(t.shape) != shape or
+                                  not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous int32 CUDA tensor {shape}")
+        out_dtype = torch.float32 if out_dtype is None else out_dtype
+        dev = src_k.device
+        B = Lt * H * 2
+        for name, t, shape in (("x", x, (B, ntok, k * hd)), ("y", y, (B, ntok, hd))):
+            if t is not None and (t.dtype != out_dtype or tuple(t.shape) != shape or
+                                  not t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous {out_dtype} CUDA tensor {shape}")
+        if x is None:
+            x = torch.empty((B, ntok, k * hd), dtype=out_dtype, device=dev)
+        if with_y and y is None:
+            y = torch.empty((B, ntok, hd), dtype=out_dtype, device=dev)
+        ptr = lambda t: None if t is None else t.data_ptr()
+        a = FeatureArgs(src_k.data_ptr(), src_v.data_ptr(), ptr(tgt_k), ptr(tgt_v), int(ntok),
+                        int(R), ptr(cu_seqlens), ptr(src_pos), layer_idx.data_ptr(),
+                        _dtype_code(out_dtype), x.data_ptr(), ptr(y if with_y else None),
+                        ptr(status))
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        st = kvx_ridge_features(self.handle, a, ctypes.c_void_p(stream.cuda_stream))
+        if st != KVX_OK:
+            raise KvxError(st, "kvx_ridge_features")
+        return x, (y if with_y else None)
 
     def kv_diagnostics(self, stream=None, **tensors) -> None:
         """Enqueue the fidelity statistics [Lt][H][2][d + 4] (fp64, into

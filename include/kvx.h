@@ -440,6 +440,58 @@ size_t kvx_layer_scores_workspace_bytes(const kvx_plan *plan, int64_t ntok);
  * target without variance gives NaN (KVX_FLAG_NOT_SPD for the former). */
 kvx_status kvx_layer_scores(const kvx_plan *plan, const kvx_score_args *args, void *stream);
 
+/* Arguments of kvx_ridge_features.  DEVICE pointers, 16-byte aligned; shapes
+ * come from the plan (Ls, Lt, H, d, k, the two RoPE bases, max_position, the
+ * cache dtype).  As for kvx_score_args, both caches hold the same tokens in
+ * the same packed order. */
+typedef struct {
+  const void *src_k, *src_v;  /* [Ls][ntok][H][d] the pilot's cache (keys
+                                 RoPE-rotated with rope_theta_src)           */
+  const void *tgt_k, *tgt_v;  /* [Lt][ntok][H][d] the target's own cache (keys
+                                 with rope_theta_tgt); needed only with y    */
+  int64_t ntok;               /* tokens, 0 .. 2^31 - 1                        */
+  int32_t num_requests;       /* R >= 1                                       */
+  const int32_t *cu_seqlens;  /* [R+1] or NULL (R == 1), as for kvx_transfer  */
+  const int32_t *src_pos;     /* [ntok] positions, or NULL: 0..len-1 per
+                                 request; both caches are at these positions */
+  const int32_t *layer_idx;   /* [Lt][k] the layer table the maps will serve  */
+  int32_t out_dtype;          /* kvx_dtype of x and y                         */
+  void *x;                    /* [Lt][H][2][ntok][k d] output                 */
+  void *y;                    /* [Lt][H][2][ntok][d] output, or NULL          */
+  uint32_t *status;           /* optional device word; KVX_FLAG_* OR-ed in    */
+} kvx_feature_args;
+
+/* The observations of the ridge fits of a per-head plan's maps, in content
+ * space.  "Перенос KV-кэша между моделями Qwen3 вместо повторного префилла",
+ * section "Линейного моста, как ни странно, хватает": each target (layer,
+ * head) gets one ridge map for keys and one for values, fitted on the
+ * concatenated features of the source layers chosen for that target layer,
+ * with the source RoPE stripped from the keys before the map and the target
+ * RoPE applied after it.  For target layer lt, head h and m (0 keys,
+ * 1 values), batch b = (lt H + h) 2 + m and token g at position p (from
+ * src_pos, else its offset in its request):
+ *   x[b][g][j d + i] = dim i of source layer layer_idx[lt][j], head h;
+ *                      keys un-rotated at p with rope_theta_src;
+ *   y[b][g][i]       = dim i of target layer lt, head h; keys un-rotated at
+ *                      p with rope_theta_tgt.
+ * Values are copied as stored.  x and y are exactly the x and y of one
+ * kvx_ridge_fit batch (p = k d, q = d) whose W and b kvx_transfer then reads
+ * for this plan.  The un-rotation runs in fp32 with angles from the plan's
+ * fixed-point RoPE phases (about 1e-6 relative error); a bf16 output is the
+ * fp32 result rounded to nearest.  Device-detected: a token whose position
+ * lies outside [0, max_position) gets zero rows in x and y
+ * (KVX_FLAG_BAD_POSITION); a table row naming a layer outside [0, Ls) leaves
+ * that target layer's x rows zero (KVX_FLAG_BAD_LAYER_INDEX; y is still
+ * written); a malformed request table leaves x and y all zero
+ * (KVX_FLAG_BAD_SEQLENS).  Asynchronous on `stream`, no allocation, one kernel
+ * launch (none for ntok == 0).  Returns KVX_ERR_INVALID_ARG for a NULL plan,
+ * args or required pointer, y without both target caches, a pointer that is
+ * not 16-byte aligned, sizes outside the limits, a bad out_dtype, or a plan
+ * of another device; KVX_ERR_UNSUPPORTED for a wide-mapper plan, a head_dim
+ * that is not a multiple of 8 or exceeds 128, k above 8, or 2 Lt H above
+ * 2^31 - 1; KVX_ERR_CUDA if the launch fails. */
+kvx_status kvx_ridge_features(const kvx_plan *plan, const kvx_feature_args *args, void *stream);
+
 /* Allocation-free transfer.  The sources have no counterpart for this call:
  * it exists for callers that may not allocate device memory -- engines that
  * reserve nearly all of the GPU for their own paged KV-cache pool and forbid

@@ -39,7 +39,8 @@ def test_library_exports_every_declared_symbol():
 def test_ctypes_structs_match_the_c_layout(tmp_path):
     # Compile a probe against include/kvx.h that prints sizes and offsets.
     fields = {"kvx_plan_desc": kvx.PlanDesc, "kvx_transfer_args": kvx.TransferArgs,
-              "kvx_diag_args": kvx.DiagArgs, "kvx_ridge_args": kvx.RidgeArgs}
+              "kvx_diag_args": kvx.DiagArgs, "kvx_ridge_args": kvx.RidgeArgs,
+              "kvx_score_args": kvx.ScoreArgs, "kvx_feature_args": kvx.FeatureArgs}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kvx.h"', "int main(void){"]
     for cname, cls in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -143,3 +144,10 @@ def test_ridge_workspace_size_and_host_validation():
     a = kvx.RidgeArgs(1, 65535 * 16384 + 1, 4, 2, 0.01, kvx.KVX_F32, 16, 16, 16, 16, 16, 1 << 20,
                       None)
     assert kvx.kvx_ridge_fit(a, None) == kvx.KVX_ERR_INVALID_ARG
+
+
+def test_ridge_features_rejects_null_before_touching_the_device():
+    lib = kvx.load()
+    assert lib.kvx_ridge_features(None, None, None) == kvx.KVX_ERR_INVALID_ARG
+    a = kvx.FeatureArgs()
+    assert kvx.kvx_ridge_features(None, a, None) == kvx.KVX_ERR_INVALID_ARG

@@ -140,3 +140,13 @@ def test_phase_roofline_picks_the_phase_with_the_largest_ideal_time():
     assert abs(r["frac"] - 0.3) < 1e-9 and abs(r["frac_of_ideal_sum"] - 0.45) < 1e-6
     r = bench.phase_roofline(2.0, tf32 * 1e9, 0.0, 0.0, "ridge", "none")
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-9 and r["traffic"] is None
+
+
+def test_feature_bytes_count_named_source_layers_once_and_both_outputs():
+    import torch
+    from cross_model_kv_transfer_gb300.workloads import WORKLOADS
+    wl = WORKLOADS["qwen3_14b_32b"]
+    table = torch.tensor([[0, 1, 2, 3], [3, 2, 1, 0]] * 32, dtype=torch.int32)
+    row = 32768 * 8 * 128 * 2 * 2                  # one layer's K and V, bf16
+    out = 64 * 8 * 2 * 32768 * (4 * 128 + 128) * 4  # x and y, fp32
+    assert bench.feature_bytes(wl, table, 2) == (4 + 64) * row + out

@@ -22,6 +22,7 @@ MODES = {
     "kv_diagnostics": ["--op", "kv_diagnostics"],
     "ridge_fit": ["--op", "ridge_fit"],
     "layer_scores": ["--op", "layer_scores"],
+    "ridge_features": ["--op", "ridge_features"],
     "small_override": ["--tokens", "4096", "--tgt-layers", "8"],
 }
 
@@ -53,6 +54,9 @@ def test_reference_line_matches_the_gpu_arm_contract(mode):
         wl = WORKLOADS[args.workload].with_tokens([args.score_tokens], [0])
         metric, unit = bench.SCORE_METRIC, "tokens/s"
         config = bench.score_config(wl, args.score_tokens)
+    elif args.op == "ridge_features":
+        wl = WORKLOADS[args.workload]
+        metric, unit, config = bench.FEATURE_METRIC, "tokens/s", bench.feature_config(wl)
     elif args.op == "kv_diagnostics":
         wl = bench.select_workload(args)
         metric, unit, config = bench.DIAG_METRIC, "tokens/s", bench.diag_config(wl)

@@ -1,7 +1,7 @@
 """The method end to end through the library, on one synthetic model pair:
 choose each target layer's source layers by their scores (kvx_layer_scores),
 fit the per-(target layer, head, K|V) maps on those layers' content features
-(kvx_ridge_fit), transfer the pilot's cache with them (kvx_transfer), and
+(kvx_ridge_features, kvx_ridge_fit), transfer the pilot's cache with them (kvx_transfer), and
 measure the mapped cache against the target's own (kvx_kv_diagnostics).
 
 The pieces check one another: the scorer must find the planted source
@@ -20,20 +20,6 @@ from cross_model_kv_transfer_gb300 import kvx
 from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_score_inputs
 
 pytestmark = pytest.mark.gpu
-
-
-def content(x, theta, d):
-    """[L][n][H][d] keys as stored (turned by theta at positions 0..n-1) back
-    to content space, fp32 (test-side preparation of the ridge features)."""
-    n, half = x.shape[1], d // 2
-    pos = torch.arange(n, dtype=torch.float64, device=x.device)
-    w = theta ** (-2.0 * torch.arange(half, dtype=torch.float64, device=x.device) / d)
-    a = pos[:, None] * w[None, :]
-    c = torch.cos(a).float()[None, :, None, :]
-    s = torch.sin(a).float()[None, :, None, :]
-    x = x.float()
-    x0, x1 = x[..., :half], x[..., half:]
-    return torch.cat((x0 * c + x1 * s, x1 * c - x0 * s), dim=-1)
 
 
 def test_scores_fit_transfer_and_diagnostics_agree():
@@ -61,17 +47,12 @@ def test_scores_fit_transfer_and_diagnostics_agree():
                                   tgt_v=inp["tgt_v"], lam=0.01, layer_idx=table, status=status)
 
     # 2. the maps: one ridge fit per (target layer, head, K|V) on the content
-    #    features of the chosen layers (batch ordered as the transfer reads W)
-    src_c = (content(inp["src_k"], wl.theta_src, d), inp["src_v"].float())
-    tgt_c = (content(inp["tgt_k"], wl.theta_tgt, d), inp["tgt_v"].float())
-    xs, ys = [], []
-    for lt in range(Lt):
-        for h in range(H):
-            for m in range(2):
-                xs.append(torch.cat([src_c[m][int(s), :, h, :] for s in table[lt]], dim=1))
-                ys.append(tgt_c[m][lt, :, h, :])
-    w, b = kvx.ridge_fit(torch.stack(xs).contiguous(), torch.stack(ys).contiguous(), lam=0.01)
-    del xs, ys
+    #    features of the chosen layers (kvx_ridge_features writes them in the
+    #    batch order the transfer reads W in)
+    x, y = plan.ridge_features(src_k=inp["src_k"], src_v=inp["src_v"], tgt_k=inp["tgt_k"],
+                               tgt_v=inp["tgt_v"], layer_idx=table, status=status)
+    w, b = kvx.ridge_fit(x, y, lam=0.01)
+    del x, y
 
     # 3. the transfer with the chosen table and the fitted maps
     mk = torch.empty((Lt, n, H, d), dtype=wl.kv_dtype, device="cuda")
