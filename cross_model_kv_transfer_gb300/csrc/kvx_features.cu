@@ -15,9 +15,9 @@
 //
 // One pass, bound by HBM writes (x is k rows per source row read).  A thread
 // carries 4 RoPE pairs of one token (dims 4q .. 4q+3 and d/2 + 4q ..),
-// computes each base's 4 angles once and reuses them for the k source rows;
-// it issues the k rows' loads before the first store, and consecutive threads
-// write consecutive 16-byte (fp32) or 8-byte (bf16) pieces of a row.
+// computes each base's 4 angles once and reuses them for the k source rows,
+// and consecutive threads write consecutive 16-byte (fp32) or 8-byte (bf16)
+// pieces of a row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -27,7 +27,6 @@
 
 namespace {
 
-constexpr int kFeatMaxK = 8;
 constexpr int kFeatMaxD = 128;
 constexpr int kFeatThreads = 256;
 
@@ -88,27 +87,31 @@ __device__ __forceinline__ int request_of(const int32_t *cu, int R, int64_t g) {
 
 // Grid: x = (lt H + h) 2 + m, fastest, so that the CTAs of one group of
 // 256 / (d / 8) tokens run together and share its source rows in L2; the
-// token group is blockIdx.z * gridDim.y + blockIdx.y.
+// token group is blockIdx.z * gridDim.y + blockIdx.y.  The k rows go one at a
+// time (load, un-rotate, store): about 40 registers, 6 CTAs per SM, and the
+// 48 warps of an SM keep enough loads in flight to stream the writes at HBM
+// speed.  (Holding all k rows' loads in registers before the first store
+// needs ~100 registers and 2 CTAs per SM, and ran at half the speed.)
 template <typename T, typename O>
-__global__ void __launch_bounds__(kFeatThreads) features_kernel(const __grid_constant__ FeatParams p) {
+__global__ void __launch_bounds__(kFeatThreads, 6) features_kernel(const __grid_constant__ FeatParams p) {
   const int per_tok = p.d / 8;
   const int tpb = kFeatThreads / per_tok;
   const int m = blockIdx.x & 1, h = (blockIdx.x >> 1) % p.H, lt = (blockIdx.x >> 1) / p.H;
   const int64_t group = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
   const int tid = threadIdx.x;
-  // every CTA checks the request table: a malformed one leaves only zeros
+  // every CTA checks the request table (a malformed one leaves only zeros);
+  // without one there is nothing to check and no barrier
   bool table_ok = true;
   if (p.cu) {
     for (int r = tid; r < p.R; r += blockDim.x) table_ok = table_ok && p.cu[r + 1] >= p.cu[r];
     if (tid == 0) table_ok = table_ok && p.cu[0] == 0 && (int64_t)p.cu[p.R] == p.n;
+    table_ok = __syncthreads_and(table_ok);
   }
-  table_ok = __syncthreads_and(table_ok);
-  int32_t layers[kFeatMaxK];
+  const int32_t *__restrict__ layers = p.layer_idx + (int64_t)lt * p.k;
   bool row_ok = true;
-#pragma unroll
-  for (int j = 0; j < kFeatMaxK; ++j) {
-    layers[j] = j < p.k ? __ldg(p.layer_idx + lt * p.k + j) : 0;
-    if (j < p.k) row_ok = row_ok && layers[j] >= 0 && layers[j] < p.Ls;
+  for (int j = 0; j < p.k; ++j) {
+    const int32_t s = __ldg(layers + j);
+    row_ok = row_ok && s >= 0 && s < p.Ls;
   }
   if (tid == 0 && group == 0 && m == 0 && h == 0 && p.status) {
     if (!table_ok && lt == 0) atomicOr(p.status, KVX_FLAG_BAD_SEQLENS);
@@ -117,7 +120,8 @@ __global__ void __launch_bounds__(kFeatThreads) features_kernel(const __grid_con
   const int q = tid % per_tok;
   const int64_t g = group * tpb + tid / per_tok;
   if (g >= p.n) return;
-  const int d = p.d, half = d / 2, kd = p.k * d;
+  const int d = p.d, half = d / 2;
+  const int64_t kd = (int64_t)p.k * d;
   const int64_t b = ((int64_t)lt * p.H + h) * 2 + m;
   O *__restrict__ xrow = reinterpret_cast<O *>(p.x) + (b * p.n + g) * kd + 4 * q;
   O *__restrict__ yrow = p.y ? reinterpret_cast<O *>(p.y) + (b * p.n + g) * d + 4 * q : nullptr;
@@ -130,62 +134,44 @@ __global__ void __launch_bounds__(kFeatThreads) features_kernel(const __grid_con
   if (table_ok && !pos_ok && blockIdx.x == 0 && q == 0 && p.status)
     atomicOr(p.status, KVX_FLAG_BAD_POSITION);
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-  if (!pos_ok) {
-    for (int j = 0; j < p.k; ++j) {
-      store4(xrow + j * d, zero);
-      store4(xrow + j * d + half, zero);
-    }
-    if (yrow) {
-      store4(yrow, zero);
-      store4(yrow + half, zero);
-    }
-    return;
-  }
-  // the source rows: all loads first, then the un-rotation and the stores
-  const T *__restrict__ src = reinterpret_cast<const T *>(m ? p.src_v : p.src_k);
-  float lo[kFeatMaxK][4], hi[kFeatMaxK][4];
-#pragma unroll
-  for (int j = 0; j < kFeatMaxK; ++j) {
-    if (j < p.k && row_ok) {
-      const T *row = src + (((int64_t)layers[j] * p.n + g) * p.H + h) * d + 4 * q;
-      load4(row, lo[j]);
-      load4(row + half, hi[j]);
-    }
-  }
-  float ty_lo[4], ty_hi[4];
-  if (yrow) {
-    const T *tgt = reinterpret_cast<const T *>(m ? p.tgt_v : p.tgt_k);
-    const T *row = tgt + (((int64_t)lt * p.n + g) * p.H + h) * d + 4 * q;
-    load4(row, ty_lo);
-    load4(row + half, ty_hi);
-  }
   float c[4], s[4];
-  if (m == 0) {
+  if (m == 0 && pos_ok) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) rope_cs((uint32_t)pos, p.turns_src[4 * q + e], c[e], s[e]);
   }
-#pragma unroll
-  for (int j = 0; j < kFeatMaxK; ++j) {
-    if (j < p.k) {
-      if (!row_ok) {
-        store4(xrow + j * d, zero);
-        store4(xrow + j * d + half, zero);
-        continue;
-      }
-      if (m == 0) unrotate(lo[j], hi[j], c, s);
-      store4(xrow + j * d, lo[j]);
-      store4(xrow + j * d + half, hi[j]);
+  const T *__restrict__ src = reinterpret_cast<const T *>(m ? p.src_v : p.src_k);
+  for (int j = 0; j < p.k; ++j) {
+    if (!(pos_ok && row_ok)) {
+      store4(xrow + (int64_t)j * d, zero);
+      store4(xrow + (int64_t)j * d + half, zero);
+      continue;
     }
+    const T *row = src + (((int64_t)__ldg(layers + j) * p.n + g) * p.H + h) * d + 4 * q;
+    float lo[4], hi[4];
+    load4(row, lo);
+    load4(row + half, hi);
+    if (m == 0) unrotate(lo, hi, c, s);
+    store4(xrow + (int64_t)j * d, lo);
+    store4(xrow + (int64_t)j * d + half, hi);
   }
-  if (yrow) {
-    if (m == 0) {
+  if (!yrow) return;
+  if (!pos_ok) {
+    store4(yrow, zero);
+    store4(yrow + half, zero);
+    return;
+  }
+  const T *tgt = reinterpret_cast<const T *>(m ? p.tgt_v : p.tgt_k);
+  const T *row = tgt + (((int64_t)lt * p.n + g) * p.H + h) * d + 4 * q;
+  float lo[4], hi[4];
+  load4(row, lo);
+  load4(row + half, hi);
+  if (m == 0) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) rope_cs((uint32_t)pos, p.turns_tgt[4 * q + e], c[e], s[e]);
-      unrotate(ty_lo, ty_hi, c, s);
-    }
-    store4(yrow, ty_lo);
-    store4(yrow + half, ty_hi);
+    for (int e = 0; e < 4; ++e) rope_cs((uint32_t)pos, p.turns_tgt[4 * q + e], c[e], s[e]);
+    unrotate(lo, hi, c, s);
   }
+  store4(yrow, lo);
+  store4(yrow + half, hi);
 }
 
 template <typename T>
@@ -207,7 +193,7 @@ extern "C" kvx_status kvx_ridge_features(const kvx_plan *plan, const kvx_feature
   const kvx_plan_desc &d = plan->desc;
   const int D = d.src_head_dim;
   if (d.mapper != KVX_MAPPER_PER_HEAD || D % 8 != 0 || D > kFeatMaxD || d.k < 1 ||
-      d.k > kFeatMaxK || d.src_kv_heads != d.tgt_kv_heads || D != d.tgt_head_dim ||
+      d.src_kv_heads != d.tgt_kv_heads || D != d.tgt_head_dim ||
       (d.kv_dtype != KVX_F32 && d.kv_dtype != KVX_BF16))
     return KVX_ERR_UNSUPPORTED;
   const bool with_y = a->y != nullptr;

@@ -488,8 +488,8 @@ typedef struct {
  * args or required pointer, y without both target caches, a pointer that is
  * not 16-byte aligned, sizes outside the limits, a bad out_dtype, or a plan
  * of another device; KVX_ERR_UNSUPPORTED for a wide-mapper plan, a head_dim
- * that is not a multiple of 8 or exceeds 128, k above 8, or 2 Lt H above
- * 2^31 - 1; KVX_ERR_CUDA if the launch fails. */
+ * that is not a multiple of 8 or exceeds 128, or 2 Lt H above 2^31 - 1;
+ * KVX_ERR_CUDA if the launch fails. */
 kvx_status kvx_ridge_features(const kvx_plan *plan, const kvx_feature_args *args, void *stream);
 
 /* Allocation-free transfer.  The sources have no counterpart for this call:

@@ -163,6 +163,16 @@ def test_features_single_request_small_head_dim_without_target():
     check(c, gx, gy2, ox, oy)
 
 
+def test_features_long_table_rows():
+    # k = 10 selected layers per target layer (rows of 160 features)
+    c = Case(Ls=12, Lt=2, H=1, d=16, k=10, lens=(97, 64))
+    inp = make_inputs(c, 26)
+    gx, gy, st = run_gpu(c, inp)
+    ox, oy, ost = run_oracle(c, inp)
+    assert st == 0 and ost == 0
+    check(c, gx, gy, ox, oy)
+
+
 def test_features_flags_zero_what_they_name():
     c = Case(Ls=3, Lt=2, H=2, d=32, k=2, lens=(50, 30), max_position=64)
     inp = make_inputs(c, 24)
