@@ -3,9 +3,12 @@
 // scores (kvx_scores.cu).  G is [batch][p][p] fp64 in global memory holding
 // the upper triangle of a symmetric matrix; after chol_factor it holds L in
 // its lower triangle and L^T in its upper one.  Right-looking: per diagonal
-// block, factor it (one CTA per fit), solve the panel below it (one CTA per
-// block row) and update the trailing lower triangle (one CTA per 64 x 64
-// block), so that the update, most of the work, is spread over the GPU.  A
+// block, factor it (one CTA per fit), solve the panel below it (two CTAs of
+// four warps per block row) and update the trailing lower triangle (one CTA
+// per 64 x 64 block), so that the update, most of the work, is spread over
+// the GPU.  GB300 retires about two fp64 lanes per clock per SM, so the
+// diagonal and panel steps, a few CTAs each, are bound by latency: both keep
+// one barrier per column and independent multiply-adds within a step.  A
 // fit whose pivot is not positive gets G[0] = NaN (later steps skip it) and
 // KVX_FLAG_NOT_SPD in *status.  chol_solve_cols then solves columns against
 // the factor.
@@ -35,49 +38,61 @@ __global__ void __launch_bounds__(256) chol_prep_kernel(double *__restrict__ G, 
 __device__ __forceinline__ int blk_len(int p, int kb) { return p - kb * kB < kB ? p - kb * kB : kB; }
 
 // Factor the diagonal block kb of each fit in shared memory, right-looking
-// over all threads: per column, the pivot's square root (one thread, with
-// its reciprocal), the column below it scaled, then the trailing lower
-// triangle updated; the update of earlier blocks is already applied.
+// over all threads, one barrier per column: step j updates the trailing lower
+// triangle with L[i][m] -= (L[i][j] / d_j) L[m][j] from the unscaled column
+// (a 16 x 16 thread grid walking rows and columns), scales column j - 1 by
+// 1 / sqrt(d_{j-1}) (no one reads it any more), and thread 0, which alone
+// owns element (j + 1, j + 1), updates it first and takes the next pivot's
+// reciprocal square root while the others update.  The update of earlier
+// blocks is already applied.  (Holding the rows in registers instead issues
+// every thread's predicated multiply-adds on the narrow fp64 pipe and ran
+// 1.4x slower.)
+__device__ __forceinline__ bool chol_pivot(double d, double &diag, double &rp, double &rd) {
+  if (!(d > 0.0)) return false;
+  const double r = rsqrt(d);
+  diag = d * r;
+  rp = r;
+  rd = r * r;
+  return true;
+}
+
 __global__ void __launch_bounds__(256) chol_diag_kernel(double *__restrict__ G, int p, int kb,
                                                         uint32_t *status) {
   __shared__ double L[kB][kB + 1];
-  __shared__ double s_rpiv;
-  __shared__ int s_fail;
+  __shared__ double rp[kB], rd[kB];   // 1 / sqrt(d_j) and 1 / d_j
+  // pivot failures by step parity: step j reads fail[j & 1] and thread 0
+  // writes fail[(j + 1) & 1] in the same step, so no read races a write
+  __shared__ int fail[2];
   double *A = G + (int64_t)blockIdx.x * p * p;
   if (isnan(A[0])) return;
   const int o = kb * kB, nb = blk_len(p, kb);
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  for (int e = tid; e < nb * nb; e += nthreads) {
-    const int i = e / nb, j = e % nb;
-    L[i][j] = A[(int64_t)(o + i) * p + o + j];
-  }
-  if (tid == 0) s_fail = 0;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  for (int i = ty; i < nb; i += 16)
+    for (int j = tx; j < nb; j += 16) L[i][j] = A[(int64_t)(o + i) * p + o + j];
   __syncthreads();
+  if (tid == 0) fail[0] = chol_pivot(L[0][0], L[0][0], rp[0], rd[0]) ? 0 : 1;
+  __syncthreads();
+  bool failed = false;
   for (int j = 0; j < nb; ++j) {
-    if (tid == 0) {
-      const double d = L[j][j];
-      if (!(d > 0.0)) {
-        s_fail = 1;
-        s_rpiv = 1.0;
-      } else {
-        const double r = sqrt(d);
-        L[j][j] = r;
-        s_rpiv = 1.0 / r;
-      }
+    if (fail[j & 1]) {
+      failed = true;
+      break;
     }
-    __syncthreads();
-    if (s_fail) break;
-    const double rp = s_rpiv;
-    for (int i = j + 1 + tid; i < nb; i += nthreads) L[i][j] *= rp;
-    __syncthreads();
-    const int w = nb - j - 1;                  // trailing block: rows and columns j + 1 ..
-    for (int e = tid; e < w * w; e += nthreads) {
-      const int i = j + 1 + e / w, m = j + 1 + e % w;
-      if (m <= i) L[i][m] = fma(-L[i][j], L[m][j], L[i][m]);
+    if (j > 0 && tid >= j && tid < nb) L[tid][j - 1] *= rp[j - 1];
+    const double inv = rd[j];
+    int i0 = j + 1 + ty;
+    if (tid == 0 && j + 1 < nb) {
+      const double d = fma(-L[j + 1][j] * inv, L[j + 1][j], L[j + 1][j + 1]);
+      fail[(j + 1) & 1] = chol_pivot(d, L[j + 1][j + 1], rp[j + 1], rd[j + 1]) ? 0 : 1;
+      i0 += 16;
+    }
+    for (int i = i0; i < nb; i += 16) {
+      const double a = L[i][j] * inv;
+      for (int m = j + 1 + tx; m <= i; m += 16) L[i][m] = fma(-a, L[m][j], L[i][m]);
     }
     __syncthreads();
   }
-  if (s_fail) {
+  if (failed) {
     if (tid == 0) {
       A[0] = nan("");
       if (status) atomicOr(status, KVX_FLAG_NOT_SPD);
@@ -86,46 +101,71 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(double *__restrict__ G, 
   }
   // L in the lower triangle, L^T in the upper (rows of L^T are what the
   // back substitution reads)
-  for (int e = tid; e < nb * nb; e += blockDim.x) {
-    const int i = e / nb, j = e % nb;
-    A[(int64_t)(o + i) * p + o + j] = i >= j ? L[i][j] : L[j][i];
-  }
+  for (int i = ty; i < nb; i += 16)
+    for (int j = tx; j < nb; j += 16)
+      A[(int64_t)(o + i) * p + o + j] = i >= j ? L[i][j] : L[j][i];
 }
 
-// Panel: block row ib = kb + 1 + blockIdx.y of fit blockIdx.x solves
-// X L_kb^T = A[ib][kb] (rows independent: one thread per row).
-__global__ void __launch_bounds__(64) chol_panel_kernel(double *__restrict__ G, int p, int kb) {
+// Panel: rows r0 .. r0 + 31 of block row ib = kb + 1 + blockIdx.y / 2 of fit
+// blockIdx.x solve X L_kb^T = A[ib][kb].  Lane l of every warp holds row
+// r0 + l; warp w holds its columns 16 w .. 16 w + 15 in registers, so a block
+// row spreads over two CTAs of four warps.  Right-looking: at step j the warp
+// owning column j finishes x_j (times the pivot's reciprocal, taken once in
+// shared memory) and publishes it; every warp with columns beyond j then
+// takes its terms, L[m][j] x_j, all independent of one another.  The
+// published values alternate between two buffers, one barrier per step.
+constexpr int kPanelRows = 32;
+constexpr int kPanelThreads = kB / 16 * 32;
+__global__ void __launch_bounds__(kPanelThreads) chol_panel_kernel(double *__restrict__ G, int p,
+                                                                  int kb) {
   __shared__ double L[kB][kB + 1];
+  __shared__ double rd[kB];
+  __shared__ double xs[2][kPanelRows];
   double *A = G + (int64_t)blockIdx.x * p * p;
   if (isnan(A[0])) return;
   const int o = kb * kB, nb = blk_len(p, kb);
-  const int ib = kb + 1 + blockIdx.y;
-  const int r0 = ib * kB, nr = blk_len(p, ib);
-  for (int e = threadIdx.x; e < nb * nb; e += blockDim.x) {
-    const int i = e / nb, j = e % nb;
-    L[i][j] = i >= j ? A[(int64_t)(o + i) * p + o + j] : 0.0;
+  const int ib = kb + 1 + blockIdx.y / (kB / kPanelRows);
+  const int r0 = ib * kB + (blockIdx.y % (kB / kPanelRows)) * kPanelRows;
+  const int nr = p - r0 < kPanelRows ? p - r0 : kPanelRows;
+  // the factor's lower triangle, zero elsewhere
+#pragma unroll 8
+  for (int e = threadIdx.x; e < kB * kB; e += kPanelThreads) {
+    const int i = e / kB, j = e % kB;
+    L[i][j] = (i < nb && j <= i) ? A[(int64_t)(o + i) * p + o + j] : 0.0;
   }
   __syncthreads();
-  const int r = threadIdx.x;
-  if (r >= nr) return;
-  double *row = A + (int64_t)(r0 + r) * p + o;
-  double x[kB];
+  for (int j = threadIdx.x; j < nb; j += kPanelThreads) rd[j] = 1.0 / L[j][j];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const bool live = lane < nr;
+  double *row = A + (int64_t)(r0 + lane) * p + o + 16 * w;
+  double x[16];
 #pragma unroll
-  for (int j = 0; j < kB; ++j) x[j] = j < nb ? row[j] : 0.0;
+  for (int v = 0; v < 16; ++v) x[v] = (live && 16 * w + v < nb) ? row[v] : 0.0;
+  __syncthreads();
 #pragma unroll
   for (int j = 0; j < kB; ++j) {
     if (j >= nb) break;
-    double v = x[j];
-#pragma unroll
-    for (int m = 0; m < j; ++m) v = fma(-x[m], L[j][m], v);
-    x[j] = v / L[j][j];
-  }
-#pragma unroll
-  for (int j = 0; j < kB; ++j)
-    if (j < nb) {
-      row[j] = x[j];                                   // L[r0 + r][o + j]
-      A[(int64_t)(o + j) * p + r0 + r] = x[j];         // and L^T
+    if (w == (j >> 4)) {
+      x[j & 15] *= rd[j];
+      xs[j & 1][lane] = x[j & 15];
     }
+    __syncthreads();
+    if (16 * w + 15 > j) {
+      const double xj = xs[j & 1][lane];
+#pragma unroll
+      for (int v = 0; v < 16; ++v)
+        if (16 * w + v > j) x[v] = fma(-xj, L[16 * w + v][j], x[v]);
+    }
+  }
+  if (!live) return;
+#pragma unroll
+  for (int v = 0; v < 16; ++v) {
+    const int c = 16 * w + v;
+    if (c < nb) {
+      row[v] = x[v];                                   // L[r0 + lane][o + c]
+      A[(int64_t)(o + c) * p + r0 + lane] = x[v];      // and L^T
+    }
+  }
 }
 
 // Trailing update: lower-triangle block (ib, jb), ib >= jb > kb, of fit
@@ -422,7 +462,8 @@ inline cudaError_t chol_factor(double *G, int batch, int p, double lam, uint32_t
     chol_diag_kernel<<<batch, 256, 0, s>>>(G, p, kb, status);
     const int rest = nblk - 1 - kb;
     if (rest > 0) {
-      chol_panel_kernel<<<dim3((unsigned)batch, (unsigned)rest), 64, 0, s>>>(G, p, kb);
+      chol_panel_kernel<<<dim3((unsigned)batch, (unsigned)(rest * (kB / kPanelRows))),
+                          kPanelThreads, 0, s>>>(G, p, kb);
       chol_update_kernel<<<dim3((unsigned)batch, (unsigned)(rest * (rest + 1) / 2)), 256, 0, s>>>(
           G, p, kb);
     }
