@@ -552,7 +552,7 @@ def run_ridge(args):
                    "l2": f"inputs larger than L2 ({(x.numel() + y.numel()) * 4 / 1e9:.2f} GB "
                          "read per step, no flush needed)"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": (3 + 2 * ((n + 16383) // 16384) + 3 * ((p + 63) // 64) - 1) * args.steps,
+        "gpu_launches": (4 + 2 * ((n + 16383) // 16384) + 3 * ((p + 63) // 64) - 1) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:

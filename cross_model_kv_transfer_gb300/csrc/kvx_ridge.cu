@@ -6,21 +6,28 @@
 // ridge demo centres X and Y on their column means, solves
 // (XcT Xc + lam I) W = XcT Yc and sets b = ybar - xbar W.  For a batch of
 // independent fits (X [n][p], Y [n][q] each) this runs as
-// 3 + 2 ceil(n / 16384) + 3 ceil(p / 64) - 1 launches:
+// 4 + 2 ceil(n / 16384) + 3 ceil(p / 64) - 1 launches:
 //   1. clear the fp64 workspace;
-//   2. column means of X and Y (fp32 partial sums over 256 rows, fp64 across
-//      them, chunks of rows in parallel with fp64 atomics);
-//   3. per chunk of 16,384 observations: the centred values of [X | Y] split
-//      into tf32 hi and lo planes, transposed so that each feature's
-//      observations are contiguous, then the centred Gram blocks G = XcT Xc
-//      (upper triangle of 128 x 128 tiles) and C = XcT Yc on the tensor cores
-//      as hi*hi + hi*lo + lo*hi (kvx_moments.cuh), fp32 partial sums over
-//      256 observations in tensor memory, summed in fp32 over slices of
-//      4,096 and added in fp64;
-//   4. G + lam I mirrored to full, then a Cholesky factorisation in fp64
+//   2. a shift per column of X and Y: the mean of 256 of its observations
+//      spread evenly over all of them, rounded to fp32 (one short pass
+//      instead of a pass over all observations for the exact means);
+//   3. per chunk of 16,384 observations: the shifted values v = [X | Y] -
+//      shift split into tf32 hi and lo planes, transposed so that each
+//      feature's observations are contiguous, with the column sums of v
+//      (fp32 per thread, fp64 atomics per CTA); then the Gram blocks
+//      V_xT V_x (upper triangle of 128 x 128 tiles) and V_xT V_y on the
+//      tensor cores as hi*hi + hi*lo + lo*hi (kvx_moments.cuh), fp32 partial
+//      sums over 256 observations in tensor memory, summed in fp32 over
+//      slices of 4,096 and added in fp64;
+//   4. the centring as an exact rank-one correction, G = V_xT V_x - s_x s_xT / n
+//      and C = V_xT V_y - s_x s_yT / n with s the column sums of v (the
+//      shifted-data form of the centred moments: the shift leaves each column
+//      within a fraction of its spread of its mean, so the correction is small
+//      against G and cancels nothing), and the column sums n shift + s;
+//   5. G + lam I mirrored to full, then a Cholesky factorisation in fp64
 //      blocked by 64 (per diagonal block: factor it, solve the panel below,
 //      update the trailing blocks, each step spread over CTAs);
-//   5. per (fit, nc output columns), one CTA: forward and back
+//   6. per (fit, nc output columns), one CTA: forward and back
 //      substitution in fp64 (the columns in shared memory, the threads
 //      split over the columns and the rows of each right-looking update),
 //      b = ybar - xbar W; W and b stored as fp32.  A non-positive
@@ -40,7 +47,7 @@
 
 namespace {
 
-constexpr int64_t kMeanRows = 2048;  // observations per CTA of the means (256 per thread)
+constexpr int64_t kShiftRows = 256;  // observations behind each column's shift
 constexpr int kSplitObs = 128;       // observations per CTA of the split pass
 
 template <typename T>
@@ -58,76 +65,81 @@ __global__ void clear_kernel(double *x, int64_t n) {
     x[i] = 0.0;
 }
 
-// sums[b][c] += column c of [X | Y] over this CTA's kMeanRows observations.
-// A CTA covers 32 columns (one per lane, so a warp's loads are one line per
-// row) and 8 row groups; each thread keeps 8 fp32 partial sums over its 256
-// rows (8 loads in flight), the CTA adds its groups in fp64 and one atomic
-// per column goes to the output.
+// shift[b][c] = the mean of min(n, kShiftRows) observations of column c of
+// [X | Y] spread evenly over all n (rows k n / m), rounded to fp32 (the split
+// subtracts it in fp32); a sample spread over the whole set keeps the shift
+// near the mean even when the observations drift in order.  A CTA covers 32
+// columns (one per lane, so a warp's loads are consecutive columns of a row)
+// and 8 groups of the sample, summed in fp64 and combined in shared memory.
 template <typename T>
-__global__ void __launch_bounds__(256) mean_kernel(const T *__restrict__ x, const T *__restrict__ y,
-                                                   double *__restrict__ sums, int64_t n, int p,
-                                                   int q) {
+__global__ void __launch_bounds__(256) shift_kernel(const T *__restrict__ x, const T *__restrict__ y,
+                                                    double *__restrict__ shift, int64_t n, int p,
+                                                    int q) {
   __shared__ double red[8][32];
-  const int b = blockIdx.z, pq = p + q;
+  const int b = blockIdx.y, pq = p + q;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int c = blockIdx.y * 32 + tx;
-  const int64_t t0 = (int64_t)blockIdx.x * kMeanRows;
-  const int64_t t1 = t0 + kMeanRows < n ? t0 + kMeanRows : n;
+  const int c = blockIdx.x * 32 + tx;
+  const int64_t m = n < kShiftRows ? n : kShiftRows;
   double acc = 0.0;
   if (c < pq) {
     const T *col = c < p ? x + (int64_t)b * n * p + c : y + (int64_t)b * n * q + (c - p);
     const int64_t ld = c < p ? p : q;
-    float part[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) part[u] = 0.f;
-    int64_t t = t0 + ty;
-    for (; t + 56 < t1; t += 64) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) part[u] += ldv<T>(col + (t + 8 * u) * ld);
-    }
-    for (; t < t1; t += 8) part[0] += ldv<T>(col + t * ld);
-    acc = (double)(((part[0] + part[1]) + (part[2] + part[3])) +
-                   ((part[4] + part[5]) + (part[6] + part[7])));
+#pragma unroll 4
+    for (int64_t k = ty; k < m; k += 8) acc += (double)ldv<T>(col + (k * n / m) * ld);
   }
   red[ty][tx] = acc;
   __syncthreads();
   if (ty == 0 && c < pq) {
-    double sum = 0.0;
+    double t = 0.0;
 #pragma unroll
-    for (int g = 0; g < 8; ++g) sum += red[g][tx];
-    atomicAdd(sums + (int64_t)b * pq + c, sum);
+    for (int g = 0; g < 8; ++g) t += red[g][tx];
+    shift[(int64_t)b * pq + c] = (double)(float)(t / (double)m);
   }
 }
 
-// Per chunk [n0, n0 + np): the centred values of [X | Y] of fit b as tf32 hi
-// and lo planes, plane row b (p + q) + f, column t - n0 (observations beyond
-// n are zero).  A CTA transposes 32 features x 128 observations through
-// shared memory: loads run along the features (16 per thread in flight),
-// stores along the observations.
+// Per chunk [n0, n0 + np): the shifted values v of [X | Y] of fit b as tf32
+// hi and lo planes, plane row b (p + q) + f, column t - n0 (observations
+// beyond n are zero), and sums[b][f] += the column sums of v.  A CTA
+// transposes 32 features x 128 observations through shared memory: loads run
+// along the features (16 per thread in flight), stores along the
+// observations; the sums go fp32 per thread, fp64 across the CTA, one atomic
+// per feature.
 template <typename T>
 __global__ void __launch_bounds__(256) split_kernel(const T *__restrict__ x, const T *__restrict__ y,
-                                                    const double *__restrict__ sums, int64_t n,
-                                                    int p, int q, int64_t n0, int64_t np,
-                                                    int64_t R, float *__restrict__ planes) {
+                                                    const double *__restrict__ shift,
+                                                    double *__restrict__ sums, int64_t n, int p,
+                                                    int q, int64_t n0, int64_t np, int64_t R,
+                                                    float *__restrict__ planes) {
   __shared__ float blk[kSplitObs][33];
+  __shared__ double part[8][32];
   const int b = blockIdx.z, pq = p + q;
   const int f0 = blockIdx.y * 32;
   const int64_t c0 = (int64_t)blockIdx.x * kSplitObs;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int f = f0 + tx;
-  float mean = 0.f;
-  if (f < pq) mean = (float)(sums[(int64_t)b * pq + f] / (double)n);
+  const float sh = f < pq ? (float)shift[(int64_t)b * pq + f] : 0.f;
   const T *base = f < p ? x + (int64_t)b * n * p + f : y + (int64_t)b * n * q + (f - p);
   const int64_t ld = f < p ? p : q;
   float v[kSplitObs / 8];
 #pragma unroll
   for (int i = 0; i < kSplitObs / 8; ++i) {
     const int64_t t = n0 + c0 + ty + 8 * i;
-    v[i] = f < pq && t < n ? ldv<T>(base + t * ld) - mean : 0.f;
+    v[i] = f < pq && t < n ? ldv<T>(base + t * ld) - sh : 0.f;
   }
+  float acc = 0.f;
 #pragma unroll
-  for (int i = 0; i < kSplitObs / 8; ++i) blk[ty + 8 * i][tx] = v[i];
+  for (int i = 0; i < kSplitObs / 8; ++i) {
+    blk[ty + 8 * i][tx] = v[i];
+    acc += v[i];
+  }
+  part[ty][tx] = (double)acc;
   __syncthreads();
+  if (ty == 0 && f < pq) {
+    double t = 0.0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) t += part[g][tx];
+    atomicAdd(sums + (int64_t)b * pq + f, t);
+  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int fr = f0 + ty + 8 * i;
@@ -138,6 +150,29 @@ __global__ void __launch_bounds__(256) split_kernel(const T *__restrict__ x, con
       if (col < np) mom_put(planes, R, np, (int64_t)b * pq + fr, col, blk[tx + 32 * j][ty + 8 * i]);
     }
   }
+}
+
+// The centring, as a rank-one correction of the shifted moments: for fit b,
+// row i (CTA blockIdx.x) of G (its upper triangle, the part the
+// factorisation reads) and of C, subtract s_i s_j / n, s = sums (the column
+// sums of the shifted values); thread 0 also turns columns i, i + p, ... of
+// the shift into column sums of [X | Y], n shift + s, in `shift`.
+__global__ void __launch_bounds__(256) centre_kernel(double *__restrict__ G, double *__restrict__ C,
+                                                     const double *__restrict__ sums,
+                                                     double *__restrict__ shift, int64_t n, int p,
+                                                     int q) {
+  const int b = blockIdx.y, i = blockIdx.x, pq = p + q;
+  const double *sb = sums + (int64_t)b * pq;
+  const double si = sb[i] / (double)n;
+  double *g = G + ((int64_t)b * p + i) * p;
+  for (int j = i + threadIdx.x; j < p; j += blockDim.x) g[j] = fma(-si, sb[j], g[j]);
+  double *c = C + ((int64_t)b * p + i) * q;
+  for (int j = threadIdx.x; j < q; j += blockDim.x) c[j] = fma(-si, sb[p + j], c[j]);
+  if (threadIdx.x == 0)
+    for (int k = i; k < pq; k += p) {
+      double *sh = shift + (int64_t)b * pq + k;
+      *sh = fma((double)n, *sh, sb[k]);
+    }
 }
 
 // Tiles of one chunk: fit b, row block mi of G, column block nj >= mi of
@@ -249,7 +284,8 @@ size_t ws_planes(int batch, int p, int q) {
 extern "C" size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q) {
   if (batch < 1 || p < 1 || q < 1 || p > kMaxDim || q > kMaxDim) return 0;
   return round256(ws_sums(batch, p, q)) + round256(ws_gram(batch, p)) +
-         round256(ws_cross(batch, p, q)) + round256(ws_planes(batch, p, q)) + ws_dinv(batch, p);
+         round256(ws_cross(batch, p, q)) + round256(ws_planes(batch, p, q)) +
+         round256(ws_dinv(batch, p)) + ws_sums(batch, p, q);
 }
 
 extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
@@ -263,9 +299,7 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
       (reinterpret_cast<uintptr_t>(a->workspace) & 15u) != 0)
     return KVX_ERR_INVALID_ARG;
   const int64_t n = a->n;
-  const int64_t slices64 = (n + kMeanRows - 1) / kMeanRows;
   if (n > 65535LL * 16384) return KVX_ERR_INVALID_ARG;   // the documented limit
-  const int slices = (int)slices64;
   cudaStream_t s = (cudaStream_t)stream;
   const int batch = a->batch, p = a->p, q = a->q;
   unsigned char *ws = reinterpret_cast<unsigned char *>(a->workspace);
@@ -276,19 +310,24 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
   float *planes = reinterpret_cast<float *>(ws + round256(ws_sums(batch, p, q)) +
                                             round256(ws_gram(batch, p)) +
                                             round256(ws_cross(batch, p, q)));
+  double *dinv = reinterpret_cast<double *>(reinterpret_cast<unsigned char *>(planes) +
+                                            round256(ws_planes(batch, p, q)));
+  double *shift = reinterpret_cast<double *>(reinterpret_cast<unsigned char *>(dinv) +
+                                             round256(ws_dinv(batch, p)));
   const int64_t words = (int64_t)(round256(ws_sums(batch, p, q)) + round256(ws_gram(batch, p)) +
                                   ws_cross(batch, p, q)) / 8;
   clear_kernel<<<1024, 256, 0, s>>>(sums, words);
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
 
-  dim3 mgrid((unsigned)slices, (unsigned)((p + q + 31) / 32), (unsigned)batch);
+  dim3 hgrid((unsigned)((p + q + 31) / 32), (unsigned)batch);
   if (a->x_dtype == KVX_F32)
-    mean_kernel<float><<<mgrid, 256, 0, s>>>(reinterpret_cast<const float *>(a->x),
-                                             reinterpret_cast<const float *>(a->y), sums, n, p, q);
+    shift_kernel<float><<<hgrid, 256, 0, s>>>(reinterpret_cast<const float *>(a->x),
+                                              reinterpret_cast<const float *>(a->y), shift, n, p,
+                                              q);
   else
-    mean_kernel<__nv_bfloat16><<<mgrid, 256, 0, s>>>(
+    shift_kernel<__nv_bfloat16><<<hgrid, 256, 0, s>>>(
         reinterpret_cast<const __nv_bfloat16 *>(a->x),
-        reinterpret_cast<const __nv_bfloat16 *>(a->y), sums, n, p, q);
+        reinterpret_cast<const __nv_bfloat16 *>(a->y), shift, n, p, q);
   if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
   // centred moments on the tensor cores, one chunk of observations at a time
   const int64_t R = (int64_t)batch * (p + q);
@@ -301,23 +340,25 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
                (unsigned)batch);
     if (a->x_dtype == KVX_F32)
       split_kernel<float><<<sgrid, 256, 0, s>>>(reinterpret_cast<const float *>(a->x),
-                                                reinterpret_cast<const float *>(a->y), sums, n, p,
-                                                q, n0, np, R, planes);
+                                                reinterpret_cast<const float *>(a->y), shift, sums,
+                                                n, p, q, n0, np, R, planes);
     else
       split_kernel<__nv_bfloat16><<<sgrid, 256, 0, s>>>(
           reinterpret_cast<const __nv_bfloat16 *>(a->x),
-          reinterpret_cast<const __nv_bfloat16 *>(a->y), sums, n, p, q, n0, np, R, planes);
+          reinterpret_cast<const __nv_bfloat16 *>(a->y), shift, sums, n, p, q, n0, np, R,
+          planes);
     if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
     if (mom_launch(planes, R, np, tiles, batch * tiles.per_fit, a->status, s) != cudaSuccess)
       return KVX_ERR_CUDA;
   }
+  // centring: G and C corrected, `shift` now holds the column sums
+  centre_kernel<<<dim3((unsigned)p, (unsigned)batch), 256, 0, s>>>(G, C, sums, shift, n, p, q);
+  if (cudaGetLastError() != cudaSuccess) return KVX_ERR_CUDA;
   // blocked fp64 Cholesky
   if (chol_factor(G, batch, p, a->lambda, a->status, s) != cudaSuccess) return KVX_ERR_CUDA;
   // triangular solves: by 64-row blocks (p <= 1024), else right-looking
   // with nc output columns per CTA in shared memory
   if (p <= kBlkMaxP) {
-    double *dinv = reinterpret_cast<double *>(reinterpret_cast<unsigned char *>(planes) +
-                                              round256(ws_planes(batch, p, q)));
     chol_block_inverse_kernel<<<dim3((unsigned)batch, (unsigned)((p + 63) / 64)), 64, 0, s>>>(
         G, p, dinv);
     if (cudaFuncSetAttribute(chol_solve_blocked_kernel<RidgeEpi>,
@@ -326,7 +367,7 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
       return KVX_ERR_CUDA;
     chol_solve_blocked_kernel<RidgeEpi>
         <<<dim3((unsigned)batch, (unsigned)((q + kBlkCols - 1) / kBlkCols)), kBlkThreads,
-           blk_solve_smem_bytes(p), s>>>(G, dinv, C, p, q, RidgeEpi{sums, n, p, q, a->w, a->b});
+           blk_solve_smem_bytes(p), s>>>(G, dinv, C, p, q, RidgeEpi{shift, n, p, q, a->w, a->b});
   } else {
     const int nc = solve_cols_per_cta(p, batch, q);
     if (solve_smem_bytes(p, nc) > 48 * 1024 &&
@@ -334,7 +375,7 @@ extern "C" kvx_status kvx_ridge_fit(const kvx_ridge_args *a, void *stream) {
                              (int)solve_smem_bytes(p, nc)) != cudaSuccess)
       return KVX_ERR_CUDA;
     dim3 tgrid((unsigned)batch, (unsigned)((q + nc - 1) / nc));
-    trsm_kernel<<<tgrid, kSolveThreads, solve_smem_bytes(p, nc), s>>>(G, C, sums, n, p, q, nc,
+    trsm_kernel<<<tgrid, kSolveThreads, solve_smem_bytes(p, nc), s>>>(G, C, shift, n, p, q, nc,
                                                                       a->w, a->b);
   }
   return cudaGetLastError() == cudaSuccess ? KVX_OK : KVX_ERR_CUDA;

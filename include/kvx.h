@@ -348,9 +348,10 @@ typedef struct {
 /* Bytes of scratch a kvx_ridge_fit call with these sizes needs: fp64 column
  * sums, Gram blocks and cross products (8 * batch * (p + q + p*p + p*q)),
  * the split-precision planes of one chunk of 16,384 observations
- * (2 * 4 * batch * (p + q) * 16384 bytes) and the inverses of the factor's
- * 64 x 64 diagonal blocks (8 * batch * ceil(p / 64) * 4096), each part but the
- * last rounded up to 256 bytes; 0 for sizes outside the limits above. */
+ * (2 * 4 * batch * (p + q) * 16384 bytes), the inverses of the factor's
+ * 64 x 64 diagonal blocks (8 * batch * ceil(p / 64) * 4096) and the columns'
+ * shifts (8 * batch * (p + q)), each part but the last rounded up to 256
+ * bytes; 0 for sizes outside the limits above. */
 size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
 
 /* Fit the maps: for each fit, W = (XcT Xc + lambda I)^-1 XcT Yc and
@@ -361,15 +362,18 @@ size_t kvx_ridge_workspace_bytes(int32_t batch, int32_t p, int32_t q);
  * source / target observations; its ridge demo centres X and Y and adds
  * lambda I unscaled (0.01 there).  A batch ordered (target layer, head, K|V)
  * with p = k*d and q = d writes W and b in exactly the layouts kvx_transfer
- * reads for a per-head plan with fp32 W and b.  The centred Gram blocks are
- * formed on the tensor cores with each centred fp32 value split into two tf32
- * values (products hi*hi + hi*lo + lo*hi, about 22 significant bits; fp32
- * partial sums over 256 observations, summed in fp32 over slices of 4,096,
- * slices added in fp64), the Cholesky factorisation and both triangular
- * solves run in fp64, W and b are stored as fp32; the factorisation is
- * blocked by 64 and spread over CTAs.  Asynchronous on `stream`; no
- * allocation (the caller passes the scratch); 3 + 2 ceil(n / 16384) +
- * 3 ceil(p / 64) - 1 kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL
+ * reads for a per-head plan with fp32 W and b.  The observations are first
+ * shifted by a per-column fp32 value (the mean of 256 of the column's
+ * observations spread evenly over all n) and the Gram blocks of the shifted values formed on the
+ * tensor cores with each shifted fp32 value split into two tf32 values
+ * (products hi*hi + hi*lo + lo*hi, about 22 significant bits; fp32 partial
+ * sums over 256 observations, summed in fp32 over slices of 4,096, slices
+ * added in fp64); the centring is then exact in fp64 as a rank-one
+ * correction with the shifted values' column sums.  The Cholesky
+ * factorisation and both triangular solves run in fp64, W and b are stored
+ * as fp32; the factorisation is blocked by 64 and spread over CTAs.
+ * Asynchronous on `stream`; no allocation (the caller passes the scratch);
+ * 4 + 2 ceil(n / 16384) + 3 ceil(p / 64) - 1 kernel launches.  Returns KVX_ERR_INVALID_ARG for a NULL
  * pointer, sizes outside the limits, a non-finite lambda, or a workspace that
  * is too small or not 16-byte aligned; KVX_ERR_CUDA if a launch fails.  A fit
  * whose matrix is not positive definite gets NaN W and b and sets

@@ -128,11 +128,12 @@ def test_status_strings():
 def test_ridge_workspace_size_and_host_validation():
     # 8 bytes per column sum, Gram entry and cross product, each block
     # rounded up to 256 bytes, the hi and lo fp32 planes of one chunk of
-    # 16,384 observations of every feature and output, and the fp64 inverses
-    # of the factor's 64 x 64 diagonal blocks
+    # 16,384 observations of every feature and output, the fp64 inverses of
+    # the factor's 64 x 64 diagonal blocks, and one fp64 shift per column
     r = lambda x: (x + 255) // 256 * 256
     assert kvx.kvx_ridge_workspace_bytes(3, 10, 4) == \
-        r(8 * 3 * 14) + r(8 * 3 * 100) + r(8 * 3 * 40) + r(2 * 4 * 3 * 14 * 16384) + 3 * 64 * 64 * 8
+        r(8 * 3 * 14) + r(8 * 3 * 100) + r(8 * 3 * 40) + r(2 * 4 * 3 * 14 * 16384) + \
+        r(3 * 64 * 64 * 8) + 8 * 3 * 14
     assert kvx.kvx_ridge_workspace_bytes(0, 10, 4) == 0
     assert kvx.kvx_ridge_workspace_bytes(1, 5000, 4) == 0
     assert kvx.load().kvx_ridge_fit(None, None) == kvx.KVX_ERR_INVALID_ARG

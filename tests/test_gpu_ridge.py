@@ -171,3 +171,26 @@ def test_ridge_fit_centres_before_the_products_large_offsets():
     wg, bg = kvx.ridge_fit(x.contiguous(), y.contiguous(), lam=0.01)
     torch.cuda.synchronize()
     _check(x, y, wg, bg, 0.01)
+
+
+def test_ridge_fit_drifting_observations_and_fewer_than_the_shift_sample():
+    # column means that drift along the observation order by several
+    # spreads, on top of a large offset: the moments are formed about a
+    # per-column shift taken from observations spread over the whole set and
+    # centred exactly afterwards, so neither the offset nor the drift costs
+    # digits; and a fit with fewer observations (120) than the shift's
+    # sample of 256
+    g = torch.Generator(device="cuda").manual_seed(37)
+    n, p, q = 20000, 48, 24
+    t = torch.linspace(0.0, 1.0, n, device="cuda")[None, :, None]
+    x = torch.randn((1, n, p), generator=g, device="cuda") + \
+        5.0 * t * torch.randn((1, 1, p), generator=g, device="cuda") + 50.0
+    w = torch.randn((p, q), generator=g, device="cuda") / p ** 0.5
+    y = x @ w - 20.0 + 0.1 * torch.randn((1, n, q), generator=g, device="cuda")
+    wg, bg = kvx.ridge_fit(x.contiguous(), y.contiguous(), lam=0.01)
+    torch.cuda.synchronize()
+    _check(x, y, wg, bg, 0.01)
+    x, y = _data(2, 120, 32, 8, seed=38)
+    wg, bg = kvx.ridge_fit(x, y, lam=0.01)
+    torch.cuda.synchronize()
+    _check(x, y, wg, bg, 0.01)
