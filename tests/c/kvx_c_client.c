@@ -40,6 +40,7 @@ int main(void) {
   kvx_ridge_args r;
   kvx_diag_args g;
   kvx_transfer_args a;
+  kvx_feature_args f;
   int s;
 
   memset(&d, 0, sizeof d);
@@ -67,6 +68,10 @@ int main(void) {
   if (kvx_layer_scores(NULL, NULL, NULL) != KVX_ERR_INVALID_ARG ||
       kvx_layer_scores_workspace_bytes(NULL, 4096) != 0)
     return 13;
+  memset(&f, 0, sizeof f);
+  if (kvx_ridge_features(NULL, &f, NULL) != KVX_ERR_INVALID_ARG ||
+      kvx_ridge_features(NULL, NULL, NULL) != KVX_ERR_INVALID_ARG)
+    return 14;
   memset(&g, 0, sizeof g);
   if (kvx_kv_diagnostics(NULL, &g, NULL) != KVX_ERR_INVALID_ARG) return 10;
 
