@@ -197,10 +197,12 @@ extern "C" kvx_status kvx_ridge_features(const kvx_plan *plan, const kvx_feature
       (d.kv_dtype != KVX_F32 && d.kv_dtype != KVX_BF16))
     return KVX_ERR_UNSUPPORTED;
   const bool with_y = a->y != nullptr;
-  if (!a->src_k || !a->src_v || !a->x || !a->layer_idx || a->ntok < 0 || a->ntok > INT32_MAX ||
-      a->num_requests < 1 || (!a->cu_seqlens && a->num_requests != 1) ||
-      (a->out_dtype != KVX_F32 && a->out_dtype != KVX_BF16) ||
-      (with_y && (!a->tgt_k || !a->tgt_v)))
+  if (a->ntok < 0 || a->ntok > INT32_MAX || !a->layer_idx || a->num_requests < 1 ||
+      (!a->cu_seqlens && a->num_requests != 1) ||
+      (a->out_dtype != KVX_F32 && a->out_dtype != KVX_BF16))
+    return KVX_ERR_INVALID_ARG;
+  // the caches and outputs may be NULL when there are no tokens
+  if (a->ntok > 0 && (!a->src_k || !a->src_v || !a->x || (with_y && (!a->tgt_k || !a->tgt_v))))
     return KVX_ERR_INVALID_ARG;
   if (!aligned16(a->src_k) || !aligned16(a->src_v) || !aligned16(a->x) ||
       (with_y && (!aligned16(a->tgt_k) || !aligned16(a->tgt_v) || !aligned16(a->y))))

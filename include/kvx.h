@@ -488,10 +488,10 @@ typedef struct {
  * that target layer's x rows zero (KVX_FLAG_BAD_LAYER_INDEX; y is still
  * written); a malformed request table leaves x and y all zero
  * (KVX_FLAG_BAD_SEQLENS).  Asynchronous on `stream`, no allocation, one kernel
- * launch (none for ntok == 0).  Returns KVX_ERR_INVALID_ARG for a NULL plan,
- * args or required pointer, y without both target caches, a pointer that is
- * not 16-byte aligned, sizes outside the limits, a bad out_dtype, or a plan
- * of another device; KVX_ERR_UNSUPPORTED for a wide-mapper plan, a head_dim
+ * launch (none for ntok == 0, when the caches and outputs may be NULL).
+ * Returns KVX_ERR_INVALID_ARG for a NULL plan, args or required pointer, y
+ * without both target caches, a pointer that is not 16-byte aligned, sizes
+ * outside the limits, a bad out_dtype, or a plan of another device; KVX_ERR_UNSUPPORTED for a wide-mapper plan, a head_dim
  * that is not a multiple of 8 or exceeds 128, or 2 Lt H above 2^31 - 1;
  * KVX_ERR_CUDA if the launch fails. */
 kvx_status kvx_ridge_features(const kvx_plan *plan, const kvx_feature_args *args, void *stream);

@@ -231,6 +231,13 @@ def test_features_refusals():
     assert call(ntok=0) == kvx.KVX_OK
     torch.cuda.synchronize()
     assert bool((x == 7.0).all())
+    # zero tokens through the binding: torch gives the empty caches NULL data
+    e = torch.empty((c.Ls, 0, c.H, c.d), device="cuda")
+    et = torch.empty((c.Lt, 0, c.H, c.d), device="cuda")
+    xe, ye = plan.ridge_features(src_k=e, src_v=e, tgt_k=et, tgt_v=et,
+                                 layer_idx=inp["layer_idx"])
+    torch.cuda.synchronize()
+    assert tuple(xe.shape) == (c.Lt * c.H * 2, 0, c.k * c.d) and ye.shape[1] == 0
     # a wide-mapper plan has no per-head fits
     wide = kvx.Plan(src_layers=2, tgt_layers=2, kv_heads=1, head_dim=128, k=1,
                     rope_theta_src=1e4, rope_theta_tgt=1e4, max_position=64,
