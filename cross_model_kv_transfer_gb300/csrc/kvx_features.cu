@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(kFeatThreads, 6) features_kernel(const __grid_
   }
   const int32_t *__restrict__ layers = p.layer_idx + (int64_t)lt * p.k;
   bool row_ok = true;
-  for (int j = 0; j < p.k; ++j) {
+#pragma unroll 4
+  for (int j = 0; j < p.k; ++j) {   // the row's loads issue together
     const int32_t s = __ldg(layers + j);
     row_ok = row_ok && s >= 0 && s < p.Ls;
   }
