@@ -1205,3 +1205,26 @@ def test_ridge_features_flag_bad_inputs_and_zero_their_rows():
     x, y, st = oracle.ridge_features(max_position=10, layer_idx=np.array([[0, 1], [1, 2]]),
                                      cu_seqlens=np.array([0, 4, 3, 6]), **kw)
     assert st == oracle.BAD_SEQLENS and not x.any() and not y.any()
+
+
+def test_ridge_features_are_what_the_transfer_maps():
+    # the transfer applies each (target layer, head, K|V) map to exactly these
+    # features: x W + b, with keys then turned into the target RoPE at the
+    # token's target position (numpy here), equals the transfer's output row
+    rng = np.random.default_rng(13)
+    Ls, Lt, H, d, k, n, off = 4, 3, 2, 8, 2, 11, 5
+    sk = rng.normal(size=(Ls, n, H, d)); sv = rng.normal(size=(Ls, n, H, d))
+    table = np.array([[3, 1], [0, 0], [2, 3]])
+    w = rng.normal(size=(Lt, H, 2, k * d, d)); b = rng.normal(size=(Lt, H, 2, d))
+    kw = dict(theta_src=1e4, theta_tgt=5e5, max_position=n + off)
+    x, _, st = oracle.ridge_features(src_k=sk, src_v=sv, layer_idx=table, **kw)
+    dk, dv, st2 = oracle.transfer(src_k=sk, src_v=sv, layer_idx=table, w=w, b=b,
+                                  tgt_offset=np.array([off]), dst_capacity=n + off, **kw)
+    assert st == 0 and st2 == 0
+    pos = np.arange(n) + off
+    for lt in range(Lt):
+        for h in range(H):
+            yk = x[lt, h, 0] @ w[lt, h, 0] + b[lt, h, 0]
+            yv = x[lt, h, 1] @ w[lt, h, 1] + b[lt, h, 1]
+            np.testing.assert_allclose(_rotate_np(yk, pos, 5e5), dk[lt, off:, h], atol=1e-10)
+            np.testing.assert_allclose(yv, dv[lt, off:, h], atol=1e-10)
