@@ -17,7 +17,7 @@ from cross_model_kv_transfer_gb300 import kvx
 from cross_model_kv_transfer_gb300.workloads import (PAGED, WORKLOADS, make_inputs,
                                                      make_paged_source, make_wide_weights)
 
-from parity import TC_SINGLE, TOL, assert_parity, kernel_code, run_gpu, run_oracle
+from parity import TC_SINGLE, assert_parity, kernel_code, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 

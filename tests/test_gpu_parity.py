@@ -13,9 +13,9 @@ import torch
 
 import oracle
 from cross_model_kv_transfer_gb300 import kvx
-from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs, sentinel_like
+from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_inputs, sentinel_like
 
-from parity import (TC_SINGLE, TOL, assert_parity, gpu_args, kernel_code, make_plan, run_gpu,
+from parity import (TC_SINGLE, assert_parity, gpu_args, kernel_code, make_plan, run_gpu,
                     run_oracle)
 
 pytestmark = pytest.mark.gpu

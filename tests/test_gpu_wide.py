@@ -19,7 +19,7 @@ from cross_model_kv_transfer_gb300 import kvx
 from cross_model_kv_transfer_gb300.workloads import (PAGED, WORKLOADS, make_inputs,
                                                      make_wide_weights)
 
-from parity import TOL, assert_parity, run_gpu, run_oracle
+from parity import assert_parity, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 

@@ -5,11 +5,9 @@ for a ragged paged batch with per-request offsets and for the wide map."""
 import dataclasses
 
 import numpy as np
-import torch
 
 import oracle
-from cross_model_kv_transfer_gb300.workloads import PAGED, WORKLOADS, make_inputs, \
-    make_wide_weights
+from cross_model_kv_transfer_gb300.workloads import WORKLOADS, make_inputs, make_wide_weights
 
 from parity import dst_rows_of, oracle_tokens, run_oracle
 
